@@ -1,0 +1,7 @@
+"""CPU fp64 oracle of the SSD chunked-scan forward.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; never by the product path.
+"""
+from .ssd_oracle import (dt_process, dt_process_c, f64, scan_chunked,  # noqa: F401
+                         scan_quadratic, scan_sequential, default_threads)

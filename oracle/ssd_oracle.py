@@ -1,0 +1,356 @@
+"""CPU fp64 oracle for the Mamba-2 SSD chunked-scan forward.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers; the product path never
+imports this package.  Nothing here is shared with the CUDA library.
+
+Three independent forms of the same computation:
+
+* ``scan_sequential``  the token-by-token recurrence, in plain C
+  (``ssd_oracle.c``), run over batch x heads with OpenMP.  This is the
+  definition: h_t = exp(dt_t A_h) h_{t-1} + dt_t x_t (outer) B_t,
+  y_t = h_t C_t + D_h x_t, gated by silu(z_t).
+* ``scan_quadratic``   the materialised "attention-like" form.  The pages
+  state that SSD is scalar-gated linear attention with q = C, k = B,
+  v = dt * x and log-gate dt * A, no 1/sqrt(d) scaling, B/C shared by head
+  groups like grouped-query attention ("Differences between simple_gla kernel
+  and mamba2_ssd kernel", fla-org/flash-linear-attention PR #49).  Written out
+  for one (batch, head): Y = (Lmask * C B^T) (dt * x) with
+  Lmask[t, s] = exp(sum_{k=s+1..t} dt_k A) for s <= t within one document.
+* ``scan_chunked``     the chunked algorithm (intra-chunk quadratic part plus
+  inter-chunk state passing), parameterised by the chunk length and
+  returning its intermediates (processed dt, per-chunk cumsum of dt*A, chunk
+  states, states entering each chunk).  It is the chunked SSD scan of
+  ``mamba_chunk_scan_combined`` as named on the PR #49 page, written from its
+  mathematics.
+
+Readings of the pages (see the design notes): bias -> softplus -> clamp for
+dt, the clamp skipped for the default dt_limit (0, inf); the gate multiplies
+the whole y including the D skip; a seq_idx change between t-1 and t resets
+the state to zero before token t; initial_states seed the first document only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+_LIBS = {}
+
+
+def _lib(mutation: int = 0):
+    if mutation not in _LIBS:
+        path = _build.build(mutation)
+        lib = ctypes.CDLL(str(path))
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int32)
+        i64 = ctypes.c_int64
+        lib.ssd_oracle_scan.restype = ctypes.c_int
+        lib.ssd_oracle_scan.argtypes = [i64, i64, i64, i64, i64, i64,
+                                        dp, dp, dp, ctypes.c_int,
+                                        ctypes.c_double, ctypes.c_double, dp,
+                                        dp, dp, dp, dp, dp, ip, dp, dp,
+                                        ctypes.c_int]
+        lib.ssd_oracle_dt.restype = None
+        lib.ssd_oracle_dt.argtypes = [i64, i64, i64, dp, dp, ctypes.c_int,
+                                      ctypes.c_double, ctypes.c_double, dp]
+        lib.ssd_oracle_mutation.restype = ctypes.c_int
+        _LIBS[mutation] = lib
+    return _LIBS[mutation]
+
+
+def f64(t) -> Optional[np.ndarray]:
+    """torch tensor / array -> contiguous float64 numpy (bf16 upcast exactly)."""
+    if t is None:
+        return None
+    if hasattr(t, "detach"):
+        import torch
+        t = t.detach().to("cpu")
+        if t.dtype != torch.float64:
+            t = t.to(torch.float64)
+        return np.ascontiguousarray(t.numpy())
+    return np.ascontiguousarray(np.asarray(t, dtype=np.float64))
+
+
+def i32(t) -> Optional[np.ndarray]:
+    if t is None:
+        return None
+    if hasattr(t, "detach"):
+        t = t.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _unpack(inp: dict):
+    x = f64(inp["x"])
+    Bsz, L, H, P = x.shape
+    Bm = f64(inp["B"])
+    G, N = Bm.shape[2], Bm.shape[3]
+    lo, hi = inp.get("dt_limit", (0.0, float("inf")))
+    return dict(
+        x=x, dt=f64(inp["dt"]), dt_bias=f64(inp.get("dt_bias")),
+        A=f64(inp["A"]), B=Bm, C=f64(inp["C"]), D=f64(inp.get("D")),
+        z=f64(inp.get("z")), init=f64(inp.get("initial_states")),
+        seq_idx=i32(inp.get("seq_idx")),
+        softplus=bool(inp.get("dt_softplus", True)), lo=float(lo), hi=float(hi),
+        batch=Bsz, seqlen=L, nheads=H, headdim=P, dstate=N, ngroups=G)
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# dt preprocessing
+# ----------------------------------------------------------------------------
+
+def dt_process(dt_raw, dt_bias, softplus: bool, lo: float, hi: float) -> np.ndarray:
+    """dt = clamp(softplus(dt_raw + dt_bias)); numpy fp64.  The clamp is
+    skipped for the default limit (0, +inf), as the p1 call passes
+    dt_limit=(0.0, float("inf")) to mean "no limit"."""
+    d = f64(dt_raw).copy()
+    if dt_bias is not None:
+        d = d + f64(dt_bias)
+    if softplus:
+        d = np.logaddexp(0.0, d)
+    if not (lo == 0.0 and np.isinf(hi) and hi > 0):
+        d = np.clip(d, lo, hi)
+    return d
+
+
+def dt_process_c(dt_raw, dt_bias, softplus: bool, lo: float, hi: float) -> np.ndarray:
+    d = f64(dt_raw)
+    out = np.empty_like(d)
+    Bsz, L, H = d.shape
+    _lib().ssd_oracle_dt(Bsz, L, H, _ptr(d), _ptr(f64(dt_bias)), int(softplus),
+                         lo, hi, _ptr(out))
+    return out
+
+
+# ----------------------------------------------------------------------------
+# form 1: sequential recurrence (C)
+# ----------------------------------------------------------------------------
+
+def scan_sequential(inp: dict, nthreads: Optional[int] = None, mutation: int = 0,
+                    heads=None, batches=None):
+    """Token-by-token recurrence in fp64.  Returns (out, final_states) as
+    float64 arrays [B,L,H,P] and [B,H,P,N].
+
+    ``heads`` / ``batches`` restrict the run to a subset (the recurrence of
+    each (batch, head) pair is independent), for sampled checks on large
+    workloads; the returned arrays then cover only that subset, in the order
+    given.
+    """
+    u = _unpack(inp)
+    if heads is not None or batches is not None:
+        u = _subset(u, heads, batches)
+    Bsz, L, H, P, N, G = (u["batch"], u["seqlen"], u["nheads"], u["headdim"],
+                          u["dstate"], u["ngroups"])
+    out = np.empty((Bsz, L, H, P), dtype=np.float64)
+    final = np.empty((Bsz, H, P, N), dtype=np.float64)
+    rc = _lib(mutation).ssd_oracle_scan(
+        Bsz, L, H, P, N, G, _ptr(u["x"]), _ptr(u["dt"]), _ptr(u["dt_bias"]),
+        int(u["softplus"]), u["lo"], u["hi"], _ptr(u["A"]), _ptr(u["B"]),
+        _ptr(u["C"]), _ptr(u["D"]), _ptr(u["z"]), _ptr(u["init"]),
+        _ptr(u["seq_idx"], ctypes.c_int32), _ptr(out), _ptr(final),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle: bad sizes")
+    return out, final
+
+
+def _subset(u: dict, heads, batches) -> dict:
+    """Restrict to the given batch rows and heads; each selected head keeps
+    its own B/C group by giving it a private group (G' = #heads)."""
+    u = dict(u)
+    H = u["nheads"]
+    hpg = H // u["ngroups"]
+    bsel = np.arange(u["batch"]) if batches is None else np.asarray(batches)
+    hsel = np.arange(H) if heads is None else np.asarray(heads)
+    gsel = hsel // hpg
+    u["x"] = np.ascontiguousarray(u["x"][bsel][:, :, hsel])
+    u["dt"] = np.ascontiguousarray(u["dt"][bsel][:, :, hsel])
+    if u["z"] is not None:
+        u["z"] = np.ascontiguousarray(u["z"][bsel][:, :, hsel])
+    u["B"] = np.ascontiguousarray(u["B"][bsel][:, :, gsel])
+    u["C"] = np.ascontiguousarray(u["C"][bsel][:, :, gsel])
+    for k in ("dt_bias", "A", "D"):
+        if u[k] is not None:
+            u[k] = np.ascontiguousarray(u[k][hsel])
+    if u["init"] is not None:
+        u["init"] = np.ascontiguousarray(u["init"][bsel][:, hsel])
+    if u["seq_idx"] is not None:
+        u["seq_idx"] = np.ascontiguousarray(u["seq_idx"][bsel])
+    u["batch"], u["nheads"], u["ngroups"] = len(bsel), len(hsel), len(hsel)
+    return u
+
+
+# ----------------------------------------------------------------------------
+# helpers shared by the two numpy forms
+# ----------------------------------------------------------------------------
+
+def _segment_ids(seq_idx: Optional[np.ndarray], Bsz: int, L: int) -> np.ndarray:
+    """seg[b, t] = number of state resets at positions 1..t, where a reset
+    happens at t when seq_idx[b, t] != seq_idx[b, t-1].  Two tokens share a
+    recurrence (no reset between them) iff their seg values are equal."""
+    if seq_idx is None:
+        return np.zeros((Bsz, L), dtype=np.int64)
+    change = np.zeros((Bsz, L), dtype=np.int64)
+    change[:, 1:] = (seq_idx[:, 1:] != seq_idx[:, :-1])
+    return np.cumsum(change, axis=1)
+
+
+def _silu(v: np.ndarray) -> np.ndarray:
+    return v / (1.0 + np.exp(-v))
+
+
+def _group_of(H: int, G: int) -> np.ndarray:
+    return np.arange(H) // (H // G)
+
+
+# ----------------------------------------------------------------------------
+# form 2: materialised quadratic (attention-like) form
+# ----------------------------------------------------------------------------
+
+def scan_quadratic(inp: dict):
+    """Brute-force quadratic form, O(L^2) per (batch, head); tiny inputs only.
+
+    For one (b, h) with a_t = dt_t * A_h and seg the document segmentation:
+      Lmask[t, s] = exp(sum_{k=s+1..t} a_k) * [s <= t] * [seg_s == seg_t]
+      Y = (Lmask * (C B^T)) (dt * x)
+          + [seg_t == 0] exp(sum_{k=0..t} a_k) * (h0 C_t)      (initial state)
+          + D x;  out = Y * silu(z)
+      final = [seg_last == 0] exp(sum_k a_k) h0
+              + sum_{s: seg_s == seg_last} exp(sum_{k=s+1..L-1} a_k) dt_s x_s (outer) B_s
+    The segment sums are formed by cumulative sums over a masked matrix, not
+    by differences of one running sum.
+    """
+    u = _unpack(inp)
+    Bsz, L, H, P, N, G = (u["batch"], u["seqlen"], u["nheads"], u["headdim"],
+                          u["dstate"], u["ngroups"])
+    dt = dt_process(u["dt"], u["dt_bias"], u["softplus"], u["lo"], u["hi"])
+    seg = _segment_ids(u["seq_idx"], Bsz, L)
+    grp = _group_of(H, G)
+    out = np.zeros((Bsz, L, H, P))
+    final = np.zeros((Bsz, H, P, N))
+    tri_incl = np.tril(np.ones((L, L), dtype=bool))           # s <= t
+    for b in range(Bsz):
+        same = seg[b][:, None] == seg[b][None, :]
+        for h in range(H):
+            g = grp[h]
+            a = dt[b, :, h] * u["A"][h]                        # [L]
+            # segsum[t, s] = sum_{k=s+1..t} a_k  (for s <= t)
+            rep = np.broadcast_to(a[:, None], (L, L)).copy()   # rep[k, s] = a_k
+            rep[~np.tril(np.ones((L, L), dtype=bool), -1)] = 0.0  # keep k > s
+            segsum = np.cumsum(rep, axis=0)                    # [t, s]
+            Lmask = np.where(tri_incl & same, np.exp(segsum), 0.0)
+            Cg = u["C"][b, :, g, :]                            # [L, N]
+            Bg = u["B"][b, :, g, :]
+            v = dt[b, :, h][:, None] * u["x"][b, :, h, :]      # [L, P]
+            y = (Lmask * (Cg @ Bg.T)) @ v
+            tot = np.cumsum(a)                                 # sum_{k=0..t} a_k
+            if u["init"] is not None:
+                h0 = u["init"][b, h]                           # [P, N]
+                first = (seg[b] == 0).astype(np.float64)
+                y += (first * np.exp(tot))[:, None] * (Cg @ h0.T)
+            if u["D"] is not None:
+                y += u["D"][h] * u["x"][b, :, h, :]
+            if u["z"] is not None:
+                y = y * _silu(u["z"][b, :, h, :])
+            out[b, :, h, :] = y
+            if L > 0:
+                last = L - 1
+                w = np.where(seg[b] == seg[b, last], np.exp(segsum[last]), 0.0) * dt[b, :, h]
+                fin = (w[:, None] * u["x"][b, :, h, :]).T @ Bg  # [P, N]
+                if u["init"] is not None and seg[b, last] == 0:
+                    fin += np.exp(tot[last]) * u["init"][b, h]
+            else:
+                fin = u["init"][b, h] if u["init"] is not None else np.zeros((P, N))
+            final[b, h] = fin
+    return out, final
+
+
+# ----------------------------------------------------------------------------
+# form 3: chunked algorithm with intermediates
+# ----------------------------------------------------------------------------
+
+def scan_chunked(inp: dict, chunk_size: int, return_intermediates: bool = False):
+    """Chunked SSD scan in fp64 (chunk length Q; the last chunk may be short).
+
+    Step 1  dt processing and, per chunk, cs = inclusive cumsum of dt*A.
+    Step 2  chunk states: S_c = sum_{j in c, same segment as the chunk's last
+            token} exp(cs_last - cs_j) dt_j x_j (outer) B_j          [P, N]
+    Step 3  state passing: H_{-1} = h0;
+            H_c = [no reset in chunk c] exp(cs_last) H_{c-1} + S_c
+            (the state entering chunk c is H_{c-1}).
+    Step 4  outputs: y_i = sum_{j<=i in c, same segment} exp(cs_i - cs_j)
+            (C_i . B_j) dt_j x_j + [no reset in c up to i] exp(cs_i) H_{c-1} C_i
+            + D x_i;  out = y * silu(z_i).
+    Segments inside a chunk are counted from the chunk start, a reset at the
+    chunk's first token included.
+    """
+    u = _unpack(inp)
+    Bsz, L, H, P, N, G = (u["batch"], u["seqlen"], u["nheads"], u["headdim"],
+                          u["dstate"], u["ngroups"])
+    Q = int(chunk_size)
+    assert Q >= 1
+    nc = (L + Q - 1) // Q
+    dt = dt_process(u["dt"], u["dt_bias"], u["softplus"], u["lo"], u["hi"])
+    seg = _segment_ids(u["seq_idx"], Bsz, L)
+    grp = _group_of(H, G)
+    out = np.zeros((Bsz, L, H, P))
+    cs_all = np.zeros((Bsz, H, nc, Q))
+    S_all = np.zeros((Bsz, nc, H, P, N))
+    Hprev_all = np.zeros((Bsz, nc, H, P, N))
+    final = np.zeros((Bsz, H, P, N))
+    for b in range(Bsz):
+        for h in range(H):
+            g = grp[h]
+            Hc = u["init"][b, h].copy() if u["init"] is not None else np.zeros((P, N))
+            for c in range(nc):
+                s0, s1 = c * Q, min(L, (c + 1) * Q)
+                n = s1 - s0
+                d = dt[b, s0:s1, h]
+                cs = np.cumsum(d * u["A"][h])                         # step 1
+                cs_all[b, h, c, :n] = cs
+                prev_seg = seg[b, s0 - 1] if s0 > 0 else seg[b, 0]
+                lseg = seg[b, s0:s1] - prev_seg                       # 0 = continues
+                xc = u["x"][b, s0:s1, h, :]
+                Bc = u["B"][b, s0:s1, g, :]
+                Cc = u["C"][b, s0:s1, g, :]
+                # step 2
+                w = np.where(lseg == lseg[-1], np.exp(cs[-1] - cs), 0.0) * d
+                S = (w[:, None] * xc).T @ Bc
+                S_all[b, c, h] = S
+                # step 3
+                Hprev_all[b, c, h] = Hc
+                keep = 1.0 if lseg[-1] == 0 else 0.0
+                Hnew = keep * np.exp(cs[-1]) * Hc + S
+                # step 4
+                diff = cs[:, None] - cs[None, :]
+                mask = np.tril(np.ones((n, n), dtype=bool)) & (lseg[:, None] == lseg[None, :])
+                Lm = np.where(mask, np.exp(np.where(mask, diff, 0.0)), 0.0)
+                y = (Lm * (Cc @ Bc.T)) @ (d[:, None] * xc)
+                y += (np.where(lseg == 0, np.exp(cs), 0.0))[:, None] * (Cc @ Hc.T)
+                if u["D"] is not None:
+                    y += u["D"][h] * xc
+                if u["z"] is not None:
+                    y = y * _silu(u["z"][b, s0:s1, h, :])
+                out[b, s0:s1, h, :] = y
+                Hc = Hnew
+            final[b, h] = Hc
+    if return_intermediates:
+        return out, final, dict(dt=dt, cs=cs_all, states=S_all, prev_states=Hprev_all)
+    return out, final

@@ -1,0 +1,342 @@
+"""Pins for the CPU fp64 oracle (no GPU).
+
+Each check ties the oracle to something other than itself: printed values on
+the pages, closed forms, a library routine, brute force on tiny inputs and the
+invariants the method must satisfy (chunk-size independence, chaining through
+final/initial states, group replication, document packing).  The last test
+plants mistakes in the C oracle and shows that these pins catch each one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_inputs as si
+from oracle import ssd_oracle as so
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+TIGHT = 1e-11
+
+
+def rel(a, b):
+    a, b = np.asarray(a), np.asarray(b)
+    den = np.abs(b).max()
+    return float(np.abs(a - b).max() / (den if den > 0 else 1.0))
+
+
+# --------------------------------------------------------------------------
+# worked example printed on the "ngroups > 1" issue page
+# --------------------------------------------------------------------------
+
+def _p1_block_out(G: int, grouped: bool, mutation: int = 0) -> float:
+    """out[0,0,0] of the page's block at t = 0, built around the oracle.
+
+    At t = 0 the causal width-4 conv sees only its last tap: every conv
+    channel is 0.1*0.1 + 0.1 = 0.11, then SiLU; so x, B and C all equal
+    s = silu(0.11).  z = dt_raw = 0.1.  The oracle runs the scan (D-skip and
+    silu(z) gate included; the page's block applies the gate before the norm,
+    norm_before_gate=False).  The rest is the page's RMSNorm (weight 0.1,
+    eps 1e-5, over dim/ngroups channels when grouped) and out-projection
+    (weight 0.1, bias 0.1), written here as test-side glue.
+    """
+    H, P, N = 32, 64, 128
+    dim = H * P
+    s = 0.11 / (1.0 + math.exp(-0.11))
+    f = torch.float64
+    d = dict(x=torch.full((1, 1, H, P), s, dtype=f),
+             dt=torch.full((1, 1, H), 0.1, dtype=f),
+             dt_bias=torch.full((H,), 0.1, dtype=f),
+             A=-torch.exp(torch.zeros(H, dtype=f)),
+             B=torch.full((1, 1, G, N), s, dtype=f),
+             C=torch.full((1, 1, G, N), s, dtype=f),
+             D=torch.arange(H, dtype=f) * 1000.0,
+             z=torch.full((1, 1, H, P), 0.1, dtype=f),
+             dt_softplus=True, dt_limit=(0.0, float("inf")))
+    y, _ = so.scan_sequential(d, mutation=mutation)
+    y = y.reshape(dim)                       # channel = h * headdim + p
+    gs = dim // G if grouped else dim
+    yg = y.reshape(-1, gs)
+    yn = (yg / np.sqrt((yg ** 2).mean(axis=1, keepdims=True) + 1e-5)).reshape(dim) * 0.1
+    return float(0.1 * yn.sum() + 0.1)
+
+
+def test_p1_worked_example_golden():
+    g = json.load(open(os.path.join(GOLDEN, "p1_worked_example.json")))
+    for G in (1, 2, 4):
+        assert abs(_p1_block_out(G, True) - g["printed"]["combined"][str(G)]) < 1.5e-4
+        assert abs(_p1_block_out(G, False) - g["printed"]["ref"][str(G)]) < 1.5e-4
+
+
+# --------------------------------------------------------------------------
+# dt preprocessing
+# --------------------------------------------------------------------------
+
+def test_dt_processing_matches_library_softplus():
+    rng = np.random.default_rng(0)
+    raw = rng.normal(size=(2, 9, 3)) * 30
+    bias = rng.normal(size=3)
+    # softplus(v) = log(1 + e^v) = numpy's logaddexp(0, v)
+    ref = np.logaddexp(0.0, raw + bias)
+    assert rel(oracle.dt_process_c(raw, bias, True, 0.0, math.inf), ref) < 1e-15
+    assert rel(oracle.dt_process(raw, bias, True, 0.0, math.inf), ref) < 1e-15
+    # clamp after softplus
+    ref_c = np.clip(ref, 0.05, 2.0)
+    assert rel(oracle.dt_process_c(raw, bias, True, 0.05, 2.0), ref_c) < 1e-15
+    # no softplus, default limit: untouched (negative values stay)
+    assert np.array_equal(oracle.dt_process_c(raw, None, False, 0.0, math.inf), raw)
+    # known values: softplus(0) = ln 2
+    z = np.zeros((1, 1, 1))
+    assert abs(oracle.dt_process_c(z, None, True, 0.0, math.inf)[0, 0, 0] - math.log(2)) < 1e-16
+
+
+# --------------------------------------------------------------------------
+# brute force: sequential recurrence == materialised quadratic form
+# --------------------------------------------------------------------------
+
+CASES = [
+    dict(),
+    dict(init_std=0.5),
+    dict(seq_idx_lengths=[5, 1, 20, 11]),
+    dict(seq_idx_lengths=[1, 35, 1], init_std=0.2),
+    dict(has_z=False, has_D=False, dt_bias=False),
+    dict(ngroups=1, nheads=3),
+    dict(ngroups=4, nheads=4, init_std=1.0, seq_idx_lengths=[16, 16, 5]),
+    dict(dt_softplus=False, a_log_range=(-3.0, 0.0)),
+    dict(dt_limit=(0.02, 0.3)),
+    dict(a_log_range=(math.log(1e-3), math.log(1e-1)), seqlen=60, init_std=0.3),
+]
+
+
+@pytest.mark.parametrize("kw", CASES, ids=[str(i) for i in range(len(CASES))])
+def test_sequential_equals_quadratic(kw):
+    d = si.random_small(11, **kw)
+    y1, f1 = so.scan_sequential(d)
+    y2, f2 = so.scan_quadratic(d)
+    assert rel(y1, y2) < TIGHT
+    assert rel(f1, f2) < TIGHT
+
+
+# --------------------------------------------------------------------------
+# chunked form: any chunk length gives the recurrence's result
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Q", [1, 7, 16, 64, 37, 50])
+def test_chunk_size_invariance(Q):
+    d = si.random_small(3, seqlen=37, init_std=0.4, seq_idx_lengths=[9, 7, 1, 20])
+    y1, f1 = so.scan_sequential(d)
+    y2, f2 = so.scan_chunked(d, Q)
+    assert rel(y1, y2) < TIGHT
+    assert rel(f1, f2) < TIGHT
+
+
+def test_chunked_intermediates_shapes_and_states():
+    d = si.random_small(4, seqlen=40, init_std=0.4)
+    y, f, im = so.scan_chunked(d, 16, return_intermediates=True)
+    assert im["cs"].shape == (2, 4, 3, 16)
+    assert im["states"].shape == (2, 3, 4, 8, 6)
+    # state entering chunk 0 is the initial state
+    assert np.array_equal(im["prev_states"][:, 0], so.f64(d["initial_states"]))
+
+
+# --------------------------------------------------------------------------
+# chaining: final_states fed back as initial_states == one whole run
+# --------------------------------------------------------------------------
+
+def _slice(d, t0, t1, init):
+    e = dict(d)
+    for k in ("x", "dt", "B", "C", "z", "seq_idx"):
+        if e.get(k) is not None:
+            e[k] = e[k][:, t0:t1].contiguous()
+    e["initial_states"] = None if init is None else torch.from_numpy(init)
+    return e
+
+
+@pytest.mark.parametrize("nseg,docs", [(2, None), (4, None), (3, [10, 30, 8])])
+def test_chaining(nseg, docs):
+    L = 48
+    d = si.random_small(5, seqlen=L, init_std=0.3, seq_idx_lengths=docs)
+    y_all, f_all = so.scan_sequential(d)
+    cuts = np.linspace(0, L, nseg + 1).astype(int)
+    st = so.f64(d["initial_states"])
+    ys = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        y, st = so.scan_sequential(_slice(d, a, b, st))
+        ys.append(y)
+    assert rel(np.concatenate(ys, axis=1), y_all) < TIGHT
+    assert rel(st, f_all) < TIGHT
+
+
+# --------------------------------------------------------------------------
+# head -> group mapping: G > 1 == G' = H with each head's B/C replicated
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_group_replication(G):
+    H = 8
+    d = si.random_small(6, nheads=H, ngroups=G, init_std=0.2)
+    y1, f1 = so.scan_sequential(d)
+    e = dict(d)
+    idx = torch.arange(H) // (H // G)            # head h reads group h / (H/G)
+    e["B"] = d["B"][:, :, idx].contiguous()
+    e["C"] = d["C"][:, :, idx].contiguous()
+    y2, f2 = so.scan_sequential(e)
+    assert rel(y1, y2) < 1e-15 and rel(f1, f2) < 1e-15
+    # and the mapping is not the interleaved one h % G
+    e2 = dict(d)
+    idx2 = torch.arange(H) % G
+    e2["B"] = d["B"][:, :, idx2].contiguous()
+    e2["C"] = d["C"][:, :, idx2].contiguous()
+    y3, _ = so.scan_sequential(e2)
+    assert rel(y1, y3) > 1e-3
+
+
+# --------------------------------------------------------------------------
+# closed forms
+# --------------------------------------------------------------------------
+
+def test_closed_form_linear_attention():
+    """A = 0, dt = 1 (no softplus, no bias): no decay, unit step, so
+    y_t = C_t . sum_{s<=t} x_s (outer) B_s -- causal linear attention, here a
+    cumulative sum of outer products."""
+    d = si.random_small(7, has_z=False, has_D=False, dt_bias=False, dt_softplus=False)
+    d["dt"] = torch.ones_like(d["dt"])
+    d["A"] = torch.zeros_like(d["A"])
+    x, Bm, Cm = (so.f64(d[k]) for k in ("x", "B", "C"))
+    H, G = x.shape[2], Bm.shape[2]
+    gi = np.arange(H) // (H // G)
+    kv = np.cumsum(np.einsum("blhp,blhn->blhpn", x, Bm[:, :, gi]), axis=1)
+    ref = np.einsum("blhpn,blhn->blhp", kv, Cm[:, :, gi])
+    y, f = so.scan_sequential(d)
+    assert rel(y, ref) < TIGHT
+    assert rel(f, kv[:, -1]) < TIGHT
+
+
+def test_closed_form_constant_inputs():
+    """Constant dt, x, B, C: h_t = dt x B^T (1 - r^(t+1)) / (1 - r), r = e^{dt A}
+    (a geometric series); y_t = (C . B) dt x (1 - r^(t+1)) / (1 - r)."""
+    L, H, P, N = 50, 3, 2, 5
+    f = torch.float64
+    A = torch.tensor([-0.3, -1.0, -4.0], dtype=f)
+    dtv, xv, bv, cv = 0.7, 1.3, -0.4, 0.9
+    d = dict(x=torch.full((1, L, H, P), xv, dtype=f), dt=torch.full((1, L, H), dtv, dtype=f),
+             dt_bias=None, A=A, B=torch.full((1, L, 1, N), bv, dtype=f),
+             C=torch.full((1, L, 1, N), cv, dtype=f), D=None, z=None,
+             dt_softplus=False)
+    y, fin = so.scan_sequential(d)
+    t = np.arange(L)
+    for h in range(H):
+        r = math.exp(dtv * float(A[h]))
+        geo = (1 - r ** (t + 1)) / (1 - r)
+        ref = N * cv * bv * dtv * xv * geo
+        assert rel(y[0, :, h, 0], ref) < 1e-13
+        assert abs(fin[0, h, 0, 0] - dtv * xv * bv * geo[-1]) < 1e-13
+
+
+def test_closed_form_decay_of_initial_state():
+    """x = 0: the state only decays, h_t = exp(dt A (t+1)) h0 for constant dt,
+    and y_t = exp(dt A (t+1)) h0 C_t."""
+    L, H, P, N = 20, 2, 3, 4
+    rng = np.random.default_rng(1)
+    h0 = rng.normal(size=(1, H, P, N))
+    Cm = rng.normal(size=(1, L, 1, N))
+    f = torch.float64
+    A = torch.tensor([-0.5, -2.0], dtype=f)
+    d = dict(x=torch.zeros(1, L, H, P, dtype=f), dt=torch.full((1, L, H), 0.25, dtype=f),
+             A=A, B=torch.ones(1, L, 1, N, dtype=f), C=torch.from_numpy(Cm),
+             initial_states=torch.from_numpy(h0), dt_softplus=False)
+    y, fin = so.scan_sequential(d)
+    for h in range(H):
+        e = np.exp(0.25 * float(A[h]) * (np.arange(L) + 1))
+        ref = e[:, None] * (Cm[0, :, 0, :] @ h0[0, h].T)
+        assert rel(y[0, :, h, :], ref) < 1e-13
+        assert rel(fin[0, h], e[-1] * h0[0, h]) < 1e-13
+
+
+def test_closed_form_single_token():
+    """L = 1 from a zero state: y = dt (C . B) x + D x."""
+    d = si.random_small(8, seqlen=1, has_z=False)
+    dt = oracle.dt_process(d["dt"], d["dt_bias"], True, 0.0, math.inf)
+    x, Bm, Cm, D = (so.f64(d[k]) for k in ("x", "B", "C", "D"))
+    H, G = x.shape[2], Bm.shape[2]
+    gi = np.arange(H) // (H // G)
+    cb = np.einsum("bln,bln->bl", Cm[:, :, gi].reshape(-1, H, Bm.shape[-1]),
+                   Bm[:, :, gi].reshape(-1, H, Bm.shape[-1])).reshape(x.shape[0], 1, H)
+    ref = (dt * cb)[..., None] * x + D[None, None, :, None] * x
+    y, _ = so.scan_sequential(d)
+    assert rel(y, ref) < 1e-14
+
+
+def test_scalar_case_matches_iir_filter():
+    """P = N = H = 1 with constant dt: h_t = r h_{t-1} + dt B_t x_t is a
+    first-order IIR filter; scipy.signal.lfilter computes it independently."""
+    signal = pytest.importorskip("scipy.signal")
+    L = 300
+    rng = np.random.default_rng(2)
+    x, Bv, Cv = rng.normal(size=L), rng.normal(size=L), rng.normal(size=L)
+    dtv, A = 0.3, -0.8
+    f = torch.float64
+    d = dict(x=torch.tensor(x, dtype=f).view(1, L, 1, 1),
+             dt=torch.full((1, L, 1), dtv, dtype=f), A=torch.tensor([A], dtype=f),
+             B=torch.tensor(Bv, dtype=f).view(1, L, 1, 1),
+             C=torch.tensor(Cv, dtype=f).view(1, L, 1, 1), dt_softplus=False)
+    y, _ = so.scan_sequential(d)
+    r = math.exp(dtv * A)
+    h = signal.lfilter([1.0], [1.0, -r], dtv * Bv * x)
+    assert rel(y[0, :, 0, 0], Cv * h) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# document packing: seq_idx resets == separate runs from zero state
+# --------------------------------------------------------------------------
+
+def test_packed_documents_equal_separate_runs():
+    lens = [7, 1, 13, 19]
+    L = sum(lens)
+    d = si.random_small(9, seqlen=L, seq_idx_lengths=lens, init_std=0.5)
+    y, fin = so.scan_sequential(d)
+    t0 = 0
+    for i, n in enumerate(lens):
+        e = _slice(d, t0, t0 + n, so.f64(d["initial_states"]) if i == 0 else None)
+        e["seq_idx"] = None
+        ye, fe = so.scan_sequential(e)
+        assert rel(y[:, t0:t0 + n], ye) < TIGHT
+        t0 += n
+    assert rel(fin, fe) < TIGHT   # final state belongs to the last document
+
+
+def test_head_subset_matches_full_run():
+    d = si.random_small(10, nheads=8, ngroups=2, init_std=0.1, seq_idx_lengths=[20, 17])
+    y, f = so.scan_sequential(d)
+    ys, fs = so.scan_sequential(d, heads=[1, 6], batches=[1])
+    assert np.array_equal(ys[0], y[1][:, [1, 6]])
+    assert np.array_equal(fs[0], f[1][[1, 6]])
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: every mutation of the C oracle fails at least one pin
+# --------------------------------------------------------------------------
+
+MUTATIONS = {1: "decay sign flipped", 2: "dt dropped from the input term",
+             3: "B and C swapped", 4: "head->group map h % G",
+             5: "seq_idx resets ignored", 6: "D skip dropped",
+             7: "gate without sigmoid"}
+
+
+@pytest.mark.parametrize("k", sorted(MUTATIONS), ids=[MUTATIONS[k] for k in sorted(MUTATIONS)])
+def test_planted_mistakes_are_caught(k):
+    failures = 0
+    # pin A: brute-force quadratic form on a case with every option on
+    d = si.random_small(12, nheads=4, ngroups=2, init_std=0.3,
+                        seq_idx_lengths=[10, 1, 26])
+    y_m, f_m = so.scan_sequential(d, mutation=k)
+    y_q, f_q = so.scan_quadratic(d)
+    failures += rel(y_m, y_q) > 1e-9 or rel(f_m, f_q) > 1e-9
+    # pin B: the page's printed worked example
+    g = json.load(open(os.path.join(GOLDEN, "p1_worked_example.json")))
+    for G in (1, 2, 4):
+        failures += abs(_p1_block_out(G, True, mutation=k) - g["printed"]["combined"][str(G)]) > 1.5e-4
+    assert failures > 0, f"mutation {k} ({MUTATIONS[k]}) not caught"
