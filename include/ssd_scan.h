@@ -1,0 +1,176 @@
+/*
+ * ssd_scan.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked-scan forward.
+ *
+ * The operation (one independent recurrence per batch row b and head h, with
+ * B/C group g = h / (nheads / ngroups)):
+ *
+ *   dt_t = clamp(softplus(dt_raw[b,t,h] + dt_bias[h]))
+ *   h_t  = exp(dt_t * A[h]) * h_{t-1} + dt_t * x[b,t,h,:] (outer) B[b,t,g,:]
+ *   y_t  = h_t . C[b,t,g,:] + D[h] * x[b,t,h,:],   out = y_t * silu(z[b,t,h,:])
+ *
+ * The argument set (dt_bias, dt_limit, D, z with the "silu" activation,
+ * initial_states, seq_idx, chunk_size, returned final states) is the one of
+ * the mamba_split_conv1d_scan_combined / mamba_chunk_scan_combined calls in
+ * the repro script of state-spaces/mamba issue #647.  The layout
+ * [batch, seq, head, hidden] of x, z and out is the "mamba2_ssd" layout named
+ * in the differences list of fla-org/flash-linear-attention PR #49, which
+ * also states that B/C are shared by groups of heads.  Initial and final
+ * states give chunked prefill as described in state-spaces/mamba PR #488.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, dense
+ *    row-major (C-contiguous) in the layout given, 16-byte aligned.  The
+ *    library keeps no pointer after the call returns.
+ *  - "x dtype" is the dtype argument: SSD_DTYPE_F32 (float) or
+ *    SSD_DTYPE_BF16 (__nv_bfloat16).  dt_bias, A, D, states are float.
+ *  - Everything is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream); no call synchronises the host.  Inputs must stay valid
+ *    and unmodified until the work completes on that stream.
+ *  - Arguments are validated before anything is launched.  On error nothing
+ *    is launched, a negative SSD_ERR_* code is returned and
+ *    ssd_last_error() describes it (per host thread).
+ *  - Sizes: headdim in {16, 32, 64, 128}; dstate a multiple of 16 in
+ *    [16, 256]; chunk_size in {16, 32, 64, 128, 256}; nheads divisible by
+ *    ngroups; batch >= 1; seqlen >= 1.
+ */
+#ifndef SSD_SCAN_H
+#define SSD_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_ABI_VERSION 1
+
+typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype_t;
+
+enum {
+    SSD_OK = 0,
+    SSD_ERR_ARG = -1,          /* bad size, option or dtype                  */
+    SSD_ERR_NULL = -2,         /* a required pointer is NULL                 */
+    SSD_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned           */
+    SSD_ERR_UNSUPPORTED = -4,  /* valid but outside the supported shapes     */
+    SSD_ERR_WORKSPACE = -5,    /* caller workspace too small                 */
+    SSD_ERR_CUDA = -6          /* a CUDA runtime call or launch failed       */
+};
+
+/* Version of this ABI.  New behaviour goes into new symbols; an existing
+ * signature is never changed in place (an in-place change of a native fwd
+ * signature broke its callers in state-spaces/mamba PR #488). */
+int ssd_abi_version(void);
+
+/* Message for the last error returned on the calling host thread ("" if
+ * none).  The string stays valid until the next call on that thread. */
+const char *ssd_last_error(void);
+
+/* Bytes of device workspace ssd_scan_fwd needs for these sizes: processed
+ * dt and per-chunk cumsum [batch, nheads, nchunks, chunk_size] float each,
+ * per-chunk segment counts [batch, nchunks, chunk_size] int32, and chunk
+ * states [batch, nchunks, nheads, headdim, dstate] float.  0 on bad sizes. */
+size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
+                                int headdim, int dstate, int ngroups,
+                                int chunk_size, ssd_dtype_t dtype);
+
+/*
+ * Full SSD chunked-scan forward.
+ *
+ *   x              [batch, seqlen, nheads, headdim]   x dtype
+ *   dt             [batch, seqlen, nheads]            x dtype (raw, before bias)
+ *   dt_bias        [nheads] float, or NULL (= 0)
+ *   dt_softplus    nonzero: dt = softplus(dt + dt_bias)
+ *   dt_limit_lo/hi clamp of dt after softplus; (0, +inf) means no clamp
+ *   A              [nheads] float (negative for a decaying state)
+ *   B, C           [batch, seqlen, ngroups, dstate]   x dtype
+ *   D              [nheads] float, or NULL (= 0)
+ *   z              [batch, seqlen, nheads, headdim]   x dtype, or NULL (no gate)
+ *   initial_states [batch, nheads, headdim, dstate] float, or NULL (= 0)
+ *   seq_idx        [batch, seqlen] int32, or NULL.  The state is reset to
+ *                  zero before token t whenever seq_idx[b,t] != seq_idx[b,t-1]
+ *                  (packed documents); initial_states then only reach the
+ *                  first document.
+ *   chunk_size     chunk length of the chunked algorithm (the result does not
+ *                  depend on it beyond rounding)
+ *   out            [batch, seqlen, nheads, headdim]   x dtype (written)
+ *   final_states   [batch, nheads, headdim, dstate] float, or NULL; the
+ *                  state after the last token (written)
+ *   workspace      device buffer of >= ssd_scan_workspace_bytes(...) bytes,
+ *                  or NULL: the library then takes it from the stream-ordered
+ *                  allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *   stream         cudaStream_t
+ * Returns SSD_OK or a negative SSD_ERR_* code.
+ */
+int ssd_scan_fwd(const void *x, const void *dt, const float *dt_bias,
+                 int dt_softplus, float dt_limit_lo, float dt_limit_hi,
+                 const float *A, const void *B, const void *C, const float *D,
+                 const void *z, const float *initial_states,
+                 const int32_t *seq_idx, int64_t batch, int64_t seqlen,
+                 int nheads, int headdim, int dstate, int ngroups,
+                 int chunk_size, ssd_dtype_t dtype, void *out,
+                 float *final_states, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The four stages of ssd_scan_fwd, exposed one by one (same conventions).
+ * nchunks = ceil(seqlen / chunk_size).  Chunk-major intermediates:
+ *   dt_out, dA_cumsum  [batch, nheads, nchunks, chunk_size] float
+ *   chunk_seg          [batch, nchunks, chunk_size] int32: for each token,
+ *                      the number of seq_idx changes (state resets) from the
+ *                      chunk's first token up to and including it; 0 means
+ *                      "same document as the token before the chunk".
+ *   states             [batch, nchunks, nheads, headdim, dstate] float
+ * Positions past seqlen in the last chunk hold dt = 0, the chunk's last
+ * cumsum and last segment count.
+ * ------------------------------------------------------------------------- */
+
+/* Stage 1: dt preprocessing (bias, softplus, clamp) fused with the
+ * inclusive per-chunk cumsum of dt*A.  chunk_seg may be NULL iff seq_idx is
+ * NULL. */
+int ssd_dt_cumsum(const void *dt, const float *dt_bias, int dt_softplus,
+                  float dt_limit_lo, float dt_limit_hi, const float *A,
+                  const int32_t *seq_idx, int64_t batch, int64_t seqlen,
+                  int nheads, int chunk_size, ssd_dtype_t dtype,
+                  float *dt_out, float *dA_cumsum, int32_t *chunk_seg,
+                  void *stream);
+
+/* Stage 2: chunk states, for each (b, chunk c, head h):
+ *   states[b,c,h,p,n] = sum_{j in c, same segment as the chunk's last token}
+ *        exp(cs_last - cs_j) * dt_j * x[b,j,h,p] * B[b,j,g,n]
+ * chunk_seg may be NULL (no resets). */
+int ssd_chunk_state(const void *x, const void *B, const float *dt_out,
+                    const float *dA_cumsum, const int32_t *chunk_seg,
+                    int64_t batch, int64_t seqlen, int nheads, int headdim,
+                    int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype,
+                    float *states, void *stream);
+
+/* Stage 3: inter-chunk state passing, sequential over chunks, in place:
+ * on entry states[b,c] holds chunk c's own state S_c; on return it holds the
+ * state entering chunk c, H_{c-1}, with H_{-1} = initial_states (or 0) and
+ *   H_c = [no reset in chunk c] * exp(cs_last(c)) * H_{c-1} + S_c.
+ * final_states (may be NULL) receives H_{nchunks-1}. */
+int ssd_state_passing(float *states, const float *dA_cumsum,
+                      const int32_t *chunk_seg, const float *initial_states,
+                      float *final_states, int64_t batch, int64_t seqlen,
+                      int nheads, int headdim, int dstate, int chunk_size,
+                      void *stream);
+
+/* Stage 4: outputs.  For token i of chunk c:
+ *   y_i = sum_{j<=i in c, same segment} exp(cs_i - cs_j) (C_i . B_j) dt_j x_j
+ *       + [no reset since the chunk start] exp(cs_i) * (H_{c-1} . C_i)
+ *       + D x_i,            out_i = y_i * silu(z_i)  (z may be NULL)
+ * prev_states is stage 3's output. */
+int ssd_chunk_scan(const void *x, const void *B, const void *C,
+                   const float *dt_out, const float *dA_cumsum,
+                   const int32_t *chunk_seg, const float *prev_states,
+                   const float *D, const void *z, int64_t batch,
+                   int64_t seqlen, int nheads, int headdim, int dstate,
+                   int ngroups, int chunk_size, ssd_dtype_t dtype, void *out,
+                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_SCAN_H */

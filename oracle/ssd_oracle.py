@@ -153,9 +153,9 @@ def scan_sequential(inp: dict, nthreads: Optional[int] = None, mutation: int = 0
     workloads; the returned arrays then cover only that subset, in the order
     given.
     """
-    u = _unpack(inp)
     if heads is not None or batches is not None:
-        u = _subset(u, heads, batches)
+        inp = select(inp, heads, batches)
+    u = _unpack(inp)
     Bsz, L, H, P, N, G = (u["batch"], u["seqlen"], u["nheads"], u["headdim"],
                           u["dstate"], u["ngroups"])
     out = np.empty((Bsz, L, H, P), dtype=np.float64)
@@ -171,30 +171,39 @@ def scan_sequential(inp: dict, nthreads: Optional[int] = None, mutation: int = 0
     return out, final
 
 
-def _subset(u: dict, heads, batches) -> dict:
-    """Restrict to the given batch rows and heads; each selected head keeps
-    its own B/C group by giving it a private group (G' = #heads)."""
-    u = dict(u)
-    H = u["nheads"]
-    hpg = H // u["ngroups"]
-    bsel = np.arange(u["batch"]) if batches is None else np.asarray(batches)
-    hsel = np.arange(H) if heads is None else np.asarray(heads)
-    gsel = hsel // hpg
-    u["x"] = np.ascontiguousarray(u["x"][bsel][:, :, hsel])
-    u["dt"] = np.ascontiguousarray(u["dt"][bsel][:, :, hsel])
-    if u["z"] is not None:
-        u["z"] = np.ascontiguousarray(u["z"][bsel][:, :, hsel])
-    u["B"] = np.ascontiguousarray(u["B"][bsel][:, :, gsel])
-    u["C"] = np.ascontiguousarray(u["C"][bsel][:, :, gsel])
+def select(inp: dict, heads=None, batches=None) -> dict:
+    """Restrict raw inputs to the given batch rows and heads, before any
+    upcast.  Each selected head keeps its own B/C group by becoming its own
+    group (G' = number of selected heads), so the result of the recurrence
+    for every selected (batch, head) pair is unchanged."""
+    import torch
+    x = inp["x"]
+    Bsz, _, H, _ = x.shape
+    G = inp["B"].shape[2]
+    bsel = list(range(Bsz)) if batches is None else [int(b) for b in batches]
+    hsel = list(range(H)) if heads is None else [int(h) for h in heads]
+    gsel = [h // (H // G) for h in hsel]
+
+    def pick(t, dims):
+        if t is None:
+            return None
+        t = torch.as_tensor(t)
+        for dim, idx in dims:
+            t = t.index_select(dim, torch.tensor(idx, dtype=torch.long))
+        return t.contiguous()
+
+    e = dict(inp)
+    e["x"] = pick(inp["x"], [(0, bsel), (2, hsel)])
+    e["dt"] = pick(inp["dt"], [(0, bsel), (2, hsel)])
+    e["z"] = pick(inp.get("z"), [(0, bsel), (2, hsel)])
+    gdims = [(0, bsel)] if heads is None else [(0, bsel), (2, gsel)]
+    e["B"] = pick(inp["B"], gdims)       # all heads kept: groups unchanged
+    e["C"] = pick(inp["C"], gdims)
     for k in ("dt_bias", "A", "D"):
-        if u[k] is not None:
-            u[k] = np.ascontiguousarray(u[k][hsel])
-    if u["init"] is not None:
-        u["init"] = np.ascontiguousarray(u["init"][bsel][:, hsel])
-    if u["seq_idx"] is not None:
-        u["seq_idx"] = np.ascontiguousarray(u["seq_idx"][bsel])
-    u["batch"], u["nheads"], u["ngroups"] = len(bsel), len(hsel), len(hsel)
-    return u
+        e[k] = pick(inp.get(k), [(0, hsel)])
+    e["initial_states"] = pick(inp.get("initial_states"), [(0, bsel), (1, hsel)])
+    e["seq_idx"] = pick(inp.get("seq_idx"), [(0, bsel)])
+    return e
 
 
 # ----------------------------------------------------------------------------

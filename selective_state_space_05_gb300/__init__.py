@@ -1,0 +1,7 @@
+"""GB300-native (sm_103a) Mamba-2 SSD chunked-scan forward.
+
+The computation lives in ``libssd_gb300.so`` (CUDA kernels behind the C ABI
+of include/ssd_scan.h); this package only marshals torch tensors into it.
+"""
+from .scan import (abi_version, ssd_chunk_scan, ssd_chunk_state,  # noqa: F401
+                   ssd_dt_cumsum, ssd_scan_fwd, ssd_state_passing, workspace_bytes)

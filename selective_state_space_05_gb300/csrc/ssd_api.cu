@@ -1,0 +1,286 @@
+// C-ABI entry points of the SSD chunked-scan library: argument validation,
+// workspace carving and the launch sequence.  Declared in include/ssd_scan.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/ssd_scan.h"
+#include "ssd_common.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(SSD_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Validates sizes shared by every entry point and fills Dims.  need_state:
+// headdim/dstate/ngroups are used by this entry point.
+int check_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+               int chunk, bool need_state, ssd::Dims* d) {
+  if (batch < 1 || seqlen < 1 || nheads < 1)
+    return fail(SSD_ERR_ARG, "batch, seqlen and nheads must be >= 1 (got %lld, %lld, %d)",
+                (long long)batch, (long long)seqlen, nheads);
+  if (!(chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128 || chunk == 256))
+    return fail(SSD_ERR_UNSUPPORTED, "chunk_size must be one of 16, 32, 64, 128, 256 (got %d)",
+                chunk);
+  if (batch > 65535) return fail(SSD_ERR_UNSUPPORTED, "batch > 65535");
+  if (nheads > 65535) return fail(SSD_ERR_UNSUPPORTED, "nheads > 65535");
+  if (need_state) {
+    if (ngroups < 1 || nheads % ngroups != 0)
+      return fail(SSD_ERR_ARG, "nheads (%d) must be a positive multiple of ngroups (%d)",
+                  nheads, ngroups);
+    if (!(headdim == 16 || headdim == 32 || headdim == 64 || headdim == 128))
+      return fail(SSD_ERR_UNSUPPORTED, "headdim must be one of 16, 32, 64, 128 (got %d)",
+                  headdim);
+    if (dstate < 16 || dstate > 256 || dstate % 16 != 0)
+      return fail(SSD_ERR_UNSUPPORTED, "dstate must be a multiple of 16 in [16, 256] (got %d)",
+                  dstate);
+  }
+  const int64_t nc = (seqlen + chunk - 1) / chunk;
+  if (nc * (int64_t)batch > 65535LL * 1024)
+    return fail(SSD_ERR_UNSUPPORTED, "batch * nchunks too large");
+  d->batch = batch;
+  d->seqlen = seqlen;
+  d->nheads = nheads;
+  d->headdim = headdim;
+  d->dstate = dstate;
+  d->ngroups = ngroups;
+  d->chunk = chunk;
+  d->nchunks = (int)nc;
+  return SSD_OK;
+}
+
+int check_dtype(ssd_dtype_t t) {
+  if (t != SSD_DTYPE_F32 && t != SSD_DTYPE_BF16) return fail(SSD_ERR_ARG, "unknown dtype %d", (int)t);
+  return SSD_OK;
+}
+
+struct Workspace {
+  float* dt;
+  float* cs;
+  int32_t* seg;
+  float* states;
+  size_t bytes;
+};
+
+Workspace carve(const ssd::Dims& d, void* base) {
+  const size_t nq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk;
+  const size_t sq = (size_t)d.batch * d.nchunks * d.chunk;
+  const size_t st = (size_t)d.batch * d.nchunks * d.nheads * d.headdim * d.dstate;
+  Workspace w;
+  size_t off = 0;
+  char* p = static_cast<char*>(base);
+  w.dt = reinterpret_cast<float*>(p + off);
+  off = round_up(off + nq * sizeof(float), 256);
+  w.cs = reinterpret_cast<float*>(p + off);
+  off = round_up(off + nq * sizeof(float), 256);
+  w.seg = reinterpret_cast<int32_t*>(p + off);
+  off = round_up(off + sq * sizeof(int32_t), 256);
+  w.states = reinterpret_cast<float*>(p + off);
+  off = round_up(off + st * sizeof(float), 256);
+  w.bytes = off;
+  return w;
+}
+
+int do_clamp_of(float lo, float hi) { return !(lo == 0.f && isinf(hi) && hi > 0.f); }
+
+}  // namespace
+
+extern "C" {
+
+int ssd_abi_version(void) { return SSD_ABI_VERSION; }
+
+const char* ssd_last_error(void) { return g_err; }
+
+size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int headdim,
+                                int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype) {
+  ssd::Dims d;
+  if (check_dtype(dtype) != SSD_OK) return 0;
+  if (check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d) != SSD_OK)
+    return 0;
+  return carve(d, nullptr).bytes;
+}
+
+int ssd_dt_cumsum(const void* dt, const float* dt_bias, int dt_softplus, float lo, float hi,
+                  const float* A, const int32_t* seq_idx, int64_t batch, int64_t seqlen,
+                  int nheads, int chunk_size, ssd_dtype_t dtype, float* dt_out,
+                  float* dA_cumsum, int32_t* chunk_seg, void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_dims(batch, seqlen, nheads, 16, 16, 1, chunk_size, false, &d);
+  if (rc) return rc;
+  if (!dt || !A || !dt_out || !dA_cumsum)
+    return fail(SSD_ERR_NULL, "dt, A, dt_out, dA_cumsum are required");
+  if (seq_idx && !chunk_seg) return fail(SSD_ERR_NULL, "chunk_seg is required with seq_idx");
+  if (!(lo <= hi)) return fail(SSD_ERR_ARG, "dt_limit lo > hi");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == SSD_DTYPE_F32)
+    e = ssd::launch_dt_cumsum<float>(static_cast<const float*>(dt), dt_bias, dt_softplus, lo, hi,
+                                     do_clamp_of(lo, hi), A, seq_idx, d, dt_out, dA_cumsum,
+                                     chunk_seg, st);
+  else
+    e = ssd::launch_dt_cumsum<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(dt), dt_bias,
+                                             dt_softplus, lo, hi, do_clamp_of(lo, hi), A, seq_idx,
+                                             d, dt_out, dA_cumsum, chunk_seg, st);
+  return e == cudaSuccess ? SSD_OK : cuda_fail(e, "dt_cumsum launch");
+}
+
+int ssd_chunk_state(const void* x, const void* B, const float* dt_out, const float* dA_cumsum,
+                    const int32_t* chunk_seg, int64_t batch, int64_t seqlen, int nheads,
+                    int headdim, int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype,
+                    float* states, void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d);
+  if (rc) return rc;
+  if (!x || !B || !dt_out || !dA_cumsum || !states)
+    return fail(SSD_ERR_NULL, "x, B, dt_out, dA_cumsum, states are required");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == SSD_DTYPE_F32)
+    e = ssd::launch_chunk_state<float>(static_cast<const float*>(x), static_cast<const float*>(B),
+                                       dt_out, dA_cumsum, chunk_seg, d, states, st);
+  else
+    e = ssd::launch_chunk_state<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x),
+                                               static_cast<const __nv_bfloat16*>(B), dt_out,
+                                               dA_cumsum, chunk_seg, d, states, st);
+  return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_state launch");
+}
+
+int ssd_state_passing(float* states, const float* dA_cumsum, const int32_t* chunk_seg,
+                      const float* initial_states, float* final_states, int64_t batch,
+                      int64_t seqlen, int nheads, int headdim, int dstate, int chunk_size,
+                      void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dims(batch, seqlen, nheads, headdim, dstate, 1, chunk_size, true, &d);
+  if (rc) return rc;
+  if (!states || !dA_cumsum) return fail(SSD_ERR_NULL, "states and dA_cumsum are required");
+  if (!aligned16(states) || !aligned16(initial_states) || !aligned16(final_states))
+    return fail(SSD_ERR_ALIGN, "states, initial_states, final_states must be 16-byte aligned");
+  cudaError_t e = ssd::launch_state_passing(states, dA_cumsum, chunk_seg, initial_states,
+                                            final_states, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSD_OK : cuda_fail(e, "state_passing launch");
+}
+
+int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_out,
+                   const float* dA_cumsum, const int32_t* chunk_seg, const float* prev_states,
+                   const float* D, const void* z, int64_t batch, int64_t seqlen, int nheads,
+                   int headdim, int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype,
+                   void* out, void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d);
+  if (rc) return rc;
+  if (!x || !B || !C || !dt_out || !dA_cumsum || !prev_states || !out)
+    return fail(SSD_ERR_NULL, "x, B, C, dt_out, dA_cumsum, prev_states, out are required");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == SSD_DTYPE_F32)
+    e = ssd::launch_chunk_scan<float>(
+        static_cast<const float*>(x), static_cast<const float*>(B), static_cast<const float*>(C),
+        dt_out, dA_cumsum, chunk_seg, prev_states, D, static_cast<const float*>(z), d,
+        static_cast<float*>(out), st);
+  else
+    e = ssd::launch_chunk_scan<__nv_bfloat16>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
+        static_cast<const __nv_bfloat16*>(C), dt_out, dA_cumsum, chunk_seg, prev_states, D,
+        static_cast<const __nv_bfloat16*>(z), d, static_cast<__nv_bfloat16*>(out), st);
+  return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_scan launch");
+}
+
+int ssd_scan_fwd(const void* x, const void* dt, const float* dt_bias, int dt_softplus,
+                 float dt_limit_lo, float dt_limit_hi, const float* A, const void* B,
+                 const void* C, const float* D, const void* z, const float* initial_states,
+                 const int32_t* seq_idx, int64_t batch, int64_t seqlen, int nheads, int headdim,
+                 int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype, void* out,
+                 float* final_states, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d);
+  if (rc) return rc;
+  if (!x || !dt || !A || !B || !C || !out)
+    return fail(SSD_ERR_NULL, "x, dt, A, B, C and out are required");
+  if (!(dt_limit_lo <= dt_limit_hi)) return fail(SSD_ERR_ARG, "dt_limit lo > hi");
+  const void* ptrs[] = {x, dt, dt_bias, A, B, C, D, z, initial_states, seq_idx, out,
+                        final_states, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t need = carve(d, nullptr).bytes;
+  void* base = workspace;
+  bool owned = false;
+  if (base == nullptr) {
+    cudaError_t e = cudaMallocAsync(&base, need, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+    owned = true;
+  } else if (workspace_bytes < need) {
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  }
+  Workspace w = carve(d, base);
+  int32_t* seg = seq_idx ? w.seg : nullptr;
+  const int clamp = do_clamp_of(dt_limit_lo, dt_limit_hi);
+  cudaError_t e;
+  if (dtype == SSD_DTYPE_F32) {
+    const float* xf = static_cast<const float*>(x);
+    e = ssd::launch_dt_cumsum<float>(static_cast<const float*>(dt), dt_bias, dt_softplus,
+                                     dt_limit_lo, dt_limit_hi, clamp, A, seq_idx, d, w.dt, w.cs,
+                                     seg, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_chunk_state<float>(xf, static_cast<const float*>(B), w.dt, w.cs, seg, d,
+                                         w.states, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, d, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_chunk_scan<float>(xf, static_cast<const float*>(B),
+                                        static_cast<const float*>(C), w.dt, w.cs, seg, w.states,
+                                        D, static_cast<const float*>(z), d,
+                                        static_cast<float*>(out), st);
+  } else {
+    using bf = __nv_bfloat16;
+    const bf* xb = static_cast<const bf*>(x);
+    e = ssd::launch_dt_cumsum<bf>(static_cast<const bf*>(dt), dt_bias, dt_softplus, dt_limit_lo,
+                                  dt_limit_hi, clamp, A, seq_idx, d, w.dt, w.cs, seg, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_chunk_state<bf>(xb, static_cast<const bf*>(B), w.dt, w.cs, seg, d,
+                                      w.states, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, d, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_chunk_scan<bf>(xb, static_cast<const bf*>(B), static_cast<const bf*>(C),
+                                     w.dt, w.cs, seg, w.states, D, static_cast<const bf*>(z), d,
+                                     static_cast<bf*>(out), st);
+  }
+  if (owned) {
+    cudaError_t e2 = cudaFreeAsync(base, st);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? SSD_OK : cuda_fail(e, "ssd_scan_fwd launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Shared device helpers and the launcher interface between the C-ABI layer
+// (ssd_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// 2^x on the SFU (PTX ex2.approx, flush-to-zero).  Every exponential of the
+// scan is exp(v) with v <= 0 (a decay), evaluated as 2^(v*log2 e).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Problem sizes as every launcher sees them.
+struct Dims {
+  int64_t batch, seqlen;
+  int nheads, headdim, dstate, ngroups, chunk;
+  int nchunks;
+};
+
+// Launchers (return cudaGetLastError() of their launches).
+template <typename T>
+cudaError_t launch_dt_cumsum(const T* dt, const float* dt_bias, int softplus, float lo,
+                             float hi, int do_clamp, const float* A, const int32_t* seq_idx,
+                             const Dims& d, float* dt_out, float* cs, int32_t* seg,
+                             cudaStream_t st);
+template <typename T>
+cudaError_t launch_chunk_state(const T* x, const T* B, const float* dt_out, const float* cs,
+                               const int32_t* seg, const Dims& d, float* states,
+                               cudaStream_t st);
+cudaError_t launch_state_passing(float* states, const float* cs, const int32_t* seg,
+                                 const float* init, float* final_states, const Dims& d,
+                                 cudaStream_t st);
+template <typename T>
+cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* dt_out,
+                              const float* cs, const int32_t* seg, const float* prev,
+                              const float* D, const T* z, const Dims& d, T* out,
+                              cudaStream_t st);
+
+}  // namespace ssd

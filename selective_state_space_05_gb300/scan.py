@@ -1,0 +1,205 @@
+"""Python binding of the SSD chunked-scan C ABI (include/ssd_scan.h).
+
+Argument marshalling only: checks that torch tensors are CUDA, contiguous and
+of the expected dtypes, allocates outputs and workspace with torch, and passes
+raw device pointers plus the current CUDA stream to the library.  Every step
+of the computation runs in the library's kernels.  Names and argument meaning
+follow the C functions of the same names.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+_DT = {torch.float32: _lib.SSD_DTYPE_F32, torch.bfloat16: _lib.SSD_DTYPE_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, device=None,
+          optional=False) -> None:
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def abi_version() -> int:
+    return _lib.load().ssd_abi_version()
+
+
+def workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
+                    dtype=torch.bfloat16) -> int:
+    return int(_lib.load().ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                                    ngroups, chunk_size, _DT[dtype]))
+
+
+def ssd_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                 C: torch.Tensor, *, chunk_size: int = 256,
+                 dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
+                 dt_limit: Tuple[float, float] = (0.0, math.inf),
+                 D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                 initial_states: Optional[torch.Tensor] = None,
+                 seq_idx: Optional[torch.Tensor] = None, return_final_states: bool = False,
+                 out: Optional[torch.Tensor] = None,
+                 final_states: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+    """SSD chunked-scan forward.  x, z, out: [batch, seqlen, nheads, headdim];
+    dt: [batch, seqlen, nheads] (x dtype); B, C: [batch, seqlen, ngroups, dstate];
+    dt_bias, A, D: [nheads] fp32; states [batch, nheads, headdim, dstate] fp32;
+    seq_idx [batch, seqlen] int32.  Returns out, or (out, final_states)."""
+    if x.dtype not in _DT:
+        raise ValueError(f"x must be float32 or bfloat16, got {x.dtype}")
+    dev = x.device
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    xd = x.dtype
+    _need(x, "x", xd, device=dev)
+    _need(dt, "dt", xd, (Bsz, L, H), dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(B, "B", xd, (Bsz, L, G, N), dev)
+    _need(C, "C", xd, (Bsz, L, G, N), dev)
+    _need(dt_bias, "dt_bias", torch.float32, (H,), dev, optional=True)
+    _need(D, "D", torch.float32, (H,), dev, optional=True)
+    _need(z, "z", xd, (Bsz, L, H, P), dev, optional=True)
+    _need(initial_states, "initial_states", torch.float32, (Bsz, H, P, N), dev, optional=True)
+    _need(seq_idx, "seq_idx", torch.int32, (Bsz, L), dev, optional=True)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", xd, (Bsz, L, H, P), dev)
+    if return_final_states and final_states is None:
+        final_states = torch.empty(Bsz, H, P, N, dtype=torch.float32, device=dev)
+    _need(final_states, "final_states", torch.float32, (Bsz, H, P, N), dev, optional=True)
+    lib = _lib.load()
+    ws_need = int(lib.ssd_scan_workspace_bytes(Bsz, L, H, P, N, G, chunk_size, _DT[xd]))
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lo, hi = dt_limit
+    _lib.check(lib.ssd_scan_fwd(
+        _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi),
+        _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(initial_states), _ptr(seq_idx),
+        Bsz, L, H, P, N, G, int(chunk_size), _DT[xd], _ptr(out), _ptr(final_states),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+    if return_final_states:
+        return out, final_states
+    return out
+
+
+# --- the four stages, one call each -----------------------------------------
+
+def ssd_dt_cumsum(dt: torch.Tensor, A: torch.Tensor, *, chunk_size: int,
+                  dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
+                  dt_limit: Tuple[float, float] = (0.0, math.inf),
+                  seq_idx: Optional[torch.Tensor] = None, stream=None):
+    """Stage 1.  Returns (dt_out, dA_cumsum, chunk_seg or None), the first two
+    [batch, nheads, nchunks, chunk_size] fp32, chunk_seg
+    [batch, nchunks, chunk_size] int32."""
+    Bsz, L, H = dt.shape
+    dev = dt.device
+    _need(dt, "dt", None, device=dev)
+    if dt.dtype not in _DT:
+        raise ValueError("dt must be float32 or bfloat16")
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(dt_bias, "dt_bias", torch.float32, (H,), dev, optional=True)
+    _need(seq_idx, "seq_idx", torch.int32, (Bsz, L), dev, optional=True)
+    nc = (L + chunk_size - 1) // chunk_size
+    dt_out = torch.empty(Bsz, H, nc, chunk_size, dtype=torch.float32, device=dev)
+    cs = torch.empty_like(dt_out)
+    seg = (torch.empty(Bsz, nc, chunk_size, dtype=torch.int32, device=dev)
+           if seq_idx is not None else None)
+    lo, hi = dt_limit
+    _lib.check(_lib.load().ssd_dt_cumsum(
+        _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi), _ptr(A),
+        _ptr(seq_idx), Bsz, L, H, int(chunk_size), _DT[dt.dtype], _ptr(dt_out), _ptr(cs),
+        _ptr(seg), _stream(stream)))
+    return dt_out, cs, seg
+
+
+def ssd_chunk_state(x: torch.Tensor, B: torch.Tensor, dt_out: torch.Tensor,
+                    dA_cumsum: torch.Tensor, chunk_seg: Optional[torch.Tensor], *,
+                    chunk_size: int, stream=None) -> torch.Tensor:
+    """Stage 2.  Returns states [batch, nchunks, nheads, headdim, dstate] fp32."""
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    nc = (L + chunk_size - 1) // chunk_size
+    _need(x, "x", None, device=dev)
+    _need(B, "B", x.dtype, (Bsz, L, G, N), dev)
+    _need(dt_out, "dt_out", torch.float32, (Bsz, H, nc, chunk_size), dev)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, (Bsz, H, nc, chunk_size), dev)
+    _need(chunk_seg, "chunk_seg", torch.int32, (Bsz, nc, chunk_size), dev, optional=True)
+    states = torch.empty(Bsz, nc, H, P, N, dtype=torch.float32, device=dev)
+    _lib.check(_lib.load().ssd_chunk_state(
+        _ptr(x), _ptr(B), _ptr(dt_out), _ptr(dA_cumsum), _ptr(chunk_seg), Bsz, L, H, P, N, G,
+        int(chunk_size), _DT[x.dtype], _ptr(states), _stream(stream)))
+    return states
+
+
+def ssd_state_passing(states: torch.Tensor, dA_cumsum: torch.Tensor,
+                      chunk_seg: Optional[torch.Tensor], *, seqlen: int, chunk_size: int,
+                      initial_states: Optional[torch.Tensor] = None,
+                      return_final_states: bool = True, stream=None):
+    """Stage 3, in place on ``states``.  Returns final_states (or None)."""
+    Bsz, nc, H, P, N = states.shape
+    dev = states.device
+    _need(states, "states", torch.float32, device=dev)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, (Bsz, H, nc, chunk_size), dev)
+    _need(chunk_seg, "chunk_seg", torch.int32, (Bsz, nc, chunk_size), dev, optional=True)
+    _need(initial_states, "initial_states", torch.float32, (Bsz, H, P, N), dev, optional=True)
+    fin = (torch.empty(Bsz, H, P, N, dtype=torch.float32, device=dev)
+           if return_final_states else None)
+    _lib.check(_lib.load().ssd_state_passing(
+        _ptr(states), _ptr(dA_cumsum), _ptr(chunk_seg), _ptr(initial_states), _ptr(fin),
+        Bsz, int(seqlen), H, P, N, int(chunk_size), _stream(stream)))
+    return fin
+
+
+def ssd_chunk_scan(x: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dt_out: torch.Tensor,
+                   dA_cumsum: torch.Tensor, chunk_seg: Optional[torch.Tensor],
+                   prev_states: torch.Tensor, *, chunk_size: int,
+                   D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Stage 4.  Returns out [batch, seqlen, nheads, headdim] in x's dtype."""
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    nc = (L + chunk_size - 1) // chunk_size
+    _need(x, "x", None, device=dev)
+    _need(B, "B", x.dtype, (Bsz, L, G, N), dev)
+    _need(C, "C", x.dtype, (Bsz, L, G, N), dev)
+    _need(dt_out, "dt_out", torch.float32, (Bsz, H, nc, chunk_size), dev)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, (Bsz, H, nc, chunk_size), dev)
+    _need(chunk_seg, "chunk_seg", torch.int32, (Bsz, nc, chunk_size), dev, optional=True)
+    _need(prev_states, "prev_states", torch.float32, (Bsz, nc, H, P, N), dev)
+    _need(D, "D", torch.float32, (H,), dev, optional=True)
+    _need(z, "z", x.dtype, (Bsz, L, H, P), dev, optional=True)
+    if out is None:
+        out = torch.empty_like(x)
+    _lib.check(_lib.load().ssd_chunk_scan(
+        _ptr(x), _ptr(B), _ptr(C), _ptr(dt_out), _ptr(dA_cumsum), _ptr(chunk_seg),
+        _ptr(prev_states), _ptr(D), _ptr(z), Bsz, L, H, P, N, G, int(chunk_size),
+        _DT[x.dtype], _ptr(out), _stream(stream)))
+    return out

@@ -1,0 +1,92 @@
+"""The C-ABI library loads and exports every symbol include/*.h declares;
+host-side validation answers before anything touches a GPU."""
+import ctypes
+import math
+import re
+from pathlib import Path
+
+import pytest
+
+from selective_state_space_05_gb300 import _lib
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+def declared_functions():
+    names = []
+    for h in sorted((ROOT / "include").glob("*.h")):
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(ssd_[a-z0-9_]+)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from selective_state_space_05_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_expected_calls():
+    names = declared_functions()
+    for n in ("ssd_scan_fwd", "ssd_last_error", "ssd_abi_version", "ssd_scan_workspace_bytes",
+              "ssd_dt_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"binding lacks {n}"
+
+
+def test_abi_version(lib):
+    assert lib.ssd_abi_version() == 1
+
+
+def test_workspace_bytes(lib):
+    # dt + cumsum [B,H,nc,Q] f32, segments [B,nc,Q] i32, states [B,nc,H,P,N] f32
+    B, L, H, P, N, G, Q = 8, 4096, 80, 64, 128, 1, 256
+    nc = L // Q
+    want = 2 * B * H * nc * Q * 4 + B * nc * Q * 4 + B * nc * H * P * N * 4
+    got = lib.ssd_scan_workspace_bytes(B, L, H, P, N, G, Q, _lib.SSD_DTYPE_BF16)
+    assert want <= got <= want + 4 * 256
+    assert lib.ssd_scan_workspace_bytes(B, L, H, P, N, G, 100, 1) == 0      # bad chunk
+    assert lib.ssd_scan_workspace_bytes(B, L, H, 48, N, G, Q, 1) == 0       # bad headdim
+    assert lib.ssd_scan_workspace_bytes(B, L, 80, P, N, 3, Q, 1) == 0       # H % G != 0
+
+
+def _fwd(lib, **kw):
+    a = dict(x=16, dt=16, dt_bias=None, sp=1, lo=0.0, hi=math.inf, A=16, B=16, C=16, D=None,
+             z=None, init=None, seq=None, batch=1, L=64, H=2, P=16, N=16, G=1, Q=64, dtype=0,
+             out=16, fin=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.ssd_scan_fwd(a["x"], a["dt"], a["dt_bias"], a["sp"], a["lo"], a["hi"], a["A"],
+                            a["B"], a["C"], a["D"], a["z"], a["init"], a["seq"], a["batch"],
+                            a["L"], a["H"], a["P"], a["N"], a["G"], a["Q"], a["dtype"], a["out"],
+                            a["fin"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_validation_errors_before_any_launch(lib):
+    # fake (never dereferenced) addresses: validation fails before any CUDA call
+    assert _fwd(lib, Q=100) == -4 and b"chunk_size" in lib.ssd_last_error()
+    assert _fwd(lib, x=None) == -2
+    assert _fwd(lib, x=24) == -3                      # not 16-byte aligned
+    assert _fwd(lib, dtype=7) == -1
+    assert _fwd(lib, H=3, G=2) == -1
+    assert _fwd(lib, P=48) == -4
+    assert _fwd(lib, N=8) == -4
+    assert _fwd(lib, L=0) == -1
+    assert _fwd(lib, lo=1.0, hi=0.5) == -1
+    assert _fwd(lib, ws=4096, wsb=16) == -5           # caller workspace too small
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        saved = _lib._LIB
+        _lib._LIB = None
+        try:
+            _lib.load(tmp_path / "nope.so")
+        finally:
+            _lib._LIB = saved
