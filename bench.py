@@ -106,6 +106,26 @@ def kernel_models(cfg, peaks) -> dict:
     return m
 
 
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/
+    dram_traffic.txt), or None when none was taken or the kernel's source
+    has changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) != 5 or line.startswith("#") or f[0] != kernel or f[4] != workload:
+            continue
+        src = os.path.join(ROOT, f[2])
+        if not os.path.exists(src):
+            return None
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
+        return int(f[1]) if sha == f[3] else None
+    return None
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -329,7 +349,9 @@ def main():
     else:
         achieved, peak, unit = mdl["flops"] / dur_s / 1e12, mdl["peak"] / 1e12, "TFLOP/s"
     roofline = {"kernel": top, "bound": mdl["bound"], "achieved": achieved, "peak": peak,
-                "unit": unit, "frac": achieved / peak, "traffic": None,
+                "unit": unit, "frac": achieved / peak,
+                "traffic": measured_traffic(top, cfg.name),
+                "alg_bytes": mdl["bytes"], "alg_flops": mdl["flops"],
                 "peak_source": peaks.get("source"),
                 "kernel_ms": {n: round(v, 4) for n, v in per.items()},
                 "share": {n: round(v / sum(per.values()), 4) for n, v in per.items()}}

@@ -52,7 +52,7 @@ int check_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstat
                   dstate);
   }
   const int64_t nc = (seqlen + chunk - 1) / chunk;
-  if (nc * (int64_t)batch > 65535LL * 1024)
+  if (nc * (int64_t)batch > 2147483647LL)
     return fail(SSD_ERR_UNSUPPORTED, "batch * nchunks too large");
   d->batch = batch;
   d->seqlen = seqlen;

@@ -119,7 +119,7 @@ cudaError_t launch_dt_cumsum(const T* dt, const float* dt_bias, int softplus, fl
 }
 
 // ---------------------------------------------------------------------------
-// Stage 2: chunk states.  One block per (n-tile, head, batch*chunk) computes
+// Stage 2: chunk states.  One block per (batch*chunk, head, n-tile) computes
 // a [P x NT] tile of S_c as a 32-token-deep SIMT GEMM; the per-token weight
 // w_j is applied to x while it is staged in shared memory.
 // ---------------------------------------------------------------------------
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(
   __shared__ float xs[TJ][P];
   __shared__ float bs[TJ][NT];
   __shared__ float wj[TJ];
-  const int ntile = blockIdx.x, h = blockIdx.y, bc = blockIdx.z;
+  const int bc = blockIdx.x, h = blockIdx.y, ntile = blockIdx.z;
   const int b = bc / d.nchunks, c = bc % d.nchunks;
   const int g = h / (d.nheads / d.ngroups);
   const int Q = d.chunk;
@@ -202,7 +202,7 @@ static cudaError_t chunk_state_p(const T* x, const T* B, const float* dtp, const
                                  const int32_t* seg, const Dims& d, float* states,
                                  cudaStream_t st) {
   const int NT = d.dstate % 64 == 0 ? 64 : (d.dstate % 32 == 0 ? 32 : 16);
-  dim3 grid(d.dstate / NT, d.nheads, (unsigned)(d.batch * d.nchunks));
+  dim3 grid((unsigned)(d.batch * d.nchunks), d.nheads, d.dstate / NT);
   if (NT == 64)
     chunk_state_kernel<T, P, 64><<<grid, 256, 0, st>>>(x, B, dtp, cs, seg, d, states);
   else if (NT == 32)
@@ -280,7 +280,7 @@ cudaError_t launch_state_passing(float* states, const float* cs, const int32_t* 
 }
 
 // ---------------------------------------------------------------------------
-// Stage 4: chunk scan.  One block per (32-row tile, head, batch*chunk); 256
+// Stage 4: chunk scan.  One block per (batch*chunk, head, 32-row tile); 256
 // threads = 32 rows x 8 column groups, each thread accumulating P/8 outputs
 // of its row.  Inter-chunk term first (C_i . H_{c-1}, scaled by exp(cs_i)),
 // then the causal intra-chunk term one 32-token tile at a time, then the
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
   int* sg_i = reinterpret_cast<int*>(cs_j + TJ);
   int* sg_j = sg_i + TI;
 
-  const int rt = blockIdx.x, h = blockIdx.y, bc = blockIdx.z;
+  const int bc = blockIdx.x, h = blockIdx.y, rt = blockIdx.z;
   const int b = bc / d.nchunks, c = bc % d.nchunks;
   const int g = h / (d.nheads / d.ngroups);
   const int Q = d.chunk;
@@ -432,7 +432,7 @@ static cudaError_t chunk_scan_p(const T* x, const T* B, const T* C, const float*
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid((d.chunk + TI - 1) / TI, d.nheads, (unsigned)(d.batch * d.nchunks));
+  dim3 grid((unsigned)(d.batch * d.nchunks), d.nheads, (d.chunk + TI - 1) / TI);
   kern<<<grid, 256, smem, st>>>(x, B, C, dtp, cs, seg, prev, D, z, d, out);
   return cudaGetLastError();
 }
