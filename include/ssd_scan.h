@@ -169,6 +169,44 @@ int ssd_chunk_scan(const void *x, const void *B, const void *C,
                    int ngroups, int chunk_size, ssd_dtype_t dtype, void *out,
                    void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Variant of ssd_scan_fwd that allocates nothing.  (The pages have no
+ * counterpart of this call; it exists for callers of this library.)
+ *
+ * Some callers cannot allocate device memory at all: a host application
+ * whose own allocator owns the whole device and forbids plug-in code from
+ * calling cudaMalloc, or a latency-critical path on which an allocation call,
+ * which can synchronise the device or fail under memory pressure, is not
+ * acceptable.  For them this call keeps its scratch (processed dt, per-chunk
+ * cumsum and reset counts, chunk states) in one static device array of
+ * SSD_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine; the caller still passes all inputs
+ * and outputs, with the arguments and meaning of ssd_scan_fwd.
+ *
+ *  - Sizes whose scratch (ssd_scan_workspace_bytes) exceeds
+ *    SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_WORKSPACE before
+ *    anything is launched; use ssd_scan_fwd with a workspace for those.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last
+ *    call's contents; no part of it needs to start at zero.  Calls whose
+ *    work overlaps on the GPU (different streams, or other host threads)
+ *    race on the array: order them on one stream or serialise them.
+ * ------------------------------------------------------------------------- */
+#define SSD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+int ssd_scan_fwd_noalloc(const void *x, const void *dt, const float *dt_bias,
+                         int dt_softplus, float dt_limit_lo, float dt_limit_hi,
+                         const float *A, const void *B, const void *C,
+                         const float *D, const void *z,
+                         const float *initial_states, const int32_t *seq_idx,
+                         int64_t batch, int64_t seqlen, int nheads, int headdim,
+                         int dstate, int ngroups, int chunk_size,
+                         ssd_dtype_t dtype, void *out, float *final_states,
+                         void *stream);
+
 #ifdef __cplusplus
 }
 #endif

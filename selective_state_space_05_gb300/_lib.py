@@ -12,6 +12,7 @@ LIB_PATH = Path(__file__).resolve().parent / "libssd_gb300.so"
 
 SSD_DTYPE_F32 = 0
 SSD_DTYPE_BF16 = 1
+SSD_NOALLOC_SCRATCH_BYTES = 64 << 20   # static scratch of ssd_scan_fwd_noalloc
 
 SSD_OK = 0
 ERRORS = {-1: "SSD_ERR_ARG", -2: "SSD_ERR_NULL", -3: "SSD_ERR_ALIGN",
@@ -33,6 +34,8 @@ SIGNATURES = {
     "ssd_chunk_state": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _i, _i,
                              _vp, _vp]),
     "ssd_state_passing": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _vp]),
+    "ssd_scan_fwd_noalloc": (_i, [_vp, _vp, _vp, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _i64, _i64, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
     "ssd_chunk_scan": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i,
                             _i, _i, _i, _i, _vp, _vp]),
 }

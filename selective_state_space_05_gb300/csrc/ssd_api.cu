@@ -101,6 +101,11 @@ int do_clamp_of(float lo, float hi) { return !(lo == 0.f && isinf(hi) && hi > 0.
 
 }  // namespace
 
+namespace ssd {
+// Records an error message for ssd_last_error() from another translation unit.
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace ssd
+
 extern "C" {
 
 int ssd_abi_version(void) { return SSD_ABI_VERSION; }

@@ -53,4 +53,7 @@ cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* d
                               const float* D, const T* z, const Dims& d, T* out,
                               cudaStream_t st);
 
+// Sets the per-thread message returned by ssd_last_error(); returns code.
+int set_error(int code, const char* msg);
+
 }  // namespace ssd

@@ -1,0 +1,82 @@
+// ssd_scan_fwd_noalloc: the scan forward for callers that cannot allocate
+// device memory.  The scratch that ssd_scan_fwd would take from the caller or
+// from cudaMallocAsync (processed dt, per-chunk cumsum and reset counts, chunk
+// states) lives here in one file-scope device array instead.
+#include <mutex>
+#include <stdio.h>
+
+#include "../../include/ssd_scan.h"
+#include "ssd_common.cuh"
+
+namespace {
+
+// Fixed scratch, reserved in every GPU's memory when the library's module is
+// loaded on that device and held until the process exits.
+constexpr size_t kScratchBytes = SSD_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_scratch on the current device.  In host code the name
+// g_scratch is only a host-side stand-in; the real address comes from
+// cudaGetSymbolAddress, looked up once per device (with that device current)
+// and cached.
+int scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    char m[256];
+    snprintf(m, sizeof(m), "cudaGetDevice: %s", cudaGetErrorString(e));
+    return ssd::set_error(SSD_ERR_CUDA, m);
+  }
+  if (dev < 0 || dev >= kMaxDevices) return ssd::set_error(SSD_ERR_UNSUPPORTED, "device index too large");
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      char m[256];
+      snprintf(m, sizeof(m), "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+      return ssd::set_error(SSD_ERR_CUDA, m);
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_scan_fwd_noalloc(const void* x, const void* dt, const float* dt_bias, int dt_softplus,
+                         float dt_limit_lo, float dt_limit_hi, const float* A, const void* B,
+                         const void* C, const float* D, const void* z,
+                         const float* initial_states, const int32_t* seq_idx, int64_t batch,
+                         int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                         int chunk_size, ssd_dtype_t dtype, void* out, float* final_states,
+                         void* stream) {
+  const size_t need = ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                               chunk_size, dtype);
+  if (need > kScratchBytes) {
+    char m[256];
+    snprintf(m, sizeof(m),
+             "ssd_scan_fwd_noalloc: these sizes need %zu bytes of scratch but the static "
+             "scratch holds %zu; use ssd_scan_fwd with a workspace",
+             need, kScratchBytes);
+    return ssd::set_error(SSD_ERR_WORKSPACE, m);
+  }
+  void* scratch = nullptr;
+  int rc = scratch_address(&scratch);
+  if (rc != SSD_OK) return rc;
+  // need == 0 means invalid sizes: ssd_scan_fwd reports which one.  Nothing in
+  // the scratch has to start at zero: every element a call reads is written
+  // earlier in the same call.
+  return ssd_scan_fwd(x, dt, dt_bias, dt_softplus, dt_limit_lo, dt_limit_hi, A, B, C, D, z,
+                      initial_states, seq_idx, batch, seqlen, nheads, headdim, dstate, ngroups,
+                      chunk_size, dtype, out, final_states, scratch, kScratchBytes, stream);
+}
+
+}  // extern "C"
