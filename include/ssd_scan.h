@@ -66,10 +66,18 @@ int ssd_abi_version(void);
  * none).  The string stays valid until the next call on that thread. */
 const char *ssd_last_error(void);
 
-/* Bytes of device workspace ssd_scan_fwd needs for these sizes: processed
- * dt and per-chunk cumsum [batch, nheads, nchunks, chunk_size] float each,
- * per-chunk segment counts [batch, nchunks, chunk_size] int32, and chunk
- * states [batch, nchunks, nheads, headdim, dstate] float.  0 on bad sizes. */
+/* Bytes of device workspace ssd_scan_fwd needs for these sizes: a control
+ * block of (64 + batch*nheads) int32 (work counter, error word, per-(b, h)
+ * hand-off flags of the fused kernel), processed dt and per-chunk cumsum
+ * [batch, nheads, nchunks, chunk_size] float each, per-chunk segment counts
+ * [batch, nchunks, chunk_size] int32, and chunk states
+ * [batch, nchunks, nheads, headdim, dstate] float (the fused kernel uses the
+ * start of this region for its state hand-off slots).  Each piece starts on
+ * a 256-byte boundary.  0 on bad sizes.
+ *
+ * For bf16 inputs with headdim 64, dstate 128 and chunk_size 128 or 256,
+ * ssd_scan_fwd runs stage 1 and then ssd_chunk_fused's kernel; otherwise the
+ * four stage kernels below. */
 size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
                                 int headdim, int dstate, int ngroups,
                                 int chunk_size, ssd_dtype_t dtype);
@@ -168,6 +176,24 @@ int ssd_chunk_scan(const void *x, const void *B, const void *C,
                    int64_t seqlen, int nheads, int headdim, int dstate,
                    int ngroups, int chunk_size, ssd_dtype_t dtype, void *out,
                    void *stream);
+
+/* Stages 2-4 fused into one tensor-core (tcgen05) kernel, for bf16 inputs
+ * with headdim 64, dstate 128 and chunk_size 128 or 256 (SSD_ERR_UNSUPPORTED
+ * otherwise).  Inputs are stage 1's dt_out / dA_cumsum / chunk_seg plus x, B,
+ * C, D, z, initial_states as in ssd_scan_fwd; writes out and (if not NULL)
+ * final_states.  workspace (>= ssd_scan_workspace_bytes) is required: the
+ * kernel hands each chunk's final state to the next chunk through it.  If a
+ * bounded internal wait gives up (which it should never do), the int32 at
+ * byte offset 4 of the workspace is nonzero after the kernel; the outputs
+ * are then not valid. */
+int ssd_chunk_fused(const void *x, const void *B, const void *C,
+                    const float *dt_out, const float *dA_cumsum,
+                    const int32_t *chunk_seg, const float *D, const void *z,
+                    const float *initial_states, int64_t batch, int64_t seqlen,
+                    int nheads, int headdim, int dstate, int ngroups,
+                    int chunk_size, ssd_dtype_t dtype, void *out,
+                    float *final_states, void *workspace,
+                    size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Variant of ssd_scan_fwd that allocates nothing.  (The pages have no

@@ -3,5 +3,5 @@
 The computation lives in ``libssd_gb300.so`` (CUDA kernels behind the C ABI
 of include/ssd_scan.h); this package only marshals torch tensors into it.
 """
-from .scan import (abi_version, ssd_chunk_scan, ssd_chunk_state,  # noqa: F401
+from .scan import (abi_version, ssd_chunk_fused, ssd_chunk_scan, ssd_chunk_state,  # noqa: F401
                    ssd_dt_cumsum, ssd_scan_fwd, ssd_state_passing, workspace_bytes)

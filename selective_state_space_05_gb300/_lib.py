@@ -34,6 +34,8 @@ SIGNATURES = {
     "ssd_chunk_state": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _i, _i,
                              _vp, _vp]),
     "ssd_state_passing": (_i, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _vp]),
+    "ssd_chunk_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i,
+                             _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "ssd_scan_fwd_noalloc": (_i, [_vp, _vp, _vp, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp,
                                   _vp, _i64, _i64, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
     "ssd_chunk_scan": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i,

@@ -71,6 +71,7 @@ int check_dtype(ssd_dtype_t t) {
 }
 
 struct Workspace {
+  int* ctrl;   // fused path: ticket counter, error word, per-(b,h) flags
   float* dt;
   float* cs;
   int32_t* seg;
@@ -85,6 +86,8 @@ Workspace carve(const ssd::Dims& d, void* base) {
   Workspace w;
   size_t off = 0;
   char* p = static_cast<char*>(base);
+  w.ctrl = reinterpret_cast<int*>(p + off);
+  off = round_up(off + ssd::fused_ctrl_ints(d) * sizeof(int), 256);
   w.dt = reinterpret_cast<float*>(p + off);
   off = round_up(off + nq * sizeof(float), 256);
   w.cs = reinterpret_cast<float*>(p + off);
@@ -216,6 +219,38 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_scan launch");
 }
 
+int ssd_chunk_fused(const void* x, const void* B, const void* C, const float* dt_out,
+                    const float* dA_cumsum, const int32_t* chunk_seg, const float* D,
+                    const void* z, const float* initial_states, int64_t batch, int64_t seqlen,
+                    int nheads, int headdim, int dstate, int ngroups, int chunk_size,
+                    ssd_dtype_t dtype, void* out, float* final_states, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d);
+  if (rc) return rc;
+  if (!ssd::fused_eligible(d, dtype == SSD_DTYPE_BF16))
+    return fail(SSD_ERR_UNSUPPORTED,
+                "ssd_chunk_fused needs bf16, headdim 64, dstate 128 and chunk_size 128 or 256");
+  if (!x || !B || !C || !dt_out || !dA_cumsum || !out || !workspace)
+    return fail(SSD_ERR_NULL, "x, B, C, dt_out, dA_cumsum, out and workspace are required");
+  const void* ptrs[] = {x, B, C, z, out, initial_states, final_states, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  const size_t need = carve(d, nullptr).bytes;
+  if (workspace_bytes < need)
+    return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  Workspace w = carve(d, workspace);
+  using bf = __nv_bfloat16;
+  cudaError_t e = ssd::launch_fused(
+      static_cast<const bf*>(x), static_cast<const bf*>(B), static_cast<const bf*>(C), dt_out,
+      dA_cumsum, chunk_seg, D, static_cast<const bf*>(z), initial_states, final_states,
+      static_cast<bf*>(out), w.states, w.ctrl, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_fused launch");
+}
+
 int ssd_scan_fwd(const void* x, const void* dt, const float* dt_bias, int dt_softplus,
                  float dt_limit_lo, float dt_limit_hi, const float* A, const void* B,
                  const void* C, const float* D, const void* z, const float* initial_states,
@@ -271,15 +306,22 @@ int ssd_scan_fwd(const void* x, const void* dt, const float* dt_bias, int dt_sof
     const bf* xb = static_cast<const bf*>(x);
     e = ssd::launch_dt_cumsum<bf>(static_cast<const bf*>(dt), dt_bias, dt_softplus, dt_limit_lo,
                                   dt_limit_hi, clamp, A, seq_idx, d, w.dt, w.cs, seg, st);
-    if (e == cudaSuccess)
-      e = ssd::launch_chunk_state<bf>(xb, static_cast<const bf*>(B), w.dt, w.cs, seg, d,
-                                      w.states, st);
-    if (e == cudaSuccess)
-      e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, d, st);
-    if (e == cudaSuccess)
-      e = ssd::launch_chunk_scan<bf>(xb, static_cast<const bf*>(B), static_cast<const bf*>(C),
-                                     w.dt, w.cs, seg, w.states, D, static_cast<const bf*>(z), d,
-                                     static_cast<bf*>(out), st);
+    if (ssd::fused_eligible(d, true)) {
+      if (e == cudaSuccess)
+        e = ssd::launch_fused(xb, static_cast<const bf*>(B), static_cast<const bf*>(C), w.dt, w.cs,
+                              seg, D, static_cast<const bf*>(z), initial_states, final_states,
+                              static_cast<bf*>(out), w.states, w.ctrl, d, st);
+    } else {
+      if (e == cudaSuccess)
+        e = ssd::launch_chunk_state<bf>(xb, static_cast<const bf*>(B), w.dt, w.cs, seg, d,
+                                        w.states, st);
+      if (e == cudaSuccess)
+        e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, d, st);
+      if (e == cudaSuccess)
+        e = ssd::launch_chunk_scan<bf>(xb, static_cast<const bf*>(B), static_cast<const bf*>(C),
+                                       w.dt, w.cs, seg, w.states, D, static_cast<const bf*>(z),
+                                       d, static_cast<bf*>(out), st);
+    }
   }
   if (owned) {
     cudaError_t e2 = cudaFreeAsync(base, st);

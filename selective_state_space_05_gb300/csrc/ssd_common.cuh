@@ -53,6 +53,17 @@ cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* d
                               const float* D, const T* z, const Dims& d, T* out,
                               cudaStream_t st);
 
+// Fused tensor-core chunk kernel (stages 2-4), bf16, headdim 64, dstate 128,
+// chunk 128 or 256.  ctrl: fused_ctrl_ints(d) ints of workspace, cleared by
+// the launcher; slots: 2 * batch * nheads * headdim * dstate floats.
+bool fused_eligible(const Dims& d, bool bf16);
+size_t fused_ctrl_ints(const Dims& d);
+cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
+                         const float* dt_out, const float* cs, const int32_t* seg,
+                         const float* D, const __nv_bfloat16* z, const float* init,
+                         float* final_states, __nv_bfloat16* out, float* slots, int* ctrl,
+                         const Dims& d, cudaStream_t st);
+
 // Sets the per-thread message returned by ssd_last_error(); returns code.
 int set_error(int code, const char* msg);
 

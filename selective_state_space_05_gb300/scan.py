@@ -203,3 +203,40 @@ def ssd_chunk_scan(x: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dt_out: to
         _ptr(prev_states), _ptr(D), _ptr(z), Bsz, L, H, P, N, G, int(chunk_size),
         _DT[x.dtype], _ptr(out), _stream(stream)))
     return out
+
+
+def ssd_chunk_fused(x: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dt_out: torch.Tensor,
+                    dA_cumsum: torch.Tensor, chunk_seg: Optional[torch.Tensor], *,
+                    chunk_size: int, workspace: torch.Tensor, D: Optional[torch.Tensor] = None,
+                    z: Optional[torch.Tensor] = None,
+                    initial_states: Optional[torch.Tensor] = None,
+                    return_final_states: bool = False, out: Optional[torch.Tensor] = None,
+                    final_states: Optional[torch.Tensor] = None, stream=None):
+    """Stages 2-4 in one tensor-core kernel (bf16, headdim 64, dstate 128,
+    chunk 128/256).  Returns out, or (out, final_states)."""
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    nc = (L + chunk_size - 1) // chunk_size
+    _need(x, "x", torch.bfloat16, device=dev)
+    _need(B, "B", torch.bfloat16, (Bsz, L, G, N), dev)
+    _need(C, "C", torch.bfloat16, (Bsz, L, G, N), dev)
+    _need(dt_out, "dt_out", torch.float32, (Bsz, H, nc, chunk_size), dev)
+    _need(dA_cumsum, "dA_cumsum", torch.float32, (Bsz, H, nc, chunk_size), dev)
+    _need(chunk_seg, "chunk_seg", torch.int32, (Bsz, nc, chunk_size), dev, optional=True)
+    _need(D, "D", torch.float32, (H,), dev, optional=True)
+    _need(z, "z", torch.bfloat16, (Bsz, L, H, P), dev, optional=True)
+    _need(initial_states, "initial_states", torch.float32, (Bsz, H, P, N), dev, optional=True)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty_like(x)
+    if return_final_states and final_states is None:
+        final_states = torch.empty(Bsz, H, P, N, dtype=torch.float32, device=dev)
+    _lib.check(_lib.load().ssd_chunk_fused(
+        _ptr(x), _ptr(B), _ptr(C), _ptr(dt_out), _ptr(dA_cumsum), _ptr(chunk_seg), _ptr(D),
+        _ptr(z), _ptr(initial_states), Bsz, L, H, P, N, G, int(chunk_size),
+        _lib.SSD_DTYPE_BF16, _ptr(out), _ptr(final_states), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    if return_final_states:
+        return out, final_states
+    return out

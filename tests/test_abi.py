@@ -31,7 +31,8 @@ def lib():
 def test_header_declares_the_expected_calls():
     names = declared_functions()
     for n in ("ssd_scan_fwd", "ssd_last_error", "ssd_abi_version", "ssd_scan_workspace_bytes",
-              "ssd_dt_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan"):
+              "ssd_dt_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
+              "ssd_chunk_fused"):
         assert n in names
 
 
@@ -49,9 +50,10 @@ def test_workspace_bytes(lib):
     # dt + cumsum [B,H,nc,Q] f32, segments [B,nc,Q] i32, states [B,nc,H,P,N] f32
     B, L, H, P, N, G, Q = 8, 4096, 80, 64, 128, 1, 256
     nc = L // Q
-    want = 2 * B * H * nc * Q * 4 + B * nc * Q * 4 + B * nc * H * P * N * 4
+    ctrl = (64 + B * H) * 4
+    want = ctrl + 2 * B * H * nc * Q * 4 + B * nc * Q * 4 + B * nc * H * P * N * 4
     got = lib.ssd_scan_workspace_bytes(B, L, H, P, N, G, Q, _lib.SSD_DTYPE_BF16)
-    assert want <= got <= want + 4 * 256
+    assert want <= got <= want + 5 * 256
     assert lib.ssd_scan_workspace_bytes(B, L, H, P, N, G, 100, 1) == 0      # bad chunk
     assert lib.ssd_scan_workspace_bytes(B, L, H, 48, N, G, Q, 1) == 0       # bad headdim
     assert lib.ssd_scan_workspace_bytes(B, L, 80, P, N, 3, Q, 1) == 0       # H % G != 0

@@ -1,0 +1,129 @@
+"""GPU parity of the fused tensor-core path (bf16, headdim 64, dstate 128,
+chunk 128 / 256): ssd_scan_fwd routes these shapes to stage 1 + the fused
+tcgen05 kernel.  Compared with the fp64 oracle (max|err|/max|ref| <= 2e-2)
+and with the four SIMT stage kernels; the kernel's error word must stay 0."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_inputs as si
+from ssd_testutil import TOL, assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_fused(d, chunk, check_error_word=True):
+    import selective_state_space_05_gb300 as ssd
+    g = to_dev(d)
+    Bsz, L, H, P = g["x"].shape
+    G, N = g["B"].shape[2], g["B"].shape[3]
+    ws = torch.empty(ssd.workspace_bytes(Bsz, L, H, P, N, G, chunk), dtype=torch.uint8,
+                     device="cuda")
+    out, fin = ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=chunk,
+                                dt_bias=g["dt_bias"], dt_softplus=d.get("dt_softplus", True),
+                                dt_limit=d.get("dt_limit", (0.0, math.inf)), D=g["D"], z=g["z"],
+                                initial_states=g["initial_states"], seq_idx=g["seq_idx"],
+                                return_final_states=True, workspace=ws)
+    torch.cuda.synchronize()
+    if check_error_word:
+        assert int(ws[4:8].view(torch.int32).item()) == 0, "fused kernel gave up a wait"
+    return out.double().cpu().numpy(), fin.double().cpu().numpy()
+
+
+def _small(seed, **kw):
+    base = dict(batch=2, nheads=4, ngroups=2, headdim=64, dstate=128, dtype="bf16")
+    base.update(kw)
+    return si.random_small(seed, **base)
+
+
+CASES = [
+    ("L1_q128", dict(seqlen=1, chunk_size=128)),
+    ("L100_q128", dict(seqlen=100, chunk_size=128)),
+    ("L128_q128", dict(seqlen=128, chunk_size=128)),
+    ("L129_q128", dict(seqlen=129, chunk_size=128)),
+    ("L255_q256", dict(seqlen=255, chunk_size=256)),
+    ("L256_q256", dict(seqlen=256, chunk_size=256)),
+    ("L257_q256", dict(seqlen=257, chunk_size=256)),
+    ("L700_q256_init", dict(seqlen=700, chunk_size=256, init_std=0.5)),
+    ("L1000_q128_init_G1", dict(seqlen=1000, chunk_size=128, ngroups=1, init_std=0.5)),
+    ("docs_on_sub_edges", dict(seqlen=640, chunk_size=256, init_std=0.3,
+                               seq_idx_lengths=[128, 128, 1, 127, 256])),
+    ("docs_inside_subs", dict(seqlen=600, chunk_size=256, init_std=0.3,
+                              seq_idx_lengths=[5, 200, 1, 1, 300, 93])),
+    ("no_z_no_D", dict(seqlen=300, chunk_size=256, has_z=False, has_D=False)),
+    ("slow_decay", dict(seqlen=1024, chunk_size=128, init_std=0.5,
+                        a_log_range=(math.log(1e-3), math.log(1e-1)))),
+    ("many_heads", dict(seqlen=512, chunk_size=256, nheads=16, ngroups=4, batch=3)),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fused_matches_oracle(case):
+    _, kw = case
+    d = _small(3000 + len(case[0]), **kw)
+    y, f = _run_fused(d, kw["chunk_size"])
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["bf16"], "out")
+    assert_close(f, rf, TOL["bf16"], "final")
+
+
+def test_fused_matches_simt_stages():
+    """Same inputs through the fused kernel and through the four SIMT stage
+    kernels (which the fp32 path uses)."""
+    import selective_state_space_05_gb300 as ssd
+    Q = 256
+    d = _small(41, seqlen=1500, chunk_size=Q, init_std=0.3, seq_idx_lengths=[700, 800])
+    y_f, f_f = _run_fused(d, Q)
+    g = to_dev(d)
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q, dt_bias=g["dt_bias"],
+                                        seq_idx=g["seq_idx"])
+    st = ssd.ssd_chunk_state(g["x"], g["B"], dt_out, cs, seg, chunk_size=Q)
+    fin = ssd.ssd_state_passing(st, cs, seg, seqlen=1500, chunk_size=Q,
+                                initial_states=g["initial_states"])
+    y_s = ssd.ssd_chunk_scan(g["x"], g["B"], g["C"], dt_out, cs, seg, st, chunk_size=Q,
+                             D=g["D"], z=g["z"])
+    torch.cuda.synchronize()
+    assert_close(y_f, y_s.double().cpu().numpy(), TOL["bf16"], "out fused vs SIMT")
+    assert_close(f_f, fin.double().cpu().numpy(), TOL["bf16"], "final fused vs SIMT")
+
+
+def test_fused_stage_entry_point():
+    """ssd_chunk_fused called on its own after ssd_dt_cumsum."""
+    import selective_state_space_05_gb300 as ssd
+    Q = 128
+    d = _small(42, seqlen=777, chunk_size=Q, init_std=0.2)
+    g = to_dev(d)
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q, dt_bias=g["dt_bias"])
+    ws = torch.empty(ssd.workspace_bytes(2, 777, 4, 64, 128, 2, Q), dtype=torch.uint8,
+                     device="cuda")
+    y, f = ssd.ssd_chunk_fused(g["x"], g["B"], g["C"], dt_out, cs, seg, chunk_size=Q,
+                               workspace=ws, D=g["D"], z=g["z"],
+                               initial_states=g["initial_states"], return_final_states=True)
+    torch.cuda.synchronize()
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y.double().cpu().numpy(), ry, TOL["bf16"], "out")
+    assert_close(f.double().cpu().numpy(), rf, TOL["bf16"], "final")
+
+
+def test_fused_long_lookback_chain():
+    """Many chunks per sequence and more work items than resident CTAs."""
+    d = _small(43, batch=4, seqlen=8192, nheads=32, ngroups=4, chunk_size=256, init_std=0.2)
+    y, f = _run_fused(d, 256)
+    heads = [0, 9, 31]
+    ry, rf = oracle.scan_sequential(d, heads=heads, batches=[0, 3])
+    assert_close(y[[0, 3]][:, :, heads], ry, TOL["bf16"], "out (sampled)")
+    assert_close(f[[0, 3]][:, heads], rf, TOL["bf16"], "final (sampled)")
+
+
+def test_fused_rejects_other_shapes():
+    import selective_state_space_05_gb300 as ssd
+    from selective_state_space_05_gb300._lib import SSDError
+    d = to_dev(si.random_small(44, headdim=32, dstate=128, dtype="bf16", seqlen=64,
+                               chunk_size=128))
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(d["dt"], d["A"], chunk_size=128)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(SSDError, match="headdim 64"):
+        ssd.ssd_chunk_fused(d["x"], d["B"], d["C"], dt_out, cs, seg, chunk_size=128, workspace=ws)
