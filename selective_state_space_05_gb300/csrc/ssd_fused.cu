@@ -32,10 +32,14 @@ namespace fused {
 constexpr int kSub = 128;   // tokens per sub-step (MMA M)
 constexpr int kP = 64;      // headdim
 constexpr int kN = 128;     // dstate
-constexpr int kThreads = 192;
-constexpr int kComputeWarp0 = 2;
+constexpr int kComputeWarp0 = 2;        // warps 0 (TMA) and 1 (MMA) come first
+constexpr int kSplit = 1;               // compute warps per TMEM lane quarter
+constexpr int kComputeThreads = 128 * kSplit;
+constexpr int kColsPerWarp = kP / kSplit;   // headdim columns each compute warp owns
+constexpr int kThreads = kComputeWarp0 * 32 + kComputeThreads;
 constexpr uint32_t kTmemCols = 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // any single wait: 2 s at most
+constexpr uint32_t kSleepHintNs = 20000;                 // suspend hint of one try_wait
 
 // error bits in the control block word ctrl[1]; once one is set every later
 // wait of the launch returns at once, so a broken launch still ends quickly
@@ -46,13 +50,13 @@ struct alignas(1024) Smem {
   unsigned char C[kSub * kN * 2];    // two 64-column halves, 128B swizzle
   unsigned char B[kSub * kN * 2];    // same
   unsigned char X[kSub * kP * 2];    // x; after Yi has read it: h as bf16
-  unsigned char XW[kSub * kP * 2];   // w o x
+  unsigned char XW[kSub * kP * 2];   // w o x; after the MMAs: z, then out
   float csv[kSub];      // the sub-step's cumsum values (bulk-copied)
   float dtv[kSub];      // its dt values
   int segv[kSub];       // its reset counts
   float mcol[kSub];     // l_j - log2(dt_j): column term of the diagonal blocks
   float bcol[kSub];     // exp2(l_e - l_j) dt_j, e = last column of j's 32-block
-  uint64_t full, cb, m_ready, yi_done, h_ready, y_done, stage_free;
+  uint64_t full, zfull, cb, m_ready, yi_done, h_ready, y_done, tmem_free;
   uint32_t tmem_base;
   int ticket[2];
 };
@@ -62,11 +66,9 @@ struct Params {
   const float* cs;       // [B, H, nc, Q]
   const int32_t* seg;    // [B, nc, Q] or null
   const float* D;        // [H] or null
-  const __nv_bfloat16* x;  // [B, L, H, P]
-  const __nv_bfloat16* z;  // [B, L, H, P] or null
+  bool has_z;
   const float* init;     // [B, H, P, N] or null
   float* final_states;   // [B, H, P, N] or null
-  __nv_bfloat16* out;    // [B, L, H, P]
   float* slots;          // [B*H, 2, N, P]
   int* flags;            // [B*H]
   int* ctrl;             // [0] ticket counter, [1] error word
@@ -97,8 +99,8 @@ __device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, int
   if (tc::mbar_try_wait(bar, parity)) return;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
-    if (tc::mbar_try_wait(bar, parity)) return;
-    if ((i & 255u) == 0) {
+    if (tc::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return;
+    if ((i & 15u) == 0) {
       if (aborted(ctrl)) return;
       if (global_ns() - t0 > kWaitNs) {
         atomicOr(ctrl + 1, kErrBarrier);
@@ -122,22 +124,12 @@ __device__ __forceinline__ float silu(float v) {
   return fmaf(hv, tanh_fast(hv), hv);
 }
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap map_x,
                      const __grid_constant__ CUtensorMap map_b,
-                     const __grid_constant__ CUtensorMap map_c, Params p) {
+                     const __grid_constant__ CUtensorMap map_c,
+                     const __grid_constant__ CUtensorMap map_z,
+                     const __grid_constant__ CUtensorMap map_out, Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (128-byte swizzle atoms), derived from the shared
   // array itself so that accesses stay shared-memory accesses
@@ -151,24 +143,27 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (tid == 0) {
     tc::mbar_init(&s.full, 1);
+    tc::mbar_init(&s.zfull, 1);
     tc::mbar_init(&s.cb, 1);
     tc::mbar_init(&s.m_ready, 1);
     tc::mbar_init(&s.yi_done, 1);
     tc::mbar_init(&s.h_ready, 1);
     tc::mbar_init(&s.y_done, 1);
-    tc::mbar_init(&s.stage_free, 1);
+    tc::mbar_init(&s.tmem_free, 1);
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&map_x);
     tc::tma_prefetch_desc(&map_b);
     tc::tma_prefetch_desc(&map_c);
+    tc::tma_prefetch_desc(&map_out);
+    if (p.has_z) tc::tma_prefetch_desc(&map_z);
     s.ticket[0] = atomicAdd(p.ctrl, 1);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
-  const uint32_t T_A = tmem + 0;     // CB fp32 [0,128) -> M bf16 [0,64), Ye [64,128)
-  const uint32_t T_Y = tmem + 128;   // Yi
+  const uint32_t T_A = tmem + 0;     // CB fp32 [0,128); then Yi [0,64) and Ye [64,128)
+  const uint32_t T_M = tmem + 128;   // M as bf16 pairs (A operand of Yi)
   const uint32_t T_H = tmem + 192;   // fp32 state, row n = dstate index, columns = headdim
 
   const int pairs = p.B * p.H;
@@ -189,13 +184,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t pq = ((int64_t)b * p.H + h) * p.nc + c;
 
     if (warp == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer: a sub-step's C, B, x tiles as soon as
+      // the previous sub-step's MMAs are done with them; its z tile into XW
+      // once its own MMAs are done with w o x
       if (lane == 0) {
         const uint32_t vec_bytes = (p.seg ? 3u : 2u) * kSub * 4u;
         for (int sub = 0; sub < nsub; ++sub, ++k) {
-          wait_or_flag(&s.stage_free, (k & 1) ^ 1, p.ctrl);
-          tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kSub * kP * 2 + vec_bytes);
           const int tok = (int)(t0 + sub * kSub);
+          wait_or_flag(&s.y_done, (k & 1) ^ 1, p.ctrl);
+          tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kSub * kP * 2 + vec_bytes);
           tc::tma_load_4d(s.C, &map_c, &s.full, 0, g, tok, b);
           tc::tma_load_4d(s.C + kSub * 128, &map_c, &s.full, 64, g, tok, b);
           tc::tma_load_4d(s.B, &map_b, &s.full, 0, g, tok, b);
@@ -206,6 +203,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (p.seg)
             tc::bulk_load(s.segv, p.seg + ((int64_t)b * p.nc + c) * p.Q + sub * kSub, kSub * 4,
                           &s.full);
+          if (p.has_z) {
+            wait_or_flag(&s.y_done, k & 1, p.ctrl);
+            tc::mbar_arrive_expect_tx(&s.zfull, kSub * kP * 2);
+            tc::tma_load_4d(s.XW, &map_z, &s.zfull, 0, h, tok, b);
+          }
         }
       } else {
         k += nsub;
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         constexpr uint32_t id_s = tc::idesc_bf16(kN, kP, true, true);
         for (int sub = 0; sub < nsub; ++sub, ++k) {
           const uint32_t ph = k & 1;
-          wait_or_flag(&s.stage_free, ph ^ 1, p.ctrl);
+          wait_or_flag(&s.tmem_free, ph ^ 1, p.ctrl);
           wait_or_flag(&s.full, ph, p.ctrl);
           tc::fence_after_sync();
           for (int kk = 0; kk < 8; ++kk) {   // CB = C B^T, K = dstate
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           tc::mma_commit(&s.cb);
           wait_or_flag(&s.m_ready, ph, p.ctrl);
           tc::fence_after_sync();
-          for (int kk = 0; kk < 8; ++kk)     // Yi = M x, K = tokens
-            tc::mma_ts(T_Y, T_A + kk * 8, tc::sdesc_sw128(sX + kk * 2048, 16384, 1024), id_y,
+          for (int kk = 0; kk < 8; ++kk)     // Yi = M x (M holds the D skip), K = tokens
+            tc::mma_ts(T_A, T_M + kk * 8, tc::sdesc_sw128(sX + kk * 2048, 16384, 1024), id_y,
                        kk > 0);
           tc::mma_commit(&s.yi_done);
           wait_or_flag(&s.h_ready, ph, p.ctrl);
@@ -251,137 +253,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         k += nsub;
       }
     } else {
-      // ---------------- compute warpgroup: one TMEM lane (row) per thread
-      const int q = warp & 3;
-      const int r = q * 32 + lane;                 // row: token (or dstate index) of the tile
-      const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-      const int ct = tid - kComputeWarp0 * 32;     // 0..127
+      // ---------------- compute: kSplit warps per TMEM lane quarter; warp
+      // (quarter qr, part hc) owns row r = 32 qr + lane and its share of the
+      // columns in every phase
+      const int cw = warp - kComputeWarp0;
+      const int qr = warp & 3;                      // TMEM lane quarter
+      const int hc = cw >> 2;                       // column part, 0..kSplit-1
+      const int r = qr * 32 + lane;                 // row: token (or dstate index)
+      const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
+      const int ct = tid - kComputeWarp0 * 32;
       const float Dh = p.D ? p.D[h] : 0.f;
-      const bool has_seg = p.seg != nullptr;   // s.segv is only filled with seq_idx
+      const bool has_seg = p.seg != nullptr;        // s.segv is only filled with seq_idx
       float l_prev = 0.f;
       int sg_prev = 0;
 
-      for (int sub = 0; sub < nsub; ++sub, ++k) {
-        const uint32_t ph = k & 1;
-        const int tok = sub * kSub + r;            // token within the chunk
-        const bool valid = tok < nvalid;
-        const int64_t grow = ((int64_t)b * p.L + t0 + tok) * p.H + h;   // (b, token, h)
-        if (valid && p.z) prefetch_l2(p.z + grow * kP);   // z row towards L2 early
-        wait_or_flag(&s.full, ph, p.ctrl);
-        // per-token scalars of the sub-step (positions past the end hold the
-        // chunk's last values)
-        const float l_r = s.csv[r] * kLog2e;
-        const float dt_r = s.dtv[r];
-        const int sg_r = has_seg ? s.segv[r] : 0;
-        const float l_last = s.csv[kSub - 1] * kLog2e;
-        const int sg_last = has_seg ? s.segv[kSub - 1] : 0;
-        s.mcol[r] = dt_r > 0.f ? l_r - __log2f(dt_r) : __int_as_float(0x7f800000);
-        s.bcol[r] = ex2(s.csv[r | 31] * kLog2e - l_r) * dt_r;
-        const float w_r = (valid && sg_r == sg_last) ? ex2(l_last - l_r) * dt_r : 0.f;
-        const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
-        const float carry = sg_last == sg_prev ? ex2(l_last - l_prev) : 0.f;
-        named_bar_sync(1, 128);
-
-        // ---- M = CB o decay (in place in TMEM) and w o x into shared memory
-        wait_or_flag(&s.cb, ph, p.ctrl);
-        tc::fence_after_sync();
-        // Blocks of 32 columns.  Below the diagonal block the decay factors as
-        // exp2(l_r - l_e) * [exp2(l_e - l_j) dt_j] with e the block's last
-        // column (both factors <= 1); the diagonal block takes one exp2 per
-        // element.  Masks are selects, never branches.
-#pragma unroll 1
-        for (int qc = 0; qc < 4; ++qc) {
-          uint32_t packed[16];
-          if (qc <= q) {
-            const bool diag = qc == q;
-            const float arow = diag ? 0.f : ex2(l_r - s.csv[qc * 32 + 31] * kLog2e);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int c0 = qc * 32 + hf * 16;
-              uint32_t v[16];
-              tc::tmem_ld16(T_A + lane_addr + c0, v);
-              float colv[16];
-              int sgv[16];
-              const float4* cp4 = reinterpret_cast<const float4*>((diag ? s.mcol : s.bcol) + c0);
-#pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                const float4 f = cp4[v4];
-                colv[4 * v4] = f.x;
-                colv[4 * v4 + 1] = f.y;
-                colv[4 * v4 + 2] = f.z;
-                colv[4 * v4 + 3] = f.w;
-              }
-              if (has_seg) {
-                const int4* sp4 = reinterpret_cast<const int4*>(s.segv + c0);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                  const int4 f = sp4[v4];
-                  sgv[4 * v4] = f.x;
-                  sgv[4 * v4 + 1] = f.y;
-                  sgv[4 * v4 + 2] = f.z;
-                  sgv[4 * v4 + 3] = f.w;
-                }
-              }
-              tc::tmem_ld_wait();
-              float m[16];
-              if (diag) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const float val = __uint_as_float(v[e]) * ex2(l_r - colv[e]);
-                  const bool ok = (c0 + e <= r) && (!has_seg || sgv[e] == sg_r);
-                  m[e] = ok ? val : 0.f;
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const float val = __uint_as_float(v[e]) * colv[e] * arow;
-                  m[e] = (!has_seg || sgv[e] == sg_r) ? val : 0.f;
-                }
-              }
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                packed[hf * 8 + e] = tc::pack_bf16x2(m[2 * e], m[2 * e + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) packed[e] = 0u;
-          }
-          tc::tmem_st16(T_A + lane_addr + qc * 16, packed);
-        }
-        uint4 xrow[8];   // this token's x (bf16), kept for the D skip
-        {
-          const unsigned char* xr = s.X + r * 128;
-          unsigned char* wr = s.XW + r * 128;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
-            const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
-            xrow[ch] = xv;
-            uint4 o;
-            o.x = tc::pack_bf16x2(bf_lo(xv.x) * w_r, bf_hi(xv.x) * w_r);
-            o.y = tc::pack_bf16x2(bf_lo(xv.y) * w_r, bf_hi(xv.y) * w_r);
-            o.z = tc::pack_bf16x2(bf_lo(xv.z) * w_r, bf_hi(xv.z) * w_r);
-            o.w = tc::pack_bf16x2(bf_lo(xv.w) * w_r, bf_hi(xv.w) * w_r);
-            *reinterpret_cast<uint4*>(wr + off) = o;
-          }
-        }
-        tc::tmem_st_wait();
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        named_bar_sync(1, 128);
-        if (ct == 0) tc::mbar_arrive(&s.m_ready);
-
-        // ---- this token's z, loaded now so the epilogue does not wait
-        uint4 zrow[8];
-        if (p.z && valid) {
-          const uint4* zp = reinterpret_cast<const uint4*>(p.z + grow * kP);
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) zrow[ch] = ldg_nc_v4(zp + ch);
-        }
-
-        // ---- the state entering the chunk, into TMEM (first sub-step only)
-        if (sub == 0) {
-          if (c > 0 && ct == 0) {
+      // the state entering the chunk, into TMEM (this warp's columns), while
+      // the first tiles are loading
+      {
+        if (c > 0) {
+          if (ct == 0) {
             const int* fl = p.flags + pair;
             const unsigned long long w0 = global_ns();
             int v;
@@ -398,48 +288,156 @@ __global__ void __launch_bounds__(kThreads, 2)
               __nanosleep(64);
             }
           }
-          if (c > 0) named_bar_sync(1, 128);
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t hv[32];
-            if (c == 0) {
-              if (p.init) {
-                const float* src = p.init + ((int64_t)b * p.H + h) * kP * kN + r;
+          named_bar_sync(1, kComputeThreads);
+        }
 #pragma unroll
-                for (int e = 0; e < 32; ++e) hv[e] = __float_as_uint(src[(half * 32 + e) * kN]);
+        for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
+          const int col = hc * kColsPerWarp + qd * 16;
+          uint32_t hv[16];
+          if (c == 0) {
+            if (p.init) {
+              const float* src = p.init + ((int64_t)b * p.H + h) * kP * kN + r;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) hv[e] = __float_as_uint(src[(col + e) * kN]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) hv[e] = 0u;
+            }
+          } else {
+            const float* src = p.slots + (((int64_t)pair * 2 + ((c - 1) & 1)) * kN + r) * kP + col;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(hv[4 * v4]), "=r"(hv[4 * v4 + 1]), "=r"(hv[4 * v4 + 2]),
+                             "=r"(hv[4 * v4 + 3])
+                           : "l"(src + 4 * v4)
+                           : "memory");
+            }
+          }
+          tc::tmem_st16(T_H + lane_addr + col, hv);
+        }
+        tc::tmem_st_wait();
+      }
+
+      for (int sub = 0; sub < nsub; ++sub, ++k) {
+        const uint32_t ph = k & 1;
+        const int tok = sub * kSub + r;            // token within the chunk
+        const bool valid = tok < nvalid;
+        wait_or_flag(&s.full, ph, p.ctrl);
+        // per-token scalars of the sub-step (positions past the end hold the
+        // chunk's last values)
+        const float l_r = s.csv[r] * kLog2e;
+        const float dt_r = s.dtv[r];
+        const int sg_r = has_seg ? s.segv[r] : 0;
+        const float l_last = s.csv[kSub - 1] * kLog2e;
+        const int sg_last = has_seg ? s.segv[kSub - 1] : 0;
+        if (hc == 0) {   // one writer per row
+          s.mcol[r] = dt_r > 0.f ? l_r - __log2f(dt_r) : __int_as_float(0x7f800000);
+          s.bcol[r] = ex2(s.csv[r | 31] * kLog2e - l_r) * dt_r;
+        }
+        const float w_r = (valid && sg_r == sg_last) ? ex2(l_last - l_r) * dt_r : 0.f;
+        const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
+        const float carry = sg_last == sg_prev ? ex2(l_last - l_prev) : 0.f;
+        named_bar_sync(1, kComputeThreads);
+
+        // ---- M = CB o decay into T_M, 32-column blocks hc, hc + kSplit, ...
+        // Below the diagonal block the decay factors as exp2(l_r - l_e) *
+        // [exp2(l_e - l_j) dt_j] with e the block's last column (both <= 1);
+        // the diagonal block takes one exp2 per element.  The D skip rides on
+        // the diagonal: M_rr += D, so that M x includes D x_r.  Masks are selects.
+        wait_or_flag(&s.cb, ph, p.ctrl);
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int bi = 0; bi < 4 / kSplit; ++bi) {
+          const int qc = hc + kSplit * bi;
+          const bool live = qc <= qr;
+          const bool diag = qc == qr;
+          const float arow = (live && !diag) ? ex2(l_r - s.csv[qc * 32 + 31] * kLog2e) : 0.f;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            const int c0 = qc * 32 + hf * 16;
+            uint32_t packed[8];
+            if (live) {
+              uint32_t v[16];
+              tc::tmem_ld16(T_A + lane_addr + c0, v);
+              float colv[16];
+              const float4* cp4 = reinterpret_cast<const float4*>((diag ? s.mcol : s.bcol) + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                const float4 f = cp4[v4];
+                colv[4 * v4] = f.x;
+                colv[4 * v4 + 1] = f.y;
+                colv[4 * v4 + 2] = f.z;
+                colv[4 * v4 + 3] = f.w;
+              }
+              tc::tmem_ld_wait();
+              float m[16];
+              if (diag) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const float val = __uint_as_float(v[e]) * ex2(l_r - colv[e]);
+                  m[e] = (c0 + e < r) ? val : (c0 + e == r ? val + Dh : 0.f);
+                }
               } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) hv[e] = 0u;
+                for (int e = 0; e < 16; ++e) m[e] = __uint_as_float(v[e]) * colv[e] * arow;
               }
-            } else {
-              const float* src =
-                  p.slots + (((int64_t)pair * 2 + ((c - 1) & 1)) * kN + r) * kP + half * 32;
+              if (has_seg) {   // a reset between j and r zeroes the entry
+                const int4* sp4 = reinterpret_cast<const int4*>(s.segv + c0);
 #pragma unroll
-              for (int v4 = 0; v4 < 8; ++v4) {
-                asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(hv[4 * v4]), "=r"(hv[4 * v4 + 1]), "=r"(hv[4 * v4 + 2]),
-                               "=r"(hv[4 * v4 + 3])
-                             : "l"(src + 4 * v4)
-                             : "memory");
+                for (int v4 = 0; v4 < 4; ++v4) {
+                  const int4 f = sp4[v4];
+                  m[4 * v4] = f.x == sg_r ? m[4 * v4] : 0.f;
+                  m[4 * v4 + 1] = f.y == sg_r ? m[4 * v4 + 1] : 0.f;
+                  m[4 * v4 + 2] = f.z == sg_r ? m[4 * v4 + 2] : 0.f;
+                  m[4 * v4 + 3] = f.w == sg_r ? m[4 * v4 + 3] : 0.f;
+                }
               }
+#pragma unroll
+              for (int e = 0; e < 8; ++e) packed[e] = tc::pack_bf16x2(m[2 * e], m[2 * e + 1]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) packed[e] = 0u;
             }
-            tc::tmem_st32(T_H + lane_addr + half * 32, hv);
+            tc::tmem_st8(T_M + lane_addr + (c0 >> 1), packed);
           }
-          tc::tmem_st_wait();
         }
+        // w o x for this warp's share of the row
+        {
+          const unsigned char* xr = s.X + r * 128;
+          unsigned char* wr = s.XW + r * 128;
+#pragma unroll
+          for (int cc = 0; cc < kColsPerWarp / 8; ++cc) {
+            const int ch = hc * (kColsPerWarp / 8) + cc;
+            const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
+            const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
+            uint4 o;
+            o.x = tc::pack_bf16x2(bf_lo(xv.x) * w_r, bf_hi(xv.x) * w_r);
+            o.y = tc::pack_bf16x2(bf_lo(xv.y) * w_r, bf_hi(xv.y) * w_r);
+            o.z = tc::pack_bf16x2(bf_lo(xv.z) * w_r, bf_hi(xv.z) * w_r);
+            o.w = tc::pack_bf16x2(bf_lo(xv.w) * w_r, bf_hi(xv.w) * w_r);
+            *reinterpret_cast<uint4*>(wr + off) = o;
+          }
+        }
+        tc::tmem_st_wait();
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        named_bar_sync(1, kComputeThreads);
+        if (ct == 0) tc::mbar_arrive(&s.m_ready);
 
         // ---- h (entering) -> bf16 operand of Ye in X; H <- carry H in TMEM
         wait_or_flag(&s.yi_done, ph, p.ctrl);   // Yi has read x
         tc::fence_after_sync();
-#pragma unroll 1
-        for (int qd = 0; qd < 4; ++qd) {
+#pragma unroll
+        for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
+          const int col = hc * kColsPerWarp + qd * 16;
           uint32_t hv[16];
-          tc::tmem_ld16(T_H + lane_addr + qd * 16, hv);
+          tc::tmem_ld16(T_H + lane_addr + col, hv);
           tc::tmem_ld_wait();
           unsigned char* hr = s.X + r * 128;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            const int ch = qd * 2 + cc;
+            const int ch = (col >> 3) + cc;
             uint4 o;
             o.x = tc::pack_bf16x2(__uint_as_float(hv[8 * cc + 0]), __uint_as_float(hv[8 * cc + 1]));
             o.y = tc::pack_bf16x2(__uint_as_float(hv[8 * cc + 2]), __uint_as_float(hv[8 * cc + 3]));
@@ -449,42 +447,43 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) hv[e] = __float_as_uint(carry * __uint_as_float(hv[e]));
-          tc::tmem_st16(T_H + lane_addr + qd * 16, hv);
+          tc::tmem_st16(T_H + lane_addr + col, hv);
         }
         tc::tmem_st_wait();
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kComputeThreads);
         if (ct == 0) tc::mbar_arrive(&s.h_ready);
 
         wait_or_flag(&s.y_done, ph, p.ctrl);
         tc::fence_after_sync();
 
-        // ---- hand the chunk's final state on
+        // ---- hand the chunk's final state on (this warp's columns)
         if (sub == nsub - 1) {
           const bool last_chunk = c == p.nc - 1;
           if (!last_chunk || p.final_states) {
-#pragma unroll 1
-            for (int qd = 0; qd < 4; ++qd) {
+#pragma unroll
+            for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
+              const int col = hc * kColsPerWarp + qd * 16;
               uint32_t hv[16];
-              tc::tmem_ld16(T_H + lane_addr + qd * 16, hv);
+              tc::tmem_ld16(T_H + lane_addr + col, hv);
               tc::tmem_ld_wait();
               if (last_chunk) {
                 float* dst = p.final_states + ((int64_t)b * p.H + h) * kP * kN + r;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dst[(qd * 16 + e) * kN] = __uint_as_float(hv[e]);
+                for (int e = 0; e < 16; ++e) dst[(col + e) * kN] = __uint_as_float(hv[e]);
               } else {
                 uint4* dst = reinterpret_cast<uint4*>(
-                    p.slots + (((int64_t)pair * 2 + (c & 1)) * kN + r) * kP + qd * 16);
+                    p.slots + (((int64_t)pair * 2 + (c & 1)) * kN + r) * kP + col);
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4)
                   dst[v4] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
               }
             }
             if (!last_chunk) {
-              __threadfence();
-              named_bar_sync(1, 128);
+              named_bar_sync(1, kComputeThreads);   // every thread's slot stores are done
               if (ct == 0) {
+                __threadfence();
                 const int nv = c + 1;
                 asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pair), "r"(nv)
                              : "memory");
@@ -493,53 +492,58 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
 
-        // ---- epilogue: out = (Yi + rho Ye + D x) * silu(z), 16 columns at a time
-        const bool gate = p.z != nullptr;
+        // ---- epilogue: out = (Yi + rho Ye) * silu(z), z read from (and out
+        // written back into) this row of XW, then one TMA store of the tile
+        if (p.has_z) wait_or_flag(&s.zfull, ph, p.ctrl);
+        unsigned char* zr = s.XW + r * 128;
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
+        for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
+          const int col = hc * kColsPerWarp + qd * 16;
           uint32_t yi[16], ye[16];
-          tc::tmem_ld16(T_Y + lane_addr + qd * 16, yi);
-          tc::tmem_ld16(T_A + 64 + lane_addr + qd * 16, ye);
+          tc::tmem_ld16(T_A + lane_addr + col, yi);
+          tc::tmem_ld16(T_A + 64 + lane_addr + col, ye);
           tc::tmem_ld_wait();
-          if (valid) {
-            uint4* op = reinterpret_cast<uint4*>(p.out + grow * kP) + qd * 2;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int ch = qd * 2 + cc;
-              const uint4 xv = xrow[ch];
-              const uint4 zv = gate ? zrow[ch] : make_uint4(0u, 0u, 0u, 0u);
-              const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-              const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
-              uint32_t o[4];
+          for (int cc = 0; cc < 2; ++cc) {
+            const int ch = (col >> 3) + cc;
+            uint4* slot = reinterpret_cast<uint4*>(zr + ((ch ^ (r & 7)) << 4));
+            const uint4 zv = p.has_z ? *slot : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+            uint32_t o[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                float y2[2];
+            for (int u = 0; u < 4; ++u) {
+              float y2[2];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  const int e = cc * 8 + u * 2 + hh;
-                  const float xval = hh ? bf_hi(xw[u]) : bf_lo(xw[u]);
-                  float y = fmaf(rho_r, __uint_as_float(ye[e]), __uint_as_float(yi[e]));
-                  y = fmaf(Dh, xval, y);
-                  if (gate) y *= silu(hh ? bf_hi(zw[u]) : bf_lo(zw[u]));
-                  y2[hh] = y;
-                }
-                o[u] = tc::pack_bf16x2(y2[0], y2[1]);
+              for (int hh = 0; hh < 2; ++hh) {
+                const int e = cc * 8 + u * 2 + hh;
+                float y = fmaf(rho_r, __uint_as_float(ye[e]), __uint_as_float(yi[e]));
+                if (p.has_z) y *= silu(hh ? bf_hi(zw[u]) : bf_lo(zw[u]));
+                y2[hh] = y;
               }
-              op[cc] = make_uint4(o[0], o[1], o[2], o[3]);
+              o[u] = tc::pack_bf16x2(y2[0], y2[1]);
             }
+            *slot = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
+        tc::fence_proxy_async_smem();
         tc::fence_before_sync();
-        named_bar_sync(1, 128);
-        if (ct == 0) tc::mbar_arrive(&s.stage_free);
+        named_bar_sync(1, kComputeThreads);
+        if (ct == 0) {
+          tc::mbar_arrive(&s.tmem_free);   // Yi / Ye read out
+          // rows past the sequence end are outside the tensor map and not written
+          tc::tma_store_4d(&map_out, s.XW, 0, h, (int)(t0 + sub * kSub), b);
+          tc::bulk_commit();
+          tc::bulk_wait_read();            // XW may be rewritten after this
+        }
         l_prev = l_last;
         sg_prev = sg_last;
       }
     }
   }
 
-  // drain: the compute warps have waited for every MMA before releasing the
-  // last stage; release TMEM
+  // drain: the compute warps have waited for every MMA; the storing thread
+  // waits for its last tile store; release TMEM
+  if (tid == kComputeWarp0 * 32) tc::bulk_wait_all();
   __syncwarp();
   tc::fence_before_sync();
   __syncthreads();
@@ -615,11 +619,14 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
                          const int32_t* seg, const float* D, const __nv_bfloat16* z,
                          const float* init, float* final_states, __nv_bfloat16* out,
                          float* slots, int* ctrl, const Dims& d, cudaStream_t st) {
-  CUtensorMap mx, mb, mc;
+  CUtensorMap mx, mb, mc, mz, mo;
   if (!make_map(&mx, x, fused::kP, d.nheads, d.seqlen, d.batch) ||
       !make_map(&mb, Bm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
-      !make_map(&mc, Cm, fused::kN, d.ngroups, d.seqlen, d.batch))
+      !make_map(&mc, Cm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
+      !make_map(&mo, out, fused::kP, d.nheads, d.seqlen, d.batch))
     return cudaErrorInvalidValue;
+  if (z && !make_map(&mz, z, fused::kP, d.nheads, d.seqlen, d.batch)) return cudaErrorInvalidValue;
+  if (!z) mz = mx;   // never used
   cudaError_t e = cudaMemsetAsync(ctrl, 0, fused_ctrl_ints(d) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   fused::Params p;
@@ -627,11 +634,9 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.cs = cs;
   p.seg = seg;
   p.D = D;
-  p.x = x;
-  p.z = z;
+  p.has_z = z != nullptr;
   p.init = init;
   p.final_states = final_states;
-  p.out = out;
   p.slots = slots;
   p.ctrl = ctrl;
   p.flags = ctrl + 64;
@@ -652,7 +657,7 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
     attr_set = true;
   }
   const long long grid = std::min<long long>(p.items, 2LL * sm_count());
-  fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, p);
+  fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz, mo, p);
   return cudaGetLastError();
 }
 
