@@ -69,7 +69,7 @@ struct Params {
   bool has_z;
   const float* init;     // [B, H, P, N] or null
   float* final_states;   // [B, H, P, N] or null
-  float* slots;          // [B*H, 2, N, P]
+  float* slots;          // [B*H, 2, P/4, N, 4]: hand-off states, column quads outermost
   int* flags;            // [B*H]
   int* ctrl;             // [0] ticket counter, [1] error word
   int64_t L;
@@ -267,57 +267,40 @@ __global__ void __launch_bounds__(kThreads, 2)
       float l_prev = 0.f;
       int sg_prev = 0;
 
-      // the state entering the chunk, into TMEM (this warp's columns), while
-      // the first tiles are loading
-      {
-        if (c > 0) {
-          if (ct == 0) {
-            const int* fl = p.flags + pair;
-            const unsigned long long w0 = global_ns();
-            int v;
-            for (uint32_t i = 0;; ++i) {
-              asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(fl) : "memory");
-              if (v >= c) break;
-              if ((i & 63u) == 63u) {
-                if (aborted(p.ctrl)) break;
-                if (global_ns() - w0 > kWaitNs) {
-                  atomicOr(p.ctrl + 1, kErrLookback);
-                  break;
-                }
-              }
-              __nanosleep(64);
-            }
-          }
-          named_bar_sync(1, kComputeThreads);
+      // the state entering the chunk, this row: issued now (each thread
+      // acquires the predecessor's flag itself), consumed at the first state
+      // phase, so the loads overlap the first sub-step's tiles and M build
+      uint32_t hin[kColsPerWarp];
+      bool hin_ready = true;
+      const float* hin_src = nullptr;
+      if (c == 0) {
+        if (p.init) {
+          const float* src = p.init + ((int64_t)b * p.H + h) * kP * kN + r;
+#pragma unroll
+          for (int e = 0; e < kColsPerWarp; ++e)
+            hin[e] = __float_as_uint(src[(hc * kColsPerWarp + e) * kN]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < kColsPerWarp; ++e) hin[e] = 0u;
         }
+      } else {
+        // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
+        hin_src = p.slots + ((((int64_t)pair * 2 + ((c - 1) & 1)) * (kP / 4) + hc * (kColsPerWarp / 4)) *
+                                 kN + r) * 4;
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + pair) : "memory");
+        hin_ready = v >= c;
+        if (hin_ready) {
 #pragma unroll
-        for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
-          const int col = hc * kColsPerWarp + qd * 16;
-          uint32_t hv[16];
-          if (c == 0) {
-            if (p.init) {
-              const float* src = p.init + ((int64_t)b * p.H + h) * kP * kN + r;
-#pragma unroll
-              for (int e = 0; e < 16; ++e) hv[e] = __float_as_uint(src[(col + e) * kN]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) hv[e] = 0u;
-            }
-          } else {
-            const float* src = p.slots + (((int64_t)pair * 2 + ((c - 1) & 1)) * kN + r) * kP + col;
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
-                           : "=r"(hv[4 * v4]), "=r"(hv[4 * v4 + 1]), "=r"(hv[4 * v4 + 2]),
-                             "=r"(hv[4 * v4 + 3])
-                           : "l"(src + 4 * v4)
-                           : "memory");
-            }
-          }
-          tc::tmem_st16(T_H + lane_addr + col, hv);
+          for (int v4 = 0; v4 < kColsPerWarp / 4; ++v4)
+            asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(hin[4 * v4]), "=r"(hin[4 * v4 + 1]), "=r"(hin[4 * v4 + 2]),
+                           "=r"(hin[4 * v4 + 3])
+                         : "l"(hin_src + (int64_t)v4 * kN * 4)
+                         : "memory");
         }
-        tc::tmem_st_wait();
       }
+      bool publish_pending = false;
 
       for (int sub = 0; sub < nsub; ++sub, ++k) {
         const uint32_t ph = k & 1;
@@ -425,6 +408,30 @@ __global__ void __launch_bounds__(kThreads, 2)
         named_bar_sync(1, kComputeThreads);
         if (ct == 0) tc::mbar_arrive(&s.m_ready);
 
+        if (sub == 0 && !hin_ready) {   // the predecessor had not handed on yet
+          const unsigned long long w0 = global_ns();
+          int v;
+          for (uint32_t i = 0;; ++i) {
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + pair) : "memory");
+            if (v >= c) break;
+            if ((i & 63u) == 63u) {
+              if (aborted(p.ctrl)) break;
+              if (global_ns() - w0 > kWaitNs) {
+                atomicOr(p.ctrl + 1, kErrLookback);
+                break;
+              }
+            }
+            __nanosleep(64);
+          }
+#pragma unroll
+          for (int v4 = 0; v4 < kColsPerWarp / 4; ++v4)
+            asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(hin[4 * v4]), "=r"(hin[4 * v4 + 1]), "=r"(hin[4 * v4 + 2]),
+                           "=r"(hin[4 * v4 + 3])
+                         : "l"(hin_src + (int64_t)v4 * kN * 4)
+                         : "memory");
+        }
+
         // ---- h (entering) -> bf16 operand of Ye in X; H <- carry H in TMEM
         wait_or_flag(&s.yi_done, ph, p.ctrl);   // Yi has read x
         tc::fence_after_sync();
@@ -432,8 +439,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
           const int col = hc * kColsPerWarp + qd * 16;
           uint32_t hv[16];
-          tc::tmem_ld16(T_H + lane_addr + col, hv);
-          tc::tmem_ld_wait();
+          if (sub == 0) {   // the entering state, from registers
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hv[e] = hin[qd * 16 + e];
+          } else {
+            tc::tmem_ld16(T_H + lane_addr + col, hv);
+            tc::tmem_ld_wait();
+          }
           unsigned char* hr = s.X + r * 128;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
@@ -473,22 +485,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) dst[(col + e) * kN] = __uint_as_float(hv[e]);
               } else {
-                uint4* dst = reinterpret_cast<uint4*>(
-                    p.slots + (((int64_t)pair * 2 + (c & 1)) * kN + r) * kP + col);
+                uint4* dst = reinterpret_cast<uint4*>(p.slots) +
+                             (((int64_t)pair * 2 + (c & 1)) * (kP / 4) + col / 4) * kN + r;
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4)
-                  dst[v4] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
+                  dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
               }
             }
-            if (!last_chunk) {
-              named_bar_sync(1, kComputeThreads);   // every thread's slot stores are done
-              if (ct == 0) {
-                __threadfence();
-                const int nv = c + 1;
-                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pair), "r"(nv)
-                             : "memory");
-              }
-            }
+            publish_pending = !last_chunk;   // flag raised after the epilogue
           }
         }
 
@@ -529,6 +533,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc::fence_before_sync();
         named_bar_sync(1, kComputeThreads);
         if (ct == 0) {
+          if (publish_pending) {   // every thread's slot stores came before the barrier
+            __threadfence();
+            const int nv = c + 1;
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pair), "r"(nv)
+                         : "memory");
+          }
           tc::mbar_arrive(&s.tmem_free);   // Yi / Ye read out
           // rows past the sequence end are outside the tensor map and not written
           tc::tma_store_4d(&map_out, s.XW, 0, h, (int)(t0 + sub * kSub), b);
