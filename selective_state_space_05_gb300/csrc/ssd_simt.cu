@@ -19,9 +19,10 @@ namespace ssd {
 
 // ---------------------------------------------------------------------------
 // Stage 1: dt preprocessing + per-chunk cumsum of dt*A (+ segment counts)
-// grid (nchunks, batch), 256 threads.  Heads are processed 32 at a time
-// through a [Q][32] shared tile so that the dt loads are coalesced along heads
-// and each warp then scans one head along the chunk.
+// grid (nchunks, batch, ceil(nheads/32)), 256 threads: each block takes 32
+// heads of one chunk through a [Q][32] shared tile, so that the dt loads are
+// coalesced along heads, and each warp then scans one head along the chunk.
+// The head-block-0 blocks also write the chunk's segment counts.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) dt_cumsum_kernel(
@@ -30,13 +31,13 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(
     Dims d, float* __restrict__ dt_out, float* __restrict__ cs_out, int32_t* __restrict__ seg) {
   __shared__ float tile[256][33];
   __shared__ int warp_tot[8];
-  const int c = blockIdx.x, b = blockIdx.y;
+  const int c = blockIdx.x, b = blockIdx.y, hb = blockIdx.z;
   const int Q = d.chunk, H = d.nheads;
   const int64_t t0 = (int64_t)c * Q;
   const int n = (int)min((int64_t)Q, d.seqlen - t0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  if (seq_idx != nullptr && seg != nullptr) {
+  if (seq_idx != nullptr && seg != nullptr && hb == 0) {
     // inclusive count of resets over the chunk; position t0 compares with t0-1
     int flag = 0;
     if (tid < n) {
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(
   }
 
   const int E = Q >= 32 ? Q / 32 : 1;  // consecutive positions per lane
-  for (int hg = 0; hg < H; hg += 32) {
+  for (int hg = hb * 32; hg < min(H, hb * 32 + 32); hg += 32) {
     const int hw = min(32, H - hg);
     for (int idx = tid; idx < Q * 32; idx += 256) {
       const int t = idx >> 5, j = idx & 31;
@@ -112,7 +113,7 @@ cudaError_t launch_dt_cumsum(const T* dt, const float* dt_bias, int softplus, fl
                              float hi, int do_clamp, const float* A, const int32_t* seq_idx,
                              const Dims& d, float* dt_out, float* cs, int32_t* seg,
                              cudaStream_t st) {
-  dim3 grid(d.nchunks, (unsigned)d.batch);
+  dim3 grid(d.nchunks, (unsigned)d.batch, (unsigned)((d.nheads + 31) / 32));
   dt_cumsum_kernel<T><<<grid, 256, 0, st>>>(dt, dt_bias, softplus, lo, hi, do_clamp, A,
                                             seq_idx, d, dt_out, cs, seg);
   return cudaGetLastError();
