@@ -244,10 +244,14 @@ int ssd_chunk_fused(const void* x, const void* B, const void* C, const float* dt
     return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   Workspace w = carve(d, workspace);
   using bf = __nv_bfloat16;
+  ssd::FusedVectors v = {};
+  v.dt = dt_out;
+  v.cs = dA_cumsum;
+  v.seg = chunk_seg;
   cudaError_t e = ssd::launch_fused(
-      static_cast<const bf*>(x), static_cast<const bf*>(B), static_cast<const bf*>(C), dt_out,
-      dA_cumsum, chunk_seg, D, static_cast<const bf*>(z), initial_states, final_states,
-      static_cast<bf*>(out), w.states, w.ctrl, d, static_cast<cudaStream_t>(stream));
+      static_cast<const bf*>(x), static_cast<const bf*>(B), static_cast<const bf*>(C), v, D,
+      static_cast<const bf*>(z), initial_states, final_states, static_cast<bf*>(out), w.states,
+      w.ctrl, d, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_fused launch");
 }
 
@@ -304,14 +308,22 @@ int ssd_scan_fwd(const void* x, const void* dt, const float* dt_bias, int dt_sof
   } else {
     using bf = __nv_bfloat16;
     const bf* xb = static_cast<const bf*>(x);
-    e = ssd::launch_dt_cumsum<bf>(static_cast<const bf*>(dt), dt_bias, dt_softplus, dt_limit_lo,
-                                  dt_limit_hi, clamp, A, seq_idx, d, w.dt, w.cs, seg, st);
-    if (ssd::fused_eligible(d, true)) {
-      if (e == cudaSuccess)
-        e = ssd::launch_fused(xb, static_cast<const bf*>(B), static_cast<const bf*>(C), w.dt, w.cs,
-                              seg, D, static_cast<const bf*>(z), initial_states, final_states,
-                              static_cast<bf*>(out), w.states, w.ctrl, d, st);
+    if (ssd::fused_eligible(d, true)) {   // all four stages in one kernel
+      ssd::FusedVectors v = {};
+      v.dt_raw = static_cast<const bf*>(dt);
+      v.dt_bias = dt_bias;
+      v.A = A;
+      v.seq_idx = seq_idx;
+      v.softplus = dt_softplus;
+      v.do_clamp = clamp;
+      v.lo = dt_limit_lo;
+      v.hi = dt_limit_hi;
+      e = ssd::launch_fused(xb, static_cast<const bf*>(B), static_cast<const bf*>(C), v, D,
+                            static_cast<const bf*>(z), initial_states, final_states,
+                            static_cast<bf*>(out), w.states, w.ctrl, d, st);
     } else {
+      e = ssd::launch_dt_cumsum<bf>(static_cast<const bf*>(dt), dt_bias, dt_softplus, dt_limit_lo,
+                                    dt_limit_hi, clamp, A, seq_idx, d, w.dt, w.cs, seg, st);
       if (e == cudaSuccess)
         e = ssd::launch_chunk_state<bf>(xb, static_cast<const bf*>(B), w.dt, w.cs, seg, d,
                                         w.states, st);

@@ -53,16 +53,28 @@ cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* d
                               const float* D, const T* z, const Dims& d, T* out,
                               cudaStream_t st);
 
-// Fused tensor-core chunk kernel (stages 2-4), bf16, headdim 64, dstate 128,
-// chunk 128 or 256.  ctrl: fused_ctrl_ints(d) ints of workspace, cleared by
-// the launcher; slots: 2 * batch * nheads * headdim * dstate floats.
+// Fused tensor-core kernel, bf16, headdim 64, dstate 128, chunk 128 or 256.
+// Stages 2-4 always; stage 1 too when the per-token vectors are given raw
+// (dt_raw set): then dt / cs / seg are not read.  ctrl: fused_ctrl_ints(d)
+// ints of workspace, cleared by the launcher; slots: 2 * batch * nheads *
+// headdim * dstate floats.
+struct FusedVectors {
+  const __nv_bfloat16* dt_raw;   // [B, L, H] raw dt, or null
+  const float* dt_bias;          // [H] or null
+  const float* A;                // [H] (with dt_raw)
+  const int32_t* seq_idx;        // [B, L] or null (with dt_raw)
+  int softplus, do_clamp;
+  float lo, hi;
+  const float* dt;               // stage-1 outputs (without dt_raw)
+  const float* cs;
+  const int32_t* seg;            // or null
+};
 bool fused_eligible(const Dims& d, bool bf16);
 size_t fused_ctrl_ints(const Dims& d);
 cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
-                         const float* dt_out, const float* cs, const int32_t* seg,
-                         const float* D, const __nv_bfloat16* z, const float* init,
-                         float* final_states, __nv_bfloat16* out, float* slots, int* ctrl,
-                         const Dims& d, cudaStream_t st);
+                         const FusedVectors& v, const float* D, const __nv_bfloat16* z,
+                         const float* init, float* final_states, __nv_bfloat16* out,
+                         float* slots, int* ctrl, const Dims& d, cudaStream_t st);
 
 // Sets the per-thread message returned by ssd_last_error(); returns code.
 int set_error(int code, const char* msg);

@@ -1,12 +1,19 @@
-// Fused tensor-core SSD chunk kernel for sm_103a (bf16 inputs, headdim 64,
-// dstate 128, chunk 128 or 256): chunk states, inter-chunk state passing and
-// chunk outputs in one persistent kernel.  Stage 1 (dt preprocessing and the
-// per-chunk cumsum of dt*A) runs before it as its own kernel.
+// Fused tensor-core SSD kernel for sm_103a (bf16 inputs, headdim 64, dstate
+// 128, chunk 128 or 256): dt preprocessing and the per-chunk cumsum of dt*A,
+// chunk states, inter-chunk state passing and chunk outputs in one persistent
+// kernel.
 //
 // Work item = (batch b, chunk c, head h), taken from an atomic ticket counter
 // in chunk-major order, so an item's predecessor (b, c-1, h) always holds an
-// earlier ticket.  A chunk is processed as 128-token sub-steps; per sub-step,
-// with rows/columns = the sub-step's tokens and cs the chunk's cumsum:
+// earlier ticket.  Warp roles:
+//   warp 0    takes the tickets and, one item ahead, computes the item's
+//             per-token vectors (dt = softplus(dt_raw + dt_bias) clamped, the
+//             cumsum of dt*A, the reset counts of seq_idx) into a two-slot
+//             ring; lane 0 issues the TMA tile loads
+//   warp 1    lane 0 issues the tcgen05 MMAs
+//   warps 2-5 build the decay matrix, move the state and run the epilogue
+// A chunk is processed as 128-token sub-steps; per sub-step, with rows /
+// columns = the sub-step's tokens and cs the chunk's cumsum:
 //   CB   = C B^T                       tcgen05, A = C (K-major), B = B (K-major)
 //   M    = CB o exp(cs_i - cs_j) dt_j  (j <= i, same document)   CUDA cores -> TMEM
 //   Yi   = M x                         tcgen05, A = M from TMEM, B = x (MN-major)
@@ -16,10 +23,10 @@
 //          w_j = exp(cs_last - cs_j) dt_j  (the sub-step's own chunk state)
 //   out  = (Yi + exp(cs_i - cs_prev) Ye + D x) * silu(z)
 // where h is the state entering the sub-step; the fp32 state stays in TMEM
-// (one row of dstate per TMEM lane, headdim columns) for the whole chunk.  The state entering a chunk is
-// handed from item (b, c-1, h) through an L2-resident fp32 slot and a flag
-// (decoupled look-back); every wait is bounded and gives up with an error
-// word instead of hanging.
+// (one row of dstate per TMEM lane, headdim columns) for the whole chunk.  The
+// state entering a chunk is handed from item (b, c-1, h) through an
+// L2-resident fp32 slot and a flag (decoupled look-back); every wait is
+// bounded and gives up with an error word instead of hanging.
 #include <cudaTypedefs.h>
 
 #include "../../include/ssd_scan.h"
@@ -32,10 +39,10 @@ namespace fused {
 constexpr int kSub = 128;   // tokens per sub-step (MMA M)
 constexpr int kP = 64;      // headdim
 constexpr int kN = 128;     // dstate
+constexpr int kQmax = 256;  // largest chunk
+constexpr int kRing = 2;    // items whose tickets / vectors are published
 constexpr int kComputeWarp0 = 2;        // warps 0 (TMA) and 1 (MMA) come first
-constexpr int kSplit = 1;               // compute warps per TMEM lane quarter
-constexpr int kComputeThreads = 128 * kSplit;
-constexpr int kColsPerWarp = kP / kSplit;   // headdim columns each compute warp owns
+constexpr int kComputeThreads = 128;    // one warp per TMEM lane quarter
 constexpr int kThreads = kComputeWarp0 * 32 + kComputeThreads;
 constexpr uint32_t kTmemCols = 256;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // any single wait: 2 s at most
@@ -51,20 +58,31 @@ struct alignas(1024) Smem {
   unsigned char B[kSub * kN * 2];    // same
   unsigned char X[kSub * kP * 2];    // x; after Yi has read it: h as bf16
   unsigned char XW[kSub * kP * 2];   // w o x; after the MMAs: z, then out
-  float csv[kSub];      // the sub-step's cumsum values (bulk-copied)
-  float dtv[kSub];      // its dt values
-  int segv[kSub];       // its reset counts
+  float lv[kRing][kQmax];   // l = log2(e) * cumsum of dt*A over the chunk
+  float dtv[kRing][kQmax];  // dt
+  int segv[kRing][kQmax];   // reset counts (with seq_idx)
   float mcol[kSub];     // l_j - log2(dt_j): column term of the diagonal blocks
   float bcol[kSub];     // exp2(l_e - l_j) dt_j, e = last column of j's 32-block
+  long long tk[kRing];  // published tickets (>= items: no more work)
+  uint64_t tk_full[kRing], tk_empty[kRing];
   uint64_t full, zfull, cb, m_ready, yi_done, h_ready, y_done, tmem_free;
   uint32_t tmem_base;
-  int ticket[2];
+  long long first_ticket;
 };
 
 struct Params {
+  // per-token vectors: computed here from the raw inputs (dt_raw != null) or
+  // read from the stage-1 outputs dt / cs / seg
+  const __nv_bfloat16* dt_raw;   // [B, L, H]
+  const float* dt_bias;          // [H] or null
+  const float* A;                // [H]
+  const int32_t* seq_idx;        // [B, L] or null
+  int softplus, do_clamp;
+  float lo, hi;
   const float* dt;       // [B, H, nc, Q]
   const float* cs;       // [B, H, nc, Q]
   const int32_t* seg;    // [B, nc, Q] or null
+  bool has_seg;          // reset counts exist (seq_idx or seg given)
   const float* D;        // [H] or null
   bool has_z;
   const float* init;     // [B, H, P, N] or null
@@ -73,9 +91,28 @@ struct Params {
   int* flags;            // [B*H]
   int* ctrl;             // [0] ticket counter, [1] error word
   int64_t L;
-  int B, H, G, Q, nc, nsub_max;
+  int B, H, G, Q, nc;
   long long items;
 };
+
+struct Item {
+  int b, c, h, g, pair, nvalid, nsub;
+  int64_t t0;
+};
+
+__device__ __forceinline__ Item decode(const Params& p, long long t) {
+  Item it;
+  const int pairs = p.B * p.H;
+  it.c = (int)(t / pairs);
+  it.pair = (int)(t % pairs);
+  it.b = it.pair / p.H;
+  it.h = it.pair % p.H;
+  it.g = it.h / (p.H / p.G);
+  it.t0 = (int64_t)it.c * p.Q;
+  it.nvalid = (int)min((int64_t)p.Q, p.L - it.t0);
+  it.nsub = (it.nvalid + kSub - 1) / kSub;
+  return it;
+}
 
 // Named barrier over a subset of warps; the non-aligned form tolerates
 // threads of a warp arriving separately.
@@ -110,8 +147,95 @@ __device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, int
   }
 }
 
+template <typename T>
+__device__ __forceinline__ T warp_incl_scan(T v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const T o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += o;
+  }
+  return v;
+}
+
+// The per-token vectors of one item, written by the 32 lanes of a warp: lane
+// i owns positions [i E, i E + E) of the chunk, E = Q / 32.  Positions past
+// the sequence end get dt = 0, so that l and the reset count keep their last
+// values there.
+__device__ __forceinline__ void item_vectors(const Params& p, const Item& it, float* lv, float* dtv,
+                                          int* segv, int lane) {
+  const int Q = p.Q, E = Q / 32;
+  if (p.dt_raw) {
+    const float a = p.A[it.h] * kLog2e;
+    const float bias = p.dt_bias ? p.dt_bias[it.h] : 0.f;
+    const __nv_bfloat16* src = p.dt_raw + ((int64_t)it.b * p.L + it.t0) * p.H + it.h;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int tok = lane * E + e;
+      v[e] = (e < E && tok < it.nvalid) ? __bfloat162float(src[(int64_t)tok * p.H]) : 0.f;
+    }
+    float run = 0.f, loc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float d = 0.f;
+      if (e < E && lane * E + e < it.nvalid) {
+        d = v[e] + bias;
+        if (p.softplus) d = d <= 20.f ? log1pf(__expf(d)) : d;
+        if (p.do_clamp) d = fminf(fmaxf(d, p.lo), p.hi);
+      }
+      v[e] = d;
+      run += d * a;
+      loc[e] = run;
+    }
+    const float excl = warp_incl_scan(run, lane) - run;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e < E) {
+        dtv[lane * E + e] = v[e];
+        lv[lane * E + e] = excl + loc[e];
+      }
+    }
+    if (p.seq_idx) {
+      const int32_t* sq = p.seq_idx + (int64_t)it.b * p.L;
+      int cnt = 0, lc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int tok = lane * E + e;
+        const int64_t gt = it.t0 + tok;
+        int f = 0;
+        if (e < E && tok < it.nvalid && gt >= 1) f = sq[gt] != sq[gt - 1];
+        cnt += f;
+        lc[e] = cnt;
+      }
+      const int cex = warp_incl_scan(cnt, lane) - cnt;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (e < E) segv[lane * E + e] = cex + lc[e];
+    }
+  } else {
+    const int64_t pq = ((int64_t)it.b * p.H + it.h) * p.nc + it.c;
+    for (int i = lane; i < Q; i += 32) {
+      lv[i] = p.cs[pq * Q + i] * kLog2e;
+      dtv[i] = p.dt[pq * Q + i];
+    }
+    if (p.seg)
+      for (int i = lane; i < Q; i += 32) segv[i] = p.seg[((int64_t)it.b * p.nc + it.c) * Q + i];
+  }
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Eight fp32 values (bit patterns) from position i as one 16-byte bf16 chunk.
+template <int n>
+__device__ __forceinline__ uint4 pack8(const uint32_t (&v)[n], int i) {
+  uint4 o;
+  o.x = tc::pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+  o.y = tc::pack_bf16x2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+  o.z = tc::pack_bf16x2(__uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+  o.w = tc::pack_bf16x2(__uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
+  return o;
+}
 
 __device__ __forceinline__ float tanh_fast(float v) {
   float r;
@@ -122,6 +246,17 @@ __device__ __forceinline__ float tanh_fast(float v) {
 __device__ __forceinline__ float silu(float v) {
   const float hv = 0.5f * v;
   return fmaf(hv, tanh_fast(hv), hv);
+}
+
+// Eight column quads of one row (dstate index) of a handed-on state; quads
+// are kN * 4 floats apart, so that a warp's 32 rows of one quad are contiguous.
+__device__ __forceinline__ void load_slot_quads(uint32_t (&hv)[32], const float* src) {
+#pragma unroll
+  for (int v4 = 0; v4 < 8; ++v4)
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(hv[4 * v4]), "=r"(hv[4 * v4 + 1]), "=r"(hv[4 * v4 + 2]), "=r"(hv[4 * v4 + 3])
+                 : "l"(src + (int64_t)v4 * kN * 4)
+                 : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -150,13 +285,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::mbar_init(&s.h_ready, 1);
     tc::mbar_init(&s.y_done, 1);
     tc::mbar_init(&s.tmem_free, 1);
+    for (int i = 0; i < kRing; ++i) {
+      tc::mbar_init(&s.tk_full[i], 32);      // the 32 lanes of warp 0
+      tc::mbar_init(&s.tk_empty[i], 1 + 4);  // MMA lane + the 4 compute warps
+    }
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&map_x);
     tc::tma_prefetch_desc(&map_b);
     tc::tma_prefetch_desc(&map_c);
     tc::tma_prefetch_desc(&map_out);
     if (p.has_z) tc::tma_prefetch_desc(&map_z);
-    s.ticket[0] = atomicAdd(p.ctrl, 1);
+    s.first_ticket = atomicAdd(p.ctrl, 1);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -166,232 +305,265 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t T_M = tmem + 128;   // M as bf16 pairs (A operand of Yi)
   const uint32_t T_H = tmem + 192;   // fp32 state, row n = dstate index, columns = headdim
 
-  const int pairs = p.B * p.H;
-  uint32_t k = 0;   // sub-steps done by this CTA (barrier phase counter)
-  for (int it = 0;; ++it) {
-    __syncwarp();      // lane 0 of warp 0 wrote this ticket before reaching here
-    const long long t = s.ticket[it & 1];
-    __syncthreads();   // everyone has read this item's ticket
-    if (t >= p.items) break;
-    if (tid == 0) s.ticket[(it + 1) & 1] = atomicAdd(p.ctrl, 1);   // next item, ahead
-    const int c = (int)(t / pairs);
-    const int pair = (int)(t % pairs);
-    const int b = pair / p.H, h = pair % p.H;
-    const int g = h / (p.H / p.G);
-    const int64_t t0 = (int64_t)c * p.Q;
-    const int nvalid = (int)min((int64_t)p.Q, p.L - t0);
-    const int nsub = (nvalid + kSub - 1) / kSub;
-    const int64_t pq = ((int64_t)b * p.H + h) * p.nc + c;
-
-    if (warp == 0) {
-      // ---------------- TMA producer: a sub-step's C, B, x tiles as soon as
-      // the previous sub-step's MMAs are done with them; its z tile into XW
-      // once its own MMAs are done with w o x
-      if (lane == 0) {
-        const uint32_t vec_bytes = (p.seg ? 3u : 2u) * kSub * 4u;
-        for (int sub = 0; sub < nsub; ++sub, ++k) {
-          const int tok = (int)(t0 + sub * kSub);
+  if (warp == 0) {
+    // ---------------- tickets, per-token vectors (one item ahead) and the
+    // TMA loads: a sub-step's C, B, x tiles as soon as the previous
+    // sub-step's MMAs are done with them, its z tile into XW once its own
+    // MMAs are done with w o x
+    long long t_cur = s.first_ticket;
+    if (t_cur < p.items) item_vectors(p, decode(p, t_cur), s.lv[0], s.dtv[0], s.segv[0], lane);
+    if (lane == 0) s.tk[0] = t_cur;
+    tc::mbar_arrive(&s.tk_full[0]);
+    long long t_pend = p.items;   // lane 0: the ticket after the published ones
+    if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ctrl, 1);
+    uint32_t k = 0;
+    for (int it = 0; t_cur < p.items && !aborted(p.ctrl); ++it) {
+      const Item cur = decode(p, t_cur);
+      long long t_nxt = p.items;
+      for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
+        const int tok = (int)(cur.t0 + sub * kSub);
+        if (lane == 0) {
           wait_or_flag(&s.y_done, (k & 1) ^ 1, p.ctrl);
-          tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kSub * kP * 2 + vec_bytes);
-          tc::tma_load_4d(s.C, &map_c, &s.full, 0, g, tok, b);
-          tc::tma_load_4d(s.C + kSub * 128, &map_c, &s.full, 64, g, tok, b);
-          tc::tma_load_4d(s.B, &map_b, &s.full, 0, g, tok, b);
-          tc::tma_load_4d(s.B + kSub * 128, &map_b, &s.full, 64, g, tok, b);
-          tc::tma_load_4d(s.X, &map_x, &s.full, 0, h, tok, b);
-          tc::bulk_load(s.csv, p.cs + pq * p.Q + sub * kSub, kSub * 4, &s.full);
-          tc::bulk_load(s.dtv, p.dt + pq * p.Q + sub * kSub, kSub * 4, &s.full);
-          if (p.seg)
-            tc::bulk_load(s.segv, p.seg + ((int64_t)b * p.nc + c) * p.Q + sub * kSub, kSub * 4,
-                          &s.full);
-          if (p.has_z) {
-            wait_or_flag(&s.y_done, k & 1, p.ctrl);
-            tc::mbar_arrive_expect_tx(&s.zfull, kSub * kP * 2);
-            tc::tma_load_4d(s.XW, &map_z, &s.zfull, 0, h, tok, b);
-          }
+          tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kSub * kP * 2);
+          tc::tma_load_4d(s.C, &map_c, &s.full, 0, cur.g, tok, cur.b);
+          tc::tma_load_4d(s.C + kSub * 128, &map_c, &s.full, 64, cur.g, tok, cur.b);
+          tc::tma_load_4d(s.B, &map_b, &s.full, 0, cur.g, tok, cur.b);
+          tc::tma_load_4d(s.B + kSub * 128, &map_b, &s.full, 64, cur.g, tok, cur.b);
+          tc::tma_load_4d(s.X, &map_x, &s.full, 0, cur.h, tok, cur.b);
         }
-      } else {
-        k += nsub;
+        if (sub == 0) {   // publish the next item into the other ring slot
+          t_nxt = __shfl_sync(0xffffffffu, t_pend, 0);
+          const int j = it + 1, slot = j % kRing;
+          wait_or_flag(&s.tk_empty[slot], ((j / kRing) & 1) ^ 1, p.ctrl);
+          if (t_nxt < p.items)
+            item_vectors(p, decode(p, t_nxt), s.lv[slot], s.dtv[slot], s.segv[slot], lane);
+          if (lane == 0) {
+            s.tk[slot] = t_nxt;
+            if (t_nxt < p.items) t_pend = atomicAdd(p.ctrl, 1);
+          }
+          tc::mbar_arrive(&s.tk_full[slot]);
+        }
+        if (lane == 0 && p.has_z) {
+          wait_or_flag(&s.y_done, k & 1, p.ctrl);
+          tc::mbar_arrive_expect_tx(&s.zfull, kSub * kP * 2);
+          tc::tma_load_4d(s.XW, &map_z, &s.zfull, 0, cur.h, tok, cur.b);
+        }
       }
-    } else if (warp == 1) {
-      // ---------------- MMA issuer
-      if (lane == 0) {
-        const uint32_t sC = tc::smem_u32(s.C), sB = tc::smem_u32(s.B);
-        const uint32_t sX = tc::smem_u32(s.X), sXW = tc::smem_u32(s.XW);
-        constexpr uint32_t id_cb = tc::idesc_bf16(kSub, kSub, false, false);
-        constexpr uint32_t id_y = tc::idesc_bf16(kSub, kP, false, true);
-        constexpr uint32_t id_s = tc::idesc_bf16(kN, kP, true, true);
+      t_cur = t_nxt;
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint64_t dC = tc::sdesc_sw128(tc::smem_u32(s.C), 16, 1024);
+      const uint64_t dB = tc::sdesc_sw128(tc::smem_u32(s.B), 16, 1024);
+      const uint64_t dBmn = tc::sdesc_sw128(tc::smem_u32(s.B), kSub * 128, 1024);
+      const uint64_t dX = tc::sdesc_sw128(tc::smem_u32(s.X), 16384, 1024);
+      const uint64_t dXW = tc::sdesc_sw128(tc::smem_u32(s.XW), 16384, 1024);
+      constexpr uint32_t id_cb = tc::idesc_bf16(kSub, kSub, false, false);
+      constexpr uint32_t id_y = tc::idesc_bf16(kSub, kP, false, true);
+      constexpr uint32_t id_s = tc::idesc_bf16(kN, kP, true, true);
+      uint32_t k = 0;
+      for (int it = 0;; ++it) {
+        const int slot = it % kRing;
+        wait_or_flag(&s.tk_full[slot], (it / kRing) & 1, p.ctrl);
+        const long long t = s.tk[slot];
+        tc::mbar_arrive(&s.tk_empty[slot]);
+        if (t >= p.items || aborted(p.ctrl)) break;
+        const int nsub = decode(p, t).nsub;
         for (int sub = 0; sub < nsub; ++sub, ++k) {
           const uint32_t ph = k & 1;
           wait_or_flag(&s.tmem_free, ph ^ 1, p.ctrl);
           wait_or_flag(&s.full, ph, p.ctrl);
           tc::fence_after_sync();
+          // descriptor start addresses advance in 16-byte units: K-major
+          // k-steps are 32 bytes inside a 64-column half (16 KB apart),
+          // MN-major k-steps are 8 rows of 128 bytes
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk) {   // CB = C B^T, K = dstate
-            const uint32_t ko = (kk >> 2) * (kSub * 128) + (kk & 3) * 32;
-            tc::mma_ss(T_A, tc::sdesc_sw128(sC + ko, 16, 1024), tc::sdesc_sw128(sB + ko, 16, 1024),
-                       id_cb, kk > 0);
+            const uint32_t ko = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
+            tc::mma_ss(T_A, dC + ko, dB + ko, id_cb, kk > 0);
           }
           tc::mma_commit(&s.cb);
           wait_or_flag(&s.m_ready, ph, p.ctrl);
           tc::fence_after_sync();
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)     // Yi = M x (M holds the D skip), K = tokens
-            tc::mma_ts(T_A, T_M + kk * 8, tc::sdesc_sw128(sX + kk * 2048, 16384, 1024), id_y,
-                       kk > 0);
+            tc::mma_ts(T_A, T_M + kk * 8, dX + kk * 128, id_y, kk > 0);
           tc::mma_commit(&s.yi_done);
           wait_or_flag(&s.h_ready, ph, p.ctrl);
           tc::fence_after_sync();
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk) {   // Ye = C h, K = dstate (h as bf16 in X)
-            const uint32_t ko = (kk >> 2) * (kSub * 128) + (kk & 3) * 32;
-            tc::mma_ss(T_A + 64, tc::sdesc_sw128(sC + ko, 16, 1024),
-                       tc::sdesc_sw128(sX + kk * 2048, 16384, 1024), id_y, kk > 0);
+            const uint32_t ko = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
+            tc::mma_ss(T_A + 64, dC + ko, dX + kk * 128, id_y, kk > 0);
           }
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)     // H += B^T (w o x), K = tokens
-            tc::mma_ss(T_H, tc::sdesc_sw128(sB + kk * 2048, kSub * 128, 1024),
-                       tc::sdesc_sw128(sXW + kk * 2048, 16384, 1024), id_s, 1);
+            tc::mma_ss(T_H, dBmn + kk * 128, dXW + kk * 128, id_s, 1);
           tc::mma_commit(&s.y_done);
         }
-      } else {
-        k += nsub;
       }
-    } else {
-      // ---------------- compute: kSplit warps per TMEM lane quarter; warp
-      // (quarter qr, part hc) owns row r = 32 qr + lane and its share of the
-      // columns in every phase
-      const int cw = warp - kComputeWarp0;
-      const int qr = warp & 3;                      // TMEM lane quarter
-      const int hc = cw >> 2;                       // column part, 0..kSplit-1
-      const int r = qr * 32 + lane;                 // row: token (or dstate index)
-      const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
-      const int ct = tid - kComputeWarp0 * 32;
-      const float Dh = p.D ? p.D[h] : 0.f;
-      const bool has_seg = p.seg != nullptr;        // s.segv is only filled with seq_idx
+    }
+  } else {
+    // ---------------- compute: warp (quarter qr) owns row r = 32 qr + lane
+    // of every TMEM tile and of the sub-step's smem tiles
+    const int qr = warp & 3;                      // TMEM lane quarter
+    const int r = qr * 32 + lane;                 // row: token (or dstate index)
+    const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
+    const int ct = tid - kComputeWarp0 * 32;
+    {   // the blocks of M above the diagonal stay zero
+      uint32_t zero[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) zero[e] = 0u;
+      tc::tmem_st32(T_M + lane_addr, zero);
+      tc::tmem_st32(T_M + lane_addr + 32, zero);
+      tc::tmem_st_wait();
+    }
+    uint32_t k = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it % kRing;
+      wait_or_flag(&s.tk_full[slot], (it / kRing) & 1, p.ctrl);
+      const long long t = s.tk[slot];
+      if (t >= p.items || aborted(p.ctrl)) break;
+      const Item cur = decode(p, t);
+      const int c = cur.c, pair = cur.pair;
+      const float Dh = p.D ? p.D[cur.h] : 0.f;
       float l_prev = 0.f;
       int sg_prev = 0;
 
-      // the state entering the chunk, this row: issued now (each thread
-      // acquires the predecessor's flag itself), consumed at the first state
-      // phase, so the loads overlap the first sub-step's tiles and M build
-      uint32_t hin[kColsPerWarp];
+      // the state entering the chunk, this row: loads issued now (each
+      // thread acquires the predecessor's flag itself) and written to T_H
+      // once the first sub-step's tiles have landed, so that they overlap
+      // that wait
+      uint32_t hin0[32], hin1[32];   // headdim columns 0-31 and 32-63
       bool hin_ready = true;
       const float* hin_src = nullptr;
       if (c == 0) {
         if (p.init) {
-          const float* src = p.init + ((int64_t)b * p.H + h) * kP * kN + r;
+          const float* src = p.init + ((int64_t)cur.b * p.H + cur.h) * kP * kN + r;
 #pragma unroll
-          for (int e = 0; e < kColsPerWarp; ++e)
-            hin[e] = __float_as_uint(src[(hc * kColsPerWarp + e) * kN]);
+          for (int e = 0; e < 32; ++e) {
+            hin0[e] = __float_as_uint(src[e * kN]);
+            hin1[e] = __float_as_uint(src[(32 + e) * kN]);
+          }
         } else {
 #pragma unroll
-          for (int e = 0; e < kColsPerWarp; ++e) hin[e] = 0u;
+          for (int e = 0; e < 32; ++e) hin0[e] = hin1[e] = 0u;
         }
       } else {
         // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
-        hin_src = p.slots + ((((int64_t)pair * 2 + ((c - 1) & 1)) * (kP / 4) + hc * (kColsPerWarp / 4)) *
-                                 kN + r) * 4;
+        hin_src = p.slots + (((int64_t)pair * 2 + ((c - 1) & 1)) * (kP / 4) * kN + r) * 4;
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + pair) : "memory");
         hin_ready = v >= c;
         if (hin_ready) {
-#pragma unroll
-          for (int v4 = 0; v4 < kColsPerWarp / 4; ++v4)
-            asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(hin[4 * v4]), "=r"(hin[4 * v4 + 1]), "=r"(hin[4 * v4 + 2]),
-                           "=r"(hin[4 * v4 + 3])
-                         : "l"(hin_src + (int64_t)v4 * kN * 4)
-                         : "memory");
+          load_slot_quads(hin0, hin_src);
+          load_slot_quads(hin1, hin_src + 8 * kN * 4);
         }
       }
       bool publish_pending = false;
+      wait_or_flag(&s.full, k & 1, p.ctrl);   // the first sub-step's tiles
+      if (!hin_ready) {   // the predecessor had not handed on yet
+        const unsigned long long w0 = global_ns();
+        int v;
+        for (uint32_t i = 0;; ++i) {
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + pair) : "memory");
+          if (v >= c) break;
+          if ((i & 63u) == 63u) {
+            if (aborted(p.ctrl)) break;
+            if (global_ns() - w0 > kWaitNs) {
+              atomicOr(p.ctrl + 1, kErrLookback);
+              break;
+            }
+          }
+          __nanosleep(64);
+        }
+        load_slot_quads(hin0, hin_src);
+        load_slot_quads(hin1, hin_src + 8 * kN * 4);
+      }
+      tc::tmem_st32(T_H + lane_addr, hin0);
+      tc::tmem_st32(T_H + lane_addr + 32, hin1);
 
-      for (int sub = 0; sub < nsub; ++sub, ++k) {
+      for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
         const uint32_t ph = k & 1;
-        const int tok = sub * kSub + r;            // token within the chunk
-        const bool valid = tok < nvalid;
-        wait_or_flag(&s.full, ph, p.ctrl);
+        const bool valid = sub * kSub + r < cur.nvalid;   // this row's token exists
+        if (sub > 0) wait_or_flag(&s.full, ph, p.ctrl);
         // per-token scalars of the sub-step (positions past the end hold the
         // chunk's last values)
-        const float l_r = s.csv[r] * kLog2e;
-        const float dt_r = s.dtv[r];
-        const int sg_r = has_seg ? s.segv[r] : 0;
-        const float l_last = s.csv[kSub - 1] * kLog2e;
-        const int sg_last = has_seg ? s.segv[kSub - 1] : 0;
-        if (hc == 0) {   // one writer per row
-          s.mcol[r] = dt_r > 0.f ? l_r - __log2f(dt_r) : __int_as_float(0x7f800000);
-          s.bcol[r] = ex2(s.csv[r | 31] * kLog2e - l_r) * dt_r;
-        }
+        const float* lv = s.lv[slot] + sub * kSub;
+        const int* sgv = s.segv[slot] + sub * kSub;
+        const float l_r = lv[r];
+        const float dt_r = s.dtv[slot][sub * kSub + r];
+        const int sg_r = p.has_seg ? sgv[r] : 0;
+        const float l_last = lv[kSub - 1];
+        const int sg_last = p.has_seg ? sgv[kSub - 1] : 0;
+        s.mcol[r] = dt_r > 0.f ? l_r - __log2f(dt_r) : __int_as_float(0x7f800000);
+        s.bcol[r] = ex2(lv[r | 31] - l_r) * dt_r;
         const float w_r = (valid && sg_r == sg_last) ? ex2(l_last - l_r) * dt_r : 0.f;
         const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
         const float carry = sg_last == sg_prev ? ex2(l_last - l_prev) : 0.f;
+        if (ct == 0) tc::bulk_wait_read();   // the last out tile has left XW
         named_bar_sync(1, kComputeThreads);
 
-        // ---- M = CB o decay into T_M, 32-column blocks hc, hc + kSplit, ...
-        // Below the diagonal block the decay factors as exp2(l_r - l_e) *
+        // ---- M = CB o decay into T_M, the live 32-column blocks 0..qr of
+        // this row (the blocks above the diagonal were zeroed once).  Below
+        // the diagonal block the decay factors as exp2(l_r - l_e) *
         // [exp2(l_e - l_j) dt_j] with e the block's last column (both <= 1);
         // the diagonal block takes one exp2 per element.  The D skip rides on
         // the diagonal: M_rr += D, so that M x includes D x_r.  Masks are selects.
         wait_or_flag(&s.cb, ph, p.ctrl);
         tc::fence_after_sync();
 #pragma unroll 1
-        for (int bi = 0; bi < 4 / kSplit; ++bi) {
-          const int qc = hc + kSplit * bi;
-          const bool live = qc <= qr;
+        for (int qc = 0; qc <= qr; ++qc) {
           const bool diag = qc == qr;
-          const float arow = (live && !diag) ? ex2(l_r - s.csv[qc * 32 + 31] * kLog2e) : 0.f;
-#pragma unroll 1
-          for (int hf = 0; hf < 2; ++hf) {
-            const int c0 = qc * 32 + hf * 16;
-            uint32_t packed[8];
-            if (live) {
-              uint32_t v[16];
-              tc::tmem_ld16(T_A + lane_addr + c0, v);
-              float colv[16];
-              const float4* cp4 = reinterpret_cast<const float4*>((diag ? s.mcol : s.bcol) + c0);
+          const int c0 = qc * 32;
+          uint32_t v[32];
+          tc::tmem_ld32(T_A + lane_addr + c0, v);
+          const float arow = diag ? 0.f : ex2(l_r - lv[c0 + 31]);
+          float colv[32];
+          const float4* cp4 = reinterpret_cast<const float4*>((diag ? s.mcol : s.bcol) + c0);
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                const float4 f = cp4[v4];
-                colv[4 * v4] = f.x;
-                colv[4 * v4 + 1] = f.y;
-                colv[4 * v4 + 2] = f.z;
-                colv[4 * v4 + 3] = f.w;
-              }
-              tc::tmem_ld_wait();
-              float m[16];
-              if (diag) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const float val = __uint_as_float(v[e]) * ex2(l_r - colv[e]);
-                  m[e] = (c0 + e < r) ? val : (c0 + e == r ? val + Dh : 0.f);
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) m[e] = __uint_as_float(v[e]) * colv[e] * arow;
-              }
-              if (has_seg) {   // a reset between j and r zeroes the entry
-                const int4* sp4 = reinterpret_cast<const int4*>(s.segv + c0);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                  const int4 f = sp4[v4];
-                  m[4 * v4] = f.x == sg_r ? m[4 * v4] : 0.f;
-                  m[4 * v4 + 1] = f.y == sg_r ? m[4 * v4 + 1] : 0.f;
-                  m[4 * v4 + 2] = f.z == sg_r ? m[4 * v4 + 2] : 0.f;
-                  m[4 * v4 + 3] = f.w == sg_r ? m[4 * v4 + 3] : 0.f;
-                }
-              }
-#pragma unroll
-              for (int e = 0; e < 8; ++e) packed[e] = tc::pack_bf16x2(m[2 * e], m[2 * e + 1]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) packed[e] = 0u;
-            }
-            tc::tmem_st8(T_M + lane_addr + (c0 >> 1), packed);
+          for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 f = cp4[v4];
+            colv[4 * v4] = f.x;
+            colv[4 * v4 + 1] = f.y;
+            colv[4 * v4 + 2] = f.z;
+            colv[4 * v4 + 3] = f.w;
           }
+          tc::tmem_ld_wait_regs(v);
+          float m[32];
+          if (diag) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float val = __uint_as_float(v[e]) * ex2(l_r - colv[e]);
+              m[e] = (c0 + e < r) ? val : (c0 + e == r ? val + Dh : 0.f);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) m[e] = __uint_as_float(v[e]) * (colv[e] * arow);
+          }
+          if (p.has_seg) {   // a reset between j and r zeroes the entry
+            const int4* sp4 = reinterpret_cast<const int4*>(sgv + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              const int4 f = sp4[v4];
+              m[4 * v4] = f.x == sg_r ? m[4 * v4] : 0.f;
+              m[4 * v4 + 1] = f.y == sg_r ? m[4 * v4 + 1] : 0.f;
+              m[4 * v4 + 2] = f.z == sg_r ? m[4 * v4 + 2] : 0.f;
+              m[4 * v4 + 3] = f.w == sg_r ? m[4 * v4 + 3] : 0.f;
+            }
+          }
+          uint32_t packed[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) packed[e] = tc::pack_bf16x2(m[2 * e], m[2 * e + 1]);
+          tc::tmem_st16(T_M + lane_addr + (c0 >> 1), packed);
         }
-        // w o x for this warp's share of the row
+        // w o x for the row
         {
           const unsigned char* xr = s.X + r * 128;
           unsigned char* wr = s.XW + r * 128;
 #pragma unroll
-          for (int cc = 0; cc < kColsPerWarp / 8; ++cc) {
-            const int ch = hc * (kColsPerWarp / 8) + cc;
+          for (int ch = 0; ch < 8; ++ch) {
             const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
             const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
             uint4 o;
@@ -408,58 +580,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         named_bar_sync(1, kComputeThreads);
         if (ct == 0) tc::mbar_arrive(&s.m_ready);
 
-        if (sub == 0 && !hin_ready) {   // the predecessor had not handed on yet
-          const unsigned long long w0 = global_ns();
-          int v;
-          for (uint32_t i = 0;; ++i) {
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + pair) : "memory");
-            if (v >= c) break;
-            if ((i & 63u) == 63u) {
-              if (aborted(p.ctrl)) break;
-              if (global_ns() - w0 > kWaitNs) {
-                atomicOr(p.ctrl + 1, kErrLookback);
-                break;
-              }
-            }
-            __nanosleep(64);
-          }
-#pragma unroll
-          for (int v4 = 0; v4 < kColsPerWarp / 4; ++v4)
-            asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(hin[4 * v4]), "=r"(hin[4 * v4 + 1]), "=r"(hin[4 * v4 + 2]),
-                           "=r"(hin[4 * v4 + 3])
-                         : "l"(hin_src + (int64_t)v4 * kN * 4)
-                         : "memory");
-        }
-
         // ---- h (entering) -> bf16 operand of Ye in X; H <- carry H in TMEM
         wait_or_flag(&s.yi_done, ph, p.ctrl);   // Yi has read x
         tc::fence_after_sync();
-#pragma unroll
-        for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
-          const int col = hc * kColsPerWarp + qd * 16;
-          uint32_t hv[16];
-          if (sub == 0) {   // the entering state, from registers
-#pragma unroll
-            for (int e = 0; e < 16; ++e) hv[e] = hin[qd * 16 + e];
-          } else {
-            tc::tmem_ld16(T_H + lane_addr + col, hv);
-            tc::tmem_ld_wait();
-          }
+        {   // 16 columns at a time (wider pieces raise the register peak)
           unsigned char* hr = s.X + r * 128;
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int ch = (col >> 3) + cc;
-            uint4 o;
-            o.x = tc::pack_bf16x2(__uint_as_float(hv[8 * cc + 0]), __uint_as_float(hv[8 * cc + 1]));
-            o.y = tc::pack_bf16x2(__uint_as_float(hv[8 * cc + 2]), __uint_as_float(hv[8 * cc + 3]));
-            o.z = tc::pack_bf16x2(__uint_as_float(hv[8 * cc + 4]), __uint_as_float(hv[8 * cc + 5]));
-            o.w = tc::pack_bf16x2(__uint_as_float(hv[8 * cc + 6]), __uint_as_float(hv[8 * cc + 7]));
-            *reinterpret_cast<uint4*>(hr + ((ch ^ (r & 7)) << 4)) = o;
-          }
+          for (int qd = 0; qd < 4; ++qd) {
+            uint32_t hv[16];
+            tc::tmem_ld16(T_H + lane_addr + qd * 16, hv);
+            tc::tmem_ld_wait_regs(hv);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) hv[e] = __float_as_uint(carry * __uint_as_float(hv[e]));
-          tc::tmem_st16(T_H + lane_addr + col, hv);
+            for (int cc = 0; cc < 2; ++cc)
+              *reinterpret_cast<uint4*>(hr + (((qd * 2 + cc) ^ (r & 7)) << 4)) = pack8(hv, 8 * cc);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hv[e] = __float_as_uint(carry * __uint_as_float(hv[e]));
+            tc::tmem_st16(T_H + lane_addr + qd * 16, hv);
+          }
         }
         tc::tmem_st_wait();
         tc::fence_proxy_async_smem();
@@ -470,26 +607,30 @@ __global__ void __launch_bounds__(kThreads, 2)
         wait_or_flag(&s.y_done, ph, p.ctrl);
         tc::fence_after_sync();
 
-        // ---- hand the chunk's final state on (this warp's columns)
-        if (sub == nsub - 1) {
+        // ---- hand the chunk's final state on
+        if (sub == cur.nsub - 1) {
           const bool last_chunk = c == p.nc - 1;
           if (!last_chunk || p.final_states) {
+            uint32_t h0[32], h1[32];
+            tc::tmem_ld32(T_H + lane_addr, h0);
+            tc::tmem_ld32(T_H + lane_addr + 32, h1);
+            tc::tmem_ld_wait_regs(h0);
+            tc::tmem_ld_wait_regs(h1);
+            if (last_chunk) {
+              float* dst = p.final_states + ((int64_t)cur.b * p.H + cur.h) * kP * kN + r;
 #pragma unroll
-            for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
-              const int col = hc * kColsPerWarp + qd * 16;
-              uint32_t hv[16];
-              tc::tmem_ld16(T_H + lane_addr + col, hv);
-              tc::tmem_ld_wait();
-              if (last_chunk) {
-                float* dst = p.final_states + ((int64_t)b * p.H + h) * kP * kN + r;
+              for (int e = 0; e < 32; ++e) {
+                dst[e * kN] = __uint_as_float(h0[e]);
+                dst[(32 + e) * kN] = __uint_as_float(h1[e]);
+              }
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(p.slots) +
+                           ((int64_t)pair * 2 + (c & 1)) * (kP / 4) * kN + r;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dst[(col + e) * kN] = __uint_as_float(hv[e]);
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(p.slots) +
-                             (((int64_t)pair * 2 + (c & 1)) * (kP / 4) + col / 4) * kN + r;
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                  dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
+              for (int v4 = 0; v4 < 8; ++v4) {
+                dst[v4 * kN] = make_uint4(h0[4 * v4], h0[4 * v4 + 1], h0[4 * v4 + 2], h0[4 * v4 + 3]);
+                dst[(8 + v4) * kN] =
+                    make_uint4(h1[4 * v4], h1[4 * v4 + 1], h1[4 * v4 + 2], h1[4 * v4 + 3]);
               }
             }
             publish_pending = !last_chunk;   // flag raised after the epilogue
@@ -501,17 +642,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (p.has_z) wait_or_flag(&s.zfull, ph, p.ctrl);
         unsigned char* zr = s.XW + r * 128;
 #pragma unroll
-        for (int qd = 0; qd < kColsPerWarp / 16; ++qd) {
-          const int col = hc * kColsPerWarp + qd * 16;
-          uint32_t yi[16], ye[16];
-          tc::tmem_ld16(T_A + lane_addr + col, yi);
-          tc::tmem_ld16(T_A + 64 + lane_addr + col, ye);
-          tc::tmem_ld_wait();
+        for (int half = 0; half < 2; ++half) {
+          uint32_t yi[32], ye[32];
+          tc::tmem_ld32(T_A + lane_addr + half * 32, yi);
+          tc::tmem_ld32(T_A + 64 + lane_addr + half * 32, ye);
+          tc::tmem_ld_wait_regs(yi);
+          tc::tmem_ld_wait_regs(ye);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int ch = (col >> 3) + cc;
-            uint4* slot = reinterpret_cast<uint4*>(zr + ((ch ^ (r & 7)) << 4));
-            const uint4 zv = p.has_z ? *slot : make_uint4(0u, 0u, 0u, 0u);
+          for (int cc = 0; cc < 4; ++cc) {
+            const int ch = half * 4 + cc;
+            uint4* zslot = reinterpret_cast<uint4*>(zr + ((ch ^ (r & 7)) << 4));
+            const uint4 zv = p.has_z ? *zslot : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
             uint32_t o[4];
 #pragma unroll
@@ -526,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               }
               o[u] = tc::pack_bf16x2(y2[0], y2[1]);
             }
-            *slot = make_uint4(o[0], o[1], o[2], o[3]);
+            *zslot = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
         tc::fence_proxy_async_smem();
@@ -541,13 +682,14 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           tc::mbar_arrive(&s.tmem_free);   // Yi / Ye read out
           // rows past the sequence end are outside the tensor map and not written
-          tc::tma_store_4d(&map_out, s.XW, 0, h, (int)(t0 + sub * kSub), b);
+          tc::tma_store_4d(&map_out, s.XW, 0, cur.h, (int)(cur.t0 + sub * kSub), cur.b);
           tc::bulk_commit();
-          tc::bulk_wait_read();            // XW may be rewritten after this
         }
         l_prev = l_last;
         sg_prev = sg_last;
       }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&s.tk_empty[slot]);   // this item's vectors are read
     }
   }
 
@@ -625,10 +767,10 @@ bool fused_eligible(const Dims& d, bool bf16) {
 size_t fused_ctrl_ints(const Dims& d) { return 64 + (size_t)d.batch * d.nheads; }
 
 cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
-                         const __nv_bfloat16* Cm, const float* dt_out, const float* cs,
-                         const int32_t* seg, const float* D, const __nv_bfloat16* z,
-                         const float* init, float* final_states, __nv_bfloat16* out,
-                         float* slots, int* ctrl, const Dims& d, cudaStream_t st) {
+                         const __nv_bfloat16* Cm, const FusedVectors& v, const float* D,
+                         const __nv_bfloat16* z, const float* init, float* final_states,
+                         __nv_bfloat16* out, float* slots, int* ctrl, const Dims& d,
+                         cudaStream_t st) {
   CUtensorMap mx, mb, mc, mz, mo;
   if (!make_map(&mx, x, fused::kP, d.nheads, d.seqlen, d.batch) ||
       !make_map(&mb, Bm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
@@ -640,9 +782,18 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   cudaError_t e = cudaMemsetAsync(ctrl, 0, fused_ctrl_ints(d) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   fused::Params p;
-  p.dt = dt_out;
-  p.cs = cs;
-  p.seg = seg;
+  p.dt_raw = v.dt_raw;
+  p.dt_bias = v.dt_bias;
+  p.A = v.A;
+  p.seq_idx = v.dt_raw ? v.seq_idx : nullptr;
+  p.softplus = v.softplus;
+  p.do_clamp = v.do_clamp;
+  p.lo = v.lo;
+  p.hi = v.hi;
+  p.dt = v.dt;
+  p.cs = v.cs;
+  p.seg = v.dt_raw ? nullptr : v.seg;
+  p.has_seg = v.dt_raw ? v.seq_idx != nullptr : v.seg != nullptr;
   p.D = D;
   p.has_z = z != nullptr;
   p.init = init;
@@ -656,7 +807,6 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.G = d.ngroups;
   p.Q = d.chunk;
   p.nc = d.nchunks;
-  p.nsub_max = d.chunk / fused::kSub;
   p.items = (long long)d.batch * d.nchunks * d.nheads;
   const size_t smem = sizeof(fused::Smem) + 1024;
   static bool attr_set = false;
