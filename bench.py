@@ -326,7 +326,7 @@ def main():
     # per-kernel durations, with events between the launches: the fused path
     # is one kernel (all four stages); the SIMT path is the four stage kernels
     fused = (cfg.dtype == "bf16" and cfg.headdim == 64 and cfg.dstate == 128
-             and Q in (128, 256))
+             and Q in (128, 256) and (cfg.nheads // cfg.ngroups) % 2 == 0)
     names = (["scan_fused"] if fused else
              ["dt_cumsum", "chunk_state", "state_passing", "chunk_scan"])
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]

@@ -67,17 +67,19 @@ int ssd_abi_version(void);
 const char *ssd_last_error(void);
 
 /* Bytes of device workspace ssd_scan_fwd needs for these sizes: a control
- * block of (64 + batch*nheads) int32 (work counter, error word, per-(b, h)
- * hand-off flags of the fused kernel), processed dt and per-chunk cumsum
+ * block of (64 + batch*nheads) int32 (work counter, error word, hand-off
+ * flags of the fused kernel), processed dt and per-chunk cumsum
  * [batch, nheads, nchunks, chunk_size] float each, per-chunk segment counts
  * [batch, nchunks, chunk_size] int32, and chunk states
  * [batch, nchunks, nheads, headdim, dstate] float (the fused kernel uses the
  * start of this region for its state hand-off slots).  Each piece starts on
  * a 256-byte boundary.  0 on bad sizes.
  *
- * For bf16 inputs with headdim 64, dstate 128 and chunk_size 128 or 256,
- * ssd_scan_fwd runs stage 1 and then ssd_chunk_fused's kernel; otherwise the
- * four stage kernels below. */
+ * For bf16 inputs with headdim 64, dstate 128, chunk_size 128 or 256 and an
+ * even number of heads per group (nheads / ngroups), ssd_scan_fwd runs all
+ * four stages in the fused tensor-core kernel of ssd_chunk_fused (which then
+ * computes stage 1 itself and leaves the dt / cumsum / segment regions of
+ * the workspace unused); otherwise the four stage kernels below. */
 size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
                                 int headdim, int dstate, int ngroups,
                                 int chunk_size, ssd_dtype_t dtype);
@@ -178,8 +180,9 @@ int ssd_chunk_scan(const void *x, const void *B, const void *C,
                    void *stream);
 
 /* Stages 2-4 fused into one tensor-core (tcgen05) kernel, for bf16 inputs
- * with headdim 64, dstate 128 and chunk_size 128 or 256 (SSD_ERR_UNSUPPORTED
- * otherwise).  Inputs are stage 1's dt_out / dA_cumsum / chunk_seg plus x, B,
+ * with headdim 64, dstate 128, chunk_size 128 or 256 and an even number of
+ * heads per group (SSD_ERR_UNSUPPORTED otherwise; the kernel takes the heads
+ * of a group in pairs that share the B / C tiles).  Inputs are stage 1's dt_out / dA_cumsum / chunk_seg plus x, B,
  * C, D, z, initial_states as in ssd_scan_fwd; writes out and (if not NULL)
  * final_states.  workspace (>= ssd_scan_workspace_bytes) is required: the
  * kernel hands each chunk's final state to the next chunk through it.  If a

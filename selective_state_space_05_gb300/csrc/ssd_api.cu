@@ -71,7 +71,7 @@ int check_dtype(ssd_dtype_t t) {
 }
 
 struct Workspace {
-  int* ctrl;   // fused path: ticket counter, error word, per-(b,h) flags
+  int* ctrl;   // fused path: ticket counter, error word, hand-off flags
   float* dt;
   float* cs;
   int32_t* seg;
@@ -233,7 +233,8 @@ int ssd_chunk_fused(const void* x, const void* B, const void* C, const float* dt
   if (rc) return rc;
   if (!ssd::fused_eligible(d, dtype == SSD_DTYPE_BF16))
     return fail(SSD_ERR_UNSUPPORTED,
-                "ssd_chunk_fused needs bf16, headdim 64, dstate 128 and chunk_size 128 or 256");
+                "ssd_chunk_fused needs bf16, headdim 64, dstate 128, chunk_size 128 or 256 and an "
+                "even number of heads per group");
   if (!x || !B || !C || !dt_out || !dA_cumsum || !out || !workspace)
     return fail(SSD_ERR_NULL, "x, B, C, dt_out, dA_cumsum, out and workspace are required");
   const void* ptrs[] = {x, B, C, z, out, initial_states, final_states, workspace};

@@ -1,32 +1,36 @@
 // Fused tensor-core SSD kernel for sm_103a (bf16 inputs, headdim 64, dstate
-// 128, chunk 128 or 256): dt preprocessing and the per-chunk cumsum of dt*A,
-// chunk states, inter-chunk state passing and chunk outputs in one persistent
-// kernel.
+// 128, chunk 128 or 256, an even number of heads per group): dt
+// preprocessing and the per-chunk cumsum of dt*A, chunk states, inter-chunk
+// state passing and chunk outputs in one persistent kernel, one CTA per SM.
 //
-// Work item = (batch b, chunk c, head h), taken from an atomic ticket counter
-// in chunk-major order, so an item's predecessor (b, c-1, h) always holds an
-// earlier ticket.  Warp roles:
+// Work item = (batch b, chunk c, head pair h0 = 2 hp, h1 = h0 + 1), both
+// heads of one B/C group, taken from an atomic ticket counter in chunk-major
+// order, so an item's predecessor (b, c-1, hp) always holds an earlier
+// ticket.  Warp roles:
 //   warp 0    takes the tickets and, one item ahead, computes the item's
 //             per-token vectors (dt = softplus(dt_raw + dt_bias) clamped, the
-//             cumsum of dt*A, the reset counts of seq_idx) into a two-slot
-//             ring; lane 0 issues the TMA tile loads
+//             cumsum of dt*A per head, the reset counts of seq_idx) into a
+//             two-slot ring; lane 0 issues the TMA tile loads
 //   warp 1    lane 0 issues the tcgen05 MMAs
-//   warps 2-5 build the decay matrix, move the state and run the epilogue
+//   warps 2-9 four per head (one per TMEM lane quarter): decay matrix,
+//             state moves, epilogue
 // A chunk is processed as 128-token sub-steps; per sub-step, with rows /
-// columns = the sub-step's tokens and cs the chunk's cumsum:
-//   CB   = C B^T                       tcgen05, A = C (K-major), B = B (K-major)
-//   M    = CB o exp(cs_i - cs_j) dt_j  (j <= i, same document)   CUDA cores -> TMEM
-//   Yi   = M x                         tcgen05, A = M from TMEM, B = x (MN-major)
-//   Ye   = C h                         tcgen05, A = C, B = h as bf16 (MN-major)
-//   H   <- exp(cs_last - cs_prev) H    CUDA cores, in TMEM (fp32 state H = h^T)
-//   H   += B^T (w o x)                 tcgen05, A = B (MN-major), B = w o x (MN-major)
+// columns = the sub-step's tokens, cs the chunk's cumsum and h_e the state
+// entering the sub-step (head e = 0, 1):
+//   [CB | Ye_0 | Ye_1] = C [B^T | h_0 | h_1]   one N=256 tcgen05 chain, A = C
+//   M_e  = CB o exp(cs_i - cs_j) dt_j  (j <= i, same document)   CUDA cores -> TMEM
+//   Yi_e = M_e x_e                     tcgen05, A = M_e from TMEM
+//   H_e <- exp(cs_last - cs_prev) H_e  CUDA cores, in TMEM (fp32 state H = h^T)
+//   [H_0 | H_1] += B^T [w_0 o x_0 | w_1 o x_1]   one N=128 chain, A = B^T
 //          w_j = exp(cs_last - cs_j) dt_j  (the sub-step's own chunk state)
-//   out  = (Yi + exp(cs_i - cs_prev) Ye + D x) * silu(z)
-// where h is the state entering the sub-step; the fp32 state stays in TMEM
-// (one row of dstate per TMEM lane, headdim columns) for the whole chunk.  The
-// state entering a chunk is handed from item (b, c-1, h) through an
-// L2-resident fp32 slot and a flag (decoupled look-back); every wait is
-// bounded and gives up with an error word instead of hanging.
+//   out_e = (Yi_e + exp(cs_i - cs_prev) Ye_e + D x_e) * silu(z_e)
+// Sharing the A operand across the pair halves the MMA instructions per head
+// (an M=128 tcgen05.mma costs about the same for N = 64 .. 256).  The fp32
+// states stay in TMEM (one row of dstate per TMEM lane, headdim columns) for
+// the whole chunk.  The states entering a chunk are handed from the item
+// (b, c-1, hp) through L2-resident fp32 slots and a flag (decoupled
+// look-back); every wait is bounded and gives up with an error word instead
+// of hanging.
 #include <cudaTypedefs.h>
 
 #include "../../include/ssd_scan.h"
@@ -41,34 +45,46 @@ constexpr int kP = 64;      // headdim
 constexpr int kN = 128;     // dstate
 constexpr int kQmax = 256;  // largest chunk
 constexpr int kRing = 2;    // items whose tickets / vectors are published
+constexpr int kNH = 2;      // heads per item
 constexpr int kComputeWarp0 = 2;        // warps 0 (TMA) and 1 (MMA) come first
-constexpr int kComputeThreads = 128;    // one warp per TMEM lane quarter
+constexpr int kComputeThreads = 128 * kNH;   // one warp per head and TMEM lane quarter
 constexpr int kThreads = kComputeWarp0 * 32 + kComputeThreads;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // any single wait: 2 s at most
 constexpr uint32_t kSleepHintNs = 20000;                 // suspend hint of one try_wait
+
+// TMEM columns: [CB | Ye_0 | Ye_1], then Yi_0 / Yi_1 over CB; M_e; H_e
+constexpr uint32_t kT_CB = 0, kT_YE = 128, kT_M = 256, kT_H = 384;
 
 // error bits in the control block word ctrl[1]; once one is set every later
 // wait of the launch returns at once, so a broken launch still ends quickly
 constexpr int kErrBarrier = 1;
 constexpr int kErrLookback = 2;
 
+// B operand of the [CB | Ye] chain, K-major with the 128-byte swizzle: per
+// 64-column (dstate) half, 256 rows of 128 bytes -- rows 0-127 the B tile
+// (tokens), rows 128 + 64 e + p the entering state of head e, headdim p.
+constexpr int kBhHalf = 256 * 128;
+
 struct alignas(1024) Smem {
-  unsigned char C[kSub * kN * 2];    // two 64-column halves, 128B swizzle
-  unsigned char B[kSub * kN * 2];    // same
-  unsigned char X[kSub * kP * 2];    // x; after Yi has read it: h as bf16
-  unsigned char XW[kSub * kP * 2];   // w o x; after the MMAs: z, then out
-  float lv[kRing][kQmax];   // l = log2(e) * cumsum of dt*A over the chunk
-  float dtv[kRing][kQmax];  // dt
-  int segv[kRing][kQmax];   // reset counts (with seq_idx)
-  float mcol[kSub];     // l_j - log2(dt_j): column term of the diagonal blocks
-  float bcol[kSub];     // exp2(l_e - l_j) dt_j, e = last column of j's 32-block
-  long long tk[kRing];  // published tickets (>= items: no more work)
+  unsigned char C[kSub * kN * 2];      // two 64-column halves, 128B swizzle
+  unsigned char BH[2 * kBhHalf];       // see kBhHalf
+  unsigned char X[kNH][kSub * kP * 2]; // x_e (MN-major B operand of Yi_e)
+  unsigned char XW[kNH][kSub * kP * 2];   // w o x_e (state B operand); then out_e
+  float lv[kRing][kNH][kQmax];   // l = log2(e) * cumsum of dt*A over the chunk
+  float dtv[kRing][kNH][kQmax];  // dt
+  int segv[kRing][kQmax];        // reset counts (with seq_idx)
+  float mcol[kNH][kSub];   // l_j - log2(dt_j): column term of the diagonal blocks
+  float bcol[kNH][kSub];   // exp2(l_e - l_j) dt_j, e = last column of j's 32-block
+  long long tk[kRing];     // published tickets (>= items: no more work)
   uint64_t tk_full[kRing], tk_empty[kRing];
-  uint64_t full, zfull, cb, m_ready, yi_done, h_ready, y_done, tmem_free;
+  uint64_t full, h_ready, cb, m_ready, y_done, tmem_free;
   uint32_t tmem_base;
   long long first_ticket;
 };
+
+// one CTA per SM: the tiles and the alignment slack within the 227 KB a block may use
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory");
 
 struct Params {
   // per-token vectors: computed here from the raw inputs (dt_raw != null) or
@@ -84,11 +100,11 @@ struct Params {
   const int32_t* seg;    // [B, nc, Q] or null
   bool has_seg;          // reset counts exist (seq_idx or seg given)
   const float* D;        // [H] or null
-  bool has_z;
+  const __nv_bfloat16* z;   // [B, L, H, P] or null
   const float* init;     // [B, H, P, N] or null
   float* final_states;   // [B, H, P, N] or null
   float* slots;          // [B*H, 2, P/4, N, 4]: hand-off states, column quads outermost
-  int* flags;            // [B*H]
+  int* flags;            // [B * H/2]: chunks handed on per head pair
   int* ctrl;             // [0] ticket counter, [1] error word
   int64_t L;
   int B, H, G, Q, nc;
@@ -96,18 +112,19 @@ struct Params {
 };
 
 struct Item {
-  int b, c, h, g, pair, nvalid, nsub;
+  int b, c, h0, g, pair, nvalid, nsub;   // pair = b * H/2 + h0/2
   int64_t t0;
 };
 
 __device__ __forceinline__ Item decode(const Params& p, long long t) {
   Item it;
-  const int pairs = p.B * p.H;
+  const int hp = p.H / kNH;
+  const int pairs = p.B * hp;
   it.c = (int)(t / pairs);
   it.pair = (int)(t % pairs);
-  it.b = it.pair / p.H;
-  it.h = it.pair % p.H;
-  it.g = it.h / (p.H / p.G);
+  it.b = it.pair / hp;
+  it.h0 = (it.pair % hp) * kNH;
+  it.g = it.h0 / (p.H / p.G);
   it.t0 = (int64_t)it.c * p.Q;
   it.nvalid = (int)min((int64_t)p.Q, p.L - it.t0);
   it.nsub = (it.nvalid + kSub - 1) / kSub;
@@ -157,17 +174,17 @@ __device__ __forceinline__ T warp_incl_scan(T v, int lane) {
   return v;
 }
 
-// The per-token vectors of one item, written by the 32 lanes of a warp: lane
-// i owns positions [i E, i E + E) of the chunk, E = Q / 32.  Positions past
-// the sequence end get dt = 0, so that l and the reset count keep their last
-// values there.
-__device__ __forceinline__ void item_vectors(const Params& p, const Item& it, float* lv, float* dtv,
-                                          int* segv, int lane) {
+// The per-token vectors of head h of one item, written by the 32 lanes of a
+// warp: lane i owns positions [i E, i E + E) of the chunk, E = Q / 32.
+// Positions past the sequence end get dt = 0, so that l and the reset count
+// keep their last values there.  segv == null: no reset counts wanted.
+__device__ __forceinline__ void item_vectors(const Params& p, const Item& it, int h, float* lv,
+                                             float* dtv, int* segv, int lane) {
   const int Q = p.Q, E = Q / 32;
   if (p.dt_raw) {
-    const float a = p.A[it.h] * kLog2e;
-    const float bias = p.dt_bias ? p.dt_bias[it.h] : 0.f;
-    const __nv_bfloat16* src = p.dt_raw + ((int64_t)it.b * p.L + it.t0) * p.H + it.h;
+    const float a = p.A[h] * kLog2e;
+    const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
+    const __nv_bfloat16* src = p.dt_raw + ((int64_t)it.b * p.L + it.t0) * p.H + h;
     float v[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -195,7 +212,7 @@ __device__ __forceinline__ void item_vectors(const Params& p, const Item& it, fl
         lv[lane * E + e] = excl + loc[e];
       }
     }
-    if (p.seq_idx) {
+    if (p.seq_idx && segv) {
       const int32_t* sq = p.seq_idx + (int64_t)it.b * p.L;
       int cnt = 0, lc[8];
 #pragma unroll
@@ -213,29 +230,18 @@ __device__ __forceinline__ void item_vectors(const Params& p, const Item& it, fl
         if (e < E) segv[lane * E + e] = cex + lc[e];
     }
   } else {
-    const int64_t pq = ((int64_t)it.b * p.H + it.h) * p.nc + it.c;
+    const int64_t pq = ((int64_t)it.b * p.H + h) * p.nc + it.c;
     for (int i = lane; i < Q; i += 32) {
       lv[i] = p.cs[pq * Q + i] * kLog2e;
       dtv[i] = p.dt[pq * Q + i];
     }
-    if (p.seg)
+    if (p.seg && segv)
       for (int i = lane; i < Q; i += 32) segv[i] = p.seg[((int64_t)it.b * p.nc + it.c) * Q + i];
   }
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-// Eight fp32 values (bit patterns) from position i as one 16-byte bf16 chunk.
-template <int n>
-__device__ __forceinline__ uint4 pack8(const uint32_t (&v)[n], int i) {
-  uint4 o;
-  o.x = tc::pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-  o.y = tc::pack_bf16x2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-  o.z = tc::pack_bf16x2(__uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
-  o.w = tc::pack_bf16x2(__uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
-  return o;
-}
 
 __device__ __forceinline__ float tanh_fast(float v) {
   float r;
@@ -259,11 +265,10 @@ __device__ __forceinline__ void load_slot_quads(uint32_t (&hv)[32], const float*
                  : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap map_x,
                      const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_c,
-                     const __grid_constant__ CUtensorMap map_z,
                      const __grid_constant__ CUtensorMap map_out, Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (128-byte swizzle atoms), derived from the shared
@@ -278,40 +283,38 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (tid == 0) {
     tc::mbar_init(&s.full, 1);
-    tc::mbar_init(&s.zfull, 1);
+    tc::mbar_init(&s.h_ready, 1);
     tc::mbar_init(&s.cb, 1);
     tc::mbar_init(&s.m_ready, 1);
-    tc::mbar_init(&s.yi_done, 1);
-    tc::mbar_init(&s.h_ready, 1);
     tc::mbar_init(&s.y_done, 1);
     tc::mbar_init(&s.tmem_free, 1);
     for (int i = 0; i < kRing; ++i) {
-      tc::mbar_init(&s.tk_full[i], 32);      // the 32 lanes of warp 0
-      tc::mbar_init(&s.tk_empty[i], 1 + 4);  // MMA lane + the 4 compute warps
+      tc::mbar_init(&s.tk_full[i], 32);                          // the 32 lanes of warp 0
+      tc::mbar_init(&s.tk_empty[i], 1 + kComputeThreads / 32);   // MMA lane + compute warps
     }
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&map_x);
     tc::tma_prefetch_desc(&map_b);
     tc::tma_prefetch_desc(&map_c);
     tc::tma_prefetch_desc(&map_out);
-    if (p.has_z) tc::tma_prefetch_desc(&map_z);
     s.first_ticket = atomicAdd(p.ctrl, 1);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
-  const uint32_t T_A = tmem + 0;     // CB fp32 [0,128); then Yi [0,64) and Ye [64,128)
-  const uint32_t T_M = tmem + 128;   // M as bf16 pairs (A operand of Yi)
-  const uint32_t T_H = tmem + 192;   // fp32 state, row n = dstate index, columns = headdim
 
   if (warp == 0) {
     // ---------------- tickets, per-token vectors (one item ahead) and the
-    // TMA loads: a sub-step's C, B, x tiles as soon as the previous
-    // sub-step's MMAs are done with them, its z tile into XW once its own
-    // MMAs are done with w o x
+    // TMA loads: a sub-step's C, B, x_0, x_1 tiles as soon as the previous
+    // sub-step's MMAs are done with them
     long long t_cur = s.first_ticket;
-    if (t_cur < p.items) item_vectors(p, decode(p, t_cur), s.lv[0], s.dtv[0], s.segv[0], lane);
+    if (t_cur < p.items) {
+      const Item it0 = decode(p, t_cur);
+      for (int e = 0; e < kNH; ++e)
+        item_vectors(p, it0, it0.h0 + e, s.lv[0][e], s.dtv[0][e], e == 0 ? s.segv[0] : nullptr,
+                     lane);
+    }
     if (lane == 0) s.tk[0] = t_cur;
     tc::mbar_arrive(&s.tk_full[0]);
     long long t_pend = p.items;   // lane 0: the ticket after the published ones
@@ -324,29 +327,29 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int tok = (int)(cur.t0 + sub * kSub);
         if (lane == 0) {
           wait_or_flag(&s.y_done, (k & 1) ^ 1, p.ctrl);
-          tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kSub * kP * 2);
+          tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kNH * kSub * kP * 2);
           tc::tma_load_4d(s.C, &map_c, &s.full, 0, cur.g, tok, cur.b);
           tc::tma_load_4d(s.C + kSub * 128, &map_c, &s.full, 64, cur.g, tok, cur.b);
-          tc::tma_load_4d(s.B, &map_b, &s.full, 0, cur.g, tok, cur.b);
-          tc::tma_load_4d(s.B + kSub * 128, &map_b, &s.full, 64, cur.g, tok, cur.b);
-          tc::tma_load_4d(s.X, &map_x, &s.full, 0, cur.h, tok, cur.b);
+          tc::tma_load_4d(s.BH, &map_b, &s.full, 0, cur.g, tok, cur.b);
+          tc::tma_load_4d(s.BH + kBhHalf, &map_b, &s.full, 64, cur.g, tok, cur.b);
+          tc::tma_load_4d(s.X[0], &map_x, &s.full, 0, cur.h0, tok, cur.b);
+          tc::tma_load_4d(s.X[1], &map_x, &s.full, 0, cur.h0 + 1, tok, cur.b);
         }
         if (sub == 0) {   // publish the next item into the other ring slot
           t_nxt = __shfl_sync(0xffffffffu, t_pend, 0);
           const int j = it + 1, slot = j % kRing;
           wait_or_flag(&s.tk_empty[slot], ((j / kRing) & 1) ^ 1, p.ctrl);
-          if (t_nxt < p.items)
-            item_vectors(p, decode(p, t_nxt), s.lv[slot], s.dtv[slot], s.segv[slot], lane);
+          if (t_nxt < p.items) {
+            const Item nx = decode(p, t_nxt);
+            for (int e = 0; e < kNH; ++e)
+              item_vectors(p, nx, nx.h0 + e, s.lv[slot][e], s.dtv[slot][e],
+                           e == 0 ? s.segv[slot] : nullptr, lane);
+          }
           if (lane == 0) {
             s.tk[slot] = t_nxt;
             if (t_nxt < p.items) t_pend = atomicAdd(p.ctrl, 1);
           }
           tc::mbar_arrive(&s.tk_full[slot]);
-        }
-        if (lane == 0 && p.has_z) {
-          wait_or_flag(&s.y_done, k & 1, p.ctrl);
-          tc::mbar_arrive_expect_tx(&s.zfull, kSub * kP * 2);
-          tc::tma_load_4d(s.XW, &map_z, &s.zfull, 0, cur.h, tok, cur.b);
         }
       }
       t_cur = t_nxt;
@@ -354,14 +357,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
+      // descriptor start addresses advance in 16-byte units: K-major k-steps
+      // are 32 bytes inside a 64-column half, MN-major k-steps 8 rows of 128 bytes
       const uint64_t dC = tc::sdesc_sw128(tc::smem_u32(s.C), 16, 1024);
-      const uint64_t dB = tc::sdesc_sw128(tc::smem_u32(s.B), 16, 1024);
-      const uint64_t dBmn = tc::sdesc_sw128(tc::smem_u32(s.B), kSub * 128, 1024);
-      const uint64_t dX = tc::sdesc_sw128(tc::smem_u32(s.X), 16384, 1024);
-      const uint64_t dXW = tc::sdesc_sw128(tc::smem_u32(s.XW), 16384, 1024);
-      constexpr uint32_t id_cb = tc::idesc_bf16(kSub, kSub, false, false);
+      const uint64_t dBH = tc::sdesc_sw128(tc::smem_u32(s.BH), 16, 1024);
+      const uint64_t dBmn = tc::sdesc_sw128(tc::smem_u32(s.BH), kBhHalf, 1024);
+      const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(s.X[0]), 16384, 1024);
+      const uint64_t dX1 = tc::sdesc_sw128(tc::smem_u32(s.X[1]), 16384, 1024);
+      const uint64_t dXW = tc::sdesc_sw128(tc::smem_u32(s.XW[0]), kSub * kP * 2, 1024);
+      constexpr uint32_t id_cbye = tc::idesc_bf16(kSub, 256, false, false);
       constexpr uint32_t id_y = tc::idesc_bf16(kSub, kP, false, true);
-      constexpr uint32_t id_s = tc::idesc_bf16(kN, kP, true, true);
+      constexpr uint32_t id_s = tc::idesc_bf16(kN, kNH * kP, true, true);
       uint32_t k = 0;
       for (int it = 0;; ++it) {
         const int slot = it % kRing;
@@ -374,51 +380,56 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t ph = k & 1;
           wait_or_flag(&s.tmem_free, ph ^ 1, p.ctrl);
           wait_or_flag(&s.full, ph, p.ctrl);
+          wait_or_flag(&s.h_ready, ph, p.ctrl);
           tc::fence_after_sync();
-          // descriptor start addresses advance in 16-byte units: K-major
-          // k-steps are 32 bytes inside a 64-column half (16 KB apart),
-          // MN-major k-steps are 8 rows of 128 bytes
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {   // CB = C B^T, K = dstate
-            const uint32_t ko = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
-            tc::mma_ss(T_A, dC + ko, dB + ko, id_cb, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {   // [CB | Ye_0 | Ye_1] = C [B^T | h_0 | h_1], K = dstate
+            const uint32_t kc = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
+            const uint32_t kb = ((kk >> 2) * kBhHalf + (kk & 3) * 32) >> 4;
+            tc::mma_ss(tmem + kT_CB, dC + kc, dBH + kb, id_cbye, kk > 0);
           }
           tc::mma_commit(&s.cb);
           wait_or_flag(&s.m_ready, ph, p.ctrl);
           tc::fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)     // Yi = M x (M holds the D skip), K = tokens
-            tc::mma_ts(T_A, T_M + kk * 8, dX + kk * 128, id_y, kk > 0);
-          tc::mma_commit(&s.yi_done);
-          wait_or_flag(&s.h_ready, ph, p.ctrl);
-          tc::fence_after_sync();
+          for (int kk = 0; kk < 8; ++kk)     // Yi_0 = M_0 x_0 (M holds the D skip), K = tokens
+            tc::mma_ts(tmem + kT_CB, tmem + kT_M + kk * 8, dX0 + kk * 128, id_y, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {   // Ye = C h, K = dstate (h as bf16 in X)
-            const uint32_t ko = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
-            tc::mma_ss(T_A + 64, dC + ko, dX + kk * 128, id_y, kk > 0);
-          }
+          for (int kk = 0; kk < 8; ++kk)     // Yi_1 = M_1 x_1
+            tc::mma_ts(tmem + kT_CB + kP, tmem + kT_M + kP + kk * 8, dX1 + kk * 128, id_y, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)     // H += B^T (w o x), K = tokens
-            tc::mma_ss(T_H, dBmn + kk * 128, dXW + kk * 128, id_s, 1);
+          for (int kk = 0; kk < 8; ++kk)     // [H_0 | H_1] += B^T [w o x_0 | w o x_1], K = tokens
+            tc::mma_ss(tmem + kT_H, dBmn + kk * 128, dXW + kk * 128, id_s, 1);
           tc::mma_commit(&s.y_done);
         }
       }
     }
   } else {
-    // ---------------- compute: warp (quarter qr) owns row r = 32 qr + lane
-    // of every TMEM tile and of the sub-step's smem tiles
+    // ---------------- compute: warp (head e, quarter qr) owns row r = 32 qr
+    // + lane of head e's TMEM tiles and of the sub-step's smem tiles
+    const int cw = warp - kComputeWarp0;
+    const int e = cw >> 2;                        // head of the pair
     const int qr = warp & 3;                      // TMEM lane quarter
     const int r = qr * 32 + lane;                 // row: token (or dstate index)
     const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
+    const uint32_t T_CBr = tmem + kT_CB + lane_addr;        // CB row r
+    const uint32_t T_YIr = tmem + kT_CB + e * kP + lane_addr;
+    const uint32_t T_YEr = tmem + kT_YE + e * kP + lane_addr;
+    const uint32_t T_Mr = tmem + kT_M + e * kP + lane_addr;
+    const uint32_t T_Hr = tmem + kT_H + e * kP + lane_addr;
     const int ct = tid - kComputeWarp0 * 32;
     {   // the blocks of M above the diagonal stay zero
       uint32_t zero[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) zero[e] = 0u;
-      tc::tmem_st32(T_M + lane_addr, zero);
-      tc::tmem_st32(T_M + lane_addr + 32, zero);
+      for (int i = 0; i < 32; ++i) zero[i] = 0u;
+      tc::tmem_st32(T_Mr, zero);
+      tc::tmem_st32(T_Mr + 32, zero);
       tc::tmem_st_wait();
     }
+    // entering-state rows of the [B^T | h] operand for this thread: dstate
+    // index r is K; headdim p of head e is row 128 + 64 e + p of r's half
+    unsigned char* hk = s.BH + (r >> 6) * kBhHalf + (128 + e * kP) * 128 + (r & 7) * 2;
+    const int kchunk = (r & 63) >> 3;
     uint32_t k = 0;
     for (int it = 0;; ++it) {
       const int slot = it % kRing;
@@ -426,102 +437,115 @@ __global__ void __launch_bounds__(kThreads, 2)
       const long long t = s.tk[slot];
       if (t >= p.items || aborted(p.ctrl)) break;
       const Item cur = decode(p, t);
-      const int c = cur.c, pair = cur.pair;
-      const float Dh = p.D ? p.D[cur.h] : 0.f;
+      const int c = cur.c, h = cur.h0 + e;
+      const int64_t bh = (int64_t)cur.b * p.H + h;   // this head's state slots
+      const float Dh = p.D ? p.D[h] : 0.f;
       float l_prev = 0.f;
       int sg_prev = 0;
 
-      // the state entering the chunk, this row: loads issued now (each
-      // thread acquires the predecessor's flag itself) and written to T_H
-      // once the first sub-step's tiles have landed, so that they overlap
-      // that wait
-      uint32_t hin0[32], hin1[32];   // headdim columns 0-31 and 32-63
-      bool hin_ready = true;
-      const float* hin_src = nullptr;
-      if (c == 0) {
-        if (p.init) {
-          const float* src = p.init + ((int64_t)cur.b * p.H + cur.h) * kP * kN + r;
+      // the state entering the chunk, this row: loaded, then written to T_H
+      // (the predecessor item raised its flag after both heads' slots)
+      {
+        uint32_t hin0[32], hin1[32];   // headdim columns 0-31 and 32-63
+        if (c == 0) {
+          if (p.init) {
+            const float* src = p.init + bh * kP * kN + r;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            hin0[e] = __float_as_uint(src[e * kN]);
-            hin1[e] = __float_as_uint(src[(32 + e) * kN]);
+            for (int i = 0; i < 32; ++i) {
+              hin0[i] = __float_as_uint(src[i * kN]);
+              hin1[i] = __float_as_uint(src[(32 + i) * kN]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hin0[i] = hin1[i] = 0u;
           }
         } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) hin0[e] = hin1[e] = 0u;
+          // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
+          const float* src = p.slots + ((bh * 2 + ((c - 1) & 1)) * (kP / 4) * kN + r) * 4;
+          const unsigned long long w0 = global_ns();
+          int v;
+          for (uint32_t i = 0;; ++i) {
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + cur.pair) : "memory");
+            if (v >= c) break;
+            if ((i & 63u) == 63u) {
+              if (aborted(p.ctrl)) break;
+              if (global_ns() - w0 > kWaitNs) {
+                atomicOr(p.ctrl + 1, kErrLookback);
+                break;
+              }
+            }
+            __nanosleep(64);
+          }
+          load_slot_quads(hin0, src);
+          load_slot_quads(hin1, src + 8 * kN * 4);
         }
-      } else {
-        // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
-        hin_src = p.slots + (((int64_t)pair * 2 + ((c - 1) & 1)) * (kP / 4) * kN + r) * 4;
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + pair) : "memory");
-        hin_ready = v >= c;
-        if (hin_ready) {
-          load_slot_quads(hin0, hin_src);
-          load_slot_quads(hin1, hin_src + 8 * kN * 4);
-        }
+        tc::tmem_st32(T_Hr, hin0);
+        tc::tmem_st32(T_Hr + 32, hin1);
       }
       bool publish_pending = false;
-      wait_or_flag(&s.full, k & 1, p.ctrl);   // the first sub-step's tiles
-      if (!hin_ready) {   // the predecessor had not handed on yet
-        const unsigned long long w0 = global_ns();
-        int v;
-        for (uint32_t i = 0;; ++i) {
-          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + pair) : "memory");
-          if (v >= c) break;
-          if ((i & 63u) == 63u) {
-            if (aborted(p.ctrl)) break;
-            if (global_ns() - w0 > kWaitNs) {
-              atomicOr(p.ctrl + 1, kErrLookback);
-              break;
-            }
-          }
-          __nanosleep(64);
-        }
-        load_slot_quads(hin0, hin_src);
-        load_slot_quads(hin1, hin_src + 8 * kN * 4);
-      }
-      tc::tmem_st32(T_H + lane_addr, hin0);
-      tc::tmem_st32(T_H + lane_addr + 32, hin1);
 
       for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
         const uint32_t ph = k & 1;
         const bool valid = sub * kSub + r < cur.nvalid;   // this row's token exists
-        if (sub > 0) wait_or_flag(&s.full, ph, p.ctrl);
         // per-token scalars of the sub-step (positions past the end hold the
         // chunk's last values)
-        const float* lv = s.lv[slot] + sub * kSub;
+        const float* lv = s.lv[slot][e] + sub * kSub;
         const int* sgv = s.segv[slot] + sub * kSub;
         const float l_r = lv[r];
-        const float dt_r = s.dtv[slot][sub * kSub + r];
+        const float dt_r = s.dtv[slot][e][sub * kSub + r];
         const int sg_r = p.has_seg ? sgv[r] : 0;
         const float l_last = lv[kSub - 1];
         const int sg_last = p.has_seg ? sgv[kSub - 1] : 0;
-        s.mcol[r] = dt_r > 0.f ? l_r - __log2f(dt_r) : __int_as_float(0x7f800000);
-        s.bcol[r] = ex2(lv[r | 31] - l_r) * dt_r;
+        s.mcol[e][r] = dt_r > 0.f ? l_r - __log2f(dt_r) : __int_as_float(0x7f800000);
+        s.bcol[e][r] = ex2(lv[r | 31] - l_r) * dt_r;
         const float w_r = (valid && sg_r == sg_last) ? ex2(l_last - l_r) * dt_r : 0.f;
         const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
         const float carry = sg_last == sg_prev ? ex2(l_last - l_prev) : 0.f;
-        if (ct == 0) tc::bulk_wait_read();   // the last out tile has left XW
-        named_bar_sync(1, kComputeThreads);
 
-        // ---- M = CB o decay into T_M, the live 32-column blocks 0..qr of
+        // ---- h_e (entering) -> bf16 rows of the [B^T | h] operand (thread r
+        // writes dstate column r of every headdim row); H_e <- carry H_e
+        tc::tmem_st_wait();   // the entering state's stores (first sub-step)
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+          uint32_t hv[16];
+          tc::tmem_ld16(T_Hr + qd * 16, hv);
+          tc::tmem_ld_wait_regs(hv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int pcol = qd * 16 + i;   // headdim p: row 128 + 64 e + p, swizzle phase p % 8
+            const __nv_bfloat16 hb = __float2bfloat16_rn(__uint_as_float(hv[i]));
+            *reinterpret_cast<__nv_bfloat16*>(hk + pcol * 128 + ((kchunk ^ (pcol & 7)) << 4)) = hb;
+            hv[i] = __float_as_uint(carry * __uint_as_float(hv[i]));
+          }
+          tc::tmem_st16(T_Hr + qd * 16, hv);
+        }
+        if (ct == 0) tc::bulk_wait_read();   // the last out tiles have left XW
+        tc::tmem_st_wait();
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        named_bar_sync(1, kComputeThreads);
+        if (ct == 0) tc::mbar_arrive(&s.h_ready);
+
+        // ---- M_e = CB o decay into T_M, the live 32-column blocks 0..qr of
         // this row (the blocks above the diagonal were zeroed once).  Below
         // the diagonal block the decay factors as exp2(l_r - l_e) *
         // [exp2(l_e - l_j) dt_j] with e the block's last column (both <= 1);
         // the diagonal block takes one exp2 per element.  The D skip rides on
         // the diagonal: M_rr += D, so that M x includes D x_r.  Masks are selects.
+        wait_or_flag(&s.full, ph, p.ctrl);   // x_e has landed
         wait_or_flag(&s.cb, ph, p.ctrl);
         tc::fence_after_sync();
+        const float* mcol = s.mcol[e];
+        const float* bcol = s.bcol[e];
 #pragma unroll 1
         for (int qc = 0; qc <= qr; ++qc) {
           const bool diag = qc == qr;
           const int c0 = qc * 32;
           uint32_t v[32];
-          tc::tmem_ld32(T_A + lane_addr + c0, v);
+          tc::tmem_ld32(T_CBr + c0, v);
           const float arow = diag ? 0.f : ex2(l_r - lv[c0 + 31]);
           float colv[32];
-          const float4* cp4 = reinterpret_cast<const float4*>((diag ? s.mcol : s.bcol) + c0);
+          const float4* cp4 = reinterpret_cast<const float4*>((diag ? mcol : bcol) + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
             const float4 f = cp4[v4];
@@ -534,13 +558,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           float m[32];
           if (diag) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float val = __uint_as_float(v[e]) * ex2(l_r - colv[e]);
-              m[e] = (c0 + e < r) ? val : (c0 + e == r ? val + Dh : 0.f);
+            for (int i = 0; i < 32; ++i) {
+              const float val = __uint_as_float(v[i]) * ex2(l_r - colv[i]);
+              m[i] = (c0 + i < r) ? val : (c0 + i == r ? val + Dh : 0.f);
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) m[e] = __uint_as_float(v[e]) * (colv[e] * arow);
+            for (int i = 0; i < 32; ++i) m[i] = __uint_as_float(v[i]) * (colv[i] * arow);
           }
           if (p.has_seg) {   // a reset between j and r zeroes the entry
             const int4* sp4 = reinterpret_cast<const int4*>(sgv + c0);
@@ -555,13 +579,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           uint32_t packed[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) packed[e] = tc::pack_bf16x2(m[2 * e], m[2 * e + 1]);
-          tc::tmem_st16(T_M + lane_addr + (c0 >> 1), packed);
+          for (int i = 0; i < 16; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
+          tc::tmem_st16(T_Mr + (c0 >> 1), packed);
         }
-        // w o x for the row
+        // w o x_e for the row
         {
-          const unsigned char* xr = s.X + r * 128;
-          unsigned char* wr = s.XW + r * 128;
+          const unsigned char* xr = s.X[e] + r * 128;
+          unsigned char* wr = s.XW[e] + r * 128;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
@@ -580,30 +604,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         named_bar_sync(1, kComputeThreads);
         if (ct == 0) tc::mbar_arrive(&s.m_ready);
 
-        // ---- h (entering) -> bf16 operand of Ye in X; H <- carry H in TMEM
-        wait_or_flag(&s.yi_done, ph, p.ctrl);   // Yi has read x
-        tc::fence_after_sync();
-        {   // 16 columns at a time (wider pieces raise the register peak)
-          unsigned char* hr = s.X + r * 128;
+        // this row's z (64 bf16, 128 contiguous bytes), for the epilogue
+        uint4 zv[8];
+        if (p.z != nullptr && valid) {
+          const uint4* zsrc = reinterpret_cast<const uint4*>(
+              p.z + ((((int64_t)cur.b * p.L + cur.t0 + sub * kSub + r) * p.H + h) * kP));
 #pragma unroll
-          for (int qd = 0; qd < 4; ++qd) {
-            uint32_t hv[16];
-            tc::tmem_ld16(T_H + lane_addr + qd * 16, hv);
-            tc::tmem_ld_wait_regs(hv);
+          for (int i = 0; i < 8; ++i) zv[i] = __ldg(zsrc + i);
+        } else {
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc)
-              *reinterpret_cast<uint4*>(hr + (((qd * 2 + cc) ^ (r & 7)) << 4)) = pack8(hv, 8 * cc);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) hv[e] = __float_as_uint(carry * __uint_as_float(hv[e]));
-            tc::tmem_st16(T_H + lane_addr + qd * 16, hv);
-          }
+          for (int i = 0; i < 8; ++i) zv[i] = make_uint4(0u, 0u, 0u, 0u);
         }
-        tc::tmem_st_wait();
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        named_bar_sync(1, kComputeThreads);
-        if (ct == 0) tc::mbar_arrive(&s.h_ready);
-
         wait_or_flag(&s.y_done, ph, p.ctrl);
         tc::fence_after_sync();
 
@@ -611,79 +622,74 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (sub == cur.nsub - 1) {
           const bool last_chunk = c == p.nc - 1;
           if (!last_chunk || p.final_states) {
-            uint32_t h0[32], h1[32];
-            tc::tmem_ld32(T_H + lane_addr, h0);
-            tc::tmem_ld32(T_H + lane_addr + 32, h1);
-            tc::tmem_ld_wait_regs(h0);
-            tc::tmem_ld_wait_regs(h1);
-            if (last_chunk) {
-              float* dst = p.final_states + ((int64_t)cur.b * p.H + cur.h) * kP * kN + r;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                dst[e * kN] = __uint_as_float(h0[e]);
-                dst[(32 + e) * kN] = __uint_as_float(h1[e]);
-              }
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(p.slots) +
-                           ((int64_t)pair * 2 + (c & 1)) * (kP / 4) * kN + r;
+            for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+              uint32_t hv[16];
+              tc::tmem_ld16(T_Hr + qd * 16, hv);
+              tc::tmem_ld_wait_regs(hv);
+              if (last_chunk) {
+                float* dst = p.final_states + bh * kP * kN + r;
 #pragma unroll
-              for (int v4 = 0; v4 < 8; ++v4) {
-                dst[v4 * kN] = make_uint4(h0[4 * v4], h0[4 * v4 + 1], h0[4 * v4 + 2], h0[4 * v4 + 3]);
-                dst[(8 + v4) * kN] =
-                    make_uint4(h1[4 * v4], h1[4 * v4 + 1], h1[4 * v4 + 2], h1[4 * v4 + 3]);
+                for (int i = 0; i < 16; ++i) dst[(qd * 16 + i) * kN] = __uint_as_float(hv[i]);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(p.slots) +
+                             ((bh * 2 + (c & 1)) * (kP / 4) + qd * 4) * kN + r;
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                  dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
               }
             }
             publish_pending = !last_chunk;   // flag raised after the epilogue
           }
         }
 
-        // ---- epilogue: out = (Yi + rho Ye) * silu(z), z read from (and out
-        // written back into) this row of XW, then one TMA store of the tile
-        if (p.has_z) wait_or_flag(&s.zfull, ph, p.ctrl);
-        unsigned char* zr = s.XW + r * 128;
+        // ---- epilogue: out_e = (Yi_e + rho Ye_e) * silu(z_e) into this row of
+        // XW_e (free once the MMAs are done), then TMA stores of both tiles
+        unsigned char* orow = s.XW[e] + r * 128;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t yi[32], ye[32];
-          tc::tmem_ld32(T_A + lane_addr + half * 32, yi);
-          tc::tmem_ld32(T_A + 64 + lane_addr + half * 32, ye);
+        for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+          uint32_t yi[16], ye[16];
+          tc::tmem_ld16(T_YIr + qd * 16, yi);
+          tc::tmem_ld16(T_YEr + qd * 16, ye);
           tc::tmem_ld_wait_regs(yi);
           tc::tmem_ld_wait_regs(ye);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int ch = half * 4 + cc;
-            uint4* zslot = reinterpret_cast<uint4*>(zr + ((ch ^ (r & 7)) << 4));
-            const uint4 zv = p.has_z ? *zslot : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+          for (int cc = 0; cc < 2; ++cc) {
+            const int ch = qd * 2 + cc;
+            const uint32_t zw[4] = {zv[ch].x, zv[ch].y, zv[ch].z, zv[ch].w};
             uint32_t o[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               float y2[2];
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
-                const int e = cc * 8 + u * 2 + hh;
-                float y = fmaf(rho_r, __uint_as_float(ye[e]), __uint_as_float(yi[e]));
-                if (p.has_z) y *= silu(hh ? bf_hi(zw[u]) : bf_lo(zw[u]));
+                const int i = cc * 8 + u * 2 + hh;
+                float y = fmaf(rho_r, __uint_as_float(ye[i]), __uint_as_float(yi[i]));
+                if (p.z) y *= silu(hh ? bf_hi(zw[u]) : bf_lo(zw[u]));
                 y2[hh] = y;
               }
               o[u] = tc::pack_bf16x2(y2[0], y2[1]);
             }
-            *zslot = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(orow + ((ch ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         named_bar_sync(1, kComputeThreads);
         if (ct == 0) {
-          if (publish_pending) {   // every thread's slot stores came before the barrier
-            __threadfence();
-            const int nv = c + 1;
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pair), "r"(nv)
-                         : "memory");
-          }
           tc::mbar_arrive(&s.tmem_free);   // Yi / Ye read out
           // rows past the sequence end are outside the tensor map and not written
-          tc::tma_store_4d(&map_out, s.XW, 0, cur.h, (int)(cur.t0 + sub * kSub), cur.b);
+          const int tok = (int)(cur.t0 + sub * kSub);
+          tc::tma_store_4d(&map_out, s.XW[0], 0, cur.h0, tok, cur.b);
+          tc::tma_store_4d(&map_out, s.XW[1], 0, cur.h0 + 1, tok, cur.b);
           tc::bulk_commit();
+          if (publish_pending) {
+            // every thread's slot stores came before the barrier above; the
+            // release store orders them before the flag at gpu scope
+            const int nv = c + 1;
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + cur.pair), "r"(nv)
+                         : "memory");
+          }
         }
         l_prev = l_last;
         sg_prev = sg_last;
@@ -694,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // drain: the compute warps have waited for every MMA; the storing thread
-  // waits for its last tile store; release TMEM
+  // waits for its last tile stores; release TMEM
   if (tid == kComputeWarp0 * 32) tc::bulk_wait_all();
   __syncwarp();
   tc::fence_before_sync();
@@ -761,7 +767,8 @@ int sm_count() {
 
 bool fused_eligible(const Dims& d, bool bf16) {
   return bf16 && d.headdim == fused::kP && d.dstate == fused::kN &&
-         (d.chunk == 128 || d.chunk == 256) && d.seqlen <= (int64_t)1 << 30;
+         (d.chunk == 128 || d.chunk == 256) && (d.nheads / d.ngroups) % fused::kNH == 0 &&
+         d.seqlen <= (int64_t)1 << 30;
 }
 
 size_t fused_ctrl_ints(const Dims& d) { return 64 + (size_t)d.batch * d.nheads; }
@@ -771,14 +778,12 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
                          const __nv_bfloat16* z, const float* init, float* final_states,
                          __nv_bfloat16* out, float* slots, int* ctrl, const Dims& d,
                          cudaStream_t st) {
-  CUtensorMap mx, mb, mc, mz, mo;
+  CUtensorMap mx, mb, mc, mo;
   if (!make_map(&mx, x, fused::kP, d.nheads, d.seqlen, d.batch) ||
       !make_map(&mb, Bm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
       !make_map(&mc, Cm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
       !make_map(&mo, out, fused::kP, d.nheads, d.seqlen, d.batch))
     return cudaErrorInvalidValue;
-  if (z && !make_map(&mz, z, fused::kP, d.nheads, d.seqlen, d.batch)) return cudaErrorInvalidValue;
-  if (!z) mz = mx;   // never used
   cudaError_t e = cudaMemsetAsync(ctrl, 0, fused_ctrl_ints(d) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   fused::Params p;
@@ -795,7 +800,7 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.seg = v.dt_raw ? nullptr : v.seg;
   p.has_seg = v.dt_raw ? v.seq_idx != nullptr : v.seg != nullptr;
   p.D = D;
-  p.has_z = z != nullptr;
+  p.z = z;
   p.init = init;
   p.final_states = final_states;
   p.slots = slots;
@@ -807,7 +812,7 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.G = d.ngroups;
   p.Q = d.chunk;
   p.nc = d.nchunks;
-  p.items = (long long)d.batch * d.nchunks * d.nheads;
+  p.items = (long long)d.batch * d.nchunks * (d.nheads / fused::kNH);
   const size_t smem = sizeof(fused::Smem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -816,8 +821,8 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long grid = std::min<long long>(p.items, 2LL * sm_count());
-  fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz, mo, p);
+  const long long grid = std::min<long long>(p.items, sm_count());   // one CTA per SM
+  fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mo, p);
   return cudaGetLastError();
 }
 

@@ -213,7 +213,8 @@ def ssd_chunk_fused(x: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dt_out: t
                     return_final_states: bool = False, out: Optional[torch.Tensor] = None,
                     final_states: Optional[torch.Tensor] = None, stream=None):
     """Stages 2-4 in one tensor-core kernel (bf16, headdim 64, dstate 128,
-    chunk 128/256).  Returns out, or (out, final_states)."""
+    chunk 128/256, an even number of heads per group).  Returns out, or
+    (out, final_states)."""
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     dev = x.device

@@ -1,7 +1,8 @@
 """GPU parity of the fused tensor-core path (bf16, headdim 64, dstate 128,
-chunk 128 / 256): ssd_scan_fwd routes these shapes to stage 1 + the fused
-tcgen05 kernel.  Compared with the fp64 oracle (max|err|/max|ref| <= 2e-2)
-and with the four SIMT stage kernels; the kernel's error word must stay 0."""
+chunk 128 / 256, an even number of heads per group): ssd_scan_fwd routes
+these shapes to the fused tcgen05 kernel, which also runs stage 1.
+Compared with the fp64 oracle (max|err|/max|ref| <= 2e-2) and with the four
+SIMT stage kernels; the kernel's error word must stay 0."""
 import math
 
 import numpy as np
@@ -127,3 +128,25 @@ def test_fused_rejects_other_shapes():
     ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     with pytest.raises(SSDError, match="headdim 64"):
         ssd.ssd_chunk_fused(d["x"], d["B"], d["C"], dt_out, cs, seg, chunk_size=128, workspace=ws)
+
+
+def test_fused_rejects_odd_heads_per_group():
+    """The kernel pairs the heads of a group; an odd count is refused."""
+    import selective_state_space_05_gb300 as ssd
+    from selective_state_space_05_gb300._lib import SSDError
+    d = to_dev(si.random_small(45, nheads=3, ngroups=1, headdim=64, dstate=128, dtype="bf16",
+                               seqlen=200, chunk_size=128))
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(d["dt"], d["A"], chunk_size=128)
+    ws = torch.empty(ssd.workspace_bytes(2, 200, 3, 64, 128, 1, 128), dtype=torch.uint8,
+                     device="cuda")
+    with pytest.raises(SSDError, match="even number of heads"):
+        ssd.ssd_chunk_fused(d["x"], d["B"], d["C"], dt_out, cs, seg, chunk_size=128, workspace=ws)
+
+
+def test_scan_fwd_odd_heads_per_group_takes_stage_kernels():
+    """ssd_scan_fwd still serves such shapes, through the four stage kernels."""
+    d = _small(46, seqlen=300, chunk_size=256, nheads=3, ngroups=1, init_std=0.3)
+    y, f = _run_fused(d, 256, check_error_word=False)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["bf16"], "out")
+    assert_close(f, rf, TOL["bf16"], "final")
