@@ -79,7 +79,12 @@ const char *ssd_last_error(void);
  * even number of heads per group (nheads / ngroups), ssd_scan_fwd runs all
  * four stages in the fused tensor-core kernel of ssd_chunk_fused (which then
  * computes stage 1 itself and leaves the dt / cumsum / segment regions of
- * the workspace unused); otherwise the four stage kernels below. */
+ * the workspace unused); otherwise the four stage kernels below.  The fused
+ * kernel keeps each head pair's state on chip for a segment of consecutive
+ * chunks and hands it on between segments; the segment length is chosen from
+ * the shape (1 or 2 chunks) unless the environment variable
+ * SSD_FUSED_SEGMENT_CHUNKS gives one (a tuning / test override; results
+ * agree to rounding for every length). */
 size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
                                 int headdim, int dstate, int ngroups,
                                 int chunk_size, ssd_dtype_t dtype);

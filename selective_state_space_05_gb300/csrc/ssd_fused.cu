@@ -71,14 +71,17 @@ struct alignas(1024) Smem {
   unsigned char BH[2 * kBhHalf];       // see kBhHalf
   unsigned char X[kNH][kSub * kP * 2]; // x_e (MN-major B operand of Yi_e)
   unsigned char XW[kNH][kSub * kP * 2];   // w o x_e (state B operand); then out_e
+  unsigned char Z[kNH][kSub * kP * 2];    // z_e
   float lv[kRing][kNH][kQmax];   // l = log2(e) * cumsum of dt*A over the chunk
   float dtv[kRing][kNH][kQmax];  // dt
   int segv[kRing][kQmax];        // reset counts (with seq_idx)
   float mcol[kNH][kSub];   // l_j - log2(dt_j): column term of the diagonal blocks
   float bcol[kNH][kSub];   // exp2(l_e - l_j) dt_j, e = last column of j's 32-block
-  long long tk[kRing];     // published tickets (>= items: no more work)
+  long long tk[kRing];     // published units: ticket (>= items: no more work) ...
+  int tj[kRing];           // ... and chunk of its segment
   uint64_t tk_full[kRing], tk_empty[kRing];
-  uint64_t full, h_ready, cb, m_ready, y_done, tmem_free;
+  uint64_t full, zfull, h_ready, cb, m_ready, y_done, tmem_free;
+  uint64_t pub;            // the segment's final states are in their slots
   uint32_t tmem_base;
   long long first_ticket;
 };
@@ -108,27 +111,35 @@ struct Params {
   int* ctrl;             // [0] ticket counter, [1] error word
   int64_t L;
   int B, H, G, Q, nc;
-  long long items;
+  int seg_chunks;        // chunks per work item (the state stays in TMEM across them)
+  long long items;       // B * H/2 * ceil(nc / seg_chunks)
 };
 
-struct Item {
+// One chunk of a work item: ticket t = (segment, head pair), chunk j of the
+// segment.
+struct Unit {
   int b, c, h0, g, pair, nvalid, nsub;   // pair = b * H/2 + h0/2
+  int j, nch;                            // chunk of the segment, chunks in it
   int64_t t0;
 };
 
-__device__ __forceinline__ Item decode(const Params& p, long long t) {
-  Item it;
+__device__ __forceinline__ Unit decode(const Params& p, long long t, int j) {
+  Unit u;
   const int hp = p.H / kNH;
   const int pairs = p.B * hp;
-  it.c = (int)(t / pairs);
-  it.pair = (int)(t % pairs);
-  it.b = it.pair / hp;
-  it.h0 = (it.pair % hp) * kNH;
-  it.g = it.h0 / (p.H / p.G);
-  it.t0 = (int64_t)it.c * p.Q;
-  it.nvalid = (int)min((int64_t)p.Q, p.L - it.t0);
-  it.nsub = (it.nvalid + kSub - 1) / kSub;
-  return it;
+  const int sgm = (int)(t / pairs);
+  u.pair = (int)(t % pairs);
+  u.b = u.pair / hp;
+  u.h0 = (u.pair % hp) * kNH;
+  u.g = u.h0 / (p.H / p.G);
+  const int c0 = sgm * p.seg_chunks;
+  u.nch = min(p.seg_chunks, p.nc - c0);
+  u.j = j;
+  u.c = c0 + j;
+  u.t0 = (int64_t)u.c * p.Q;
+  u.nvalid = (int)min((int64_t)p.Q, p.L - u.t0);
+  u.nsub = (u.nvalid + kSub - 1) / kSub;
+  return u;
 }
 
 // Named barrier over a subset of warps; the non-aligned form tolerates
@@ -174,68 +185,105 @@ __device__ __forceinline__ T warp_incl_scan(T v, int lane) {
   return v;
 }
 
-// The per-token vectors of head h of one item, written by the 32 lanes of a
-// warp: lane i owns positions [i E, i E + E) of the chunk, E = Q / 32.
-// Positions past the sequence end get dt = 0, so that l and the reset count
-// keep their last values there.  segv == null: no reset counts wanted.
-__device__ __forceinline__ void item_vectors(const Params& p, const Item& it, int h, float* lv,
-                                             float* dtv, int* segv, int lane) {
+// The raw inputs of a unit's per-token vectors as lane `lane` of the warp
+// computing them holds them: positions [lane E, lane E + E) of the chunk,
+// E = Q / 32 (both heads' dt, the seq_idx values around them).  Loaded one
+// unit ahead so that the loads are in flight while the warp waits.
+struct VecRaw {
+  float2 dt[8];
+  int sq[9];   // seq_idx at positions lane E - 1 .. lane E + 7 (-1: none)
+  float a[kNH], bias[kNH];   // A log2(e) and dt_bias of the two heads
+};
+
+__device__ __forceinline__ void vec_load(const Params& p, const Unit& it, int lane, VecRaw& r) {
+  const int E = p.Q / 32;
+  if (p.dt_raw) {
+#pragma unroll
+    for (int e = 0; e < kNH; ++e) {
+      r.a[e] = p.A[it.h0 + e] * kLog2e;
+      r.bias[e] = p.dt_bias ? p.dt_bias[it.h0 + e] : 0.f;
+    }
+    // the pair's two dt values of a token are adjacent
+    const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(
+        p.dt_raw + ((int64_t)it.b * p.L + it.t0) * p.H + it.h0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int tok = lane * E + i;
+      r.dt[i] = (i < E && tok < it.nvalid) ? __bfloat1622float2(src[(int64_t)tok * (p.H / 2)])
+                                           : make_float2(0.f, 0.f);
+    }
+    if (p.seq_idx) {
+      const int32_t* sq = p.seq_idx + (int64_t)it.b * p.L;
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        const int tok = lane * E + i - 1;
+        const int64_t gt = it.t0 + tok;
+        r.sq[i] = (i <= E && tok < it.nvalid && gt >= 0) ? sq[gt] : -1;
+      }
+    }
+  }
+}
+
+// The per-token vectors of both heads of one unit, written by the 32 lanes
+// of a warp from what vec_load fetched.  Positions past the sequence end get
+// dt = 0, so that l and the reset count keep their last values there.
+__device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, const VecRaw& r,
+                                            float (*lv)[kQmax], float (*dtv)[kQmax], int* segv,
+                                            int lane) {
   const int Q = p.Q, E = Q / 32;
   if (p.dt_raw) {
-    const float a = p.A[h] * kLog2e;
-    const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
-    const __nv_bfloat16* src = p.dt_raw + ((int64_t)it.b * p.L + it.t0) * p.H + h;
-    float v[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int tok = lane * E + e;
-      v[e] = (e < E && tok < it.nvalid) ? __bfloat162float(src[(int64_t)tok * p.H]) : 0.f;
-    }
-    float run = 0.f, loc[8];
+    for (int e = 0; e < kNH; ++e) {
+      const float a = r.a[e], bias = r.bias[e];
+      float run = 0.f, loc[8], dv[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float d = 0.f;
-      if (e < E && lane * E + e < it.nvalid) {
-        d = v[e] + bias;
-        if (p.softplus) d = d <= 20.f ? log1pf(__expf(d)) : d;
-        if (p.do_clamp) d = fminf(fmaxf(d, p.lo), p.hi);
+      for (int i = 0; i < 8; ++i) {
+        float d = 0.f;
+        if (i < E && lane * E + i < it.nvalid) {
+          d = (e == 0 ? r.dt[i].x : r.dt[i].y) + bias;
+          // softplus on the SFU: log(1 + exp(d)); below -15 it equals exp(d)
+          // to fp32 precision, above 20 it equals d
+          if (p.softplus) d = d > 20.f ? d : (d < -15.f ? __expf(d) : __logf(1.f + __expf(d)));
+          if (p.do_clamp) d = fminf(fmaxf(d, p.lo), p.hi);
+        }
+        dv[i] = d;
+        run += d * a;
+        loc[i] = run;
       }
-      v[e] = d;
-      run += d * a;
-      loc[e] = run;
-    }
-    const float excl = warp_incl_scan(run, lane) - run;
+      const float excl = warp_incl_scan(run, lane) - run;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if (e < E) {
-        dtv[lane * E + e] = v[e];
-        lv[lane * E + e] = excl + loc[e];
+      for (int i = 0; i < 8; ++i) {
+        if (i < E) {
+          dtv[e][lane * E + i] = dv[i];
+          lv[e][lane * E + i] = excl + loc[i];
+        }
       }
     }
-    if (p.seq_idx && segv) {
-      const int32_t* sq = p.seq_idx + (int64_t)it.b * p.L;
+    if (p.seq_idx) {   // a reset before token t: seq_idx[t] != seq_idx[t-1] (t >= 1)
       int cnt = 0, lc[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int tok = lane * E + e;
-        const int64_t gt = it.t0 + tok;
+      for (int i = 0; i < 8; ++i) {
+        const int tok = lane * E + i;
         int f = 0;
-        if (e < E && tok < it.nvalid && gt >= 1) f = sq[gt] != sq[gt - 1];
+        if (i < E && tok < it.nvalid && it.t0 + tok >= 1) f = r.sq[i + 1] != r.sq[i];
         cnt += f;
-        lc[e] = cnt;
+        lc[i] = cnt;
       }
       const int cex = warp_incl_scan(cnt, lane) - cnt;
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (e < E) segv[lane * E + e] = cex + lc[e];
+      for (int i = 0; i < 8; ++i)
+        if (i < E) segv[lane * E + i] = cex + lc[i];
     }
   } else {
-    const int64_t pq = ((int64_t)it.b * p.H + h) * p.nc + it.c;
-    for (int i = lane; i < Q; i += 32) {
-      lv[i] = p.cs[pq * Q + i] * kLog2e;
-      dtv[i] = p.dt[pq * Q + i];
+#pragma unroll
+    for (int e = 0; e < kNH; ++e) {
+      const int64_t pq = ((int64_t)it.b * p.H + it.h0 + e) * p.nc + it.c;
+      for (int i = lane; i < Q; i += 32) {
+        lv[e][i] = p.cs[pq * Q + i] * kLog2e;
+        dtv[e][i] = p.dt[pq * Q + i];
+      }
     }
-    if (p.seg && segv)
+    if (p.seg)
       for (int i = lane; i < Q; i += 32) segv[i] = p.seg[((int64_t)it.b * p.nc + it.c) * Q + i];
   }
 }
@@ -269,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap map_x,
                      const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_c,
+                     const __grid_constant__ CUtensorMap map_z,
                      const __grid_constant__ CUtensorMap map_out, Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned start (128-byte swizzle atoms), derived from the shared
@@ -283,11 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     tc::mbar_init(&s.full, 1);
+    tc::mbar_init(&s.zfull, 1);
     tc::mbar_init(&s.h_ready, 1);
     tc::mbar_init(&s.cb, 1);
     tc::mbar_init(&s.m_ready, 1);
     tc::mbar_init(&s.y_done, 1);
     tc::mbar_init(&s.tmem_free, 1);
+    tc::mbar_init(&s.pub, kComputeThreads);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(&s.tk_full[i], 32);                          // the 32 lanes of warp 0
       tc::mbar_init(&s.tk_empty[i], 1 + kComputeThreads / 32);   // MMA lane + compute warps
@@ -297,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tma_prefetch_desc(&map_b);
     tc::tma_prefetch_desc(&map_c);
     tc::tma_prefetch_desc(&map_out);
+    if (p.z) tc::tma_prefetch_desc(&map_z);
     s.first_ticket = atomicAdd(p.ctrl, 1);
   }
   tc::fence_before_sync();
@@ -305,24 +357,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.tmem_base;
 
   if (warp == 0) {
-    // ---------------- tickets, per-token vectors (one item ahead) and the
-    // TMA loads: a sub-step's C, B, x_0, x_1 tiles as soon as the previous
-    // sub-step's MMAs are done with them
+    // ---------------- tickets, per-token vectors (one unit ahead: loaded at
+    // the start of a unit, computed and published once its first tiles are
+    // requested) and the TMA loads: a sub-step's C, B, x_0, x_1 tiles as soon
+    // as the previous sub-step's MMAs are done with them, its z tiles once
+    // the previous epilogue has read Z; after a segment that hands on, the
+    // flag release
     long long t_cur = s.first_ticket;
+    int j_cur = 0;
     if (t_cur < p.items) {
-      const Item it0 = decode(p, t_cur);
-      for (int e = 0; e < kNH; ++e)
-        item_vectors(p, it0, it0.h0 + e, s.lv[0][e], s.dtv[0][e], e == 0 ? s.segv[0] : nullptr,
-                     lane);
+      const Unit u0 = decode(p, t_cur, 0);
+      VecRaw r0;
+      vec_load(p, u0, lane, r0);
+      vec_compute(p, u0, r0, s.lv[0], s.dtv[0], s.segv[0], lane);
     }
-    if (lane == 0) s.tk[0] = t_cur;
+    if (lane == 0) {
+      s.tk[0] = t_cur;
+      s.tj[0] = 0;
+    }
     tc::mbar_arrive(&s.tk_full[0]);
-    long long t_pend = p.items;   // lane 0: the ticket after the published ones
+    long long t_pend = p.items;   // lane 0: the ticket of the item after the published ones
     if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ctrl, 1);
-    uint32_t k = 0;
-    for (int it = 0; t_cur < p.items && !aborted(p.ctrl); ++it) {
-      const Item cur = decode(p, t_cur);
-      long long t_nxt = p.items;
+    uint32_t k = 0, npub = 0;
+    bool pub_pending = false;     // a segment's flag still to raise ...
+    int pub_pair = 0, pub_val = 0;   // ... for this pair, with this value
+    for (int u = 0; t_cur < p.items && !aborted(p.ctrl); ++u) {
+      const Unit cur = decode(p, t_cur, j_cur);
+      long long t_nxt = t_cur;
+      int j_nxt = j_cur + 1;
+      if (j_nxt == cur.nch) {   // the next unit starts the next item
+        t_nxt = __shfl_sync(0xffffffffu, t_pend, 0);
+        j_nxt = 0;
+      }
+      VecRaw raw;   // the next unit's raw per-token inputs, in flight meanwhile
+      if (t_nxt < p.items) vec_load(p, decode(p, t_nxt, j_nxt), lane, raw);
       for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
         const int tok = (int)(cur.t0 + sub * kSub);
         if (lane == 0) {
@@ -334,25 +402,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_load_4d(s.BH + kBhHalf, &map_b, &s.full, 64, cur.g, tok, cur.b);
           tc::tma_load_4d(s.X[0], &map_x, &s.full, 0, cur.h0, tok, cur.b);
           tc::tma_load_4d(s.X[1], &map_x, &s.full, 0, cur.h0 + 1, tok, cur.b);
-        }
-        if (sub == 0) {   // publish the next item into the other ring slot
-          t_nxt = __shfl_sync(0xffffffffu, t_pend, 0);
-          const int j = it + 1, slot = j % kRing;
-          wait_or_flag(&s.tk_empty[slot], ((j / kRing) & 1) ^ 1, p.ctrl);
-          if (t_nxt < p.items) {
-            const Item nx = decode(p, t_nxt);
-            for (int e = 0; e < kNH; ++e)
-              item_vectors(p, nx, nx.h0 + e, s.lv[slot][e], s.dtv[slot][e],
-                           e == 0 ? s.segv[slot] : nullptr, lane);
+          if (pub_pending) {
+            // the previous segment's final states are in their slots once
+            // every compute thread has arrived on pub; the release store
+            // orders them before the flag at gpu scope (its consumer waits
+            // for flag >= its first chunk).  Done here, after this unit's
+            // first loads are on their way.
+            wait_or_flag(&s.pub, npub & 1, p.ctrl);
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pub_pair),
+                         "r"(pub_val)
+                         : "memory");
+            ++npub;
+            pub_pending = false;
           }
+          if (p.z) {
+            wait_or_flag(&s.tmem_free, (k & 1) ^ 1, p.ctrl);
+            tc::mbar_arrive_expect_tx(&s.zfull, kNH * kSub * kP * 2);
+            tc::tma_load_4d(s.Z[0], &map_z, &s.zfull, 0, cur.h0, tok, cur.b);
+            tc::tma_load_4d(s.Z[1], &map_z, &s.zfull, 0, cur.h0 + 1, tok, cur.b);
+          }
+        }
+        if (sub == 0) {   // publish the next unit into the other ring slot
+          const int nu = u + 1, slot = nu % kRing;
+          wait_or_flag(&s.tk_empty[slot], ((nu / kRing) & 1) ^ 1, p.ctrl);
+          if (t_nxt < p.items)
+            vec_compute(p, decode(p, t_nxt, j_nxt), raw, s.lv[slot], s.dtv[slot], s.segv[slot], lane);
           if (lane == 0) {
             s.tk[slot] = t_nxt;
-            if (t_nxt < p.items) t_pend = atomicAdd(p.ctrl, 1);
+            s.tj[slot] = j_nxt;
+            if (j_nxt == 0 && t_nxt < p.items) t_pend = atomicAdd(p.ctrl, 1);
           }
           tc::mbar_arrive(&s.tk_full[slot]);
         }
       }
+      if (cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
+        pub_pending = true;
+        pub_pair = cur.pair;
+        pub_val = cur.c + 1;
+      }
       t_cur = t_nxt;
+      j_cur = j_nxt;
+    }
+    if (lane == 0 && pub_pending) {
+      wait_or_flag(&s.pub, npub & 1, p.ctrl);
+      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pub_pair), "r"(pub_val)
+                   : "memory");
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -369,13 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_y = tc::idesc_bf16(kSub, kP, false, true);
       constexpr uint32_t id_s = tc::idesc_bf16(kN, kNH * kP, true, true);
       uint32_t k = 0;
-      for (int it = 0;; ++it) {
-        const int slot = it % kRing;
-        wait_or_flag(&s.tk_full[slot], (it / kRing) & 1, p.ctrl);
+      for (int u = 0;; ++u) {
+        const int slot = u % kRing;
+        wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
         const long long t = s.tk[slot];
+        const int j = s.tj[slot];
         tc::mbar_arrive(&s.tk_empty[slot]);
         if (t >= p.items || aborted(p.ctrl)) break;
-        const int nsub = decode(p, t).nsub;
+        const int nsub = decode(p, t, j).nsub;
         for (int sub = 0; sub < nsub; ++sub, ++k) {
           const uint32_t ph = k & 1;
           wait_or_flag(&s.tmem_free, ph ^ 1, p.ctrl);
@@ -431,21 +526,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* hk = s.BH + (r >> 6) * kBhHalf + (128 + e * kP) * 128 + (r & 7) * 2;
     const int kchunk = (r & 63) >> 3;
     uint32_t k = 0;
-    for (int it = 0;; ++it) {
-      const int slot = it % kRing;
-      wait_or_flag(&s.tk_full[slot], (it / kRing) & 1, p.ctrl);
+    for (int u = 0;; ++u) {
+      const int slot = u % kRing;
+      wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
       const long long t = s.tk[slot];
+      const int j = s.tj[slot];
       if (t >= p.items || aborted(p.ctrl)) break;
-      const Item cur = decode(p, t);
+      const Unit cur = decode(p, t, j);
       const int c = cur.c, h = cur.h0 + e;
       const int64_t bh = (int64_t)cur.b * p.H + h;   // this head's state slots
       const float Dh = p.D ? p.D[h] : 0.f;
-      float l_prev = 0.f;
+      float l_prev = 0.f;   // the cumsum restarts with every chunk
       int sg_prev = 0;
 
-      // the state entering the chunk, this row: loaded, then written to T_H
-      // (the predecessor item raised its flag after both heads' slots)
-      {
+      // first chunk of a segment: the state entering it, this row, loaded and
+      // written to T_H (the predecessor segment raised its flag after both
+      // heads' slots); later chunks continue from the state in T_H
+      if (j == 0) {
         uint32_t hin0[32], hin1[32];   // headdim columns 0-31 and 32-63
         if (c == 0) {
           if (p.init) {
@@ -482,7 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st32(T_Hr, hin0);
         tc::tmem_st32(T_Hr + 32, hin1);
       }
-      bool publish_pending = false;
 
       for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
         const uint32_t ph = k & 1;
@@ -604,22 +700,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, kComputeThreads);
         if (ct == 0) tc::mbar_arrive(&s.m_ready);
 
-        // this row's z (64 bf16, 128 contiguous bytes), for the epilogue
-        uint4 zv[8];
-        if (p.z != nullptr && valid) {
-          const uint4* zsrc = reinterpret_cast<const uint4*>(
-              p.z + ((((int64_t)cur.b * p.L + cur.t0 + sub * kSub + r) * p.H + h) * kP));
-#pragma unroll
-          for (int i = 0; i < 8; ++i) zv[i] = __ldg(zsrc + i);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) zv[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
         wait_or_flag(&s.y_done, ph, p.ctrl);
         tc::fence_after_sync();
 
-        // ---- hand the chunk's final state on
-        if (sub == cur.nsub - 1) {
+        // ---- hand the segment's final state on (or write the final states)
+        if (sub == cur.nsub - 1 && j == cur.nch - 1) {
           const bool last_chunk = c == p.nc - 1;
           if (!last_chunk || p.final_states) {
 #pragma unroll
@@ -639,13 +724,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                   dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
               }
             }
-            publish_pending = !last_chunk;   // flag raised after the epilogue
           }
+          if (!last_chunk) tc::mbar_arrive(&s.pub);   // warp 0 raises the flag
         }
 
-        // ---- epilogue: out_e = (Yi_e + rho Ye_e) * silu(z_e) into this row of
-        // XW_e (free once the MMAs are done), then TMA stores of both tiles
+        // ---- epilogue: out_e = (Yi_e + rho Ye_e) * silu(z_e), z_e from Z, into
+        // this row of XW_e (free once the MMAs are done), then TMA stores of
+        // both tiles
         unsigned char* orow = s.XW[e] + r * 128;
+        const unsigned char* zrow = s.Z[e] + r * 128;
+        if (p.z) wait_or_flag(&s.zfull, ph, p.ctrl);
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
           uint32_t yi[16], ye[16];
@@ -656,7 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int ch = qd * 2 + cc;
-            const uint32_t zw[4] = {zv[ch].x, zv[ch].y, zv[ch].z, zv[ch].w};
+            const uint4 zv = p.z ? *reinterpret_cast<const uint4*>(zrow + ((ch ^ (r & 7)) << 4))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
             uint32_t o[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -683,19 +773,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_store_4d(&map_out, s.XW[0], 0, cur.h0, tok, cur.b);
           tc::tma_store_4d(&map_out, s.XW[1], 0, cur.h0 + 1, tok, cur.b);
           tc::bulk_commit();
-          if (publish_pending) {
-            // every thread's slot stores came before the barrier above; the
-            // release store orders them before the flag at gpu scope
-            const int nv = c + 1;
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + cur.pair), "r"(nv)
-                         : "memory");
-          }
         }
         l_prev = l_last;
         sg_prev = sg_last;
       }
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&s.tk_empty[slot]);   // this item's vectors are read
+      if (lane == 0) tc::mbar_arrive(&s.tk_empty[slot]);   // this unit's vectors are read
     }
   }
 
@@ -715,6 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+#include <stdlib.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -778,12 +863,14 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
                          const __nv_bfloat16* z, const float* init, float* final_states,
                          __nv_bfloat16* out, float* slots, int* ctrl, const Dims& d,
                          cudaStream_t st) {
-  CUtensorMap mx, mb, mc, mo;
+  CUtensorMap mx, mb, mc, mz, mo;
   if (!make_map(&mx, x, fused::kP, d.nheads, d.seqlen, d.batch) ||
       !make_map(&mb, Bm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
       !make_map(&mc, Cm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
       !make_map(&mo, out, fused::kP, d.nheads, d.seqlen, d.batch))
     return cudaErrorInvalidValue;
+  if (z && !make_map(&mz, z, fused::kP, d.nheads, d.seqlen, d.batch)) return cudaErrorInvalidValue;
+  if (!z) mz = mx;   // never used
   cudaError_t e = cudaMemsetAsync(ctrl, 0, fused_ctrl_ints(d) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   fused::Params p;
@@ -812,7 +899,21 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.G = d.ngroups;
   p.Q = d.chunk;
   p.nc = d.nchunks;
-  p.items = (long long)d.batch * d.nchunks * (d.nheads / fused::kNH);
+  // chunks per work item: the state stays in TMEM across a segment and is
+  // handed on only between segments; segments stay short enough that every
+  // SM gets several items (dynamic scheduling evens out the tail).  Two
+  // chunks measured best on the 2.7B shape (1: 0.474 ms, 2: 0.456, 4: 0.466)
+  const long long pairs = (long long)d.batch * (d.nheads / fused::kNH);
+  int seg = 1;
+  while (seg < 2 && seg * 2 <= d.nchunks &&
+         pairs * ((d.nchunks + seg * 2 - 1) / (seg * 2)) >= 8LL * sm_count())
+    seg *= 2;
+  if (const char* ov = getenv("SSD_FUSED_SEGMENT_CHUNKS")) {   // tuning / test override
+    const int v = atoi(ov);
+    if (v >= 1 && v <= d.nchunks) seg = v;
+  }
+  p.seg_chunks = seg;
+  p.items = pairs * ((d.nchunks + seg - 1) / seg);
   const size_t smem = sizeof(fused::Smem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -822,7 +923,7 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
     attr_set = true;
   }
   const long long grid = std::min<long long>(p.items, sm_count());   // one CTA per SM
-  fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mo, p);
+  fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz, mo, p);
   return cudaGetLastError();
 }
 

@@ -150,3 +150,17 @@ def test_scan_fwd_odd_heads_per_group_takes_stage_kernels():
     ry, rf = oracle.scan_sequential(d)
     assert_close(y, ry, TOL["bf16"], "out")
     assert_close(f, rf, TOL["bf16"], "final")
+
+
+@pytest.mark.parametrize("seg", [1, 2, 3, 4])
+def test_fused_segments(seg, monkeypatch):
+    """The state stays on chip across a segment of chunks and is handed on
+    between segments; every segment length (ragged last segment included)
+    gives the same result."""
+    monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", str(seg))
+    d = _small(47, batch=2, seqlen=1800, nheads=4, ngroups=2, chunk_size=128, init_std=0.3,
+               seq_idx_lengths=[700, 1100])
+    y, f = _run_fused(d, 128)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["bf16"], f"out (segments of {seg})")
+    assert_close(f, rf, TOL["bf16"], f"final (segments of {seg})")
