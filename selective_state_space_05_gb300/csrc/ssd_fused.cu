@@ -3,17 +3,22 @@
 // preprocessing and the per-chunk cumsum of dt*A, chunk states, inter-chunk
 // state passing and chunk outputs in one persistent kernel, one CTA per SM.
 //
-// Work item = (batch b, chunk c, head pair h0 = 2 hp, h1 = h0 + 1), both
-// heads of one B/C group, taken from an atomic ticket counter in chunk-major
-// order, so an item's predecessor (b, c-1, hp) always holds an earlier
-// ticket.  Warp roles:
-//   warp 0    takes the tickets and, one item ahead, computes the item's
+// Work item = a segment of consecutive chunks (the launcher picks 1 or 2)
+// of one head pair (h0 = 2 hp, h1 = h0 + 1, both in one B/C group) of one
+// batch row, taken from an atomic ticket counter in segment-major order, so
+// an item's predecessor (previous segment, same pair) always holds an
+// earlier ticket; the state stays in TMEM across the segment's chunks.
+// Warp roles:
+//   warp 10   takes the tickets and, one chunk ("unit") ahead, computes the
 //             per-token vectors (dt = softplus(dt_raw + dt_bias) clamped, the
-//             cumsum of dt*A per head, the reset counts of seq_idx) into a
-//             two-slot ring; lane 0 issues the TMA tile loads
+//             cumsum of dt*A per head, the decay-matrix column factors, the
+//             reset counts of seq_idx) into a two-slot ring
+//   warp 0    lane 0 issues the TMA loads (C, B, x, z) and out stores and
+//             raises the hand-off flag after a segment
 //   warp 1    lane 0 issues the tcgen05 MMAs
 //   warps 2-9 four per head (one per TMEM lane quarter): decay matrix,
-//             state moves, epilogue
+//             state moves, epilogue; they never wait for one another (every
+//             thread arrives on the mbarriers its consumers wait on)
 // A chunk is processed as 128-token sub-steps; per sub-step, with rows /
 // columns = the sub-step's tokens, cs the chunk's cumsum and h_e the state
 // entering the sub-step (head e = 0, 1):
@@ -25,12 +30,14 @@
 //          w_j = exp(cs_last - cs_j) dt_j  (the sub-step's own chunk state)
 //   out_e = (Yi_e + exp(cs_i - cs_prev) Ye_e + D x_e) * silu(z_e)
 // Sharing the A operand across the pair halves the MMA instructions per head
-// (an M=128 tcgen05.mma costs about the same for N = 64 .. 256).  The fp32
-// states stay in TMEM (one row of dstate per TMEM lane, headdim columns) for
-// the whole chunk.  The states entering a chunk are handed from the item
-// (b, c-1, hp) through L2-resident fp32 slots and a flag (decoupled
-// look-back); every wait is bounded and gives up with an error word instead
-// of hanging.
+// (an M=128 tcgen05.mma costs about the same for N = 64 .. 256).  Yi_0 and
+// Yi_1 are committed separately so that each head's epilogue starts as soon
+// as its own product is ready, and the next sub-step's entering state is
+// converted right after the MMAs, before the epilogue ends.  The fp32 states
+// stay in TMEM (one row of dstate per TMEM lane, headdim columns) for the
+// whole segment and are handed to the next segment through L2-resident fp32
+// slots and a flag (decoupled look-back); every wait is bounded and gives up
+// with an error word instead of hanging.
 #include <cudaTypedefs.h>
 
 #include "../../include/ssd_scan.h"
@@ -46,9 +53,10 @@ constexpr int kN = 128;     // dstate
 constexpr int kQmax = 256;  // largest chunk
 constexpr int kRing = 2;    // items whose tickets / vectors are published
 constexpr int kNH = 2;      // heads per item
-constexpr int kComputeWarp0 = 2;        // warps 0 (TMA) and 1 (MMA) come first
+constexpr int kComputeWarp0 = 2;        // warps 0 (TMA) and 1 (MMA) come first, then compute
 constexpr int kComputeThreads = 128 * kNH;   // one warp per head and TMEM lane quarter
-constexpr int kThreads = kComputeWarp0 * 32 + kComputeThreads;
+constexpr int kVecWarp = kComputeWarp0 + kComputeThreads / 32;   // tickets and vectors
+constexpr int kThreads = (kVecWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // any single wait: 2 s at most
 constexpr uint32_t kSleepHintNs = 20000;                 // suspend hint of one try_wait
@@ -70,20 +78,19 @@ struct alignas(1024) Smem {
   unsigned char C[kSub * kN * 2];      // two 64-column halves, 128B swizzle
   unsigned char BH[2 * kBhHalf];       // see kBhHalf
   unsigned char X[kNH][kSub * kP * 2]; // x_e (MN-major B operand of Yi_e)
-  unsigned char XW[kNH][kSub * kP * 2];   // w o x_e (state B operand); then out_e
-  unsigned char Z[kNH][kSub * kP * 2];    // z_e
+  unsigned char XW[kNH][kSub * kP * 2];   // w o x_e (B operand of the state chain)
+  unsigned char Z[kNH][kSub * kP * 2];    // z_e; the epilogue writes out_e over it
   float lv[kRing][kNH][kQmax];   // l = log2(e) * cumsum of dt*A over the chunk
   float dtv[kRing][kNH][kQmax];  // dt
+  float mv[kRing][kNH][kQmax];   // l_j - log2(dt_j): column term of the diagonal blocks
+  float bv[kRing][kNH][kQmax];   // exp2(l_f - l_j) dt_j, f = last position of j's 32-block
   int segv[kRing][kQmax];        // reset counts (with seq_idx)
-  float mcol[kNH][kSub];   // l_j - log2(dt_j): column term of the diagonal blocks
-  float bcol[kNH][kSub];   // exp2(l_e - l_j) dt_j, e = last column of j's 32-block
   long long tk[kRing];     // published units: ticket (>= items: no more work) ...
   int tj[kRing];           // ... and chunk of its segment
   uint64_t tk_full[kRing], tk_empty[kRing];
-  uint64_t full, zfull, h_ready, cb, m_ready, y_done, tmem_free;
+  uint64_t full, zfull, h_ready, cb, m_ready, yi_done[kNH], y_done, tmem_free;
   uint64_t pub;            // the segment's final states are in their slots
   uint32_t tmem_base;
-  long long first_ticket;
 };
 
 // one CTA per SM: the tiles and the alignment slack within the 227 KB a block may use
@@ -140,12 +147,6 @@ __device__ __forceinline__ Unit decode(const Params& p, long long t, int j) {
   u.nvalid = (int)min((int64_t)p.Q, p.L - u.t0);
   u.nsub = (u.nvalid + kSub - 1) / kSub;
   return u;
-}
-
-// Named barrier over a subset of warps; the non-aligned form tolerates
-// threads of a warp arriving separately.
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -228,7 +229,8 @@ __device__ __forceinline__ void vec_load(const Params& p, const Unit& it, int la
 // of a warp from what vec_load fetched.  Positions past the sequence end get
 // dt = 0, so that l and the reset count keep their last values there.
 __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, const VecRaw& r,
-                                            float (*lv)[kQmax], float (*dtv)[kQmax], int* segv,
+                                            float (*lv)[kQmax], float (*dtv)[kQmax],
+                                            float (*mv)[kQmax], float (*bv)[kQmax], int* segv,
                                             int lane) {
   const int Q = p.Q, E = Q / 32;
   if (p.dt_raw) {
@@ -251,11 +253,16 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
         loc[i] = run;
       }
       const float excl = warp_incl_scan(run, lane) - run;
+      // l at the last position of this lane's 32-block (E divides 32)
+      const float lf = __shfl_sync(0xffffffffu, excl + loc[E == 8 ? 7 : 3], lane | (32 / E - 1));
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (i < E) {
+          const float l = excl + loc[i];
           dtv[e][lane * E + i] = dv[i];
-          lv[e][lane * E + i] = excl + loc[i];
+          lv[e][lane * E + i] = l;
+          mv[e][lane * E + i] = dv[i] > 0.f ? l - __log2f(dv[i]) : __int_as_float(0x7f800000);
+          bv[e][lane * E + i] = ex2(lf - l) * dv[i];
         }
       }
     }
@@ -279,9 +286,13 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
     for (int e = 0; e < kNH; ++e) {
       const int64_t pq = ((int64_t)it.b * p.H + it.h0 + e) * p.nc + it.c;
       for (int i = lane; i < Q; i += 32) {
-        lv[e][i] = p.cs[pq * Q + i] * kLog2e;
-        dtv[e][i] = p.dt[pq * Q + i];
+        const float l = p.cs[pq * Q + i] * kLog2e, d = p.dt[pq * Q + i];
+        lv[e][i] = l;
+        dtv[e][i] = d;
+        mv[e][i] = d > 0.f ? l - __log2f(d) : __int_as_float(0x7f800000);
       }
+      __syncwarp();
+      for (int i = lane; i < Q; i += 32) bv[e][i] = ex2(lv[e][i | 31] - lv[e][i]) * dtv[e][i];
     }
     if (p.seg)
       for (int i = lane; i < Q; i += 32) segv[i] = p.seg[((int64_t)it.b * p.nc + it.c) * Q + i];
@@ -333,15 +344,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     tc::mbar_init(&s.full, 1);
     tc::mbar_init(&s.zfull, 1);
-    tc::mbar_init(&s.h_ready, 1);
     tc::mbar_init(&s.cb, 1);
-    tc::mbar_init(&s.m_ready, 1);
+    for (int e = 0; e < kNH; ++e) tc::mbar_init(&s.yi_done[e], 1);
     tc::mbar_init(&s.y_done, 1);
-    tc::mbar_init(&s.tmem_free, 1);
+    // arrived on by every compute thread after its own writes, so that the
+    // compute warps never wait for one another
+    tc::mbar_init(&s.h_ready, kComputeThreads);
+    tc::mbar_init(&s.m_ready, kComputeThreads);
+    tc::mbar_init(&s.tmem_free, kComputeThreads);
     tc::mbar_init(&s.pub, kComputeThreads);
     for (int i = 0; i < kRing; ++i) {
-      tc::mbar_init(&s.tk_full[i], 32);                          // the 32 lanes of warp 0
-      tc::mbar_init(&s.tk_empty[i], 1 + kComputeThreads / 32);   // MMA lane + compute warps
+      tc::mbar_init(&s.tk_full[i], 32);   // the 32 lanes of the vector warp
+      tc::mbar_init(&s.tk_empty[i], 2 + kComputeThreads / 32);   // TMA, MMA lanes + compute warps
     }
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&map_x);
@@ -349,7 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tma_prefetch_desc(&map_c);
     tc::tma_prefetch_desc(&map_out);
     if (p.z) tc::tma_prefetch_desc(&map_z);
-    s.first_ticket = atomicAdd(p.ctrl, 1);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -357,43 +370,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.tmem_base;
 
   if (warp == 0) {
-    // ---------------- tickets, per-token vectors (one unit ahead: loaded at
-    // the start of a unit, computed and published once its first tiles are
-    // requested) and the TMA loads: a sub-step's C, B, x_0, x_1 tiles as soon
-    // as the previous sub-step's MMAs are done with them, its z tiles once
-    // the previous epilogue has read Z; after a segment that hands on, the
-    // flag release
-    long long t_cur = s.first_ticket;
-    int j_cur = 0;
-    if (t_cur < p.items) {
-      const Unit u0 = decode(p, t_cur, 0);
-      VecRaw r0;
-      vec_load(p, u0, lane, r0);
-      vec_compute(p, u0, r0, s.lv[0], s.dtv[0], s.segv[0], lane);
-    }
+    // ---------------- TMA: a sub-step's C, B, x_0, x_1 tiles as soon as the
+    // previous sub-step's MMAs are done with them; the previous sub-step's
+    // out tiles (written over Z) by TMA store once its epilogue is done, then
+    // this sub-step's z tiles; after a segment that hands on, the flag release
     if (lane == 0) {
-      s.tk[0] = t_cur;
-      s.tj[0] = 0;
-    }
-    tc::mbar_arrive(&s.tk_full[0]);
-    long long t_pend = p.items;   // lane 0: the ticket of the item after the published ones
-    if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ctrl, 1);
-    uint32_t k = 0, npub = 0;
-    bool pub_pending = false;     // a segment's flag still to raise ...
-    int pub_pair = 0, pub_val = 0;   // ... for this pair, with this value
-    for (int u = 0; t_cur < p.items && !aborted(p.ctrl); ++u) {
-      const Unit cur = decode(p, t_cur, j_cur);
-      long long t_nxt = t_cur;
-      int j_nxt = j_cur + 1;
-      if (j_nxt == cur.nch) {   // the next unit starts the next item
-        t_nxt = __shfl_sync(0xffffffffu, t_pend, 0);
-        j_nxt = 0;
-      }
-      VecRaw raw;   // the next unit's raw per-token inputs, in flight meanwhile
-      if (t_nxt < p.items) vec_load(p, decode(p, t_nxt, j_nxt), lane, raw);
-      for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
-        const int tok = (int)(cur.t0 + sub * kSub);
-        if (lane == 0) {
+      uint32_t k = 0, npub = 0;
+      int st_h0 = 0, st_tok = 0, st_b = 0;   // where the last sub-step's out tiles go
+      bool pub_pending = false;              // a segment's flag still to raise ...
+      int pub_pair = 0, pub_val = 0;         // ... for this pair, with this value
+      for (int u = 0;; ++u) {
+        const int slot = u % kRing;
+        wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
+        const long long t = s.tk[slot];
+        const int j = s.tj[slot];
+        tc::mbar_arrive(&s.tk_empty[slot]);
+        if (t >= p.items || aborted(p.ctrl)) break;
+        const Unit cur = decode(p, t, j);
+        for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
+          const int tok = (int)(cur.t0 + sub * kSub);
           wait_or_flag(&s.y_done, (k & 1) ^ 1, p.ctrl);
           tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kNH * kSub * kP * 2);
           tc::tma_load_4d(s.C, &map_c, &s.full, 0, cur.g, tok, cur.b);
@@ -404,10 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_load_4d(s.X[1], &map_x, &s.full, 0, cur.h0 + 1, tok, cur.b);
           if (pub_pending) {
             // the previous segment's final states are in their slots once
-            // every compute thread has arrived on pub; the release store
-            // orders them before the flag at gpu scope (its consumer waits
-            // for flag >= its first chunk).  Done here, after this unit's
-            // first loads are on their way.
+            // every compute warp has arrived on pub; the release store orders
+            // them before the flag at gpu scope (its consumer waits for flag
+            // >= its first chunk).  Done here, after this unit's first loads
+            // are on their way.
             wait_or_flag(&s.pub, npub & 1, p.ctrl);
             asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pub_pair),
                          "r"(pub_val)
@@ -415,38 +410,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++npub;
             pub_pending = false;
           }
+          wait_or_flag(&s.tmem_free, (k & 1) ^ 1, p.ctrl);
+          if (k > 0) {
+            // rows past the sequence end are outside the tensor map and not written
+            tc::tma_store_4d(&map_out, s.Z[0], 0, st_h0, st_tok, st_b);
+            tc::tma_store_4d(&map_out, s.Z[1], 0, st_h0 + 1, st_tok, st_b);
+            tc::bulk_commit();
+            tc::bulk_wait_read();
+          }
+          st_h0 = cur.h0;
+          st_tok = tok;
+          st_b = cur.b;
           if (p.z) {
-            wait_or_flag(&s.tmem_free, (k & 1) ^ 1, p.ctrl);
             tc::mbar_arrive_expect_tx(&s.zfull, kNH * kSub * kP * 2);
             tc::tma_load_4d(s.Z[0], &map_z, &s.zfull, 0, cur.h0, tok, cur.b);
             tc::tma_load_4d(s.Z[1], &map_z, &s.zfull, 0, cur.h0 + 1, tok, cur.b);
           }
         }
-        if (sub == 0) {   // publish the next unit into the other ring slot
-          const int nu = u + 1, slot = nu % kRing;
-          wait_or_flag(&s.tk_empty[slot], ((nu / kRing) & 1) ^ 1, p.ctrl);
-          if (t_nxt < p.items)
-            vec_compute(p, decode(p, t_nxt, j_nxt), raw, s.lv[slot], s.dtv[slot], s.segv[slot], lane);
-          if (lane == 0) {
-            s.tk[slot] = t_nxt;
-            s.tj[slot] = j_nxt;
-            if (j_nxt == 0 && t_nxt < p.items) t_pend = atomicAdd(p.ctrl, 1);
-          }
-          tc::mbar_arrive(&s.tk_full[slot]);
+        if (cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
+          pub_pending = true;
+          pub_pair = cur.pair;
+          pub_val = cur.c + 1;
         }
       }
-      if (cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
-        pub_pending = true;
-        pub_pair = cur.pair;
-        pub_val = cur.c + 1;
+      if (pub_pending) {
+        wait_or_flag(&s.pub, npub & 1, p.ctrl);
+        asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pub_pair), "r"(pub_val)
+                     : "memory");
       }
-      t_cur = t_nxt;
-      j_cur = j_nxt;
+      if (k > 0) {   // the last sub-step's out tiles
+        wait_or_flag(&s.tmem_free, (k & 1) ^ 1, p.ctrl);
+        tc::tma_store_4d(&map_out, s.Z[0], 0, st_h0, st_tok, st_b);
+        tc::tma_store_4d(&map_out, s.Z[1], 0, st_h0 + 1, st_tok, st_b);
+        tc::bulk_commit();
+        tc::bulk_wait_all();
+      }
     }
-    if (lane == 0 && pub_pending) {
-      wait_or_flag(&s.pub, npub & 1, p.ctrl);
-      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pub_pair), "r"(pub_val)
-                   : "memory");
+  } else if (warp == kVecWarp) {
+    // ---------------- tickets and per-token vectors: the raw inputs of the
+    // next unit are loaded while the ring slot it goes to is still in use
+    long long t_cur = p.items, t_pend = p.items;
+    if (lane == 0) t_cur = atomicAdd(p.ctrl, 1);
+    t_cur = __shfl_sync(0xffffffffu, t_cur, 0);
+    if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ctrl, 1);
+    int j_cur = 0;
+    VecRaw raw;
+    if (t_cur < p.items) vec_load(p, decode(p, t_cur, 0), lane, raw);
+    for (int u = 0;; ++u) {
+      const int slot = u % kRing;
+      wait_or_flag(&s.tk_empty[slot], ((u / kRing) & 1) ^ 1, p.ctrl);
+      if (t_cur < p.items)
+        vec_compute(p, decode(p, t_cur, j_cur), raw, s.lv[slot], s.dtv[slot], s.mv[slot],
+                    s.bv[slot], s.segv[slot], lane);
+      if (lane == 0) {
+        s.tk[slot] = t_cur;
+        s.tj[slot] = j_cur;
+      }
+      tc::mbar_arrive(&s.tk_full[slot]);
+      if (t_cur >= p.items || aborted(p.ctrl)) break;
+      if (j_cur + 1 < decode(p, t_cur, j_cur).nch) {   // the segment's next chunk
+        ++j_cur;
+      } else {                                          // the next item
+        t_cur = __shfl_sync(0xffffffffu, t_pend, 0);
+        j_cur = 0;
+        if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ctrl, 1);
+      }
+      if (t_cur < p.items) vec_load(p, decode(p, t_cur, j_cur), lane, raw);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -489,9 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)     // Yi_0 = M_0 x_0 (M holds the D skip), K = tokens
             tc::mma_ts(tmem + kT_CB, tmem + kT_M + kk * 8, dX0 + kk * 128, id_y, kk > 0);
+          tc::mma_commit(&s.yi_done[0]);     // head 0's epilogue may start
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)     // Yi_1 = M_1 x_1
             tc::mma_ts(tmem + kT_CB + kP, tmem + kT_M + kP + kk * 8, dX1 + kk * 128, id_y, kk > 0);
+          tc::mma_commit(&s.yi_done[1]);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)     // [H_0 | H_1] += B^T [w o x_0 | w o x_1], K = tokens
             tc::mma_ss(tmem + kT_H, dBmn + kk * 128, dXW + kk * 128, id_s, 1);
@@ -512,7 +543,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t T_YEr = tmem + kT_YE + e * kP + lane_addr;
     const uint32_t T_Mr = tmem + kT_M + e * kP + lane_addr;
     const uint32_t T_Hr = tmem + kT_H + e * kP + lane_addr;
-    const int ct = tid - kComputeWarp0 * 32;
     {   // the blocks of M above the diagonal stay zero
       uint32_t zero[32];
 #pragma unroll
@@ -525,6 +555,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // index r is K; headdim p of head e is row 128 + 64 e + p of r's half
     unsigned char* hk = s.BH + (r >> 6) * kBhHalf + (128 + e * kP) * 128 + (r & 7) * 2;
     const int kchunk = (r & 63) >> 3;
+    // h_e (entering) -> bf16 rows of the [B^T | h] operand (thread r writes
+    // dstate column r of every headdim row); H_e <- carry H_e in TMEM
+    auto h_convert = [&](float carry) {
+      tc::tmem_st_wait();   // the entering state's stores (segment start)
+#pragma unroll
+      for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+        uint32_t hv[16];
+        tc::tmem_ld16(T_Hr + qd * 16, hv);
+        tc::tmem_ld_wait_regs(hv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int pcol = qd * 16 + i;   // headdim p: row 128 + 64 e + p, swizzle phase p % 8
+          const __nv_bfloat16 hb = __float2bfloat16_rn(__uint_as_float(hv[i]));
+          *reinterpret_cast<__nv_bfloat16*>(hk + pcol * 128 + ((kchunk ^ (pcol & 7)) << 4)) = hb;
+          hv[i] = __float_as_uint(carry * __uint_as_float(hv[i]));
+        }
+        tc::tmem_st16(T_Hr + qd * 16, hv);
+      }
+      tc::tmem_st_wait();
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&s.h_ready);
+    };
+    bool h_done = false;   // the coming sub-step's entering state is converted
     uint32_t k = 0;
     for (int u = 0;; ++u) {
       const int slot = u % kRing;
@@ -592,47 +646,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sg_r = p.has_seg ? sgv[r] : 0;
         const float l_last = lv[kSub - 1];
         const int sg_last = p.has_seg ? sgv[kSub - 1] : 0;
-        s.mcol[e][r] = dt_r > 0.f ? l_r - __log2f(dt_r) : __int_as_float(0x7f800000);
-        s.bcol[e][r] = ex2(lv[r | 31] - l_r) * dt_r;
         const float w_r = (valid && sg_r == sg_last) ? ex2(l_last - l_r) * dt_r : 0.f;
         const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
-        const float carry = sg_last == sg_prev ? ex2(l_last - l_prev) : 0.f;
+        if (!h_done) h_convert(sg_last == sg_prev ? ex2(l_last - l_prev) : 0.f);
+        h_done = false;
 
-        // ---- h_e (entering) -> bf16 rows of the [B^T | h] operand (thread r
-        // writes dstate column r of every headdim row); H_e <- carry H_e
-        tc::tmem_st_wait();   // the entering state's stores (first sub-step)
+        // ---- w o x_e for the row, while the [CB | Ye] chain runs
+        wait_or_flag(&s.full, ph, p.ctrl);   // x_e has landed
+        {
+          const unsigned char* xr = s.X[e] + r * 128;
+          unsigned char* wr = s.XW[e] + r * 128;
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
-          uint32_t hv[16];
-          tc::tmem_ld16(T_Hr + qd * 16, hv);
-          tc::tmem_ld_wait_regs(hv);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int pcol = qd * 16 + i;   // headdim p: row 128 + 64 e + p, swizzle phase p % 8
-            const __nv_bfloat16 hb = __float2bfloat16_rn(__uint_as_float(hv[i]));
-            *reinterpret_cast<__nv_bfloat16*>(hk + pcol * 128 + ((kchunk ^ (pcol & 7)) << 4)) = hb;
-            hv[i] = __float_as_uint(carry * __uint_as_float(hv[i]));
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
+            const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
+            uint4 o;
+            o.x = tc::pack_bf16x2(bf_lo(xv.x) * w_r, bf_hi(xv.x) * w_r);
+            o.y = tc::pack_bf16x2(bf_lo(xv.y) * w_r, bf_hi(xv.y) * w_r);
+            o.z = tc::pack_bf16x2(bf_lo(xv.z) * w_r, bf_hi(xv.z) * w_r);
+            o.w = tc::pack_bf16x2(bf_lo(xv.w) * w_r, bf_hi(xv.w) * w_r);
+            *reinterpret_cast<uint4*>(wr + off) = o;
           }
-          tc::tmem_st16(T_Hr + qd * 16, hv);
         }
-        if (ct == 0) tc::bulk_wait_read();   // the last out tiles have left XW
-        tc::tmem_st_wait();
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        named_bar_sync(1, kComputeThreads);
-        if (ct == 0) tc::mbar_arrive(&s.h_ready);
 
         // ---- M_e = CB o decay into T_M, the live 32-column blocks 0..qr of
         // this row (the blocks above the diagonal were zeroed once).  Below
-        // the diagonal block the decay factors as exp2(l_r - l_e) *
-        // [exp2(l_e - l_j) dt_j] with e the block's last column (both <= 1);
+        // the diagonal block the decay factors as exp2(l_r - l_f) *
+        // [exp2(l_f - l_j) dt_j] with f the block's last column (both <= 1);
         // the diagonal block takes one exp2 per element.  The D skip rides on
         // the diagonal: M_rr += D, so that M x includes D x_r.  Masks are selects.
-        wait_or_flag(&s.full, ph, p.ctrl);   // x_e has landed
         wait_or_flag(&s.cb, ph, p.ctrl);
         tc::fence_after_sync();
-        const float* mcol = s.mcol[e];
-        const float* bcol = s.bcol[e];
+        const float* mcol = s.mv[slot][e] + sub * kSub;
+        const float* bcol = s.bv[slot][e] + sub * kSub;
 #pragma unroll 1
         for (int qc = 0; qc <= qr; ++qc) {
           const bool diag = qc == qr;
@@ -678,32 +724,59 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
           tc::tmem_st16(T_Mr + (c0 >> 1), packed);
         }
-        // w o x_e for the row
+        tc::tmem_st_wait();
+        tc::fence_proxy_async_smem();   // w o x for the state chain
+        tc::fence_before_sync();
+        tc::mbar_arrive(&s.m_ready);
+
+        // ---- epilogue: out_e = (Yi_e + rho Ye_e) * silu(z_e), written over
+        // z_e in Z (warp 0 stores the tile); Yi_e is committed on its own, so
+        // head 0 starts while Yi_1 and the state chain run
+        wait_or_flag(&s.yi_done[e], ph, p.ctrl);
+        if (p.z) wait_or_flag(&s.zfull, ph, p.ctrl);
+        tc::fence_after_sync();
         {
-          const unsigned char* xr = s.X[e] + r * 128;
-          unsigned char* wr = s.XW[e] + r * 128;
+          unsigned char* zrow = s.Z[e] + r * 128;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
-            const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
-            uint4 o;
-            o.x = tc::pack_bf16x2(bf_lo(xv.x) * w_r, bf_hi(xv.x) * w_r);
-            o.y = tc::pack_bf16x2(bf_lo(xv.y) * w_r, bf_hi(xv.y) * w_r);
-            o.z = tc::pack_bf16x2(bf_lo(xv.z) * w_r, bf_hi(xv.z) * w_r);
-            o.w = tc::pack_bf16x2(bf_lo(xv.w) * w_r, bf_hi(xv.w) * w_r);
-            *reinterpret_cast<uint4*>(wr + off) = o;
+          for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+            uint32_t yi[16], ye[16];
+            tc::tmem_ld16(T_YIr + qd * 16, yi);
+            tc::tmem_ld16(T_YEr + qd * 16, ye);
+            tc::tmem_ld_wait_regs(yi);
+            tc::tmem_ld_wait_regs(ye);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int ch = qd * 2 + cc;
+              uint4* zp = reinterpret_cast<uint4*>(zrow + ((ch ^ (r & 7)) << 4));
+              const uint4 zv = p.z ? *zp : make_uint4(0u, 0u, 0u, 0u);
+              const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+              uint32_t o[4];
+#pragma unroll
+              for (int u4 = 0; u4 < 4; ++u4) {
+                float y2[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  const int i = cc * 8 + u4 * 2 + hh;
+                  float y = fmaf(rho_r, __uint_as_float(ye[i]), __uint_as_float(yi[i]));
+                  if (p.z) y *= silu(hh ? bf_hi(zw[u4]) : bf_lo(zw[u4]));
+                  y2[hh] = y;
+                }
+                o[u4] = tc::pack_bf16x2(y2[0], y2[1]);
+              }
+              *zp = make_uint4(o[0], o[1], o[2], o[3]);
+            }
           }
         }
-        tc::tmem_st_wait();
-        tc::fence_proxy_async_smem();
+        tc::fence_proxy_async_smem();   // out for warp 0's TMA store
         tc::fence_before_sync();
-        named_bar_sync(1, kComputeThreads);
-        if (ct == 0) tc::mbar_arrive(&s.m_ready);
+        tc::mbar_arrive(&s.tmem_free);  // Yi / Ye read out, out written
 
+        // ---- once the MMAs are done: a segment's final states are handed on
+        // (or written out); otherwise the next sub-step's entering state is
+        // converted now, so that its [CB | Ye] chain can start right after
+        // this epilogue
         wait_or_flag(&s.y_done, ph, p.ctrl);
         tc::fence_after_sync();
-
-        // ---- hand the segment's final state on (or write the final states)
         if (sub == cur.nsub - 1 && j == cur.nch - 1) {
           const bool last_chunk = c == p.nc - 1;
           if (!last_chunk || p.final_states) {
@@ -726,53 +799,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!last_chunk) tc::mbar_arrive(&s.pub);   // warp 0 raises the flag
-        }
-
-        // ---- epilogue: out_e = (Yi_e + rho Ye_e) * silu(z_e), z_e from Z, into
-        // this row of XW_e (free once the MMAs are done), then TMA stores of
-        // both tiles
-        unsigned char* orow = s.XW[e] + r * 128;
-        const unsigned char* zrow = s.Z[e] + r * 128;
-        if (p.z) wait_or_flag(&s.zfull, ph, p.ctrl);
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
-          uint32_t yi[16], ye[16];
-          tc::tmem_ld16(T_YIr + qd * 16, yi);
-          tc::tmem_ld16(T_YEr + qd * 16, ye);
-          tc::tmem_ld_wait_regs(yi);
-          tc::tmem_ld_wait_regs(ye);
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int ch = qd * 2 + cc;
-            const uint4 zv = p.z ? *reinterpret_cast<const uint4*>(zrow + ((ch ^ (r & 7)) << 4))
-                                 : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float y2[2];
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int i = cc * 8 + u * 2 + hh;
-                float y = fmaf(rho_r, __uint_as_float(ye[i]), __uint_as_float(yi[i]));
-                if (p.z) y *= silu(hh ? bf_hi(zw[u]) : bf_lo(zw[u]));
-                y2[hh] = y;
-              }
-              o[u] = tc::pack_bf16x2(y2[0], y2[1]);
-            }
-            *reinterpret_cast<uint4*>(orow + ((ch ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          // the next sub-step: the next 128 tokens of this chunk, or the first
+          // of the segment's next chunk (its cumsum starts again at 0)
+          const float* lvn;
+          const int* sgvn;
+          float lp = l_last;
+          int sp = sg_last;
+          if (sub + 1 < cur.nsub) {
+            lvn = lv + kSub;
+            sgvn = sgv + kSub;
+          } else {
+            const int ns = (u + 1) % kRing;
+            wait_or_flag(&s.tk_full[ns], ((u + 1) / kRing) & 1, p.ctrl);
+            lvn = s.lv[ns][e];
+            sgvn = s.segv[ns];
+            lp = 0.f;
+            sp = 0;
           }
-        }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        named_bar_sync(1, kComputeThreads);
-        if (ct == 0) {
-          tc::mbar_arrive(&s.tmem_free);   // Yi / Ye read out
-          // rows past the sequence end are outside the tensor map and not written
-          const int tok = (int)(cur.t0 + sub * kSub);
-          tc::tma_store_4d(&map_out, s.XW[0], 0, cur.h0, tok, cur.b);
-          tc::tma_store_4d(&map_out, s.XW[1], 0, cur.h0 + 1, tok, cur.b);
-          tc::bulk_commit();
+          const int sgn = p.has_seg ? sgvn[kSub - 1] : 0;
+          h_convert(sgn == sp ? ex2(lvn[kSub - 1] - lp) : 0.f);
+          h_done = true;
         }
         l_prev = l_last;
         sg_prev = sg_last;
@@ -782,9 +829,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // drain: the compute warps have waited for every MMA; the storing thread
-  // waits for its last tile stores; release TMEM
-  if (tid == kComputeWarp0 * 32) tc::bulk_wait_all();
+  // drain: the compute warps have waited for every MMA, warp 0 for its last
+  // tile stores; release TMEM
   __syncwarp();
   tc::fence_before_sync();
   __syncthreads();
