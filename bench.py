@@ -378,23 +378,28 @@ def main():
              "hbm_time_us": a["io_bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6,
              "frac_of_hbm_roofline": (a["io_bytes"] / (peaks["hbm_gbs"] * 1e9)) / (ms / 1e3)}
 
-    # end to end: pinned host inputs in, output back, every step
+    # end to end through ssd_scan_fwd_host: the inputs live in pinned host
+    # memory and the output goes back to it, every step (the library pipelines
+    # the copies with the scan over batch slices)
     e2e = None
     if not args.no_e2e:
-        hin = {k: host[k].pin_memory() for k in ("x", "dt", "B", "C", "z")}
+        hin = {k: host[k].contiguous().pin_memory() for k in ("x", "dt", "B", "C", "z")}
+        hsmall = {k: (host[k].contiguous() if torch.is_tensor(host[k]) else None)
+                  for k in ("A", "dt_bias", "D", "initial_states", "seq_idx")}
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        dbuf = {k: torch.empty_like(g[k]) for k in hin}
-        h2d = sum(v.numel() * v.element_size() for v in hin.values())
+        h2d = sum(v.numel() * v.element_size() for v in list(hin.values()) + list(hsmall.values())
+                  if v is not None)
         d2h = hout.numel() * hout.element_size()
+        hws = torch.empty(ssd.host_workspace_bytes(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim,
+                                                   cfg.dstate, cfg.ngroups, Q, g["x"].dtype),
+                          dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            for k, v in hin.items():
-                dbuf[k].copy_(v, non_blocking=True)
-            ssd.ssd_scan_fwd(dbuf["x"], dbuf["dt"], g["A"], dbuf["B"], dbuf["C"], chunk_size=Q,
-                             dt_bias=g["dt_bias"], D=g["D"], z=dbuf["z"],
-                             initial_states=g["initial_states"], seq_idx=g["seq_idx"],
-                             out=out, workspace=ws, stream=stream)
-            hout.copy_(out, non_blocking=True)
+            ssd.ssd_scan_fwd_host(hin["x"], hin["dt"], hsmall["A"], hin["B"], hin["C"],
+                                  chunk_size=Q, dt_bias=hsmall["dt_bias"], D=hsmall["D"],
+                                  z=hin["z"], initial_states=hsmall["initial_states"],
+                                  seq_idx=hsmall["seq_idx"], out=hout, workspace=hws,
+                                  stream=stream, synchronize=False)
 
         for _ in range(2):
             e2e_step()

@@ -241,6 +241,43 @@ int ssd_scan_fwd_noalloc(const void *x, const void *dt, const float *dt_bias,
                          ssd_dtype_t dtype, void *out, float *final_states,
                          void *stream);
 
+/* ---------------------------------------------------------------------------
+ * The forward with the tensors in HOST memory.  (The pages have no
+ * counterpart of this call; it is the library's runtime for callers whose
+ * data lives on the host.)  Arguments as in ssd_scan_fwd, except that x, dt,
+ * dt_bias, A, B, C, D, z, initial_states, seq_idx are host pointers (read)
+ * and out, final_states host pointers (written).  The batch is processed in
+ * slices of rows_per_slice batch rows (<= 0: the library picks about a
+ * quarter of the batch) through two device staging buffers carved from
+ * `workspace` (device memory of >= ssd_scan_host_workspace_bytes(...) bytes,
+ * 256-byte aligned): each slice is copied in, scanned by ssd_scan_fwd's
+ * kernels and copied out on three internal streams ordered with events, so
+ * that the copies of one slice overlap the scan and copies of its
+ * neighbours.  The work starts after the caller's earlier work on `stream`,
+ * and `stream` waits for the last copy out: to the caller the call behaves
+ * like one operation on `stream` (synchronise it before reading out).  Host
+ * memory should be page-locked (cudaHostAlloc / cudaHostRegister); pageable
+ * memory works, but its copies do not overlap.  The host buffers and the
+ * workspace must stay untouched until `stream` has passed the call.  Calls
+ * on one device share the internal streams; their enqueueing is serialised
+ * by a lock, so calls from several host threads are safe but do not
+ * overlap each other.  Returns SSD_OK or a negative SSD_ERR_* code. */
+size_t ssd_scan_host_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
+                                     int headdim, int dstate, int ngroups,
+                                     int chunk_size, ssd_dtype_t dtype,
+                                     int64_t rows_per_slice);
+
+int ssd_scan_fwd_host(const void *x, const void *dt, const float *dt_bias,
+                      int dt_softplus, float dt_limit_lo, float dt_limit_hi,
+                      const float *A, const void *B, const void *C,
+                      const float *D, const void *z,
+                      const float *initial_states, const int32_t *seq_idx,
+                      int64_t batch, int64_t seqlen, int nheads, int headdim,
+                      int dstate, int ngroups, int chunk_size,
+                      ssd_dtype_t dtype, void *out, float *final_states,
+                      int64_t rows_per_slice, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,10 @@ SIGNATURES = {
                                   _vp, _i64, _i64, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
     "ssd_chunk_scan": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i,
                             _i, _i, _i, _i, _vp, _vp]),
+    "ssd_scan_host_workspace_bytes": (_sz, [_i64, _i64, _i, _i, _i, _i, _i, _i, _i64]),
+    "ssd_scan_fwd_host": (_i, [_vp, _vp, _vp, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _i64, _i64, _i, _i, _i, _i, _i, _i, _vp, _vp, _i64, _vp, _sz,
+                               _vp]),
 }
 
 _LIB = None

@@ -29,12 +29,14 @@ def _stream(stream) -> int:
 
 
 def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, device=None,
-          optional=False) -> None:
+          optional=False, host=False) -> None:
     if t is None:
         if optional:
             return
         raise ValueError(f"{name} is required")
-    if not t.is_cuda:
+    if host and t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not host and not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
@@ -238,6 +240,80 @@ def ssd_chunk_fused(x: torch.Tensor, B: torch.Tensor, C: torch.Tensor, dt_out: t
         _ptr(z), _ptr(initial_states), Bsz, L, H, P, N, G, int(chunk_size),
         _lib.SSD_DTYPE_BF16, _ptr(out), _ptr(final_states), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+    if return_final_states:
+        return out, final_states
+    return out
+
+
+# --- host-resident tensors ---------------------------------------------------
+
+def host_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
+                         dtype=torch.bfloat16, rows_per_slice: int = 0) -> int:
+    return int(_lib.load().ssd_scan_host_workspace_bytes(
+        batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, _DT[dtype],
+        rows_per_slice))
+
+
+def ssd_scan_fwd_host(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                      C: torch.Tensor, *, chunk_size: int = 256,
+                      dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
+                      dt_limit: Tuple[float, float] = (0.0, math.inf),
+                      D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                      initial_states: Optional[torch.Tensor] = None,
+                      seq_idx: Optional[torch.Tensor] = None,
+                      return_final_states: bool = False, out: Optional[torch.Tensor] = None,
+                      final_states: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, rows_per_slice: int = 0,
+                      device=None, stream=None, synchronize: bool = True):
+    """ssd_scan_fwd with every tensor on the host (CPU tensors, ideally
+    pinned); the library stages them through `workspace` on `device` (default
+    the current CUDA device) in pipelined batch slices.  Outputs are written
+    to host tensors (allocated pinned when not given).  With synchronize=False
+    the call returns once the work is queued on `stream`; the outputs are
+    valid after that stream is synchronised."""
+    if x.dtype not in _DT:
+        raise ValueError(f"x must be float32 or bfloat16, got {x.dtype}")
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    xd = x.dtype
+    cpu = torch.device("cpu")
+    _need(x, "x", xd, host=True)
+    _need(dt, "dt", xd, (Bsz, L, H), cpu, host=True)
+    _need(A, "A", torch.float32, (H,), cpu, host=True)
+    _need(B, "B", xd, (Bsz, L, G, N), cpu, host=True)
+    _need(C, "C", xd, (Bsz, L, G, N), cpu, host=True)
+    _need(dt_bias, "dt_bias", torch.float32, (H,), cpu, optional=True, host=True)
+    _need(D, "D", torch.float32, (H,), cpu, optional=True, host=True)
+    _need(z, "z", xd, (Bsz, L, H, P), cpu, optional=True, host=True)
+    _need(initial_states, "initial_states", torch.float32, (Bsz, H, P, N), cpu, optional=True,
+          host=True)
+    _need(seq_idx, "seq_idx", torch.int32, (Bsz, L), cpu, optional=True, host=True)
+    if out is None:
+        out = torch.empty(x.shape, dtype=xd).pin_memory()
+    _need(out, "out", xd, (Bsz, L, H, P), cpu, host=True)
+    if return_final_states and final_states is None:
+        final_states = torch.empty(Bsz, H, P, N, dtype=torch.float32).pin_memory()
+    _need(final_states, "final_states", torch.float32, (Bsz, H, P, N), cpu, optional=True,
+          host=True)
+    lib = _lib.load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    need = int(lib.ssd_scan_host_workspace_bytes(Bsz, L, H, P, N, G, chunk_size, _DT[xd],
+                                                 rows_per_slice))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    lo, hi = dt_limit
+    with torch.cuda.device(dev):
+        _lib.check(lib.ssd_scan_fwd_host(
+            _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi),
+            _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(initial_states), _ptr(seq_idx),
+            Bsz, L, H, P, N, G, int(chunk_size), _DT[xd], _ptr(out), _ptr(final_states),
+            int(rows_per_slice), _ptr(workspace), workspace.numel(), _stream(stream)))
+    if synchronize:
+        stream.synchronize()
     if return_final_states:
         return out, final_states
     return out

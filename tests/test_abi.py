@@ -92,3 +92,29 @@ def test_missing_library_fails_loudly(tmp_path):
             _lib.load(tmp_path / "nope.so")
         finally:
             _lib._LIB = saved
+
+
+def test_host_workspace_bytes(lib):
+    # two staging buffers of rows_per_slice rows (x, z, out, dt, B, C, seq_idx,
+    # initial / final states and the slice's scan workspace) plus dt_bias, A, D
+    B, L, H, P, N, G, Q = 8, 4096, 80, 64, 128, 1, 256
+    bf16 = _lib.SSD_DTYPE_BF16
+    for rows in (1, 2, 8):
+        per_row = 3 * L * H * P * 2 + L * H * 2 + 2 * L * G * N * 2 + L * 4 + 2 * H * P * N * 4
+        scan = lib.ssd_scan_workspace_bytes(rows, L, H, P, N, G, Q, bf16)
+        want = 2 * (rows * per_row + scan)
+        got = lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, Q, bf16, rows)
+        assert want <= got <= want + 2 * 11 * 256 + 3 * (H * 4 + 256)
+    # default: a quarter of the batch per slice
+    assert (lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, Q, bf16, 0)
+            == lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, Q, bf16, 2))
+    assert lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, 100, bf16, 0) == 0   # bad chunk
+
+
+def test_host_call_validation_before_any_cuda_call(lib):
+    args = [16, 16, None, 1, 0.0, math.inf, 16, 16, 16, None, None, None, None,
+            1, 64, 2, 16, 16, 1, 64, 0, 16, None, 0, None, 0, None]
+    assert lib.ssd_scan_fwd_host(*args) == -2                # no workspace
+    args[24], args[25] = 4096, 16
+    assert lib.ssd_scan_fwd_host(*args) == -5                # workspace too small
+    assert b"workspace" in lib.ssd_last_error()
