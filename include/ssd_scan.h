@@ -19,8 +19,9 @@
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller, dense
- *    row-major (C-contiguous) in the layout given, 16-byte aligned.  The
- *    library keeps no pointer after the call returns.
+ *    row-major (C-contiguous) in the layout given, 16-byte aligned (except
+ *    in ssd_scan_fwd_host, whose tensors are in host memory).  The library
+ *    keeps no pointer after the call returns.
  *  - "x dtype" is the dtype argument: SSD_DTYPE_F32 (float) or
  *    SSD_DTYPE_BF16 (__nv_bfloat16).  dt_bias, A, D, states are float.
  *  - Everything is enqueued on `stream` (a cudaStream_t; NULL = legacy
@@ -247,8 +248,8 @@ int ssd_scan_fwd_noalloc(const void *x, const void *dt, const float *dt_bias,
  * data lives on the host.)  Arguments as in ssd_scan_fwd, except that x, dt,
  * dt_bias, A, B, C, D, z, initial_states, seq_idx are host pointers (read)
  * and out, final_states host pointers (written).  The batch is processed in
- * slices of rows_per_slice batch rows (<= 0: the library picks about a
- * quarter of the batch) through two device staging buffers carved from
+ * slices of rows_per_slice batch rows (<= 0: the library picks about an
+ * eighth of the batch) through two device staging buffers carved from
  * `workspace` (device memory of >= ssd_scan_host_workspace_bytes(...) bytes,
  * 256-byte aligned): each slice is copied in, scanned by ssd_scan_fwd's
  * kernels and copied out on three internal streams ordered with events, so

@@ -63,7 +63,9 @@ HostLayout host_layout(int64_t rows, int64_t L, int H, int P, int N, int G, int 
   return l;
 }
 
-int64_t default_rows(int64_t batch) { return (batch + 3) / 4; }   // four slices
+// about eight slices: short fill and drain of the pipeline (measured on the
+// 2.7B shape: 1 row of 8 per slice 4.21 ms, 2 rows 4.35, 4 rows 4.66)
+int64_t default_rows(int64_t batch) { return (batch + 7) / 8; }
 
 // Streams and events of the pipeline, one set per device, created on first
 // use; `lock` serialises the enqueueing of calls that share them.

@@ -105,9 +105,9 @@ def test_host_workspace_bytes(lib):
         want = 2 * (rows * per_row + scan)
         got = lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, Q, bf16, rows)
         assert want <= got <= want + 2 * 11 * 256 + 3 * (H * 4 + 256)
-    # default: a quarter of the batch per slice
+    # default: an eighth of the batch per slice
     assert (lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, Q, bf16, 0)
-            == lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, Q, bf16, 2))
+            == lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, Q, bf16, 1))
     assert lib.ssd_scan_host_workspace_bytes(B, L, H, P, N, G, 100, bf16, 0) == 0   # bad chunk
 
 
