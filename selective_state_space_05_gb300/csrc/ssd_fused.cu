@@ -299,6 +299,38 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
   }
 }
 
+// Packed pairs of fp32 (sm_100-family f32x2 arithmetic: one instruction per
+// two lanes of work).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float2 up2(uint64_t d) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// the two bf16 of a 32-bit word as a packed fp32 pair (low half first)
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// a packed fp32 pair rounded to two bf16 (low half first)
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t d) {
+  const float2 f = up2(d);
+  return tc::pack_bf16x2(f.x, f.y);
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -558,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // h_e (entering) -> bf16 rows of the [B^T | h] operand (thread r writes
     // dstate column r of every headdim row); H_e <- carry H_e in TMEM
     auto h_convert = [&](float carry) {
+      const uint64_t carry2 = pk2(carry, carry);
       tc::tmem_st_wait();   // the entering state's stores (segment start)
 #pragma unroll
       for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
@@ -569,7 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pcol = qd * 16 + i;   // headdim p: row 128 + 64 e + p, swizzle phase p % 8
           const __nv_bfloat16 hb = __float2bfloat16_rn(__uint_as_float(hv[i]));
           *reinterpret_cast<__nv_bfloat16*>(hk + pcol * 128 + ((kchunk ^ (pcol & 7)) << 4)) = hb;
-          hv[i] = __float_as_uint(carry * __uint_as_float(hv[i]));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const float2 c2 = up2(mul2(pk2(__uint_as_float(hv[i]), __uint_as_float(hv[i + 1])),
+                                     carry2));
+          hv[i] = __float_as_uint(c2.x);
+          hv[i + 1] = __float_as_uint(c2.y);
         }
         tc::tmem_st16(T_Hr + qd * 16, hv);
       }
@@ -656,15 +695,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const unsigned char* xr = s.X[e] + r * 128;
           unsigned char* wr = s.XW[e] + r * 128;
+          const uint64_t w2 = pk2(w_r, w_r);
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
             const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
             uint4 o;
-            o.x = tc::pack_bf16x2(bf_lo(xv.x) * w_r, bf_hi(xv.x) * w_r);
-            o.y = tc::pack_bf16x2(bf_lo(xv.y) * w_r, bf_hi(xv.y) * w_r);
-            o.z = tc::pack_bf16x2(bf_lo(xv.z) * w_r, bf_hi(xv.z) * w_r);
-            o.w = tc::pack_bf16x2(bf_lo(xv.w) * w_r, bf_hi(xv.w) * w_r);
+            o.x = f2_to_bf2(mul2(bf2_to_f2(xv.x), w2));
+            o.y = f2_to_bf2(mul2(bf2_to_f2(xv.y), w2));
+            o.z = f2_to_bf2(mul2(bf2_to_f2(xv.z), w2));
+            o.w = f2_to_bf2(mul2(bf2_to_f2(xv.w), w2));
             *reinterpret_cast<uint4*>(wr + off) = o;
           }
         }
@@ -699,14 +739,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld_wait_regs(v);
           float m[32];
           if (diag) {
+            const uint64_t lr2 = pk2(l_r, l_r), neg2 = pk2(-1.f, -1.f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float val = __uint_as_float(v[i]) * ex2(l_r - colv[i]);
-              m[i] = (c0 + i < r) ? val : (c0 + i == r ? val + Dh : 0.f);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 d = up2(fma2(pk2(colv[i], colv[i + 1]), neg2, lr2));   // l_r - mcol
+              const float2 val = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                          pk2(ex2(d.x), ex2(d.y))));
+              m[i] = (c0 + i < r) ? val.x : (c0 + i == r ? val.x + Dh : 0.f);
+              m[i + 1] = (c0 + i + 1 < r) ? val.y : (c0 + i + 1 == r ? val.y + Dh : 0.f);
             }
           } else {
+            const uint64_t a2 = pk2(arow, arow);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) m[i] = __uint_as_float(v[i]) * (colv[i] * arow);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 mm = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                         mul2(pk2(colv[i], colv[i + 1]), a2)));
+              m[i] = mm.x;
+              m[i + 1] = mm.y;
+            }
           }
           if (p.has_seg) {   // a reset between j and r zeroes the entry
             const int4* sp4 = reinterpret_cast<const int4*>(sgv + c0);
@@ -737,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         {
           unsigned char* zrow = s.Z[e] + r * 128;
+          const uint64_t rho2 = pk2(rho_r, rho_r), half2 = pk2(0.5f, 0.5f);
 #pragma unroll
           for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
             uint32_t yi[16], ye[16];
@@ -753,15 +804,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t o[4];
 #pragma unroll
               for (int u4 = 0; u4 < 4; ++u4) {
-                float y2[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  const int i = cc * 8 + u4 * 2 + hh;
-                  float y = fmaf(rho_r, __uint_as_float(ye[i]), __uint_as_float(yi[i]));
-                  if (p.z) y *= silu(hh ? bf_hi(zw[u4]) : bf_lo(zw[u4]));
-                  y2[hh] = y;
+                const int i = cc * 8 + u4 * 2;
+                uint64_t y = fma2(rho2, pk2(__uint_as_float(ye[i]), __uint_as_float(ye[i + 1])),
+                                  pk2(__uint_as_float(yi[i]), __uint_as_float(yi[i + 1])));
+                if (p.z) {   // silu(z) = z (1 + tanh(z/2)) / 2
+                  const uint64_t hz = mul2(bf2_to_f2(zw[u4]), half2);
+                  const float2 h = up2(hz);
+                  y = mul2(y, fma2(hz, pk2(tanh_fast(h.x), tanh_fast(h.y)), hz));
                 }
-                o[u4] = tc::pack_bf16x2(y2[0], y2[1]);
+                o[u4] = f2_to_bf2(y);
               }
               *zp = make_uint4(o[0], o[1], o[2], o[3]);
             }
