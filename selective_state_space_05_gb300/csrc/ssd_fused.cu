@@ -51,7 +51,7 @@ constexpr int kSub = 128;   // tokens per sub-step (MMA M)
 constexpr int kP = 64;      // headdim
 constexpr int kN = 128;     // dstate
 constexpr int kQmax = 256;  // largest chunk
-constexpr int kRing = 2;    // items whose tickets / vectors are published
+constexpr int kRing = 3;    // units whose tickets / vectors are published
 constexpr int kNH = 2;      // heads per item
 constexpr int kComputeWarp0 = 2;        // warps 0 (TMA) and 1 (MMA) come first, then compute
 constexpr int kComputeThreads = 128 * kNH;   // one warp per head and TMEM lane quarter
@@ -74,6 +74,14 @@ constexpr int kErrLookback = 2;
 // (tokens), rows 128 + 64 e + p the entering state of head e, headdim p.
 constexpr int kBhHalf = 256 * 128;
 
+// One chunk of a work item: ticket t = (segment, head pair), chunk j of the
+// segment.
+struct Unit {
+  int b, c, h0, g, pair, nvalid, nsub;   // pair = b * H/2 + h0/2
+  int j, nch;                            // chunk of the segment, chunks in it
+  int64_t t0;
+};
+
 struct alignas(1024) Smem {
   unsigned char C[kSub * kN * 2];      // two 64-column halves, 128B swizzle
   unsigned char BH[2 * kBhHalf];       // see kBhHalf
@@ -86,7 +94,8 @@ struct alignas(1024) Smem {
   float bv[kRing][kNH][kQmax];   // exp2(l_f - l_j) dt_j, f = last position of j's 32-block
   int segv[kRing][kQmax];        // reset counts (with seq_idx)
   long long tk[kRing];     // published units: ticket (>= items: no more work) ...
-  int tj[kRing];           // ... and chunk of its segment
+  Unit uk[kRing];          // ... decoded
+  float dk[kRing][kNH];    // ... and the two heads' D (0 without D)
   uint64_t tk_full[kRing], tk_empty[kRing];
   uint64_t full, zfull, h_ready, cb, m_ready, yi_done[kNH], y_done, tmem_free;
   uint64_t pub;            // the segment's final states are in their slots
@@ -122,13 +131,6 @@ struct Params {
   long long items;       // B * H/2 * ceil(nc / seg_chunks)
 };
 
-// One chunk of a work item: ticket t = (segment, head pair), chunk j of the
-// segment.
-struct Unit {
-  int b, c, h0, g, pair, nvalid, nsub;   // pair = b * H/2 + h0/2
-  int j, nch;                            // chunk of the segment, chunks in it
-  int64_t t0;
-};
 
 __device__ __forceinline__ Unit decode(const Params& p, long long t, int j) {
   Unit u;
@@ -415,10 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = u % kRing;
         wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
         const long long t = s.tk[slot];
-        const int j = s.tj[slot];
+        const Unit cur = s.uk[slot];
         tc::mbar_arrive(&s.tk_empty[slot]);
         if (t >= p.items || aborted(p.ctrl)) break;
-        const Unit cur = decode(p, t, j);
         for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
           const int tok = (int)(cur.t0 + sub * kSub);
           wait_or_flag(&s.y_done, (k & 1) ^ 1, p.ctrl);
@@ -496,7 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s.bv[slot], s.segv[slot], lane);
       if (lane == 0) {
         s.tk[slot] = t_cur;
-        s.tj[slot] = j_cur;
+        if (t_cur < p.items) {
+          const Unit uu = decode(p, t_cur, j_cur);
+          s.uk[slot] = uu;
+          for (int e = 0; e < kNH; ++e) s.dk[slot][e] = p.D ? p.D[uu.h0 + e] : 0.f;
+        }
       }
       tc::mbar_arrive(&s.tk_full[slot]);
       if (t_cur >= p.items || aborted(p.ctrl)) break;
@@ -528,10 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = u % kRing;
         wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
         const long long t = s.tk[slot];
-        const int j = s.tj[slot];
+        const int nsub = s.uk[slot].nsub;
         tc::mbar_arrive(&s.tk_empty[slot]);
         if (t >= p.items || aborted(p.ctrl)) break;
-        const int nsub = decode(p, t, j).nsub;
         for (int sub = 0; sub < nsub; ++sub, ++k) {
           const uint32_t ph = k & 1;
           wait_or_flag(&s.tmem_free, ph ^ 1, p.ctrl);
@@ -623,12 +627,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = u % kRing;
       wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
       const long long t = s.tk[slot];
-      const int j = s.tj[slot];
       if (t >= p.items || aborted(p.ctrl)) break;
-      const Unit cur = decode(p, t, j);
+      const Unit cur = s.uk[slot];
+      const int j = cur.j;
       const int c = cur.c, h = cur.h0 + e;
       const int64_t bh = (int64_t)cur.b * p.H + h;   // this head's state slots
-      const float Dh = p.D ? p.D[h] : 0.f;
+      const float Dh = s.dk[slot][e];
       float l_prev = 0.f;   // the cumsum restarts with every chunk
       int sg_prev = 0;
 
