@@ -12,32 +12,37 @@
 //   warp 10   takes the tickets and, one chunk ("unit") ahead, computes the
 //             per-token vectors (dt = softplus(dt_raw + dt_bias) clamped, the
 //             cumsum of dt*A per head, the decay-matrix column factors, the
-//             reset counts of seq_idx) into a two-slot ring
+//             reset counts of seq_idx) into a three-slot ring
 //   warp 0    lane 0 issues the TMA loads (C, B, x, z) and out stores and
 //             raises the hand-off flag after a segment
 //   warp 1    lane 0 issues the tcgen05 MMAs
 //   warps 2-9 four per head (one per TMEM lane quarter): decay matrix,
 //             state moves, epilogue; they never wait for one another (every
 //             thread arrives on the mbarriers its consumers wait on)
-// A chunk is processed as 128-token sub-steps; per sub-step, with rows /
+// A chunk is processed as 128-token sub-steps; per sub-step k, with rows /
 // columns = the sub-step's tokens, cs the chunk's cumsum and h_e the state
 // entering the sub-step (head e = 0, 1):
-//   [CB | Ye_0 | Ye_1] = C [B^T | h_0 | h_1]   one N=256 tcgen05 chain, A = C
+//   CB   = C B^T                       tcgen05, issued during step k-1's epilogue
 //   M_e  = CB o exp(cs_i - cs_j) dt_j  (j <= i, same document)   CUDA cores -> TMEM
 //   Yi_e = M_e x_e                     tcgen05, A = M_e from TMEM
 //   H_e <- exp(cs_last - cs_prev) H_e  CUDA cores, in TMEM (fp32 state H = h^T)
+//   [Ye_0 | Ye_1] = C [h_0 | h_1]      tcgen05, A = C
 //   [H_0 | H_1] += B^T [w_0 o x_0 | w_1 o x_1]   one N=128 chain, A = B^T
 //          w_j = exp(cs_last - cs_j) dt_j  (the sub-step's own chunk state)
 //   out_e = (Yi_e + exp(cs_i - cs_prev) Ye_e + D x_e) * silu(z_e)
-// Sharing the A operand across the pair halves the MMA instructions per head
-// (an M=128 tcgen05.mma costs about the same for N = 64 .. 256).  Yi_0 and
-// Yi_1 are committed separately so that each head's epilogue starts as soon
-// as its own product is ready, and the next sub-step's entering state is
-// converted right after the MMAs, before the epilogue ends.  The fp32 states
-// stay in TMEM (one row of dstate per TMEM lane, headdim columns) for the
-// whole segment and are handed to the next segment through L2-resident fp32
-// slots and a flag (decoupled look-back); every wait is bounded and gives up
-// with an error word instead of hanging.
+// Sharing the operands across the pair halves the MMA instructions per head
+// (an M=128 tcgen05.mma costs about the same for N = 64 .. 256).  Only the
+// state recurrence (state chain of step k -> h and carried state of step k+1)
+// is serial; the rest is pipelined one step ahead: two TMEM regions trade the
+// CB / Yi and M roles every step, so CB of step k+1 runs on the tensor cores
+// during step k's epilogue, and x of step k+1 lands in the buffer that w o x
+// of step k has left.  The compute warps convert step k+1's entering state
+// while step k's Yi MMAs run.  Yi_0 and Yi_1 are committed separately so that
+// each head's epilogue starts as soon as its own product is ready.  The fp32
+// states stay in TMEM (one row of dstate per TMEM lane, headdim columns) for
+// the whole segment and are handed to the next segment through L2-resident
+// fp32 slots and a flag (decoupled look-back); every wait is bounded and
+// gives up with an error word instead of hanging.
 #include <cudaTypedefs.h>
 
 #include "../../include/ssd_scan.h"
@@ -61,8 +66,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // any single wait: 2 s at most
 constexpr uint32_t kSleepHintNs = 20000;                 // suspend hint of one try_wait
 
-// TMEM columns: [CB | Ye_0 | Ye_1], then Yi_0 / Yi_1 over CB; M_e; H_e
-constexpr uint32_t kT_CB = 0, kT_YE = 128, kT_M = 256, kT_H = 384;
+// TMEM columns: two 128-column regions R0 / R1 that trade roles every
+// sub-step (CB_k then Yi_0 | Yi_1 over it in R[k%2], M_0 | M_1 in R[(k+1)%2]),
+// [Ye_0 | Ye_1], [H_0 | H_1]
+constexpr uint32_t kT_R0 = 0, kT_YE = 128, kT_R1 = 256, kT_H = 384;
 
 // error bits in the control block word ctrl[1]; once one is set every later
 // wait of the launch returns at once, so a broken launch still ends quickly
@@ -85,8 +92,9 @@ struct Unit {
 struct alignas(1024) Smem {
   unsigned char C[kSub * kN * 2];      // two 64-column halves, 128B swizzle
   unsigned char BH[2 * kBhHalf];       // see kBhHalf
-  unsigned char X[kNH][kSub * kP * 2]; // x_e (MN-major B operand of Yi_e)
-  unsigned char XW[kNH][kSub * kP * 2];   // w o x_e (B operand of the state chain)
+  // x_e of sub-step k in XB[k%2] (MN-major B operand of Yi_e); w o x_e in
+  // XB[(k+1)%2] (B operand of the state chain), written over x of step k-1
+  unsigned char XB[2][kNH][kSub * kP * 2];
   unsigned char Z[kNH][kSub * kP * 2];    // z_e; the epilogue writes out_e over it
   float lv[kRing][kNH][kQmax];   // l = log2(e) * cumsum of dt*A over the chunk
   float dtv[kRing][kNH][kQmax];  // dt
@@ -97,7 +105,9 @@ struct alignas(1024) Smem {
   Unit uk[kRing];          // ... decoded
   float dk[kRing][kNH];    // ... and the two heads' D (0 without D)
   uint64_t tk_full[kRing], tk_empty[kRing];
-  uint64_t full, zfull, h_ready, cb, m_ready, yi_done[kNH], y_done, tmem_free;
+  uint64_t cbfull, xfull, zfull;   // C and B / x / z tiles of a sub-step landed
+  uint64_t cb, yi_done[kNH], y_done;   // MMA commits: CB; Yi_e; Ye and the state chain
+  uint64_t hx_ready, m_ready, out_ready;   // compute: h and w o x; M; out tile written
   uint64_t pub;            // the segment's final states are in their slots
   uint32_t tmem_base;
 };
@@ -376,16 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(&s.full, 1);
+    tc::mbar_init(&s.cbfull, 1);
+    tc::mbar_init(&s.xfull, 1);
     tc::mbar_init(&s.zfull, 1);
     tc::mbar_init(&s.cb, 1);
     for (int e = 0; e < kNH; ++e) tc::mbar_init(&s.yi_done[e], 1);
     tc::mbar_init(&s.y_done, 1);
     // arrived on by every compute thread after its own writes, so that the
     // compute warps never wait for one another
-    tc::mbar_init(&s.h_ready, kComputeThreads);
+    tc::mbar_init(&s.hx_ready, kComputeThreads);
     tc::mbar_init(&s.m_ready, kComputeThreads);
-    tc::mbar_init(&s.tmem_free, kComputeThreads);
+    tc::mbar_init(&s.out_ready, kComputeThreads);
     tc::mbar_init(&s.pub, kComputeThreads);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(&s.tk_full[i], 32);   // the 32 lanes of the vector warp
@@ -403,80 +414,89 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
 
+  // Every role walks the same sequence of sub-steps k = 0, 1, ... (the units
+  // the vector warp publishes, nsub sub-steps each); the barriers complete
+  // once per sub-step, so the parity of step k is k & 1.
   if (warp == 0) {
-    // ---------------- TMA: a sub-step's C, B, x_0, x_1 tiles as soon as the
-    // previous sub-step's MMAs are done with them; the previous sub-step's
-    // out tiles (written over Z) by TMA store once its epilogue is done, then
-    // this sub-step's z tiles; after a segment that hands on, the flag release
+    // ---------------- TMA: step k+1's C, B and x tiles as soon as step k's
+    // Ye and state chains are done with C, B and w o x (x lands in the buffer
+    // w o x of step k occupied); step k's out tiles (written over Z) once its
+    // epilogue is done, then step k+1's z tiles; after a segment that hands
+    // on, the flag release
     if (lane == 0) {
-      uint32_t k = 0, npub = 0;
-      int st_h0 = 0, st_tok = 0, st_b = 0;   // where the last sub-step's out tiles go
-      bool pub_pending = false;              // a segment's flag still to raise ...
-      int pub_pair = 0, pub_val = 0;         // ... for this pair, with this value
-      for (int u = 0;; ++u) {
-        const int slot = u % kRing;
-        wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
-        const long long t = s.tk[slot];
-        const Unit cur = s.uk[slot];
-        tc::mbar_arrive(&s.tk_empty[slot]);
-        if (t >= p.items || aborted(p.ctrl)) break;
-        for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
+      int u = 0, sub = 0;
+      uint32_t npub = 0;
+      wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+      Unit cur = s.uk[0];
+      bool live = s.tk[0] < p.items && !aborted(p.ctrl);
+      tc::mbar_arrive(&s.tk_empty[0]);
+      auto load_cbx = [&](const Unit& it, int sb, int xb) {
+        const int tok = (int)(it.t0 + sb * kSub);
+        tc::mbar_arrive_expect_tx(&s.cbfull, 2 * kSub * kN * 2);
+        tc::tma_load_4d(s.C, &map_c, &s.cbfull, 0, it.g, tok, it.b);
+        tc::tma_load_4d(s.C + kSub * 128, &map_c, &s.cbfull, 64, it.g, tok, it.b);
+        tc::tma_load_4d(s.BH, &map_b, &s.cbfull, 0, it.g, tok, it.b);
+        tc::tma_load_4d(s.BH + kBhHalf, &map_b, &s.cbfull, 64, it.g, tok, it.b);
+        tc::mbar_arrive_expect_tx(&s.xfull, kNH * kSub * kP * 2);
+        tc::tma_load_4d(s.XB[xb][0], &map_x, &s.xfull, 0, it.h0, tok, it.b);
+        tc::tma_load_4d(s.XB[xb][1], &map_x, &s.xfull, 0, it.h0 + 1, tok, it.b);
+      };
+      auto load_z = [&](const Unit& it, int sb) {
+        if (p.z) {
+          const int tok = (int)(it.t0 + sb * kSub);
+          tc::mbar_arrive_expect_tx(&s.zfull, kNH * kSub * kP * 2);
+          tc::tma_load_4d(s.Z[0], &map_z, &s.zfull, 0, it.h0, tok, it.b);
+          tc::tma_load_4d(s.Z[1], &map_z, &s.zfull, 0, it.h0 + 1, tok, it.b);
+        } else {
+          tc::mbar_arrive(&s.zfull);   // Z is free for the epilogue
+        }
+      };
+      if (live) {
+        load_cbx(cur, 0, 0);
+        load_z(cur, 0);
+      }
+      for (uint32_t k = 0; live; ++k) {
+        // the step after this one: the unit's next sub-step or the next unit
+        Unit nxt = cur;
+        int nsb = sub + 1;
+        bool has_next = true;
+        if (nsb == cur.nsub) {
+          const int ns = (u + 1) % kRing;
+          wait_or_flag(&s.tk_full[ns], ((u + 1) / kRing) & 1, p.ctrl);
+          has_next = s.tk[ns] < p.items && !aborted(p.ctrl);
+          nxt = s.uk[ns];
+          tc::mbar_arrive(&s.tk_empty[ns]);
+          nsb = 0;
+        }
+        wait_or_flag(&s.y_done, k & 1, p.ctrl);
+        if (has_next) load_cbx(nxt, nsb, (k + 1) & 1);
+        if (sub == cur.nsub - 1 && cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
+          // the segment's final states are in their slots once every compute
+          // thread has arrived on pub; the release store orders them before
+          // the flag at gpu scope (its consumer waits for flag >= its first chunk)
+          wait_or_flag(&s.pub, npub & 1, p.ctrl);
+          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + cur.pair),
+                       "r"(cur.c + 1)
+                       : "memory");
+          ++npub;
+        }
+        wait_or_flag(&s.out_ready, k & 1, p.ctrl);
+        {
+          // rows past the sequence end are outside the tensor map and not written
           const int tok = (int)(cur.t0 + sub * kSub);
-          wait_or_flag(&s.y_done, (k & 1) ^ 1, p.ctrl);
-          tc::mbar_arrive_expect_tx(&s.full, 2 * kSub * kN * 2 + kNH * kSub * kP * 2);
-          tc::tma_load_4d(s.C, &map_c, &s.full, 0, cur.g, tok, cur.b);
-          tc::tma_load_4d(s.C + kSub * 128, &map_c, &s.full, 64, cur.g, tok, cur.b);
-          tc::tma_load_4d(s.BH, &map_b, &s.full, 0, cur.g, tok, cur.b);
-          tc::tma_load_4d(s.BH + kBhHalf, &map_b, &s.full, 64, cur.g, tok, cur.b);
-          tc::tma_load_4d(s.X[0], &map_x, &s.full, 0, cur.h0, tok, cur.b);
-          tc::tma_load_4d(s.X[1], &map_x, &s.full, 0, cur.h0 + 1, tok, cur.b);
-          if (pub_pending) {
-            // the previous segment's final states are in their slots once
-            // every compute warp has arrived on pub; the release store orders
-            // them before the flag at gpu scope (its consumer waits for flag
-            // >= its first chunk).  Done here, after this unit's first loads
-            // are on their way.
-            wait_or_flag(&s.pub, npub & 1, p.ctrl);
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pub_pair),
-                         "r"(pub_val)
-                         : "memory");
-            ++npub;
-            pub_pending = false;
-          }
-          wait_or_flag(&s.tmem_free, (k & 1) ^ 1, p.ctrl);
-          if (k > 0) {
-            // rows past the sequence end are outside the tensor map and not written
-            tc::tma_store_4d(&map_out, s.Z[0], 0, st_h0, st_tok, st_b);
-            tc::tma_store_4d(&map_out, s.Z[1], 0, st_h0 + 1, st_tok, st_b);
-            tc::bulk_commit();
-            tc::bulk_wait_read();
-          }
-          st_h0 = cur.h0;
-          st_tok = tok;
-          st_b = cur.b;
-          if (p.z) {
-            tc::mbar_arrive_expect_tx(&s.zfull, kNH * kSub * kP * 2);
-            tc::tma_load_4d(s.Z[0], &map_z, &s.zfull, 0, cur.h0, tok, cur.b);
-            tc::tma_load_4d(s.Z[1], &map_z, &s.zfull, 0, cur.h0 + 1, tok, cur.b);
-          }
+          tc::tma_store_4d(&map_out, s.Z[0], 0, cur.h0, tok, cur.b);
+          tc::tma_store_4d(&map_out, s.Z[1], 0, cur.h0 + 1, tok, cur.b);
+          tc::bulk_commit();
         }
-        if (cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
-          pub_pending = true;
-          pub_pair = cur.pair;
-          pub_val = cur.c + 1;
+        if (!has_next) {
+          tc::bulk_wait_all();
+          break;
         }
-      }
-      if (pub_pending) {
-        wait_or_flag(&s.pub, npub & 1, p.ctrl);
-        asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + pub_pair), "r"(pub_val)
-                     : "memory");
-      }
-      if (k > 0) {   // the last sub-step's out tiles
-        wait_or_flag(&s.tmem_free, (k & 1) ^ 1, p.ctrl);
-        tc::tma_store_4d(&map_out, s.Z[0], 0, st_h0, st_tok, st_b);
-        tc::tma_store_4d(&map_out, s.Z[1], 0, st_h0 + 1, st_tok, st_b);
-        tc::bulk_commit();
-        tc::bulk_wait_all();
+        tc::bulk_wait_read();
+        load_z(nxt, nsb);
+        if (nsb == 0) ++u;
+        cur = nxt;
+        sub = nsb;
       }
     }
   } else if (warp == kVecWarp) {
@@ -515,78 +535,105 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t_cur < p.items) vec_load(p, decode(p, t_cur, j_cur), lane, raw);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer.  Per step k, in issue order:
+    //   [Ye_0 | Ye_1] = C_k [h_0 | h_1]; [H_0 | H_1] += B_k^T [w o x_0 | w o x_1]
+    //   Yi_e = M_e x_e (A = M_e from R[(k+1)%2], D over CB_k in R[k%2])
+    //   CB_{k+1} = C_{k+1} B_{k+1}^T into R[(k+1)%2], which M_e of step k has left
+    // so that CB of the next step runs during this step's epilogue.
     if (lane == 0) {
       // descriptor start addresses advance in 16-byte units: K-major k-steps
       // are 32 bytes inside a 64-column half, MN-major k-steps 8 rows of 128 bytes
       const uint64_t dC = tc::sdesc_sw128(tc::smem_u32(s.C), 16, 1024);
       const uint64_t dBH = tc::sdesc_sw128(tc::smem_u32(s.BH), 16, 1024);
       const uint64_t dBmn = tc::sdesc_sw128(tc::smem_u32(s.BH), kBhHalf, 1024);
-      const uint64_t dX0 = tc::sdesc_sw128(tc::smem_u32(s.X[0]), 16384, 1024);
-      const uint64_t dX1 = tc::sdesc_sw128(tc::smem_u32(s.X[1]), 16384, 1024);
-      const uint64_t dXW = tc::sdesc_sw128(tc::smem_u32(s.XW[0]), kSub * kP * 2, 1024);
-      constexpr uint32_t id_cbye = tc::idesc_bf16(kSub, 256, false, false);
+      // x_e of buffer b starts (b kNH + e) tiles after XB (16-byte units)
+      const uint64_t dX = tc::sdesc_sw128(tc::smem_u32(s.XB[0][0]), 16384, 1024);
+      const uint64_t dXW = tc::sdesc_sw128(tc::smem_u32(s.XB[0][0]), kSub * kP * 2, 1024);
+      constexpr uint32_t kXTile = (kSub * kP * 2) >> 4;
+      auto TR = [&](uint32_t b) { return tmem + kT_R0 + b * (kT_R1 - kT_R0); };
+      constexpr uint32_t id_cb = tc::idesc_bf16(kSub, 128, false, false);
       constexpr uint32_t id_y = tc::idesc_bf16(kSub, kP, false, true);
       constexpr uint32_t id_s = tc::idesc_bf16(kN, kNH * kP, true, true);
-      uint32_t k = 0;
-      for (int u = 0;; ++u) {
-        const int slot = u % kRing;
-        wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
-        const long long t = s.tk[slot];
-        const int nsub = s.uk[slot].nsub;
-        tc::mbar_arrive(&s.tk_empty[slot]);
-        if (t >= p.items || aborted(p.ctrl)) break;
-        for (int sub = 0; sub < nsub; ++sub, ++k) {
-          const uint32_t ph = k & 1;
-          wait_or_flag(&s.tmem_free, ph ^ 1, p.ctrl);
-          wait_or_flag(&s.full, ph, p.ctrl);
-          wait_or_flag(&s.h_ready, ph, p.ctrl);
-          tc::fence_after_sync();
+      constexpr uint32_t kHrows = (kSub * 128) >> 4;   // the h rows of [B^T | h], 16-byte units
+      // CB = C B^T into TMEM columns d, K = dstate
+      auto cb_chain = [&](uint32_t d) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {   // [CB | Ye_0 | Ye_1] = C [B^T | h_0 | h_1], K = dstate
-            const uint32_t kc = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
-            const uint32_t kb = ((kk >> 2) * kBhHalf + (kk & 3) * 32) >> 4;
-            tc::mma_ss(tmem + kT_CB, dC + kc, dBH + kb, id_cbye, kk > 0);
-          }
-          tc::mma_commit(&s.cb);
-          wait_or_flag(&s.m_ready, ph, p.ctrl);
-          tc::fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)     // Yi_0 = M_0 x_0 (M holds the D skip), K = tokens
-            tc::mma_ts(tmem + kT_CB, tmem + kT_M + kk * 8, dX0 + kk * 128, id_y, kk > 0);
-          tc::mma_commit(&s.yi_done[0]);     // head 0's epilogue may start
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)     // Yi_1 = M_1 x_1
-            tc::mma_ts(tmem + kT_CB + kP, tmem + kT_M + kP + kk * 8, dX1 + kk * 128, id_y, kk > 0);
-          tc::mma_commit(&s.yi_done[1]);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)     // [H_0 | H_1] += B^T [w o x_0 | w o x_1], K = tokens
-            tc::mma_ss(tmem + kT_H, dBmn + kk * 128, dXW + kk * 128, id_s, 1);
-          tc::mma_commit(&s.y_done);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t kc = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t kb = ((kk >> 2) * kBhHalf + (kk & 3) * 32) >> 4;
+          tc::mma_ss(d, dC + kc, dBH + kb, id_cb, kk > 0);
         }
+      };
+      int u = 0, sub = 0;
+      wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+      int nsub = s.uk[0].nsub;
+      bool live = s.tk[0] < p.items && !aborted(p.ctrl);
+      tc::mbar_arrive(&s.tk_empty[0]);
+      if (live) {
+        wait_or_flag(&s.cbfull, 0, p.ctrl);
+        tc::fence_after_sync();
+        cb_chain(TR(0));
+        tc::mma_commit(&s.cb);
+      }
+      for (uint32_t k = 0; live; ++k) {
+        const uint32_t ph = k & 1, bc = k & 1;
+        wait_or_flag(&s.hx_ready, ph, p.ctrl);   // h_e and w o x_e written, Ye read out
+        tc::fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {   // [Ye_0 | Ye_1] = C [h_0 | h_1], K = dstate
+          const uint32_t kc = ((kk >> 2) * (kSub * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t kb = ((kk >> 2) * kBhHalf + (kk & 3) * 32) >> 4;
+          tc::mma_ss(tmem + kT_YE, dC + kc, dBH + kHrows + kb, id_cb, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)     // [H_0 | H_1] += B^T [w o x_0 | w o x_1], K = tokens
+          tc::mma_ss(tmem + kT_H, dBmn + kk * 128, dXW + (bc ^ 1) * kNH * kXTile + kk * 128, id_s, 1);
+        tc::mma_commit(&s.y_done);
+        wait_or_flag(&s.m_ready, ph, p.ctrl);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < kNH; ++e) {    // Yi_e = M_e x_e (M holds the D skip), K = tokens
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_ts(TR(bc) + e * kP, TR(bc ^ 1) + e * kP + kk * 8,
+                       dX + (bc * kNH + e) * kXTile + kk * 128, id_y, kk > 0);
+          tc::mma_commit(&s.yi_done[e]);   // head e's epilogue may start
+        }
+        if (++sub == nsub) {
+          ++u;
+          const int ns = u % kRing;
+          wait_or_flag(&s.tk_full[ns], (u / kRing) & 1, p.ctrl);
+          nsub = s.uk[ns].nsub;
+          live = s.tk[ns] < p.items && !aborted(p.ctrl);
+          tc::mbar_arrive(&s.tk_empty[ns]);
+          sub = 0;
+        }
+        if (!live) break;
+        // CB_{k+1} overwrites the columns Yi read M from: wait until Yi is done
+        // (in-order execution is only promised along one accumulator)
+        wait_or_flag(&s.yi_done[kNH - 1], ph, p.ctrl);
+        wait_or_flag(&s.cbfull, ph ^ 1, p.ctrl);   // C, B of step k+1
+        tc::fence_after_sync();
+        cb_chain(TR(bc ^ 1));
+        tc::mma_commit(&s.cb);
       }
     }
   } else {
     // ---------------- compute: warp (head e, quarter qr) owns row r = 32 qr
-    // + lane of head e's TMEM tiles and of the sub-step's smem tiles
+    // + lane of head e's TMEM tiles and of the sub-step's smem tiles.  Per
+    // step k: M_e (needs CB_k) -> h and the carried state of step k+1 (needs
+    // step k's state chain; the Yi MMAs run meanwhile) -> epilogue of step k
+    // -> w o x_e of step k+1.  At the end of a segment the final state is
+    // handed on first and the next segment's entering state is loaded after
+    // the epilogue.
     const int cw = warp - kComputeWarp0;
     const int e = cw >> 2;                        // head of the pair
     const int qr = warp & 3;                      // TMEM lane quarter
     const int r = qr * 32 + lane;                 // row: token (or dstate index)
     const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
-    const uint32_t T_CBr = tmem + kT_CB + lane_addr;        // CB row r
-    const uint32_t T_YIr = tmem + kT_CB + e * kP + lane_addr;
+    auto T_R = [&](uint32_t b) { return tmem + kT_R0 + b * (kT_R1 - kT_R0) + lane_addr; };
     const uint32_t T_YEr = tmem + kT_YE + e * kP + lane_addr;
-    const uint32_t T_Mr = tmem + kT_M + e * kP + lane_addr;
     const uint32_t T_Hr = tmem + kT_H + e * kP + lane_addr;
-    {   // the blocks of M above the diagonal stay zero
-      uint32_t zero[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) zero[i] = 0u;
-      tc::tmem_st32(T_Mr, zero);
-      tc::tmem_st32(T_Mr + 32, zero);
-      tc::tmem_st_wait();
-    }
     // entering-state rows of the [B^T | h] operand for this thread: dstate
     // index r is K; headdim p of head e is row 128 + 64 e + p of r's half
     unsigned char* hk = s.BH + (r >> 6) * kBhHalf + (128 + e * kP) * 128 + (r & 7) * 2;
@@ -617,270 +664,315 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st16(T_Hr + qd * 16, hv);
       }
       tc::tmem_st_wait();
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      tc::mbar_arrive(&s.h_ready);
     };
-    bool h_done = false;   // the coming sub-step's entering state is converted
-    uint32_t k = 0;
-    for (int u = 0;; ++u) {
-      const int slot = u % kRing;
-      wait_or_flag(&s.tk_full[slot], (u / kRing) & 1, p.ctrl);
-      const long long t = s.tk[slot];
-      if (t >= p.items || aborted(p.ctrl)) break;
-      const Unit cur = s.uk[slot];
-      const int j = cur.j;
-      const int c = cur.c, h = cur.h0 + e;
-      const int64_t bh = (int64_t)cur.b * p.H + h;   // this head's state slots
-      const float Dh = s.dk[slot][e];
-      float l_prev = 0.f;   // the cumsum restarts with every chunk
-      int sg_prev = 0;
-
-      // first chunk of a segment: the state entering it, this row, loaded and
-      // written to T_H (the predecessor segment raised its flag after both
-      // heads' slots); later chunks continue from the state in T_H
-      if (j == 0) {
-        uint32_t hin0[32], hin1[32];   // headdim columns 0-31 and 32-63
-        if (c == 0) {
-          if (p.init) {
-            const float* src = p.init + bh * kP * kN + r;
+    // w o x_e of a step: x from XB[xb], the product into XB[xb ^ 1]
+    auto wx = [&](float w_r, int xb) {
+      const unsigned char* xr = s.XB[xb][e] + r * 128;
+      unsigned char* wr = s.XB[xb ^ 1][e] + r * 128;
+      const uint64_t w2 = pk2(w_r, w_r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              hin0[i] = __float_as_uint(src[i * kN]);
-              hin1[i] = __float_as_uint(src[(32 + i) * kN]);
-            }
-          } else {
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
+        const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
+        uint4 o;
+        o.x = f2_to_bf2(mul2(bf2_to_f2(xv.x), w2));
+        o.y = f2_to_bf2(mul2(bf2_to_f2(xv.y), w2));
+        o.z = f2_to_bf2(mul2(bf2_to_f2(xv.z), w2));
+        o.w = f2_to_bf2(mul2(bf2_to_f2(xv.w), w2));
+        *reinterpret_cast<uint4*>(wr + off) = o;
+      }
+    };
+    // the state entering a segment (its first chunk), this row, into T_H:
+    // the initial state or zeros for chunk 0, else the predecessor segment's
+    // final state once its flag is raised (it raises the flag after both
+    // heads' slots are written)
+    auto load_hin = [&](const Unit& it) {
+      const int64_t bh = (int64_t)it.b * p.H + it.h0 + e;
+      uint32_t hin0[32], hin1[32];   // headdim columns 0-31 and 32-63
+      if (it.c == 0) {
+        if (p.init) {
+          const float* src = p.init + bh * kP * kN + r;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) hin0[i] = hin1[i] = 0u;
+          for (int i = 0; i < 32; ++i) {
+            hin0[i] = __float_as_uint(src[i * kN]);
+            hin1[i] = __float_as_uint(src[(32 + i) * kN]);
           }
         } else {
-          // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
-          const float* src = p.slots + ((bh * 2 + ((c - 1) & 1)) * (kP / 4) * kN + r) * 4;
-          const unsigned long long w0 = global_ns();
-          int v;
-          for (uint32_t i = 0;; ++i) {
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + cur.pair) : "memory");
-            if (v >= c) break;
-            if ((i & 63u) == 63u) {
-              if (aborted(p.ctrl)) break;
-              if (global_ns() - w0 > kWaitNs) {
-                atomicOr(p.ctrl + 1, kErrLookback);
-                break;
-              }
-            }
-            __nanosleep(64);
-          }
-          load_slot_quads(hin0, src);
-          load_slot_quads(hin1, src + 8 * kN * 4);
-        }
-        tc::tmem_st32(T_Hr, hin0);
-        tc::tmem_st32(T_Hr + 32, hin1);
-      }
-
-      for (int sub = 0; sub < cur.nsub; ++sub, ++k) {
-        const uint32_t ph = k & 1;
-        const bool valid = sub * kSub + r < cur.nvalid;   // this row's token exists
-        // per-token scalars of the sub-step (positions past the end hold the
-        // chunk's last values)
-        const float* lv = s.lv[slot][e] + sub * kSub;
-        const int* sgv = s.segv[slot] + sub * kSub;
-        const float l_r = lv[r];
-        const float dt_r = s.dtv[slot][e][sub * kSub + r];
-        const int sg_r = p.has_seg ? sgv[r] : 0;
-        const float l_last = lv[kSub - 1];
-        const int sg_last = p.has_seg ? sgv[kSub - 1] : 0;
-        const float w_r = (valid && sg_r == sg_last) ? ex2(l_last - l_r) * dt_r : 0.f;
-        const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
-        if (!h_done) h_convert(sg_last == sg_prev ? ex2(l_last - l_prev) : 0.f);
-        h_done = false;
-
-        // ---- w o x_e for the row, while the [CB | Ye] chain runs
-        wait_or_flag(&s.full, ph, p.ctrl);   // x_e has landed
-        {
-          const unsigned char* xr = s.X[e] + r * 128;
-          unsigned char* wr = s.XW[e] + r * 128;
-          const uint64_t w2 = pk2(w_r, w_r);
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
-            const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
-            uint4 o;
-            o.x = f2_to_bf2(mul2(bf2_to_f2(xv.x), w2));
-            o.y = f2_to_bf2(mul2(bf2_to_f2(xv.y), w2));
-            o.z = f2_to_bf2(mul2(bf2_to_f2(xv.z), w2));
-            o.w = f2_to_bf2(mul2(bf2_to_f2(xv.w), w2));
-            *reinterpret_cast<uint4*>(wr + off) = o;
+          for (int i = 0; i < 32; ++i) hin0[i] = hin1[i] = 0u;
+        }
+      } else {
+        // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
+        const float* src = p.slots + ((bh * 2 + ((it.c - 1) & 1)) * (kP / 4) * kN + r) * 4;
+        const unsigned long long w0 = global_ns();
+        int v;
+        for (uint32_t i = 0;; ++i) {
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + it.pair) : "memory");
+          if (v >= it.c) break;
+          if ((i & 63u) == 63u) {
+            if (aborted(p.ctrl)) break;
+            if (global_ns() - w0 > kWaitNs) {
+              atomicOr(p.ctrl + 1, kErrLookback);
+              break;
+            }
+          }
+          __nanosleep(64);
+        }
+        load_slot_quads(hin0, src);
+        load_slot_quads(hin1, src + 8 * kN * 4);
+      }
+      tc::tmem_st32(T_Hr, hin0);
+      tc::tmem_st32(T_Hr + 32, hin1);
+    };
+    // per-row scalars of a step (positions past the end hold the chunk's last values)
+    struct RowV {
+      float l_r, l_last, dt_r;
+      int sg_r, sg_last;
+    };
+    auto row_of = [&](int slot, int sub) {
+      RowV v;
+      const float* lv = s.lv[slot][e] + sub * kSub;
+      const int* sgv = s.segv[slot] + sub * kSub;
+      v.l_r = lv[r];
+      v.l_last = lv[kSub - 1];
+      v.dt_r = s.dtv[slot][e][sub * kSub + r];
+      v.sg_r = p.has_seg ? sgv[r] : 0;
+      v.sg_last = p.has_seg ? sgv[kSub - 1] : 0;
+      return v;
+    };
+    // w_r = exp(cs_last - cs_r) dt_r: row r's weight in the step's own state
+    auto w_of = [&](const RowV& v, int sub, int nvalid) {
+      const bool valid = sub * kSub + r < nvalid;   // this row's token exists
+      return (valid && v.sg_r == v.sg_last) ? ex2(v.l_last - v.l_r) * v.dt_r : 0.f;
+    };
+
+    int u = 0, slot = 0, sub = 0;
+    wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+    bool live = s.tk[0] < p.items && !aborted(p.ctrl);
+    float l_prev = 0.f;   // l and reset count where the previous sub-step of the
+    int sg_prev = 0;      // chunk ended (0 at a chunk start: the cumsum restarts)
+    if (live) {           // step 0: entering state, h and w o x
+      const Unit& it = s.uk[0];
+      load_hin(it);
+      const RowV v = row_of(0, 0);
+      h_convert(v.sg_last == 0 ? ex2(v.l_last) : 0.f);
+      wait_or_flag(&s.xfull, 0, p.ctrl);
+      wx(w_of(v, 0, it.nvalid), 0);
+      tc::fence_proxy_async_smem();   // h and w o x for the MMAs
+      tc::fence_before_sync();
+      tc::mbar_arrive(&s.hx_ready);
+    }
+    for (uint32_t k = 0; live; ++k) {
+      const uint32_t ph = k & 1, bc = k & 1;
+      const Unit& cur = s.uk[slot];
+      const RowV v = row_of(slot, sub);
+      const float l_r = v.l_r;
+      const int sg_r = v.sg_r;
+      const float Dh = s.dk[slot][e];
+      const float* lv = s.lv[slot][e] + sub * kSub;
+      const int* sgv = s.segv[slot] + sub * kSub;
+      const uint32_t T_CBr = T_R(bc);              // CB_k row r
+      const uint32_t T_Mr = T_R(bc ^ 1) + e * kP;  // M_e row r (bf16 pairs)
+
+      // ---- M_e = CB o decay into T_M, the live 32-column blocks 0..qr of
+      // this row; the blocks above the diagonal are zeroed (the region held
+      // Yi of step k-1).  Below the diagonal block the decay factors as
+      // exp2(l_r - l_f) * [exp2(l_f - l_j) dt_j] with f the block's last
+      // column (both <= 1); the diagonal block takes one exp2 per element.
+      // The D skip rides on the diagonal: M_rr += D, so that M x includes
+      // D x_r.  Masks are selects.
+      wait_or_flag(&s.cb, ph, p.ctrl);
+      tc::fence_after_sync();
+      const float* mcol = s.mv[slot][e] + sub * kSub;
+      const float* bcol = s.bv[slot][e] + sub * kSub;
+#pragma unroll 1
+      for (int qc = 0; qc <= qr; ++qc) {
+        const bool diag = qc == qr;
+        const int c0 = qc * 32;
+        uint32_t v[32];
+        tc::tmem_ld32(T_CBr + c0, v);
+        const float arow = diag ? 0.f : ex2(l_r - lv[c0 + 31]);
+        float colv[32];
+        const float4* cp4 = reinterpret_cast<const float4*>((diag ? mcol : bcol) + c0);
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) {
+          const float4 f = cp4[v4];
+          colv[4 * v4] = f.x;
+          colv[4 * v4 + 1] = f.y;
+          colv[4 * v4 + 2] = f.z;
+          colv[4 * v4 + 3] = f.w;
+        }
+        tc::tmem_ld_wait_regs(v);
+        float m[32];
+        if (diag) {
+          const uint64_t lr2 = pk2(l_r, l_r), neg2 = pk2(-1.f, -1.f);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 d = up2(fma2(pk2(colv[i], colv[i + 1]), neg2, lr2));   // l_r - mcol
+            const float2 val = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                        pk2(ex2(d.x), ex2(d.y))));
+            m[i] = (c0 + i < r) ? val.x : (c0 + i == r ? val.x + Dh : 0.f);
+            m[i + 1] = (c0 + i + 1 < r) ? val.y : (c0 + i + 1 == r ? val.y + Dh : 0.f);
+          }
+        } else {
+          const uint64_t a2 = pk2(arow, arow);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 mm = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                       mul2(pk2(colv[i], colv[i + 1]), a2)));
+            m[i] = mm.x;
+            m[i + 1] = mm.y;
           }
         }
-
-        // ---- M_e = CB o decay into T_M, the live 32-column blocks 0..qr of
-        // this row (the blocks above the diagonal were zeroed once).  Below
-        // the diagonal block the decay factors as exp2(l_r - l_f) *
-        // [exp2(l_f - l_j) dt_j] with f the block's last column (both <= 1);
-        // the diagonal block takes one exp2 per element.  The D skip rides on
-        // the diagonal: M_rr += D, so that M x includes D x_r.  Masks are selects.
-        wait_or_flag(&s.cb, ph, p.ctrl);
-        tc::fence_after_sync();
-        const float* mcol = s.mv[slot][e] + sub * kSub;
-        const float* bcol = s.bv[slot][e] + sub * kSub;
-#pragma unroll 1
-        for (int qc = 0; qc <= qr; ++qc) {
-          const bool diag = qc == qr;
-          const int c0 = qc * 32;
-          uint32_t v[32];
-          tc::tmem_ld32(T_CBr + c0, v);
-          const float arow = diag ? 0.f : ex2(l_r - lv[c0 + 31]);
-          float colv[32];
-          const float4* cp4 = reinterpret_cast<const float4*>((diag ? mcol : bcol) + c0);
+        if (p.has_seg) {   // a reset between j and r zeroes the entry
+          const int4* sp4 = reinterpret_cast<const int4*>(sgv + c0);
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 f = cp4[v4];
-            colv[4 * v4] = f.x;
-            colv[4 * v4 + 1] = f.y;
-            colv[4 * v4 + 2] = f.z;
-            colv[4 * v4 + 3] = f.w;
+            const int4 f = sp4[v4];
+            m[4 * v4] = f.x == sg_r ? m[4 * v4] : 0.f;
+            m[4 * v4 + 1] = f.y == sg_r ? m[4 * v4 + 1] : 0.f;
+            m[4 * v4 + 2] = f.z == sg_r ? m[4 * v4 + 2] : 0.f;
+            m[4 * v4 + 3] = f.w == sg_r ? m[4 * v4 + 3] : 0.f;
           }
-          tc::tmem_ld_wait_regs(v);
-          float m[32];
-          if (diag) {
-            const uint64_t lr2 = pk2(l_r, l_r), neg2 = pk2(-1.f, -1.f);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 d = up2(fma2(pk2(colv[i], colv[i + 1]), neg2, lr2));   // l_r - mcol
-              const float2 val = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
-                                          pk2(ex2(d.x), ex2(d.y))));
-              m[i] = (c0 + i < r) ? val.x : (c0 + i == r ? val.x + Dh : 0.f);
-              m[i + 1] = (c0 + i + 1 < r) ? val.y : (c0 + i + 1 == r ? val.y + Dh : 0.f);
-            }
-          } else {
-            const uint64_t a2 = pk2(arow, arow);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 mm = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
-                                         mul2(pk2(colv[i], colv[i + 1]), a2)));
-              m[i] = mm.x;
-              m[i + 1] = mm.y;
-            }
-          }
-          if (p.has_seg) {   // a reset between j and r zeroes the entry
-            const int4* sp4 = reinterpret_cast<const int4*>(sgv + c0);
-#pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) {
-              const int4 f = sp4[v4];
-              m[4 * v4] = f.x == sg_r ? m[4 * v4] : 0.f;
-              m[4 * v4 + 1] = f.y == sg_r ? m[4 * v4 + 1] : 0.f;
-              m[4 * v4 + 2] = f.z == sg_r ? m[4 * v4 + 2] : 0.f;
-              m[4 * v4 + 3] = f.w == sg_r ? m[4 * v4 + 3] : 0.f;
-            }
-          }
-          uint32_t packed[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
-          tc::tmem_st16(T_Mr + (c0 >> 1), packed);
         }
-        tc::tmem_st_wait();
-        tc::fence_proxy_async_smem();   // w o x for the state chain
-        tc::fence_before_sync();
-        tc::mbar_arrive(&s.m_ready);
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
+        tc::tmem_st16(T_Mr + (c0 >> 1), packed);
+      }
+      {
+        uint32_t zero[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) zero[i] = 0u;
+#pragma unroll 1
+        for (int qc = qr + 1; qc < 4; ++qc) tc::tmem_st16(T_Mr + qc * 16, zero);
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&s.m_ready);
 
-        // ---- epilogue: out_e = (Yi_e + rho Ye_e) * silu(z_e), written over
-        // z_e in Z (warp 0 stores the tile); Yi_e is committed on its own, so
-        // head 0 starts while Yi_1 and the state chain run
-        wait_or_flag(&s.yi_done[e], ph, p.ctrl);
-        if (p.z) wait_or_flag(&s.zfull, ph, p.ctrl);
-        tc::fence_after_sync();
-        {
-          unsigned char* zrow = s.Z[e] + r * 128;
-          const uint64_t rho2 = pk2(rho_r, rho_r), half2 = pk2(0.5f, 0.5f);
+      // ---- the next step: the unit's next sub-step or the next unit's first
+      int nslot = slot, nsb = sub + 1;
+      bool has_next = true;
+      if (nsb == cur.nsub) {
+        nslot = (u + 1) % kRing;
+        wait_or_flag(&s.tk_full[nslot], ((u + 1) / kRing) & 1, p.ctrl);
+        has_next = s.tk[nslot] < p.items && !aborted(p.ctrl);
+        nsb = 0;
+      }
+      const Unit& nxt = s.uk[nslot];
+      const bool seg_end = sub == cur.nsub - 1 && cur.j == cur.nch - 1;
+      const float lp_n = nsb == 0 ? 0.f : v.l_last;
+      const int sp_n = nsb == 0 ? 0 : v.sg_last;
+      RowV vn = v;
+      float carry_n = 0.f;
+      if (has_next) {
+        vn = row_of(nslot, nsb);
+        carry_n = vn.sg_last == sp_n ? ex2(vn.l_last - lp_n) : 0.f;
+      }
+
+      // ---- once step k's state chain is done: a segment's final states are
+      // handed on (or written out); otherwise step k+1's h and carried state,
+      // while the Yi MMAs run
+      wait_or_flag(&s.y_done, ph, p.ctrl);
+      tc::fence_after_sync();
+      if (seg_end) {
+        const int64_t bh = (int64_t)cur.b * p.H + cur.h0 + e;
+        const bool last_chunk = cur.c == p.nc - 1;
+        if (!last_chunk || p.final_states) {
 #pragma unroll
           for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
-            uint32_t yi[16], ye[16];
-            tc::tmem_ld16(T_YIr + qd * 16, yi);
-            tc::tmem_ld16(T_YEr + qd * 16, ye);
-            tc::tmem_ld_wait_regs(yi);
-            tc::tmem_ld_wait_regs(ye);
+            uint32_t hv[16];
+            tc::tmem_ld16(T_Hr + qd * 16, hv);
+            tc::tmem_ld_wait_regs(hv);
+            if (last_chunk) {
+              float* dst = p.final_states + bh * kP * kN + r;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int ch = qd * 2 + cc;
-              uint4* zp = reinterpret_cast<uint4*>(zrow + ((ch ^ (r & 7)) << 4));
-              const uint4 zv = p.z ? *zp : make_uint4(0u, 0u, 0u, 0u);
-              const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
-              uint32_t o[4];
+              for (int i = 0; i < 16; ++i) dst[(qd * 16 + i) * kN] = __uint_as_float(hv[i]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(p.slots) +
+                           ((bh * 2 + (cur.c & 1)) * (kP / 4) + qd * 4) * kN + r;
 #pragma unroll
-              for (int u4 = 0; u4 < 4; ++u4) {
-                const int i = cc * 8 + u4 * 2;
-                uint64_t y = fma2(rho2, pk2(__uint_as_float(ye[i]), __uint_as_float(ye[i + 1])),
-                                  pk2(__uint_as_float(yi[i]), __uint_as_float(yi[i + 1])));
-                if (p.z) {   // silu(z) = z (1 + tanh(z/2)) / 2
-                  const uint64_t hz = mul2(bf2_to_f2(zw[u4]), half2);
-                  const float2 h = up2(hz);
-                  y = mul2(y, fma2(hz, pk2(tanh_fast(h.x), tanh_fast(h.y)), hz));
-                }
-                o[u4] = f2_to_bf2(y);
-              }
-              *zp = make_uint4(o[0], o[1], o[2], o[3]);
+              for (int v4 = 0; v4 < 4; ++v4)
+                dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
             }
           }
         }
-        tc::fence_proxy_async_smem();   // out for warp 0's TMA store
-        tc::fence_before_sync();
-        tc::mbar_arrive(&s.tmem_free);  // Yi / Ye read out, out written
-
-        // ---- once the MMAs are done: a segment's final states are handed on
-        // (or written out); otherwise the next sub-step's entering state is
-        // converted now, so that its [CB | Ye] chain can start right after
-        // this epilogue
-        wait_or_flag(&s.y_done, ph, p.ctrl);
-        tc::fence_after_sync();
-        if (sub == cur.nsub - 1 && j == cur.nch - 1) {
-          const bool last_chunk = c == p.nc - 1;
-          if (!last_chunk || p.final_states) {
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
-              uint32_t hv[16];
-              tc::tmem_ld16(T_Hr + qd * 16, hv);
-              tc::tmem_ld_wait_regs(hv);
-              if (last_chunk) {
-                float* dst = p.final_states + bh * kP * kN + r;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) dst[(qd * 16 + i) * kN] = __uint_as_float(hv[i]);
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(p.slots) +
-                             ((bh * 2 + (c & 1)) * (kP / 4) + qd * 4) * kN + r;
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                  dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
-              }
-            }
-          }
-          if (!last_chunk) tc::mbar_arrive(&s.pub);   // warp 0 raises the flag
-        } else {
-          // the next sub-step: the next 128 tokens of this chunk, or the first
-          // of the segment's next chunk (its cumsum starts again at 0)
-          const float* lvn;
-          const int* sgvn;
-          float lp = l_last;
-          int sp = sg_last;
-          if (sub + 1 < cur.nsub) {
-            lvn = lv + kSub;
-            sgvn = sgv + kSub;
-          } else {
-            const int ns = (u + 1) % kRing;
-            wait_or_flag(&s.tk_full[ns], ((u + 1) / kRing) & 1, p.ctrl);
-            lvn = s.lv[ns][e];
-            sgvn = s.segv[ns];
-            lp = 0.f;
-            sp = 0;
-          }
-          const int sgn = p.has_seg ? sgvn[kSub - 1] : 0;
-          h_convert(sgn == sp ? ex2(lvn[kSub - 1] - lp) : 0.f);
-          h_done = true;
-        }
-        l_prev = l_last;
-        sg_prev = sg_last;
+        if (!last_chunk) tc::mbar_arrive(&s.pub);   // warp 0 raises the flag
+      } else if (has_next) {
+        h_convert(carry_n);
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&s.tk_empty[slot]);   // this unit's vectors are read
+
+      // ---- epilogue: out_e = (Yi_e + rho Ye_e) * silu(z_e), written over
+      // z_e in Z (warp 0 stores the tile); Yi_e is committed on its own, so
+      // head 0 starts while Yi_1 runs
+      {
+        const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
+        wait_or_flag(&s.yi_done[e], ph, p.ctrl);
+        wait_or_flag(&s.zfull, ph, p.ctrl);
+        tc::fence_after_sync();
+        const uint32_t T_YIr = T_R(bc) + e * kP;
+        unsigned char* zrow = s.Z[e] + r * 128;
+        const uint64_t rho2 = pk2(rho_r, rho_r), half2 = pk2(0.5f, 0.5f);
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+          uint32_t yi[16], ye[16];
+          tc::tmem_ld16(T_YIr + qd * 16, yi);
+          tc::tmem_ld16(T_YEr + qd * 16, ye);
+          tc::tmem_ld_wait_regs(yi);
+          tc::tmem_ld_wait_regs(ye);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int ch = qd * 2 + cc;
+            uint4* zp = reinterpret_cast<uint4*>(zrow + ((ch ^ (r & 7)) << 4));
+            const uint4 zv = p.z ? *zp : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+              const int i = cc * 8 + u4 * 2;
+              uint64_t y = fma2(rho2, pk2(__uint_as_float(ye[i]), __uint_as_float(ye[i + 1])),
+                                pk2(__uint_as_float(yi[i]), __uint_as_float(yi[i + 1])));
+              if (p.z) {   // silu(z) = z (1 + tanh(z/2)) / 2
+                const uint64_t hz = mul2(bf2_to_f2(zw[u4]), half2);
+                const float2 h = up2(hz);
+                y = mul2(y, fma2(hz, pk2(tanh_fast(h.x), tanh_fast(h.y)), hz));
+              }
+              o[u4] = f2_to_bf2(y);
+            }
+            *zp = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+      tc::fence_proxy_async_smem();   // out for warp 0's TMA store
+      tc::fence_before_sync();
+      tc::mbar_arrive(&s.out_ready);  // Yi / Ye read out, out written
+      if (nsb == 0) {                 // this unit's vectors are read
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&s.tk_empty[slot]);
+      }
+      if (!has_next) break;
+
+      // ---- step k+1: a new segment's entering state; then w o x
+      if (seg_end) {
+        load_hin(nxt);
+        h_convert(carry_n);
+      }
+      wait_or_flag(&s.xfull, ph ^ 1, p.ctrl);
+      wx(w_of(vn, nsb, nxt.nvalid), bc ^ 1);
+      tc::fence_proxy_async_smem();   // h and w o x for the MMAs
+      tc::fence_before_sync();
+      tc::mbar_arrive(&s.hx_ready);
+      if (nsb == 0) {
+        ++u;
+        slot = nslot;
+        l_prev = 0.f;
+        sg_prev = 0;
+      } else {
+        l_prev = v.l_last;
+        sg_prev = v.sg_last;
+      }
+      sub = nsb;
     }
   }
 
