@@ -9,16 +9,17 @@
 // an item's predecessor (previous segment, same pair) always holds an
 // earlier ticket; the state stays in TMEM across the segment's chunks.
 // Warp roles:
-//   warp 10   takes the tickets and, one chunk ("unit") ahead, computes the
+//   warp 18   takes the tickets and, one chunk ("unit") ahead, computes the
 //             per-token vectors (dt = softplus(dt_raw + dt_bias) clamped, the
 //             cumsum of dt*A per head, the decay-matrix column factors, the
 //             reset counts of seq_idx) into a three-slot ring
 //   warp 0    lane 0 issues the TMA loads (C, B, x, z) and out stores and
 //             raises the hand-off flag after a segment
 //   warp 1    lane 0 issues the tcgen05 MMAs
-//   warps 2-9 four per head (one per TMEM lane quarter): decay matrix,
-//             state moves, epilogue; they never wait for one another (every
-//             thread arrives on the mbarriers its consumers wait on)
+//   warps 2-17  eight per head, one per TMEM lane quarter and headdim half
+//             (four per SM sub-partition): decay matrix, state moves,
+//             epilogue; they never wait for one another (every thread
+//             arrives on the mbarriers its consumers wait on)
 // A chunk is processed as 128-token sub-steps; per sub-step k, with rows /
 // columns = the sub-step's tokens, cs the chunk's cumsum and h_e the state
 // entering the sub-step (head e = 0, 1):
@@ -59,7 +60,11 @@ constexpr int kQmax = 256;  // largest chunk
 constexpr int kRing = 3;    // units whose tickets / vectors are published
 constexpr int kNH = 2;      // heads per item
 constexpr int kComputeWarp0 = 2;        // warps 0 (TMA) and 1 (MMA) come first, then compute
-constexpr int kComputeThreads = 128 * kNH;   // one warp per head and TMEM lane quarter
+constexpr int kHalves = 2;              // compute warps per head and TMEM lane quarter
+constexpr int kPW = kP / kHalves;       // headdim columns of one compute warp
+// one warp per head, headdim half and TMEM lane quarter: four per SM
+// sub-partition, so that each one's latency-bound phases overlap
+constexpr int kComputeThreads = 128 * kNH * kHalves;
 constexpr int kVecWarp = kComputeWarp0 + kComputeThreads / 32;   // tickets and vectors
 constexpr int kThreads = (kVecWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -357,11 +362,11 @@ __device__ __forceinline__ float silu(float v) {
   return fmaf(hv, tanh_fast(hv), hv);
 }
 
-// Eight column quads of one row (dstate index) of a handed-on state; quads
+// Four column quads of one row (dstate index) of a handed-on state; quads
 // are kN * 4 floats apart, so that a warp's 32 rows of one quad are contiguous.
-__device__ __forceinline__ void load_slot_quads(uint32_t (&hv)[32], const float* src) {
+__device__ __forceinline__ void load_slot_quads(uint32_t (&hv)[16], const float* src) {
 #pragma unroll
-  for (int v4 = 0; v4 < 8; ++v4)
+  for (int v4 = 0; v4 < 4; ++v4)
     asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(hv[4 * v4]), "=r"(hv[4 * v4 + 1]), "=r"(hv[4 * v4 + 2]), "=r"(hv[4 * v4 + 3])
                  : "l"(src + (int64_t)v4 * kN * 4)
@@ -619,21 +624,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- compute: warp (head e, quarter qr) owns row r = 32 qr
-    // + lane of head e's TMEM tiles and of the sub-step's smem tiles.  Per
+    // ---------------- compute: warp (head e, half hf, quarter qr) owns row
+    // r = 32 qr + lane of head e's TMEM tiles and of the sub-step's smem
+    // tiles, headdim columns p0 .. p0 + 31 (and columns 16 hf .. 16 hf + 15 of
+    // every 32-column block of the decay matrix).  Per
     // step k: M_e (needs CB_k) -> h and the carried state of step k+1 (needs
     // step k's state chain; the Yi MMAs run meanwhile) -> epilogue of step k
     // -> w o x_e of step k+1.  At the end of a segment the final state is
     // handed on first and the next segment's entering state is loaded after
     // the epilogue.
     const int cw = warp - kComputeWarp0;
-    const int e = cw >> 2;                        // head of the pair
+    const int e = cw >> 3;                        // head of the pair
+    const int hf = (cw >> 2) & 1;                 // half: headdim columns / decay-block columns
+    const int p0 = hf * kPW;                      // first headdim column of this warp
     const int qr = warp & 3;                      // TMEM lane quarter
     const int r = qr * 32 + lane;                 // row: token (or dstate index)
     const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
     auto T_R = [&](uint32_t b) { return tmem + kT_R0 + b * (kT_R1 - kT_R0) + lane_addr; };
-    const uint32_t T_YEr = tmem + kT_YE + e * kP + lane_addr;
-    const uint32_t T_Hr = tmem + kT_H + e * kP + lane_addr;
+    const uint32_t T_YEr = tmem + kT_YE + e * kP + p0 + lane_addr;
+    const uint32_t T_Hr = tmem + kT_H + e * kP + p0 + lane_addr;
     // entering-state rows of the [B^T | h] operand for this thread: dstate
     // index r is K; headdim p of head e is row 128 + 64 e + p of r's half
     unsigned char* hk = s.BH + (r >> 6) * kBhHalf + (128 + e * kP) * 128 + (r & 7) * 2;
@@ -644,13 +653,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t carry2 = pk2(carry, carry);
       tc::tmem_st_wait();   // the entering state's stores (segment start)
 #pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+      for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 columns at a time
         uint32_t hv[16];
         tc::tmem_ld16(T_Hr + qd * 16, hv);
         tc::tmem_ld_wait_regs(hv);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int pcol = qd * 16 + i;   // headdim p: row 128 + 64 e + p, swizzle phase p % 8
+          const int pcol = p0 + qd * 16 + i;   // headdim p: row 128 + 64 e + p, swizzle phase p % 8
           const __nv_bfloat16 hb = __float2bfloat16_rn(__uint_as_float(hv[i]));
           *reinterpret_cast<__nv_bfloat16*>(hk + pcol * 128 + ((kchunk ^ (pcol & 7)) << 4)) = hb;
         }
@@ -671,7 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char* wr = s.XB[xb ^ 1][e] + r * 128;
       const uint64_t w2 = pk2(w_r, w_r);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int c8 = 0; c8 < kPW / 8; ++c8) {   // 16-byte chunks of this warp's columns
+        const int ch = p0 / 8 + c8;
         const uint32_t off = (uint32_t)((ch ^ (r & 7)) << 4);
         const uint4 xv = *reinterpret_cast<const uint4*>(xr + off);
         uint4 o;
@@ -688,22 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // heads' slots are written)
     auto load_hin = [&](const Unit& it) {
       const int64_t bh = (int64_t)it.b * p.H + it.h0 + e;
-      uint32_t hin0[32], hin1[32];   // headdim columns 0-31 and 32-63
-      if (it.c == 0) {
-        if (p.init) {
-          const float* src = p.init + bh * kP * kN + r;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            hin0[i] = __float_as_uint(src[i * kN]);
-            hin1[i] = __float_as_uint(src[(32 + i) * kN]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) hin0[i] = hin1[i] = 0u;
-        }
-      } else {
-        // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
-        const float* src = p.slots + ((bh * 2 + ((it.c - 1) & 1)) * (kP / 4) * kN + r) * 4;
+      // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
+      const float* slot_src = p.slots + ((bh * 2 + ((it.c - 1) & 1)) * (kP / 4) * kN + r) * 4;
+      if (it.c > 0) {
         const unsigned long long w0 = global_ns();
         int v;
         for (uint32_t i = 0;; ++i) {
@@ -718,11 +715,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __nanosleep(64);
         }
-        load_slot_quads(hin0, src);
-        load_slot_quads(hin1, src + 8 * kN * 4);
       }
-      tc::tmem_st32(T_Hr, hin0);
-      tc::tmem_st32(T_Hr + 32, hin1);
+#pragma unroll
+      for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 headdim columns at a time
+        const int pc = p0 + qd * 16;
+        uint32_t hv[16];
+        if (it.c > 0) {
+          load_slot_quads(hv, slot_src + (int64_t)(pc / 4) * kN * 4);
+        } else if (p.init) {
+          const float* src = p.init + bh * kP * kN + r;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hv[i] = __float_as_uint(src[(pc + i) * kN]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hv[i] = 0u;
+        }
+        tc::tmem_st16(T_Hr + qd * 16, hv);
+      }
     };
     // per-row scalars of a step (positions past the end hold the chunk's last values)
     struct RowV {
@@ -788,14 +797,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int qc = 0; qc <= qr; ++qc) {
         const bool diag = qc == qr;
-        const int c0 = qc * 32;
-        uint32_t v[32];
-        tc::tmem_ld32(T_CBr + c0, v);
-        const float arow = diag ? 0.f : ex2(l_r - lv[c0 + 31]);
-        float colv[32];
+        const int c0 = qc * 32 + hf * 16;   // this warp's 16 columns of the block
+        uint32_t v[16];
+        tc::tmem_ld16(T_CBr + c0, v);
+        const float arow = diag ? 0.f : ex2(l_r - lv[qc * 32 + 31]);
+        float colv[16];
         const float4* cp4 = reinterpret_cast<const float4*>((diag ? mcol : bcol) + c0);
 #pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4) {
+        for (int v4 = 0; v4 < 4; ++v4) {
           const float4 f = cp4[v4];
           colv[4 * v4] = f.x;
           colv[4 * v4 + 1] = f.y;
@@ -803,11 +812,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           colv[4 * v4 + 3] = f.w;
         }
         tc::tmem_ld_wait_regs(v);
-        float m[32];
+        float m[16];
         if (diag) {
           const uint64_t lr2 = pk2(l_r, l_r), neg2 = pk2(-1.f, -1.f);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
+          for (int i = 0; i < 16; i += 2) {
             const float2 d = up2(fma2(pk2(colv[i], colv[i + 1]), neg2, lr2));   // l_r - mcol
             const float2 val = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
                                         pk2(ex2(d.x), ex2(d.y))));
@@ -817,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const uint64_t a2 = pk2(arow, arow);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
+          for (int i = 0; i < 16; i += 2) {
             const float2 mm = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
                                        mul2(pk2(colv[i], colv[i + 1]), a2)));
             m[i] = mm.x;
@@ -827,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.has_seg) {   // a reset between j and r zeroes the entry
           const int4* sp4 = reinterpret_cast<const int4*>(sgv + c0);
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4) {
+          for (int v4 = 0; v4 < 4; ++v4) {
             const int4 f = sp4[v4];
             m[4 * v4] = f.x == sg_r ? m[4 * v4] : 0.f;
             m[4 * v4 + 1] = f.y == sg_r ? m[4 * v4 + 1] : 0.f;
@@ -835,17 +844,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             m[4 * v4 + 3] = f.w == sg_r ? m[4 * v4 + 3] : 0.f;
           }
         }
-        uint32_t packed[16];
+        uint32_t packed[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
-        tc::tmem_st16(T_Mr + (c0 >> 1), packed);
+        for (int i = 0; i < 8; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
+        tc::tmem_st8(T_Mr + (c0 >> 1), packed);
       }
       {
-        uint32_t zero[16];
+        uint32_t zero[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) zero[i] = 0u;
+        for (int i = 0; i < 8; ++i) zero[i] = 0u;
 #pragma unroll 1
-        for (int qc = qr + 1; qc < 4; ++qc) tc::tmem_st16(T_Mr + qc * 16, zero);
+        for (int qc = qr + 1; qc < 4; ++qc) tc::tmem_st8(T_Mr + ((qc * 32 + hf * 16) >> 1), zero);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -881,17 +890,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool last_chunk = cur.c == p.nc - 1;
         if (!last_chunk || p.final_states) {
 #pragma unroll
-          for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+          for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 columns at a time
+            const int pc = p0 + qd * 16;
             uint32_t hv[16];
             tc::tmem_ld16(T_Hr + qd * 16, hv);
             tc::tmem_ld_wait_regs(hv);
             if (last_chunk) {
               float* dst = p.final_states + bh * kP * kN + r;
 #pragma unroll
-              for (int i = 0; i < 16; ++i) dst[(qd * 16 + i) * kN] = __uint_as_float(hv[i]);
+              for (int i = 0; i < 16; ++i) dst[(pc + i) * kN] = __uint_as_float(hv[i]);
             } else {
               uint4* dst = reinterpret_cast<uint4*>(p.slots) +
-                           ((bh * 2 + (cur.c & 1)) * (kP / 4) + qd * 4) * kN + r;
+                           ((bh * 2 + (cur.c & 1)) * (kP / 4) + pc / 4) * kN + r;
 #pragma unroll
               for (int v4 = 0; v4 < 4; ++v4)
                 dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
@@ -911,11 +921,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_or_flag(&s.yi_done[e], ph, p.ctrl);
         wait_or_flag(&s.zfull, ph, p.ctrl);
         tc::fence_after_sync();
-        const uint32_t T_YIr = T_R(bc) + e * kP;
+        const uint32_t T_YIr = T_R(bc) + e * kP + p0;
         unsigned char* zrow = s.Z[e] + r * 128;
         const uint64_t rho2 = pk2(rho_r, rho_r), half2 = pk2(0.5f, 0.5f);
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {   // 16 columns at a time
+        for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 columns at a time
           uint32_t yi[16], ye[16];
           tc::tmem_ld16(T_YIr + qd * 16, yi);
           tc::tmem_ld16(T_YEr + qd * 16, ye);
@@ -923,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld_wait_regs(ye);
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            const int ch = qd * 2 + cc;
+            const int ch = p0 / 8 + qd * 2 + cc;
             uint4* zp = reinterpret_cast<uint4*>(zrow + ((ch ^ (r & 7)) << 4));
             const uint4 zv = p.z ? *zp : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
