@@ -177,17 +177,19 @@ __device__ __forceinline__ bool aborted(const int* ctrl) {
 }
 
 // Bounded wait on an mbarrier phase: gives up after kWaitNs (or at once when
-// the launch has already been aborted) and records the error.
-__device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, int* ctrl) {
-  if (tc::mbar_try_wait(bar, parity)) return;
+// the launch has already been aborted) and records the error.  Returns
+// whether the phase completed, so that a loop can stop after a failed wait
+// without reading the error word on its fast path.
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int* ctrl) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
-    if (tc::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return;
+    if (tc::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if ((i & 15u) == 0) {
-      if (aborted(ctrl)) return;
+      if (aborted(ctrl)) return false;
       if (global_ns() - t0 > kWaitNs) {
         atomicOr(ctrl + 1, kErrBarrier);
-        return;
+        return false;
       }
     }
   }
@@ -211,10 +213,13 @@ struct VecRaw {
   float2 dt[8];
   int sq[9];   // seq_idx at positions lane E - 1 .. lane E + 7 (-1: none)
   float a[kNH], bias[kNH];   // A log2(e) and dt_bias of the two heads
+  float d[kNH];              // D of the two heads (0 without D)
 };
 
 __device__ __forceinline__ void vec_load(const Params& p, const Unit& it, int lane, VecRaw& r) {
   const int E = p.Q / 32;
+#pragma unroll
+  for (int e = 0; e < kNH; ++e) r.d[e] = p.D ? p.D[it.h0 + e] : 0.f;
   if (p.dt_raw) {
 #pragma unroll
     for (int e = 0; e < kNH; ++e) {
@@ -431,9 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int u = 0, sub = 0;
       uint32_t npub = 0;
-      wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+      bool live = wait_or_flag(&s.tk_full[0], 0, p.ctrl);
       Unit cur = s.uk[0];
-      bool live = s.tk[0] < p.items && !aborted(p.ctrl);
+      live = live && s.tk[0] < p.items;
       tc::mbar_arrive(&s.tk_empty[0]);
       auto load_cbx = [&](const Unit& it, int sb, int xb) {
         const int tok = (int)(it.t0 + sb * kSub);
@@ -467,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool has_next = true;
         if (nsb == cur.nsub) {
           const int ns = (u + 1) % kRing;
-          wait_or_flag(&s.tk_full[ns], ((u + 1) / kRing) & 1, p.ctrl);
-          has_next = s.tk[ns] < p.items && !aborted(p.ctrl);
+          has_next = wait_or_flag(&s.tk_full[ns], ((u + 1) / kRing) & 1, p.ctrl);
+          has_next = has_next && s.tk[ns] < p.items;
           nxt = s.uk[ns];
           tc::mbar_arrive(&s.tk_empty[ns]);
           nsb = 0;
@@ -516,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t_cur < p.items) vec_load(p, decode(p, t_cur, 0), lane, raw);
     for (int u = 0;; ++u) {
       const int slot = u % kRing;
-      wait_or_flag(&s.tk_empty[slot], ((u / kRing) & 1) ^ 1, p.ctrl);
+      const bool ok = wait_or_flag(&s.tk_empty[slot], ((u / kRing) & 1) ^ 1, p.ctrl);
       if (t_cur < p.items)
         vec_compute(p, decode(p, t_cur, j_cur), raw, s.lv[slot], s.dtv[slot], s.mv[slot],
                     s.bv[slot], s.segv[slot], lane);
@@ -525,11 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t_cur < p.items) {
           const Unit uu = decode(p, t_cur, j_cur);
           s.uk[slot] = uu;
-          for (int e = 0; e < kNH; ++e) s.dk[slot][e] = p.D ? p.D[uu.h0 + e] : 0.f;
+          for (int e = 0; e < kNH; ++e) s.dk[slot][e] = raw.d[e];
         }
       }
       tc::mbar_arrive(&s.tk_full[slot]);
-      if (t_cur >= p.items || aborted(p.ctrl)) break;
+      if (t_cur >= p.items || !ok) break;
       if (j_cur + 1 < decode(p, t_cur, j_cur).nch) {   // the segment's next chunk
         ++j_cur;
       } else {                                          // the next item
@@ -570,9 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       int u = 0, sub = 0;
-      wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+      bool live = wait_or_flag(&s.tk_full[0], 0, p.ctrl);
       int nsub = s.uk[0].nsub;
-      bool live = s.tk[0] < p.items && !aborted(p.ctrl);
+      live = live && s.tk[0] < p.items;
       tc::mbar_arrive(&s.tk_empty[0]);
       if (live) {
         wait_or_flag(&s.cbfull, 0, p.ctrl);
@@ -607,9 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++sub == nsub) {
           ++u;
           const int ns = u % kRing;
-          wait_or_flag(&s.tk_full[ns], (u / kRing) & 1, p.ctrl);
+          live = wait_or_flag(&s.tk_full[ns], (u / kRing) & 1, p.ctrl);
           nsub = s.uk[ns].nsub;
-          live = s.tk[ns] < p.items && !aborted(p.ctrl);
+          live = live && s.tk[ns] < p.items;
           tc::mbar_arrive(&s.tk_empty[ns]);
           sub = 0;
         }
@@ -756,8 +761,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     int u = 0, slot = 0, sub = 0;
-    wait_or_flag(&s.tk_full[0], 0, p.ctrl);
-    bool live = s.tk[0] < p.items && !aborted(p.ctrl);
+    bool live = wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+    live = live && s.tk[0] < p.items;
     float l_prev = 0.f;   // l and reset count where the previous sub-step of the
     int sg_prev = 0;      // chunk ended (0 at a chunk start: the cumsum restarts)
     if (live) {           // step 0: entering state, h and w o x
@@ -865,8 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool has_next = true;
       if (nsb == cur.nsub) {
         nslot = (u + 1) % kRing;
-        wait_or_flag(&s.tk_full[nslot], ((u + 1) / kRing) & 1, p.ctrl);
-        has_next = s.tk[nslot] < p.items && !aborted(p.ctrl);
+        has_next = wait_or_flag(&s.tk_full[nslot], ((u + 1) / kRing) & 1, p.ctrl);
+        has_next = has_next && s.tk[nslot] < p.items;
         nsb = 0;
       }
       const Unit& nxt = s.uk[nslot];
