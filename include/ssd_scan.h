@@ -83,9 +83,9 @@ const char *ssd_last_error(void);
  * the workspace unused); otherwise the four stage kernels below.  The fused
  * kernel keeps each head pair's state on chip for a segment of consecutive
  * chunks and hands it on between segments; the segment length is chosen from
- * the shape (1 or 2 chunks) unless the environment variable
- * SSD_FUSED_SEGMENT_CHUNKS gives one (a tuning / test override; results
- * agree to rounding for every length). */
+ * the shape (the longest that leaves every SM about twelve work items) unless
+ * the environment variable SSD_FUSED_SEGMENT_CHUNKS gives one (a tuning /
+ * test override; results agree to rounding for every length). */
 size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
                                 int headdim, int dstate, int ngroups,
                                 int chunk_size, ssd_dtype_t dtype);

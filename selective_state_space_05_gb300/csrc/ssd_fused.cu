@@ -75,6 +75,12 @@ constexpr uint32_t kSleepHintNs = 20000;                 // suspend hint of one 
 // sub-step (CB_k then Yi_0 | Yi_1 over it in R[k%2], M_0 | M_1 in R[(k+1)%2]),
 // [Ye_0 | Ye_1], [H_0 | H_1]
 constexpr uint32_t kT_R0 = 0, kT_YE = 128, kT_R1 = 256, kT_H = 384;
+// M_e column placement (bf16 pairs, 64 columns per head): the 16 tokens
+// 16 h .. 16 h + 15 (h = 0..7, one K step of Yi_e) sit at column
+// 32 (h % 2) + 8 (h / 2), so that the compute warp of headdim half hf, which
+// builds the half-blocks h % 2 == hf, writes only the 32 columns of the
+// region from which it read its own Yi_e half of the previous step
+__host__ __device__ constexpr uint32_t m_col(int h) { return 32 * (h & 1) + 8 * (h >> 1); }
 
 // error bits in the control block word ctrl[1]; once one is set every later
 // wait of the launch returns at once, so a broken launch still ends quickly
@@ -605,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < kNH; ++e) {    // Yi_e = M_e x_e (M holds the D skip), K = tokens
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            tc::mma_ts(TR(bc) + e * kP, TR(bc ^ 1) + e * kP + kk * 8,
+            tc::mma_ts(TR(bc) + e * kP, TR(bc ^ 1) + e * kP + m_col(kk),
                        dX + (bc * kNH + e) * kXTile + kk * 128, id_y, kk > 0);
           tc::mma_commit(&s.yi_done[e]);   // head e's epilogue may start
         }
@@ -852,14 +858,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t packed[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
-        tc::tmem_st8(T_Mr + (c0 >> 1), packed);
+        tc::tmem_st8(T_Mr + m_col(2 * qc + hf), packed);
       }
       {
         uint32_t zero[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) zero[i] = 0u;
 #pragma unroll 1
-        for (int qc = qr + 1; qc < 4; ++qc) tc::tmem_st8(T_Mr + ((qc * 32 + hf * 16) >> 1), zero);
+        for (int qc = qr + 1; qc < 4; ++qc) tc::tmem_st8(T_Mr + m_col(2 * qc + hf), zero);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -1108,14 +1114,15 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.Q = d.chunk;
   p.nc = d.nchunks;
   // chunks per work item: the state stays in TMEM across a segment and is
-  // handed on only between segments; segments stay short enough that every
-  // SM gets several items (dynamic scheduling evens out the tail).  Two
-  // chunks measured best on the 2.7B shape (1: 0.474 ms, 2: 0.456, 4: 0.466)
+  // handed on only between segments (a boundary costs about one sub-step);
+  // segments are the longest that still give every SM about twelve items, so
+  // that dynamic scheduling evens out the tail.  On the 2.7B shape (16 chunks,
+  // 320 head pairs) 1: 0.317 ms, 2: 0.292, 3: 0.282, 4: 0.287, 6: 0.285, 8: 0.300
   const long long pairs = (long long)d.batch * (d.nheads / fused::kNH);
   int seg = 1;
-  while (seg < 2 && seg * 2 <= d.nchunks &&
-         pairs * ((d.nchunks + seg * 2 - 1) / (seg * 2)) >= 8LL * sm_count())
-    seg *= 2;
+  while (seg < d.nchunks &&
+         pairs * ((d.nchunks + seg) / (seg + 1)) >= 12LL * sm_count())
+    ++seg;
   if (const char* ov = getenv("SSD_FUSED_SEGMENT_CHUNKS")) {   // tuning / test override
     const int v = atoi(ov);
     if (v >= 1 && v <= d.nchunks) seg = v;
