@@ -446,23 +446,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       Unit cur = s.uk[0];
       live = live && s.tk[0] < p.items;
       tc::mbar_arrive(&s.tk_empty[0]);
+      // L2: x, z and out stream through once (evict first); B and C are read
+      // by every head pair of the group, the hand-off slots by the next
+      // segment (both kept)
+      const uint64_t pol_stream = tc::l2_policy_evict_first();
+      const uint64_t pol_keep = tc::l2_policy_evict_last();
       auto load_cbx = [&](const Unit& it, int sb, int xb) {
         const int tok = (int)(it.t0 + sb * kSub);
         tc::mbar_arrive_expect_tx(&s.cbfull, 2 * kSub * kN * 2);
-        tc::tma_load_4d(s.C, &map_c, &s.cbfull, 0, it.g, tok, it.b);
-        tc::tma_load_4d(s.C + kSub * 128, &map_c, &s.cbfull, 64, it.g, tok, it.b);
-        tc::tma_load_4d(s.BH, &map_b, &s.cbfull, 0, it.g, tok, it.b);
-        tc::tma_load_4d(s.BH + kBhHalf, &map_b, &s.cbfull, 64, it.g, tok, it.b);
+        tc::tma_load_4d_hint(s.C, &map_c, &s.cbfull, 0, it.g, tok, it.b, pol_keep);
+        tc::tma_load_4d_hint(s.C + kSub * 128, &map_c, &s.cbfull, 64, it.g, tok, it.b, pol_keep);
+        tc::tma_load_4d_hint(s.BH, &map_b, &s.cbfull, 0, it.g, tok, it.b, pol_keep);
+        tc::tma_load_4d_hint(s.BH + kBhHalf, &map_b, &s.cbfull, 64, it.g, tok, it.b, pol_keep);
         tc::mbar_arrive_expect_tx(&s.xfull, kNH * kSub * kP * 2);
-        tc::tma_load_4d(s.XB[xb][0], &map_x, &s.xfull, 0, it.h0, tok, it.b);
-        tc::tma_load_4d(s.XB[xb][1], &map_x, &s.xfull, 0, it.h0 + 1, tok, it.b);
+        tc::tma_load_4d_hint(s.XB[xb][0], &map_x, &s.xfull, 0, it.h0, tok, it.b, pol_stream);
+        tc::tma_load_4d_hint(s.XB[xb][1], &map_x, &s.xfull, 0, it.h0 + 1, tok, it.b, pol_stream);
       };
       auto load_z = [&](const Unit& it, int sb) {
         if (p.z) {
           const int tok = (int)(it.t0 + sb * kSub);
           tc::mbar_arrive_expect_tx(&s.zfull, kNH * kSub * kP * 2);
-          tc::tma_load_4d(s.Z[0], &map_z, &s.zfull, 0, it.h0, tok, it.b);
-          tc::tma_load_4d(s.Z[1], &map_z, &s.zfull, 0, it.h0 + 1, tok, it.b);
+          tc::tma_load_4d_hint(s.Z[0], &map_z, &s.zfull, 0, it.h0, tok, it.b, pol_stream);
+          tc::tma_load_4d_hint(s.Z[1], &map_z, &s.zfull, 0, it.h0 + 1, tok, it.b, pol_stream);
         } else {
           tc::mbar_arrive(&s.zfull);   // Z is free for the epilogue
         }
@@ -500,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           // rows past the sequence end are outside the tensor map and not written
           const int tok = (int)(cur.t0 + sub * kSub);
-          tc::tma_store_4d(&map_out, s.Z[0], 0, cur.h0, tok, cur.b);
-          tc::tma_store_4d(&map_out, s.Z[1], 0, cur.h0 + 1, tok, cur.b);
+          tc::tma_store_4d_hint(&map_out, s.Z[0], 0, cur.h0, tok, cur.b, pol_stream);
+          tc::tma_store_4d_hint(&map_out, s.Z[1], 0, cur.h0 + 1, tok, cur.b, pol_stream);
           tc::bulk_commit();
         }
         if (!has_next) {
@@ -913,9 +918,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               uint4* dst = reinterpret_cast<uint4*>(p.slots) +
                            ((bh * 2 + (cur.c & 1)) * (kP / 4) + pc / 4) * kN + r;
+              const uint64_t pol = tc::l2_policy_evict_last();   // read by the next segment
 #pragma unroll
               for (int v4 = 0; v4 < 4; ++v4)
-                dst[v4 * kN] = make_uint4(hv[4 * v4], hv[4 * v4 + 1], hv[4 * v4 + 2], hv[4 * v4 + 3]);
+                asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst + v4 * kN),
+                             "r"(hv[4 * v4]), "r"(hv[4 * v4 + 1]), "r"(hv[4 * v4 + 2]), "r"(hv[4 * v4 + 3]), "l"(pol)
+                             : "memory");
             }
           }
         }
