@@ -87,7 +87,7 @@ __host__ __device__ constexpr uint32_t m_col(int h) { return 32 * (h & 1) + 8 * 
 constexpr int kErrBarrier = 1;
 constexpr int kErrLookback = 2;
 
-// B operand of the [CB | Ye] chain, K-major with the 128-byte swizzle: per
+// B operand of the CB and Ye chains, K-major with the 128-byte swizzle: per
 // 64-column (dstate) half, 256 rows of 128 bytes -- rows 0-127 the B tile
 // (tokens), rows 128 + 64 e + p the entering state of head e, headdim p.
 constexpr int kBhHalf = 256 * 128;
@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t T_CBr = T_R(bc);              // CB_k row r
       const uint32_t T_Mr = T_R(bc ^ 1) + e * kP;  // M_e row r (bf16 pairs)
 
-      // ---- M_e = CB o decay into T_M, the live 32-column blocks 0..qr of
+      // ---- M_e = CB o decay into TMEM, the live 32-column blocks 0..qr of
       // this row; the blocks above the diagonal are zeroed (the region held
       // Yi of step k-1).  Below the diagonal block the decay factors as
       // exp2(l_r - l_f) * [exp2(l_f - l_j) dt_j] with f the block's last
