@@ -344,6 +344,11 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -830,14 +835,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld_wait_regs(v);
         float m[16];
         if (diag) {
+          // unmasked here; D goes onto the diagonal element (column r - c0 of
+          // these 16), the causal mask is applied to the packed words below
           const uint64_t lr2 = pk2(l_r, l_r), neg2 = pk2(-1.f, -1.f);
+          const int t = r - c0;
+          const uint64_t dpair = (t & 1) ? pk2(0.f, Dh) : pk2(Dh, 0.f);
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             const float2 d = up2(fma2(pk2(colv[i], colv[i + 1]), neg2, lr2));   // l_r - mcol
-            const float2 val = up2(mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
-                                        pk2(ex2(d.x), ex2(d.y))));
-            m[i] = (c0 + i < r) ? val.x : (c0 + i == r ? val.x + Dh : 0.f);
-            m[i + 1] = (c0 + i + 1 < r) ? val.y : (c0 + i + 1 == r ? val.y + Dh : 0.f);
+            uint64_t val = mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                pk2(ex2(d.x), ex2(d.y)));
+            if ((i >> 1) == (t >> 1)) val = add2(val, dpair);
+            const float2 f = up2(val);
+            m[i] = f.x;
+            m[i + 1] = f.y;
           }
         } else {
           const uint64_t a2 = pk2(arow, arow);
@@ -863,6 +874,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t packed[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) packed[i] = tc::pack_bf16x2(m[2 * i], m[2 * i + 1]);
+        if (diag) {
+          // causal mask j <= r on the bf16 pairs: word w keeps its low half
+          // when 2w <= r - c0 and its high half when 2w + 1 <= r - c0 (the
+          // masked entries become exact zeros whatever their value was)
+          const int s16 = 16 * (r - c0 + 1);
+#pragma unroll
+          for (int w = 0; w < 8; ++w)
+            packed[w] &= __funnelshift_lc(0xFFFFFFFFu, 0u, (unsigned)max(s16 - 32 * w, 0));
+        }
         tc::tmem_st8(T_Mr + m_col(2 * qc + hf), packed);
       }
       {
