@@ -225,6 +225,42 @@ def cpu_model() -> str:
 
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of a per-rank float over all ranks of the job (a
+    replicated job's step time is its slowest rank's); x itself for one rank.
+    Uses the default process group (nccl on the GPU machine, gloo in the tests)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def bench_line(cfg, world: int, steps: int, warmup: int, ms: float, extra: dict) -> dict:
+    """The JSON line of the device-timed arm: every rank runs the whole
+    workload (replicas, weak scaling), so the job's throughput counts all
+    ranks' tokens over the slowest rank's step time ms.  extra carries the
+    measured sections (roofline, whole_call, cpu_baseline, e2e, gpu_launches,
+    clocks)."""
+    line = {
+        "metric": METRIC, "value": cfg.tokens * world / (ms / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: batch {cfg.batch}, seqlen {cfg.seqlen}, "
+                               f"nheads {cfg.nheads}, headdim {cfg.headdim}, dstate "
+                               f"{cfg.dstate}, ngroups {cfg.ngroups}, chunk "
+                               f"{cfg.chunk_size}, z gate + D skip, fp32 state",
+                   "global_batch": cfg.batch * world, "seq_len": cfg.seqlen,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (x, z, out are 335 MB each; L2 129 MB)"},
+    }
+    line.update(extra)
+    return line
+
+
 def run_reference(args, cfg):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -315,13 +351,8 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
     tokens = cfg.tokens * world
-    value = tokens / (ms / 1e3)
 
     # per-kernel durations, with events between the launches: the fused path
     # is one kernel (all four stages); the SIMT path is the four stage kernels
@@ -413,11 +444,7 @@ def main():
         s1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = s0.elapsed_time(s1) / args.steps
-        if world > 1:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = max_over_ranks(s0.elapsed_time(s1) / args.steps, world, dev)
         e2e = {"value": tokens / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
@@ -428,21 +455,10 @@ def main():
                "cpu": cpu_model()}
 
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: batch {cfg.batch}, seqlen {cfg.seqlen}, "
-                                   f"nheads {cfg.nheads}, headdim {cfg.headdim}, dstate "
-                                   f"{cfg.dstate}, ngroups {cfg.ngroups}, chunk "
-                                   f"{cfg.chunk_size}, z gate + D skip, fp32 state",
-                       "global_batch": cfg.batch * world, "seq_len": cfg.seqlen,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (x, z, out are 335 MB each; L2 129 MB)"},
-            "roofline": roofline, "whole_call": whole, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (1 if fused else 4) * args.steps, "clocks": clk,
-        }
+        line = bench_line(cfg, world, args.steps, args.warmup, ms,
+                          {"roofline": roofline, "whole_call": whole, "cpu_baseline": cpu,
+                           "e2e": e2e, "gpu_launches": (1 if fused else 4) * args.steps,
+                           "clocks": clk})
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
