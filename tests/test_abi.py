@@ -79,7 +79,11 @@ def test_validation_errors_before_any_launch(lib):
     assert _fwd(lib, H=3, G=2) == -1
     assert _fwd(lib, P=48) == -4
     assert _fwd(lib, N=8) == -4
-    assert _fwd(lib, L=0) == -1
+    assert _fwd(lib, L=0) == -1                       # empty sequence
+    assert _fwd(lib, batch=0) == -1                   # empty batch
+    assert _fwd(lib, batch=-1) == -1
+    assert _fwd(lib, H=0) == -1
+    assert _fwd(lib, batch=65536) == -4               # above the supported batch
     assert _fwd(lib, lo=1.0, hi=0.5) == -1
     assert _fwd(lib, ws=4096, wsb=16) == -5           # caller workspace too small
 
