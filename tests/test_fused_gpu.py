@@ -164,3 +164,53 @@ def test_fused_segments(seg, monkeypatch):
     ry, rf = oracle.scan_sequential(d)
     assert_close(y, ry, TOL["bf16"], f"out (segments of {seg})")
     assert_close(f, rf, TOL["bf16"], f"final (segments of {seg})")
+
+
+def _run_raw(g, chunk):
+    """The fused path on device inputs; out and final states as device tensors."""
+    import selective_state_space_05_gb300 as ssd
+    Bsz, L, H, P = g["x"].shape
+    G, N = g["B"].shape[2], g["B"].shape[3]
+    ws = torch.empty(ssd.workspace_bytes(Bsz, L, H, P, N, G, chunk), dtype=torch.uint8,
+                     device="cuda")
+    out, fin = ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=chunk,
+                                dt_bias=g["dt_bias"], D=g["D"], z=g["z"],
+                                initial_states=g["initial_states"], seq_idx=g["seq_idx"],
+                                return_final_states=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[4:8].view(torch.int32).item()) == 0, "fused kernel gave up a wait"
+    return out, fin
+
+
+@pytest.mark.parametrize("shape", [
+    dict(batch=2, seqlen=1800, nheads=4, ngroups=2, chunk_size=128,
+         seq_idx_lengths=[700, 1100]),
+    dict(batch=4, seqlen=8192, nheads=32, ngroups=4, chunk_size=256),
+    dict(batch=8, seqlen=1000, nheads=40, ngroups=4, chunk_size=256,
+         seq_idx_lengths=[300, 1, 699]),
+], ids=["docs_15_chunks", "32_chunks", "160_pairs_ragged"])
+def test_fused_segment_lengths_bit_identical(shape, monkeypatch):
+    """The hand-off between segments is an exact fp32 copy of the state
+    (TMEM -> slot -> TMEM), so the segment length changes nothing in the
+    result, bit for bit, down to one segment per sequence (no hand-off at
+    all); the result also matches the oracle on sampled heads."""
+    d = _small(48, init_std=0.3, **shape)
+    g = to_dev(d)
+    Q = shape["chunk_size"]
+    nc = -(-shape["seqlen"] // Q)
+    monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", "1")
+    y_1, f_1 = _run_raw(g, Q)
+    for seg in sorted({2, 3, nc} - {1}):
+        if seg > nc:
+            continue
+        monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", str(seg))
+        y_s, f_s = _run_raw(g, Q)
+        assert torch.equal(y_1, y_s), f"out: segments of 1 vs {seg}"
+        assert torch.equal(f_1, f_s), f"final: segments of 1 vs {seg}"
+    H = shape["nheads"]
+    heads, batches = sorted({0, H // 2 + 1, H - 1}), sorted({0, shape["batch"] - 1})
+    ry, rf = oracle.scan_sequential(d, heads=heads, batches=batches)
+    y = y_1.double().cpu().numpy()[batches][:, :, heads]
+    f = f_1.double().cpu().numpy()[batches][:, heads]
+    assert_close(y, ry, TOL["bf16"], "out (sampled)")
+    assert_close(f, rf, TOL["bf16"], "final (sampled)")
