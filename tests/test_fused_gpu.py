@@ -58,6 +58,12 @@ CASES = [
     ("slow_decay", dict(seqlen=1024, chunk_size=128, init_std=0.5,
                         a_log_range=(math.log(1e-3), math.log(1e-1)))),
     ("many_heads", dict(seqlen=512, chunk_size=256, nheads=16, ngroups=4, batch=3)),
+    # without dt_bias dt is about 0.7: a 32-token block decays by 2^40 to 2^600,
+    # so the diagonal blocks take both the factored and the per-element form
+    ("strong_decay_mixed", dict(seqlen=600, chunk_size=256, dt_bias=False, init_std=0.3,
+                                a_log_range=(0.0, math.log(4.0)),
+                                seq_idx_lengths=[250, 1, 349])),
+    ("strong_decay", dict(seqlen=300, chunk_size=128, dt_bias=False, init_std=0.3)),
 ]
 
 
