@@ -228,7 +228,7 @@ def cpu_model() -> str:
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest value of a per-rank float over all ranks of the job (a
     replicated job's step time is its slowest rank's); x itself for one rank.
-    Uses the default process group (nccl on the GPU machine, gloo in the tests)."""
+    Uses the default process group (nccl on GPUs, gloo in the CPU tests)."""
     if world <= 1:
         return x
     import torch
