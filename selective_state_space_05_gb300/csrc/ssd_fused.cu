@@ -1043,6 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace ssd {
@@ -1078,16 +1079,18 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// per device; host threads may launch concurrently
 int sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 148;
+    n = n > 0 ? n : 148;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 }  // namespace
@@ -1158,12 +1161,17 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.seg_chunks = seg;
   p.items = pairs * ((d.nchunks + seg - 1) / seg);
   const size_t smem = sizeof(fused::Smem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory opt-in is a property of the kernel on each device
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool known = dev >= 0 && dev < 64;
+  if (!known || !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(fused::ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (known) attr_set[dev].store(true, std::memory_order_release);
   }
   const long long grid = std::min<long long>(p.items, sm_count());   // one CTA per SM
   fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz, mo, p);
