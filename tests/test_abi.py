@@ -1,6 +1,5 @@
 """The C-ABI library loads and exports every symbol include/*.h declares;
 host-side validation answers before anything touches a GPU."""
-import ctypes
 import math
 import re
 from pathlib import Path

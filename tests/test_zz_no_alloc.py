@@ -8,7 +8,6 @@ different sizes and options, so that the second call runs on scratch that
 still holds the first call's contents.  This file is collected last so that a
 run stopping at the first failure has run every other test before it.
 """
-import ctypes
 
 import pytest
 import torch
