@@ -7,11 +7,16 @@ synthetic seeded inputs (ssd_inputs.py).  One step = one ssd_scan_fwd call
 over the whole batch (all four stages).
 
 Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs
-resident in HBM; `e2e` is the same metric with the host->device copy of the
-inputs and the device->host copy of the output inside the timed region.
-`roofline` rates the kernel that takes most of the step against the measured
-peaks in MEASURED_PEAKS.json.  `cpu_baseline` times the fp64 CPU oracle on a
-bounded sample of the same workload.
+resident in HBM (one event pair per call: mean, median and p90 per call; a
+second, seconds-long block of back-to-back calls gives ms_per_step_long);
+`e2e` is the same metric with the host->device copy of the inputs and the
+device->host copy of the output inside the timed region.  `roofline` rates
+the kernel that takes most of the step against the measured peaks in
+MEASURED_PEAKS.json.  `cpu_baseline` times the fp64 CPU oracle on a bounded
+sample of the same workload, and `parity` compares that sample with the GPU
+output (max and mean relative error, mean signed error, 99.9th percentile).
+`other_configs` times the chained-prefill and packed-documents workloads the
+same way (inputs drawn on the device).
 
 `--impl reference` times the oracle alone (the only reference this workload
 has) and prints its own line.
@@ -36,7 +41,6 @@ UNIT = "tokens/s"
 WORKLOAD = "mamba2_2p7b"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0, "source": "fallback"}
-NUM_SMS = 152
 FP32_LANES_PER_SM = 128
 
 
@@ -51,6 +55,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--long-seconds", type=float, default=3.0,
+                    help="length of the back-to-back block (0: skip)")
+    ap.add_argument("--no-other", action="store_true", help="skip the other workloads")
     return ap.parse_args()
 
 
@@ -68,17 +75,22 @@ def load_peaks() -> dict:
 # algorithmic work per call (counts the method needs, not what a kernel does)
 # ---------------------------------------------------------------------------
 
-def algorithmic(cfg) -> dict:
+def algorithmic(cfg, seqlen=None, init=False, final=False, seq=False) -> dict:
+    """Counts of one call over `seqlen` tokens (default the workload's):
+    read x, z, dt, B, C, A, D, dt_bias (and initial states, seq_idx) once,
+    write out (and final states) once."""
     e = 2 if cfg.dtype == "bf16" else 4
-    Bz, L, H, P, N, G, Q = (cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
-                            cfg.ngroups, cfg.chunk_size)
+    Bz, L, H, P, N, G, Q = (cfg.batch, seqlen or cfg.seqlen, cfg.nheads, cfg.headdim,
+                            cfg.dstate, cfg.ngroups, cfg.chunk_size)
     nc = -(-L // Q)
     x = Bz * L * H * P * e
     bc = Bz * L * G * N * e
     dt = Bz * L * H * e
     state = Bz * nc * H * P * N * 4
     chunk_f32 = Bz * H * nc * Q * 4
-    io = 3 * x + 2 * bc + dt + 3 * H * 4          # x, z, out, B, C, dt, (A, D, dt_bias)
+    hstate = Bz * H * P * N * 4
+    io = ((3 if cfg.has_z else 2) * x + 2 * bc + dt + 3 * H * 4
+          + (hstate if init else 0) + (hstate if final else 0) + (Bz * L * 4 if seq else 0))
     tri = Q * (Q + 1) // 2
     # causal flops: C B^T once per group, masked (CB) x and C h per head, B^T x per head
     flops = Bz * nc * (G * tri * N * 2 + H * (tri * P * 2 + 2 * Q * N * P * 2))
@@ -86,13 +98,13 @@ def algorithmic(cfg) -> dict:
                 tri=tri, nc=nc)
 
 
-def kernel_models(cfg, peaks) -> dict:
+def kernel_models(cfg, peaks, num_sms, **kw) -> dict:
     """Per-kernel algorithmic bytes / flops and the roofline that bounds it."""
-    a = algorithmic(cfg)
+    a = algorithmic(cfg, **kw)
     Bz, H, P, N, G, Q, nc = (cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups,
                              cfg.chunk_size, a["nc"])
     hbm = peaks["hbm_gbs"] * 1e9
-    alu = NUM_SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+    alu = num_sms * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
     m = {}
     m["dt_cumsum"] = dict(bytes=a["dt"] + 2 * a["chunk_f32"], flops=0, bound="hbm", peak=hbm)
     m["chunk_state"] = dict(bytes=a["x"] + a["bc"] + 2 * a["chunk_f32"] + a["state"],
@@ -185,10 +197,11 @@ class ClockSampler:
 # CPU oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(cfg, inputs, target_s: float, seed_heads=0):
+def oracle_sample(cfg, inputs, target_s: float, seed_heads=0):
     """Times the fp64 oracle on a sample of (batch row, head) recurrences sized
-    to about target_s seconds; returns (tokens/s equivalent, cores,
-    description, seconds).  A token-equivalent is one token through all heads."""
+    to about target_s seconds.  Returns a dict: rate (tokens/s equivalent; a
+    token-equivalent is one token through all heads), cores, description,
+    seconds, and the sample's outputs with the batch rows and heads it covers."""
     from oracle import ssd_oracle as so
     cores = so.default_threads()
     H, L, Bz = cfg.nheads, cfg.seqlen, cfg.batch
@@ -201,14 +214,37 @@ def oracle_sample_rate(cfg, inputs, target_s: float, seed_heads=0):
     else:
         batches, heads = list(range(min(Bz, -(-pairs // H)))), None
     t = time.perf_counter()
-    so.scan_sequential(inputs, heads=heads, batches=batches, nthreads=cores)
+    y, fin = so.scan_sequential(inputs, heads=heads, batches=batches, nthreads=cores)
     dt = time.perf_counter() - t
     nh = H if heads is None else len(heads)
     tokens_equiv = L * len(batches) * nh / H
     desc = (f"fp64 sequential oracle on {len(batches)} batch row(s) x {nh} of {H} "
             f"heads, seqlen {L}: {tokens_equiv:.0f} token-equivalents (one token through "
             f"all heads) in {dt:.2f} s")
-    return tokens_equiv / dt, cores, desc, dt
+    return dict(rate=tokens_equiv / dt, cores=cores, desc=desc, seconds=dt, y=y, fin=fin,
+                batches=batches, heads=list(range(H)) if heads is None else heads)
+
+
+def error_metrics(pairs) -> dict:
+    """max |err| / max |ref|, mean |err| / mean |ref|, mean signed error and
+    the 99.9th percentile of |err| / max |ref| (the largest over the pieces,
+    which are batch rows of equal size) over (got, ref) array pairs."""
+    import numpy as np
+    mx = mref = sabs = sref = sdiff = 0.0
+    n = 0
+    qs = []
+    for got, ref in pairs:
+        d = np.asarray(got, dtype=np.float64) - ref
+        ad = np.abs(d)
+        mx, mref = max(mx, float(ad.max())), max(mref, float(np.abs(ref).max()))
+        sabs += float(ad.sum())
+        sref += float(np.abs(ref).sum())
+        sdiff += float(d.sum())
+        n += ad.size
+        qs.append(np.quantile(ad, 0.999))   # per piece; the pieces are equal-sized rows
+    return {"max_rel": mx / max(mref, 1e-300), "mean_rel": sabs / max(sref, 1e-300),
+            "mean_diff": sdiff / max(n, 1), "p999_rel": float(max(qs)) / max(mref, 1e-300),
+            "elements": n}
 
 
 def cpu_model() -> str:
@@ -237,6 +273,12 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def workload_string(cfg) -> str:
+    return (f"{cfg.name}: batch {cfg.batch}, seqlen {cfg.seqlen}, nheads {cfg.nheads}, "
+            f"headdim {cfg.headdim}, dstate {cfg.dstate}, ngroups {cfg.ngroups}, chunk "
+            f"{cfg.chunk_size}, z gate + D skip, fp32 state")
+
+
 def bench_line(cfg, world: int, steps: int, warmup: int, ms: float, extra: dict) -> dict:
     """The JSON line of the device-timed arm: every rank runs the whole
     workload (replicas, weak scaling), so the job's throughput counts all
@@ -248,10 +290,7 @@ def bench_line(cfg, world: int, steps: int, warmup: int, ms: float, extra: dict)
         "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: batch {cfg.batch}, seqlen {cfg.seqlen}, "
-                               f"nheads {cfg.nheads}, headdim {cfg.headdim}, dstate "
-                               f"{cfg.dstate}, ngroups {cfg.ngroups}, chunk "
-                               f"{cfg.chunk_size}, z gate + D skip, fp32 state",
+        "config": {"workload": workload_string(cfg),
                    "global_batch": cfg.batch * world, "seq_len": cfg.seqlen,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (x, z, out are 335 MB each; L2 129 MB)"},
@@ -270,24 +309,95 @@ def run_reference(args, cfg):
     rates = []
     desc = cores = None
     for i in range(args.warmup + args.steps):
-        r, cores, desc, _ = oracle_sample_rate(cfg, inputs, per_step, seed_heads=i)
+        s = oracle_sample(cfg, inputs, per_step, seed_heads=i)
+        cores, desc = s["cores"], s["desc"]
+        del s["y"], s["fin"]
         if i >= args.warmup:
-            rates.append(r)
+            rates.append(s["rate"])
     value = statistics.median(rates)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * cfg.tokens / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: batch {cfg.batch}, seqlen {cfg.seqlen}, "
-                               f"nheads {cfg.nheads}, headdim {cfg.headdim}, dstate "
-                               f"{cfg.dstate}, ngroups {cfg.ngroups}, chunk {cfg.chunk_size}",
-                   "sample": desc},
+        "config": {"workload": workload_string(cfg), "sample": desc},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc, "cpu": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def time_calls(torch, step, n, stream):
+    """n calls of step() with one CUDA event between consecutive calls, on the
+    launching stream; returns (mean ms per call, per-call ms list)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
+        step()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    return evs[0].elapsed_time(evs[n]) / n, per
+
+
+def spread(per) -> dict:
+    s = sorted(per)
+    return {"median": statistics.median(s), "p90": s[min(len(s) - 1, int(0.9 * len(s)))],
+            "min": s[0], "max": s[-1]}
+
+
+def other_workload(torch, ssd, si, name, dev, stream, peaks, steps, warmup, num_sms):
+    """Times one more workload through ssd_scan_fwd with inputs drawn on the
+    device: the chained prefill (segments with the final states fed back as
+    the next initial states; all tokens counted) or the packed documents (one
+    call with seq_idx)."""
+    cfg = si.CONFIGS[name]
+    g = si.make_inputs(cfg, 2000 + len(name), device=dev)
+    Q = cfg.chunk_size
+    S = cfg.segments
+    seg_len = cfg.seqlen // S
+    Bz, H, P, N = cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate
+    parts = [{k: g[k][:, s * seg_len:(s + 1) * seg_len].contiguous()
+              for k in ("x", "dt", "B", "C", "z")} for s in range(S)] if S > 1 else [g]
+    outs = [torch.empty_like(p["x"]) for p in parts]
+    fins = [torch.empty(Bz, H, P, N, dtype=torch.float32, device=dev) for _ in range(2)]
+    ws = torch.empty(ssd.workspace_bytes(Bz, seg_len, H, P, N, cfg.ngroups, Q, g["x"].dtype),
+                     dtype=torch.uint8, device=dev)
+    chained = S > 1
+
+    def step():
+        init = g["initial_states"]
+        for s, p in enumerate(parts):
+            ssd.ssd_scan_fwd(p["x"], p["dt"], g["A"], p["B"], p["C"], chunk_size=Q,
+                             dt_bias=g["dt_bias"], D=g["D"], z=p["z"], initial_states=init,
+                             seq_idx=g["seq_idx"], out=outs[s],
+                             final_states=fins[s % 2] if chained else None,
+                             return_final_states=chained, workspace=ws, stream=stream)
+            init = fins[s % 2]
+
+    for _ in range(max(warmup, 2)):
+        step()
+    torch.cuda.synchronize()
+    ms, per = time_calls(torch, step, steps, stream)
+    ssd.scan_status(reset=True, stream=stream)
+    a = algorithmic(cfg, seqlen=seg_len, init=g["initial_states"] is not None or chained,
+                    final=chained, seq=g["seq_idx"] is not None)
+    ms_call = ms / S
+    achieved = a["io_bytes"] / (ms_call / 1e3) / 1e9
+    del g, parts, outs, fins, ws
+    torch.cuda.empty_cache()
+    return {"workload": workload_string(cfg) + (f", {S} chained calls of {seg_len} tokens"
+                                                if chained else ", seq_idx documents"),
+            "tokens_per_step": cfg.tokens, "calls_per_step": S, "ms_per_step": ms,
+            "ms_per_call": ms_call, "value": cfg.tokens / (ms / 1e3), "unit": UNIT,
+            "per_step_ms": spread(per), "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "alg_bytes_per_call": a["io_bytes"], "alg_flops_per_call": a["flops"],
+                         "tensor_frac": a["flops"] / (ms_call / 1e3) / (peaks["bf16_tflops"]
+                                                                        * 1e12)},
+            "gpu_launches": steps * S, "data": "synthetic, drawn on the device"}
 
 
 def main():
@@ -310,6 +420,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     host = si.make_inputs(cfg, 1002 + rank)
     g = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in host.items()}
@@ -341,49 +452,60 @@ def main():
     clocks.start()
     barrier()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize()
+    ms_local, per_call = time_calls(torch, step, args.steps, stream)
+    barrier()
+    # a second, seconds-long block of back-to-back calls (steadier clocks)
+    long = None
+    if args.long_seconds > 0:
+        n_long = max(args.steps, int(args.long_seconds / (ms_local / 1e3)))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_long):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        long = {"calls": n_long, "ms_per_step": e0.elapsed_time(e1) / n_long}
     barrier()
     clk = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+    ssd.scan_status(reset=True, stream=stream)   # no launch gave up a bounded wait
+    ms = max_over_ranks(ms_local, world, dev)
     tokens = cfg.tokens * world
 
-    # per-kernel durations, with events between the launches: the fused path
-    # is one kernel (all four stages); the SIMT path is the four stage kernels
+    # per-kernel durations: the fused path is one kernel (all four stages),
+    # timed by the per-call events above; the SIMT path is the four stage
+    # kernels, timed with events between them
     fused = (cfg.dtype == "bf16" and cfg.headdim == 64 and cfg.dstate == 128
              and Q in (128, 256) and (cfg.nheads // cfg.ngroups) % 2 == 0)
-    names = (["scan_fused"] if fused else
-             ["dt_cumsum", "chunk_state", "state_passing", "chunk_scan"])
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
-           for _ in range(args.steps)]
-    for k in range(args.steps):
-        e = evs[k]
-        e[0].record(stream)
-        if fused:
-            step()
+    if fused:
+        per = {"scan_fused": statistics.mean(per_call)}
+    else:
+        names = ["dt_cumsum", "chunk_state", "state_passing", "chunk_scan"]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+               for _ in range(args.steps)]
+        for k in range(args.steps):
+            e = evs[k]
+            e[0].record(stream)
+            dto, cso, sego = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q,
+                                               dt_bias=g["dt_bias"], seq_idx=g["seq_idx"],
+                                               stream=stream)
             e[1].record(stream)
-            continue
-        dto, cso, sego = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q, dt_bias=g["dt_bias"],
-                                           seq_idx=g["seq_idx"], stream=stream)
-        e[1].record(stream)
-        st2 = ssd.ssd_chunk_state(g["x"], g["B"], dto, cso, sego, chunk_size=Q, stream=stream)
-        e[2].record(stream)
-        ssd.ssd_state_passing(st2, cso, sego, seqlen=cfg.seqlen, chunk_size=Q,
-                              initial_states=g["initial_states"], stream=stream)
-        e[3].record(stream)
-        ssd.ssd_chunk_scan(g["x"], g["B"], g["C"], dto, cso, sego, st2, chunk_size=Q,
-                           D=g["D"], z=g["z"], out=out, stream=stream)
-        e[4].record(stream)
-        del st2, dto, cso, sego
-    torch.cuda.synchronize()
-    per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
-           for i, n in enumerate(names)}
-    models = kernel_models(cfg, peaks)
+            st2 = ssd.ssd_chunk_state(g["x"], g["B"], dto, cso, sego, chunk_size=Q,
+                                      stream=stream)
+            e[2].record(stream)
+            ssd.ssd_state_passing(st2, cso, sego, seqlen=cfg.seqlen, chunk_size=Q,
+                                  initial_states=g["initial_states"], stream=stream)
+            e[3].record(stream)
+            ssd.ssd_chunk_scan(g["x"], g["B"], g["C"], dto, cso, sego, st2, chunk_size=Q,
+                               D=g["D"], z=g["z"], out=out, stream=stream)
+            e[4].record(stream)
+            del st2, dto, cso, sego
+        torch.cuda.synchronize()
+        per = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1])
+                                  for k in range(args.steps))
+               for i, n in enumerate(names)}
+    has_init = g["initial_states"] is not None
+    has_seq = g["seq_idx"] is not None
+    models = kernel_models(cfg, peaks, num_sms, init=has_init, final=True, seq=has_seq)
     top = max(per, key=per.get)
     mdl = models[top]
     dur_s = per[top] / 1e3
@@ -395,18 +517,31 @@ def main():
     if "tensor_peak" in mdl:
         extra["tensor_tflops"] = mdl["flops"] / dur_s / 1e12
         extra["tensor_frac"] = mdl["flops"] / dur_s / mdl["tensor_peak"]
+    a = algorithmic(cfg, init=has_init, final=True, seq=has_seq)
+    a_io = algorithmic(cfg, init=has_init, final=False, seq=has_seq)
     roofline = {"kernel": top, "bound": mdl["bound"], "achieved": achieved, "peak": peak,
                 **extra,
                 "unit": unit, "frac": achieved / peak,
+                "frac_without_final_states": (a_io["io_bytes"] / dur_s / 1e9 / peak
+                                              if mdl["bound"] == "hbm" else None),
                 "traffic": measured_traffic(top, cfg.name),
                 "alg_bytes": mdl["bytes"], "alg_flops": mdl["flops"],
+                "alg_bytes_note": "x, z, out, B, C, dt, A, D, dt_bias and the final states "
+                                  "the step writes",
                 "peak_source": peaks.get("source"),
                 "kernel_ms": {n: round(v, 4) for n, v in per.items()},
                 "share": {n: round(v / sum(per.values()), 4) for n, v in per.items()}}
-    a = algorithmic(cfg)
     whole = {"alg_bytes": a["io_bytes"], "alg_flops": a["flops"],
              "hbm_time_us": a["io_bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6,
              "frac_of_hbm_roofline": (a["io_bytes"] / (peaks["hbm_gbs"] * 1e9)) / (ms / 1e3)}
+    timing = {"per_call_ms": spread(per_call)}
+    if long is not None:
+        timing["ms_per_step_long"] = long["ms_per_step"]
+        timing["calls_long"] = long["calls"]
+    if clk.get("sm_mhz"):
+        timing["kcycles_per_call_at_median_sm_clock"] = ms * clk["sm_mhz"]   # ms x MHz = kcycles
+        if long is not None:
+            timing["kcycles_per_call_long"] = long["ms_per_step"] * clk["sm_mhz"]
 
     # end to end through ssd_scan_fwd_host: the inputs live in pinned host
     # memory and the output goes back to it, every step (the library pipelines
@@ -435,28 +570,45 @@ def main():
             e2e_step()
         torch.cuda.synchronize()
         barrier()
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        s1.record(stream)
-        torch.cuda.synchronize()
+        ems_local, eper = time_calls(torch, e2e_step, args.steps, stream)
         barrier()
-        ems = max_over_ranks(s0.elapsed_time(s1) / args.steps, world, dev)
+        ems = max_over_ranks(ems_local, world, dev)
         e2e = {"value": tokens / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems, "per_call_ms": spread(eper)}
+        del hws, hin, hout
 
-    cpu = None
+    others = None
+    if not args.no_other and world == 1 and args.workload == WORKLOAD:
+        others = {}
+        for name in ("chained", "packed"):
+            others[name] = other_workload(torch, ssd, si, name, dev, stream, peaks, args.steps,
+                                          args.warmup, num_sms)
+
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, cores, desc, _ = oracle_sample_rate(cfg, host, args.cpu_seconds)
-        cpu = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
-               "cpu": cpu_model()}
+        s = oracle_sample(cfg, host, args.cpu_seconds)
+        cpu = {"value": s["rate"], "unit": UNIT, "cores": s["cores"], "kind": "oracle",
+               "sample": s["desc"], "cpu": cpu_model()}
+        # the GPU output of the timed calls (same inputs) against the sample
+        yg, fg = out.cpu(), fin.cpu()
+        hs = s["heads"]
+        pieces_y = [(yg[b:b + 1][:, :, hs].double().numpy(), s["y"][i:i + 1])
+                    for i, b in enumerate(s["batches"])]
+        pieces_f = [(fg[b:b + 1][:, hs].double().numpy(), s["fin"][i:i + 1])
+                    for i, b in enumerate(s["batches"])]
+        parity = {"out": error_metrics(pieces_y), "final_states": error_metrics(pieces_f),
+                  "tol": 2e-2 if cfg.dtype == "bf16" else 1e-4,
+                  "pairs": len(s["batches"]) * len(hs),
+                  "against": "fp64 oracle on the cpu_baseline sample"}
+        parity["pass"] = (parity["out"]["max_rel"] <= parity["tol"]
+                          and parity["final_states"]["max_rel"] <= parity["tol"])
 
     if rank == 0:
         line = bench_line(cfg, world, args.steps, args.warmup, ms,
-                          {"roofline": roofline, "whole_call": whole, "cpu_baseline": cpu,
-                           "e2e": e2e, "gpu_launches": (1 if fused else 4) * args.steps,
+                          {"roofline": roofline, "whole_call": whole, "timing": timing,
+                           "cpu_baseline": cpu, "parity": parity, "e2e": e2e,
+                           "other_configs": others,
+                           "gpu_launches": (1 if fused else 4) * args.steps,
                            "clocks": clk})
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 1
+#define SSD_ABI_VERSION 2
 
 typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype_t;
 
@@ -55,17 +55,36 @@ enum {
     SSD_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned           */
     SSD_ERR_UNSUPPORTED = -4,  /* valid but outside the supported shapes     */
     SSD_ERR_WORKSPACE = -5,    /* caller workspace too small                 */
-    SSD_ERR_CUDA = -6          /* a CUDA runtime call or launch failed       */
+    SSD_ERR_CUDA = -6,         /* a CUDA runtime call or launch failed       */
+    SSD_ERR_TIMEOUT = -7       /* a launch gave up a bounded wait (ssd_scan_status) */
 };
 
 /* Version of this ABI.  New behaviour goes into new symbols; an existing
  * signature is never changed in place (an in-place change of a native fwd
- * signature broke its callers in state-spaces/mamba PR #488). */
+ * signature broke its callers in state-spaces/mamba PR #488).
+ *   1  the calls below up to ssd_scan_fwd_host
+ *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status and ssd_scan_fwd_strided; every
+ *      version-1 symbol is unchanged */
 int ssd_abi_version(void);
 
 /* Message for the last error returned on the calling host thread ("" if
  * none).  The string stays valid until the next call on that thread. */
 const char *ssd_last_error(void);
+
+/* Status of the work already launched on the current device.  The
+ * tensor-core kernel bounds every internal wait (2 s; it should never need
+ * more than microseconds).  A wait that gives up ends the launch early: its
+ * `out` and `final_states` are then NOT valid although the launching call
+ * returned SSD_OK, because the launching call does not synchronise.  The
+ * kernel records that in a device-wide status word (sticky across launches
+ * and streams until reset), which this call reads.
+ *   reset   nonzero: clear the word after reading it
+ *   stream  cudaStream_t; the call synchronises it first (so every launch
+ *           enqueued on it before has finished) and copies 4 bytes to the
+ *           host; it allocates nothing.
+ * Returns SSD_OK (no launch gave up), SSD_ERR_TIMEOUT (ssd_last_error()
+ * names the wait) or SSD_ERR_CUDA. */
+int ssd_scan_status(int reset, void *stream);
 
 /* Bytes of device workspace ssd_scan_fwd needs for these sizes: a control
  * block of (64 + batch*nheads) int32 (work counter, error word, hand-off
@@ -127,6 +146,44 @@ int ssd_scan_fwd(const void *x, const void *dt, const float *dt_bias,
                  int chunk_size, ssd_dtype_t dtype, void *out,
                  float *final_states, void *workspace, size_t workspace_bytes,
                  void *stream);
+
+/* Element strides of a [batch, seqlen, ...] input whose per-token part is
+ * dense: `batch` elements between batch rows, `token` elements between
+ * consecutive tokens.  The dense layout of ssd_scan_fwd is
+ * {seqlen * row, row} with row = nheads * headdim (x, z), nheads (dt) or
+ * ngroups * dstate (B, C). */
+typedef struct {
+    int64_t batch;
+    int64_t token;
+} ssd_stride_t;
+
+/*
+ * ssd_scan_fwd on strided views of x, dt, B, C and z, such as the slices of
+ * the fused input projection `zxbcdt` (z, xBC, dt) and of the convolved xBC
+ * (x, B, C) in the block around the scan (the repro script of
+ * state-spaces/mamba issue #647 splits one projection into them).  Within a
+ * token each input is dense as in ssd_scan_fwd ([nheads, headdim] for x and
+ * z, [nheads] for dt, [ngroups, dstate] for B and C); between tokens and
+ * batch rows it advances by the given strides (elements, >= 0 and at most
+ * 2^40; z_stride is ignored when z is NULL).  out, final_states and the
+ * [nheads] / state arguments are dense, every pointer 16-byte aligned, and
+ * everything else is as in ssd_scan_fwd.  The tensor-core path takes strides
+ * that are multiples of 8 elements for x, z, B, C and even for dt (TMA needs
+ * 16-byte strides; dt is read in pairs of heads); other strides run the
+ * four stage kernels.  Returns SSD_OK or a negative SSD_ERR_* code.
+ */
+int ssd_scan_fwd_strided(const void *x, ssd_stride_t x_stride, const void *dt,
+                         ssd_stride_t dt_stride, const float *dt_bias,
+                         int dt_softplus, float dt_limit_lo, float dt_limit_hi,
+                         const float *A, const void *B, ssd_stride_t B_stride,
+                         const void *C, ssd_stride_t C_stride, const float *D,
+                         const void *z, ssd_stride_t z_stride,
+                         const float *initial_states, const int32_t *seq_idx,
+                         int64_t batch, int64_t seqlen, int nheads,
+                         int headdim, int dstate, int ngroups, int chunk_size,
+                         ssd_dtype_t dtype, void *out, float *final_states,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream);
 
 /* ---------------------------------------------------------------------------
  * The four stages of ssd_scan_fwd, exposed one by one (same conventions).
@@ -193,8 +250,8 @@ int ssd_chunk_scan(const void *x, const void *B, const void *C,
  * final_states.  workspace (>= ssd_scan_workspace_bytes) is required: the
  * kernel hands each chunk's final state to the next chunk through it.  If a
  * bounded internal wait gives up (which it should never do), the int32 at
- * byte offset 4 of the workspace is nonzero after the kernel; the outputs
- * are then not valid. */
+ * byte offset 4 of the workspace is nonzero after the kernel and
+ * ssd_scan_status returns SSD_ERR_TIMEOUT; the outputs are then not valid. */
 int ssd_chunk_fused(const void *x, const void *B, const void *C,
                     const float *dt_out, const float *dA_cumsum,
                     const int32_t *chunk_seg, const float *D, const void *z,
@@ -222,9 +279,13 @@ int ssd_chunk_fused(const void *x, const void *B, const void *C,
  *  - Sizes whose scratch (ssd_scan_workspace_bytes) exceeds
  *    SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_WORKSPACE before
  *    anything is launched; use ssd_scan_fwd with a workspace for those.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *  - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *    with the calling device current; nothing is cached, so a reset or
+ *    re-created context is safe).  The first call on a device may load the
+ *    library's module there: make it before any stream capture.
+ *  - Like ssd_scan_fwd the call does not synchronise; ssd_scan_status (which
+ *    allocates nothing either) tells whether its launch gave up a bounded
+ *    internal wait.
  *  - Every call on a device shares the one array, which keeps the last
  *    call's contents; no part of it needs to start at zero.  Calls whose
  *    work overlaps on the GPU (different streams, or other host threads)

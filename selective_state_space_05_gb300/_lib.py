@@ -15,17 +15,30 @@ SSD_DTYPE_BF16 = 1
 SSD_NOALLOC_SCRATCH_BYTES = 64 << 20   # static scratch of ssd_scan_fwd_noalloc
 
 SSD_OK = 0
+SSD_ERR_TIMEOUT = -7
 ERRORS = {-1: "SSD_ERR_ARG", -2: "SSD_ERR_NULL", -3: "SSD_ERR_ALIGN",
-          -4: "SSD_ERR_UNSUPPORTED", -5: "SSD_ERR_WORKSPACE", -6: "SSD_ERR_CUDA"}
+          -4: "SSD_ERR_UNSUPPORTED", -5: "SSD_ERR_WORKSPACE", -6: "SSD_ERR_CUDA",
+          -7: "SSD_ERR_TIMEOUT"}
+
+
+class Stride(ctypes.Structure):
+    """ssd_stride_t: element strides between batch rows and between tokens."""
+    _fields_ = [("batch", ctypes.c_int64), ("token", ctypes.c_int64)]
+
 
 _vp = ctypes.c_void_p
 _i, _i64, _f, _sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_st = Stride
 
 # every symbol the header declares, with (restype, argtypes); pointers are
 # passed as integers (device addresses) through c_void_p
 SIGNATURES = {
     "ssd_abi_version": (_i, []),
     "ssd_last_error": (ctypes.c_char_p, []),
+    "ssd_scan_status": (_i, [_i, _vp]),
+    "ssd_scan_fwd_strided": (_i, [_vp, _st, _vp, _st, _vp, _i, _f, _f, _vp, _vp, _st, _vp, _st,
+                                  _vp, _vp, _st, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _i, _i,
+                                  _vp, _vp, _vp, _sz, _vp]),
     "ssd_scan_workspace_bytes": (_sz, [_i64, _i64, _i, _i, _i, _i, _i, _i]),
     "ssd_scan_fwd": (_i, [_vp, _vp, _vp, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                           _i64, _i64, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),

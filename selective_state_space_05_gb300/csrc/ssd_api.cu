@@ -62,6 +62,13 @@ int check_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstat
   d->ngroups = ngroups;
   d->chunk = chunk;
   d->nchunks = (int)nc;
+  // dense inputs unless the strided entry point sets other strides
+  const int64_t hp = (int64_t)nheads * headdim, gn = (int64_t)ngroups * dstate;
+  d->sx = {seqlen * hp, hp};
+  d->sz = d->sx;
+  d->sdt = {seqlen * nheads, nheads};
+  d->sB = {seqlen * gn, gn};
+  d->sC = d->sB;
   return SSD_OK;
 }
 
@@ -114,6 +121,19 @@ extern "C" {
 int ssd_abi_version(void) { return SSD_ABI_VERSION; }
 
 const char* ssd_last_error(void) { return g_err; }
+
+int ssd_scan_status(int reset, void* stream) {
+  g_err[0] = 0;
+  int bits = 0;
+  const int e = ssd::fused_status(reset, static_cast<cudaStream_t>(stream), &bits);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "ssd_scan_status");
+  if (bits != 0)
+    return fail(SSD_ERR_TIMEOUT,
+                "a tensor-core scan launch gave up a bounded wait (error bits 0x%x: 1 barrier, "
+                "2 state hand-off, 4 drain); its outputs are not valid",
+                bits);
+  return SSD_OK;
+}
 
 size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int headdim,
                                 int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype) {
@@ -256,26 +276,17 @@ int ssd_chunk_fused(const void* x, const void* B, const void* C, const float* dt
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_fused launch");
 }
 
-int ssd_scan_fwd(const void* x, const void* dt, const float* dt_bias, int dt_softplus,
-                 float dt_limit_lo, float dt_limit_hi, const float* A, const void* B,
-                 const void* C, const float* D, const void* z, const float* initial_states,
-                 const int32_t* seq_idx, int64_t batch, int64_t seqlen, int nheads, int headdim,
-                 int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype, void* out,
-                 float* final_states, void* workspace, size_t workspace_bytes, void* stream) {
-  g_err[0] = 0;
-  ssd::Dims d;
-  int rc = check_dtype(dtype);
-  if (rc) return rc;
-  rc = check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d);
-  if (rc) return rc;
-  if (!x || !dt || !A || !B || !C || !out)
-    return fail(SSD_ERR_NULL, "x, dt, A, B, C and out are required");
-  if (!(dt_limit_lo <= dt_limit_hi)) return fail(SSD_ERR_ARG, "dt_limit lo > hi");
-  const void* ptrs[] = {x, dt, dt_bias, A, B, C, D, z, initial_states, seq_idx, out,
-                        final_states, workspace};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
+}  // extern "C"
 
+namespace {
+
+// The forward on validated sizes (and strides): workspace, dispatch, launches.
+int scan_fwd_run(const ssd::Dims& d, const void* x, const void* dt, const float* dt_bias,
+                 int dt_softplus, float dt_limit_lo, float dt_limit_hi, const float* A,
+                 const void* B, const void* C, const float* D, const void* z,
+                 const float* initial_states, const int32_t* seq_idx, ssd_dtype_t dtype,
+                 void* out, float* final_states, void* workspace, size_t workspace_bytes,
+                 void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t need = carve(d, nullptr).bytes;
   void* base = workspace;
@@ -341,6 +352,81 @@ int ssd_scan_fwd(const void* x, const void* dt, const float* dt_bias, int dt_sof
     if (e == cudaSuccess) e = e2;
   }
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "ssd_scan_fwd launch");
+}
+
+int check_fwd_args(const void* x, const void* dt, const float* dt_bias, float lo, float hi,
+                   const float* A, const void* B, const void* C, const float* D, const void* z,
+                   const float* initial_states, const int32_t* seq_idx, void* out,
+                   float* final_states, void* workspace) {
+  if (!x || !dt || !A || !B || !C || !out)
+    return fail(SSD_ERR_NULL, "x, dt, A, B, C and out are required");
+  if (!(lo <= hi)) return fail(SSD_ERR_ARG, "dt_limit lo > hi");
+  const void* ptrs[] = {x, dt, dt_bias, A, B, C, D, z, initial_states, seq_idx, out,
+                        final_states, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
+  return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_scan_fwd(const void* x, const void* dt, const float* dt_bias, int dt_softplus,
+                 float dt_limit_lo, float dt_limit_hi, const float* A, const void* B,
+                 const void* C, const float* D, const void* z, const float* initial_states,
+                 const int32_t* seq_idx, int64_t batch, int64_t seqlen, int nheads, int headdim,
+                 int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype, void* out,
+                 float* final_states, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d);
+  if (rc) return rc;
+  rc = check_fwd_args(x, dt, dt_bias, dt_limit_lo, dt_limit_hi, A, B, C, D, z, initial_states,
+                      seq_idx, out, final_states, workspace);
+  if (rc) return rc;
+  return scan_fwd_run(d, x, dt, dt_bias, dt_softplus, dt_limit_lo, dt_limit_hi, A, B, C, D, z,
+                      initial_states, seq_idx, dtype, out, final_states, workspace,
+                      workspace_bytes, stream);
+}
+
+int ssd_scan_fwd_strided(const void* x, ssd_stride_t x_stride, const void* dt,
+                         ssd_stride_t dt_stride, const float* dt_bias, int dt_softplus,
+                         float dt_limit_lo, float dt_limit_hi, const float* A, const void* B,
+                         ssd_stride_t B_stride, const void* C, ssd_stride_t C_stride,
+                         const float* D, const void* z, ssd_stride_t z_stride,
+                         const float* initial_states, const int32_t* seq_idx, int64_t batch,
+                         int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                         int chunk_size, ssd_dtype_t dtype, void* out, float* final_states,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  ssd::Dims d;
+  int rc = check_dtype(dtype);
+  if (rc) return rc;
+  rc = check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d);
+  if (rc) return rc;
+  rc = check_fwd_args(x, dt, dt_bias, dt_limit_lo, dt_limit_hi, A, B, C, D, z, initial_states,
+                      seq_idx, out, final_states, workspace);
+  if (rc) return rc;
+  const ssd_stride_t given[5] = {x_stride, dt_stride, B_stride, C_stride, z_stride};
+  const char* names[5] = {"x", "dt", "B", "C", "z"};
+  for (int i = 0; i < 5; ++i) {
+    if (i == 4 && z == nullptr) continue;
+    if (given[i].batch < 0 || given[i].token < 0 || given[i].batch > (1LL << 40) ||
+        given[i].token > (1LL << 40))
+      return fail(SSD_ERR_ARG, "%s strides must be in [0, 2^40] elements (got %lld, %lld)",
+                  names[i], (long long)given[i].batch, (long long)given[i].token);
+  }
+  d.sx = {x_stride.batch, x_stride.token};
+  d.sdt = {dt_stride.batch, dt_stride.token};
+  d.sB = {B_stride.batch, B_stride.token};
+  d.sC = {C_stride.batch, C_stride.token};
+  if (z) d.sz = {z_stride.batch, z_stride.token};
+  return scan_fwd_run(d, x, dt, dt_bias, dt_softplus, dt_limit_lo, dt_limit_hi, A, B, C, D, z,
+                      initial_states, seq_idx, dtype, out, final_states, workspace,
+                      workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -20,18 +20,33 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 }
 
 // 2^x on the SFU (PTX ex2.approx, flush-to-zero).  Every exponential of the
-// scan is exp(v) with v <= 0 (a decay), evaluated as 2^(v*log2 e).
+// scan is exp(v), evaluated as 2^(v*log2 e); v <= 0 (a decay) whenever dt >= 0,
+// and v > 0 only when the caller turns softplus off and passes negative dt
+// (the state then grows; the result overflows only where the true value
+// leaves the fp32 range).
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// Problem sizes as every launcher sees them.
+// Element strides between batch rows and between tokens of a
+// [batch, seqlen, ...] input whose per-token part is dense (x, z: [nheads,
+// headdim]; dt: [nheads]; B, C: [ngroups, dstate]).
+struct TokStride {
+  int64_t b, t;
+};
+__host__ __device__ __forceinline__ int64_t toff(const TokStride& s, int64_t b, int64_t t) {
+  return b * s.b + t * s.t;
+}
+
+// Problem sizes as every launcher sees them, and the strides of the inputs
+// (dense unless the caller gave others); out is always dense.
 struct Dims {
   int64_t batch, seqlen;
   int nheads, headdim, dstate, ngroups, chunk;
   int nchunks;
+  TokStride sx, sdt, sB, sC, sz;
 };
 
 // Launchers (return cudaGetLastError() of their launches).
@@ -70,6 +85,10 @@ struct FusedVectors {
   const int32_t* seg;            // or null
 };
 bool fused_eligible(const Dims& d, bool bf16);
+// Device-wide status of the fused kernel's bounded waits: the error bits
+// recorded since the last reset into *bits (0: none); synchronises st.
+// Returns 0 or the cudaError_t of a failed copy.
+int fused_status(int reset, cudaStream_t st, int* bits);
 size_t fused_ctrl_ints(const Dims& d);
 cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* B, const __nv_bfloat16* C,
                          const FusedVectors& v, const float* D, const __nv_bfloat16* z,

@@ -68,7 +68,7 @@ constexpr int kComputeThreads = 128 * kNH * kHalves;
 constexpr int kVecWarp = kComputeWarp0 + kComputeThreads / 32;   // tickets and vectors
 constexpr int kThreads = (kVecWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr unsigned long long kWaitNs = 2000000000ull;   // any single wait: 2 s at most
+constexpr unsigned long long kWaitNs = 2000000000ull;   // default limit of any single wait: 2 s
 constexpr uint32_t kSleepHintNs = 20000;                 // suspend hint of one try_wait
 
 // TMEM columns: two 128-column regions R0 / R1 that trade roles every
@@ -82,10 +82,17 @@ constexpr uint32_t kT_R0 = 0, kT_YE = 128, kT_R1 = 256, kT_H = 384;
 // region from which it read its own Yi_e half of the previous step
 __host__ __device__ constexpr uint32_t m_col(int h) { return 32 * (h & 1) + 8 * (h >> 1); }
 
-// error bits in the control block word ctrl[1]; once one is set every later
-// wait of the launch returns at once, so a broken launch still ends quickly
+// error bits in the control block word ctrl[1] (and in the device-wide
+// status word below); once one is set every later wait of the launch
+// returns at once, every role stops issuing work, waits for its own copies
+// and MMAs in flight, and the launch ends
 constexpr int kErrBarrier = 1;
 constexpr int kErrLookback = 2;
+constexpr int kErrDrain = 4;   // an in-flight copy or MMA did not complete in time
+
+// Sticky status of this device: the error bits of every launch since the
+// last reset (ssd_scan_status), whatever workspace the launch used.
+__device__ int g_status;
 
 // B operand of the CB and Ye chains, K-major with the 128-byte swizzle: per
 // 64-column (dstate) half, 256 rows of 128 bytes -- rows 0-127 the B tile
@@ -120,6 +127,7 @@ struct alignas(1024) Smem {
   uint64_t cb, yi_done[kNH], y_done;   // MMA commits: CB; Yi_e; Ye and the state chain
   uint64_t hx_ready, m_ready, out_ready;   // compute: h and w o x; M; out tile written
   uint64_t pub;            // the segment's final states are in their slots
+  uint64_t mma_drain;      // every MMA the issuer started has completed (launch end)
   uint32_t tmem_base;
 };
 
@@ -129,7 +137,8 @@ static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory");
 struct Params {
   // per-token vectors: computed here from the raw inputs (dt_raw != null) or
   // read from the stage-1 outputs dt / cs / seg
-  const __nv_bfloat16* dt_raw;   // [B, L, H]
+  const __nv_bfloat16* dt_raw;   // [B, L, H] (strides sdt_b, sdt_t, both even)
+  int64_t sdt_b, sdt_t;
   const float* dt_bias;          // [H] or null
   const float* A;                // [H]
   const int32_t* seq_idx;        // [B, L] or null
@@ -150,6 +159,8 @@ struct Params {
   int B, H, G, Q, nc;
   int seg_chunks;        // chunks per work item (the state stays in TMEM across them)
   long long items;       // B * H/2 * ceil(nc / seg_chunks)
+  unsigned long long wait_ns;   // limit of any single wait
+  int lookback_extra;    // > 0 only in the time-out test: a hand-off flag value never reached
 };
 
 
@@ -182,21 +193,41 @@ __device__ __forceinline__ bool aborted(const int* ctrl) {
   return *reinterpret_cast<const volatile int*>(ctrl + 1) != 0;
 }
 
-// Bounded wait on an mbarrier phase: gives up after kWaitNs (or at once when
+__device__ __forceinline__ void record_error(int* ctrl, int bits) {
+  atomicOr(ctrl + 1, bits);
+  atomicOr(&g_status, bits);
+}
+
+// Bounded wait on an mbarrier phase: gives up after wait_ns (or at once when
 // the launch has already been aborted) and records the error.  Returns
-// whether the phase completed, so that a loop can stop after a failed wait
-// without reading the error word on its fast path.
-__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int* ctrl) {
+// whether the phase completed; every caller stops issuing work after a
+// failed wait.
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int* ctrl,
+                                             unsigned long long wait_ns) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (tc::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if ((i & 15u) == 0) {
       if (aborted(ctrl)) return false;
-      if (global_ns() - t0 > kWaitNs) {
-        atomicOr(ctrl + 1, kErrBarrier);
+      if (global_ns() - t0 > wait_ns) {
+        record_error(ctrl, kErrBarrier);
         return false;
       }
+    }
+  }
+}
+
+// Wait at the end of a launch for a phase of asynchronous work this thread
+// started (TMA loads, MMAs): bounded, but not cut short by an abort, so that
+// nothing is still writing shared memory or TMEM when the CTA releases them.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* ctrl,
+                                           unsigned long long wait_ns) {
+  const unsigned long long t0 = global_ns();
+  while (!tc::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
+    if (global_ns() - t0 > wait_ns) {
+      record_error(ctrl, kErrDrain);
+      return;
     }
   }
 }
@@ -232,14 +263,16 @@ __device__ __forceinline__ void vec_load(const Params& p, const Unit& it, int la
       r.a[e] = p.A[it.h0 + e] * kLog2e;
       r.bias[e] = p.dt_bias ? p.dt_bias[it.h0 + e] : 0.f;
     }
-    // the pair's two dt values of a token are adjacent
-    const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(
-        p.dt_raw + ((int64_t)it.b * p.L + it.t0) * p.H + it.h0);
+    // the pair's two dt values of a token are adjacent (h0 and the strides
+    // are even, so each pair is one aligned 32-bit word)
+    const __nv_bfloat16* src = p.dt_raw + it.b * p.sdt_b + it.t0 * p.sdt_t + it.h0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int tok = lane * E + i;
-      r.dt[i] = (i < E && tok < it.nvalid) ? __bfloat1622float2(src[(int64_t)tok * (p.H / 2)])
-                                           : make_float2(0.f, 0.f);
+      r.dt[i] = (i < E && tok < it.nvalid)
+                    ? __bfloat1622float2(
+                          *reinterpret_cast<const __nv_bfloat162*>(src + (int64_t)tok * p.sdt_t))
+                    : make_float2(0.f, 0.f);
     }
     if (p.seq_idx) {
       const int32_t* sq = p.seq_idx + (int64_t)it.b * p.L;
@@ -256,6 +289,9 @@ __device__ __forceinline__ void vec_load(const Params& p, const Unit& it, int la
 // The per-token vectors of both heads of one unit, written by the 32 lanes
 // of a warp from what vec_load fetched.  Positions past the sequence end get
 // dt = 0, so that l and the reset count keep their last values there.
+// kSigned: dt may be negative (softplus off); mv then holds l itself and the
+// diagonal blocks multiply by dt explicitly.
+template <bool kSigned>
 __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, const VecRaw& r,
                                             float (*lv)[kQmax], float (*dtv)[kQmax],
                                             float (*mv)[kQmax], float (*bv)[kQmax], int* segv,
@@ -289,7 +325,8 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
           const float l = excl + loc[i];
           dtv[e][lane * E + i] = dv[i];
           lv[e][lane * E + i] = l;
-          mv[e][lane * E + i] = dv[i] > 0.f ? l - __log2f(dv[i]) : __int_as_float(0x7f800000);
+          mv[e][lane * E + i] = kSigned ? l
+                                        : (dv[i] > 0.f ? l - __log2f(dv[i]) : __int_as_float(0x7f800000));
           bv[e][lane * E + i] = ex2(lf - l) * dv[i];
         }
       }
@@ -317,7 +354,7 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
         const float l = p.cs[pq * Q + i] * kLog2e, d = p.dt[pq * Q + i];
         lv[e][i] = l;
         dtv[e][i] = d;
-        mv[e][i] = d > 0.f ? l - __log2f(d) : __int_as_float(0x7f800000);
+        mv[e][i] = kSigned ? l : (d > 0.f ? l - __log2f(d) : __int_as_float(0x7f800000));
       }
       __syncwarp();
       for (int i = lane; i < Q; i += 32) bv[e][i] = ex2(lv[e][i | 31] - lv[e][i]) * dtv[e][i];
@@ -389,6 +426,7 @@ __device__ __forceinline__ void load_slot_quads(uint32_t (&hv)[16], const float*
                  : "memory");
 }
 
+template <bool kSigned>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_kernel(const __grid_constant__ CUtensorMap map_x,
                      const __grid_constant__ CUtensorMap map_b,
@@ -419,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&s.m_ready, kComputeThreads);
     tc::mbar_init(&s.out_ready, kComputeThreads);
     tc::mbar_init(&s.pub, kComputeThreads);
+    tc::mbar_init(&s.mma_drain, 1);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(&s.tk_full[i], 32);   // the 32 lanes of the vector warp
       tc::mbar_init(&s.tk_empty[i], 2 + kComputeThreads / 32);   // TMA, MMA lanes + compute warps
@@ -434,6 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem_base;
+  auto W = [&](uint64_t* bar, uint32_t parity) {
+    return wait_or_flag(bar, parity, p.ctrl, p.wait_ns);
+  };
+  // the same for all 32 lanes of a warp that then runs warp-collective code
+  // (tcgen05.ld / st, shuffles): a lane stops only when the whole warp does
+  auto WW = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, W(bar, parity)) != 0;
+  };
 
   // Every role walks the same sequence of sub-steps k = 0, 1, ... (the units
   // the vector warp publishes, nsub sub-steps each); the barriers complete
@@ -447,7 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int u = 0, sub = 0;
       uint32_t npub = 0;
-      bool live = wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+      uint32_t n_cbx = 0, n_z = 0;   // phases armed on cbfull / xfull and on zfull
+      bool live = W(&s.tk_full[0], 0);
       Unit cur = s.uk[0];
       live = live && s.tk[0] < p.items;
       tc::mbar_arrive(&s.tk_empty[0]);
@@ -457,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_stream = tc::l2_policy_evict_first();
       const uint64_t pol_keep = tc::l2_policy_evict_last();
       auto load_cbx = [&](const Unit& it, int sb, int xb) {
+        ++n_cbx;
         const int tok = (int)(it.t0 + sb * kSub);
         tc::mbar_arrive_expect_tx(&s.cbfull, 2 * kSub * kN * 2);
         tc::tma_load_4d_hint(s.C, &map_c, &s.cbfull, 0, it.g, tok, it.b, pol_keep);
@@ -468,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_load_4d_hint(s.XB[xb][1], &map_x, &s.xfull, 0, it.h0 + 1, tok, it.b, pol_stream);
       };
       auto load_z = [&](const Unit& it, int sb) {
+        ++n_z;
         if (p.z) {
           const int tok = (int)(it.t0 + sb * kSub);
           tc::mbar_arrive_expect_tx(&s.zfull, kNH * kSub * kP * 2);
@@ -488,25 +538,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool has_next = true;
         if (nsb == cur.nsub) {
           const int ns = (u + 1) % kRing;
-          has_next = wait_or_flag(&s.tk_full[ns], ((u + 1) / kRing) & 1, p.ctrl);
+          has_next = W(&s.tk_full[ns], ((u + 1) / kRing) & 1);
           has_next = has_next && s.tk[ns] < p.items;
           nxt = s.uk[ns];
           tc::mbar_arrive(&s.tk_empty[ns]);
           nsb = 0;
         }
-        wait_or_flag(&s.y_done, k & 1, p.ctrl);
+        // after a failed wait nothing more is issued (the launch is aborted)
+        if (!W(&s.y_done, k & 1)) break;
         if (has_next) load_cbx(nxt, nsb, (k + 1) & 1);
         if (sub == cur.nsub - 1 && cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
           // the segment's final states are in their slots once every compute
           // thread has arrived on pub; the release store orders them before
           // the flag at gpu scope (its consumer waits for flag >= its first chunk)
-          wait_or_flag(&s.pub, npub & 1, p.ctrl);
+          if (!W(&s.pub, npub & 1)) break;
           asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + cur.pair),
                        "r"(cur.c + 1)
                        : "memory");
           ++npub;
         }
-        wait_or_flag(&s.out_ready, k & 1, p.ctrl);
+        if (!W(&s.out_ready, k & 1)) break;
         {
           // rows past the sequence end are outside the tensor map and not written
           const int tok = (int)(cur.t0 + sub * kSub);
@@ -514,16 +565,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_store_4d_hint(&map_out, s.Z[1], 0, cur.h0 + 1, tok, cur.b, pol_stream);
           tc::bulk_commit();
         }
-        if (!has_next) {
-          tc::bulk_wait_all();
-          break;
-        }
+        if (!has_next) break;
         tc::bulk_wait_read();
         load_z(nxt, nsb);
         if (nsb == 0) ++u;
         cur = nxt;
         sub = nsb;
       }
+      // the loads in flight land before the CTA may exit: every phase but the
+      // last armed one of each barrier has been waited for by its consumers
+      if (n_cbx > 0) {
+        drain_wait(&s.cbfull, (n_cbx - 1) & 1, p.ctrl, p.wait_ns);
+        drain_wait(&s.xfull, (n_cbx - 1) & 1, p.ctrl, p.wait_ns);
+      }
+      if (n_z > 0) drain_wait(&s.zfull, (n_z - 1) & 1, p.ctrl, p.wait_ns);
+      tc::bulk_wait_all();
     }
   } else if (warp == kVecWarp) {
     // ---------------- tickets and per-token vectors: the raw inputs of the
@@ -537,9 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t_cur < p.items) vec_load(p, decode(p, t_cur, 0), lane, raw);
     for (int u = 0;; ++u) {
       const int slot = u % kRing;
-      const bool ok = wait_or_flag(&s.tk_empty[slot], ((u / kRing) & 1) ^ 1, p.ctrl);
+      const bool ok = WW(&s.tk_empty[slot], ((u / kRing) & 1) ^ 1);
       if (t_cur < p.items)
-        vec_compute(p, decode(p, t_cur, j_cur), raw, s.lv[slot], s.dtv[slot], s.mv[slot],
+        vec_compute<kSigned>(p, decode(p, t_cur, j_cur), raw, s.lv[slot], s.dtv[slot], s.mv[slot],
                     s.bv[slot], s.segv[slot], lane);
       if (lane == 0) {
         s.tk[slot] = t_cur;
@@ -591,19 +647,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       int u = 0, sub = 0;
-      bool live = wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+      bool live = W(&s.tk_full[0], 0);
       int nsub = s.uk[0].nsub;
       live = live && s.tk[0] < p.items;
       tc::mbar_arrive(&s.tk_empty[0]);
       if (live) {
-        wait_or_flag(&s.cbfull, 0, p.ctrl);
+        live = W(&s.cbfull, 0);
         tc::fence_after_sync();
-        cb_chain(TR(0));
-        tc::mma_commit(&s.cb);
+        if (live) {
+          cb_chain(TR(0));
+          tc::mma_commit(&s.cb);
+        }
       }
+      // after a failed wait nothing more is issued (the launch is aborted)
       for (uint32_t k = 0; live; ++k) {
         const uint32_t ph = k & 1, bc = k & 1;
-        wait_or_flag(&s.hx_ready, ph, p.ctrl);   // h_e and w o x_e written, Ye read out
+        if (!W(&s.hx_ready, ph)) break;   // h_e and w o x_e written, Ye read out
         tc::fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {   // [Ye_0 | Ye_1] = C [h_0 | h_1], K = dstate
@@ -615,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk)     // [H_0 | H_1] += B^T [w o x_0 | w o x_1], K = tokens
           tc::mma_ss(tmem + kT_H, dBmn + kk * 128, dXW + (bc ^ 1) * kNH * kXTile + kk * 128, id_s, 1);
         tc::mma_commit(&s.y_done);
-        wait_or_flag(&s.m_ready, ph, p.ctrl);
+        if (!W(&s.m_ready, ph)) break;
         tc::fence_after_sync();
 #pragma unroll
         for (int e = 0; e < kNH; ++e) {    // Yi_e = M_e x_e (M holds the D skip), K = tokens
@@ -628,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++sub == nsub) {
           ++u;
           const int ns = u % kRing;
-          live = wait_or_flag(&s.tk_full[ns], (u / kRing) & 1, p.ctrl);
+          live = W(&s.tk_full[ns], (u / kRing) & 1);
           nsub = s.uk[ns].nsub;
           live = live && s.tk[ns] < p.items;
           tc::mbar_arrive(&s.tk_empty[ns]);
@@ -637,12 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!live) break;
         // CB_{k+1} overwrites the columns Yi read M from: wait until Yi is done
         // (in-order execution is only promised along one accumulator)
-        wait_or_flag(&s.yi_done[kNH - 1], ph, p.ctrl);
-        wait_or_flag(&s.cbfull, ph ^ 1, p.ctrl);   // C, B of step k+1
+        if (!W(&s.yi_done[kNH - 1], ph)) break;
+        if (!W(&s.cbfull, ph ^ 1)) break;   // C, B of step k+1
         tc::fence_after_sync();
         cb_chain(TR(bc ^ 1));
         tc::mma_commit(&s.cb);
       }
+      // every MMA issued above completes before TMEM is released
+      tc::mma_commit(&s.mma_drain);
+      drain_wait(&s.mma_drain, 0, p.ctrl, p.wait_ns);
     }
   } else {
     // ---------------- compute: warp (head e, half hf, quarter qr) owns row
@@ -716,27 +778,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the state entering a segment (its first chunk), this row, into T_H:
     // the initial state or zeros for chunk 0, else the predecessor segment's
     // final state once its flag is raised (it raises the flag after both
-    // heads' slots are written)
-    auto load_hin = [&](const Unit& it) {
+    // heads' slots are written).  Returns false when the wait for the flag
+    // gave up (the launch is then aborted and nothing is stored).
+    auto load_hin = [&](const Unit& it) -> bool {
       const int64_t bh = (int64_t)it.b * p.H + it.h0 + e;
       // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
       const float* slot_src = p.slots + ((bh * 2 + ((it.c - 1) & 1)) * (kP / 4) * kN + r) * 4;
+      bool ok = true;
       if (it.c > 0) {
         const unsigned long long w0 = global_ns();
         int v;
         for (uint32_t i = 0;; ++i) {
           asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + it.pair) : "memory");
-          if (v >= it.c) break;
+          if (v >= it.c + p.lookback_extra) break;
           if ((i & 63u) == 63u) {
-            if (aborted(p.ctrl)) break;
-            if (global_ns() - w0 > kWaitNs) {
-              atomicOr(p.ctrl + 1, kErrLookback);
+            if (aborted(p.ctrl)) {
+              ok = false;
+              break;
+            }
+            if (global_ns() - w0 > p.wait_ns) {
+              record_error(p.ctrl, kErrLookback);
+              ok = false;
               break;
             }
           }
           __nanosleep(64);
         }
       }
+      if (!__all_sync(0xffffffffu, ok)) return false;   // the whole warp stops
 #pragma unroll
       for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 headdim columns at a time
         const int pc = p0 + qd * 16;
@@ -753,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tmem_st16(T_Hr + qd * 16, hv);
       }
+      return true;
     };
     // per-row scalars of a step (positions past the end hold the chunk's last values)
     struct RowV {
@@ -777,16 +847,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     int u = 0, slot = 0, sub = 0;
-    bool live = wait_or_flag(&s.tk_full[0], 0, p.ctrl);
+    bool live = WW(&s.tk_full[0], 0);
     live = live && s.tk[0] < p.items;
     float l_prev = 0.f;   // l and reset count where the previous sub-step of the
     int sg_prev = 0;      // chunk ended (0 at a chunk start: the cumsum restarts)
     if (live) {           // step 0: entering state, h and w o x
       const Unit& it = s.uk[0];
-      load_hin(it);
+      live = load_hin(it);
       const RowV v = row_of(0, 0);
-      h_convert(v.sg_last == 0 ? ex2(v.l_last) : 0.f);
-      wait_or_flag(&s.xfull, 0, p.ctrl);
+      if (live) h_convert(v.sg_last == 0 ? ex2(v.l_last) : 0.f);
+      live = live && WW(&s.xfull, 0);
+    }
+    if (live) {
+      const Unit& it = s.uk[0];
+      const RowV v = row_of(0, 0);
       wx(w_of(v, 0, it.nvalid), 0);
       tc::fence_proxy_async_smem();   // h and w o x for the MMAs
       tc::fence_before_sync();
@@ -811,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // column (both <= 1); the diagonal block takes one exp2 per element.
       // The D skip rides on the diagonal: M_rr += D, so that M x includes
       // D x_r.  Masks are selects.
-      wait_or_flag(&s.cb, ph, p.ctrl);
+      if (!WW(&s.cb, ph)) break;
       tc::fence_after_sync();
       const float* mcol = s.mv[slot][e] + sub * kSub;
       const float* bcol = s.bv[slot][e] + sub * kSub;
@@ -845,6 +919,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 d = up2(fma2(pk2(colv[i], colv[i + 1]), neg2, lr2));   // l_r - mcol
             uint64_t val = mul2(pk2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
                                 pk2(ex2(d.x), ex2(d.y)));
+            if constexpr (kSigned) {   // mcol holds l_j: the dt_j factor comes here
+              const float* dcol = s.dtv[slot][e] + sub * kSub + c0;
+              val = mul2(val, pk2(dcol[i], dcol[i + 1]));
+            }
             if ((i >> 1) == (t >> 1)) val = add2(val, dpair);
             const float2 f = up2(val);
             m[i] = f.x;
@@ -901,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool has_next = true;
       if (nsb == cur.nsub) {
         nslot = (u + 1) % kRing;
-        has_next = wait_or_flag(&s.tk_full[nslot], ((u + 1) / kRing) & 1, p.ctrl);
+        has_next = WW(&s.tk_full[nslot], ((u + 1) / kRing) & 1);
         has_next = has_next && s.tk[nslot] < p.items;
         nsb = 0;
       }
@@ -919,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- once step k's state chain is done: a segment's final states are
       // handed on (or written out); otherwise step k+1's h and carried state,
       // while the Yi MMAs run
-      wait_or_flag(&s.y_done, ph, p.ctrl);
+      if (!WW(&s.y_done, ph)) break;
       tc::fence_after_sync();
       if (seg_end) {
         const int64_t bh = (int64_t)cur.b * p.H + cur.h0 + e;
@@ -957,8 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // head 0 starts while Yi_1 runs
       {
         const float rho_r = sg_r == sg_prev ? ex2(l_r - l_prev) : 0.f;
-        wait_or_flag(&s.yi_done[e], ph, p.ctrl);
-        wait_or_flag(&s.zfull, ph, p.ctrl);
+        if (!WW(&s.yi_done[e], ph) || !WW(&s.zfull, ph)) break;
         tc::fence_after_sync();
         const uint32_t T_YIr = T_R(bc) + e * kP + p0;
         unsigned char* zrow = s.Z[e] + r * 128;
@@ -1004,10 +1081,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- step k+1: a new segment's entering state; then w o x
       if (seg_end) {
-        load_hin(nxt);
+        if (!load_hin(nxt)) break;
         h_convert(carry_n);
       }
-      wait_or_flag(&s.xfull, ph ^ 1, p.ctrl);
+      if (!WW(&s.xfull, ph ^ 1)) break;
       wx(w_of(vn, nsb, nxt.nvalid), bc ^ 1);
       tc::fence_proxy_async_smem();   // h and w o x for the MMAs
       tc::fence_before_sync();
@@ -1063,15 +1140,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor [d3][d2][d1][d0] (d0 contiguous); box = 64 x 1 x 128 x 1 with the
-// 128-byte swizzle, i.e. one [128 rows][64] operand block per copy; rows past
-// d2 (the sequence end) are filled with zeros.
+// bf16 tensor [d3][d2][d1][d0] (d0 contiguous, d1 rows d0 apart, d2 = tokens
+// st.t elements apart, d3 = batch rows st.b apart); box = 64 x 1 x 128 x 1
+// with the 128-byte swizzle, i.e. one [128 rows][64] operand block per copy;
+// rows past d2 (the sequence end) are filled with zeros.
 bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint64_t d3) {
+              uint64_t d3, TokStride st) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {d0, d1, d2, d3};
-  cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  cuuint64_t strides[3] = {d0 * 2, (cuuint64_t)st.t * 2, (cuuint64_t)st.b * 2};
   cuuint32_t box[4] = {64, 1, 128, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
@@ -1096,9 +1174,16 @@ int sm_count() {
 }  // namespace
 
 bool fused_eligible(const Dims& d, bool bf16) {
+  // TMA: token and batch strides of x, z, B, C multiples of 16 bytes (8 bf16
+  // elements), positive and below 2^39 elements; dt read as bf16 pairs: even strides
+  auto tma_ok = [](const TokStride& s) {
+    return s.b > 0 && s.t > 0 && s.b % 8 == 0 && s.t % 8 == 0 && s.b < (1LL << 39) &&
+           s.t < (1LL << 39);
+  };
   return bf16 && d.headdim == fused::kP && d.dstate == fused::kN &&
          (d.chunk == 128 || d.chunk == 256) && (d.nheads / d.ngroups) % fused::kNH == 0 &&
-         d.seqlen <= (int64_t)1 << 30;
+         d.seqlen <= (int64_t)1 << 30 && tma_ok(d.sx) && tma_ok(d.sz) && tma_ok(d.sB) &&
+         tma_ok(d.sC) && d.sdt.b % 2 == 0 && d.sdt.t % 2 == 0;
 }
 
 size_t fused_ctrl_ints(const Dims& d) { return 64 + (size_t)d.batch * d.nheads; }
@@ -1109,17 +1194,22 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
                          __nv_bfloat16* out, float* slots, int* ctrl, const Dims& d,
                          cudaStream_t st) {
   CUtensorMap mx, mb, mc, mz, mo;
-  if (!make_map(&mx, x, fused::kP, d.nheads, d.seqlen, d.batch) ||
-      !make_map(&mb, Bm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
-      !make_map(&mc, Cm, fused::kN, d.ngroups, d.seqlen, d.batch) ||
-      !make_map(&mo, out, fused::kP, d.nheads, d.seqlen, d.batch))
+  const int64_t hp = (int64_t)d.nheads * fused::kP;
+  const TokStride dense_out = {d.seqlen * hp, hp};
+  if (!make_map(&mx, x, fused::kP, d.nheads, d.seqlen, d.batch, d.sx) ||
+      !make_map(&mb, Bm, fused::kN, d.ngroups, d.seqlen, d.batch, d.sB) ||
+      !make_map(&mc, Cm, fused::kN, d.ngroups, d.seqlen, d.batch, d.sC) ||
+      !make_map(&mo, out, fused::kP, d.nheads, d.seqlen, d.batch, dense_out))
     return cudaErrorInvalidValue;
-  if (z && !make_map(&mz, z, fused::kP, d.nheads, d.seqlen, d.batch)) return cudaErrorInvalidValue;
+  if (z && !make_map(&mz, z, fused::kP, d.nheads, d.seqlen, d.batch, d.sz))
+    return cudaErrorInvalidValue;
   if (!z) mz = mx;   // never used
   cudaError_t e = cudaMemsetAsync(ctrl, 0, fused_ctrl_ints(d) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   fused::Params p;
   p.dt_raw = v.dt_raw;
+  p.sdt_b = d.sdt.b;
+  p.sdt_t = d.sdt.t;
   p.dt_bias = v.dt_bias;
   p.A = v.A;
   p.seq_idx = v.dt_raw ? v.seq_idx : nullptr;
@@ -1160,22 +1250,60 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   }
   p.seg_chunks = seg;
   p.items = pairs * ((d.nchunks + seg - 1) / seg);
+  // any single wait gives up after 2 s; the time-out test shortens the limit
+  // and asks for a hand-off flag value that is never reached
+  p.wait_ns = fused::kWaitNs;
+  p.lookback_extra = 0;
+  if (const char* ov = getenv("SSD_FUSED_WAIT_NS")) {
+    const long long v = atoll(ov);
+    if (v > 0) p.wait_ns = (unsigned long long)v;
+  }
+  if (const char* ov = getenv("SSD_FUSED_TEST_STALL"))
+    if (atoi(ov) == 1) p.lookback_extra = 1 << 24;
+  // dt can be negative only without softplus (and no clamp to a non-negative
+  // floor), or when the clamp's ceiling is negative; stage-1 outputs given
+  // by the caller are taken as possibly negative
+  const bool nonneg = v.dt_raw && (v.softplus ? (!v.do_clamp || v.hi >= 0.f)
+                                              : (v.do_clamp && v.lo >= 0.f));
   const size_t smem = sizeof(fused::Smem) + 1024;
-  // the shared-memory opt-in is a property of the kernel on each device
-  static std::atomic<bool> attr_set[64];
+  // the shared-memory opt-in is a property of each kernel on each device
+  static std::atomic<bool> attr_set[2][64];
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const bool known = dev >= 0 && dev < 64;
-  if (!known || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(fused::ssd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+  const int which = nonneg ? 0 : 1;
+  if (!known || !attr_set[which][dev].load(std::memory_order_acquire)) {
+    e = nonneg ? cudaFuncSetAttribute(fused::ssd_fused_kernel<false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+               : cudaFuncSetAttribute(fused::ssd_fused_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (known) attr_set[dev].store(true, std::memory_order_release);
+    if (known) attr_set[which][dev].store(true, std::memory_order_release);
   }
   const long long grid = std::min<long long>(p.items, sm_count());   // one CTA per SM
-  fused::ssd_fused_kernel<<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz, mo, p);
+  if (nonneg)
+    fused::ssd_fused_kernel<false><<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz,
+                                                                                 mo, p);
+  else
+    fused::ssd_fused_kernel<true><<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz,
+                                                                                mo, p);
   return cudaGetLastError();
+}
+
+int fused_status(int reset, cudaStream_t st, int* bits) {
+  int h = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&h, fused::g_status, sizeof(int), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && reset && h != 0) {
+    static const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(fused::g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  }
+  *bits = h;
+  return e == cudaSuccess ? 0 : (int)e;
 }
 
 }  // namespace ssd

@@ -214,11 +214,19 @@ int ssd_scan_fwd_host(const void* x, const void* dt, const float* dt_bias, int d
       e = cudaMemcpyAsync(hfin + r0 * rb.st, buf + lay.fin, nr * rb.st, d2h, pp.out);
     if (e == cudaSuccess && rc == SSD_OK) e = cudaEventRecord(pp.out_done[bi], pp.out);
   }
-  if (rc != SSD_OK) return rc;   // ssd_scan_fwd set the message
   // `stream` continues once the last slice is copied out
-  if (e == cudaSuccess) e = cudaEventRecord(pp.end, pp.out);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(user, pp.end, 0);
-  if (e != cudaSuccess) return ssd::set_error(SSD_ERR_CUDA, cudaGetErrorString(e));
+  if (e == cudaSuccess && rc == SSD_OK) e = cudaEventRecord(pp.end, pp.out);
+  if (e == cudaSuccess && rc == SSD_OK) e = cudaStreamWaitEvent(user, pp.end, 0);
+  if (e != cudaSuccess || rc != SSD_OK) {
+    // on failure part of the pipeline may already be queued: let the copies
+    // that read or write the caller's host buffers and workspace finish
+    // before the caller gets the error and may free them
+    cudaStreamSynchronize(pp.in);
+    cudaStreamSynchronize(pp.comp);
+    cudaStreamSynchronize(pp.out);
+    if (rc != SSD_OK) return rc;   // ssd_scan_fwd set the message
+    return ssd::set_error(SSD_ERR_CUDA, cudaGetErrorString(e));
+  }
   return SSD_OK;
 }
 

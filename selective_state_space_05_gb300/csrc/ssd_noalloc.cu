@@ -2,7 +2,6 @@
 // device memory.  The scratch that ssd_scan_fwd would take from the caller or
 // from cudaMallocAsync (processed dt, per-chunk cumsum and reset counts, chunk
 // states) lives here in one file-scope device array instead.
-#include <mutex>
 #include <stdio.h>
 
 #include "../../include/ssd_scan.h"
@@ -15,35 +14,20 @@ namespace {
 constexpr size_t kScratchBytes = SSD_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_scratch on the current device.  In host code the name
+// Device address of g_scratch in the current context.  In host code the name
 // g_scratch is only a host-side stand-in; the real address comes from
-// cudaGetSymbolAddress, looked up once per device (with that device current)
-// and cached.
+// cudaGetSymbolAddress with the device current.  It is looked up on every
+// call (cheap once the module is loaded), so that a context that was reset or
+// re-created in between never gets a stale address.
 int scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+  if (e != cudaSuccess || p == nullptr) {
     char m[256];
-    snprintf(m, sizeof(m), "cudaGetDevice: %s", cudaGetErrorString(e));
+    snprintf(m, sizeof(m), "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
     return ssd::set_error(SSD_ERR_CUDA, m);
   }
-  if (dev < 0 || dev >= kMaxDevices) return ssd::set_error(SSD_ERR_UNSUPPORTED, "device index too large");
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      char m[256];
-      snprintf(m, sizeof(m), "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-      return ssd::set_error(SSD_ERR_CUDA, m);
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return SSD_OK;
 }
 

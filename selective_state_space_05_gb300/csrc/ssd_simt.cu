@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(
       const int t = idx >> 5, j = idx & 31;
       float v = 0.f;
       if (t < n && j < hw) {
-        v = to_f(dt[((int64_t)b * d.seqlen + t0 + t) * H + hg + j]);
+        v = to_f(dt[toff(d.sdt, b, t0 + t) + hg + j]);
         if (dt_bias) v += dt_bias[hg + j];
         if (softplus) v = v <= 20.f ? log1pf(__expf(v)) : v;
         if (do_clamp) v = fminf(fmaxf(v, lo), hi);
@@ -165,14 +165,14 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(
     for (int idx = tid; idx < TJ * P; idx += 256) {
       const int jj = idx / P, p = idx % P, j = j0 + jj;
       float v = 0.f;
-      if (j < n) v = to_f(x[(((int64_t)b * d.seqlen + t0 + j) * d.nheads + h) * P + p]) * wj[jj];
+      if (j < n) v = to_f(x[toff(d.sx, b, t0 + j) + (int64_t)h * P + p]) * wj[jj];
       xs[jj][p] = v;
     }
     for (int idx = tid; idx < TJ * NT; idx += 256) {
       const int jj = idx / NT, nn = idx % NT, j = j0 + jj;
       float v = 0.f;
       if (j < n)
-        v = to_f(Bm[(((int64_t)b * d.seqlen + t0 + j) * d.ngroups + g) * d.dstate + ntile * NT + nn]);
+        v = to_f(Bm[toff(d.sB, b, t0 + j) + (int64_t)g * d.dstate + ntile * NT + nn]);
       bs[jj][nn] = v;
     }
     __syncthreads();
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
 
   for (int idx = tid; idx < TI * N; idx += 256) {
     const int ii = idx / N, nn = idx % N, i = i0 + ii;
-    Cs[ii * NP1 + nn] = i < n ? to_f(Cm[((rowBC + i) * d.ngroups + g) * N + nn]) : 0.f;
+    Cs[ii * NP1 + nn] = i < n ? to_f(Cm[toff(d.sC, b, t0 + i) + (int64_t)g * N + nn]) : 0.f;
   }
   if (tid < TI) {
     const int i = min(i0 + tid, Q - 1);
@@ -364,11 +364,11 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
     const int j0 = jt * TJ;
     for (int idx = tid; idx < TJ * N; idx += 256) {
       const int jj = idx / N, nn = idx % N, j = j0 + jj;
-      Bs[jj * NP1 + nn] = j < n ? to_f(Bm[((rowBC + j) * d.ngroups + g) * N + nn]) : 0.f;
+      Bs[jj * NP1 + nn] = j < n ? to_f(Bm[toff(d.sB, b, t0 + j) + (int64_t)g * N + nn]) : 0.f;
     }
     for (int idx = tid; idx < TJ * P; idx += 256) {
       const int jj = idx / P, p = idx % P, j = j0 + jj;
-      xs[jj * P + p] = j < n ? to_f(x[((rowBC + j) * d.nheads + h) * P + p]) * dtc[j] : 0.f;
+      xs[jj * P + p] = j < n ? to_f(x[toff(d.sx, b, t0 + j) + (int64_t)h * P + p]) * dtc[j] : 0.f;
     }
     if (tid < TJ) {
       const int j = min(j0 + tid, Q - 1);
@@ -401,15 +401,17 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
   }
 
   if (irow < n) {
-    const int64_t base = ((rowBC + irow) * d.nheads + h) * P;
+    const int64_t base = ((rowBC + irow) * d.nheads + h) * P;   // out (dense)
+    const int64_t xbase = toff(d.sx, b, t0 + irow) + (int64_t)h * P;
+    const int64_t zbase = toff(d.sz, b, t0 + irow) + (int64_t)h * P;
     const float Dh = D ? D[h] : 0.f;
 #pragma unroll
     for (int k = 0; k < KP; ++k) {
       const int p = cg + 8 * k;
       float y = acc[k];
-      if (D) y = fmaf(Dh, to_f(x[base + p]), y);
+      if (D) y = fmaf(Dh, to_f(x[xbase + p]), y);
       if (z) {
-        const float zz = to_f(z[base + p]);
+        const float zz = to_f(z[zbase + p]);
         y *= zz / (1.f + __expf(-zz));
       }
       out[base + p] = from_f<T>(y);

@@ -28,8 +28,19 @@ def _stream(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _token_dense(t: torch.Tensor) -> bool:
+    """Whether each token's part t[b, l] of a [batch, seqlen, ...] tensor is
+    dense (row-major), so that two strides describe the whole tensor."""
+    want = 1
+    for n, s in zip(reversed(t.shape[2:]), reversed(t.stride()[2:])):
+        if n > 1 and s != want:
+            return False
+        want *= n
+    return True
+
+
 def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, device=None,
-          optional=False, host=False) -> None:
+          optional=False, host=False, strided=False) -> None:
     if t is None:
         if optional:
             return
@@ -40,7 +51,10 @@ def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, device=N
         raise ValueError(f"{name} must be a CUDA tensor")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
-    if not t.is_contiguous():
+    if strided:
+        if not _token_dense(t):
+            raise ValueError(f"{name}: each token's [..] part must be dense")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
@@ -50,6 +64,13 @@ def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, device=N
 
 def abi_version() -> int:
     return _lib.load().ssd_abi_version()
+
+
+def scan_status(reset: bool = True, stream=None) -> None:
+    """Synchronises ``stream`` and raises SSDError(SSD_ERR_TIMEOUT) if a
+    tensor-core launch on this device gave up a bounded internal wait since
+    the last reset (its outputs are then not valid)."""
+    _lib.check(_lib.load().ssd_scan_status(int(bool(reset)), _stream(stream)))
 
 
 def workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
@@ -67,25 +88,29 @@ def ssd_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
                  seq_idx: Optional[torch.Tensor] = None, return_final_states: bool = False,
                  out: Optional[torch.Tensor] = None,
                  final_states: Optional[torch.Tensor] = None,
-                 workspace: Optional[torch.Tensor] = None, stream=None):
+                 workspace: Optional[torch.Tensor] = None, stream=None, check: bool = False):
     """SSD chunked-scan forward.  x, z, out: [batch, seqlen, nheads, headdim];
     dt: [batch, seqlen, nheads] (x dtype); B, C: [batch, seqlen, ngroups, dstate];
     dt_bias, A, D: [nheads] fp32; states [batch, nheads, headdim, dstate] fp32;
-    seq_idx [batch, seqlen] int32.  Returns out, or (out, final_states)."""
+    seq_idx [batch, seqlen] int32.  x, dt, B, C and z may be strided views
+    (slices of a fused projection) as long as each token's part is dense;
+    they then go through ssd_scan_fwd_strided.  check=True synchronises the
+    stream and raises if the launch gave up a bounded wait (ssd_scan_status).
+    Returns out, or (out, final_states)."""
     if x.dtype not in _DT:
         raise ValueError(f"x must be float32 or bfloat16, got {x.dtype}")
     dev = x.device
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     xd = x.dtype
-    _need(x, "x", xd, device=dev)
-    _need(dt, "dt", xd, (Bsz, L, H), dev)
+    _need(x, "x", xd, device=dev, strided=True)
+    _need(dt, "dt", xd, (Bsz, L, H), dev, strided=True)
     _need(A, "A", torch.float32, (H,), dev)
-    _need(B, "B", xd, (Bsz, L, G, N), dev)
-    _need(C, "C", xd, (Bsz, L, G, N), dev)
+    _need(B, "B", xd, (Bsz, L, G, N), dev, strided=True)
+    _need(C, "C", xd, (Bsz, L, G, N), dev, strided=True)
     _need(dt_bias, "dt_bias", torch.float32, (H,), dev, optional=True)
     _need(D, "D", torch.float32, (H,), dev, optional=True)
-    _need(z, "z", xd, (Bsz, L, H, P), dev, optional=True)
+    _need(z, "z", xd, (Bsz, L, H, P), dev, optional=True, strided=True)
     _need(initial_states, "initial_states", torch.float32, (Bsz, H, P, N), dev, optional=True)
     _need(seq_idx, "seq_idx", torch.int32, (Bsz, L), dev, optional=True)
     if out is None:
@@ -100,11 +125,23 @@ def ssd_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     lo, hi = dt_limit
-    _lib.check(lib.ssd_scan_fwd(
-        _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi),
-        _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(initial_states), _ptr(seq_idx),
-        Bsz, L, H, P, N, G, int(chunk_size), _DT[xd], _ptr(out), _ptr(final_states),
-        _ptr(workspace), ws_bytes, _stream(stream)))
+    ins = [x, dt, B, C] + ([z] if z is not None else [])
+    if all(t.is_contiguous() for t in ins):
+        _lib.check(lib.ssd_scan_fwd(
+            _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi),
+            _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(initial_states), _ptr(seq_idx),
+            Bsz, L, H, P, N, G, int(chunk_size), _DT[xd], _ptr(out), _ptr(final_states),
+            _ptr(workspace), ws_bytes, _stream(stream)))
+    else:
+        def st(t):
+            return _lib.Stride(0, 0) if t is None else _lib.Stride(t.stride(0), t.stride(1))
+        _lib.check(lib.ssd_scan_fwd_strided(
+            _ptr(x), st(x), _ptr(dt), st(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo),
+            float(hi), _ptr(A), _ptr(B), st(B), _ptr(C), st(C), _ptr(D), _ptr(z), st(z),
+            _ptr(initial_states), _ptr(seq_idx), Bsz, L, H, P, N, G, int(chunk_size), _DT[xd],
+            _ptr(out), _ptr(final_states), _ptr(workspace), ws_bytes, _stream(stream)))
+    if check:
+        scan_status(reset=True, stream=stream)
     if return_final_states:
         return out, final_states
     return out
@@ -312,8 +349,8 @@ def ssd_scan_fwd_host(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: tor
             _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(initial_states), _ptr(seq_idx),
             Bsz, L, H, P, N, G, int(chunk_size), _DT[xd], _ptr(out), _ptr(final_states),
             int(rows_per_slice), _ptr(workspace), workspace.numel(), _stream(stream)))
-    if synchronize:
-        stream.synchronize()
+        if synchronize:
+            scan_status(reset=True, stream=stream)   # synchronises the stream
     if return_final_states:
         return out, final_states
     return out

@@ -110,20 +110,25 @@ def seq_idx_from_lengths(lengths, batch: int) -> torch.Tensor:
     return ids.unsqueeze(0).expand(batch, -1).contiguous()
 
 
-def make_inputs(cfg: SSDConfig, seed: int, seqlen: Optional[int] = None) -> dict:
-    """Draw one set of inputs on the CPU.
+def make_inputs(cfg: SSDConfig, seed: int, seqlen: Optional[int] = None,
+                device="cpu") -> dict:
+    """Draw one set of inputs, on the CPU by default.
 
     Draw order is fixed: x, z, B, C, dt_raw, dt_bias, A, D, initial_states,
-    then the document split.  Returns a dict of CPU tensors keyed by the
-    C-ABI argument names plus the scalar options.
+    then the document split.  Returns a dict of tensors keyed by the C-ABI
+    argument names plus the scalar options.  With a CUDA ``device`` the same
+    recipe is drawn by that device's generator (same distributions, other
+    values; the benchmark uses it for workloads too large to draw on the host
+    quickly, and no parity check compares against such draws).
     """
     L = cfg.seqlen if seqlen is None else seqlen
-    g = torch.Generator().manual_seed(seed)
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(seed)
     dt_ = torch_dtype(cfg.dtype)
     Bsz, H, P, N, G = cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
 
     def normal(*shape, scale=1.0):
-        t = torch.randn(*shape, generator=g, dtype=torch.float32)
+        t = torch.randn(*shape, generator=g, dtype=torch.float32, device=dev)
         if scale != 1.0:
             t.mul_(scale)
         return t
@@ -133,21 +138,22 @@ def make_inputs(cfg: SSDConfig, seed: int, seqlen: Optional[int] = None) -> dict
     Bm = normal(Bsz, L, G, N, scale=cfg.x_scale).to(dt_)
     Cm = normal(Bsz, L, G, N, scale=cfg.x_scale).to(dt_)
     dt = normal(Bsz, L, H).to(dt_)
-    u = torch.rand(H, generator=g, dtype=torch.float64) * (1e-1 - 1e-3) + 1e-3
+    u = torch.rand(H, generator=g, dtype=torch.float64, device=dev) * (1e-1 - 1e-3) + 1e-3
     dt_bias = torch.log(torch.expm1(u)).to(torch.float32)
     lo, hi = cfg.a_log_range
-    A = -torch.exp(torch.rand(H, generator=g, dtype=torch.float64) * (hi - lo) + lo).to(torch.float32)
+    A = -torch.exp(torch.rand(H, generator=g, dtype=torch.float64, device=dev) * (hi - lo)
+                   + lo).to(torch.float32)
     if cfg.d_mode == "normal":
         D = normal(H)
     elif cfg.d_mode == "ramp":
-        D = torch.arange(H, dtype=torch.float32) * 1000.0
+        D = torch.arange(H, dtype=torch.float32, device=dev) * 1000.0
     else:
         D = None
     init = normal(Bsz, H, P, N, scale=cfg.init_std) if cfg.init_std > 0 else None
     seq_idx = None
     if cfg.ndocs > 1:
         lens = dirichlet_lengths(L, cfg.ndocs, seed)
-        seq_idx = seq_idx_from_lengths(lens, Bsz)
+        seq_idx = seq_idx_from_lengths(lens, Bsz).to(dev)
     return dict(x=x, dt=dt, dt_bias=dt_bias, A=A, B=Bm, C=Cm, D=D, z=z,
                 initial_states=init, seq_idx=seq_idx,
                 dt_softplus=cfg.dt_softplus, dt_limit=cfg.dt_limit,

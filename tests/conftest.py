@@ -25,3 +25,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    import json
+    path = os.environ.get("SSD_PARITY_REPORT")
+    if not path:
+        return
+    from ssd_testutil import PARITY_REPORT
+    if PARITY_REPORT:
+        with open(path, "w") as f:
+            json.dump(PARITY_REPORT, f, indent=1, sort_keys=True)

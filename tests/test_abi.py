@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert lib.ssd_abi_version() == 1
+    assert lib.ssd_abi_version() == 2
 
 
 def test_workspace_bytes(lib):
@@ -121,3 +121,26 @@ def test_host_call_validation_before_any_cuda_call(lib):
     args[24], args[25] = 4096, 16
     assert lib.ssd_scan_fwd_host(*args) == -5                # workspace too small
     assert b"workspace" in lib.ssd_last_error()
+
+
+def test_strided_validation_before_any_launch(lib):
+    """Negative or huge strides are refused before anything is launched."""
+    ok, bad, huge = _lib.Stride(1024, 64), _lib.Stride(-1, 64), _lib.Stride(1, 1 << 41)
+
+    def call(xs=ok, dts=ok, bs=ok, cs=ok, zs=ok, z=None, x=16):
+        return lib.ssd_scan_fwd_strided(x, xs, 16, dts, None, 1, 0.0, math.inf, 16, 16, bs, 16,
+                                        cs, None, z, zs, None, None, 1, 64, 2, 16, 16, 1, 64, 0,
+                                        16, None, None, 0, None)
+    assert call(xs=bad) == -1 and b"x strides" in lib.ssd_last_error()
+    assert call(dts=huge) == -1 and b"dt strides" in lib.ssd_last_error()
+    assert call(cs=bad) == -1
+    assert call(zs=bad, z=16) == -1 and b"z strides" in lib.ssd_last_error()
+    assert call(x=None) == -2
+    assert call(x=24) == -3
+
+
+def test_header_declares_status_and_strided_calls():
+    names = declared_functions()
+    assert "ssd_scan_status" in names and "ssd_scan_fwd_strided" in names
+    text = (ROOT / "include" / "ssd_scan.h").read_text()
+    assert "SSD_ERR_TIMEOUT = -7" in text

@@ -220,3 +220,109 @@ def test_fused_segment_lengths_bit_identical(shape, monkeypatch):
     f = f_1.double().cpu().numpy()[batches][:, heads]
     assert_close(y, ry, TOL["bf16"], "out (sampled)")
     assert_close(f, rf, TOL["bf16"], "final (sampled)")
+
+
+# --------------------------------------------------------------------------
+# stage-1 options on the fused path: the dt clamp and softplus off (dt used
+# as given, which may be negative; the kernel then runs its signed-dt form)
+# --------------------------------------------------------------------------
+
+def _signed_dt(d, scale, seed):
+    g = torch.Generator().manual_seed(seed)
+    d["dt"] = (torch.randn(d["dt"].shape, generator=g) * scale).to(d["dt"].dtype)
+    return d
+
+
+DT_OPTION_CASES = [
+    # (id, random_small kwargs, dt rewrite)
+    ("limit_0.02_0.3", dict(seqlen=700, chunk_size=256, init_std=0.3, dt_limit=(0.02, 0.3),
+                            seq_idx_lengths=[300, 400]), None),
+    # the ceiling binds on most tokens (softplus of the biased dt is about 0.7 without bias)
+    ("limit_0_0.05_mostly_clamped", dict(seqlen=600, chunk_size=128, dt_bias=False,
+                                         dt_limit=(0.0, 0.05), init_std=0.3), None),
+    # softplus off, default limit: dt used as given (here non-negative), signed form
+    ("no_softplus_nonneg", dict(seqlen=500, chunk_size=256, dt_softplus=False, dt_bias=False,
+                                init_std=0.3), "abs"),
+    # softplus off with a non-negative clamp floor: the unsigned form
+    ("no_softplus_clamped", dict(seqlen=500, chunk_size=128, dt_softplus=False, dt_bias=False,
+                                 dt_limit=(0.0, 1.0), seq_idx_lengths=[200, 1, 299]), "signed"),
+    # softplus off, negative dt on about half the tokens: the state grows there
+    ("no_softplus_signed", dict(seqlen=640, chunk_size=256, dt_softplus=False, dt_bias=False,
+                                init_std=0.3, a_log_range=(0.0, math.log(4.0)),
+                                seq_idx_lengths=[128, 300, 212]), "signed"),
+    ("no_softplus_signed_q128", dict(seqlen=1000, chunk_size=128, dt_softplus=False,
+                                     dt_bias=False, ngroups=1, nheads=4,
+                                     a_log_range=(0.0, math.log(2.0))), "signed"),
+]
+
+
+@pytest.mark.parametrize("case", DT_OPTION_CASES, ids=[c[0] for c in DT_OPTION_CASES])
+def test_fused_dt_options(case):
+    name, kw, rewrite = case
+    d = _small(3100 + len(name), **kw)
+    if rewrite == "abs":
+        d["dt"] = (d["dt"].float().abs() * 0.2).to(d["dt"].dtype)
+    elif rewrite == "signed":
+        d = _signed_dt(d, 0.05, 3200 + len(name))
+    y, f = _run_fused(d, kw["chunk_size"])
+    ry, rf = oracle.scan_sequential(d)
+    assert np.isfinite(ry).all() and np.abs(ry).max() < 1e30
+    assert_close(y, ry, TOL["bf16"], "out")
+    assert_close(f, rf, TOL["bf16"], "final")
+
+
+def test_fused_stage_entry_point_signed_dt():
+    """ssd_chunk_fused takes caller-given stage-1 outputs as possibly negative."""
+    import selective_state_space_05_gb300 as ssd
+    Q = 256
+    d = _signed_dt(_small(49, seqlen=700, chunk_size=Q, dt_softplus=False, dt_bias=False,
+                          init_std=0.2), 0.05, 50)
+    g = to_dev(d)
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q, dt_softplus=False)
+    ws = torch.empty(ssd.workspace_bytes(2, 700, 4, 64, 128, 2, Q), dtype=torch.uint8,
+                     device="cuda")
+    y, f = ssd.ssd_chunk_fused(g["x"], g["B"], g["C"], dt_out, cs, seg, chunk_size=Q,
+                               workspace=ws, D=g["D"], z=g["z"],
+                               initial_states=g["initial_states"], return_final_states=True)
+    ssd.scan_status(reset=True)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y.double().cpu().numpy(), ry, TOL["bf16"], "out")
+    assert_close(f.double().cpu().numpy(), rf, TOL["bf16"], "final")
+
+
+# --------------------------------------------------------------------------
+# a wait that gives up: reported through the status word, context still usable
+# --------------------------------------------------------------------------
+
+def test_fused_timeout_is_reported(monkeypatch):
+    """A hand-off flag value that nothing ever writes (a test-only launch
+    option) makes the look-back wait of every later segment run out after
+    the shortened limit of 0.2 s; the kernel then stops every role, lets its
+    copies and MMAs in flight finish and ends.  The status word says so, and
+    the next normal launch is correct again."""
+    import selective_state_space_05_gb300 as ssd
+    from selective_state_space_05_gb300._lib import SSD_ERR_TIMEOUT, SSDError
+    d = _small(51, batch=2, seqlen=1024, nheads=4, ngroups=2, chunk_size=128, init_std=0.3)
+    g = to_dev(d)
+    ws = torch.empty(ssd.workspace_bytes(2, 1024, 4, 64, 128, 2, 128), dtype=torch.uint8,
+                     device="cuda")
+    ssd.scan_status(reset=True)
+    monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", "1")
+    monkeypatch.setenv("SSD_FUSED_WAIT_NS", "200000000")
+    monkeypatch.setenv("SSD_FUSED_TEST_STALL", "1")
+    ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=128,
+                     dt_bias=g["dt_bias"], D=g["D"], z=g["z"], workspace=ws)
+    with pytest.raises(SSDError) as ei:
+        ssd.scan_status(reset=False)
+    assert ei.value.code == SSD_ERR_TIMEOUT
+    assert int(ws[4:8].view(torch.int32).item()) & 2, "the hand-off wait should have given up"
+    with pytest.raises(SSDError):
+        ssd.scan_status(reset=True)                  # still set, then cleared
+    ssd.scan_status(reset=True)                      # clear
+    monkeypatch.delenv("SSD_FUSED_TEST_STALL")
+    monkeypatch.delenv("SSD_FUSED_WAIT_NS")
+    y, f = _run_fused(d, 128)
+    ssd.scan_status(reset=True)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["bf16"], "out after the time-out")
+    assert_close(f, rf, TOL["bf16"], "final after the time-out")

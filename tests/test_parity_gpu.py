@@ -15,7 +15,8 @@ import torch
 import oracle
 import ssd_inputs as si
 from oracle import ssd_oracle as so
-from ssd_testutil import TOL, assert_close, errors, run_gpu, to_dev
+from ssd_testutil import (PARITY_REPORT, TOL, ErrorStats, assert_close, errors, run_gpu,
+                          to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -182,17 +183,29 @@ def test_stages_match_chunked_oracle(dtype):
 
 
 # --------------------------------------------------------------------------
-# full-size workloads, in the launch configuration the benchmark times:
-# whole GPU run, oracle on sampled (batch, head) pairs
+# full-size workloads, in the launch configuration the benchmark times: the
+# whole GPU output against the oracle, every (batch, head) pair, in pieces;
+# mean and max errors (and the 99.9th percentile) are recorded for the
+# parity report because SSD kernel errors can be heavy-tailed
 # --------------------------------------------------------------------------
 
-def _sampled_check(d, y_gpu_full, f_gpu_full, batches, heads, tol):
-    ry, rf = so.scan_sequential(d, heads=heads, batches=batches)
-    yg = y_gpu_full[batches][:, :, heads].double().cpu().numpy()
-    fg = f_gpu_full[batches][:, heads].double().cpu().numpy()
-    e = assert_close(yg, ry, tol, "out (sampled)")
-    assert_close(fg, rf, tol, "final (sampled)")
-    return e
+def _full_check(name, d, y_gpu, f_gpu, tol, head_block=16):
+    """Every (batch, head) recurrence of the GPU output against the oracle
+    (run over the whole sequence), accumulated piece by piece."""
+    Bsz, L, H, P = d["x"].shape
+    yg, fg = y_gpu.cpu(), f_gpu.cpu()
+    sy, sf = ErrorStats(), ErrorStats()
+    for b in range(Bsz):
+        for h0 in range(0, H, head_block):
+            hs = list(range(h0, min(H, h0 + head_block)))
+            ry, rf = so.scan_sequential(d, heads=hs, batches=[b])
+            sy.add(yg[b:b + 1, :, h0:h0 + len(hs)].double().numpy(), ry)
+            sf.add(fg[b:b + 1, h0:h0 + len(hs)].double().numpy(), rf)
+    ey, ef = sy.result(), sf.result()
+    PARITY_REPORT[name] = {"out": ey, "final_states": ef, "tol": tol,
+                           "pairs": Bsz * H, "tokens": Bsz * L}
+    assert ey["max_rel"] <= tol, f"{name} out: {ey}"
+    assert ef["max_rel"] <= tol, f"{name} final: {ef}"
 
 
 def _gpu_full(d, chunk):
@@ -201,8 +214,7 @@ def _gpu_full(d, chunk):
     y, f = ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=chunk,
                             dt_bias=g["dt_bias"], D=g["D"], z=g["z"],
                             initial_states=g["initial_states"], seq_idx=g["seq_idx"],
-                            return_final_states=True)
-    torch.cuda.synchronize()
+                            return_final_states=True, check=True)
     return y, f
 
 
@@ -211,7 +223,7 @@ def test_mamba2_2p7b_full_size():
     d = si.make_inputs(cfg, 1002)
     y, f = _gpu_full(d, cfg.chunk_size)
     assert torch.isfinite(y.float()).all()
-    _sampled_check(d, y, f, [0, 7], [0, 1, 40, 79], TOL["bf16"])
+    _full_check("mamba2_2p7b", d, y, f, TOL["bf16"])
 
 
 def test_chained_prefill_full_size():
@@ -221,7 +233,7 @@ def test_chained_prefill_full_size():
     cfg = si.CONFIGS["chained"]
     d = si.make_inputs(cfg, 1003)
     g = to_dev(d)
-    L, seg_len = cfg.seqlen, cfg.seqlen // cfg.segments
+    seg_len = cfg.seqlen // cfg.segments
     y = torch.empty_like(g["x"])
     st = g["initial_states"]
     for s in range(cfg.segments):
@@ -231,12 +243,34 @@ def test_chained_prefill_full_size():
                                   chunk_size=cfg.chunk_size, dt_bias=g["dt_bias"], D=g["D"],
                                   z=part["z"], initial_states=st, return_final_states=True)
         y[:, sl] = ys
-    torch.cuda.synchronize()
-    _sampled_check(d, y, st, [0, 15], [0, 17, 64, 127], TOL["bf16"])
+    ssd.scan_status(reset=True)
+    del g, part
+    _full_check("chained", d, y, st, TOL["bf16"])
 
 
 def test_packed_documents_full_size():
     cfg = si.CONFIGS["packed"]
     d = si.make_inputs(cfg, 1004)
     y, f = _gpu_full(d, cfg.chunk_size)
-    _sampled_check(d, y, f, [0], [0, 5, 77, 127], TOL["bf16"])
+    _full_check("packed", d, y, f, TOL["bf16"], head_block=8)
+
+
+def test_small_workloads_report():
+    """The tiny and grouped workloads whole, for the parity report; the
+    grouped runs also on y - D x silu(z) (D_h = 1000 h dominates max|ref| and
+    could hide scan errors; both sides lose the same exactly computed term)."""
+    for name, seed in (("tiny", 1000), ("grouped_g1", 1001), ("grouped_g2", 1001),
+                       ("grouped_g4", 1001)):
+        cfg = si.CONFIGS[name]
+        d = si.make_inputs(cfg, seed)
+        y, f = run_gpu(d)
+        ry, rf = oracle.scan_sequential(d)
+        tol = TOL[cfg.dtype]
+        entry = {"out": errors(y, ry), "final_states": errors(f, rf), "tol": tol}
+        if d["D"] is not None and d["z"] is not None:
+            x = d["x"].double().numpy()
+            zz = d["z"].double().numpy()
+            skip = d["D"].double().numpy()[None, None, :, None] * x * zz / (1 + np.exp(-zz))
+            entry["out_minus_Dx"] = errors(y - skip, ry - skip)
+        PARITY_REPORT[name] = entry
+        assert entry["out"]["max_rel"] <= tol and entry["final_states"]["max_rel"] <= tol, entry

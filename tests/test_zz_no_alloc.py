@@ -68,6 +68,9 @@ def test_noalloc_matches_scan_fwd_on_two_calls_in_a_row(lib):
         rc = _noalloc(lib, g, d, out, fin)
         torch.cuda.synchronize()
         assert rc == 0, lib.ssd_last_error().decode()
+        # no launch gave up a bounded wait (read without allocating either)
+        st = lib.ssd_scan_status(1, torch.cuda.current_stream().cuda_stream)
+        assert st == 0, lib.ssd_last_error().decode()
         assert_close(out.double().cpu().numpy(), ref_out.double().cpu().numpy(), TOL[dtype],
                      f"out, call {seed + 1}")
         assert_close(fin.double().cpu().numpy(), ref_fin.double().cpu().numpy(), TOL[dtype],
