@@ -412,6 +412,17 @@ def main():
     import torch.distributed as dist
     import selective_state_space_05_gb300 as ssd
 
+    if args.workload in ("chained", "packed"):
+        # one of the other workloads alone (for profiling it): its own line
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        res = other_workload(torch, ssd, si, args.workload, dev, torch.cuda.current_stream(),
+                             load_peaks(), args.steps, args.warmup,
+                             torch.cuda.get_device_properties(dev).multi_processor_count)
+        print(json.dumps({"metric": METRIC, **res, "n_gpus": 1, "warmup": args.warmup,
+                          "higher_is_better": True, "dtype": "bf16"}), flush=True)
+        return
+
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -450,6 +461,9 @@ def main():
 
     clocks = ClockSampler(local)
     clocks.start()
+    for _ in range(3):   # the sampler's start left the GPU idle: bring the clocks back up
+        step()
+    torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     ms_local, per_call = time_calls(torch, step, args.steps, stream)

@@ -188,6 +188,10 @@ int ssd_chunk_state(const void* x, const void* B, const float* dt_out, const flo
   if (dtype == SSD_DTYPE_F32)
     e = ssd::launch_chunk_state<float>(static_cast<const float*>(x), static_cast<const float*>(B),
                                        dt_out, dA_cumsum, chunk_seg, d, states, st);
+  else if (ssd::fused_eligible(d, true))   // tensor cores for the Mamba-2 shapes
+    e = ssd::launch_chunk_state_tc(static_cast<const __nv_bfloat16*>(x),
+                                   static_cast<const __nv_bfloat16*>(B), dt_out, dA_cumsum,
+                                   chunk_seg, d, states, st);
   else
     e = ssd::launch_chunk_state<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x),
                                                static_cast<const __nv_bfloat16*>(B), dt_out,

@@ -85,6 +85,12 @@ struct FusedVectors {
   const int32_t* seg;            // or null
 };
 bool fused_eligible(const Dims& d, bool bf16);
+// Stage 2 (chunk states, [B, nc, H, P, N]) on tensor cores from stage 1's
+// outputs, for the shapes fused_eligible accepts (bf16, headdim 64, dstate
+// 128, chunk 128 / 256, an even number of heads per group).
+cudaError_t launch_chunk_state_tc(const __nv_bfloat16* x, const __nv_bfloat16* B,
+                                  const float* dt_out, const float* cs, const int32_t* seg,
+                                  const Dims& d, float* states, cudaStream_t st);
 // Device-wide status of the fused kernel's bounded waits: the error bits
 // recorded since the last reset into *bits (0: none); synchronises st.
 // Returns 0 or the cudaError_t of a failed copy.

@@ -161,6 +161,17 @@ struct Params {
   long long items;       // B * H/2 * ceil(nc / seg_chunks)
   unsigned long long wait_ns;   // limit of any single wait
   int lookback_extra;    // > 0 only in the time-out test: a hand-off flag value never reached
+  int* ticket;           // the launch's work counter (ctrl[0]; ctrl[2] for the state pass)
+  // state pre-pass: the state entering every segment ([B*H][nseg][P/4][N][4],
+  // column quads outermost like the slots), or null: then each segment's
+  // final state is handed on to the next through the slots and flags
+  const float* hin;
+  int nseg;
+  // segment-state pass: each segment's own state, from a zero entering state
+  // ([B][nseg][H][P][N]), and the decay that carries a state across the
+  // segment ([B*H][nseg]; 0 when the segment holds a reset)
+  float* seg_states;
+  float* seg_decay;
 };
 
 
@@ -286,12 +297,101 @@ __device__ __forceinline__ void vec_load(const Params& p, const Unit& it, int la
   }
 }
 
+// The raw inputs of a unit staged in shared memory by asynchronous copies
+// (cp.async, 4 bytes each), so that a warp can have several units' loads in
+// flight without holding them in registers: the two heads' dt pair per
+// token, seq_idx at positions t0 - 1 .. t0 + Q - 1 (-1: none), and A,
+// dt_bias, D of the two heads.
+struct alignas(16) VecStage {
+  uint32_t dt[kQmax];
+  int sq[kQmax + 4];
+  float par[8];
+};
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void vec_stage(const Params& p, const Unit& it, int lane, VecStage& st) {
+  const int E = p.Q / 32;
+  const __nv_bfloat16* src = p.dt_raw + it.b * p.sdt_b + it.t0 * p.sdt_t + it.h0;
+  for (int i = 0; i < E; ++i) {
+    const int tok = lane * E + i;
+    if (tok < it.nvalid)
+      cp_async4(&st.dt[tok], src + (int64_t)tok * p.sdt_t);
+    else
+      st.dt[tok] = 0u;
+  }
+  for (int k = lane; k <= p.Q; k += 32) {
+    const int64_t pos = it.t0 - 1 + k;
+    if (p.seq_idx && pos >= 0 && k - 1 < it.nvalid)
+      cp_async4(&st.sq[k], p.seq_idx + (int64_t)it.b * p.L + pos);
+    else
+      st.sq[k] = -1;
+  }
+  if (lane < kNH) {
+    cp_async4(&st.par[lane], p.A + it.h0 + lane);
+    if (p.dt_bias) cp_async4(&st.par[2 + lane], p.dt_bias + it.h0 + lane);
+    else st.par[2 + lane] = 0.f;
+    if (p.D) cp_async4(&st.par[4 + lane], p.D + it.h0 + lane);
+    else st.par[4 + lane] = 0.f;
+  }
+}
+
+// The staged inputs of a unit into the registers vec_compute takes (the
+// same values vec_load would have loaded).
+__device__ __forceinline__ void vec_unstage(const Params& p, int lane, const VecStage& st,
+                                            VecRaw& r) {
+  const int E = p.Q / 32;
+  const uint4 d0 = *reinterpret_cast<const uint4*>(&st.dt[lane * E]);
+  const int4 s0 = *reinterpret_cast<const int4*>(&st.sq[lane * E]);
+  uint4 d1 = make_uint4(0u, 0u, 0u, 0u);
+  int4 s1 = make_int4(-1, -1, -1, -1);
+  if (E == 8) {
+    d1 = *reinterpret_cast<const uint4*>(&st.dt[lane * E + 4]);
+    s1 = *reinterpret_cast<const int4*>(&st.sq[lane * E + 4]);
+  }
+  const uint32_t dw[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+  const int sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    r.dt[i] = make_float2(__uint_as_float(dw[i] << 16), __uint_as_float(dw[i] & 0xFFFF0000u));
+    r.sq[i] = sw[i];
+  }
+  r.sq[8] = st.sq[lane * E + E];
+  if (E == 4) r.sq[4] = st.sq[lane * E + 4];
+#pragma unroll
+  for (int e = 0; e < kNH; ++e) {
+    r.a[e] = st.par[e] * kLog2e;
+    r.bias[e] = st.par[2 + e];
+    r.d[e] = st.par[4 + e];
+  }
+}
+
 // The per-token vectors of both heads of one unit, written by the 32 lanes
 // of a warp from what vec_load fetched.  Positions past the sequence end get
 // dt = 0, so that l and the reset count keep their last values there.
 // kSigned: dt may be negative (softplus off); mv then holds l itself and the
-// diagonal blocks multiply by dt explicitly.
-template <bool kSigned>
+// diagonal blocks multiply by dt explicitly.  kFull: also the decay-matrix
+// column factors mv and bv (the segment-state kernel needs only l, dt and
+// the reset counts).
+// A lane's E (4 or 8) consecutive values go to shared memory as 16-byte
+// stores: E scalar stores 4 E bytes apart would conflict E ways in the banks.
+__device__ __forceinline__ void store_run(int* dst, const int (&v)[8], int E) {
+  int4* d4 = reinterpret_cast<int4*>(dst);
+  d4[0] = make_int4(v[0], v[1], v[2], v[3]);
+  if (E == 8) d4[1] = make_int4(v[4], v[5], v[6], v[7]);
+}
+
+template <bool kSigned, bool kFull = true>
 __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, const VecRaw& r,
                                             float (*lv)[kQmax], float (*dtv)[kQmax],
                                             float (*mv)[kQmax], float (*bv)[kQmax], int* segv,
@@ -320,14 +420,26 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
       // l at the last position of this lane's 32-block (E divides 32)
       const float lf = __shfl_sync(0xffffffffu, excl + loc[E == 8 ? 7 : 3], lane | (32 / E - 1));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (i < E) {
-          const float l = excl + loc[i];
-          dtv[e][lane * E + i] = dv[i];
-          lv[e][lane * E + i] = l;
-          mv[e][lane * E + i] = kSigned ? l
-                                        : (dv[i] > 0.f ? l - __log2f(dv[i]) : __int_as_float(0x7f800000));
-          bv[e][lane * E + i] = ex2(lf - l) * dv[i];
+      for (int h4 = 0; h4 < 8; h4 += 4) {   // four positions at a time, one 16-byte store each
+        if (h4 < E) {
+          float lq[4], mq[4], bq[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float l = excl + loc[h4 + i], d = dv[h4 + i];
+            lq[i] = l;
+            if (kFull) {
+              mq[i] = kSigned ? l : (d > 0.f ? l - __log2f(d) : __int_as_float(0x7f800000));
+              bq[i] = ex2(lf - l) * d;
+            }
+          }
+          const int at = lane * E + h4;
+          *reinterpret_cast<float4*>(dtv[e] + at) =
+              make_float4(dv[h4], dv[h4 + 1], dv[h4 + 2], dv[h4 + 3]);
+          *reinterpret_cast<float4*>(lv[e] + at) = make_float4(lq[0], lq[1], lq[2], lq[3]);
+          if (kFull) {
+            *reinterpret_cast<float4*>(mv[e] + at) = make_float4(mq[0], mq[1], mq[2], mq[3]);
+            *reinterpret_cast<float4*>(bv[e] + at) = make_float4(bq[0], bq[1], bq[2], bq[3]);
+          }
         }
       }
     }
@@ -343,8 +455,8 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
       }
       const int cex = warp_incl_scan(cnt, lane) - cnt;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < E) segv[lane * E + i] = cex + lc[i];
+      for (int i = 0; i < 8; ++i) lc[i] += cex;
+      store_run(segv + lane * E, lc, E);
     }
   } else {
 #pragma unroll
@@ -354,10 +466,11 @@ __device__ __forceinline__ void vec_compute(const Params& p, const Unit& it, con
         const float l = p.cs[pq * Q + i] * kLog2e, d = p.dt[pq * Q + i];
         lv[e][i] = l;
         dtv[e][i] = d;
-        mv[e][i] = kSigned ? l : (d > 0.f ? l - __log2f(d) : __int_as_float(0x7f800000));
+        if (kFull) mv[e][i] = kSigned ? l : (d > 0.f ? l - __log2f(d) : __int_as_float(0x7f800000));
       }
       __syncwarp();
-      for (int i = lane; i < Q; i += 32) bv[e][i] = ex2(lv[e][i | 31] - lv[e][i]) * dtv[e][i];
+      if (kFull)
+        for (int i = lane; i < Q; i += 32) bv[e][i] = ex2(lv[e][i | 31] - lv[e][i]) * dtv[e][i];
     }
     if (p.seg)
       for (int i = lane; i < Q; i += 32) segv[i] = p.seg[((int64_t)it.b * p.nc + it.c) * Q + i];
@@ -547,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // after a failed wait nothing more is issued (the launch is aborted)
         if (!W(&s.y_done, k & 1)) break;
         if (has_next) load_cbx(nxt, nsb, (k + 1) & 1);
-        if (sub == cur.nsub - 1 && cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
+        if (!p.hin && sub == cur.nsub - 1 && cur.j == cur.nch - 1 && cur.c < p.nc - 1) {
           // the segment's final states are in their slots once every compute
           // thread has arrived on pub; the release store orders them before
           // the flag at gpu scope (its consumer waits for flag >= its first chunk)
@@ -585,9 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- tickets and per-token vectors: the raw inputs of the
     // next unit are loaded while the ring slot it goes to is still in use
     long long t_cur = p.items, t_pend = p.items;
-    if (lane == 0) t_cur = atomicAdd(p.ctrl, 1);
+    if (lane == 0) t_cur = atomicAdd(p.ticket, 1);
     t_cur = __shfl_sync(0xffffffffu, t_cur, 0);
-    if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ctrl, 1);
+    if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ticket, 1);
     int j_cur = 0;
     VecRaw raw;
     if (t_cur < p.items) vec_load(p, decode(p, t_cur, 0), lane, raw);
@@ -612,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {                                          // the next item
         t_cur = __shfl_sync(0xffffffffu, t_pend, 0);
         j_cur = 0;
-        if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ctrl, 1);
+        if (lane == 0 && t_cur < p.items) t_pend = atomicAdd(p.ticket, 1);
       }
       if (t_cur < p.items) vec_load(p, decode(p, t_cur, j_cur), lane, raw);
     }
@@ -783,9 +896,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_hin = [&](const Unit& it) -> bool {
       const int64_t bh = (int64_t)it.b * p.H + it.h0 + e;
       // slot layout [16 column quads][128 rows][4]: a warp's access is contiguous
-      const float* slot_src = p.slots + ((bh * 2 + ((it.c - 1) & 1)) * (kP / 4) * kN + r) * 4;
+      const float* slot_src =
+          p.hin ? p.hin + ((bh * p.nseg + it.c / p.seg_chunks) * (kP / 4) * kN + r) * 4
+                : p.slots + ((bh * 2 + ((it.c - 1) & 1)) * (kP / 4) * kN + r) * 4;
       bool ok = true;
-      if (it.c > 0) {
+      if (it.c > 0 && !p.hin) {
         const unsigned long long w0 = global_ns();
         int v;
         for (uint32_t i = 0;; ++i) {
@@ -810,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 headdim columns at a time
         const int pc = p0 + qd * 16;
         uint32_t hv[16];
-        if (it.c > 0) {
+        if (it.c > 0 || p.hin) {   // (the pre-pass table also holds segment 0's state)
           load_slot_quads(hv, slot_src + (int64_t)(pc / 4) * kN * 4);
         } else if (p.init) {
           const float* src = p.init + bh * kP * kN + r;
@@ -1002,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (seg_end) {
         const int64_t bh = (int64_t)cur.b * p.H + cur.h0 + e;
         const bool last_chunk = cur.c == p.nc - 1;
-        if (!last_chunk || p.final_states) {
+        if (last_chunk ? p.final_states != nullptr : p.hin == nullptr) {
 #pragma unroll
           for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 columns at a time
             const int pc = p0 + qd * 16;
@@ -1025,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (!last_chunk) tc::mbar_arrive(&s.pub);   // warp 0 raises the flag
+        if (!last_chunk && !p.hin) tc::mbar_arrive(&s.pub);   // warp 0 raises the flag
       } else if (has_next) {
         h_convert(carry_n);
       }
@@ -1111,6 +1226,359 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// Segment states (the chunk-state stage at segment granularity, on tensor
+// cores).  For one segment of consecutive chunks of a head pair, from a zero
+// entering state:
+//   S = sum_j w_j B_j (outer) x_j,  w_j = exp(cs(j -> segment end)) dt_j
+// over the tokens j after the segment's last reset (w_j = 0 before it), and
+// the decay that carries a state across the whole segment, exp of the sum of
+// dt*A over it (0 when the segment holds a reset).  The chunks are taken
+// last-first, so that the exponent of w_j, T + l_last(chunk) - l_j with T
+// the log-decay of the chunks after j's, is known when the chunk is scaled;
+// every sub-step then adds B^T [w o x_0 | w o x_1] to one TMEM accumulator
+// (one N = 128 chain per sub-step, no rescaling in between).  Used by the
+// state pre-pass (segments of many chunks) and, with one chunk per segment,
+// as the tensor-core chunk_state stage.
+// Warp roles: 0 TMA (B and x tiles, kStages deep), 1 MMA, 2-9 compute
+// (head e = (warp-2)/4, token / dstate row 32 (warp%4) + lane), 10 vectors.
+// ---------------------------------------------------------------------------
+constexpr int kSStages = 3;
+constexpr int kSCompute = 256;
+constexpr int kSVecWarp = 2 + kSCompute / 32;
+constexpr int kSThreads = (kSVecWarp + 1) * 32;
+constexpr uint32_t kSTmemCols = 128;
+constexpr int kSVecDepth = 4;   // units whose raw inputs are in flight or staged
+
+struct alignas(1024) SegSmem {
+  unsigned char Bt[kSStages][kSub * kN * 2];     // B tile: two 64-dstate halves, 128B swizzle
+  unsigned char X[kSStages][kNH][kSub * kP * 2];  // x_e, scaled in place to w o x_e
+  float lv[kRing][kNH][kQmax];
+  float dtv[kRing][kNH][kQmax];
+  int segv[kRing][kQmax];
+  VecStage stage[kSVecDepth];   // raw inputs of the units being fetched
+  long long tk[kRing];
+  Unit uk[kRing];
+  uint64_t tk_full[kRing], tk_empty[kRing];
+  uint64_t full[kSStages], wx[kSStages], empty[kSStages];
+  uint64_t h_done, h_free, mma_drain;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(SegSmem) + 1024 <= 227 * 1024, "shared memory");
+
+template <bool kSigned>
+__global__ void __launch_bounds__(kSThreads, 1)
+    ssd_segstate_kernel(const __grid_constant__ CUtensorMap map_x,
+                        const __grid_constant__ CUtensorMap map_b, Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  SegSmem& s = *reinterpret_cast<SegSmem*>(smem_raw +
+                                           ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 1) {
+    tc::tmem_alloc(&s.tmem_base, kSTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kSStages; ++i) {
+      tc::mbar_init(&s.full[i], 1);
+      tc::mbar_init(&s.wx[i], kSCompute);
+      tc::mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      tc::mbar_init(&s.tk_full[i], 32);
+      tc::mbar_init(&s.tk_empty[i], 2 + kSCompute / 32);
+    }
+    tc::mbar_init(&s.h_done, 1);
+    tc::mbar_init(&s.h_free, kSCompute);
+    tc::mbar_init(&s.mma_drain, 1);
+    tc::mbar_fence_init();
+    tc::tma_prefetch_desc(&map_x);
+    tc::tma_prefetch_desc(&map_b);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+  auto W = [&](uint64_t* bar, uint32_t parity) {
+    return wait_or_flag(bar, parity, p.ctrl, p.wait_ns);
+  };
+  auto WW = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, W(bar, parity)) != 0;
+  };
+  // Every role walks the same units (chunks, last-first within a segment) and
+  // sub-steps; sub-step q of the launch uses stage q % kSStages.
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_stream = tc::l2_policy_evict_first();
+      const uint64_t pol_keep = tc::l2_policy_evict_last();
+      uint32_t q = 0;   // sub-steps issued
+      bool ok = true;
+      for (int u = 0; ok; ++u) {
+        const int slot = u % kRing;
+        if (!W(&s.tk_full[slot], (u / kRing) & 1)) break;
+        const bool live = s.tk[slot] < p.items;
+        const Unit it = s.uk[slot];
+        tc::mbar_arrive(&s.tk_empty[slot]);
+        if (!live) break;
+        for (int sb = 0; sb < it.nsub; ++sb, ++q) {
+          const int st = q % kSStages;
+          if (q >= kSStages && !W(&s.empty[st], ((q / kSStages) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const int tok = (int)(it.t0 + sb * kSub);
+          tc::mbar_arrive_expect_tx(&s.full[st], kSub * kN * 2 + kNH * kSub * kP * 2);
+          tc::tma_load_4d_hint(s.Bt[st], &map_b, &s.full[st], 0, it.g, tok, it.b, pol_keep);
+          tc::tma_load_4d_hint(s.Bt[st] + kSub * 128, &map_b, &s.full[st], 64, it.g, tok, it.b,
+                               pol_keep);
+          tc::tma_load_4d_hint(s.X[st][0], &map_x, &s.full[st], 0, it.h0, tok, it.b, pol_stream);
+          tc::tma_load_4d_hint(s.X[st][1], &map_x, &s.full[st], 0, it.h0 + 1, tok, it.b,
+                               pol_stream);
+        }
+      }
+      // the loads in flight land before the CTA may exit: the stages whose
+      // last armed phase was not waited for by the MMA issuer
+      for (uint32_t i = 0; i < kSStages && i < q; ++i) {
+        const uint32_t last = q - 1 - i;   // one of the last kSStages sub-steps
+        drain_wait(&s.full[last % kSStages], (last / kSStages) & 1, p.ctrl, p.wait_ns);
+      }
+    }
+  } else if (warp == kSVecWarp) {
+    // tickets and per-token vectors; the chunks of a segment last-first.  A
+    // unit here is consumed about four times faster than in the fused
+    // kernel, so the raw inputs of the next kSVecDepth - 1 units are fetched
+    // into shared memory by asynchronous copies (one commit group per unit)
+    // while the current one is computed.
+    // (each unit is decoded once: decode divides 64-bit tickets)
+    struct Uid {
+      long long t;
+      Unit it;
+    };
+    auto claim = [&]() {
+      long long t = 0;
+      if (lane == 0) t = atomicAdd(p.ticket, 1);
+      return __shfl_sync(0xffffffffu, t, 0);
+    };
+    auto first_of = [&](long long t) {
+      Uid v;
+      v.t = t;
+      if (t < p.items) {
+        v.it = decode(p, t, 0);
+        v.it = decode(p, t, v.it.nch - 1);
+      }
+      return v;
+    };
+    auto next_of = [&](const Uid& v) {
+      if (v.t >= p.items) return v;
+      if (v.it.j > 0) {
+        Uid w = v;   // the previous chunk of the same segment
+        w.it.j -= 1;
+        w.it.c -= 1;
+        w.it.t0 -= p.Q;
+        w.it.nvalid = p.Q;   // only the sequence's last chunk can be short
+        w.it.nsub = p.Q / kSub;
+        return w;
+      }
+      return first_of(claim());
+    };
+    const bool raw_in = p.dt_raw != nullptr;   // else stage-1 outputs, read directly
+    Uid q[kSVecDepth - 1];
+    q[0] = first_of(claim());
+    for (int i = 1; i < kSVecDepth - 1; ++i) q[i] = next_of(q[i - 1]);
+#pragma unroll
+    for (int i = 0; i < kSVecDepth - 1; ++i) {
+      if (raw_in && q[i].t < p.items) vec_stage(p, q[i].it, lane, s.stage[i]);
+      cp_async_commit();
+    }
+    for (int u = 0;; ++u) {
+      const int slot = u % kRing;
+      cp_async_wait<kSVecDepth - 2>();   // this unit's copies are done (groups finish in order)
+      __syncwarp();
+      VecRaw raw;
+      if (raw_in && q[0].t < p.items) vec_unstage(p, lane, s.stage[u % kSVecDepth], raw);
+      const bool ok = WW(&s.tk_empty[slot], ((u / kRing) & 1) ^ 1);
+      if (q[0].t < p.items)
+        vec_compute<kSigned, false>(p, q[0].it, raw, s.lv[slot], s.dtv[slot], nullptr, nullptr,
+                                    s.segv[slot], lane);
+      if (lane == 0) {
+        s.tk[slot] = q[0].t;
+        if (q[0].t < p.items) s.uk[slot] = q[0].it;
+      }
+      tc::mbar_arrive(&s.tk_full[slot]);
+      if (q[0].t >= p.items || !ok) break;
+      // fetch the unit kSVecDepth - 1 ahead into the staging slot this unit left
+      const Uid nx = next_of(q[kSVecDepth - 2]);
+#pragma unroll
+      for (int i = 0; i < kSVecDepth - 2; ++i) q[i] = q[i + 1];
+      q[kSVecDepth - 2] = nx;
+      __syncwarp();
+      if (raw_in && nx.t < p.items) vec_stage(p, nx.it, lane, s.stage[(u + kSVecDepth - 1) % kSVecDepth]);
+      cp_async_commit();
+    }
+    cp_async_wait<0>();   // no copy into shared memory outlives the CTA
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t dBmn = tc::sdesc_sw128(tc::smem_u32(s.Bt[0]), kSub * 128, 1024);
+      const uint64_t dXW = tc::sdesc_sw128(tc::smem_u32(s.X[0][0]), kSub * kP * 2, 1024);
+      constexpr uint32_t kStageB = (kSub * kN * 2) >> 4, kStageX = (kNH * kSub * kP * 2) >> 4;
+      constexpr uint32_t id_s = tc::idesc_bf16(kN, kNH * kP, true, true);
+      uint32_t q = 0, items_done = 0;
+      bool ok = true;
+      bool first = true;   // the next MMA starts a segment (overwrites the accumulator)
+      for (int u = 0; ok; ++u) {
+        const int slot = u % kRing;
+        if (!W(&s.tk_full[slot], (u / kRing) & 1)) break;
+        const bool live = s.tk[slot] < p.items;
+        const Unit it = s.uk[slot];
+        tc::mbar_arrive(&s.tk_empty[slot]);
+        if (!live) break;
+        if (first && items_done > 0 && !W(&s.h_free, (items_done - 1) & 1)) break;
+        for (int sb = 0; sb < it.nsub; ++sb, ++q) {
+          const int st = q % kSStages;
+          if (!W(&s.wx[st], (q / kSStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc::mma_ss(tmem, dBmn + st * kStageB + kk * 128, dXW + st * kStageX + kk * 128, id_s,
+                       first ? (kk > 0) : 1);
+          first = false;
+          tc::mma_commit(&s.empty[st]);   // the stage may be reloaded
+        }
+        if (ok && it.j == 0) {   // the segment's first chunk comes last
+          tc::mma_commit(&s.h_done);
+          ++items_done;
+          first = true;
+        }
+      }
+      tc::mma_commit(&s.mma_drain);
+      drain_wait(&s.mma_drain, 0, p.ctrl, p.wait_ns);
+    }
+  } else {
+    // compute: scale x rows by w in place; at a segment's end read the state
+    const int cw = warp - 2;
+    const int e = cw >> 2;
+    const int qr = warp & 3;
+    const int r = qr * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
+    uint32_t q = 0, items_done = 0;
+    float T = 0.f;          // log2-decay of the segment's chunks after the current one
+    bool reset_later = false;
+    for (int u = 0;; ++u) {
+      const int slot = u % kRing;
+      if (!WW(&s.tk_full[slot], (u / kRing) & 1)) break;
+      const bool live = s.tk[slot] < p.items;
+      const Unit it = s.uk[slot];
+      if (!live) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&s.tk_empty[slot]);
+        break;
+      }
+      if (it.j == it.nch - 1) {   // a segment starts (its last chunk comes first)
+        T = 0.f;
+        reset_later = false;
+      }
+      const float* lv = s.lv[slot][e];
+      const float l_last = lv[p.Q - 1];
+      const int sg_last = p.has_seg ? s.segv[slot][p.Q - 1] : 0;
+      bool ok = true;
+      for (int sb = 0; sb < it.nsub; ++sb, ++q) {
+        const int st = q % kSStages;
+        const int tok = sb * kSub + r;
+        float w = 0.f;
+        if (tok < it.nvalid && !reset_later && (!p.has_seg || s.segv[slot][tok] == sg_last))
+          w = ex2(T + l_last - lv[tok]) * s.dtv[slot][e][tok];
+        if (!WW(&s.full[st], (q / kSStages) & 1)) {
+          ok = false;
+          break;
+        }
+        unsigned char* xr = s.X[st][e] + r * 128;
+        const uint64_t w2 = pk2(w, w);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          // the row's 64 columns, in place, in the tile's swizzled chunk
+          // order: the 8 rows of a phase then hit 8 different bank groups
+          uint4* ptr = reinterpret_cast<uint4*>(xr + ((c8 ^ (r & 7)) << 4));
+          const uint4 xv = *ptr;
+          uint4 o;
+          o.x = f2_to_bf2(mul2(bf2_to_f2(xv.x), w2));
+          o.y = f2_to_bf2(mul2(bf2_to_f2(xv.y), w2));
+          o.z = f2_to_bf2(mul2(bf2_to_f2(xv.z), w2));
+          o.w = f2_to_bf2(mul2(bf2_to_f2(xv.w), w2));
+          *ptr = o;
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&s.wx[st]);
+      }
+      T += l_last;
+      reset_later = reset_later || sg_last > 0;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&s.tk_empty[slot]);
+      if (!ok) break;
+      if (it.j == 0) {   // the segment is complete: S and its decay
+        if (!WW(&s.h_done, items_done & 1)) break;
+        tc::fence_after_sync();
+        const int sgm = it.c / p.seg_chunks;
+        const int h = it.h0 + e;
+        float* dst = p.seg_states +
+                     ((((int64_t)it.b * p.nseg + sgm) * p.H + h) * kP) * kN + r;
+#pragma unroll
+        for (int qd = 0; qd < kP / 16; ++qd) {
+          uint32_t hv[16];
+          tc::tmem_ld16(tmem + e * kP + qd * 16 + lane_addr, hv);
+          tc::tmem_ld_wait_regs(hv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dst[(qd * 16 + i) * kN] = __uint_as_float(hv[i]);
+        }
+        if (r == 0 && p.seg_decay)
+          p.seg_decay[((int64_t)it.b * p.H + h) * p.nseg + sgm] = reset_later ? 0.f : ex2(T);
+        tc::fence_before_sync();
+        tc::mbar_arrive(&s.h_free);
+        ++items_done;
+      }
+    }
+  }
+  __syncwarp();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc(tmem, kSTmemCols);
+}
+
+// The state entering every segment: h_0 = initial state (or 0),
+// h_{s+1} = decay_s h_s + S_s, written in the slot layout ([P/4][N][4] per
+// (b h, segment)) that the fused kernel reads.  One thread per (b h, column
+// quad, dstate row).
+__global__ void __launch_bounds__(256)
+    segment_passing_kernel(const float* __restrict__ seg_states,
+                           const float* __restrict__ seg_decay, const float* __restrict__ init,
+                           float* __restrict__ hin, int B, int H, int nseg) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t per_bh = (kP / 4) * kN;
+  if (idx >= (int64_t)B * H * per_bh) return;
+  const int64_t bh = idx / per_bh;
+  const int quad = (int)((idx % per_bh) / kN), n = (int)(idx % kN);
+  const int b = (int)(bh / H), h = (int)(bh % H);
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (init) {
+    const float* src = init + bh * kP * kN + (quad * 4) * kN + n;
+    v = make_float4(src[0], src[kN], src[2 * kN], src[3 * kN]);
+  }
+  for (int sg = 0; sg < nseg; ++sg) {
+    reinterpret_cast<float4*>(hin)[(bh * nseg + sg) * per_bh + quad * kN + n] = v;
+    const float dcy = seg_decay[bh * nseg + sg];
+    const float* S = seg_states + (((int64_t)b * nseg + sg) * H + h) * kP * kN +
+                     (quad * 4) * kN + n;
+    v.x = fmaf(dcy, v.x, S[0]);
+    v.y = fmaf(dcy, v.y, S[kN]);
+    v.z = fmaf(dcy, v.z, S[2 * kN]);
+    v.w = fmaf(dcy, v.w, S[3 * kN]);
+  }
+}
+
 }  // namespace fused
 }  // namespace ssd
 
@@ -1170,6 +1638,39 @@ int sm_count() {
   }
   return n;
 }
+
+// the shared-memory opt-in is a property of each kernel on each device
+template <typename K>
+cudaError_t ensure_smem(K kernel, size_t smem, int which) {
+  static std::atomic<bool> done[8][64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool known = dev >= 0 && dev < 64;
+  if (known && done[which][dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && known) done[which][dev].store(true, std::memory_order_release);
+  return e;
+}
+
+// Segment states on tensor cores (the pre-pass, or the chunk-state stage
+// with one chunk per segment).  pa: the launch's Params with items, nseg,
+// seg_chunks, ticket, seg_states and seg_decay set.
+// (The weights of this kernel need no logarithm of dt, so the vector form
+// that carries dt's sign is used whatever dt's sign.)
+cudaError_t launch_segstate(const CUtensorMap& mx, const CUtensorMap& mb, const fused::Params& pa,
+                            cudaStream_t st) {
+  const size_t smem = sizeof(fused::SegSmem) + 1024;
+  cudaError_t e = ensure_smem(fused::ssd_segstate_kernel<true>, smem, 2);
+  if (e != cudaSuccess) return e;
+  const long long grid = std::min<long long>(pa.items, sm_count());
+  fused::ssd_segstate_kernel<true><<<(unsigned)grid, fused::kSThreads, smem, st>>>(mx, mb, pa);
+  return cudaGetLastError();
+}
+
+// control words of the stand-alone chunk-state stage, which has no
+// workspace: [1] error word, [2] ticket counter (cleared before each launch)
+__device__ int g_stage_ctrl[4];
 
 }  // namespace
 
@@ -1244,6 +1745,17 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   while (seg < d.nchunks &&
          pairs * ((d.nchunks + seg) / (seg + 1)) >= 12LL * sm_count())
     ++seg;
+  // State pre-pass.  With fewer head pairs than SMs the segments of a pair
+  // would run one after another through the hand-off and leave most SMs
+  // idle (a 131k-token single sequence: 64 pairs, 512 chunks).  Instead
+  // every segment's own state is computed first, all in parallel; a short
+  // pass over the segments gives the state entering each one; the main
+  // kernel then reads those and never waits for another CTA.  The three
+  // passes use the chunk-state region of the workspace (segments of at
+  // least 3 chunks, so that the two tables fit).
+  bool prepass = pairs < sm_count() && d.nchunks >= 8;
+  if (const char* ov = getenv("SSD_FUSED_PREPASS")) prepass = atoi(ov) != 0;   // test override
+  if (prepass) seg = std::max(seg, std::min(3, d.nchunks));
   if (const char* ov = getenv("SSD_FUSED_SEGMENT_CHUNKS")) {   // tuning / test override
     const int v = atoi(ov);
     if (v >= 1 && v <= d.nchunks) seg = v;
@@ -1265,22 +1777,39 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   // by the caller are taken as possibly negative
   const bool nonneg = v.dt_raw && (v.softplus ? (!v.do_clamp || v.hi >= 0.f)
                                               : (v.do_clamp && v.lo >= 0.f));
-  const size_t smem = sizeof(fused::Smem) + 1024;
-  // the shared-memory opt-in is a property of each kernel on each device
-  static std::atomic<bool> attr_set[2][64];
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const bool known = dev >= 0 && dev < 64;
-  const int which = nonneg ? 0 : 1;
-  if (!known || !attr_set[which][dev].load(std::memory_order_acquire)) {
-    e = nonneg ? cudaFuncSetAttribute(fused::ssd_fused_kernel<false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-               : cudaFuncSetAttribute(fused::ssd_fused_kernel<true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (known) attr_set[which][dev].store(true, std::memory_order_release);
+  p.ticket = ctrl;
+  p.hin = nullptr;
+  p.nseg = 0;
+  p.seg_states = p.seg_decay = nullptr;
+  if (prepass) {
+    const int nseg = (d.nchunks + seg - 1) / seg;
+    const size_t pn = (size_t)fused::kP * fused::kN, bh = (size_t)d.batch * d.nheads;
+    const size_t decay_floats = (bh * nseg + 63) / 64 * 64;
+    if (seg < 2 || bh * nseg * 2 * pn + decay_floats > bh * (size_t)d.nchunks * pn) {
+      prepass = false;   // the table would not fit (segments too short)
+    } else {
+      fused::Params pa = p;
+      pa.items = pairs * nseg;
+      pa.nseg = nseg;
+      pa.ticket = ctrl + 2;
+      pa.seg_states = slots;
+      pa.seg_decay = slots + bh * nseg * pn;
+      float* hin = pa.seg_decay + decay_floats;
+      e = launch_segstate(mx, mb, pa, st);
+      if (e != cudaSuccess) return e;
+      const long long threads = (long long)bh * (fused::kP / 4) * fused::kN;
+      fused::segment_passing_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+          pa.seg_states, pa.seg_decay, init, hin, (int)d.batch, d.nheads, nseg);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      p.hin = hin;
+      p.nseg = nseg;
+    }
   }
+  const size_t smem = sizeof(fused::Smem) + 1024;
+  e = nonneg ? ensure_smem(fused::ssd_fused_kernel<false>, smem, 0)
+             : ensure_smem(fused::ssd_fused_kernel<true>, smem, 1);
+  if (e != cudaSuccess) return e;
   const long long grid = std::min<long long>(p.items, sm_count());   // one CTA per SM
   if (nonneg)
     fused::ssd_fused_kernel<false><<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz,
@@ -1289,6 +1818,40 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
     fused::ssd_fused_kernel<true><<<(unsigned)grid, fused::kThreads, smem, st>>>(mx, mb, mc, mz,
                                                                                 mo, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_state_tc(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
+                                  const float* dt_out, const float* cs, const int32_t* seg,
+                                  const Dims& d, float* states, cudaStream_t st) {
+  CUtensorMap mx, mb;
+  if (!make_map(&mx, x, fused::kP, d.nheads, d.seqlen, d.batch, d.sx) ||
+      !make_map(&mb, Bm, fused::kN, d.ngroups, d.seqlen, d.batch, d.sB))
+    return cudaErrorInvalidValue;
+  int* ctrl = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ctrl), g_stage_ctrl);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(ctrl, 0, sizeof(g_stage_ctrl), st);
+  if (e != cudaSuccess) return e;
+  fused::Params p = {};
+  p.dt = dt_out;
+  p.cs = cs;
+  p.seg = seg;
+  p.has_seg = seg != nullptr;
+  p.L = d.seqlen;
+  p.B = (int)d.batch;
+  p.H = d.nheads;
+  p.G = d.ngroups;
+  p.Q = d.chunk;
+  p.nc = d.nchunks;
+  p.seg_chunks = 1;   // one chunk per segment: the chunk-local states
+  p.nseg = d.nchunks;
+  p.items = (long long)d.batch * (d.nheads / fused::kNH) * d.nchunks;
+  p.wait_ns = fused::kWaitNs;
+  p.ctrl = ctrl;
+  p.ticket = ctrl + 2;
+  p.seg_states = states;
+  p.seg_decay = nullptr;
+  return launch_segstate(mx, mb, p, st);
 }
 
 int fused_status(int reset, cudaStream_t st, int* bits) {

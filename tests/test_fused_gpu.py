@@ -204,6 +204,7 @@ def test_fused_segment_lengths_bit_identical(shape, monkeypatch):
     g = to_dev(d)
     Q = shape["chunk_size"]
     nc = -(-shape["seqlen"] // Q)
+    monkeypatch.setenv("SSD_FUSED_PREPASS", "0")   # the hand-off between segments
     monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", "1")
     y_1, f_1 = _run_raw(g, Q)
     for seg in sorted({2, 3, nc} - {1}):
@@ -307,6 +308,7 @@ def test_fused_timeout_is_reported(monkeypatch):
     ws = torch.empty(ssd.workspace_bytes(2, 1024, 4, 64, 128, 2, 128), dtype=torch.uint8,
                      device="cuda")
     ssd.scan_status(reset=True)
+    monkeypatch.setenv("SSD_FUSED_PREPASS", "0")   # segments wait for their predecessors
     monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", "1")
     monkeypatch.setenv("SSD_FUSED_WAIT_NS", "200000000")
     monkeypatch.setenv("SSD_FUSED_TEST_STALL", "1")
@@ -326,3 +328,70 @@ def test_fused_timeout_is_reported(monkeypatch):
     ry, rf = oracle.scan_sequential(d)
     assert_close(y, ry, TOL["bf16"], "out after the time-out")
     assert_close(f, rf, TOL["bf16"], "final after the time-out")
+
+
+# --------------------------------------------------------------------------
+# state pre-pass (few head pairs, many chunks): segment states first, then
+# the states entering each segment, then the main kernel without hand-off
+# --------------------------------------------------------------------------
+
+PREPASS_CASES = [
+    ("docs_init_q128", dict(batch=1, nheads=4, ngroups=2, seqlen=3000, chunk_size=128,
+                            init_std=0.3, seq_idx_lengths=[1000, 1, 1200, 799]), None),
+    ("docs_on_chunk_edges", dict(batch=1, nheads=2, ngroups=1, seqlen=2500, chunk_size=128,
+                                 init_std=0.3, seq_idx_lengths=[256, 1024, 128, 1092]), None),
+    ("two_rows_q256", dict(batch=2, nheads=8, ngroups=1, seqlen=4096, chunk_size=256,
+                           init_std=0.2), None),
+    ("slow_decay", dict(batch=1, nheads=4, ngroups=2, seqlen=2048, chunk_size=128,
+                        init_std=0.5, a_log_range=(math.log(1e-3), math.log(1e-1))), None),
+    ("signed_dt", dict(batch=1, nheads=4, ngroups=1, seqlen=2048, chunk_size=256,
+                       dt_softplus=False, dt_bias=False, init_std=0.3,
+                       a_log_range=(0.0, math.log(2.0)), seq_idx_lengths=[900, 1148]), "signed"),
+]
+
+
+@pytest.mark.parametrize("seg", ["auto", "3", "5"])
+@pytest.mark.parametrize("case", PREPASS_CASES, ids=[c[0] for c in PREPASS_CASES])
+def test_fused_prepass_matches_oracle(case, seg, monkeypatch):
+    name, kw, rewrite = case
+    monkeypatch.setenv("SSD_FUSED_PREPASS", "1")
+    if seg != "auto":
+        monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", seg)
+    d = _small(3300 + len(name), **kw)
+    if rewrite == "signed":
+        d = _signed_dt(d, 0.05, 3400 + len(name))
+    y, f = _run_fused(d, kw["chunk_size"])
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["bf16"], f"out ({seg})")
+    assert_close(f, rf, TOL["bf16"], f"final ({seg})")
+
+
+def test_fused_prepass_agrees_with_handoff(monkeypatch):
+    """The two ways of carrying the state between segments give the same
+    result up to the rounding of the state sums."""
+    d = _small(52, batch=1, nheads=8, ngroups=2, seqlen=4000, chunk_size=256, init_std=0.3,
+               seq_idx_lengths=[1500, 2500])
+    monkeypatch.setenv("SSD_FUSED_SEGMENT_CHUNKS", "4")
+    monkeypatch.setenv("SSD_FUSED_PREPASS", "0")
+    y0, f0 = _run_fused(d, 256)
+    monkeypatch.setenv("SSD_FUSED_PREPASS", "1")
+    y1, f1 = _run_fused(d, 256)
+    assert_close(y1, y0, 5e-3, "out: pre-pass vs hand-off")
+    assert_close(f1, f0, 5e-3, "final: pre-pass vs hand-off")
+
+
+@pytest.mark.parametrize("Q", [128, 256])
+def test_chunk_state_stage_on_tensor_cores(Q):
+    """ssd_chunk_state routes the bf16 headdim-64 / dstate-128 shapes to the
+    tensor-core segment-state kernel (one chunk per segment)."""
+    import selective_state_space_05_gb300 as ssd
+    from oracle import ssd_oracle as so
+    d = _small(53 + Q, batch=2, nheads=4, ngroups=2, seqlen=700, chunk_size=Q,
+               seq_idx_lengths=[300, 1, 399])
+    g = to_dev(d)
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q, dt_bias=g["dt_bias"],
+                                        seq_idx=g["seq_idx"])
+    st = ssd.ssd_chunk_state(g["x"], g["B"], dt_out, cs, seg, chunk_size=Q)
+    torch.cuda.synchronize()
+    _, _, im = so.scan_chunked(d, Q, return_intermediates=True)
+    assert_close(st.double().cpu().numpy(), im["states"], TOL["bf16"], "chunk states")
