@@ -63,8 +63,9 @@ enum {
  * signature is never changed in place (an in-place change of a native fwd
  * signature broke its callers in state-spaces/mamba PR #488).
  *   1  the calls below up to ssd_scan_fwd_host
- *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status and ssd_scan_fwd_strided; every
- *      version-1 symbol is unchanged */
+ *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status, ssd_scan_fwd_strided and the
+ *      block calls ssd_causal_conv1d and ssd_group_rmsnorm; every version-1
+ *      symbol is unchanged */
 int ssd_abi_version(void);
 
 /* Message for the last error returned on the calling host thread ("" if
@@ -339,6 +340,50 @@ int ssd_scan_fwd_host(const void *x, const void *dt, const float *dt_bias,
                       ssd_dtype_t dtype, void *out, float *final_states,
                       int64_t rows_per_slice, void *workspace,
                       size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The block around the scan.  The repro script of state-spaces/mamba issue
+ * #647 calls mamba_split_conv1d_scan_combined: the input projection zxbcdt
+ * is split into z | xBC | dt, xBC goes through a causal depthwise conv1d of
+ * width 4 with bias and the "silu" activation and is split into x | B | C,
+ * the scan runs, and its gated output (norm_before_gate=False: y * silu(z))
+ * is normalised by an RMSNorm over groups of d_inner / ngroups channels
+ * (rmsnorm_weight, rmsnorm_eps) before the output projection.  With these two
+ * calls and ssd_scan_fwd_strided (which reads x, B, C, z, dt as strided
+ * views), everything but the two projections runs in this library.
+ * ------------------------------------------------------------------------- */
+
+/* Causal depthwise conv1d over the token axis, one filter per channel:
+ *   out[b,t,c] = act(bias[c] + sum_{k<width} weight[c*width + k] x[b, t-width+1+k, c])
+ * with act = SiLU if silu != 0 (else identity).  Taps before the sequence
+ * start are zero, and so are taps in another document when seq_idx
+ * ([batch, seqlen] int32, or NULL) differs from token t's (each packed
+ * document is convolved on its own).
+ *   x        [batch, seqlen, channels], x dtype, channels dense per token;
+ *            x_stride gives the batch / token strides in elements (e.g. the
+ *            xBC slice of zxbcdt), multiples of 16 bytes, token >= channels
+ *   weight   [channels, width] float;  bias [channels] float or NULL
+ *   out      [batch, seqlen, channels] x dtype, dense (written; must not
+ *            overlap x)
+ * channels a multiple of 8; width 1..8; x, out, bias, seq_idx 16-byte
+ * aligned.  Enqueued on `stream`; returns SSD_OK or a negative SSD_ERR_*. */
+int ssd_causal_conv1d(const void *x, ssd_stride_t x_stride, const float *weight,
+                      const float *bias, const int32_t *seq_idx, int64_t batch,
+                      int64_t seqlen, int channels, int width, int silu,
+                      ssd_dtype_t dtype, void *out, void *stream);
+
+/* RMSNorm over groups of channels, in place:
+ *   y[r, c] = y[r, c] * weight[c] / sqrt(mean_{c' in group(c)} y[r, c']^2 + eps)
+ * for rows r < rows (batch * seqlen tokens), channels c < dim (d_inner =
+ * nheads * headdim, head-major: channel h * headdim + p), groups of
+ * group_size consecutive channels (d_inner / ngroups gives the block's
+ * grouped norm; dim gives one norm over all channels).  Applied to
+ * ssd_scan_fwd's out (already gated by silu(z)) this is the block's norm
+ * with norm_before_gate=False.  y dense [rows, dim] x dtype, 16-byte
+ * aligned; weight [dim] float; group_size a multiple of 8 dividing dim.
+ * Sums of squares in fp32.  Returns SSD_OK or a negative SSD_ERR_*. */
+int ssd_group_rmsnorm(void *y, const float *weight, float eps, int64_t rows,
+                      int dim, int group_size, ssd_dtype_t dtype, void *stream);
 
 #ifdef __cplusplus
 }

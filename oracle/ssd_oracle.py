@@ -363,3 +363,50 @@ def scan_chunked(inp: dict, chunk_size: int, return_intermediates: bool = False)
     if return_intermediates:
         return out, final, dict(dt=dt, cs=cs_all, states=S_all, prev_states=Hprev_all)
     return out, final
+
+
+# ----------------------------------------------------------------------------
+# the block around the scan (state-spaces/mamba issue #647, repro script:
+# mamba_split_conv1d_scan_combined with conv1d_weight, conv1d_bias,
+# activation="silu", rmsnorm_weight, rmsnorm_eps, norm_before_gate=False)
+# ----------------------------------------------------------------------------
+
+def causal_conv1d(x, weight, bias=None, seq_idx=None, silu: bool = True) -> np.ndarray:
+    """Causal depthwise conv1d over the token axis in fp64, one filter per
+    channel: out[b,t,c] = act(bias[c] + sum_k w[c,k] x[b, t-W+1+k, c]), act =
+    SiLU or identity.  Taps before the sequence start are zero, and so are
+    taps in another document of seq_idx (every packed document is convolved
+    on its own).  x [B, L, C]; weight [C, W]; bias [C]; seq_idx [B, L]."""
+    x = f64(x)
+    w = f64(weight)
+    Bsz, L, C = x.shape
+    W = w.shape[1]
+    sq = i32(seq_idx)
+    out = np.zeros((Bsz, L, C)) if bias is None else np.broadcast_to(f64(bias), (Bsz, L, C)).copy()
+    for k in range(W):
+        shift = W - 1 - k                     # tap k reads token t - shift
+        if shift >= L:
+            continue
+        tap = np.zeros((Bsz, L, C))
+        tap[:, shift:, :] = x[:, :L - shift, :]
+        if sq is not None and shift > 0:
+            same = np.zeros((Bsz, L), dtype=bool)
+            same[:, shift:] = sq[:, shift:] == sq[:, :L - shift]
+            tap *= same[:, :, None]
+        out += tap * w[:, k][None, None, :]
+    if silu:
+        out = out / (1.0 + np.exp(-out))
+    return out
+
+
+def group_rmsnorm(y, weight, eps: float, group_size: int) -> np.ndarray:
+    """RMSNorm over groups of group_size consecutive channels of the last
+    axis, in fp64: y * weight / sqrt(mean over the group of y^2 + eps).  With
+    group_size = d_inner / ngroups this is the block's grouped norm; applied
+    to the gated scan output it is norm_before_gate=False."""
+    y = f64(y)
+    w = f64(weight)
+    shp = y.shape
+    yg = y.reshape(-1, shp[-1] // group_size, group_size)
+    r = 1.0 / np.sqrt((yg * yg).mean(axis=-1, keepdims=True) + eps)
+    return (yg * r).reshape(shp) * w

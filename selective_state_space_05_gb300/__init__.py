@@ -3,6 +3,7 @@
 The computation lives in ``libssd_gb300.so`` (CUDA kernels behind the C ABI
 of include/ssd_scan.h); this package only marshals torch tensors into it.
 """
-from .scan import (abi_version, host_workspace_bytes, scan_status,  # noqa: F401
-                   ssd_chunk_fused, ssd_chunk_scan, ssd_chunk_state, ssd_dt_cumsum,
-                   ssd_scan_fwd, ssd_scan_fwd_host, ssd_state_passing, workspace_bytes)
+from .scan import (abi_version, causal_conv1d, group_rmsnorm_,  # noqa: F401
+                   host_workspace_bytes, scan_status, ssd_chunk_fused, ssd_chunk_scan,
+                   ssd_chunk_state, ssd_dt_cumsum, ssd_scan_fwd, ssd_scan_fwd_host,
+                   ssd_state_passing, workspace_bytes)

@@ -354,3 +354,48 @@ def ssd_scan_fwd_host(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: tor
     if return_final_states:
         return out, final_states
     return out
+
+
+# --- the block around the scan ----------------------------------------------
+
+def causal_conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                  *, seq_idx: Optional[torch.Tensor] = None, activation: Optional[str] = "silu",
+                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal depthwise conv1d over tokens (ssd_causal_conv1d): x [batch,
+    seqlen, channels] (a strided view such as the xBC slice of zxbcdt is
+    fine), weight [channels, width] fp32, bias [channels] fp32.  Returns a
+    dense [batch, seqlen, channels] tensor of x's dtype."""
+    if x.dtype not in _DT:
+        raise ValueError("x must be float32 or bfloat16")
+    if activation not in (None, "silu"):
+        raise ValueError("activation must be None or 'silu'")
+    Bsz, L, Cn = x.shape
+    dev = x.device
+    _need(x, "x", None, device=dev, strided=True)
+    W = weight.shape[-1]
+    _need(weight, "weight", torch.float32, (Cn, W), dev)
+    _need(bias, "bias", torch.float32, (Cn,), dev, optional=True)
+    _need(seq_idx, "seq_idx", torch.int32, (Bsz, L), dev, optional=True)
+    if out is None:
+        out = torch.empty(Bsz, L, Cn, dtype=x.dtype, device=dev)
+    _need(out, "out", x.dtype, (Bsz, L, Cn), dev)
+    _lib.check(_lib.load().ssd_causal_conv1d(
+        _ptr(x), _lib.Stride(x.stride(0), x.stride(1)), _ptr(weight), _ptr(bias), _ptr(seq_idx),
+        Bsz, L, Cn, W, int(activation == "silu"), _DT[x.dtype], _ptr(out), _stream(stream)))
+    return out
+
+
+def group_rmsnorm_(y: torch.Tensor, weight: torch.Tensor, *, group_size: int,
+                   eps: float = 1e-5, stream=None) -> torch.Tensor:
+    """In-place RMSNorm over groups of group_size consecutive channels of the
+    last dimension (ssd_group_rmsnorm).  y: [..., dim] dense, e.g. the scan's
+    gated out viewed as [batch, seqlen, nheads * headdim]; weight [dim] fp32."""
+    if y.dtype not in _DT:
+        raise ValueError("y must be float32 or bfloat16")
+    dim = y.shape[-1]
+    _need(y, "y", None, device=y.device)
+    _need(weight, "weight", torch.float32, (dim,), y.device)
+    rows = y.numel() // dim
+    _lib.check(_lib.load().ssd_group_rmsnorm(_ptr(y), _ptr(weight), float(eps), rows, dim,
+                                             int(group_size), _DT[y.dtype], _stream(stream)))
+    return y

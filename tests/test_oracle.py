@@ -71,6 +71,104 @@ def test_p1_worked_example_golden():
         assert abs(_p1_block_out(G, False) - g["printed"]["ref"][str(G)]) < 1.5e-4
 
 
+def _p1_block_full(G: int, grouped: bool, L: int = 5) -> np.ndarray:
+    """The page's whole block over the first L tokens, in fp64, from the
+    oracle's conv, scan and group norm (the out-projection, weight 0.1 and
+    bias 0.1 as on the page, is test-side glue): out[0, :, 0]."""
+    H, P, N, Wc = 32, 64, 128, 4
+    dim = H * P
+    conv_dim = dim + 2 * G * N
+    zx = np.full((1, L, 2 * dim + 2 * G * N + H), 0.1)
+    xbc = oracle.causal_conv1d(zx[:, :, dim:dim + conv_dim], np.full((conv_dim, Wc), 0.1),
+                               np.full(conv_dim, 0.1), silu=True)
+    f = torch.float64
+    d = dict(x=torch.from_numpy(xbc[:, :, :dim].reshape(1, L, H, P).copy()),
+             B=torch.from_numpy(xbc[:, :, dim:dim + G * N].reshape(1, L, G, N).copy()),
+             C=torch.from_numpy(xbc[:, :, dim + G * N:].reshape(1, L, G, N).copy()),
+             dt=torch.from_numpy(zx[:, :, -H:].copy()),
+             dt_bias=torch.full((H,), 0.1, dtype=f), A=-torch.ones(H, dtype=f),
+             D=torch.arange(H, dtype=f) * 1000.0,
+             z=torch.from_numpy(zx[:, :, :dim].reshape(1, L, H, P).copy()),
+             dt_softplus=True, dt_limit=(0.0, float("inf")))
+    y, _ = so.scan_sequential(d)
+    yn = oracle.group_rmsnorm(y.reshape(1, L, dim), np.full(dim, 0.1), 1e-5,
+                              dim // G if grouped else dim)
+    return 0.1 * yn.sum(axis=-1)[0] + 0.1
+
+
+def test_p1_worked_example_through_block_oracle():
+    """The printed values again, now through the oracle's conv and group
+    norm over a short sequence (token 0 is the printed one); later tokens
+    see more conv taps and the recurrence, and must differ from token 0."""
+    g = json.load(open(os.path.join(GOLDEN, "p1_worked_example.json")))
+    for G in (1, 2, 4):
+        out = _p1_block_full(G, True)
+        assert abs(out[0] - g["printed"]["combined"][str(G)]) < 1.5e-4
+        assert abs(out[0] - _p1_block_out(G, True)) < 1e-9
+        assert abs(out[1] - out[0]) > 1e-6   # (the norm and the D skip keep it small)
+        ref = _p1_block_full(G, False)
+        assert abs(ref[0] - g["printed"]["ref"][str(G)]) < 1.5e-4
+
+
+def test_causal_conv1d_is_numpy_convolve():
+    """Per channel, the causal conv is numpy's full convolution with the
+    reversed filter, truncated to the sequence (a library routine)."""
+    rng = np.random.default_rng(3)
+    for W in (1, 2, 4, 7):
+        x = rng.normal(size=(2, 23, 5))
+        w = rng.normal(size=(5, W))
+        b = rng.normal(size=5)
+        out = oracle.causal_conv1d(x, w, b, silu=False)
+        for bi in range(2):
+            for c in range(5):
+                ref = np.convolve(x[bi, :, c], w[c, ::-1])[:23] + b[c]
+                assert rel(out[bi, :, c], ref) < 1e-14
+        s = oracle.causal_conv1d(x, w, b, silu=True)
+        assert rel(s, out / (1 + np.exp(-out))) < 1e-14
+
+
+def test_causal_conv1d_impulse_and_documents():
+    """A unit impulse at token t0 gives the filter reversed over t0..t0+W-1;
+    with seq_idx every document is convolved on its own (the result equals
+    the concatenation of the separate convolutions)."""
+    W = 4
+    w = np.arange(1.0, 1 + 3 * W).reshape(3, W)
+    x = np.zeros((1, 12, 3))
+    x[0, 5, :] = 1.0
+    out = oracle.causal_conv1d(x, w, None, silu=False)
+    for c in range(3):
+        want = np.zeros(12)
+        want[5:5 + W] = w[c, ::-1]
+        assert np.array_equal(out[0, :, c], want)
+    rng = np.random.default_rng(4)
+    lens = [7, 1, 3, 9]
+    x = rng.normal(size=(2, sum(lens), 3))
+    sq = torch.cat([torch.full((n,), i, dtype=torch.int32) for i, n in enumerate(lens)])
+    sq = sq.unsqueeze(0).expand(2, -1).contiguous()
+    packed = oracle.causal_conv1d(x, w, np.ones(3), seq_idx=sq, silu=True)
+    parts, t = [], 0
+    for n in lens:
+        parts.append(oracle.causal_conv1d(x[:, t:t + n], w, np.ones(3), silu=True))
+        t += n
+    assert rel(packed, np.concatenate(parts, axis=1)) < 1e-15
+
+
+def test_group_rmsnorm_closed_forms_and_library():
+    rng = np.random.default_rng(5)
+    y = rng.normal(size=(3, 4, 48))
+    w = rng.normal(size=48)
+    for gs in (48, 16, 8):
+        out = oracle.group_rmsnorm(y, w, 1e-5, gs)
+        # torch's own RMSNorm over each group (a library routine)
+        t = torch.nn.functional.rms_norm(torch.from_numpy(y).reshape(3, 4, 48 // gs, gs), (gs,),
+                                         eps=1e-5).reshape(3, 4, 48).numpy() * w
+        assert rel(out, t) < 1e-13
+    # a constant group: y / sqrt(y^2 + eps), times the weight
+    c = np.full((1, 1, 16), -2.0)
+    out = oracle.group_rmsnorm(c, np.full(16, 0.5), 1e-3, 8)
+    assert np.allclose(out, 0.5 * -2.0 / math.sqrt(4.0 + 1e-3), rtol=0, atol=1e-15)
+
+
 # --------------------------------------------------------------------------
 # dt preprocessing
 # --------------------------------------------------------------------------
