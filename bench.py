@@ -400,6 +400,68 @@ def other_workload(torch, ssd, si, name, dev, stream, peaks, steps, warmup, num_
             "gpu_launches": steps * S, "data": "synthetic, drawn on the device"}
 
 
+def decode_workload(torch, ssd, si, dev, stream, peaks, steps):
+    """Decode steps (ssd_decode_step) at the 2.7B shape: one token per batch
+    row from a state in HBM, advanced in place; HBM-bound on the fp32 state
+    (read and written once per step)."""
+    cfg = si.CONFIGS["mamba2_2p7b"]
+    Bz, H, P, N, G = cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
+    gen = torch.Generator(device=dev).manual_seed(77)
+    bf = torch.bfloat16
+    x = torch.randn(Bz, H, P, generator=gen, device=dev).to(bf)
+    z = torch.randn(Bz, H, P, generator=gen, device=dev).to(bf)
+    dt = torch.randn(Bz, H, generator=gen, device=dev).to(bf)
+    Bm = torch.randn(Bz, G, N, generator=gen, device=dev).to(bf)
+    Cm = torch.randn(Bz, G, N, generator=gen, device=dev).to(bf)
+    A = -torch.exp(torch.rand(H, generator=gen, device=dev) * 2.77)
+    bias = torch.full((H,), -3.0, device=dev)
+    D = torch.randn(H, generator=gen, device=dev)
+    state = torch.randn(Bz, H, P, N, generator=gen, device=dev) * 0.1
+    out = torch.empty_like(x)
+    n = max(steps, 200)
+
+    def step():
+        ssd.ssd_decode_step(x, dt, A, Bm, Cm, state, dt_bias=bias, D=D, z=z, out=out,
+                            stream=stream)
+
+    for _ in range(20):
+        step()
+    torch.cuda.synchronize()
+    ms_host, per = time_calls(torch, step, n, stream)   # one host call per step
+    # a decoding loop replays captured steps: 64 steps per CUDA graph
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            ssd.ssd_decode_step(x, dt, A, Bm, Cm, state, dt_bias=bias, D=D, z=z, out=out,
+                                stream=side)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream(dev)
+        for _ in range(64):
+            ssd.ssd_decode_step(x, dt, A, Bm, Cm, state, dt_bias=bias, D=D, z=z, out=out,
+                                stream=cap)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, n // 64)
+    ms_graph, _ = time_calls(torch, graph.replay, reps, torch.cuda.current_stream(dev))
+    ms = ms_graph / 64
+    alg = 2 * state.numel() * 4 + 3 * x.numel() * 2 + dt.numel() * 2 + 2 * Bm.numel() * 2 + 3 * H * 4
+    achieved = alg / (ms / 1e3) / 1e9
+    return {"workload": f"decode step: batch {Bz}, nheads {H}, headdim {P}, dstate {N}, ngroups "
+                        f"{G}, bf16, fp32 state", "ms_per_call": ms, "us_per_call": ms * 1e3,
+            "us_per_call_host_launched": ms_host * 1e3,
+            "value": Bz / (ms / 1e3), "unit": "tokens/s", "per_call_ms_host_launched": spread(per),
+            "calls": reps * 64, "timing": "CUDA graph of 64 steps, replayed",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "alg_bytes_per_call": alg},
+            "gpu_launches": reps * 64 + n, "data": "synthetic, drawn on the device"}
+
+
 def main():
     args = parse_args()
     import ssd_inputs as si
@@ -597,6 +659,7 @@ def main():
         for name in ("chained", "packed"):
             others[name] = other_workload(torch, ssd, si, name, dev, stream, peaks, args.steps,
                                           args.warmup, num_sms)
+        others["decode"] = decode_workload(torch, ssd, si, dev, stream, peaks, args.steps)
 
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -63,9 +63,9 @@ enum {
  * signature is never changed in place (an in-place change of a native fwd
  * signature broke its callers in state-spaces/mamba PR #488).
  *   1  the calls below up to ssd_scan_fwd_host
- *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status, ssd_scan_fwd_strided and the
- *      block calls ssd_causal_conv1d and ssd_group_rmsnorm; every version-1
- *      symbol is unchanged */
+ *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status, ssd_scan_fwd_strided, the
+ *      block calls ssd_causal_conv1d and ssd_group_rmsnorm, and
+ *      ssd_decode_step; every version-1 symbol is unchanged */
 int ssd_abi_version(void);
 
 /* Message for the last error returned on the calling host thread ("" if
@@ -384,6 +384,29 @@ int ssd_causal_conv1d(const void *x, ssd_stride_t x_stride, const float *weight,
  * Sums of squares in fp32.  Returns SSD_OK or a negative SSD_ERR_*. */
 int ssd_group_rmsnorm(void *y, const float *weight, float eps, int64_t rows,
                       int dim, int group_size, ssd_dtype_t dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * One decode step.  The initial / final states of ssd_scan_fwd are what let a
+ * prefill be continued (chunked prefill, prefix caching, speculative
+ * decoding: state-spaces/mamba PR #488); generating then advances the state
+ * one token at a time.  For every batch row, the recurrence at one token:
+ *   dt' = clamp(softplus(dt + dt_bias)) (options as in ssd_scan_fwd)
+ *   state <- exp(dt' A[h]) state + dt' x[b,h,:] (outer) B[b,g,:]   (in place)
+ *   out[b,h,:] = state C[b,g,:] + D[h] x[b,h,:],  times silu(z[b,h,:]) if z
+ *   x, z, out  [batch, nheads, headdim]  x dtype (out written)
+ *   dt         [batch, nheads]           x dtype
+ *   B, C       [batch, ngroups, dstate]  x dtype
+ *   state      [batch, nheads, headdim, dstate] float, 16-byte aligned; read
+ *              and written (the final_states of a prefill can be passed as is)
+ * dstate a multiple of 8 up to 256.  Equal, up to rounding, to ssd_scan_fwd
+ * over that one token with initial_states = state and final_states written
+ * back.  Enqueued on `stream`; returns SSD_OK or a negative SSD_ERR_*. */
+int ssd_decode_step(const void *x, const void *dt, const float *dt_bias,
+                    int dt_softplus, float dt_limit_lo, float dt_limit_hi,
+                    const float *A, const void *B, const void *C, const float *D,
+                    const void *z, float *state, int64_t batch, int nheads,
+                    int headdim, int dstate, int ngroups, ssd_dtype_t dtype,
+                    void *out, void *stream);
 
 #ifdef __cplusplus
 }

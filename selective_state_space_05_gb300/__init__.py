@@ -5,5 +5,5 @@ of include/ssd_scan.h); this package only marshals torch tensors into it.
 """
 from .scan import (abi_version, causal_conv1d, group_rmsnorm_,  # noqa: F401
                    host_workspace_bytes, scan_status, ssd_chunk_fused, ssd_chunk_scan,
-                   ssd_chunk_state, ssd_dt_cumsum, ssd_scan_fwd, ssd_scan_fwd_host,
-                   ssd_state_passing, workspace_bytes)
+                   ssd_chunk_state, ssd_decode_step, ssd_dt_cumsum, ssd_scan_fwd,
+                   ssd_scan_fwd_host, ssd_state_passing, workspace_bytes)

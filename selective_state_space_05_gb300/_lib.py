@@ -38,6 +38,8 @@ SIGNATURES = {
     "ssd_scan_status": (_i, [_i, _vp]),
     "ssd_causal_conv1d": (_i, [_vp, _st, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp]),
     "ssd_group_rmsnorm": (_i, [_vp, _vp, _f, _i64, _i, _i, _i, _vp]),
+    "ssd_decode_step": (_i, [_vp, _vp, _vp, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i,
+                             _i, _i, _i, _vp, _vp]),
     "ssd_scan_fwd_strided": (_i, [_vp, _st, _vp, _st, _vp, _i, _f, _f, _vp, _vp, _st, _vp, _st,
                                   _vp, _vp, _st, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _i, _i,
                                   _vp, _vp, _vp, _sz, _vp]),

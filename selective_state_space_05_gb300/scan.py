@@ -399,3 +399,40 @@ def group_rmsnorm_(y: torch.Tensor, weight: torch.Tensor, *, group_size: int,
     _lib.check(_lib.load().ssd_group_rmsnorm(_ptr(y), _ptr(weight), float(eps), rows, dim,
                                              int(group_size), _DT[y.dtype], _stream(stream)))
     return y
+
+
+# --- decoding ----------------------------------------------------------------
+
+def ssd_decode_step(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                    C: torch.Tensor, state: torch.Tensor, *,
+                    dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
+                    dt_limit: Tuple[float, float] = (0.0, math.inf),
+                    D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One token per batch row (ssd_decode_step): x, z [batch, nheads,
+    headdim]; dt [batch, nheads]; B, C [batch, ngroups, dstate]; state
+    [batch, nheads, headdim, dstate] fp32, advanced in place.  Returns out
+    [batch, nheads, headdim]."""
+    if x.dtype not in _DT:
+        raise ValueError("x must be float32 or bfloat16")
+    Bsz, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    dev = x.device
+    _need(x, "x", x.dtype, device=dev)
+    _need(dt, "dt", x.dtype, (Bsz, H), dev)
+    _need(A, "A", torch.float32, (H,), dev)
+    _need(B, "B", x.dtype, (Bsz, G, N), dev)
+    _need(C, "C", x.dtype, (Bsz, G, N), dev)
+    _need(state, "state", torch.float32, (Bsz, H, P, N), dev)
+    _need(dt_bias, "dt_bias", torch.float32, (H,), dev, optional=True)
+    _need(D, "D", torch.float32, (H,), dev, optional=True)
+    _need(z, "z", x.dtype, (Bsz, H, P), dev, optional=True)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", x.dtype, (Bsz, H, P), dev)
+    lo, hi = dt_limit
+    _lib.check(_lib.load().ssd_decode_step(
+        _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi), _ptr(A),
+        _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(state), Bsz, H, P, N, G, _DT[x.dtype],
+        _ptr(out), _stream(stream)))
+    return out

@@ -144,3 +144,19 @@ def test_header_declares_status_and_strided_calls():
     assert "ssd_scan_status" in names and "ssd_scan_fwd_strided" in names
     text = (ROOT / "include" / "ssd_scan.h").read_text()
     assert "SSD_ERR_TIMEOUT = -7" in text
+
+
+def test_decode_step_validation_before_any_launch(lib):
+    def call(**kw):
+        a = dict(x=16, dt=16, bias=None, sp=1, lo=0.0, hi=math.inf, A=16, B=16, C=16, D=None,
+                 z=None, state=16, batch=1, H=2, P=64, N=128, G=1, dtype=1, out=16)
+        a.update(kw)
+        return lib.ssd_decode_step(a["x"], a["dt"], a["bias"], a["sp"], a["lo"], a["hi"], a["A"],
+                                   a["B"], a["C"], a["D"], a["z"], a["state"], a["batch"], a["H"],
+                                   a["P"], a["N"], a["G"], a["dtype"], a["out"], None)
+    assert call(N=12) == -4 and b"dstate" in lib.ssd_last_error()
+    assert call(H=3, G=2) == -1
+    assert call(state=None) == -2
+    assert call(state=24) == -3
+    assert call(lo=1.0, hi=0.5) == -1
+    assert call(dtype=5) == -1
