@@ -209,7 +209,8 @@ int ssd_dt_cumsum(const void *dt, const float *dt_bias, int dt_softplus,
                   float *dt_out, float *dA_cumsum, int32_t *chunk_seg,
                   void *stream);
 
-/* Stage 2: chunk states, for each (b, chunk c, head h):
+/* Stage 2: chunk states, for each (b, chunk c, head h) (tensor cores for the
+ * bf16 headdim-64 / dstate-128 shapes of ssd_chunk_fused, else CUDA cores):
  *   states[b,c,h,p,n] = sum_{j in c, same segment as the chunk's last token}
  *        exp(cs_last - cs_j) * dt_j * x[b,j,h,p] * B[b,j,g,n]
  * chunk_seg may be NULL (no resets). */
@@ -230,7 +231,9 @@ int ssd_state_passing(float *states, const float *dA_cumsum,
                       int nheads, int headdim, int dstate, int chunk_size,
                       void *stream);
 
-/* Stage 4: outputs.  For token i of chunk c:
+/* Stage 4: outputs (tensor cores, through the fused kernel reading
+ * prev_states, for the shapes of ssd_chunk_fused; else CUDA cores).  For
+ * token i of chunk c:
  *   y_i = sum_{j<=i in c, same segment} exp(cs_i - cs_j) (C_i . B_j) dt_j x_j
  *       + [no reset since the chunk start] exp(cs_i) * (H_{c-1} . C_i)
  *       + D x_i,            out_i = y_i * silu(z_i)  (z may be NULL)

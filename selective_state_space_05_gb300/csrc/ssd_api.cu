@@ -230,6 +230,16 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
     return fail(SSD_ERR_NULL, "x, B, C, dt_out, dA_cumsum, prev_states, out are required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (dtype == SSD_DTYPE_BF16 && ssd::fused_eligible(d, true)) {   // tensor cores
+    const void* ptrs[] = {x, B, C, z, out};
+    for (const void* p : ptrs)
+      if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
+    e = ssd::launch_chunk_scan_tc(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
+        static_cast<const __nv_bfloat16*>(C), dt_out, dA_cumsum, chunk_seg, prev_states, D,
+        static_cast<const __nv_bfloat16*>(z), d, static_cast<__nv_bfloat16*>(out), st);
+    return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_scan launch");
+  }
   if (dtype == SSD_DTYPE_F32)
     e = ssd::launch_chunk_scan<float>(
         static_cast<const float*>(x), static_cast<const float*>(B), static_cast<const float*>(C),

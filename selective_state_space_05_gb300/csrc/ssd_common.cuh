@@ -83,6 +83,10 @@ struct FusedVectors {
   const float* dt;               // stage-1 outputs (without dt_raw)
   const float* cs;
   const int32_t* seg;            // or null
+  // stage 3's states entering every chunk ([B, nc, H, P, N]), or null: with
+  // them the kernel takes each chunk's entering state from there (one chunk
+  // per work item, no hand-off, no pre-pass) -- stage 4 on its own
+  const float* prev_states;
 };
 bool fused_eligible(const Dims& d, bool bf16);
 // Stage 2 (chunk states, [B, nc, H, P, N]) on tensor cores from stage 1's
@@ -91,6 +95,13 @@ bool fused_eligible(const Dims& d, bool bf16);
 cudaError_t launch_chunk_state_tc(const __nv_bfloat16* x, const __nv_bfloat16* B,
                                   const float* dt_out, const float* cs, const int32_t* seg,
                                   const Dims& d, float* states, cudaStream_t st);
+// Stage 4 (chunk outputs) on tensor cores from stage 1's outputs and stage
+// 3's prev_states, for the shapes fused_eligible accepts.
+cudaError_t launch_chunk_scan_tc(const __nv_bfloat16* x, const __nv_bfloat16* B,
+                                 const __nv_bfloat16* C, const float* dt_out, const float* cs,
+                                 const int32_t* seg, const float* prev_states, const float* D,
+                                 const __nv_bfloat16* z, const Dims& d, __nv_bfloat16* out,
+                                 cudaStream_t st);
 // Device-wide status of the fused kernel's bounded waits: the error bits
 // recorded since the last reset into *bits (0: none); synchronises st.
 // Returns 0 or the cudaError_t of a failed copy.

@@ -167,6 +167,9 @@ struct Params {
   // final state is handed on to the next through the slots and flags
   const float* hin;
   int nseg;
+  // ... or, with hin_dense, in the chunk-state layout [B][nseg][H][P][N]
+  // (stage 3's prev_states, one chunk per segment)
+  bool hin_dense;
   // segment-state pass: each segment's own state, from a zero entering state
   // ([B][nseg][H][P][N]), and the decay that carries a state across the
   // segment ([B*H][nseg]; 0 when the segment holds a reset)
@@ -925,7 +928,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int qd = 0; qd < kPW / 16; ++qd) {   // 16 headdim columns at a time
         const int pc = p0 + qd * 16;
         uint32_t hv[16];
-        if (it.c > 0 || p.hin) {   // (the pre-pass table also holds segment 0's state)
+        if (p.hin_dense) {   // [B][nseg][H][P][N]: row r, 16 consecutive headdim columns
+          const float* src = p.hin + ((((int64_t)it.b * p.nseg + it.c / p.seg_chunks) * p.H +
+                                       it.h0 + e) * kP + pc) * kN + r;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hv[i] = __float_as_uint(src[i * kN]);
+        } else if (it.c > 0 || p.hin) {   // (the pre-pass table also holds segment 0's state)
           load_slot_quads(hv, slot_src + (int64_t)(pc / 4) * kN * 4);
         } else if (p.init) {
           const float* src = p.init + bh * kP * kN + r;
@@ -1668,9 +1676,10 @@ cudaError_t launch_segstate(const CUtensorMap& mx, const CUtensorMap& mb, const 
   return cudaGetLastError();
 }
 
-// control words of the stand-alone chunk-state stage, which has no
-// workspace: [1] error word, [2] ticket counter (cleared before each launch)
-__device__ int g_stage_ctrl[4];
+// control words of the stand-alone chunk-state and chunk-scan stages, which
+// have no workspace: [0] and [2] ticket counters, [1] error word (cleared
+// before each launch; the hand-off flags after them are not used there)
+__device__ int g_stage_ctrl[64];
 
 }  // namespace
 
@@ -1705,7 +1714,9 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   if (z && !make_map(&mz, z, fused::kP, d.nheads, d.seqlen, d.batch, d.sz))
     return cudaErrorInvalidValue;
   if (!z) mz = mx;   // never used
-  cudaError_t e = cudaMemsetAsync(ctrl, 0, fused_ctrl_ints(d) * sizeof(int), st);
+  // (stage 4 on its own uses no hand-off flags: the first 64 words only)
+  cudaError_t e = cudaMemsetAsync(
+      ctrl, 0, (v.prev_states ? 64 : fused_ctrl_ints(d)) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   fused::Params p;
   p.dt_raw = v.dt_raw;
@@ -1760,6 +1771,10 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
     const int v = atoi(ov);
     if (v >= 1 && v <= d.nchunks) seg = v;
   }
+  if (v.prev_states) {   // stage 4 on its own: every chunk reads its entering state
+    seg = 1;
+    prepass = false;
+  }
   p.seg_chunks = seg;
   p.items = pairs * ((d.nchunks + seg - 1) / seg);
   // any single wait gives up after 2 s; the time-out test shortens the limit
@@ -1778,8 +1793,9 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   const bool nonneg = v.dt_raw && (v.softplus ? (!v.do_clamp || v.hi >= 0.f)
                                               : (v.do_clamp && v.lo >= 0.f));
   p.ticket = ctrl;
-  p.hin = nullptr;
-  p.nseg = 0;
+  p.hin = v.prev_states;
+  p.hin_dense = v.prev_states != nullptr;
+  p.nseg = v.prev_states ? d.nchunks : 0;
   p.seg_states = p.seg_decay = nullptr;
   if (prepass) {
     const int nseg = (d.nchunks + seg - 1) / seg;
@@ -1852,6 +1868,22 @@ cudaError_t launch_chunk_state_tc(const __nv_bfloat16* x, const __nv_bfloat16* B
   p.seg_states = states;
   p.seg_decay = nullptr;
   return launch_segstate(mx, mb, p, st);
+}
+
+cudaError_t launch_chunk_scan_tc(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
+                                 const __nv_bfloat16* Cm, const float* dt_out, const float* cs,
+                                 const int32_t* seg, const float* prev_states, const float* D,
+                                 const __nv_bfloat16* z, const Dims& d, __nv_bfloat16* out,
+                                 cudaStream_t st) {
+  int* ctrl = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ctrl), g_stage_ctrl);
+  if (e != cudaSuccess) return e;
+  FusedVectors v = {};
+  v.dt = dt_out;
+  v.cs = cs;
+  v.seg = seg;
+  v.prev_states = prev_states;
+  return launch_fused(x, Bm, Cm, v, D, z, nullptr, nullptr, out, nullptr, ctrl, d, st);
 }
 
 int fused_status(int reset, cudaStream_t st, int* bits) {

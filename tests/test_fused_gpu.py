@@ -395,3 +395,31 @@ def test_chunk_state_stage_on_tensor_cores(Q):
     torch.cuda.synchronize()
     _, _, im = so.scan_chunked(d, Q, return_intermediates=True)
     assert_close(st.double().cpu().numpy(), im["states"], TOL["bf16"], "chunk states")
+
+
+@pytest.mark.parametrize("Q", [128, 256])
+def test_four_stage_exports_on_tensor_cores(Q):
+    """The four stage calls one by one on the Mamba-2 shape: chunk_state and
+    chunk_scan run on tensor cores (the segment-state kernel with one chunk
+    per segment; the fused kernel reading stage 3's prev_states), state
+    passing on CUDA cores; each intermediate against the oracle's chunked
+    form and the result against the recurrence."""
+    import selective_state_space_05_gb300 as ssd
+    from oracle import ssd_oracle as so
+    d = _small(60 + Q, batch=2, nheads=4, ngroups=2, seqlen=900, chunk_size=Q, init_std=0.3,
+               seq_idx_lengths=[256, 1, 400, 243])
+    g = to_dev(d)
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q, dt_bias=g["dt_bias"],
+                                        seq_idx=g["seq_idx"])
+    st = ssd.ssd_chunk_state(g["x"], g["B"], dt_out, cs, seg, chunk_size=Q)
+    ry, rf, im = so.scan_chunked(d, Q, return_intermediates=True)
+    assert_close(st.double().cpu().numpy(), im["states"], TOL["bf16"], "chunk states")
+    fin = ssd.ssd_state_passing(st, cs, seg, seqlen=900, chunk_size=Q,
+                                initial_states=g["initial_states"])
+    assert_close(st.double().cpu().numpy(), im["prev_states"], TOL["bf16"], "prev states")
+    y = ssd.ssd_chunk_scan(g["x"], g["B"], g["C"], dt_out, cs, seg, st, chunk_size=Q,
+                           D=g["D"], z=g["z"])
+    torch.cuda.synchronize()
+    ssd.scan_status(reset=True)
+    assert_close(y.double().cpu().numpy(), ry, TOL["bf16"], "out")
+    assert_close(fin.double().cpu().numpy(), rf, TOL["bf16"], "final")
