@@ -188,11 +188,14 @@ int ssd_chunk_state(const void* x, const void* B, const float* dt_out, const flo
   if (dtype == SSD_DTYPE_F32)
     e = ssd::launch_chunk_state<float>(static_cast<const float*>(x), static_cast<const float*>(B),
                                        dt_out, dA_cumsum, chunk_seg, d, states, st);
-  else if (ssd::fused_eligible(d, true))   // tensor cores for the Mamba-2 shapes
+  else if (ssd::fused_eligible(d, true)) {   // tensor cores for the Mamba-2 shapes
+    const void* ptrs[] = {x, B, dt_out, dA_cumsum, chunk_seg, states};
+    for (const void* p : ptrs)
+      if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
     e = ssd::launch_chunk_state_tc(static_cast<const __nv_bfloat16*>(x),
                                    static_cast<const __nv_bfloat16*>(B), dt_out, dA_cumsum,
                                    chunk_seg, d, states, st);
-  else
+  } else
     e = ssd::launch_chunk_state<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x),
                                                static_cast<const __nv_bfloat16*>(B), dt_out,
                                                dA_cumsum, chunk_seg, d, states, st);
@@ -231,7 +234,7 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (dtype == SSD_DTYPE_BF16 && ssd::fused_eligible(d, true)) {   // tensor cores
-    const void* ptrs[] = {x, B, C, z, out};
+    const void* ptrs[] = {x, B, C, z, out, dt_out, dA_cumsum, chunk_seg, prev_states};
     for (const void* p : ptrs)
       if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
     e = ssd::launch_chunk_scan_tc(
@@ -271,7 +274,8 @@ int ssd_chunk_fused(const void* x, const void* B, const void* C, const float* dt
                 "even number of heads per group");
   if (!x || !B || !C || !dt_out || !dA_cumsum || !out || !workspace)
     return fail(SSD_ERR_NULL, "x, B, C, dt_out, dA_cumsum, out and workspace are required");
-  const void* ptrs[] = {x, B, C, z, out, initial_states, final_states, workspace};
+  const void* ptrs[] = {x, B, C, z, out, initial_states, final_states, workspace, dt_out,
+                        dA_cumsum, chunk_seg};
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(SSD_ERR_ALIGN, "every pointer must be 16-byte aligned");
   const size_t need = carve(d, nullptr).bytes;
@@ -344,6 +348,9 @@ int scan_fwd_run(const ssd::Dims& d, const void* x, const void* dt, const float*
       v.do_clamp = clamp;
       v.lo = dt_limit_lo;
       v.hi = dt_limit_hi;
+      v.work_dt = w.dt;
+      v.work_cs = w.cs;
+      v.work_seg = w.seg;
       e = ssd::launch_fused(xb, static_cast<const bf*>(B), static_cast<const bf*>(C), v, D,
                             static_cast<const bf*>(z), initial_states, final_states,
                             static_cast<bf*>(out), w.states, w.ctrl, d, st);

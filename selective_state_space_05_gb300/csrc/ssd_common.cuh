@@ -83,6 +83,11 @@ struct FusedVectors {
   const float* dt;               // stage-1 outputs (without dt_raw)
   const float* cs;
   const int32_t* seg;            // or null
+  // workspace for stage 1's outputs (dt, cs [B, H, nc, Q]; seg [B, nc, Q]),
+  // which the state pre-pass computes first when it runs from raw dt
+  float* work_dt;
+  float* work_cs;
+  int32_t* work_seg;
   // stage 3's states entering every chunk ([B, nc, H, P, N]), or null: with
   // them the kernel takes each chunk's entering state from there (one chunk
   // per work item, no hand-off, no pre-pass) -- stage 4 on its own

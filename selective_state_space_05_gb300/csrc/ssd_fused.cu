@@ -300,19 +300,11 @@ __device__ __forceinline__ void vec_load(const Params& p, const Unit& it, int la
   }
 }
 
-// The raw inputs of a unit staged in shared memory by asynchronous copies
-// (cp.async, 4 bytes each), so that a warp can have several units' loads in
-// flight without holding them in registers: the two heads' dt pair per
-// token, seq_idx at positions t0 - 1 .. t0 + Q - 1 (-1: none), and A,
-// dt_bias, D of the two heads.
-struct alignas(16) VecStage {
-  uint32_t dt[kQmax];
-  int sq[kQmax + 4];
-  float par[8];
-};
-
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src)
+// Asynchronous 16-byte copies global -> shared (cp.async, one commit group
+// per unit), so that a warp can have several units' loads in flight without
+// holding them in registers.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
@@ -321,62 +313,6 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void vec_stage(const Params& p, const Unit& it, int lane, VecStage& st) {
-  const int E = p.Q / 32;
-  const __nv_bfloat16* src = p.dt_raw + it.b * p.sdt_b + it.t0 * p.sdt_t + it.h0;
-  for (int i = 0; i < E; ++i) {
-    const int tok = lane * E + i;
-    if (tok < it.nvalid)
-      cp_async4(&st.dt[tok], src + (int64_t)tok * p.sdt_t);
-    else
-      st.dt[tok] = 0u;
-  }
-  for (int k = lane; k <= p.Q; k += 32) {
-    const int64_t pos = it.t0 - 1 + k;
-    if (p.seq_idx && pos >= 0 && k - 1 < it.nvalid)
-      cp_async4(&st.sq[k], p.seq_idx + (int64_t)it.b * p.L + pos);
-    else
-      st.sq[k] = -1;
-  }
-  if (lane < kNH) {
-    cp_async4(&st.par[lane], p.A + it.h0 + lane);
-    if (p.dt_bias) cp_async4(&st.par[2 + lane], p.dt_bias + it.h0 + lane);
-    else st.par[2 + lane] = 0.f;
-    if (p.D) cp_async4(&st.par[4 + lane], p.D + it.h0 + lane);
-    else st.par[4 + lane] = 0.f;
-  }
-}
-
-// The staged inputs of a unit into the registers vec_compute takes (the
-// same values vec_load would have loaded).
-__device__ __forceinline__ void vec_unstage(const Params& p, int lane, const VecStage& st,
-                                            VecRaw& r) {
-  const int E = p.Q / 32;
-  const uint4 d0 = *reinterpret_cast<const uint4*>(&st.dt[lane * E]);
-  const int4 s0 = *reinterpret_cast<const int4*>(&st.sq[lane * E]);
-  uint4 d1 = make_uint4(0u, 0u, 0u, 0u);
-  int4 s1 = make_int4(-1, -1, -1, -1);
-  if (E == 8) {
-    d1 = *reinterpret_cast<const uint4*>(&st.dt[lane * E + 4]);
-    s1 = *reinterpret_cast<const int4*>(&st.sq[lane * E + 4]);
-  }
-  const uint32_t dw[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-  const int sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    r.dt[i] = make_float2(__uint_as_float(dw[i] << 16), __uint_as_float(dw[i] & 0xFFFF0000u));
-    r.sq[i] = sw[i];
-  }
-  r.sq[8] = st.sq[lane * E + E];
-  if (E == 4) r.sq[4] = st.sq[lane * E + 4];
-#pragma unroll
-  for (int e = 0; e < kNH; ++e) {
-    r.a[e] = st.par[e] * kLog2e;
-    r.bias[e] = st.par[2 + e];
-    r.d[e] = st.par[4 + e];
-  }
 }
 
 // The per-token vectors of both heads of one unit, written by the 32 lanes
@@ -1242,39 +1178,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 // over the tokens j after the segment's last reset (w_j = 0 before it), and
 // the decay that carries a state across the whole segment, exp of the sum of
 // dt*A over it (0 when the segment holds a reset).  The chunks are taken
-// last-first, so that the exponent of w_j, T + l_last(chunk) - l_j with T
+// last-first, so that the exponent of w_j, T + cs_last(chunk) - cs_j with T
 // the log-decay of the chunks after j's, is known when the chunk is scaled;
 // every sub-step then adds B^T [w o x_0 | w o x_1] to one TMEM accumulator
 // (one N = 128 chain per sub-step, no rescaling in between).  Used by the
 // state pre-pass (segments of many chunks) and, with one chunk per segment,
-// as the tensor-core chunk_state stage.
+// as the tensor-core chunk_state stage; the per-token vectors come from
+// stage 1 (dt, the per-chunk cumsum cs of dt*A, reset counts) in HBM.
 // Warp roles: 0 TMA (B and x tiles, kStages deep), 1 MMA, 2-9 compute
-// (head e = (warp-2)/4, token / dstate row 32 (warp%4) + lane), 10 vectors.
+// (head e = (warp-2)/4, token / dstate row 32 (warp%4) + lane), 10 copies
+// each unit's stage-1 rows into a ring with cp.async, kSVecDepth units ahead.
 // ---------------------------------------------------------------------------
 constexpr int kSStages = 3;
 constexpr int kSCompute = 256;
 constexpr int kSVecWarp = 2 + kSCompute / 32;
 constexpr int kSThreads = (kSVecWarp + 1) * 32;
 constexpr uint32_t kSTmemCols = 128;
-constexpr int kSVecDepth = 4;   // units whose raw inputs are in flight or staged
+constexpr int kSRing = 6;       // published units (tickets, vectors)
+constexpr int kSVecDepth = 4;   // of them, units whose copies may be in flight
 
 struct alignas(1024) SegSmem {
   unsigned char Bt[kSStages][kSub * kN * 2];     // B tile: two 64-dstate halves, 128B swizzle
   unsigned char X[kSStages][kNH][kSub * kP * 2];  // x_e, scaled in place to w o x_e
-  float lv[kRing][kNH][kQmax];
-  float dtv[kRing][kNH][kQmax];
-  int segv[kRing][kQmax];
-  VecStage stage[kSVecDepth];   // raw inputs of the units being fetched
-  long long tk[kRing];
-  Unit uk[kRing];
-  uint64_t tk_full[kRing], tk_empty[kRing];
+  float csv[kSRing][kNH][kQmax];   // stage 1's cumsum of dt*A over the chunk (natural log)
+  float dtv[kSRing][kNH][kQmax];   // stage 1's dt
+  int segv[kSRing][kQmax];         // reset counts (with seq_idx)
+  long long tk[kSRing];
+  Unit uk[kSRing];
+  uint64_t tk_full[kSRing], tk_empty[kSRing];
   uint64_t full[kSStages], wx[kSStages], empty[kSStages];
   uint64_t h_done, h_free, mma_drain;
   uint32_t tmem_base;
 };
 static_assert(sizeof(SegSmem) + 1024 <= 227 * 1024, "shared memory");
 
-template <bool kSigned>
 __global__ void __launch_bounds__(kSThreads, 1)
     ssd_segstate_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_b, Params p) {
@@ -1292,7 +1229,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tc::mbar_init(&s.wx[i], kSCompute);
       tc::mbar_init(&s.empty[i], 1);
     }
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kSRing; ++i) {
       tc::mbar_init(&s.tk_full[i], 32);
       tc::mbar_init(&s.tk_empty[i], 2 + kSCompute / 32);
     }
@@ -1323,8 +1260,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       uint32_t q = 0;   // sub-steps issued
       bool ok = true;
       for (int u = 0; ok; ++u) {
-        const int slot = u % kRing;
-        if (!W(&s.tk_full[slot], (u / kRing) & 1)) break;
+        const int slot = u % kSRing;
+        if (!W(&s.tk_full[slot], (u / kSRing) & 1)) break;
         const bool live = s.tk[slot] < p.items;
         const Unit it = s.uk[slot];
         tc::mbar_arrive(&s.tk_empty[slot]);
@@ -1353,11 +1290,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
     }
   } else if (warp == kSVecWarp) {
-    // tickets and per-token vectors; the chunks of a segment last-first.  A
-    // unit here is consumed about four times faster than in the fused
-    // kernel, so the raw inputs of the next kSVecDepth - 1 units are fetched
-    // into shared memory by asynchronous copies (one commit group per unit)
-    // while the current one is computed.
+    // tickets and units (the chunks of a segment last-first), each unit's
+    // stage-1 rows (cs and dt of both heads, the reset counts) copied with
+    // cp.async into its ring slot; a unit is published once its copies
+    // landed, kSVecDepth - 1 units behind the newest copies
     // (each unit is decoded once: decode divides 64-bit tickets)
     struct Uid {
       long long t;
@@ -1390,39 +1326,47 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       return first_of(claim());
     };
-    const bool raw_in = p.dt_raw != nullptr;   // else stage-1 outputs, read directly
-    Uid q[kSVecDepth - 1];
-    q[0] = first_of(claim());
-    for (int i = 1; i < kSVecDepth - 1; ++i) q[i] = next_of(q[i - 1]);
-#pragma unroll
-    for (int i = 0; i < kSVecDepth - 1; ++i) {
-      if (raw_in && q[i].t < p.items) vec_stage(p, q[i].it, lane, s.stage[i]);
-      cp_async_commit();
-    }
-    for (int u = 0;; ++u) {
-      const int slot = u % kRing;
-      cp_async_wait<kSVecDepth - 2>();   // this unit's copies are done (groups finish in order)
-      __syncwarp();
-      VecRaw raw;
-      if (raw_in && q[0].t < p.items) vec_unstage(p, lane, s.stage[u % kSVecDepth], raw);
-      const bool ok = WW(&s.tk_empty[slot], ((u / kRing) & 1) ^ 1);
-      if (q[0].t < p.items)
-        vec_compute<kSigned, false>(p, q[0].it, raw, s.lv[slot], s.dtv[slot], nullptr, nullptr,
-                                    s.segv[slot], lane);
+    const int q4 = p.Q / 4;   // float4 / int4 per row
+    // waits for the unit's ring slot, records the unit and starts its copies
+    auto fill = [&](int u, const Uid& v) {
+      const int slot = u % kSRing;
+      const bool ok = WW(&s.tk_empty[slot], ((u / kSRing) & 1) ^ 1);
       if (lane == 0) {
-        s.tk[slot] = q[0].t;
-        if (q[0].t < p.items) s.uk[slot] = q[0].it;
+        s.tk[slot] = v.t;
+        if (v.t < p.items) s.uk[slot] = v.it;
       }
-      tc::mbar_arrive(&s.tk_full[slot]);
-      if (q[0].t >= p.items || !ok) break;
-      // fetch the unit kSVecDepth - 1 ahead into the staging slot this unit left
-      const Uid nx = next_of(q[kSVecDepth - 2]);
+      if (ok && v.t < p.items) {
 #pragma unroll
-      for (int i = 0; i < kSVecDepth - 2; ++i) q[i] = q[i + 1];
-      q[kSVecDepth - 2] = nx;
-      __syncwarp();
-      if (raw_in && nx.t < p.items) vec_stage(p, nx.it, lane, s.stage[(u + kSVecDepth - 1) % kSVecDepth]);
+        for (int e = 0; e < kNH; ++e) {
+          const int64_t row = (((int64_t)v.it.b * p.H + v.it.h0 + e) * p.nc + v.it.c) * p.Q;
+          for (int i = lane; i < q4; i += 32) {
+            cp_async16(&s.csv[slot][e][4 * i], p.cs + row + 4 * i);
+            cp_async16(&s.dtv[slot][e][4 * i], p.dt + row + 4 * i);
+          }
+        }
+        if (p.seg)
+          for (int i = lane; i < q4; i += 32)
+            cp_async16(&s.segv[slot][4 * i],
+                       p.seg + ((int64_t)v.it.b * p.nc + v.it.c) * p.Q + 4 * i);
+      }
       cp_async_commit();
+      return ok;
+    };
+    Uid q[kSVecDepth];
+    q[0] = first_of(claim());
+    for (int i = 1; i < kSVecDepth; ++i) q[i] = next_of(q[i - 1]);
+    bool ok = true;
+    for (int i = 0; i < kSVecDepth; ++i) ok = fill(i, q[i]) && ok;
+    for (int u = 0;; ++u) {
+      cp_async_wait<kSVecDepth - 1>();   // unit u's copies are done (groups finish in order)
+      __syncwarp();
+      tc::mbar_arrive(&s.tk_full[u % kSRing]);   // each lane releases its own copies
+      if (q[0].t >= p.items || !ok) break;
+      const Uid nx = next_of(q[kSVecDepth - 1]);
+#pragma unroll
+      for (int i = 0; i < kSVecDepth - 1; ++i) q[i] = q[i + 1];
+      q[kSVecDepth - 1] = nx;
+      ok = fill(u + kSVecDepth, nx) && ok;
     }
     cp_async_wait<0>();   // no copy into shared memory outlives the CTA
   } else if (warp == 1) {
@@ -1435,8 +1379,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       bool ok = true;
       bool first = true;   // the next MMA starts a segment (overwrites the accumulator)
       for (int u = 0; ok; ++u) {
-        const int slot = u % kRing;
-        if (!W(&s.tk_full[slot], (u / kRing) & 1)) break;
+        const int slot = u % kSRing;
+        if (!W(&s.tk_full[slot], (u / kSRing) & 1)) break;
         const bool live = s.tk[slot] < p.items;
         const Unit it = s.uk[slot];
         tc::mbar_arrive(&s.tk_empty[slot]);
@@ -1476,8 +1420,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     float T = 0.f;          // log2-decay of the segment's chunks after the current one
     bool reset_later = false;
     for (int u = 0;; ++u) {
-      const int slot = u % kRing;
-      if (!WW(&s.tk_full[slot], (u / kRing) & 1)) break;
+      const int slot = u % kSRing;
+      if (!WW(&s.tk_full[slot], (u / kSRing) & 1)) break;
       const bool live = s.tk[slot] < p.items;
       const Unit it = s.uk[slot];
       if (!live) {
@@ -1489,8 +1433,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         T = 0.f;
         reset_later = false;
       }
-      const float* lv = s.lv[slot][e];
-      const float l_last = lv[p.Q - 1];
+      const float* lv = s.csv[slot][e];   // natural log: times log2(e) below
+      const float l_last = lv[p.Q - 1] * kLog2e;
       const int sg_last = p.has_seg ? s.segv[slot][p.Q - 1] : 0;
       bool ok = true;
       for (int sb = 0; sb < it.nsub; ++sb, ++q) {
@@ -1498,7 +1442,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int tok = sb * kSub + r;
         float w = 0.f;
         if (tok < it.nvalid && !reset_later && (!p.has_seg || s.segv[slot][tok] == sg_last))
-          w = ex2(T + l_last - lv[tok]) * s.dtv[slot][e][tok];
+          w = ex2(fmaf(-lv[tok], kLog2e, T + l_last)) * s.dtv[slot][e][tok];
         if (!WW(&s.full[st], (q / kSStages) & 1)) {
           ok = false;
           break;
@@ -1664,15 +1608,14 @@ cudaError_t ensure_smem(K kernel, size_t smem, int which) {
 // Segment states on tensor cores (the pre-pass, or the chunk-state stage
 // with one chunk per segment).  pa: the launch's Params with items, nseg,
 // seg_chunks, ticket, seg_states and seg_decay set.
-// (The weights of this kernel need no logarithm of dt, so the vector form
-// that carries dt's sign is used whatever dt's sign.)
+// pa.dt / pa.cs / pa.seg: stage 1's outputs (the kernel reads them, never the raw dt).
 cudaError_t launch_segstate(const CUtensorMap& mx, const CUtensorMap& mb, const fused::Params& pa,
                             cudaStream_t st) {
   const size_t smem = sizeof(fused::SegSmem) + 1024;
-  cudaError_t e = ensure_smem(fused::ssd_segstate_kernel<true>, smem, 2);
+  cudaError_t e = ensure_smem(fused::ssd_segstate_kernel, smem, 2);
   if (e != cudaSuccess) return e;
   const long long grid = std::min<long long>(pa.items, sm_count());
-  fused::ssd_segstate_kernel<true><<<(unsigned)grid, fused::kSThreads, smem, st>>>(mx, mb, pa);
+  fused::ssd_segstate_kernel<<<(unsigned)grid, fused::kSThreads, smem, st>>>(mx, mb, pa);
   return cudaGetLastError();
 }
 
@@ -1797,6 +1740,7 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
   p.hin_dense = v.prev_states != nullptr;
   p.nseg = v.prev_states ? d.nchunks : 0;
   p.seg_states = p.seg_decay = nullptr;
+  if (prepass && v.dt_raw && !(v.work_dt && v.work_cs && v.work_seg)) prepass = false;
   if (prepass) {
     const int nseg = (d.nchunks + seg - 1) / seg;
     const size_t pn = (size_t)fused::kP * fused::kN, bh = (size_t)d.batch * d.nheads;
@@ -1811,6 +1755,17 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* Bm,
       pa.seg_states = slots;
       pa.seg_decay = slots + bh * nseg * pn;
       float* hin = pa.seg_decay + decay_floats;
+      if (v.dt_raw) {   // stage 1 first: the segment-state kernel reads its outputs
+        e = launch_dt_cumsum<__nv_bfloat16>(v.dt_raw, v.dt_bias, v.softplus, v.lo, v.hi,
+                                            v.do_clamp, v.A, v.seq_idx, d, v.work_dt,
+                                            v.work_cs, v.seq_idx ? v.work_seg : nullptr, st);
+        if (e != cudaSuccess) return e;
+        pa.dt_raw = nullptr;
+        pa.seq_idx = nullptr;
+        pa.dt = v.work_dt;
+        pa.cs = v.work_cs;
+        pa.seg = v.seq_idx ? v.work_seg : nullptr;
+      }
       e = launch_segstate(mx, mb, pa, st);
       if (e != cudaSuccess) return e;
       const long long threads = (long long)bh * (fused::kP / 4) * fused::kN;
