@@ -410,3 +410,70 @@ def group_rmsnorm(y, weight, eps: float, group_size: int) -> np.ndarray:
     yg = y.reshape(-1, shp[-1] // group_size, group_size)
     r = 1.0 / np.sqrt((yg * yg).mean(axis=-1, keepdims=True) + eps)
     return (yg * r).reshape(shp) * w
+
+
+# ----------------------------------------------------------------------------
+# backward: gradients of the forward, by reverse-mode differentiation of the
+# plain recurrence written in torch (fp64, one token at a time)
+# ----------------------------------------------------------------------------
+
+def scan_torch(x, dt, A, B, C, dt_bias=None, D=None, z=None, initial_states=None,
+               seq_idx=None, dt_softplus=True, dt_limit=(0.0, float("inf"))):
+    """The recurrence of scan_sequential, token by token, in torch (every
+    argument a float64 tensor that may require grad): bias -> softplus ->
+    clamp for dt; h_t = exp(dt_t A) h_{t-1} + dt_t x_t (outer) B_t with the
+    state zeroed before a seq_idx change; y_t = h_t C_t + D x_t; out = y *
+    silu(z).  Returns (out, final state)."""
+    import torch
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    rep = H // G
+    d = dt if dt_bias is None else dt + dt_bias
+    if dt_softplus:
+        d = torch.nn.functional.softplus(d)
+    lo, hi = dt_limit
+    if not (lo == 0.0 and hi == float("inf")):
+        d = d.clamp(lo, hi)
+    Bh = B.repeat_interleave(rep, dim=2)          # group of head h = h // rep
+    Ch = C.repeat_interleave(rep, dim=2)
+    h = (torch.zeros(Bsz, H, P, N, dtype=x.dtype) if initial_states is None
+         else initial_states)
+    ys = []
+    for t in range(L):
+        if seq_idx is not None and t > 0:
+            keep = (seq_idx[:, t] == seq_idx[:, t - 1]).to(x.dtype)[:, None, None, None]
+            h = h * keep
+        dec = torch.exp(d[:, t] * A)[:, :, None, None]
+        h = dec * h + (d[:, t])[:, :, None, None] * x[:, t, :, :, None] * Bh[:, t, :, None, :]
+        y = (h * Ch[:, t, :, None, :]).sum(-1)
+        if D is not None:
+            y = y + D[None, :, None] * x[:, t]
+        ys.append(y)
+    y = torch.stack(ys, dim=1)
+    if z is not None:
+        y = y * torch.nn.functional.silu(z)
+    return y, h
+
+
+def scan_backward(inp: dict, dout, names=("x", "dt", "dt_bias", "A", "B", "C", "D", "z",
+                                          "initial_states")) -> dict:
+    """Gradients of sum(out * dout) with respect to the named inputs (those
+    present), by torch autograd through scan_torch in fp64."""
+    import torch
+    args = {}
+    for k in ("x", "dt", "A", "B", "C", "dt_bias", "D", "z", "initial_states"):
+        v = inp.get(k)
+        if v is not None:
+            v = torch.as_tensor(v).detach().to(torch.float64).clone()
+            v.requires_grad_(k in names)
+        args[k] = v
+    sq = inp.get("seq_idx")
+    out, _ = scan_torch(args["x"], args["dt"], args["A"], args["B"], args["C"],
+                        dt_bias=args["dt_bias"], D=args["D"], z=args["z"],
+                        initial_states=args["initial_states"],
+                        seq_idx=None if sq is None else torch.as_tensor(sq),
+                        dt_softplus=inp.get("dt_softplus", True),
+                        dt_limit=inp.get("dt_limit", (0.0, float("inf"))))
+    (out * torch.as_tensor(dout).to(torch.float64)).sum().backward()
+    return {k: (None if args.get(k) is None or args[k].grad is None else args[k].grad.numpy())
+            for k in names}

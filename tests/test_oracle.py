@@ -438,3 +438,48 @@ def test_planted_mistakes_are_caught(k):
     for G in (1, 2, 4):
         failures += abs(_p1_block_out(G, True, mutation=k) - g["printed"]["combined"][str(G)]) > 1.5e-4
     assert failures > 0, f"mutation {k} ({MUTATIONS[k]}) not caught"
+
+
+# --------------------------------------------------------------------------
+# backward: the torch form of the recurrence and its reverse-mode gradients
+# --------------------------------------------------------------------------
+
+def test_torch_recurrence_equals_c_oracle():
+    for kw in (dict(init_std=0.5, seq_idx_lengths=[10, 1, 26]),
+               dict(has_z=False, dt_limit=(0.02, 0.3)),
+               dict(dt_softplus=False, dt_bias=False, a_log_range=(-3.0, 0.0))):
+        d = si.random_small(70, **kw)
+        if not kw.get("dt_softplus", True):
+            d["dt"] = d["dt"].abs() * 0.2
+        t = {k: (torch.as_tensor(v).to(torch.float64) if torch.is_tensor(v) and
+                 v.dtype != torch.int32 else v) for k, v in d.items()}
+        out, fin = so.scan_torch(t["x"], t["dt"], t["A"], t["B"], t["C"], dt_bias=t["dt_bias"],
+                                 D=t["D"], z=t["z"], initial_states=t["initial_states"],
+                                 seq_idx=t["seq_idx"], dt_softplus=d["dt_softplus"],
+                                 dt_limit=d["dt_limit"])
+        ry, rf = so.scan_sequential(d)
+        assert rel(out.numpy(), ry) < TIGHT and rel(fin.numpy(), rf) < TIGHT
+
+
+def test_backward_oracle_passes_gradcheck():
+    """The reverse-mode gradients the backward oracle returns agree with
+    central finite differences of the forward (torch's gradcheck), on a tiny
+    case with every input, a reset and a clamp."""
+    d = si.random_small(71, batch=1, seqlen=6, nheads=2, ngroups=1, headdim=2, dstate=3,
+                        init_std=0.5, seq_idx_lengths=[4, 2], dt_limit=(0.0, 3.0))
+    t = {k: torch.as_tensor(v).to(torch.float64).requires_grad_(True)
+         for k, v in d.items() if torch.is_tensor(v) and v.dtype != torch.int32}
+    sq = d["seq_idx"]
+
+    def f(x, dt, A, B, C, dt_bias, D, z, h0):
+        return so.scan_torch(x, dt, A, B, C, dt_bias=dt_bias, D=D, z=z, initial_states=h0,
+                             seq_idx=sq, dt_limit=(0.0, 3.0))[0]
+    args = (t["x"], t["dt"], t["A"], t["B"], t["C"], t["dt_bias"], t["D"], t["z"],
+            t["initial_states"])
+    assert torch.autograd.gradcheck(f, args, eps=1e-6, atol=1e-7, rtol=1e-6)
+    dout = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(3))
+    g = so.scan_backward(d, dout)
+    out = f(*args)
+    grads = torch.autograd.grad((out * dout.double()).sum(), args)
+    for k, gr in zip(("x", "dt", "A", "B", "C", "dt_bias", "D", "z", "initial_states"), grads):
+        assert rel(g[k], gr.numpy()) < TIGHT, k
