@@ -64,8 +64,9 @@ enum {
  * signature broke its callers in state-spaces/mamba PR #488).
  *   1  the calls below up to ssd_scan_fwd_host
  *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status, ssd_scan_fwd_strided, the
- *      block calls ssd_causal_conv1d and ssd_group_rmsnorm, and
- *      ssd_decode_step; every version-1 symbol is unchanged */
+ *      block calls ssd_causal_conv1d and ssd_group_rmsnorm,
+ *      ssd_decode_step and the backward ssd_scan_bwd (with
+ *      ssd_scan_bwd_workspace_bytes); every version-1 symbol is unchanged */
 int ssd_abi_version(void);
 
 /* Message for the last error returned on the calling host thread ("" if
@@ -410,6 +411,50 @@ int ssd_decode_step(const void *x, const void *dt, const float *dt_bias,
                     const void *z, float *state, int64_t batch, int nheads,
                     int headdim, int dstate, int ngroups, ssd_dtype_t dtype,
                     void *out, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Backward of ssd_scan_fwd: the gradients of sum(out * dout) with respect to
+ * every input.  The flash-linear-attention PR #49 page (fla-org) asks that
+ * the chunked kernels' backward be checked as well as their forward; this is
+ * that backward for the SSD scan, fp32 only.
+ *
+ * Method: the adjoint of the recurrence is the recurrence run backwards in
+ * time, so the heavy parts are three more chunked scans of the forward's own
+ * stage kernels with the operands' roles swapped (dx: time-reversed scan of
+ * dy with B and C exchanged; dB: time-reversed scan of C against dy and x;
+ * dC: forward scan of B against x and dy, started from the transposed
+ * initial states), plus the forward recomputed once for y before the gate.
+ * The gradient of the decays a_t = dt_t A is a reverse cumulative sum over
+ * the tokens; dt's gradient then goes back through clamp (the gradient
+ * passes where lo <= dt' <= hi), softplus and bias.
+ *
+ * Inputs exactly as for ssd_scan_fwd (dense, fp32, 16-byte aligned; dt the
+ * raw dt), plus dout [batch, seqlen, nheads, headdim] float.  Outputs, all
+ * dense float, shaped like their inputs and written (not accumulated):
+ *   dx, dz          [batch, seqlen, nheads, headdim]  (dz required iff z)
+ *   ddt             [batch, seqlen, nheads]   gradient w.r.t. the raw dt
+ *   dB, dC          [batch, seqlen, ngroups, dstate]
+ *   dA, d_dt_bias, dD  [nheads]   (d_dt_bias, dD may be NULL)
+ *   d_initial_states  [batch, nheads, headdim, dstate]  (may be NULL)
+ * d_dt_bias is the gradient of the bias whether or not dt_bias was given.
+ * headdim and dstate in {16, 32, 64, 128}; chunk_size as for ssd_scan_fwd.
+ * Workspace: device memory of at least ssd_scan_bwd_workspace_bytes (0 for
+ * unsupported sizes), used only during the call's stream work.  Enqueued on
+ * `stream`; returns SSD_OK or a negative SSD_ERR_* (nothing launched on an
+ * argument error). */
+size_t ssd_scan_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
+                                    int headdim, int dstate, int ngroups,
+                                    int chunk_size);
+int ssd_scan_bwd(const float *x, const float *dt, const float *dt_bias,
+                 int dt_softplus, float dt_limit_lo, float dt_limit_hi,
+                 const float *A, const float *B, const float *C, const float *D,
+                 const float *z, const float *initial_states,
+                 const int32_t *seq_idx, const float *dout, int64_t batch,
+                 int64_t seqlen, int nheads, int headdim, int dstate,
+                 int ngroups, int chunk_size, float *dx, float *ddt,
+                 float *d_dt_bias, float *dA, float *dB, float *dC, float *dD,
+                 float *dz, float *d_initial_states, void *workspace,
+                 size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

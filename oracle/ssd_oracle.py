@@ -418,12 +418,14 @@ def group_rmsnorm(y, weight, eps: float, group_size: int) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 def scan_torch(x, dt, A, B, C, dt_bias=None, D=None, z=None, initial_states=None,
-               seq_idx=None, dt_softplus=True, dt_limit=(0.0, float("inf"))):
+               seq_idx=None, dt_softplus=True, dt_limit=(0.0, float("inf")), a=None):
     """The recurrence of scan_sequential, token by token, in torch (every
     argument a float64 tensor that may require grad): bias -> softplus ->
     clamp for dt; h_t = exp(dt_t A) h_{t-1} + dt_t x_t (outer) B_t with the
     state zeroed before a seq_idx change; y_t = h_t C_t + D x_t; out = y *
-    silu(z).  Returns (out, final state)."""
+    silu(z).  With ``a`` [batch, seqlen, nheads] given, the decays are
+    exp(a_t) instead of exp(dt_t A) (the input term still uses dt).
+    Returns (out, final state)."""
     import torch
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
@@ -443,7 +445,7 @@ def scan_torch(x, dt, A, B, C, dt_bias=None, D=None, z=None, initial_states=None
         if seq_idx is not None and t > 0:
             keep = (seq_idx[:, t] == seq_idx[:, t - 1]).to(x.dtype)[:, None, None, None]
             h = h * keep
-        dec = torch.exp(d[:, t] * A)[:, :, None, None]
+        dec = torch.exp(d[:, t] * A if a is None else a[:, t])[:, :, None, None]
         h = dec * h + (d[:, t])[:, :, None, None] * x[:, t, :, :, None] * Bh[:, t, :, None, :]
         y = (h * Ch[:, t, :, None, :]).sum(-1)
         if D is not None:
@@ -477,3 +479,29 @@ def scan_backward(inp: dict, dout, names=("x", "dt", "dt_bias", "A", "B", "C", "
     (out * torch.as_tensor(dout).to(torch.float64)).sum().backward()
     return {k: (None if args.get(k) is None or args[k].grad is None else args[k].grad.numpy())
             for k in names}
+
+
+def decay_gradient(inp: dict, dout):
+    """The gradient of sum(out * dout) with respect to the per-token decay
+    exponents a_t = dt_t A_h (processed dt), as [batch, seqlen, nheads],
+    and the processed dt itself: autograd through scan_torch with a as the
+    leaf.  dA = sum over tokens of this gradient times dt."""
+    import torch
+    f = torch.float64
+    t = {k: (None if inp.get(k) is None else torch.as_tensor(inp[k]).detach().to(f))
+         for k in ("x", "dt", "A", "B", "C", "dt_bias", "D", "z", "initial_states")}
+    d = t["dt"] if t["dt_bias"] is None else t["dt"] + t["dt_bias"]
+    if inp.get("dt_softplus", True):
+        d = torch.nn.functional.softplus(d)
+    lo, hi = inp.get("dt_limit", (0.0, float("inf")))
+    if not (lo == 0.0 and hi == float("inf")):
+        d = d.clamp(lo, hi)
+    a = (d * t["A"]).clone().requires_grad_(True)
+    sq = inp.get("seq_idx")
+    out, _ = scan_torch(t["x"], t["dt"], t["A"], t["B"], t["C"], dt_bias=t["dt_bias"], D=t["D"],
+                        z=t["z"], initial_states=t["initial_states"],
+                        seq_idx=None if sq is None else torch.as_tensor(sq),
+                        dt_softplus=inp.get("dt_softplus", True),
+                        dt_limit=(lo, hi), a=a)
+    (out * torch.as_tensor(dout).to(f)).sum().backward()
+    return a.grad.numpy(), d.numpy()

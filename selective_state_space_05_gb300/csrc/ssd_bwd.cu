@@ -1,0 +1,568 @@
+// Backward of the SSD chunked-scan forward (fp32): the gradients of a loss
+// sum(out * dout) with respect to x, raw dt, dt_bias, A, B, C, D, z and the
+// initial states.  The fla-org/flash-linear-attention PR #49 page asks to
+// check backward correctness as well as the forward's; the initial-state PR
+// (state-spaces/mamba #488) left the backward out.
+//
+// The adjoint of a linear recurrence is a linear recurrence run backwards in
+// time, so every heavy part here is one of the forward's own scans (the
+// stage kernels of ssd_simt.cu, with the roles of the operands swapped),
+// written in terms of the forward's quantities: dt (processed), a = dt A and
+// the decay L_ij = exp(a_{j+1} + ... + a_i) between tokens j <= i of one
+// document.  With dy = dout * silu(z) and y the forward output before the gate:
+//   g_j  = sum_{i>=j} L_ij (C_i . B_j) dy_i            (time-reversed scan of
+//          dy with B' = C, C' = B, value coefficient 1 and the decays
+//          shifted by one token: the reversed token of t decays by a_{t+1})
+//   dx_j = dt_j g_j + D dy_j
+//   dB_j = dt_j sum_{h in group} sum_{i>=j} L_ij (x_j . dy_i) C_i
+//          (reversed scan with x' = C, B' = dy, C' = x)
+//   dC_i = sum_{h in group} [sum_{j<=i} L_ij dt_j (dy_i . x_j) B_j
+//          + exp(cs_i) h0^T dy_i]   (forward scan with x' = B, B' = x, C' = dy)
+//   da_k = sum over the pairs j < k <= i of their term
+//          P_ij = L_ij (C_i . B_j) dt_j (dy_i . x_j)   (each decays through a_k)
+//   ddt  = da A + x . g, then through the clamp, softplus and bias;
+//   dA = sum da dt,  dD = sum dy . x,  dz = dout y silu'(z),
+//   dh0 = exp(a_0) (final state of the dx scan).
+//
+// da.  With q_m = dy_m . yo_m - dt_m x_m . go_m (yo, go: y without D x and g,
+// each without the diagonal pair), sum_{m>=k} q_m telescopes to da_k, but
+// over the whole sequence that sum cancels almost entirely under strong
+// decay and its rounding grows with the length.  So the telescoping stops at
+// the end of k's chunk: the pairs that cross the boundary after chunk c sum
+// exactly to <dH_c, H_c>, H_c the forward state after chunk c and dH_c the
+// state of the reversed g scan at the same boundary, so
+//   da_k = sum_{m in chunk(k), m >= k} q_m + <dH_c, H_c>.
+// The backward runs its scans with its own chunk length (at most kBwdChunk;
+// the result does not depend on it), and pads the reversed sequence to whole
+// chunks so that the reversed chunk boundaries fall on the forward ones.
+#include <math.h>
+#include <stdio.h>
+
+#include "../../include/ssd_scan.h"
+#include "ssd_common.cuh"
+
+namespace ssd {
+namespace bwd {
+
+constexpr int kBwdChunk = 64;
+
+__device__ __forceinline__ int64_t chunk_index(int64_t b, int h, int64_t t, int H, int nc, int Q) {
+  return (((int64_t)b * H + h) * nc + t / Q) * Q + t % Q;   // [B, H, nc, Q]
+}
+
+// Over the reversed index space [B, Lp, H, P] (Lp >= L; reversed token k'
+// is forward token t = Lp-1-k', padding where t >= L): dy = dout silu(z)
+// (dout without z) in forward order, and the reversed copies of dy and x
+// (zero on the padding).
+__global__ void reversed_prep_kernel(const float* __restrict__ dout, const float* __restrict__ z,
+                                     const float* __restrict__ x, int64_t Bz, int64_t L,
+                                     int64_t Lp, int HP, float* __restrict__ dy,
+                                     float* __restrict__ dyR, float* __restrict__ xR) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= Bz * Lp * HP) return;
+  const int64_t b = r / (Lp * HP), t = Lp - 1 - (r / HP) % Lp, c = r % HP;
+  if (t >= L) {
+    dyR[r] = 0.f;
+    xR[r] = 0.f;
+    return;
+  }
+  const int64_t i = (b * L + t) * HP + c;
+  float v = dout[i];
+  if (z) {
+    const float zz = z[i];
+    v *= zz / (1.f + __expf(-zz));
+  }
+  dy[i] = v;
+  dyR[r] = v;
+  xR[r] = x[i];
+}
+
+// out[b, k, h, n] = in[b, t, h / rep, n] for the [B, L, G, N] input, with
+// t = Lp-1-k (reverse, zero where t >= L) or t = k; rep > 1 broadcasts the
+// groups to H = G rep heads.
+__global__ void reverse_kernel(const float* __restrict__ in, int64_t Bz, int64_t L, int64_t Lout,
+                               int G, int N, int rep, int reverse, float* __restrict__ out) {
+  const int64_t W = (int64_t)G * rep * N;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= Bz * Lout * W) return;
+  const int64_t b = i / (Lout * W), k = (i / W) % Lout, c = i % W;
+  const int64_t h = c / N, n = c % N;
+  const int64_t t = reverse ? Lout - 1 - k : k;
+  out[i] = t < L ? in[(b * L + t) * G * N + (h / rep) * N + n] : 0.f;
+}
+
+// The reversed decays aR[b, k', h] = a_{t+1} for the reversed token k' of
+// forward token t = Lp-1-k' (0 where t+1 >= L), and seqR[b, k'] = seq[b,
+// min(t, L-1)] (the padding continues the last document).
+__global__ void reversed_decay_kernel(const float* __restrict__ dtF, const float* __restrict__ A,
+                                      const int32_t* __restrict__ seq, int64_t Bz, int64_t L,
+                                      int64_t Lp, int H, int nc, int Q, float* __restrict__ aR,
+                                      int32_t* __restrict__ seqR) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= Bz * Lp * H) return;
+  const int64_t b = i / (Lp * H), t = Lp - 1 - (i / H) % Lp;
+  const int h = (int)(i % H);
+  aR[i] = t + 1 < L ? dtF[chunk_index(b, h, t + 1, H, nc, Q)] * A[h] : 0.f;
+  if (seq && h == 0) seqR[b * Lp + (Lp - 1 - t)] = seq[b * L + (t < L ? t : L - 1)];
+}
+
+__global__ void fill_kernel(float* __restrict__ p, int64_t n, float v) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = v;
+}
+
+// [B, H, P, N] -> [B, H, N, P]
+__global__ void transpose_state_kernel(const float* __restrict__ in, int64_t BH, int P, int N,
+                                       float* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= BH * P * N) return;
+  const int64_t bh = i / ((int64_t)P * N);
+  const int p = (int)((i / N) % P), n = (int)(i % N);
+  out[(bh * N + n) * P + p] = in[i];
+}
+
+// Per (b, t, h), one warp (lanes over P, then over N for C . B): the
+// diagonal added back (g = go + (C.B) dy, y = yo + dt x (C.B) + D x), then
+// dx, dz, and the per-token sums q, x . g and dy . x.  goR is in reversed
+// order over Lp tokens.
+__global__ void token_grads_kernel(const float* __restrict__ goR, const float* __restrict__ yo,
+                                   const float* __restrict__ x, const float* __restrict__ dout,
+                                   const float* __restrict__ z, const float* __restrict__ Bm,
+                                   const float* __restrict__ Cm, const float* __restrict__ D,
+                                   const float* __restrict__ dtF, int64_t Bz, int64_t L,
+                                   int64_t Lp, int H, int P, int N, int G, int nc, int Q,
+                                   float* __restrict__ dx, float* __restrict__ dz,
+                                   float* __restrict__ q, float* __restrict__ xg,
+                                   float* __restrict__ dyx) {
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= Bz * L * H) return;
+  const int64_t b = w / (L * H), t = (w / H) % L;
+  const int h = (int)(w % H);
+  const int64_t bg = ((b * L + t) * G + h / (H / G)) * N;
+  float cb = 0.f;
+  for (int n = lane; n < N; n += 32) cb = fmaf(Cm[bg + n], Bm[bg + n], cb);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) cb += __shfl_xor_sync(0xffffffffu, cb, off);
+  const float dt = dtF[chunk_index(b, h, t, H, nc, Q)];
+  const float Dh = D ? D[h] : 0.f;
+  const int64_t base = w * P, rbase = ((b * Lp + (Lp - 1 - t)) * H + h) * P;
+  float s_q = 0.f, s_xg = 0.f, s_dyx = 0.f;
+  for (int p = lane; p < P; p += 32) {
+    const float xv = x[base + p], go = goR[rbase + p], yv = yo[base + p];
+    float dyv = dout[base + p];
+    if (z) {
+      const float zz = z[base + p], sg = 1.f / (1.f + __expf(-zz));
+      const float y = yv + (dt * cb + Dh) * xv;
+      dz[base + p] = dyv * y * sg * (1.f + zz * (1.f - sg));
+      dyv *= zz * sg;
+    }
+    const float g = fmaf(cb, dyv, go);
+    dx[base + p] = fmaf(dt, g, Dh * dyv);
+    s_q += dyv * yv - dt * xv * go;
+    s_xg = fmaf(xv, g, s_xg);
+    s_dyx = fmaf(dyv, xv, s_dyx);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    s_q += __shfl_xor_sync(0xffffffffu, s_q, off);
+    s_xg += __shfl_xor_sync(0xffffffffu, s_xg, off);
+    s_dyx += __shfl_xor_sync(0xffffffffu, s_dyx, off);
+  }
+  if (lane == 0) {
+    q[w] = s_q;
+    xg[w] = s_xg;
+    dyx[w] = s_dyx;
+  }
+}
+
+// dB[b,t,g,n] = sum_{h in g} dt[b,t,h] oB[b, Lp-1-t, h, n] (oB reversed);
+// dC[b,t,g,n] = sum_{h in g} oC[b, t, h, n].
+__global__ void group_grads_kernel(const float* __restrict__ oB, const float* __restrict__ oC,
+                                   const float* __restrict__ dtF, int64_t Bz, int64_t L,
+                                   int64_t Lp, int H, int G, int N, int nc, int Q,
+                                   float* __restrict__ dB, float* __restrict__ dC) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= Bz * L * G * N) return;
+  const int64_t b = i / (L * G * N), t = (i / ((int64_t)G * N)) % L;
+  const int g = (int)((i / N) % G), n = (int)(i % N);
+  const int rep = H / G;
+  float sb = 0.f, sc = 0.f;
+  for (int h = g * rep; h < (g + 1) * rep; ++h) {
+    sb += dtF[chunk_index(b, h, t, H, nc, Q)] * oB[((b * Lp + (Lp - 1 - t)) * H + h) * N + n];
+    sc += oC[((b * L + t) * H + h) * N + n];
+  }
+  dB[i] = sb;
+  dC[i] = sc;
+}
+
+// The boundary term after chunk c, one block per (c, h, b):
+// bnd[b, h, c] = <dH_c, H_c> with H_c = the forward prev state of chunk c+1
+// and dH_c = exp(a at the first token of chunk c+1) times the reversed prev
+// state of reversed chunk nc-1-c (zero across a document start and after
+// the last chunk).
+__global__ void __launch_bounds__(256) boundary_kernel(
+    const float* __restrict__ prevF, const float* __restrict__ prevR,
+    const int32_t* __restrict__ segF, const float* __restrict__ dtF, const float* __restrict__ A,
+    int H, int PN, int nc, int Q, float* __restrict__ bnd) {
+  __shared__ float part[8];
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  float* out = bnd + ((int64_t)b * H + h) * nc + c;
+  if (c == nc - 1 || (segF && segF[((int64_t)b * nc + c + 1) * Q] != 0)) {
+    if (threadIdx.x == 0) *out = 0.f;
+    return;
+  }
+  const float4* hf =
+      reinterpret_cast<const float4*>(prevF + (((int64_t)b * nc + c + 1) * H + h) * (int64_t)PN);
+  const float4* hr = reinterpret_cast<const float4*>(
+      prevR + (((int64_t)b * nc + (nc - 1 - c)) * H + h) * (int64_t)PN);
+  float s = 0.f;
+  for (int e = threadIdx.x; e < PN / 4; e += 256) {
+    const float4 u = hf[e], v = hr[e];
+    s = fmaf(u.x, v.x, fmaf(u.y, v.y, fmaf(u.z, v.z, fmaf(u.w, v.w, s))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += part[w];
+    *out = __expf(dtF[chunk_index(b, h, (int64_t)(c + 1) * Q, H, nc, Q)] * A[h]) * t;
+  }
+}
+
+// One warp per (b, h, chunk): da = the boundary term after the chunk plus the
+// suffix sum of q inside the chunk, then ddt = da A + x . g through clamp,
+// softplus and bias; dA, d dt_bias and dD summed (atomics across warps).
+__global__ void dt_grads_kernel(const float* __restrict__ q, const float* __restrict__ xg,
+                                const float* __restrict__ dyx, const float* __restrict__ bnd,
+                                const float* __restrict__ dt_raw,
+                                const float* __restrict__ dt_bias, int softplus, int do_clamp,
+                                float lo, float hi, const float* __restrict__ A,
+                                const float* __restrict__ dtF, int64_t Bz, int64_t L, int H,
+                                int nc, int Q, float* __restrict__ ddt, float* __restrict__ dA,
+                                float* __restrict__ dbias, float* __restrict__ dD) {
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= Bz * H * nc) return;
+  const int c = (int)(w % nc);
+  const int h = (int)((w / nc) % H);
+  const int64_t b = w / ((int64_t)nc * H);
+  const float Ah = A[h], bias = dt_bias ? dt_bias[h] : 0.f;
+  const int64_t start = (int64_t)c * Q;
+  const int64_t n = (L - start) < Q ? (L - start) : Q;
+  float carry = bnd[w], sA = 0.f, sbias = 0.f, sD = 0.f;
+  for (int64_t t0 = start + ((n - 1) / 32) * 32; t0 >= start; t0 -= 32) {   // last 32 first
+    const int64_t t = t0 + lane;
+    const bool ok = t < start + n;
+    const int64_t idx = (b * L + t) * H + h;
+    const float qv = ok ? q[idx] : 0.f;
+    float s = qv;   // suffix sum over the lanes >= this one
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_down_sync(0xffffffffu, s, off);
+      if (lane + off < 32) s += o;
+    }
+    const float da = s + carry;
+    carry += __shfl_sync(0xffffffffu, s, 0);
+    if (ok) {
+      const float dt = dtF[chunk_index(b, h, t, H, nc, Q)];
+      sA = fmaf(da, dt, sA);
+      // back through clamp (passes where lo <= v <= hi), softplus and bias
+      const float raw = dt_raw[idx] + bias;
+      float g = fmaf(da, Ah, xg[idx]);
+      if (do_clamp) {
+        const float v = softplus ? (raw <= 20.f ? log1pf(__expf(raw)) : raw) : raw;
+        g = (v >= lo && v <= hi) ? g : 0.f;
+      }
+      if (softplus) g *= 1.f / (1.f + __expf(-raw));
+      ddt[idx] = g;
+      sbias += g;
+      sD += dyx[idx];
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sA += __shfl_xor_sync(0xffffffffu, sA, off);
+    sbias += __shfl_xor_sync(0xffffffffu, sbias, off);
+    sD += __shfl_xor_sync(0xffffffffu, sD, off);
+  }
+  if (lane == 0) {
+    atomicAdd(dA + h, sA);
+    if (dbias) atomicAdd(dbias + h, sbias);
+    if (dD) atomicAdd(dD + h, sD);
+  }
+}
+
+// dh0 = exp(a_0) F, F the final state of the reversed dx scan ([B,H,P,N]).
+__global__ void dh0_kernel(const float* __restrict__ F, const float* __restrict__ dtF,
+                           const float* __restrict__ A, int64_t Bz, int H, int PN, int nc, int Q,
+                           float* __restrict__ dh0) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= Bz * H * PN) return;
+  const int64_t bh = i / PN;
+  const int h = (int)(bh % H);
+  dh0[i] = __expf(dtF[chunk_index(bh / H, h, 0, H, nc, Q)] * A[h]) * F[i];
+}
+
+int bwd_chunk(int chunk_size) { return chunk_size < kBwdChunk ? chunk_size : kBwdChunk; }
+
+// Workspace pieces, 256-byte aligned.  Reversed arrays span Lp = nc Qb tokens.
+struct BwdLayout {
+  size_t dtF, csF, segF, statesF, yo, dy, dyR, xR, CR, BR, ChR, Bh, aR, seqR, csR, dtRo, segR,
+      ones, states1, finR, goR, states2, oB, h0T, oC, q, xg, dyx, bnd, total;
+};
+
+BwdLayout bwd_layout(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
+  const int64_t nc = (L + Q - 1) / Q, Lp = nc * Q;
+  const size_t chunk = (size_t)Bz * H * nc * Q, seg = (size_t)Bz * nc * Q;
+  const size_t xs = (size_t)Bz * L * H * P, xsR = (size_t)Bz * Lp * H * P;
+  const size_t bsR = (size_t)Bz * Lp * G * N, hs = (size_t)Bz * L * H * N;
+  const size_t hsR = (size_t)Bz * Lp * H * N, st = (size_t)Bz * nc * H * P * N;
+  const size_t tok = (size_t)Bz * L * H;
+  BwdLayout l;
+  size_t o = 0;
+  auto take = [&](size_t elems) {   // 4-byte elements
+    const size_t at = o;
+    o = (o + elems * 4 + 255) / 256 * 256;
+    return at;
+  };
+  l.dtF = take(chunk);
+  l.csF = take(chunk);
+  l.segF = take(seg);
+  l.statesF = take(st);
+  l.yo = take(xs);
+  l.dy = take(xs);
+  l.dyR = take(xsR);
+  l.xR = take(xsR);
+  l.CR = take(bsR);
+  l.BR = take(bsR);
+  l.ChR = take(hsR);
+  l.Bh = take(hs);
+  l.aR = take((size_t)Bz * Lp * H);
+  l.seqR = take((size_t)Bz * Lp);
+  l.csR = take(chunk);
+  l.dtRo = take(chunk);
+  l.segR = take(seg);
+  l.ones = take(chunk);
+  l.states1 = take(st);
+  l.finR = take((size_t)Bz * H * P * N);
+  l.goR = take(xsR);
+  l.states2 = take(st);
+  l.oB = take(hsR);
+  l.h0T = take((size_t)Bz * H * P * N);
+  l.oC = take(hs);
+  l.q = take(tok);
+  l.xg = take(tok);
+  l.dyx = take(tok);
+  l.bnd = take((size_t)Bz * H * nc);
+  l.total = o;
+  return l;
+}
+
+unsigned blocks_for(int64_t n, int per) { return (unsigned)((n + per - 1) / per); }
+
+}  // namespace bwd
+}  // namespace ssd
+
+namespace {
+
+int bfail(int code, const char* msg) { return ssd::set_error(code, msg); }
+
+bool bwd_sizes_ok(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                  int chunk) {
+  auto pow2 = [](int v, int lo, int hi) {
+    for (int s = lo; s <= hi; s *= 2)
+      if (v == s) return true;
+    return false;
+  };
+  return batch >= 1 && batch <= 65535 && seqlen >= 1 && nheads >= 1 && nheads <= 65535 &&
+         ngroups >= 1 && nheads % ngroups == 0 && pow2(headdim, 16, 128) && pow2(dstate, 16, 128) &&
+         pow2(chunk, 16, 256) && (seqlen + chunk - 1) / chunk * batch <= 2147483647LL;
+}
+
+ssd::Dims dims_of(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
+  ssd::Dims d;
+  d.batch = Bz;
+  d.seqlen = L;
+  d.nheads = H;
+  d.headdim = P;
+  d.dstate = N;
+  d.ngroups = G;
+  d.chunk = Q;
+  d.nchunks = (int)((L + Q - 1) / Q);
+  d.sx = {L * H * P, (int64_t)H * P};
+  d.sz = d.sx;
+  d.sdt = {L * H, H};
+  d.sB = {L * G * N, (int64_t)G * N};
+  d.sC = d.sB;
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssd_scan_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int headdim,
+                                    int dstate, int ngroups, int chunk_size) {
+  if (!bwd_sizes_ok(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size)) return 0;
+  return ssd::bwd::bwd_layout(batch, seqlen, nheads, headdim, dstate, ngroups,
+                              ssd::bwd::bwd_chunk(chunk_size))
+      .total;
+}
+
+int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_softplus,
+                 float dt_limit_lo, float dt_limit_hi, const float* A, const float* B,
+                 const float* C, const float* D, const float* z, const float* initial_states,
+                 const int32_t* seq_idx, const float* dout, int64_t batch, int64_t seqlen,
+                 int nheads, int headdim, int dstate, int ngroups, int chunk_size, float* dx,
+                 float* ddt, float* d_dt_bias, float* dA, float* dB, float* dC, float* dD,
+                 float* dz, float* d_initial_states, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  using namespace ssd::bwd;
+  if (!bwd_sizes_ok(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size))
+    return bfail(SSD_ERR_UNSUPPORTED,
+                 "ssd_scan_bwd: headdim and dstate in {16, 32, 64, 128}, chunk_size a power of "
+                 "two in [16, 256], ngroups dividing nheads");
+  if (!(dt_limit_lo <= dt_limit_hi)) return bfail(SSD_ERR_ARG, "dt_limit lo > hi");
+  if (!x || !dt || !A || !B || !C || !dout || !dx || !ddt || !dA || !dB || !dC || !workspace)
+    return bfail(SSD_ERR_NULL, "x, dt, A, B, C, dout, dx, ddt, dA, dB, dC, workspace required");
+  if (z && !dz) return bfail(SSD_ERR_NULL, "dz is required with z");
+  const void* ptrs[] = {x, dt, dt_bias, A, B, C, D, z, initial_states, seq_idx, dout, dx, ddt,
+                        d_dt_bias, dA, dB, dC, dD, dz, d_initial_states, workspace};
+  for (const void* p : ptrs)
+    if (((uintptr_t)p & 15u) != 0) return bfail(SSD_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const int64_t Bz = batch, L = seqlen;
+  const int H = nheads, P = headdim, N = dstate, G = ngroups, Q = bwd_chunk(chunk_size);
+  const BwdLayout lay = bwd_layout(Bz, L, H, P, N, G, Q);
+  if (workspace_bytes < lay.total) {
+    char m[160];
+    snprintf(m, sizeof(m), "workspace of %zu bytes < %zu needed", workspace_bytes, lay.total);
+    return bfail(SSD_ERR_WORKSPACE, m);
+  }
+  char* ws = static_cast<char*>(workspace);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  auto I = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const ssd::Dims d = dims_of(Bz, L, H, P, N, G, Q);
+  const int nc = d.nchunks;
+  const int64_t Lp = (int64_t)nc * Q;
+  const ssd::Dims dR = dims_of(Bz, Lp, H, P, N, G, Q);   // reversed, padded to whole chunks
+  // the swapped scans: headdim' = dstate, dstate' = headdim, one group per head
+  const ssd::Dims ds = dims_of(Bz, L, H, N, P, H, Q);
+  const ssd::Dims dsR = dims_of(Bz, Lp, H, N, P, H, Q);
+  const int clamp = !(dt_limit_lo == 0.f && isinf(dt_limit_hi) && dt_limit_hi > 0.f);
+  const bool seq = seq_idx != nullptr;
+  int32_t* segF = seq ? I(lay.segF) : nullptr;
+  int32_t* segR = seq ? I(lay.segR) : nullptr;
+  cudaError_t e = cudaSuccess;
+  auto ok = [&]() { return e == cudaSuccess && (e = cudaGetLastError()) == cudaSuccess; };
+
+  // forward quantities: stage 1, the chunk states H, and y before the gate
+  // without D x and without the diagonal (strict)
+  e = ssd::launch_dt_cumsum<float>(dt, dt_bias, dt_softplus, dt_limit_lo, dt_limit_hi, clamp, A,
+                                   seq_idx, d, F(lay.dtF), F(lay.csF), segF, st);
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_state<float>(x, B, F(lay.dtF), F(lay.csF), segF, d, F(lay.statesF), st);
+  if (e == cudaSuccess)
+    e = ssd::launch_state_passing(F(lay.statesF), F(lay.csF), segF, initial_states, nullptr, d,
+                                  st);
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_scan<float>(x, B, C, F(lay.dtF), F(lay.csF), segF, F(lay.statesF),
+                                      nullptr, nullptr, d, F(lay.yo), st, 1);
+  // gate, reversed copies, the reversed decays
+  if (e == cudaSuccess) {
+    reversed_prep_kernel<<<blocks_for(Bz * Lp * H * P, 256), 256, 0, st>>>(
+        dout, z, x, Bz, L, Lp, H * P, F(lay.dy), F(lay.dyR), F(lay.xR));
+    reverse_kernel<<<blocks_for(Bz * Lp * G * N, 256), 256, 0, st>>>(C, Bz, L, Lp, G, N, 1, 1,
+                                                                     F(lay.CR));
+    reverse_kernel<<<blocks_for(Bz * Lp * G * N, 256), 256, 0, st>>>(B, Bz, L, Lp, G, N, 1, 1,
+                                                                     F(lay.BR));
+    reverse_kernel<<<blocks_for(Bz * Lp * H * N, 256), 256, 0, st>>>(C, Bz, L, Lp, G, N, H / G,
+                                                                     1, F(lay.ChR));
+    reverse_kernel<<<blocks_for(Bz * L * H * N, 256), 256, 0, st>>>(B, Bz, L, L, G, N, H / G, 0,
+                                                                    F(lay.Bh));
+    reversed_decay_kernel<<<blocks_for(Bz * Lp * H, 256), 256, 0, st>>>(
+        F(lay.dtF), A, seq_idx, Bz, L, Lp, H, nc, Q, F(lay.aR), seq ? I(lay.seqR) : nullptr);
+    fill_kernel<<<blocks_for((int64_t)H, 256), 256, 0, st>>>(F(lay.q), H, 1.f);   // A' = 1
+    fill_kernel<<<blocks_for(Bz * H * (int64_t)nc * Q, 256), 256, 0, st>>>(
+        F(lay.ones), Bz * H * (int64_t)nc * Q, 1.f);
+    ok();
+  }
+  // stage 1 of the reversed scans: cumsum of the shifted decays (A' = 1, no softplus)
+  if (e == cudaSuccess)
+    e = ssd::launch_dt_cumsum<float>(F(lay.aR), nullptr, 0, 0.f, INFINITY, 0, F(lay.q),
+                                     seq ? I(lay.seqR) : nullptr, dR, F(lay.dtRo), F(lay.csR),
+                                     segR, st);
+  // g without the diagonal: reversed strict scan of dy with B' = C, C' = B,
+  // value coefficient 1; its chunk states are the dH of the boundaries
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_state<float>(F(lay.dyR), F(lay.CR), F(lay.ones), F(lay.csR), segR, dR,
+                                       F(lay.states1), st);
+  if (e == cudaSuccess)
+    e = ssd::launch_state_passing(F(lay.states1), F(lay.csR), segR, nullptr, F(lay.finR), dR,
+                                  st);
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_scan<float>(F(lay.dyR), F(lay.CR), F(lay.BR), F(lay.ones), F(lay.csR),
+                                      segR, F(lay.states1), nullptr, nullptr, dR, F(lay.goR), st,
+                                      1);
+  if (e == cudaSuccess) {
+    boundary_kernel<<<dim3((unsigned)nc, (unsigned)H, (unsigned)Bz), 256, 0, st>>>(
+        F(lay.statesF), F(lay.states1), segF, F(lay.dtF), A, H, P * N, nc, Q, F(lay.bnd));
+    ok();
+  }
+  // dB before the dt factor: reversed scan with x' = C, B' = dy, C' = x
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_state<float>(F(lay.ChR), F(lay.dyR), F(lay.ones), F(lay.csR), segR,
+                                       dsR, F(lay.states2), st);
+  if (e == cudaSuccess)
+    e = ssd::launch_state_passing(F(lay.states2), F(lay.csR), segR, nullptr, nullptr, dsR, st);
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_scan<float>(F(lay.ChR), F(lay.dyR), F(lay.xR), F(lay.ones), F(lay.csR),
+                                      segR, F(lay.states2), nullptr, nullptr, dsR, F(lay.oB), st);
+  // dC per head: forward scan with x' = B, B' = x, C' = dy, initial state h0^T
+  if (e == cudaSuccess && initial_states) {
+    transpose_state_kernel<<<blocks_for(Bz * H * (int64_t)P * N, 256), 256, 0, st>>>(
+        initial_states, Bz * H, P, N, F(lay.h0T));
+    ok();
+  }
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_state<float>(F(lay.Bh), x, F(lay.dtF), F(lay.csF), segF, ds,
+                                       F(lay.states2), st);
+  if (e == cudaSuccess)
+    e = ssd::launch_state_passing(F(lay.states2), F(lay.csF), segF,
+                                  initial_states ? F(lay.h0T) : nullptr, nullptr, ds, st);
+  if (e == cudaSuccess)
+    e = ssd::launch_chunk_scan<float>(F(lay.Bh), x, F(lay.dy), F(lay.dtF), F(lay.csF), segF,
+                                      F(lay.states2), nullptr, nullptr, ds, F(lay.oC), st);
+  // the per-token, per-group and per-head gradients
+  if (e == cudaSuccess) {
+    token_grads_kernel<<<blocks_for(Bz * L * H * 32, 256), 256, 0, st>>>(
+        F(lay.goR), F(lay.yo), x, dout, z, B, C, D, F(lay.dtF), Bz, L, Lp, H, P, N, G, nc, Q, dx,
+        dz, F(lay.q), F(lay.xg), F(lay.dyx));
+    group_grads_kernel<<<blocks_for(Bz * L * G * N, 256), 256, 0, st>>>(
+        F(lay.oB), F(lay.oC), F(lay.dtF), Bz, L, Lp, H, G, N, nc, Q, dB, dC);
+    e = cudaMemsetAsync(dA, 0, H * sizeof(float), st);
+    if (e == cudaSuccess && d_dt_bias) e = cudaMemsetAsync(d_dt_bias, 0, H * sizeof(float), st);
+    if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, H * sizeof(float), st);
+  }
+  if (e == cudaSuccess) {
+    dt_grads_kernel<<<blocks_for(Bz * H * (int64_t)nc * 32, 256), 256, 0, st>>>(
+        F(lay.q), F(lay.xg), F(lay.dyx), F(lay.bnd), dt, dt_bias, dt_softplus, clamp,
+        dt_limit_lo, dt_limit_hi, A, F(lay.dtF), Bz, L, H, nc, Q, ddt, dA, d_dt_bias, dD);
+    if (d_initial_states)
+      dh0_kernel<<<blocks_for(Bz * H * (int64_t)P * N, 256), 256, 0, st>>>(
+          F(lay.finR), F(lay.dtF), A, Bz, H, P * N, nc, Q, d_initial_states);
+    ok();
+  }
+  if (e != cudaSuccess) {
+    char m[200];
+    snprintf(m, sizeof(m), "ssd_scan_bwd launch: %s", cudaGetErrorString(e));
+    return bfail(SSD_ERR_CUDA, m);
+  }
+  return SSD_OK;
+}
+
+}  // extern "C"

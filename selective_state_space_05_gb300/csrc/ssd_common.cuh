@@ -62,11 +62,13 @@ cudaError_t launch_chunk_state(const T* x, const T* B, const float* dt_out, cons
 cudaError_t launch_state_passing(float* states, const float* cs, const int32_t* seg,
                                  const float* init, float* final_states, const Dims& d,
                                  cudaStream_t st);
+// strict = 1 leaves out the diagonal j = i of the intra-chunk sum (the
+// backward's scans use that form; the forward always passes 0).
 template <typename T>
 cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* dt_out,
                               const float* cs, const int32_t* seg, const float* prev,
                               const float* D, const T* z, const Dims& d, T* out,
-                              cudaStream_t st);
+                              cudaStream_t st, int strict = 0);
 
 // Fused tensor-core kernel, bf16, headdim 64, dstate 128, chunk 128 or 256.
 // Stages 2-4 always; stage 1 too when the per-token vectors are given raw

@@ -7,7 +7,7 @@
 //   1 dt_cumsum     dt = clamp(softplus(dt_raw + dt_bias)); cs
 //   2 chunk_state   S_c[p,n]  = sum_j w_j x_j[p] B_j[n],  w_j = exp(cs_last-cs_j) dt_j
 //   3 state_passing H_c = keep_c exp(cs_last) H_{c-1} + S_c
-//   4 chunk_scan    y_i = sum_{j<=i} exp(cs_i-cs_j)(C_i.B_j) dt_j x_j
+//   4 chunk_scan    y_i = sum_{j<=i} exp(cs_i-cs_j)(C_i.B_j) dt_j x_j   (j < i: strict)
 //                         + keep_i exp(cs_i) H_{c-1} C_i + D x_i, then * silu(z_i)
 // The recurrence these implement is h_t = exp(dt_t A) h_{t-1} + dt_t x_t B_t^T,
 // y_t = h_t C_t + D x_t; chunking it this way is the SSD "chunked scan" of
@@ -292,7 +292,8 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
     const T* __restrict__ x, const T* __restrict__ Bm, const T* __restrict__ Cm,
     const float* __restrict__ dtp, const float* __restrict__ cs,
     const int32_t* __restrict__ seg, const float* __restrict__ prev,
-    const float* __restrict__ D, const T* __restrict__ z, Dims d, T* __restrict__ out) {
+    const float* __restrict__ D, const T* __restrict__ z, Dims d, T* __restrict__ out,
+    int strict) {
   constexpr int TI = 32, TJ = 32, NTL = 16, KP = P / 8;
   extern __shared__ float smem[];
   const int N = d.dstate, NP1 = N + 1;
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int jj = cg + 8 * m, j = j0 + jj;
-      const bool valid = j <= irow && j < n && sg_j[jj] == sg_i[r];
+      const bool valid = j + strict <= irow && j < n && sg_j[jj] == sg_i[r];
       Ms[r * (TJ + 1) + jj] = valid ? s[m] * ex2((cs_i[r] - cs_j[jj]) * kLog2e) : 0.f;
     }
     __syncthreads();
@@ -423,7 +424,7 @@ template <typename T, int P>
 static cudaError_t chunk_scan_p(const T* x, const T* B, const T* C, const float* dtp,
                                 const float* cs, const int32_t* seg, const float* prev,
                                 const float* D, const T* z, const Dims& d, T* out,
-                                cudaStream_t st) {
+                                cudaStream_t st, int strict) {
   constexpr int TI = 32, TJ = 32, NTL = 16;
   const int NP1 = d.dstate + 1;
   const size_t smem = sizeof(float) * ((size_t)TI * NP1 + (size_t)TJ * NP1 + (size_t)P * (NTL + 1) +
@@ -436,7 +437,7 @@ static cudaError_t chunk_scan_p(const T* x, const T* B, const T* C, const float*
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)(d.batch * d.nchunks), d.nheads, (d.chunk + TI - 1) / TI);
-  kern<<<grid, 256, smem, st>>>(x, B, C, dtp, cs, seg, prev, D, z, d, out);
+  kern<<<grid, 256, smem, st>>>(x, B, C, dtp, cs, seg, prev, D, z, d, out, strict);
   return cudaGetLastError();
 }
 
@@ -444,12 +445,16 @@ template <typename T>
 cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* dtp,
                               const float* cs, const int32_t* seg, const float* prev,
                               const float* D, const T* z, const Dims& d, T* out,
-                              cudaStream_t st) {
+                              cudaStream_t st, int strict) {
   switch (d.headdim) {
-    case 16: return chunk_scan_p<T, 16>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st);
-    case 32: return chunk_scan_p<T, 32>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st);
-    case 64: return chunk_scan_p<T, 64>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st);
-    case 128: return chunk_scan_p<T, 128>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st);
+    case 16: return chunk_scan_p<T, 16>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st,
+                                             strict);
+    case 32: return chunk_scan_p<T, 32>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st,
+                                             strict);
+    case 64: return chunk_scan_p<T, 64>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st,
+                                             strict);
+    case 128: return chunk_scan_p<T, 128>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st,
+                                             strict);
   }
   return cudaErrorInvalidValue;
 }
@@ -463,7 +468,8 @@ cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* d
                                              const int32_t*, const Dims&, float*, cudaStream_t); \
   template cudaError_t launch_chunk_scan<T>(const T*, const T*, const T*, const float*,         \
                                             const float*, const int32_t*, const float*,         \
-                                            const float*, const T*, const Dims&, T*, cudaStream_t);
+                                            const float*, const T*, const Dims&, T*, cudaStream_t, \
+                                            int);
 SSD_INSTANTIATE(float)
 SSD_INSTANTIATE(__nv_bfloat16)
 

@@ -436,3 +436,60 @@ def ssd_decode_step(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch
         _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(state), Bsz, H, P, N, G, _DT[x.dtype],
         _ptr(out), _stream(stream)))
     return out
+
+
+# --- backward -----------------------------------------------------------------
+
+def bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size) -> int:
+    return int(_lib.load().ssd_scan_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                                        ngroups, chunk_size))
+
+
+def ssd_scan_bwd(dout: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor,
+                 B: torch.Tensor, C: torch.Tensor, *, chunk_size: int = 256,
+                 dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
+                 dt_limit: Tuple[float, float] = (0.0, math.inf),
+                 D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                 initial_states: Optional[torch.Tensor] = None,
+                 seq_idx: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Gradients of sum(out * dout) for the forward ssd_scan_fwd with the same
+    arguments (ssd_scan_bwd; fp32, dense tensors).  Returns a dict with
+    dx, ddt (w.r.t. the raw dt), dA, dB, dC, d_dt_bias, dD, and dz /
+    d_initial_states when z / initial_states are given."""
+    f32 = torch.float32
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    _need(dout, "dout", f32, (Bsz, L, H, P), dev)
+    _need(x, "x", f32, device=dev)
+    _need(dt, "dt", f32, (Bsz, L, H), dev)
+    _need(A, "A", f32, (H,), dev)
+    _need(B, "B", f32, (Bsz, L, G, N), dev)
+    _need(C, "C", f32, (Bsz, L, G, N), dev)
+    _need(dt_bias, "dt_bias", f32, (H,), dev, optional=True)
+    _need(D, "D", f32, (H,), dev, optional=True)
+    _need(z, "z", f32, (Bsz, L, H, P), dev, optional=True)
+    _need(initial_states, "initial_states", f32, (Bsz, H, P, N), dev, optional=True)
+    _need(seq_idx, "seq_idx", torch.int32, (Bsz, L), dev, optional=True)
+    lib = _lib.load()
+    ws_need = int(lib.ssd_scan_bwd_workspace_bytes(Bsz, L, H, P, N, G, chunk_size))
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    g = {"dx": torch.empty_like(x), "ddt": torch.empty_like(dt),
+         "dA": torch.empty(H, dtype=f32, device=dev), "dB": torch.empty_like(B),
+         "dC": torch.empty_like(C), "d_dt_bias": torch.empty(H, dtype=f32, device=dev),
+         "dD": torch.empty(H, dtype=f32, device=dev),
+         "dz": None if z is None else torch.empty_like(z),
+         "d_initial_states": (None if initial_states is None
+                              else torch.empty_like(initial_states))}
+    lo, hi = dt_limit
+    _lib.check(lib.ssd_scan_bwd(
+        _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi),
+        _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(initial_states), _ptr(seq_idx),
+        _ptr(dout), Bsz, L, H, P, N, G, int(chunk_size), _ptr(g["dx"]), _ptr(g["ddt"]),
+        _ptr(g["d_dt_bias"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+        _ptr(g["dz"]), _ptr(g["d_initial_states"]), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+    return g

@@ -31,7 +31,7 @@ def test_header_declares_the_expected_calls():
     names = declared_functions()
     for n in ("ssd_scan_fwd", "ssd_last_error", "ssd_abi_version", "ssd_scan_workspace_bytes",
               "ssd_dt_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
-              "ssd_chunk_fused"):
+              "ssd_chunk_fused", "ssd_scan_bwd", "ssd_scan_bwd_workspace_bytes"):
         assert n in names
 
 
@@ -160,3 +160,31 @@ def test_decode_step_validation_before_any_launch(lib):
     assert call(state=24) == -3
     assert call(lo=1.0, hi=0.5) == -1
     assert call(dtype=5) == -1
+
+
+def test_backward_validation_before_any_launch(lib):
+    B, L, H, P, N, G, Q = 2, 100, 4, 32, 64, 2, 64
+    need = lib.ssd_scan_bwd_workspace_bytes(B, L, H, P, N, G, Q)
+    assert need > 0
+    assert lib.ssd_scan_bwd_workspace_bytes(B, L, H, P, 48, G, Q) == 0
+    assert lib.ssd_scan_bwd_workspace_bytes(B, L, H, 256, N, G, Q) == 0
+
+    def call(**kw):
+        a = dict(x=16, dt=16, bias=None, sp=1, lo=0.0, hi=math.inf, A=16, B=16, C=16, D=None,
+                 z=None, h0=None, seq=None, dout=16, batch=B, L=L, H=H, P=P, N=N, G=G, Q=Q,
+                 dx=16, ddt=16, dbias=None, dA=16, dB=16, dC=16, dD=None, dz=None, dh0=None,
+                 ws=16, wsb=need)
+        a.update(kw)
+        return lib.ssd_scan_bwd(a["x"], a["dt"], a["bias"], a["sp"], a["lo"], a["hi"], a["A"],
+                                a["B"], a["C"], a["D"], a["z"], a["h0"], a["seq"], a["dout"],
+                                a["batch"], a["L"], a["H"], a["P"], a["N"], a["G"], a["Q"],
+                                a["dx"], a["ddt"], a["dbias"], a["dA"], a["dB"], a["dC"], a["dD"],
+                                a["dz"], a["dh0"], a["ws"], a["wsb"], None)
+    assert call(N=48) == -4 and b"dstate" in lib.ssd_last_error()
+    assert call(Q=100) == -4
+    assert call(H=3) == -4                 # ngroups must divide nheads
+    assert call(lo=1.0, hi=0.5) == -1
+    assert call(dout=None) == -2
+    assert call(z=16) == -2                # dz is required with z
+    assert call(dB=24) == -3
+    assert call(wsb=need - 1) == -5

@@ -1,0 +1,158 @@
+"""The backward of the scan on the GPU (ssd_scan_bwd, fp32) against the
+oracle's gradients: reverse-mode differentiation, in fp64, of the plain
+token-by-token recurrence.  Every gradient is compared element by element:
+x, the raw dt, dt_bias, A, B, C, D, z and the initial states.
+
+Tolerance.  Gradients with one value per input element (x, dt, B, C, z, the
+initial states): max|err| / max|ref| <= 1e-4, the forward's fp32 bound.
+Each is a sum of fp32 products over at most one chunk's tokens times dstate
+(or headdim) terms per scan, plus a sum over the chunks through the state
+chain; with fp32's 6e-8 unit roundoff and sums of random sign that stays
+near 1e-6 relative, and 1e-4 leaves the margin the forward's tests leave.
+The per-head gradients (dt_bias, A, D) are sums over every token of a head
+of per-token terms t (ddt; da dt with da the gradient of the decay exponent
+a = dt A; dy x), so the bound that the elementwise one implies is
+|err_h| <= 1e-4 sum |t_h|: a sum of terms each within a relative 1e-4.
+
+Cases span several chunks with a ragged tail, grouped B/C, documents
+(seq_idx, a one-token document among them), clamps that bite, dt without
+softplus (signed), no optional inputs at all (with the strong decays that
+unbiased dt gives), one token, and the per-head shape of the Mamba-2 2.7B
+workload."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import ssd_oracle as so
+import ssd_inputs as si
+from ssd_testutil import TOL, assert_close, errors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("x", "dt", "dt_bias", "A", "B", "C", "D", "z", "initial_states")
+OUT = {"x": "dx", "dt": "ddt", "dt_bias": "d_dt_bias", "A": "dA", "B": "dB", "C": "dC",
+       "D": "dD", "z": "dz", "initial_states": "d_initial_states"}
+
+CASES = [
+    # (id, random_small kwargs)
+    ("ragged_groups_init", dict(batch=2, seqlen=300, nheads=4, headdim=32, dstate=64,
+                                ngroups=2, chunk_size=64, init_std=0.3)),
+    ("docs_init", dict(batch=2, seqlen=300, nheads=4, headdim=32, dstate=64, ngroups=2,
+                       chunk_size=64, init_std=0.3, seq_idx_lengths=[100, 1, 199])),
+    ("clamp_softplus", dict(batch=1, seqlen=257, nheads=6, headdim=16, dstate=32, ngroups=3,
+                            chunk_size=32, dt_limit=(0.3, 1.0), init_std=0.2)),
+    ("signed_dt_no_softplus", dict(batch=2, seqlen=200, nheads=2, headdim=64, dstate=16,
+                                   ngroups=1, chunk_size=64, dt_softplus=False, dt_bias=False,
+                                   a_log_range=(math.log(0.01), math.log(0.1)))),
+    ("no_optionals", dict(batch=1, seqlen=130, nheads=4, headdim=128, dstate=16, ngroups=4,
+                          chunk_size=16, has_z=False, has_D=False, dt_bias=False)),
+    ("one_token", dict(batch=3, seqlen=1, nheads=2, headdim=16, dstate=16, ngroups=1,
+                       chunk_size=16, init_std=0.5)),
+    ("mamba2_2p7b_heads", dict(batch=1, seqlen=700, nheads=2, headdim=64, dstate=128,
+                               ngroups=1, chunk_size=256, init_std=0.1,
+                               seq_idx_lengths=[300, 400])),
+]
+
+
+def _run(d, dout):
+    import selective_state_space_05_gb300 as ssd
+    g = to_dev(d)
+    res = ssd.ssd_scan_bwd(dout.cuda(), g["x"], g["dt"], g["A"], g["B"], g["C"],
+                           chunk_size=d["chunk_size"], dt_bias=g["dt_bias"],
+                           dt_softplus=d["dt_softplus"], dt_limit=d["dt_limit"], D=g["D"],
+                           z=g["z"], initial_states=g["initial_states"], seq_idx=g["seq_idx"])
+    torch.cuda.synchronize()
+    return res
+
+
+def _head_terms(d, dout, ref):
+    """Per-token terms of the per-head gradients, as [.., H] arrays summed
+    over everything but the head: d_dt_bias <- ddt, dA <- da dt, dD <- dy x."""
+    da, dtp = so.decay_gradient(d, dout)
+    x = d["x"].double().numpy()
+    dy = dout.double().numpy()
+    if d["z"] is not None:
+        z = d["z"].double().numpy()
+        dy = dy * z / (1.0 + np.exp(-z))
+    return {"dt_bias": np.abs(ref["dt"]).sum(axis=(0, 1)),
+            "A": np.abs(da * dtp).sum(axis=(0, 1)),
+            "D": np.abs(dy * x).sum(axis=(0, 1, 3))}
+
+
+def _check(name, d, dout, got, ref):
+    scale = _head_terms(d, dout, ref)
+    bad, checked = [], 0
+    for k in NAMES:
+        if k in scale:
+            want = ref.get(k)
+            if want is None:   # not an input: its gradient is still defined
+                want = (ref["dt"].sum(axis=(0, 1)) if k == "dt_bias" else
+                        (dout.double().numpy() * d["x"].double().numpy()).sum(axis=(0, 1, 3)))
+            err = np.abs(got[OUT[k]].double().cpu().numpy() - want)
+            sc = scale[k]
+            ratio = np.where(sc > 0, err / np.where(sc > 0, sc, 1.0), np.where(err > 0, np.inf, 0.0))
+            worst = float(ratio.max())
+            if worst > TOL["f32"]:
+                bad.append(f"d{k}: max |err| / sum|terms| = {worst:.2e}")
+            checked += 1
+            continue
+        if d.get(k) is None:
+            assert got[OUT[k]] is None
+            continue
+        e = errors(got[OUT[k]].double().cpu().numpy(), ref[k])
+        if e["max_rel"] > TOL["f32"]:
+            bad.append(f"d{k}: {e}")
+        checked += 1
+    assert not bad, f"{name}: " + "; ".join(bad)
+    assert checked >= 6
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_backward_matches_oracle(case):
+    name, kw = case
+    d = si.random_small(500 + len(name), **kw)
+    dout = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(len(name)))
+    ref = so.scan_backward(d, dout)
+    _check(name, d, dout, _run(d, dout), ref)
+
+
+def test_clamped_tokens_get_no_dt_gradient():
+    """Where the clamp bites (softplus(dt + bias) outside [lo, hi]) the raw
+    dt's gradient is exactly zero; elsewhere it is not."""
+    d = si.random_small(77, batch=1, seqlen=100, nheads=2, headdim=16, dstate=16, ngroups=1,
+                        chunk_size=32, dt_limit=(0.5, 0.9))
+    dout = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(1))
+    got = _run(d, dout)["ddt"].cpu()
+    v = torch.nn.functional.softplus(d["dt"] + d["dt_bias"])
+    out = (v < 0.5) | (v > 0.9)
+    assert out.any() and (~out).any()
+    assert torch.all(got[out] == 0)
+    assert torch.count_nonzero(got[~out]) == int((~out).sum())
+
+
+def test_backward_is_linear_in_dout():
+    """The gradients are linear in dout: bwd(a u + b v) = a bwd(u) + b bwd(v)."""
+    d = si.random_small(78, batch=1, seqlen=200, nheads=2, headdim=32, dstate=32, ngroups=1,
+                        chunk_size=64, init_std=0.2, has_z=False)
+    gen = torch.Generator().manual_seed(2)
+    u, v = torch.randn(d["x"].shape, generator=gen), torch.randn(d["x"].shape, generator=gen)
+    gu, gv, gw = _run(d, u), _run(d, v), _run(d, 2.0 * u - 0.5 * v)
+    for k, t in gw.items():
+        if t is None:
+            continue
+        want = (2.0 * gu[k].double() - 0.5 * gv[k].double()).cpu().numpy()
+        assert_close(t.double().cpu().numpy(), want, 1e-5, k)
+
+
+def test_backward_rejects_bad_arguments():
+    import selective_state_space_05_gb300 as ssd
+    from selective_state_space_05_gb300._lib import SSDError
+    d = to_dev(si.random_small(79, batch=1, seqlen=40, nheads=2, headdim=16, dstate=48,
+                               ngroups=1, chunk_size=16))
+    with pytest.raises(SSDError):   # dstate 48 is not one of 16, 32, 64, 128
+        ssd.ssd_scan_bwd(torch.ones_like(d["x"]), d["x"], d["dt"], d["A"], d["B"], d["C"],
+                         chunk_size=16)
+    assert ssd.bwd_workspace_bytes(1, 40, 2, 16, 48, 1, 16) == 0
+    assert ssd.bwd_workspace_bytes(1, 40, 2, 16, 32, 1, 16) > 0

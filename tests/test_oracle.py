@@ -483,3 +483,32 @@ def test_backward_oracle_passes_gradcheck():
     grads = torch.autograd.grad((out * dout.double()).sum(), args)
     for k, gr in zip(("x", "dt", "A", "B", "C", "dt_bias", "D", "z", "initial_states"), grads):
         assert rel(g[k], gr.numpy()) < TIGHT, k
+
+
+def test_decay_gradient_by_finite_differences_and_chain_rule():
+    """decay_gradient (d loss / d a_t, a_t = dt_t A) matches central finite
+    differences of the loss in each a_t, and, since A enters the forward only
+    through a = dt A, summing it times dt over the tokens gives the
+    backward oracle's dA."""
+    d = si.random_small(72, batch=2, seqlen=7, nheads=2, ngroups=1, headdim=3, dstate=2,
+                        init_std=0.5, seq_idx_lengths=[3, 4], dt_limit=(0.0, 3.0))
+    dout = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(4)).double()
+    da, dtp = so.decay_gradient(d, dout)
+    t = {k: (None if d.get(k) is None else torch.as_tensor(d[k]).double())
+         for k in ("x", "dt", "A", "B", "C", "dt_bias", "D", "z", "initial_states")}
+
+    def loss(a):
+        out, _ = so.scan_torch(t["x"], t["dt"], t["A"], t["B"], t["C"], dt_bias=t["dt_bias"],
+                               D=t["D"], z=t["z"], initial_states=t["initial_states"],
+                               seq_idx=d["seq_idx"], dt_limit=(0.0, 3.0), a=a)
+        return float((out * dout).sum())
+    a0 = torch.from_numpy(dtp) * t["A"]
+    eps = 1e-6
+    for idx in [(0, 0, 0), (0, 2, 1), (0, 3, 0), (1, 6, 1), (1, 4, 0)]:
+        ap, am = a0.clone(), a0.clone()
+        ap[idx] += eps
+        am[idx] -= eps
+        fd = (loss(ap) - loss(am)) / (2 * eps)
+        assert abs(fd - da[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, da[idx])
+    g = so.scan_backward(d, dout)
+    assert rel((da * dtp).sum(axis=(0, 1)), g["A"]) < TIGHT
