@@ -125,12 +125,17 @@ const char* ssd_last_error(void) { return g_err; }
 int ssd_scan_status(int reset, void* stream) {
   g_err[0] = 0;
   int bits = 0;
-  const int e = ssd::fused_status(reset, static_cast<cudaStream_t>(stream), &bits);
+  int e = ssd::fused_status(reset, static_cast<cudaStream_t>(stream), &bits);
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "ssd_scan_status");
+  int bits32 = 0;
+  e = ssd::tc32_status(reset, static_cast<cudaStream_t>(stream), &bits32);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "ssd_scan_status");
+  bits |= bits32;
   if (bits != 0)
     return fail(SSD_ERR_TIMEOUT,
                 "a tensor-core scan launch gave up a bounded wait (error bits 0x%x: 1 barrier, "
-                "2 state hand-off, 4 drain); its outputs are not valid",
+                "2 state hand-off, 4 drain, 8 fp32 tensor-core stage); its outputs are not "
+                "valid",
                 bits);
   return SSD_OK;
 }

@@ -32,9 +32,10 @@
 // exactly to <dH_c, H_c>, H_c the forward state after chunk c and dH_c the
 // state of the reversed g scan at the same boundary, so
 //   da_k = sum_{m in chunk(k), m >= k} q_m + <dH_c, H_c>.
-// The backward runs its scans with its own chunk length (at most kBwdChunk;
-// the result does not depend on it), and pads the reversed sequence to whole
-// chunks so that the reversed chunk boundaries fall on the forward ones.
+// The backward runs its scans with its own chunk length (128 on the fp32
+// tensor-core stages, else at most kBwdChunk; the result does not depend on
+// it), and pads the reversed sequence to whole chunks so that the reversed
+// chunk boundaries fall on the forward ones.
 #include <math.h>
 #include <stdio.h>
 
@@ -307,7 +308,14 @@ __global__ void dh0_kernel(const float* __restrict__ F, const float* __restrict_
   dh0[i] = __expf(dtF[chunk_index(bh / H, h, 0, H, nc, Q)] * A[h]) * F[i];
 }
 
-int bwd_chunk(int chunk_size) { return chunk_size < kBwdChunk ? chunk_size : kBwdChunk; }
+// The backward's own chunk length: 128 where its scans (headdim x dstate
+// and the swapped dstate x headdim) take the fp32 tensor-core stages,
+// otherwise at most kBwdChunk (shorter in-chunk sums, see above).
+int bwd_chunk(int chunk_size, int P, int N) {
+  const bool tc = (P == 64 || P == 128) && (N == 64 || N == 128) && (P == 128 || N == 128);
+  if (tc && chunk_size >= 128) return 128;
+  return chunk_size < kBwdChunk ? chunk_size : kBwdChunk;
+}
 
 // Workspace pieces, 256-byte aligned.  Reversed arrays span Lp = nc Qb tokens.
 struct BwdLayout {
@@ -409,7 +417,7 @@ size_t ssd_scan_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, i
                                     int dstate, int ngroups, int chunk_size) {
   if (!bwd_sizes_ok(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size)) return 0;
   return ssd::bwd::bwd_layout(batch, seqlen, nheads, headdim, dstate, ngroups,
-                              ssd::bwd::bwd_chunk(chunk_size))
+                              ssd::bwd::bwd_chunk(chunk_size, headdim, dstate))
       .total;
 }
 
@@ -435,7 +443,7 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   for (const void* p : ptrs)
     if (((uintptr_t)p & 15u) != 0) return bfail(SSD_ERR_ALIGN, "pointers must be 16-byte aligned");
   const int64_t Bz = batch, L = seqlen;
-  const int H = nheads, P = headdim, N = dstate, G = ngroups, Q = bwd_chunk(chunk_size);
+  const int H = nheads, P = headdim, N = dstate, G = ngroups, Q = bwd_chunk(chunk_size, P, N);
   const BwdLayout lay = bwd_layout(Bz, L, H, P, N, G, Q);
   if (workspace_bytes < lay.total) {
     char m[160];

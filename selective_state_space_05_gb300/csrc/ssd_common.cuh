@@ -109,6 +109,24 @@ cudaError_t launch_chunk_scan_tc(const __nv_bfloat16* x, const __nv_bfloat16* B,
                                  const int32_t* seg, const float* prev_states, const float* D,
                                  const __nv_bfloat16* z, const Dims& d, __nv_bfloat16* out,
                                  cudaStream_t st);
+// fp32 stages 2 and 4 on the tensor cores (3xTF32, ssd_tc32.cu) for
+// 128-token chunks, headdim 64 or 128; chunk_state also needs dstate 64 or
+// 128 (one of the two 128), chunk_scan a dstate multiple of 32 up to 256.
+// The fp32 SIMT launchers route there when *_fits holds (16-byte aligned
+// rows; SSD_TC32=0 in the environment turns the route off).
+bool chunk_state_tc32_fits(const float* x, const float* B, const Dims& d);
+bool chunk_scan_tc32_fits(const float* x, const float* B, const float* C, const float* z,
+                          const Dims& d);
+cudaError_t launch_chunk_state_tc32(const float* x, const float* B, const float* dtp,
+                                    const float* cs, const int32_t* seg, const Dims& d,
+                                    float* states, cudaStream_t st);
+cudaError_t launch_chunk_scan_tc32(const float* x, const float* B, const float* C,
+                                   const float* dtp, const float* cs, const int32_t* seg,
+                                   const float* prev, const float* D, const float* z,
+                                   const Dims& d, float* out, cudaStream_t st, int strict);
+// Status bits of their bounded waits (8: a wait gave up), as fused_status.
+int tc32_status(int reset, cudaStream_t st, int* bits);
+
 // Device-wide status of the fused kernel's bounded waits: the error bits
 // recorded since the last reset into *bits (0: none); synchronises st.
 // Returns 0 or the cudaError_t of a failed copy.

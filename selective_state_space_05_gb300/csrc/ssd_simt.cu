@@ -13,6 +13,8 @@
 // y_t = h_t C_t + D x_t; chunking it this way is the SSD "chunked scan" of
 // mamba_chunk_scan_combined that fla-org/flash-linear-attention PR #49 compares
 // with its chunked simple-GLA kernel.
+#include <type_traits>
+
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -217,6 +219,10 @@ template <typename T>
 cudaError_t launch_chunk_state(const T* x, const T* B, const float* dtp, const float* cs,
                                const int32_t* seg, const Dims& d, float* states,
                                cudaStream_t st) {
+  if constexpr (std::is_same<T, float>::value) {
+    if (chunk_state_tc32_fits(x, B, d))
+      return launch_chunk_state_tc32(x, B, dtp, cs, seg, d, states, st);
+  }
   switch (d.headdim) {
     case 16: return chunk_state_p<T, 16>(x, B, dtp, cs, seg, d, states, st);
     case 32: return chunk_state_p<T, 32>(x, B, dtp, cs, seg, d, states, st);
@@ -446,6 +452,10 @@ cudaError_t launch_chunk_scan(const T* x, const T* B, const T* C, const float* d
                               const float* cs, const int32_t* seg, const float* prev,
                               const float* D, const T* z, const Dims& d, T* out,
                               cudaStream_t st, int strict) {
+  if constexpr (std::is_same<T, float>::value) {
+    if (chunk_scan_tc32_fits(x, B, C, z, d))
+      return launch_chunk_scan_tc32(x, B, C, dtp, cs, seg, prev, D, z, d, out, st, strict);
+  }
   switch (d.headdim) {
     case 16: return chunk_scan_p<T, 16>(x, B, C, dtp, cs, seg, prev, D, z, d, out, st,
                                              strict);

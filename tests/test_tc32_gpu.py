@@ -1,0 +1,115 @@
+"""The fp32 stages on the tensor cores (3xTF32 tcgen05, 128-token chunks):
+chunk_state and chunk_scan through the forward call and through the stage
+exports, against the oracle, for every headdim / dstate combination they
+take (and the ones where only chunk_scan does), with documents, initial
+states, ragged tails, strided views and the optional inputs missing.
+Tolerance: the forward's fp32 bound, max|err| / max|ref| <= 1e-4; the
+3xTF32 products are within about 2^-22 of fp32 ones."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import ssd_oracle as so
+import ssd_inputs as si
+from ssd_testutil import TOL, assert_close, run_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # (id, headdim, dstate): the first three take both stages on tensor
+    # cores, the last two chunk_scan only
+    ("p64_n128", 64, 128),
+    ("p128_n64", 128, 64),
+    ("p128_n128", 128, 128),
+    ("p64_n64", 64, 64),
+    ("p64_n96", 64, 96),
+]
+
+CASES = [
+    ("ragged_init_docs", dict(batch=2, seqlen=300, nheads=4, ngroups=2, init_std=0.3,
+                              seq_idx_lengths=[130, 1, 169])),
+    ("one_chunk_tail", dict(batch=1, seqlen=77, nheads=2, ngroups=1)),
+    ("no_optionals", dict(batch=2, seqlen=256, nheads=2, ngroups=2, has_z=False, has_D=False,
+                          dt_bias=False)),
+    ("docs_on_edges", dict(batch=1, seqlen=512, nheads=2, ngroups=1, init_std=0.5,
+                           seq_idx_lengths=[128, 127, 1, 256])),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
+def test_forward_fp32_chunk128_matches_oracle(shape, case):
+    _, P, N = shape
+    name, kw = case
+    d = si.random_small(3000 + P + N + len(name), headdim=P, dstate=N, chunk_size=128,
+                        dtype="f32", **kw)
+    y, f = run_gpu(d)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["f32"], "out")
+    assert_close(f, rf, TOL["f32"], "final")
+
+
+def test_forward_fp32_chunk128_strided_views():
+    """x, B, C, z as slices of one projection row per token (strides that
+    keep 16-byte rows) take the tensor-core stages and agree with the
+    oracle."""
+    import selective_state_space_05_gb300 as ssd
+    B_, L, H, P, N = 2, 200, 2, 64, 128
+    d = si.random_small(3100, batch=B_, seqlen=L, nheads=H, headdim=P, dstate=N, ngroups=1,
+                        chunk_size=128, dtype="f32", init_std=0.2)
+    W = 2 * H * P + 2 * N + 8
+    proj = torch.zeros(B_, L, W)
+    proj[:, :, :H * P] = d["z"].reshape(B_, L, -1)
+    proj[:, :, H * P:2 * H * P] = d["x"].reshape(B_, L, -1)
+    proj[:, :, 2 * H * P:2 * H * P + N] = d["B"].reshape(B_, L, -1)
+    proj[:, :, 2 * H * P + N:2 * H * P + 2 * N] = d["C"].reshape(B_, L, -1)
+    pg = proj.cuda()
+    g = to_dev(d)
+    z = pg[:, :, :H * P].unflatten(2, (H, P))
+    x = pg[:, :, H * P:2 * H * P].unflatten(2, (H, P))
+    Bm = pg[:, :, 2 * H * P:2 * H * P + N].unflatten(2, (1, N))
+    Cm = pg[:, :, 2 * H * P + N:2 * H * P + 2 * N].unflatten(2, (1, N))
+    y, f = ssd.ssd_scan_fwd(x, g["dt"], g["A"], Bm, Cm, chunk_size=128, dt_bias=g["dt_bias"],
+                            D=g["D"], z=z, initial_states=g["initial_states"],
+                            return_final_states=True, check=True)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y.double().cpu().numpy(), ry, TOL["f32"], "out")
+    assert_close(f.double().cpu().numpy(), rf, TOL["f32"], "final")
+
+
+@pytest.mark.parametrize("shape", SHAPES[:3], ids=[s[0] for s in SHAPES[:3]])
+def test_stage_exports_fp32_chunk128_match_chunked_oracle(shape):
+    """ssd_chunk_state and ssd_chunk_scan at chunk 128 in fp32 (the
+    tensor-core kernels) against the chunked oracle's intermediates."""
+    import selective_state_space_05_gb300 as ssd
+    _, P, N = shape
+    Q = 128
+    d = si.random_small(3200 + P + N, batch=2, seqlen=333, nheads=4, ngroups=2, headdim=P,
+                        dstate=N, chunk_size=Q, dtype="f32", init_std=0.3,
+                        seq_idx_lengths=[100, 1, 232])
+    ry, rf, im = so.scan_chunked(d, Q, return_intermediates=True)
+    g = to_dev(d)
+    L = d["x"].shape[1]
+    dt_out, cs, seg = ssd.ssd_dt_cumsum(g["dt"], g["A"], chunk_size=Q, dt_bias=g["dt_bias"],
+                                        seq_idx=g["seq_idx"])
+    states = ssd.ssd_chunk_state(g["x"], g["B"], dt_out, cs, seg, chunk_size=Q)
+    assert_close(states.double().cpu().numpy(), im["states"], TOL["f32"], "chunk states")
+    fin = ssd.ssd_state_passing(states, cs, seg, seqlen=L, chunk_size=Q,
+                                initial_states=g["initial_states"])
+    out = ssd.ssd_chunk_scan(g["x"], g["B"], g["C"], dt_out, cs, seg, states, chunk_size=Q,
+                             D=g["D"], z=g["z"])
+    torch.cuda.synchronize()
+    assert_close(out.double().cpu().numpy(), ry, TOL["f32"], "out")
+    assert_close(fin.double().cpu().numpy(), rf, TOL["f32"], "final")
+
+
+def test_forward_fp32_tc_status_clean():
+    """A tensor-core fp32 launch leaves the status word clear (no wait gave up)."""
+    import selective_state_space_05_gb300 as ssd
+    d = si.random_small(3300, batch=1, seqlen=256, nheads=2, headdim=64, dstate=128, ngroups=1,
+                        chunk_size=128, dtype="f32")
+    g = to_dev(d)
+    ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=128,
+                     dt_bias=g["dt_bias"], D=g["D"], z=g["z"], check=True)
+    ssd.scan_status()
