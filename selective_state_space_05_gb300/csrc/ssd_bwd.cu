@@ -78,18 +78,14 @@ __global__ void reversed_prep_kernel(const float* __restrict__ dout, const float
   xR[r] = x[i];
 }
 
-// out[b, k, h, n] = in[b, t, h / rep, n] for the [B, L, G, N] input, with
-// t = Lp-1-k (reverse, zero where t >= L) or t = k; rep > 1 broadcasts the
-// groups to H = G rep heads.
-__global__ void reverse_kernel(const float* __restrict__ in, int64_t Bz, int64_t L, int64_t Lout,
-                               int G, int N, int rep, int reverse, float* __restrict__ out) {
-  const int64_t W = (int64_t)G * rep * N;
+// out[b, k, :] = in[b, Lp-1-k, :] for a [B, L, W] input (zero where
+// Lp-1-k >= L): the time-reversed, padded copy.
+__global__ void reverse_kernel(const float* __restrict__ in, int64_t Bz, int64_t L, int64_t Lp,
+                               int64_t W, float* __restrict__ out) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= Bz * Lout * W) return;
-  const int64_t b = i / (Lout * W), k = (i / W) % Lout, c = i % W;
-  const int64_t h = c / N, n = c % N;
-  const int64_t t = reverse ? Lout - 1 - k : k;
-  out[i] = t < L ? in[(b * L + t) * G * N + (h / rep) * N + n] : 0.f;
+  if (i >= Bz * Lp * W) return;
+  const int64_t b = i / (Lp * W), t = Lp - 1 - (i / W) % Lp, c = i % W;
+  out[i] = t < L ? in[(b * L + t) * W + c] : 0.f;
 }
 
 // The reversed decays aR[b, k', h] = a_{t+1} for the reversed token k' of
@@ -319,8 +315,8 @@ int bwd_chunk(int chunk_size, int P, int N) {
 
 // Workspace pieces, 256-byte aligned.  Reversed arrays span Lp = nc Qb tokens.
 struct BwdLayout {
-  size_t dtF, csF, segF, statesF, yo, dy, dyR, xR, CR, BR, ChR, Bh, aR, seqR, csR, dtRo, segR,
-      ones, states1, finR, goR, states2, oB, h0T, oC, q, xg, dyx, bnd, total;
+  size_t dtF, csF, segF, statesF, yo, dy, dyR, xR, CR, BR, aR, seqR, csR, dtRo, segR, ones,
+      states1, finR, goR, states2, oB, h0T, oC, q, xg, dyx, bnd, total;
 };
 
 BwdLayout bwd_layout(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
@@ -347,8 +343,6 @@ BwdLayout bwd_layout(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
   l.xR = take(xsR);
   l.CR = take(bsR);
   l.BR = take(bsR);
-  l.ChR = take(hsR);
-  l.Bh = take(hs);
   l.aR = take((size_t)Bz * Lp * H);
   l.seqR = take((size_t)Bz * Lp);
   l.csR = take(chunk);
@@ -458,9 +452,15 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   const int nc = d.nchunks;
   const int64_t Lp = (int64_t)nc * Q;
   const ssd::Dims dR = dims_of(Bz, Lp, H, P, N, G, Q);   // reversed, padded to whole chunks
-  // the swapped scans: headdim' = dstate, dstate' = headdim, one group per head
-  const ssd::Dims ds = dims_of(Bz, L, H, N, P, H, Q);
-  const ssd::Dims dsR = dims_of(Bz, Lp, H, N, P, H, Q);
+  // the swapped scans: headdim' = dstate, dstate' = headdim, one group per
+  // head; their x' is the per-group B (or reversed C), read by every head of
+  // the group (xrep)
+  ssd::Dims ds = dims_of(Bz, L, H, N, P, H, Q);
+  ds.sx = {L * G * N, (int64_t)G * N};
+  ds.xrep = H / G;
+  ssd::Dims dsR = dims_of(Bz, Lp, H, N, P, H, Q);
+  dsR.sx = {Lp * G * N, (int64_t)G * N};
+  dsR.xrep = H / G;
   const int clamp = !(dt_limit_lo == 0.f && isinf(dt_limit_hi) && dt_limit_hi > 0.f);
   const bool seq = seq_idx != nullptr;
   int32_t* segF = seq ? I(lay.segF) : nullptr;
@@ -484,14 +484,10 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   if (e == cudaSuccess) {
     reversed_prep_kernel<<<blocks_for(Bz * Lp * H * P, 256), 256, 0, st>>>(
         dout, z, x, Bz, L, Lp, H * P, F(lay.dy), F(lay.dyR), F(lay.xR));
-    reverse_kernel<<<blocks_for(Bz * Lp * G * N, 256), 256, 0, st>>>(C, Bz, L, Lp, G, N, 1, 1,
-                                                                     F(lay.CR));
-    reverse_kernel<<<blocks_for(Bz * Lp * G * N, 256), 256, 0, st>>>(B, Bz, L, Lp, G, N, 1, 1,
-                                                                     F(lay.BR));
-    reverse_kernel<<<blocks_for(Bz * Lp * H * N, 256), 256, 0, st>>>(C, Bz, L, Lp, G, N, H / G,
-                                                                     1, F(lay.ChR));
-    reverse_kernel<<<blocks_for(Bz * L * H * N, 256), 256, 0, st>>>(B, Bz, L, L, G, N, H / G, 0,
-                                                                    F(lay.Bh));
+    reverse_kernel<<<blocks_for(Bz * Lp * G * N, 256), 256, 0, st>>>(C, Bz, L, Lp,
+                                                                     (int64_t)G * N, F(lay.CR));
+    reverse_kernel<<<blocks_for(Bz * Lp * G * N, 256), 256, 0, st>>>(B, Bz, L, Lp,
+                                                                     (int64_t)G * N, F(lay.BR));
     reversed_decay_kernel<<<blocks_for(Bz * Lp * H, 256), 256, 0, st>>>(
         F(lay.dtF), A, seq_idx, Bz, L, Lp, H, nc, Q, F(lay.aR), seq ? I(lay.seqR) : nullptr);
     fill_kernel<<<blocks_for((int64_t)H, 256), 256, 0, st>>>(F(lay.q), H, 1.f);   // A' = 1
@@ -521,29 +517,31 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
         F(lay.statesF), F(lay.states1), segF, F(lay.dtF), A, H, P * N, nc, Q, F(lay.bnd));
     ok();
   }
-  // dB before the dt factor: reversed scan with x' = C, B' = dy, C' = x
+  // dB before the dt factor: reversed scan with x' = C (per group), B' = dy,
+  // C' = x
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_state<float>(F(lay.ChR), F(lay.dyR), F(lay.ones), F(lay.csR), segR,
+    e = ssd::launch_chunk_state<float>(F(lay.CR), F(lay.dyR), F(lay.ones), F(lay.csR), segR,
                                        dsR, F(lay.states2), st);
   if (e == cudaSuccess)
     e = ssd::launch_state_passing(F(lay.states2), F(lay.csR), segR, nullptr, nullptr, dsR, st);
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_scan<float>(F(lay.ChR), F(lay.dyR), F(lay.xR), F(lay.ones), F(lay.csR),
+    e = ssd::launch_chunk_scan<float>(F(lay.CR), F(lay.dyR), F(lay.xR), F(lay.ones), F(lay.csR),
                                       segR, F(lay.states2), nullptr, nullptr, dsR, F(lay.oB), st);
-  // dC per head: forward scan with x' = B, B' = x, C' = dy, initial state h0^T
+  // dC per head: forward scan with x' = B (per group), B' = x, C' = dy,
+  // initial state h0^T
   if (e == cudaSuccess && initial_states) {
     transpose_state_kernel<<<blocks_for(Bz * H * (int64_t)P * N, 256), 256, 0, st>>>(
         initial_states, Bz * H, P, N, F(lay.h0T));
     ok();
   }
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_state<float>(F(lay.Bh), x, F(lay.dtF), F(lay.csF), segF, ds,
-                                       F(lay.states2), st);
+    e = ssd::launch_chunk_state<float>(B, x, F(lay.dtF), F(lay.csF), segF, ds, F(lay.states2),
+                                       st);
   if (e == cudaSuccess)
     e = ssd::launch_state_passing(F(lay.states2), F(lay.csF), segF,
                                   initial_states ? F(lay.h0T) : nullptr, nullptr, ds, st);
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_scan<float>(F(lay.Bh), x, F(lay.dy), F(lay.dtF), F(lay.csF), segF,
+    e = ssd::launch_chunk_scan<float>(B, x, F(lay.dy), F(lay.dtF), F(lay.csF), segF,
                                       F(lay.states2), nullptr, nullptr, ds, F(lay.oC), st);
   // the per-token, per-group and per-head gradients
   if (e == cudaSuccess) {

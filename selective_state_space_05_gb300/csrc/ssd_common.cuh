@@ -47,6 +47,9 @@ struct Dims {
   int nheads, headdim, dstate, ngroups, chunk;
   int nchunks;
   TokStride sx, sdt, sB, sC, sz;
+  // heads that share one x row (x row of head h: h / xrep); 1 except where
+  // the backward scans a per-group operand (B or C) in the place of x
+  int xrep = 1;
 };
 
 // Launchers (return cudaGetLastError() of their launches).

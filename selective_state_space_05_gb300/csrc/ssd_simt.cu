@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(
     for (int idx = tid; idx < TJ * P; idx += 256) {
       const int jj = idx / P, p = idx % P, j = j0 + jj;
       float v = 0.f;
-      if (j < n) v = to_f(x[toff(d.sx, b, t0 + j) + (int64_t)h * P + p]) * wj[jj];
+      if (j < n) v = to_f(x[toff(d.sx, b, t0 + j) + (int64_t)(h / d.xrep) * P + p]) * wj[jj];
       xs[jj][p] = v;
     }
     for (int idx = tid; idx < TJ * NT; idx += 256) {
@@ -375,7 +375,8 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
     }
     for (int idx = tid; idx < TJ * P; idx += 256) {
       const int jj = idx / P, p = idx % P, j = j0 + jj;
-      xs[jj * P + p] = j < n ? to_f(x[toff(d.sx, b, t0 + j) + (int64_t)h * P + p]) * dtc[j] : 0.f;
+      xs[jj * P + p] =
+          j < n ? to_f(x[toff(d.sx, b, t0 + j) + (int64_t)(h / d.xrep) * P + p]) * dtc[j] : 0.f;
     }
     if (tid < TJ) {
       const int j = min(j0 + tid, Q - 1);
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(
 
   if (irow < n) {
     const int64_t base = ((rowBC + irow) * d.nheads + h) * P;   // out (dense)
-    const int64_t xbase = toff(d.sx, b, t0 + irow) + (int64_t)h * P;
+    const int64_t xbase = toff(d.sx, b, t0 + irow) + (int64_t)(h / d.xrep) * P;
     const int64_t zbase = toff(d.sz, b, t0 + irow) + (int64_t)h * P;
     const float Dh = D ? D[h] : 0.f;
 #pragma unroll

@@ -134,11 +134,17 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
   return raw + ((1024u - (tc::smem_u32(raw) & 1023u)) & 1023u);
 }
 
+// One slice at a time: its operands are written from registers into the
+// shared tiles, one thread issues its MMAs, and while they run every thread
+// loads the next slice's operands from global memory into registers; the
+// tiles are written again only once the MMAs have completed.
+
 // ---------------------------------------------------------------------------
 // chunk_state: one CTA per (batch x chunk, head), 256 threads.  The MMA rows
 // are the 128-wide one of headdim / dstate: with dstate 128 the transposed
 // state S^T = B^T (w o x) (rows n), else S = (w o x)^T B (rows p).  K = the
-// chunk's tokens, four 32-token slices; both operands are staged transposed.
+// chunk's tokens, 32-token slices; both operands are staged transposed
+// (lane = token, rows by quads of four).
 // ---------------------------------------------------------------------------
 template <int P, int N>
 __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
@@ -147,6 +153,7 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
     float* __restrict__ states) {
   constexpr bool kT = (N == 128);
   constexpr int NR = kT ? P : N;   // MMA N: the other dimension
+  constexpr int XQ = P / 32, BQ = N / 32;   // float4 quads per thread and slice
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* tA = aligned_smem(smem_raw);    // 128 rows, hi + lo
   unsigned char* tB = tA + kQ * 256;             // NR rows, hi + lo
@@ -185,34 +192,51 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
   unsigned char* tX = kT ? tB : tA;   // (w o x)^T: P rows
   unsigned char* tBt = kT ? tA : tB;  // B^T: N rows
   constexpr uint32_t idesc = idesc_tf32(kQ, NR);
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* xh = x + (int64_t)(h / d.xrep) * P;
+  const float* bg = Bm + (int64_t)g * N;
 
-  int ns = 0;   // slices issued
-  for (int j0 = 0; j0 < n; j0 += 32, ++ns) {
-    const int j = j0 + lane;
+  float4 rx[XQ], rb[BQ];
+  auto load = [&](int s) {
+    const int j = 32 * s + lane;
     const bool tv = j < n;
-    const float wj = tv ? wsh[j] : 0.f;
-    const float* xr = x + toff(d.sx, b, t0 + (tv ? j : 0)) + (int64_t)h * P;
-    const float* br = Bm + toff(d.sB, b, t0 + (tv ? j : 0)) + (int64_t)g * N;
-    for (int q = warp; q < P / 4; q += 8) {
-      const float4 v = tv ? scale4(ld4(xr + 4 * q), wj) : make_float4(0.f, 0.f, 0.f, 0.f);
-      put1(tX, P, 4 * q, lane, v.x);
-      put1(tX, P, 4 * q + 1, lane, v.y);
-      put1(tX, P, 4 * q + 2, lane, v.z);
-      put1(tX, P, 4 * q + 3, lane, v.w);
+    const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0)), tb = toff(d.sB, b, t0 + (tv ? j : 0));
+#pragma unroll
+    for (int u = 0; u < XQ; ++u) rx[u] = tv ? ld4(xh + tx + 4 * (warp + 8 * u)) : zero4;
+#pragma unroll
+    for (int u = 0; u < BQ; ++u) rb[u] = tv ? ld4(bg + tb + 4 * (warp + 8 * u)) : zero4;
+  };
+  auto store = [&](int s) {
+    const float wj = (32 * s + lane < n) ? wsh[32 * s + lane] : 0.f;
+#pragma unroll
+    for (int u = 0; u < XQ; ++u) {
+      const int r = 4 * (warp + 8 * u);
+      put1(tX, P, r, lane, rx[u].x * wj);
+      put1(tX, P, r + 1, lane, rx[u].y * wj);
+      put1(tX, P, r + 2, lane, rx[u].z * wj);
+      put1(tX, P, r + 3, lane, rx[u].w * wj);
     }
-    for (int q = warp; q < N / 4; q += 8) {
-      const float4 v = tv ? ld4(br + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
-      put1(tBt, N, 4 * q, lane, v.x);
-      put1(tBt, N, 4 * q + 1, lane, v.y);
-      put1(tBt, N, 4 * q + 2, lane, v.z);
-      put1(tBt, N, 4 * q + 3, lane, v.w);
+#pragma unroll
+    for (int u = 0; u < BQ; ++u) {
+      const int r = 4 * (warp + 8 * u);
+      put1(tBt, N, r, lane, rb[u].x);
+      put1(tBt, N, r + 1, lane, rb[u].y);
+      put1(tBt, N, r + 2, lane, rb[u].z);
+      put1(tBt, N, r + 3, lane, rb[u].w);
     }
+  };
+
+  const int ns = (n + 31) / 32;
+  load(0);
+  for (int s = 0; s < ns; ++s) {
+    store(s);
     staged();
     if (tid == 0) {
-      mma_slice(tmem, tA, tB, NR, idesc, ns > 0);
+      mma_slice(tmem, tA, tB, NR, idesc, s > 0);
       tc::mma_commit(&bar);
     }
-    const bool ok = wait_phase(&bar, ns & 1);
+    if (s + 1 < ns) load(s + 1);
+    const bool ok = wait_phase(&bar, s & 1);
     if (!ok) ok_all = 0;
     tc::fence_after_sync();
     if (!__syncthreads_and(ok)) break;
@@ -248,6 +272,8 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
 // ---------------------------------------------------------------------------
 // chunk_scan: one CTA per (batch x chunk, head), 256 threads; TMEM columns
 // [0, 128) hold C B^T (rows i, columns j), [128, 128 + P) the output.
+// Slices: N/32 of C B^T (K = dstate), N/32 of the inter-chunk term, then one
+// per 32 tokens of M x (K = tokens).
 // ---------------------------------------------------------------------------
 template <int P>
 __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
@@ -256,6 +282,7 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
     const int32_t* __restrict__ seg, const float* __restrict__ prev,
     const float* __restrict__ D, const float* __restrict__ z, Dims d, float* __restrict__ out,
     int strict) {
+  constexpr int PQ = P / 32;   // H rows / x quads per thread and slice
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* tA = aligned_smem(smem_raw);   // 128 rows, hi + lo
   unsigned char* tB = tA + kQ * 256;            // up to 128 rows, hi + lo
@@ -294,68 +321,70 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base, tS = tmem, tY = tmem + 128;
-  uint32_t phase = 0;
-  // stage() fills the tiles, then one thread issues the slice's MMAs and all
-  // wait for them before the tiles are written again
-  auto issue = [&](uint32_t dcol, int nb, uint32_t idesc, bool acc) -> bool {
-    staged();
-    if (tid == 0) {
-      mma_slice(dcol, tA, tB, nb, idesc, acc);
-      tc::mma_commit(&bar);
-    }
-    const bool ok = wait_phase(&bar, phase);
-    phase ^= 1u;
-    if (!ok) ok_all = 0;
-    tc::fence_after_sync();
-    return __syncthreads_and(ok) != 0;
-  };
   const float* Hp = prev + (((int64_t)b * d.nchunks + c) * d.nheads + h) * (int64_t)P * N;
+  const float* xh = x + (int64_t)(h / d.xrep) * P;
+  const float* cg = Cm + (int64_t)g * N;
+  const float* bg = Bm + (int64_t)g * N;
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  // rows r of a token-major operand, 32 columns from k0: 8 threads per row
+  // token-major operands: 8 threads per row, rows sr + 32 u, columns sk .. sk + 3
   const int sr = tid >> 3, sk = (tid & 7) * 4;
-  bool ok = true;
+  const int n1 = N / 32, n3 = (n + 31) / 32, nS = 2 * n1 + n3;
+  const int q = warp & 3, half = warp >> 2;
+  const int i = 32 * q + lane;   // the row this thread builds M for and writes out
+  float4 ra[4], rb[4];
 
-  // 1. C B^T (rows i, columns j), K = dstate
-  for (int k0 = 0; ok && k0 < N; k0 += 32) {
-    for (int r = sr; r < kQ; r += 32) {
-      const bool tv = r < n;
-      const float4 cv = tv ? ld4(Cm + toff(d.sC, b, t0 + r) + (int64_t)g * N + k0 + sk) : zero4;
-      const float4 bv = tv ? ld4(Bm + toff(d.sB, b, t0 + r) + (int64_t)g * N + k0 + sk) : zero4;
-      put4(tA, kQ, r, sk, cv);
-      put4(tB, kQ, r, sk, bv);
+  auto load = [&](int s) {
+    if (s < 2 * n1) {   // C (both), B (C B^T) or H (inter-chunk)
+      const int k0 = 32 * (s < n1 ? s : s - n1);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = sr + 32 * u;
+        ra[u] = r < n ? ld4(cg + toff(d.sC, b, t0 + r) + k0 + sk) : zero4;
+      }
+      if (s < n1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = sr + 32 * u;
+          rb[u] = r < n ? ld4(bg + toff(d.sB, b, t0 + r) + k0 + sk) : zero4;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < PQ; ++u) rb[u] = ld4(Hp + (int64_t)(sr + 32 * u) * N + k0 + sk);
+      }
+    } else {            // x of tokens j0 .. j0 + 31 (lane = token)
+      const int j = 32 * (s - 2 * n1) + lane;
+      const bool tv = j < n;
+      const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0));
+#pragma unroll
+      for (int u = 0; u < PQ; ++u) rb[u] = tv ? ld4(xh + tx + 4 * (warp + 8 * u)) : zero4;
     }
-    ok = issue(tS, kQ, idesc_tf32(kQ, kQ), k0 > 0);
-  }
-  // 2. inter-chunk term (keep_i e^cs_i C_i) . H, K = dstate
-  for (int k0 = 0; ok && k0 < N; k0 += 32) {
-    for (int r = sr; r < kQ; r += 32) {
-      const bool tv = r < n;
-      const float4 cv = tv ? scale4(ld4(Cm + toff(d.sC, b, t0 + r) + (int64_t)g * N + k0 + sk),
-                                    sc_s[r])
-                           : zero4;
-      put4(tA, kQ, r, sk, cv);
-    }
-    for (int r = sr; r < P; r += 32) put4(tB, P, r, sk, ld4(Hp + (int64_t)r * N + k0 + sk));
-    ok = issue(tY, P, idesc_tf32(kQ, P), k0 > 0);
-  }
-  // 3. intra-chunk term M x, M_ij = (C_i . B_j) e^(cs_i - cs_j) dt_j over
-  //    j <= i (j < i if strict) of one document; K = tokens
-  {
-    const int q = warp & 3, half = warp >> 2;
-    const int i = 32 * q + lane;
-    const float csi = cs_s[i];
-    const int sgi = sg_s[i];
-    for (int j0 = 0; ok && j0 < n; j0 += 32) {
-      // M columns j0 + 16 half .. + 15 of row i
-      const int jb = j0 + 16 * half;
+  };
+  auto store = [&](int s) {
+    if (s < n1) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        put4(tA, kQ, sr + 32 * u, sk, ra[u]);
+        put4(tB, kQ, sr + 32 * u, sk, rb[u]);
+      }
+    } else if (s < 2 * n1) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) put4(tA, kQ, sr + 32 * u, sk, scale4(ra[u], sc_s[sr + 32 * u]));
+#pragma unroll
+      for (int u = 0; u < PQ; ++u) put4(tB, P, sr + 32 * u, sk, rb[u]);
+    } else {
+      // M_ij = (C_i . B_j) e^(cs_i - cs_j) dt_j over j <= i (j < i if strict)
+      // of one document: row i, columns j0 + 16 half .. + 15
+      const int j0 = 32 * (s - 2 * n1), jb = j0 + 16 * half;
       float m[16];
-      if (32 * q + 31 < j0) {   // every row of this block precedes the slice: zero
+      if (32 * q + 31 < j0) {   // every row of this block precedes the slice
 #pragma unroll
         for (int u = 0; u < 16; ++u) m[u] = 0.f;
       } else {
         uint32_t r[16];
         tc::tmem_ld16(tS + (static_cast<uint32_t>(32 * q) << 16) + jb, r);
         tc::tmem_ld_wait_regs(r);
+        const float csi = cs_s[i];
+        const int sgi = sg_s[i];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int j = jb + u;
@@ -366,27 +395,39 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
 #pragma unroll
       for (int u = 0; u < 16; u += 4)
         put4(tA, kQ, i, 16 * half + u, make_float4(m[u], m[u + 1], m[u + 2], m[u + 3]));
-      // x^T: rows p, columns j0 .. j0 + 31
-      const int j = j0 + lane;
-      const bool tv = j < n;
-      const float* xr = x + toff(d.sx, b, t0 + (tv ? j : 0)) + (int64_t)h * P;
-      for (int pq = warp; pq < P / 4; pq += 8) {
-        const float4 v = tv ? ld4(xr + 4 * pq) : zero4;
-        put1(tB, P, 4 * pq, lane, v.x);
-        put1(tB, P, 4 * pq + 1, lane, v.y);
-        put1(tB, P, 4 * pq + 2, lane, v.z);
-        put1(tB, P, 4 * pq + 3, lane, v.w);
+#pragma unroll
+      for (int u = 0; u < PQ; ++u) {
+        const int r = 4 * (warp + 8 * u);
+        put1(tB, P, r, lane, rb[u].x);
+        put1(tB, P, r + 1, lane, rb[u].y);
+        put1(tB, P, r + 2, lane, rb[u].z);
+        put1(tB, P, r + 3, lane, rb[u].w);
       }
-      ok = issue(tY, P, idesc_tf32(kQ, P), true);
     }
+  };
+
+  load(0);
+  for (int s = 0; s < nS; ++s) {
+    store(s);
+    staged();
+    if (tid == 0) {
+      if (s < n1)
+        mma_slice(tS, tA, tB, kQ, idesc_tf32(kQ, kQ), s > 0);
+      else
+        mma_slice(tY, tA, tB, P, idesc_tf32(kQ, P), s > n1);
+      tc::mma_commit(&bar);
+    }
+    if (s + 1 < nS) load(s + 1);
+    const bool ok = wait_phase(&bar, s & 1);
+    if (!ok) ok_all = 0;
+    tc::fence_after_sync();
+    if (!__syncthreads_and(ok)) break;
   }
-  // 4. epilogue: + D x, * silu(z), rows i < n
+  // epilogue: + D x, * silu(z), rows i < n
   if (ok_all) {
-    const int q = warp & 3, half = warp >> 2;
-    const int i = 32 * q + lane;
     const float Dh = D ? D[h] : 0.f;
     const int64_t obase = (((int64_t)b * d.seqlen + t0 + i) * d.nheads + h) * P;
-    const int64_t xbase = toff(d.sx, b, t0 + i) + (int64_t)h * P;
+    const int64_t xbase = toff(d.sx, b, t0 + i) + (int64_t)(h / d.xrep) * P;
     const int64_t zbase = toff(d.sz, b, t0 + i) + (int64_t)h * P;
 #pragma unroll
     for (int c0 = 0; c0 < P / 2; c0 += 32) {
