@@ -437,7 +437,8 @@ int ssd_decode_step(const void *x, const void *dt, const float *dt_bias,
  *   dA, d_dt_bias, dD  [nheads]   (d_dt_bias, dD may be NULL)
  *   d_initial_states  [batch, nheads, headdim, dstate]  (may be NULL)
  * d_dt_bias is the gradient of the bias whether or not dt_bias was given.
- * headdim and dstate in {16, 32, 64, 128}; chunk_size as for ssd_scan_fwd.
+ * headdim and dstate in {16, 32, 64, 128}; chunk_size as for ssd_scan_fwd;
+ * ngroups at most 8192.
  * Workspace: device memory of at least ssd_scan_bwd_workspace_bytes (0 for
  * unsupported sizes), used only during the call's stream work.  Enqueued on
  * `stream`; returns SSD_OK or a negative SSD_ERR_* (nothing launched on an

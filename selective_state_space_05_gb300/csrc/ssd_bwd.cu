@@ -52,30 +52,35 @@ __device__ __forceinline__ int64_t chunk_index(int64_t b, int h, int64_t t, int 
 }
 
 // Over the reversed index space [B, Lp, H, P] (Lp >= L; reversed token k'
-// is forward token t = Lp-1-k', padding where t >= L): dy = dout silu(z)
-// (dout without z) in forward order, and the reversed copies of dy and x
-// (zero on the padding).
+// is forward token t = Lp-1-k', padding where t >= L), four elements per
+// thread (H P is a multiple of 4): dy = dout silu(z) (dout without z) in
+// forward order, and the reversed copies of dy and x (zero on the padding).
 __global__ void reversed_prep_kernel(const float* __restrict__ dout, const float* __restrict__ z,
                                      const float* __restrict__ x, int64_t Bz, int64_t L,
                                      int64_t Lp, int HP, float* __restrict__ dy,
                                      float* __restrict__ dyR, float* __restrict__ xR) {
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (r >= Bz * Lp * HP) return;
   const int64_t b = r / (Lp * HP), t = Lp - 1 - (r / HP) % Lp, c = r % HP;
+  float4* dyr = reinterpret_cast<float4*>(dyR + r);
+  float4* xr = reinterpret_cast<float4*>(xR + r);
   if (t >= L) {
-    dyR[r] = 0.f;
-    xR[r] = 0.f;
+    *dyr = make_float4(0.f, 0.f, 0.f, 0.f);
+    *xr = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const int64_t i = (b * L + t) * HP + c;
-  float v = dout[i];
+  float4 v = *reinterpret_cast<const float4*>(dout + i);
   if (z) {
-    const float zz = z[i];
-    v *= zz / (1.f + __expf(-zz));
+    const float4 zz = *reinterpret_cast<const float4*>(z + i);
+    v.x *= zz.x / (1.f + __expf(-zz.x));
+    v.y *= zz.y / (1.f + __expf(-zz.y));
+    v.z *= zz.z / (1.f + __expf(-zz.z));
+    v.w *= zz.w / (1.f + __expf(-zz.w));
   }
-  dy[i] = v;
-  dyR[r] = v;
-  xR[r] = x[i];
+  *reinterpret_cast<float4*>(dy + i) = v;
+  *dyr = v;
+  *xr = *reinterpret_cast<const float4*>(x + i);
 }
 
 // out[b, k, :] = in[b, Lp-1-k, :] for a [B, L, W] input (zero where
@@ -118,58 +123,69 @@ __global__ void transpose_state_kernel(const float* __restrict__ in, int64_t BH,
   out[(bh * N + n) * P + p] = in[i];
 }
 
-// Per (b, t, h), one warp (lanes over P, then over N for C . B): the
-// diagonal added back (g = go + (C.B) dy, y = yo + dt x (C.B) + D x), then
-// dx, dz, and the per-token sums q, x . g and dy . x.  goR is in reversed
-// order over Lp tokens.
-__global__ void token_grads_kernel(const float* __restrict__ goR, const float* __restrict__ yo,
-                                   const float* __restrict__ x, const float* __restrict__ dout,
-                                   const float* __restrict__ z, const float* __restrict__ Bm,
-                                   const float* __restrict__ Cm, const float* __restrict__ D,
-                                   const float* __restrict__ dtF, int64_t Bz, int64_t L,
-                                   int64_t Lp, int H, int P, int N, int G, int nc, int Q,
-                                   float* __restrict__ dx, float* __restrict__ dz,
-                                   float* __restrict__ q, float* __restrict__ xg,
-                                   float* __restrict__ dyx) {
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= Bz * L * H) return;
-  const int64_t b = w / (L * H), t = (w / H) % L;
-  const int h = (int)(w % H);
-  const int64_t bg = ((b * L + t) * G + h / (H / G)) * N;
-  float cb = 0.f;
-  for (int n = lane; n < N; n += 32) cb = fmaf(Cm[bg + n], Bm[bg + n], cb);
+// One block per (b, t): C . B once per group (in shared memory), then one
+// warp per head in turn (lanes over P): the diagonal added back (g = go +
+// (C.B) dy, y = yo + dt x (C.B) + D x), dx, dz, and the per-token sums q,
+// x . g and dy . x.  goR is in reversed order over Lp tokens.
+__global__ void __launch_bounds__(256) token_grads_kernel(
+    const float* __restrict__ goR, const float* __restrict__ yo, const float* __restrict__ x,
+    const float* __restrict__ dout, const float* __restrict__ z, const float* __restrict__ Bm,
+    const float* __restrict__ Cm, const float* __restrict__ D, const float* __restrict__ dtF,
+    int64_t L, int64_t Lp, int H, int P, int N, int G, int nc, int Q, float* __restrict__ dx,
+    float* __restrict__ dz, float* __restrict__ q, float* __restrict__ xg,
+    float* __restrict__ dyx) {
+  extern __shared__ float cb_s[];   // [G]
+  const int64_t b = blockIdx.x / L, t = blockIdx.x % L;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int g = warp; g < G; g += 8) {
+    const int64_t bg = ((b * L + t) * G + g) * N;
+    float cb = 0.f;
+    for (int n = lane; n < N; n += 32) cb = fmaf(Cm[bg + n], Bm[bg + n], cb);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) cb += __shfl_xor_sync(0xffffffffu, cb, off);
-  const float dt = dtF[chunk_index(b, h, t, H, nc, Q)];
-  const float Dh = D ? D[h] : 0.f;
-  const int64_t base = w * P, rbase = ((b * Lp + (Lp - 1 - t)) * H + h) * P;
-  float s_q = 0.f, s_xg = 0.f, s_dyx = 0.f;
-  for (int p = lane; p < P; p += 32) {
-    const float xv = x[base + p], go = goR[rbase + p], yv = yo[base + p];
-    float dyv = dout[base + p];
-    if (z) {
-      const float zz = z[base + p], sg = 1.f / (1.f + __expf(-zz));
-      const float y = yv + (dt * cb + Dh) * xv;
-      dz[base + p] = dyv * y * sg * (1.f + zz * (1.f - sg));
-      dyv *= zz * sg;
+    for (int off = 16; off > 0; off >>= 1) cb += __shfl_xor_sync(0xffffffffu, cb, off);
+    if (lane == 0) cb_s[g] = cb;
+  }
+  __syncthreads();
+  for (int h = warp; h < H; h += 8) {
+    const float cb = cb_s[h / (H / G)];
+    const float dt = dtF[chunk_index(b, h, t, H, nc, Q)];
+    const float Dh = D ? D[h] : 0.f;
+    const int64_t w = (b * L + t) * H + h;
+    const int64_t base = w * P, rbase = ((b * Lp + (Lp - 1 - t)) * H + h) * P;
+    float s_q = 0.f, s_xg = 0.f, s_dyx = 0.f;
+    for (int p = 2 * lane; p < P; p += 64) {   // two consecutive elements per lane
+      const float2 xv = *reinterpret_cast<const float2*>(x + base + p);
+      const float2 go = *reinterpret_cast<const float2*>(goR + rbase + p);
+      const float2 yv = *reinterpret_cast<const float2*>(yo + base + p);
+      float2 dyv = *reinterpret_cast<const float2*>(dout + base + p);
+      if (z) {
+        const float2 zz = *reinterpret_cast<const float2*>(z + base + p);
+        const float s0 = 1.f / (1.f + __expf(-zz.x)), s1 = 1.f / (1.f + __expf(-zz.y));
+        const float y0 = yv.x + (dt * cb + Dh) * xv.x, y1 = yv.y + (dt * cb + Dh) * xv.y;
+        *reinterpret_cast<float2*>(dz + base + p) =
+            make_float2(dyv.x * y0 * s0 * (1.f + zz.x * (1.f - s0)),
+                        dyv.y * y1 * s1 * (1.f + zz.y * (1.f - s1)));
+        dyv.x *= zz.x * s0;
+        dyv.y *= zz.y * s1;
+      }
+      const float g0 = fmaf(cb, dyv.x, go.x), g1 = fmaf(cb, dyv.y, go.y);
+      *reinterpret_cast<float2*>(dx + base + p) =
+          make_float2(fmaf(dt, g0, Dh * dyv.x), fmaf(dt, g1, Dh * dyv.y));
+      s_q += dyv.x * yv.x - dt * xv.x * go.x + dyv.y * yv.y - dt * xv.y * go.y;
+      s_xg = fmaf(xv.x, g0, fmaf(xv.y, g1, s_xg));
+      s_dyx = fmaf(dyv.x, xv.x, fmaf(dyv.y, xv.y, s_dyx));
     }
-    const float g = fmaf(cb, dyv, go);
-    dx[base + p] = fmaf(dt, g, Dh * dyv);
-    s_q += dyv * yv - dt * xv * go;
-    s_xg = fmaf(xv, g, s_xg);
-    s_dyx = fmaf(dyv, xv, s_dyx);
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    s_q += __shfl_xor_sync(0xffffffffu, s_q, off);
-    s_xg += __shfl_xor_sync(0xffffffffu, s_xg, off);
-    s_dyx += __shfl_xor_sync(0xffffffffu, s_dyx, off);
-  }
-  if (lane == 0) {
-    q[w] = s_q;
-    xg[w] = s_xg;
-    dyx[w] = s_dyx;
+    for (int off = 16; off > 0; off >>= 1) {
+      s_q += __shfl_xor_sync(0xffffffffu, s_q, off);
+      s_xg += __shfl_xor_sync(0xffffffffu, s_xg, off);
+      s_dyx += __shfl_xor_sync(0xffffffffu, s_dyx, off);
+    }
+    if (lane == 0) {
+      q[w] = s_q;
+      xg[w] = s_xg;
+      dyx[w] = s_dyx;
+    }
   }
 }
 
@@ -381,7 +397,8 @@ bool bwd_sizes_ok(int64_t batch, int64_t seqlen, int nheads, int headdim, int ds
     return false;
   };
   return batch >= 1 && batch <= 65535 && seqlen >= 1 && nheads >= 1 && nheads <= 65535 &&
-         ngroups >= 1 && nheads % ngroups == 0 && pow2(headdim, 16, 128) && pow2(dstate, 16, 128) &&
+         ngroups >= 1 && ngroups <= 8192 && nheads % ngroups == 0 && pow2(headdim, 16, 128) &&
+         pow2(dstate, 16, 128) &&
          pow2(chunk, 16, 256) && (seqlen + chunk - 1) / chunk * batch <= 2147483647LL;
 }
 
@@ -427,7 +444,7 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   if (!bwd_sizes_ok(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size))
     return bfail(SSD_ERR_UNSUPPORTED,
                  "ssd_scan_bwd: headdim and dstate in {16, 32, 64, 128}, chunk_size a power of "
-                 "two in [16, 256], ngroups dividing nheads");
+                 "two in [16, 256], ngroups dividing nheads and at most 8192");
   if (!(dt_limit_lo <= dt_limit_hi)) return bfail(SSD_ERR_ARG, "dt_limit lo > hi");
   if (!x || !dt || !A || !B || !C || !dout || !dx || !ddt || !dA || !dB || !dC || !workspace)
     return bfail(SSD_ERR_NULL, "x, dt, A, B, C, dout, dx, ddt, dA, dB, dC, workspace required");
@@ -482,7 +499,7 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
                                       nullptr, nullptr, d, F(lay.yo), st, 1);
   // gate, reversed copies, the reversed decays
   if (e == cudaSuccess) {
-    reversed_prep_kernel<<<blocks_for(Bz * Lp * H * P, 256), 256, 0, st>>>(
+    reversed_prep_kernel<<<blocks_for(Bz * Lp * H * P / 4, 256), 256, 0, st>>>(
         dout, z, x, Bz, L, Lp, H * P, F(lay.dy), F(lay.dyR), F(lay.xR));
     reverse_kernel<<<blocks_for(Bz * Lp * G * N, 256), 256, 0, st>>>(C, Bz, L, Lp,
                                                                      (int64_t)G * N, F(lay.CR));
@@ -545,9 +562,9 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
                                       F(lay.states2), nullptr, nullptr, ds, F(lay.oC), st);
   // the per-token, per-group and per-head gradients
   if (e == cudaSuccess) {
-    token_grads_kernel<<<blocks_for(Bz * L * H * 32, 256), 256, 0, st>>>(
-        F(lay.goR), F(lay.yo), x, dout, z, B, C, D, F(lay.dtF), Bz, L, Lp, H, P, N, G, nc, Q, dx,
-        dz, F(lay.q), F(lay.xg), F(lay.dyx));
+    token_grads_kernel<<<(unsigned)(Bz * L), 256, G * sizeof(float), st>>>(
+        F(lay.goR), F(lay.yo), x, dout, z, B, C, D, F(lay.dtF), L, Lp, H, P, N, G, nc, Q, dx, dz,
+        F(lay.q), F(lay.xg), F(lay.dyx));
     group_grads_kernel<<<blocks_for(Bz * L * G * N, 256), 256, 0, st>>>(
         F(lay.oB), F(lay.oC), F(lay.dtF), Bz, L, Lp, H, G, N, nc, Q, dB, dC);
     e = cudaMemsetAsync(dA, 0, H * sizeof(float), st);
