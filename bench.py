@@ -16,7 +16,8 @@ MEASURED_PEAKS.json.  `cpu_baseline` times the fp64 CPU oracle on a bounded
 sample of the same workload, and `parity` compares that sample with the GPU
 output (max and mean relative error, mean signed error, 99.9th percentile).
 `other_configs` times the chained-prefill and packed-documents workloads the
-same way (inputs drawn on the device).
+same way (inputs drawn on the device), the decode step, the forward in fp32
+and the backward (ssd_scan_bwd, fp32) at the same shape.
 
 `--impl reference` times the oracle alone (the only reference this workload
 has) and prints its own line.
@@ -462,6 +463,98 @@ def decode_workload(torch, ssd, si, dev, stream, peaks, steps):
             "gpu_launches": reps * 64 + n, "data": "synthetic, drawn on the device"}
 
 
+def backward_workload(torch, ssd, si, dev, stream, peaks, steps):
+    """The backward (ssd_scan_bwd, fp32) at the 2.7B shape: gradients of
+    sum(out * dout) for every input, inputs drawn on the device.  Its
+    contractions run on the tensor cores as 3xTF32 (three tf32 MMAs per fp32
+    product), so the binding roofline is the tf32 tensor peak (the measured
+    bf16 burst x 1/2, the nominal tf32 : bf16 ratio); the HBM view of the
+    same call is reported beside it."""
+    cfg = si.CONFIGS["mamba2_2p7b"].with_(dtype="f32", init_std=0.1)
+    d = si.make_inputs(cfg, 91, device=dev)
+    Bz, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
+    gen = torch.Generator(device=dev).manual_seed(92)
+    dout = torch.randn(Bz, L, H, P, generator=gen, device=dev)
+    ws = torch.empty(ssd.bwd_workspace_bytes(Bz, L, H, P, N, G, cfg.chunk_size),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        ssd.ssd_scan_bwd(dout, d["x"], d["dt"], d["A"], d["B"], d["C"],
+                         chunk_size=cfg.chunk_size, dt_bias=d["dt_bias"], D=d["D"], z=d["z"],
+                         initial_states=d["initial_states"], workspace=ws, stream=stream)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(steps, 10))
+    ms, per = time_calls(torch, step, n, stream)
+    ssd.scan_status(stream=stream)
+    f4 = 4
+    alg = f4 * (5 * Bz * L * H * P + 2 * Bz * L * H + 4 * Bz * L * G * N + 2 * Bz * H * P * N
+                + 6 * H)
+    # MMA work per (batch row, 128-token chunk, head): two scans in each
+    # orientation (headdim x dstate and dstate x headdim), each C B^T, the
+    # inter-chunk term, M x and the chunk state, 3 tf32 products per fp32 one
+    Q = 128
+    tiles = Bz * ((L + Q - 1) // Q) * H
+
+    def scan_macs(p, n_):
+        return Q * Q * n_ + Q * p * n_ + Q * p * Q + p * n_ * Q
+    macs = 2 * (scan_macs(P, N) + scan_macs(N, P)) * tiles
+    fl_alg = 2 * macs
+    fl_exec = 3 * fl_alg
+    peak_tf32 = peaks["bf16_tflops"] / 2
+    ach = fl_exec / (ms / 1e3) / 1e12
+    hbm = alg / (ms / 1e3) / 1e9
+    return {"workload": f"backward: batch {Bz}, seqlen {L}, nheads {H}, headdim {P}, dstate {N}, "
+                        f"ngroups {G}, chunk {cfg.chunk_size} (run at 128), fp32, z gate, D, "
+                        "initial states; gradients of every input",
+            "ms_per_call": ms, "per_call_ms": spread(per), "calls": n,
+            "value": Bz * L / (ms / 1e3), "unit": "tokens/s",
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": peak_tf32,
+                         "unit": "TFLOP/s", "frac": ach / peak_tf32,
+                         "peak_source": "measured bf16 burst x 1/2 (nominal tf32 : bf16)",
+                         "flop_per_call_executed": fl_exec, "flop_per_call_fp32": fl_alg,
+                         "note": "executed = 3 tf32 MMAs per fp32 product (3xTF32)"},
+            "hbm_view": {"alg_bytes_per_call": alg, "achieved_gbs": hbm,
+                         "frac": hbm / peaks["hbm_gbs"]},
+            "data": "synthetic, drawn on the device"}
+
+
+def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps):
+    """The forward in fp32 at the 2.7B shape: the four stage kernels, with
+    chunk_state and chunk_scan on the tensor cores (3xTF32, run at 128-token
+    chunks); HBM roofline on the call's algorithmic bytes."""
+    cfg = si.CONFIGS["mamba2_2p7b"].with_(dtype="f32")
+    d = si.make_inputs(cfg, 93, device=dev)
+    Bz, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
+    out = torch.empty_like(d["x"])
+    fin = torch.empty(Bz, H, P, N, device=dev)
+    ws = torch.empty(ssd.workspace_bytes(Bz, L, H, P, N, G, cfg.chunk_size, torch.float32),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        ssd.ssd_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], chunk_size=cfg.chunk_size,
+                         dt_bias=d["dt_bias"], D=d["D"], z=d["z"], out=out, final_states=fin,
+                         return_final_states=True, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(5, min(steps, 20))
+    ms, per = time_calls(torch, step, n, stream)
+    alg = 4 * (3 * Bz * L * H * P + Bz * L * H + 2 * Bz * L * G * N + Bz * H * P * N + 3 * H)
+    ach = alg / (ms / 1e3) / 1e9
+    return {"workload": f"forward fp32: batch {Bz}, seqlen {L}, nheads {H}, headdim {P}, dstate "
+                        f"{N}, ngroups {G}, chunk {cfg.chunk_size} (stages at 128), z gate, D, "
+                        "final states",
+            "ms_per_call": ms, "per_call_ms": spread(per), "calls": n,
+            "value": Bz * L / (ms / 1e3), "unit": "tokens/s",
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "alg_bytes_per_call": alg},
+            "data": "synthetic, drawn on the device"}
+
+
 def main():
     args = parse_args()
     import ssd_inputs as si
@@ -660,6 +753,9 @@ def main():
             others[name] = other_workload(torch, ssd, si, name, dev, stream, peaks, args.steps,
                                           args.warmup, num_sms)
         others["decode"] = decode_workload(torch, ssd, si, dev, stream, peaks, args.steps)
+        others["forward_fp32"] = fp32_forward_workload(torch, ssd, si, dev, stream, peaks,
+                                                       args.steps)
+        others["backward"] = backward_workload(torch, ssd, si, dev, stream, peaks, args.steps)
 
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -109,6 +109,20 @@ Workspace carve(const ssd::Dims& d, void* base) {
 
 int do_clamp_of(float lo, float hi) { return !(lo == 0.f && isinf(hi) && hi > 0.f); }
 
+// The chunk length the forward's stages run at.  fp32 at chunk 256 runs them
+// at 128 tokens when the headdim / dstate are ones the fp32 tensor-core
+// stages take: the scan does not depend on the chunk length (only its
+// rounding does), and those stages are built for 128-token chunks.
+ssd::Dims fwd_dims(const ssd::Dims& d, ssd_dtype_t dtype) {
+  ssd::Dims e = d;
+  const bool tc = (d.headdim == 64 || d.headdim == 128) && d.dstate % 32 == 0 && d.dstate <= 256;
+  if (dtype == SSD_DTYPE_F32 && d.chunk == 256 && tc) {
+    e.chunk = 128;
+    e.nchunks = (int)((d.seqlen + 127) / 128);
+  }
+  return e;
+}
+
 }  // namespace
 
 namespace ssd {
@@ -146,7 +160,7 @@ size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int h
   if (check_dtype(dtype) != SSD_OK) return 0;
   if (check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d) != SSD_OK)
     return 0;
-  return carve(d, nullptr).bytes;
+  return carve(fwd_dims(d, dtype), nullptr).bytes;
 }
 
 int ssd_dt_cumsum(const void* dt, const float* dt_bias, int dt_softplus, float lo, float hi,
@@ -304,13 +318,14 @@ int ssd_chunk_fused(const void* x, const void* B, const void* C, const float* dt
 namespace {
 
 // The forward on validated sizes (and strides): workspace, dispatch, launches.
-int scan_fwd_run(const ssd::Dims& d, const void* x, const void* dt, const float* dt_bias,
+int scan_fwd_run(const ssd::Dims& d_in, const void* x, const void* dt, const float* dt_bias,
                  int dt_softplus, float dt_limit_lo, float dt_limit_hi, const float* A,
                  const void* B, const void* C, const float* D, const void* z,
                  const float* initial_states, const int32_t* seq_idx, ssd_dtype_t dtype,
                  void* out, float* final_states, void* workspace, size_t workspace_bytes,
                  void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const ssd::Dims d = fwd_dims(d_in, dtype);
   const size_t need = carve(d, nullptr).bytes;
   void* base = workspace;
   bool owned = false;

@@ -156,3 +156,34 @@ def test_backward_rejects_bad_arguments():
                          chunk_size=16)
     assert ssd.bwd_workspace_bytes(1, 40, 2, 16, 48, 1, 16) == 0
     assert ssd.bwd_workspace_bytes(1, 40, 2, 16, 32, 1, 16) > 0
+
+
+def test_backward_full_size_sampled_pairs():
+    """The Mamba-2 2.7B shape in fp32 (batch 8, seqlen 4096, 80 heads,
+    headdim 64, dstate 128, one group, chunk 256), the launch the benchmark
+    times: the per-element gradients of sampled (batch, head) pairs (dx, ddt,
+    dz, d_initial_states) against the oracle run on that pair alone (a head's
+    recurrence depends only on its own inputs and the shared B, C)."""
+    import selective_state_space_05_gb300 as ssd
+    cfg = si.CONFIGS["mamba2_2p7b"].with_(dtype="f32", init_std=0.1)
+    d = si.make_inputs(cfg, 95)
+    dout = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(96))
+    got = _run(d, dout)
+    for b, h in [(0, 0), (5, 47), (7, 79)]:
+        sub = {k: v for k, v in d.items()}
+        for k in ("x", "z"):
+            sub[k] = d[k][b:b + 1, :, h:h + 1].contiguous()
+        sub["dt"] = d["dt"][b:b + 1, :, h:h + 1].contiguous()
+        for k in ("B", "C"):
+            sub[k] = d[k][b:b + 1].contiguous()
+        for k in ("A", "D", "dt_bias"):
+            sub[k] = d[k][h:h + 1].contiguous()
+        sub["initial_states"] = d["initial_states"][b:b + 1, h:h + 1].contiguous()
+        sub["ngroups"] = 1
+        ref = so.scan_backward(sub, dout[b:b + 1, :, h:h + 1],
+                               names=("x", "dt", "z", "initial_states"))
+        for k, gk in (("x", "dx"), ("dt", "ddt"), ("z", "dz")):
+            g = got[gk][b:b + 1, :, h:h + 1].double().cpu().numpy()
+            assert_close(g, ref[k], TOL["f32"], f"({b},{h}) d{k}")
+        g = got["d_initial_states"][b:b + 1, h:h + 1].double().cpu().numpy()
+        assert_close(g, ref["initial_states"], TOL["f32"], f"({b},{h}) dh0")
