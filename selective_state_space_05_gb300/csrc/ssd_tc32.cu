@@ -136,8 +136,9 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
 
 // One slice at a time: its operands are written from registers into the
 // shared tiles, one thread issues its MMAs, and while they run every thread
-// loads the next slice's operands from global memory into registers; the
-// tiles are written again only once the MMAs have completed.
+// loads the operands of the slice after next from global memory into the
+// registers just stored (two register sets, so each load has two slices'
+// time to land); the tiles are written again only once the MMAs completed.
 
 // ---------------------------------------------------------------------------
 // chunk_state: one CTA per (batch x chunk, head), 256 threads.  The MMA rows
@@ -196,8 +197,10 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
   const float* xh = x + (int64_t)(h / d.xrep) * P;
   const float* bg = Bm + (int64_t)g * N;
 
-  float4 rx[XQ], rb[BQ];
-  auto load = [&](int s) {
+  const int ns = (n + 31) / 32;
+  // two register sets: slice s + 2 loads while slice s's MMAs run
+  float4 rx0[XQ], rb0[BQ], rx1[XQ], rb1[BQ];
+  auto load = [&](int s, float4(&rx)[XQ], float4(&rb)[BQ]) {
     const int j = 32 * s + lane;
     const bool tv = j < n;
     const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0)), tb = toff(d.sB, b, t0 + (tv ? j : 0));
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
 #pragma unroll
     for (int u = 0; u < BQ; ++u) rb[u] = tv ? ld4(bg + tb + 4 * (warp + 8 * u)) : zero4;
   };
-  auto store = [&](int s) {
+  auto store = [&](int s, const float4(&rx)[XQ], const float4(&rb)[BQ]) {
     const float wj = (32 * s + lane < n) ? wsh[32 * s + lane] : 0.f;
 #pragma unroll
     for (int u = 0; u < XQ; ++u) {
@@ -225,21 +228,27 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
       put1(tBt, N, r + 3, lane, rb[u].w);
     }
   };
-
-  const int ns = (n + 31) / 32;
-  load(0);
-  for (int s = 0; s < ns; ++s) {
-    store(s);
+  // one slice: store from (rx, rb), MMAs, the load of slice s + 2 into the
+  // same registers while they run, wait
+  auto step = [&](int s, float4(&rx)[XQ], float4(&rb)[BQ]) -> bool {
+    store(s, rx, rb);
     staged();
     if (tid == 0) {
       mma_slice(tmem, tA, tB, NR, idesc, s > 0);
       tc::mma_commit(&bar);
     }
-    if (s + 1 < ns) load(s + 1);
+    if (s + 2 < ns) load(s + 2, rx, rb);
     const bool ok = wait_phase(&bar, s & 1);
     if (!ok) ok_all = 0;
     tc::fence_after_sync();
-    if (!__syncthreads_and(ok)) break;
+    return __syncthreads_and(ok) != 0;
+  };
+
+  load(0, rx0, rb0);
+  if (ns > 1) load(1, rx1, rb1);
+  for (int s = 0; s < ns; s += 2) {
+    if (!step(s, rx0, rb0)) break;
+    if (s + 1 < ns && !step(s + 1, rx1, rb1)) break;
   }
   if (ok_all) {
     // each warp: TMEM lane quarter warp % 4, half of the NR columns
@@ -252,15 +261,25 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
       const int col0 = half * (NR / 2) + c0;
       tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col0, r);
       tc::tmem_ld_wait_regs(r);
-      if (kT) {
+      if (kT) {   // lanes on consecutive n: each store is one 128-byte row piece
 #pragma unroll
         for (int u = 0; u < 32; ++u) sp[(int64_t)(col0 + u) * N + row] = __uint_as_float(r[u]);
-      } else {
+      } else {    // rows of N + 4 floats in shared memory (over the tiles)
+        float* ys = reinterpret_cast<float*>(tA);
 #pragma unroll
         for (int u = 0; u < 32; u += 4)
-          *reinterpret_cast<float4*>(sp + (int64_t)row * N + col0 + u) =
+          *reinterpret_cast<float4*>(ys + row * (N + 4) + col0 + u) =
               make_float4(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
                           __uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]));
+      }
+    }
+    if (!kT) {   // then out with consecutive threads on consecutive n
+      __syncthreads();
+      const float* ys = reinterpret_cast<const float*>(tA);
+      for (int e = tid; e < P * (N / 4); e += 256) {
+        const int pr = e / (N / 4), c4 = 4 * (e % (N / 4));
+        *reinterpret_cast<float4*>(sp + (int64_t)pr * N + c4) =
+            *reinterpret_cast<const float4*>(ys + pr * (N + 4) + c4);
       }
     }
   }
@@ -331,9 +350,10 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
   const int n1 = N / 32, n3 = (n + 31) / 32, nS = 2 * n1 + n3;
   const int q = warp & 3, half = warp >> 2;
   const int i = 32 * q + lane;   // the row this thread builds M for and writes out
-  float4 ra[4], rb[4];
+  // two register sets: slice s + 2 loads while slice s's MMAs run
+  float4 ra0[4], rb0[4], ra1[4], rb1[4];
 
-  auto load = [&](int s) {
+  auto load = [&](int s, float4(&ra)[4], float4(&rb)[4]) {
     if (s < 2 * n1) {   // C (both), B (C B^T) or H (inter-chunk)
       const int k0 = 32 * (s < n1 ? s : s - n1);
 #pragma unroll
@@ -359,7 +379,7 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
       for (int u = 0; u < PQ; ++u) rb[u] = tv ? ld4(xh + tx + 4 * (warp + 8 * u)) : zero4;
     }
   };
-  auto store = [&](int s) {
+  auto store = [&](int s, const float4(&ra)[4], const float4(&rb)[4]) {
     if (s < n1) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -406,9 +426,8 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
     }
   };
 
-  load(0);
-  for (int s = 0; s < nS; ++s) {
-    store(s);
+  auto step = [&](int s, float4(&ra)[4], float4(&rb)[4]) -> bool {
+    store(s, ra, rb);
     staged();
     if (tid == 0) {
       if (s < n1)
@@ -417,46 +436,59 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
         mma_slice(tY, tA, tB, P, idesc_tf32(kQ, P), s > n1);
       tc::mma_commit(&bar);
     }
-    if (s + 1 < nS) load(s + 1);
+    if (s + 2 < nS) load(s + 2, ra, rb);
     const bool ok = wait_phase(&bar, s & 1);
     if (!ok) ok_all = 0;
     tc::fence_after_sync();
-    if (!__syncthreads_and(ok)) break;
+    return __syncthreads_and(ok) != 0;
+  };
+
+  load(0, ra0, rb0);
+  if (nS > 1) load(1, ra1, rb1);
+  for (int s = 0; s < nS; s += 2) {
+    if (!step(s, ra0, rb0)) break;
+    if (s + 1 < nS && !step(s + 1, ra1, rb1)) break;
   }
-  // epilogue: + D x, * silu(z), rows i < n
+  // epilogue: the output tile goes from TMEM through shared memory (rows of
+  // P + 4 floats, over the tiles, which the completed MMAs no longer read),
+  // then + D x and * silu(z) with consecutive threads on consecutive
+  // elements of a row, rows i < n
   if (ok_all) {
-    const float Dh = D ? D[h] : 0.f;
-    const int64_t obase = (((int64_t)b * d.seqlen + t0 + i) * d.nheads + h) * P;
-    const int64_t xbase = toff(d.sx, b, t0 + i) + (int64_t)(h / d.xrep) * P;
-    const int64_t zbase = toff(d.sz, b, t0 + i) + (int64_t)h * P;
+    constexpr int YS = P + 4;
+    float* ys = reinterpret_cast<float*>(tA);   // 128 x YS floats
 #pragma unroll
     for (int c0 = 0; c0 < P / 2; c0 += 32) {
       const int col0 = half * (P / 2) + c0;
       uint32_t r[32];
       tc::tmem_ld32(tY + (static_cast<uint32_t>(32 * q) << 16) + col0, r);
       tc::tmem_ld_wait_regs(r);
-      if (i < n) {
 #pragma unroll
-        for (int u = 0; u < 32; u += 4) {
-          float4 y = make_float4(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
-                                 __uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]));
-          if (D) {
-            const float4 xv = ld4(x + xbase + col0 + u);
-            y.x = fmaf(Dh, xv.x, y.x);
-            y.y = fmaf(Dh, xv.y, y.y);
-            y.z = fmaf(Dh, xv.z, y.z);
-            y.w = fmaf(Dh, xv.w, y.w);
-          }
-          if (z) {
-            const float4 zv = ld4(z + zbase + col0 + u);
-            y.x *= zv.x / (1.f + __expf(-zv.x));
-            y.y *= zv.y / (1.f + __expf(-zv.y));
-            y.z *= zv.z / (1.f + __expf(-zv.z));
-            y.w *= zv.w / (1.f + __expf(-zv.w));
-          }
-          *reinterpret_cast<float4*>(out + obase + col0 + u) = y;
-        }
+      for (int u = 0; u < 32; u += 4)
+        *reinterpret_cast<float4*>(ys + i * YS + col0 + u) =
+            make_float4(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
+                        __uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]));
+    }
+    __syncthreads();
+    const float Dh = D ? D[h] : 0.f;
+    for (int e = tid; e < n * (P / 4); e += 256) {
+      const int row = e / (P / 4), p = 4 * (e % (P / 4));
+      float4 y = *reinterpret_cast<const float4*>(ys + row * YS + p);
+      if (D) {
+        const float4 xv = ld4(x + toff(d.sx, b, t0 + row) + (int64_t)(h / d.xrep) * P + p);
+        y.x = fmaf(Dh, xv.x, y.x);
+        y.y = fmaf(Dh, xv.y, y.y);
+        y.z = fmaf(Dh, xv.z, y.z);
+        y.w = fmaf(Dh, xv.w, y.w);
       }
+      if (z) {
+        const float4 zv = ld4(z + toff(d.sz, b, t0 + row) + (int64_t)h * P + p);
+        y.x *= zv.x / (1.f + __expf(-zv.x));
+        y.y *= zv.y / (1.f + __expf(-zv.y));
+        y.z *= zv.z / (1.f + __expf(-zv.z));
+        y.w *= zv.w / (1.f + __expf(-zv.w));
+      }
+      *reinterpret_cast<float4*>(out + (((int64_t)b * d.seqlen + t0 + row) * d.nheads + h) * P +
+                                 p) = y;
     }
   }
   tc::fence_before_sync();
