@@ -51,7 +51,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="mamba2_2p7b (default), or one other workload alone: chained, packed, "
+                         "backward, forward_fp32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -59,6 +61,9 @@ def parse_args():
     ap.add_argument("--long-seconds", type=float, default=3.0,
                     help="length of the back-to-back block (0: skip)")
     ap.add_argument("--no-other", action="store_true", help="skip the other workloads")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="batch of --workload backward / forward_fp32 (default: the 2.7B "
+                         "shape's 8; smaller for profiler captures)")
     return ap.parse_args()
 
 
@@ -463,7 +468,7 @@ def decode_workload(torch, ssd, si, dev, stream, peaks, steps):
             "gpu_launches": reps * 64 + n, "data": "synthetic, drawn on the device"}
 
 
-def backward_workload(torch, ssd, si, dev, stream, peaks, steps):
+def backward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None):
     """The backward (ssd_scan_bwd, fp32) at the 2.7B shape: gradients of
     sum(out * dout) for every input, inputs drawn on the device.  Its
     contractions run on the tensor cores as 3xTF32 (three tf32 MMAs per fp32
@@ -471,6 +476,8 @@ def backward_workload(torch, ssd, si, dev, stream, peaks, steps):
     bf16 burst x 1/2, the nominal tf32 : bf16 ratio); the HBM view of the
     same call is reported beside it."""
     cfg = si.CONFIGS["mamba2_2p7b"].with_(dtype="f32", init_std=0.1)
+    if batch:
+        cfg = cfg.with_(batch=batch)
     d = si.make_inputs(cfg, 91, device=dev)
     Bz, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
     gen = torch.Generator(device=dev).manual_seed(92)
@@ -521,11 +528,13 @@ def backward_workload(torch, ssd, si, dev, stream, peaks, steps):
             "data": "synthetic, drawn on the device"}
 
 
-def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps):
+def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None):
     """The forward in fp32 at the 2.7B shape: the four stage kernels, with
     chunk_state and chunk_scan on the tensor cores (3xTF32, run at 128-token
     chunks); HBM roofline on the call's algorithmic bytes."""
     cfg = si.CONFIGS["mamba2_2p7b"].with_(dtype="f32")
+    if batch:
+        cfg = cfg.with_(batch=batch)
     d = si.make_inputs(cfg, 93, device=dev)
     Bz, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
     out = torch.empty_like(d["x"])
@@ -558,6 +567,21 @@ def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps):
 def main():
     args = parse_args()
     import ssd_inputs as si
+    if args.workload in ("backward", "forward_fp32"):
+        # the backward or the fp32 forward alone (for profiling it): its own line
+        import torch
+        import selective_state_space_05_gb300 as ssd
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        fn = backward_workload if args.workload == "backward" else fp32_forward_workload
+        res = fn(torch, ssd, si, dev, torch.cuda.current_stream(), load_peaks(), args.steps,
+                 batch=args.batch)
+        metric = ("SSD scan backward (all gradients) tokens/s at 2.7B shape, fp32"
+                  if args.workload == "backward" else
+                  "SSD chunked-scan fwd tokens/s at 2.7B shape, fp32")
+        print(json.dumps({"metric": metric, **res, "n_gpus": 1, "higher_is_better": True,
+                          "dtype": "f32"}), flush=True)
+        return
     cfg = si.CONFIGS[args.workload]
     if args.impl == "reference":
         run_reference(args, cfg)
