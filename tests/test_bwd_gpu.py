@@ -27,7 +27,7 @@ import torch
 
 from oracle import ssd_oracle as so
 import ssd_inputs as si
-from ssd_testutil import TOL, assert_close, errors, to_dev
+from ssd_testutil import PARITY_REPORT, TOL, assert_close, errors, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +84,7 @@ def _head_terms(d, dout, ref):
 def _check(name, d, dout, got, ref):
     scale = _head_terms(d, dout, ref)
     bad, checked = [], 0
+    report = PARITY_REPORT.setdefault(f"backward {name}", {"tol": TOL["f32"]})
     for k in NAMES:
         if k in scale:
             want = ref.get(k)
@@ -94,6 +95,7 @@ def _check(name, d, dout, got, ref):
             sc = scale[k]
             ratio = np.where(sc > 0, err / np.where(sc > 0, sc, 1.0), np.where(err > 0, np.inf, 0.0))
             worst = float(ratio.max())
+            report[f"d{k}"] = {"max_err_over_sum_abs_terms": worst}
             if worst > TOL["f32"]:
                 bad.append(f"d{k}: max |err| / sum|terms| = {worst:.2e}")
             checked += 1
@@ -102,6 +104,7 @@ def _check(name, d, dout, got, ref):
             assert got[OUT[k]] is None
             continue
         e = errors(got[OUT[k]].double().cpu().numpy(), ref[k])
+        report[f"d{k}"] = e
         if e["max_rel"] > TOL["f32"]:
             bad.append(f"d{k}: {e}")
         checked += 1
@@ -182,8 +185,11 @@ def test_backward_full_size_sampled_pairs():
         sub["ngroups"] = 1
         ref = so.scan_backward(sub, dout[b:b + 1, :, h:h + 1],
                                names=("x", "dt", "z", "initial_states"))
+        rep = PARITY_REPORT.setdefault(f"backward mamba2_2p7b fp32 pair ({b},{h})",
+                                       {"tol": TOL["f32"]})
         for k, gk in (("x", "dx"), ("dt", "ddt"), ("z", "dz")):
             g = got[gk][b:b + 1, :, h:h + 1].double().cpu().numpy()
-            assert_close(g, ref[k], TOL["f32"], f"({b},{h}) d{k}")
+            rep[f"d{k}"] = assert_close(g, ref[k], TOL["f32"], f"({b},{h}) d{k}")
         g = got["d_initial_states"][b:b + 1, h:h + 1].double().cpu().numpy()
-        assert_close(g, ref["initial_states"], TOL["f32"], f"({b},{h}) dh0")
+        rep["dinitial_states"] = assert_close(g, ref["initial_states"], TOL["f32"],
+                                              f"({b},{h}) dh0")
