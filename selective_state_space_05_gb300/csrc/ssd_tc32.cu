@@ -51,10 +51,13 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-// byte offset of fp32 element (row, k), k < 32, in a tile of 128-byte rows
-// with the 128-byte swizzle (16-byte chunks XOR row % 8)
-__device__ __forceinline__ uint32_t off32(uint32_t row, uint32_t k) {
-  return row * 128u + ((((k >> 2) ^ (row & 7u)) << 4) | ((k & 3u) << 2));
+// Operand tiles hold K slices of 16 fp32 (64-byte rows) with the 64-byte
+// swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).  A
+// split tile of R rows keeps the hi rows first and the lo rows after them.
+constexpr int kK = 16;   // K elements per slice
+
+__device__ __forceinline__ uint32_t off16(uint32_t row, uint32_t k) {   // k < 16
+  return row * 64u + ((((k >> 2) ^ ((row >> 1) & 3u)) << 4) | ((k & 3u) << 2));
 }
 
 __device__ __forceinline__ void split(float v, float& hi, float& lo) {
@@ -62,13 +65,12 @@ __device__ __forceinline__ void split(float v, float& hi, float& lo) {
   lo = v - hi;
 }
 
-// A split tile: hi rows at t, lo rows at t + rows * 128.
 __device__ __forceinline__ void put1(unsigned char* t, int rows, int r, int k, float v) {
   float hi, lo;
   split(v, hi, lo);
-  const uint32_t o = off32(r, k);
+  const uint32_t o = off16(r, k);
   *reinterpret_cast<float*>(t + o) = hi;
-  *reinterpret_cast<float*>(t + rows * 128 + o) = lo;
+  *reinterpret_cast<float*>(t + rows * 64 + o) = lo;
 }
 // four consecutive k (k % 4 == 0) of row r
 __device__ __forceinline__ void put4(unsigned char* t, int rows, int r, int k, float4 v) {
@@ -77,9 +79,9 @@ __device__ __forceinline__ void put4(unsigned char* t, int rows, int r, int k, f
   split(v.y, hi.y, lo.y);
   split(v.z, hi.z, lo.z);
   split(v.w, hi.w, lo.w);
-  const uint32_t o = off32(r, k);
+  const uint32_t o = off16(r, k);
   *reinterpret_cast<float4*>(t + o) = hi;
-  *reinterpret_cast<float4*>(t + rows * 128 + o) = lo;
+  *reinterpret_cast<float4*>(t + rows * 64 + o) = lo;
 }
 
 __device__ __forceinline__ float4 ld4(const float* p) {
@@ -104,17 +106,30 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D (+)= A B^T over one 32-wide K slice of split tiles (3 x 4 MMAs).
+// Shared-memory descriptor of a K-major tile with the 64-byte swizzle:
+// 8-row groups of 64-byte rows 512 bytes apart (SBO), one swizzle atom wide
+// in K (LBO unused), base 512-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;    // LBO (16 bytes, unused)
+  d |= static_cast<uint64_t>(512u >> 4) << 32;
+  d |= 1ull << 46;                         // descriptor version used by tcgen05
+  d |= 4ull << 61;                         // 64-byte swizzle
+  return d;
+}
+
+// D (+)= A B^T over one 16-wide K slice of split tiles (3 x 2 MMAs).
 // a: 128 rows, b: nb rows; the first MMA overwrites D unless acc.
 __device__ __forceinline__ void mma_slice(uint32_t d, const unsigned char* a,
                                           const unsigned char* b, int nb, uint32_t idesc,
                                           bool acc) {
-  const uint64_t ah = tc::sdesc_sw128(tc::smem_u32(a), 16, 1024);
-  const uint64_t al = tc::sdesc_sw128(tc::smem_u32(a + kQ * 128), 16, 1024);
-  const uint64_t bh = tc::sdesc_sw128(tc::smem_u32(b), 16, 1024);
-  const uint64_t bl = tc::sdesc_sw128(tc::smem_u32(b + nb * 128), 16, 1024);
+  const uint64_t ah = sdesc_sw64(tc::smem_u32(a));
+  const uint64_t al = sdesc_sw64(tc::smem_u32(a + kQ * 64));
+  const uint64_t bh = sdesc_sw64(tc::smem_u32(b));
+  const uint64_t bl = sdesc_sw64(tc::smem_u32(b + nb * 64));
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 2; ++k) {
     const uint64_t o = static_cast<uint64_t>(k * 2);   // 32 bytes, in 16-byte units
     mma_tf32(d, ah + o, bh + o, idesc, (acc || k > 0) ? 1u : 0u);
     mma_tf32(d, ah + o, bl + o, idesc, 1u);
@@ -122,30 +137,58 @@ __device__ __forceinline__ void mma_slice(uint32_t d, const unsigned char* a,
   }
 }
 
-// Makes this thread's shared stores visible to the MMAs, then syncs the CTA.
-__device__ __forceinline__ void staged() {
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-}
-
 __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
   return raw + ((1024u - (tc::smem_u32(raw) & 1023u)) & 1023u);
 }
 
-// One slice at a time: its operands are written from registers into the
-// shared tiles, one thread issues its MMAs, and while they run every thread
-// loads the operands of the slice after next from global memory into the
-// registers just stored (two register sets, so each load has two slices'
-// time to land); the tiles are written again only once the MMAs completed.
+// Two buffers of split tiles, 32 KB each (A: 128 rows, B: up to 128 rows,
+// hi and lo, 64-byte rows).  Slice s fills buffer s % 2 while the MMAs of
+// slice s - 1 read the other one; before the fill, the MMAs of slice s - 2
+// (the buffer's previous contents) must be complete.
+constexpr int kBuf = 2 * kQ * 64 * 2;   // bytes per buffer
+
+// The pipeline both kernels run: slice s waits for its buffer, stores its
+// operands (from registers loaded two slices earlier) and loads those of
+// slice s + 2, then, once every thread has stored, one thread issues the
+// slice's MMAs and commits them to the buffer's mbarrier.  Returns false if a
+// bounded wait gave up (uniform over the CTA).
+template <typename Store, typename Load, typename Issue>
+__device__ __forceinline__ bool pipeline_step(int s, int nS, uint64_t* bars, int tid,
+                                             int& ok_all, Store&& store, Load&& load,
+                                             Issue&& issue) {
+  bool ok = true;
+  if (s >= 2) ok = wait_phase(&bars[s & 1], ((s - 2) >> 1) & 1);
+  tc::fence_after_sync();
+  if (ok) store(s);
+  if (s + 2 < nS) load(s + 2);
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  if (!ok) ok_all = 0;
+  if (!__syncthreads_and(ok)) return false;
+  tc::fence_after_sync();
+  if (tid == 0) {
+    issue(s);
+    tc::mma_commit(&bars[s & 1]);
+  }
+  return true;
+}
+
+// Waits for the last slice's MMAs (so every earlier one) before the
+// accumulators are read or the TMEM is freed.
+__device__ __forceinline__ bool pipeline_drain(int nS, uint64_t* bars, int& ok_all) {
+  bool ok = true;
+  if (nS > 0) ok = wait_phase(&bars[(nS - 1) & 1], ((nS - 1) >> 1) & 1);
+  tc::fence_after_sync();
+  if (!ok) ok_all = 0;
+  return __syncthreads_and(ok) != 0;
+}
 
 // ---------------------------------------------------------------------------
 // chunk_state: one CTA per (batch x chunk, head), 256 threads.  The MMA rows
 // are the 128-wide one of headdim / dstate: with dstate 128 the transposed
 // state S^T = B^T (w o x) (rows n), else S = (w o x)^T B (rows p).  K = the
-// chunk's tokens, 32-token slices; both operands are staged transposed
-// (lane = token, rows by quads of four).
+// chunk's tokens, 16-token slices; both operands are staged transposed
+// (16 lanes on the tokens, the other half-warp on the next row quad).
 // ---------------------------------------------------------------------------
 template <int P, int N>
 __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
@@ -154,12 +197,11 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
     float* __restrict__ states) {
   constexpr bool kT = (N == 128);
   constexpr int NR = kT ? P : N;   // MMA N: the other dimension
-  constexpr int XQ = P / 32, BQ = N / 32;   // float4 quads per thread and slice
+  constexpr int XQ = P / 64, BQ = N / 64;   // row quads per thread and slice (16 per warp)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* tA = aligned_smem(smem_raw);    // 128 rows, hi + lo
-  unsigned char* tB = tA + kQ * 256;             // NR rows, hi + lo
+  unsigned char* base = aligned_smem(smem_raw);
   __shared__ float wsh[kQ];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bars[2];
   __shared__ uint32_t tmem_base;
   __shared__ int ok_all;
 
@@ -178,7 +220,8 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
     wsh[tid] = w;
   }
   if (tid == 0) {
-    tc::mbar_init(&bar, 1);
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
     tc::mbar_fence_init();
     ok_all = 1;
   }
@@ -190,71 +233,67 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  unsigned char* tX = kT ? tB : tA;   // (w o x)^T: P rows
-  unsigned char* tBt = kT ? tA : tB;  // B^T: N rows
   constexpr uint32_t idesc = idesc_tf32(kQ, NR);
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   const float* xh = x + (int64_t)(h / d.xrep) * P;
   const float* bg = Bm + (int64_t)g * N;
+  const int jl = lane & 15, qh = lane >> 4;   // token in the slice, row-quad half
+  // tiles of buffer u: A (128 rows) then B (NR rows)
+  auto tA = [&](int u) { return base + u * kBuf; };
+  auto tB = [&](int u) { return base + u * kBuf + kQ * 128; };
 
-  const int ns = (n + 31) / 32;
-  // two register sets: slice s + 2 loads while slice s's MMAs run
+  const int nS = (n + kK - 1) / kK;
+  // two register sets: slice s + 2 loads while slice s is stored / multiplied
   float4 rx0[XQ], rb0[BQ], rx1[XQ], rb1[BQ];
-  auto load = [&](int s, float4(&rx)[XQ], float4(&rb)[BQ]) {
-    const int j = 32 * s + lane;
+  auto load_into = [&](int s, float4(&rx)[XQ], float4(&rb)[BQ]) {
+    const int j = kK * s + jl;
     const bool tv = j < n;
     const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0)), tb = toff(d.sB, b, t0 + (tv ? j : 0));
 #pragma unroll
-    for (int u = 0; u < XQ; ++u) rx[u] = tv ? ld4(xh + tx + 4 * (warp + 8 * u)) : zero4;
+    for (int u = 0; u < XQ; ++u) rx[u] = tv ? ld4(xh + tx + 4 * (2 * warp + qh + 16 * u)) : zero4;
 #pragma unroll
-    for (int u = 0; u < BQ; ++u) rb[u] = tv ? ld4(bg + tb + 4 * (warp + 8 * u)) : zero4;
+    for (int u = 0; u < BQ; ++u) rb[u] = tv ? ld4(bg + tb + 4 * (2 * warp + qh + 16 * u)) : zero4;
   };
-  auto store = [&](int s, const float4(&rx)[XQ], const float4(&rb)[BQ]) {
-    const float wj = (32 * s + lane < n) ? wsh[32 * s + lane] : 0.f;
+  auto store_from = [&](int s, const float4(&rx)[XQ], const float4(&rb)[BQ]) {
+    unsigned char* tX = kT ? tB(s & 1) : tA(s & 1);    // (w o x)^T: P rows
+    unsigned char* tBt = kT ? tA(s & 1) : tB(s & 1);   // B^T: N rows
+    const float wj = (kK * s + jl < n) ? wsh[kK * s + jl] : 0.f;
 #pragma unroll
     for (int u = 0; u < XQ; ++u) {
-      const int r = 4 * (warp + 8 * u);
-      put1(tX, P, r, lane, rx[u].x * wj);
-      put1(tX, P, r + 1, lane, rx[u].y * wj);
-      put1(tX, P, r + 2, lane, rx[u].z * wj);
-      put1(tX, P, r + 3, lane, rx[u].w * wj);
+      const int r = 4 * (2 * warp + qh + 16 * u);
+      put1(tX, P, r, jl, rx[u].x * wj);
+      put1(tX, P, r + 1, jl, rx[u].y * wj);
+      put1(tX, P, r + 2, jl, rx[u].z * wj);
+      put1(tX, P, r + 3, jl, rx[u].w * wj);
     }
 #pragma unroll
     for (int u = 0; u < BQ; ++u) {
-      const int r = 4 * (warp + 8 * u);
-      put1(tBt, N, r, lane, rb[u].x);
-      put1(tBt, N, r + 1, lane, rb[u].y);
-      put1(tBt, N, r + 2, lane, rb[u].z);
-      put1(tBt, N, r + 3, lane, rb[u].w);
+      const int r = 4 * (2 * warp + qh + 16 * u);
+      put1(tBt, N, r, jl, rb[u].x);
+      put1(tBt, N, r + 1, jl, rb[u].y);
+      put1(tBt, N, r + 2, jl, rb[u].z);
+      put1(tBt, N, r + 3, jl, rb[u].w);
     }
   };
-  // one slice: store from (rx, rb), MMAs, the load of slice s + 2 into the
-  // same registers while they run, wait
-  auto step = [&](int s, float4(&rx)[XQ], float4(&rb)[BQ]) -> bool {
-    store(s, rx, rb);
-    staged();
-    if (tid == 0) {
-      mma_slice(tmem, tA, tB, NR, idesc, s > 0);
-      tc::mma_commit(&bar);
-    }
-    if (s + 2 < ns) load(s + 2, rx, rb);
-    const bool ok = wait_phase(&bar, s & 1);
-    if (!ok) ok_all = 0;
-    tc::fence_after_sync();
-    return __syncthreads_and(ok) != 0;
-  };
+  auto issue = [&](int s) { mma_slice(tmem, tA(s & 1), tB(s & 1), NR, idesc, s > 0); };
 
-  load(0, rx0, rb0);
-  if (ns > 1) load(1, rx1, rb1);
-  for (int s = 0; s < ns; s += 2) {
-    if (!step(s, rx0, rb0)) break;
-    if (s + 1 < ns && !step(s + 1, rx1, rb1)) break;
+  load_into(0, rx0, rb0);
+  if (nS > 1) load_into(1, rx1, rb1);
+  bool run = true;
+  for (int s = 0; run && s < nS; s += 2) {
+    run = pipeline_step(s, nS, bars, tid, ok_all, [&](int t) { store_from(t, rx0, rb0); },
+                        [&](int t) { load_into(t, rx0, rb0); }, issue);
+    if (run && s + 1 < nS)
+      run = pipeline_step(s + 1, nS, bars, tid, ok_all, [&](int t) { store_from(t, rx1, rb1); },
+                          [&](int t) { load_into(t, rx1, rb1); }, issue);
   }
-  if (ok_all) {
+  if (run) run = pipeline_drain(nS, bars, ok_all);
+  if (run) {
     // each warp: TMEM lane quarter warp % 4, half of the NR columns
     const int q = warp & 3, half = warp >> 2;
     const int row = 32 * q + lane;   // n (kT) or p
     float* sp = states + (((int64_t)b * d.nchunks + c) * d.nheads + h) * (int64_t)P * N;
+    float* ys = reinterpret_cast<float*>(base);
 #pragma unroll
     for (int c0 = 0; c0 < NR / 2; c0 += 32) {
       uint32_t r[32];
@@ -265,7 +304,6 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
 #pragma unroll
         for (int u = 0; u < 32; ++u) sp[(int64_t)(col0 + u) * N + row] = __uint_as_float(r[u]);
       } else {    // rows of N + 4 floats in shared memory (over the tiles)
-        float* ys = reinterpret_cast<float*>(tA);
 #pragma unroll
         for (int u = 0; u < 32; u += 4)
           *reinterpret_cast<float4*>(ys + row * (N + 4) + col0 + u) =
@@ -275,7 +313,6 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
     }
     if (!kT) {   // then out with consecutive threads on consecutive n
       __syncthreads();
-      const float* ys = reinterpret_cast<const float*>(tA);
       for (int e = tid; e < P * (N / 4); e += 256) {
         const int pr = e / (N / 4), c4 = 4 * (e % (N / 4));
         *reinterpret_cast<float4*>(sp + (int64_t)pr * N + c4) =
@@ -291,23 +328,23 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
 // ---------------------------------------------------------------------------
 // chunk_scan: one CTA per (batch x chunk, head), 256 threads; TMEM columns
 // [0, 128) hold C B^T (rows i, columns j), [128, 128 + P) the output.
-// Slices: N/32 of C B^T (K = dstate), N/32 of the inter-chunk term, then one
-// per 32 tokens of M x (K = tokens).
+// Slices: N/16 of C B^T (K = dstate), N/16 of the inter-chunk term, then one
+// per 16 tokens of M x (K = tokens).  kXZ: D or z given (the epilogue reads
+// x and z); without them the epilogue only copies the tile out.
 // ---------------------------------------------------------------------------
-template <int P>
-__global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
+template <int P, bool kXZ>
+__global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     const float* __restrict__ x, const float* __restrict__ Bm, const float* __restrict__ Cm,
     const float* __restrict__ dtp, const float* __restrict__ cs,
     const int32_t* __restrict__ seg, const float* __restrict__ prev,
     const float* __restrict__ D, const float* __restrict__ z, Dims d, float* __restrict__ out,
     int strict) {
-  constexpr int PQ = P / 32;   // H rows / x quads per thread and slice
+  constexpr int PQ = P / 64;   // H row pairs / x quads per thread and slice
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* tA = aligned_smem(smem_raw);   // 128 rows, hi + lo
-  unsigned char* tB = tA + kQ * 256;            // up to 128 rows, hi + lo
+  unsigned char* base = aligned_smem(smem_raw);
   __shared__ float cs_s[kQ], dt_s[kQ], sc_s[kQ];
   __shared__ int sg_s[kQ];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bars[2];
   __shared__ uint32_t tmem_base;
   __shared__ int ok_all;
 
@@ -328,7 +365,8 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
     sc_s[tid] = (sp == nullptr || sp[tid] == 0) ? ex2(v * kLog2e) : 0.f;   // keep_i e^cs_i
   }
   if (tid == 0) {
-    tc::mbar_init(&bar, 1);
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
     tc::mbar_fence_init();
     ok_all = 1;
   }
@@ -345,117 +383,140 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
   const float* cg = Cm + (int64_t)g * N;
   const float* bg = Bm + (int64_t)g * N;
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  // token-major operands: 8 threads per row, rows sr + 32 u, columns sk .. sk + 3
-  const int sr = tid >> 3, sk = (tid & 7) * 4;
-  const int n1 = N / 32, n3 = (n + 31) / 32, nS = 2 * n1 + n3;
+  // token-major operands: 4 threads per row, rows sr + 64 u, columns sk .. sk + 3
+  const int sr = tid >> 2, sk = (tid & 3) * 4;
+  const int n1 = N / kK, n3 = (n + kK - 1) / kK, nS = 2 * n1 + n3;
   const int q = warp & 3, half = warp >> 2;
   const int i = 32 * q + lane;   // the row this thread builds M for and writes out
-  // two register sets: slice s + 2 loads while slice s's MMAs run
-  float4 ra0[4], rb0[4], ra1[4], rb1[4];
+  const int jl = lane & 15, qh = lane >> 4;   // x^T: token in the slice, row-quad half
+  auto tA = [&](int u) { return base + u * kBuf; };
+  auto tB = [&](int u) { return base + u * kBuf + kQ * 128; };
 
-  auto load = [&](int s, float4(&ra)[4], float4(&rb)[4]) {
+  // two register sets: slice s + 2 loads while slice s is stored / multiplied
+  float4 ra0[2], rb0[2], ra1[2], rb1[2];
+  auto load_into = [&](int s, float4(&ra)[2], float4(&rb)[2]) {
     if (s < 2 * n1) {   // C (both), B (C B^T) or H (inter-chunk)
-      const int k0 = 32 * (s < n1 ? s : s - n1);
+      const int k0 = kK * (s < n1 ? s : s - n1);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = sr + 32 * u;
+      for (int u = 0; u < 2; ++u) {
+        const int r = sr + 64 * u;
         ra[u] = r < n ? ld4(cg + toff(d.sC, b, t0 + r) + k0 + sk) : zero4;
       }
       if (s < n1) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int r = sr + 32 * u;
+        for (int u = 0; u < 2; ++u) {
+          const int r = sr + 64 * u;
           rb[u] = r < n ? ld4(bg + toff(d.sB, b, t0 + r) + k0 + sk) : zero4;
         }
       } else {
 #pragma unroll
-        for (int u = 0; u < PQ; ++u) rb[u] = ld4(Hp + (int64_t)(sr + 32 * u) * N + k0 + sk);
+        for (int u = 0; u < PQ; ++u) rb[u] = ld4(Hp + (int64_t)(sr + 64 * u) * N + k0 + sk);
       }
-    } else {            // x of tokens j0 .. j0 + 31 (lane = token)
-      const int j = 32 * (s - 2 * n1) + lane;
+    } else {            // x of tokens j0 .. j0 + 15 (16 lanes on the tokens)
+      const int j = kK * (s - 2 * n1) + jl;
       const bool tv = j < n;
       const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0));
 #pragma unroll
-      for (int u = 0; u < PQ; ++u) rb[u] = tv ? ld4(xh + tx + 4 * (warp + 8 * u)) : zero4;
+      for (int u = 0; u < PQ; ++u) rb[u] = tv ? ld4(xh + tx + 4 * (2 * warp + qh + 16 * u)) : zero4;
     }
   };
-  auto store = [&](int s, const float4(&ra)[4], const float4(&rb)[4]) {
+  auto store_from = [&](int s, const float4(&ra)[2], const float4(&rb)[2]) {
+    unsigned char* a = tA(s & 1);
+    unsigned char* bt = tB(s & 1);
     if (s < n1) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        put4(tA, kQ, sr + 32 * u, sk, ra[u]);
-        put4(tB, kQ, sr + 32 * u, sk, rb[u]);
+      for (int u = 0; u < 2; ++u) {
+        put4(a, kQ, sr + 64 * u, sk, ra[u]);
+        put4(bt, kQ, sr + 64 * u, sk, rb[u]);
       }
     } else if (s < 2 * n1) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) put4(tA, kQ, sr + 32 * u, sk, scale4(ra[u], sc_s[sr + 32 * u]));
+      for (int u = 0; u < 2; ++u) put4(a, kQ, sr + 64 * u, sk, scale4(ra[u], sc_s[sr + 64 * u]));
 #pragma unroll
-      for (int u = 0; u < PQ; ++u) put4(tB, P, sr + 32 * u, sk, rb[u]);
+      for (int u = 0; u < PQ; ++u) put4(bt, P, sr + 64 * u, sk, rb[u]);
     } else {
       // M_ij = (C_i . B_j) e^(cs_i - cs_j) dt_j over j <= i (j < i if strict)
-      // of one document: row i, columns j0 + 16 half .. + 15
-      const int j0 = 32 * (s - 2 * n1), jb = j0 + 16 * half;
-      float m[16];
+      // of one document: row i, columns j0 + 8 half .. + 7
+      const int j0 = kK * (s - 2 * n1), jb = j0 + 8 * half;
+      float m[8];
       if (32 * q + 31 < j0) {   // every row of this block precedes the slice
 #pragma unroll
-        for (int u = 0; u < 16; ++u) m[u] = 0.f;
+        for (int u = 0; u < 8; ++u) m[u] = 0.f;
       } else {
-        uint32_t r[16];
-        tc::tmem_ld16(tS + (static_cast<uint32_t>(32 * q) << 16) + jb, r);
-        tc::tmem_ld_wait_regs(r);
+        uint32_t r[8];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                       "=r"(r[6]), "=r"(r[7])
+                     : "r"(tS + (static_cast<uint32_t>(32 * q) << 16) + jb));
+        asm volatile("tcgen05.wait::ld.sync.aligned;"
+                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                       "+r"(r[6]), "+r"(r[7])
+                     :
+                     : "memory");
         const float csi = cs_s[i];
         const int sgi = sg_s[i];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int j = jb + u;
           const bool valid = j + strict <= i && j < n && sg_s[j] == sgi;
           m[u] = valid ? __uint_as_float(r[u]) * ex2((csi - cs_s[j]) * kLog2e) * dt_s[j] : 0.f;
         }
       }
-#pragma unroll
-      for (int u = 0; u < 16; u += 4)
-        put4(tA, kQ, i, 16 * half + u, make_float4(m[u], m[u + 1], m[u + 2], m[u + 3]));
+      put4(a, kQ, i, 8 * half, make_float4(m[0], m[1], m[2], m[3]));
+      put4(a, kQ, i, 8 * half + 4, make_float4(m[4], m[5], m[6], m[7]));
 #pragma unroll
       for (int u = 0; u < PQ; ++u) {
-        const int r = 4 * (warp + 8 * u);
-        put1(tB, P, r, lane, rb[u].x);
-        put1(tB, P, r + 1, lane, rb[u].y);
-        put1(tB, P, r + 2, lane, rb[u].z);
-        put1(tB, P, r + 3, lane, rb[u].w);
+        const int r = 4 * (2 * warp + qh + 16 * u);
+        put1(bt, P, r, jl, rb[u].x);
+        put1(bt, P, r + 1, jl, rb[u].y);
+        put1(bt, P, r + 2, jl, rb[u].z);
+        put1(bt, P, r + 3, jl, rb[u].w);
       }
     }
   };
-
-  auto step = [&](int s, float4(&ra)[4], float4(&rb)[4]) -> bool {
-    store(s, ra, rb);
-    staged();
-    if (tid == 0) {
-      if (s < n1)
-        mma_slice(tS, tA, tB, kQ, idesc_tf32(kQ, kQ), s > 0);
-      else
-        mma_slice(tY, tA, tB, P, idesc_tf32(kQ, P), s > n1);
-      tc::mma_commit(&bar);
-    }
-    if (s + 2 < nS) load(s + 2, ra, rb);
-    const bool ok = wait_phase(&bar, s & 1);
-    if (!ok) ok_all = 0;
-    tc::fence_after_sync();
-    return __syncthreads_and(ok) != 0;
+  auto issue = [&](int s) {
+    if (s < n1)
+      mma_slice(tS, tA(s & 1), tB(s & 1), kQ, idesc_tf32(kQ, kQ), s > 0);
+    else
+      mma_slice(tY, tA(s & 1), tB(s & 1), P, idesc_tf32(kQ, P), s > n1);
   };
 
-  load(0, ra0, rb0);
-  if (nS > 1) load(1, ra1, rb1);
-  for (int s = 0; s < nS; s += 2) {
-    if (!step(s, ra0, rb0)) break;
-    if (s + 1 < nS && !step(s + 1, ra1, rb1)) break;
+  load_into(0, ra0, rb0);
+  if (nS > 1) load_into(1, ra1, rb1);
+  bool run = true;
+  for (int s = 0; run && s < nS; s += 2) {
+    run = pipeline_step(s, nS, bars, tid, ok_all, [&](int t) { store_from(t, ra0, rb0); },
+                        [&](int t) { load_into(t, ra0, rb0); }, issue);
+    if (run && s + 1 < nS)
+      run = pipeline_step(s + 1, nS, bars, tid, ok_all, [&](int t) { store_from(t, ra1, rb1); },
+                          [&](int t) { load_into(t, ra1, rb1); }, issue);
   }
   // epilogue: the output tile goes from TMEM through shared memory (rows of
   // P + 4 floats, over the tiles, which the completed MMAs no longer read),
   // then + D x and * silu(z) with consecutive threads on consecutive
-  // elements of a row, rows i < n
-  if (ok_all) {
+  // elements of a row, rows i < n.  Each thread's elements are taken in
+  // batches of 8 float4, every x / z load of a batch issued before any is
+  // used; the first batch loads while the last MMAs finish.
+  constexpr int kEl = kQ * (P / 4) / 256;   // float4 per thread: 8 or 16
+  constexpr int kBatch = kXZ ? 8 : 1;
+  float4 xv[kBatch], zv[kBatch];
+  auto load_batch = [&](int bt) {
+    if (!kXZ) return;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = tid + 256 * (bt * kBatch + u);
+      const int row = e / (P / 4), p = 4 * (e % (P / 4));
+      const bool ok_row = row < n;
+      xv[u] = (D && ok_row) ? ld4(x + toff(d.sx, b, t0 + row) + (int64_t)(h / d.xrep) * P + p)
+                            : zero4;
+      zv[u] = (z && ok_row) ? ld4(z + toff(d.sz, b, t0 + row) + (int64_t)h * P + p) : zero4;
+    }
+  };
+  if (run) load_batch(0);
+  if (run) run = pipeline_drain(nS, bars, ok_all);
+  if (run) {
     constexpr int YS = P + 4;
-    float* ys = reinterpret_cast<float*>(tA);   // 128 x YS floats
+    float* ys = reinterpret_cast<float*>(base);   // 128 x YS floats
 #pragma unroll
     for (int c0 = 0; c0 < P / 2; c0 += 32) {
       const int col0 = half * (P / 2) + c0;
@@ -470,25 +531,30 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
     }
     __syncthreads();
     const float Dh = D ? D[h] : 0.f;
-    for (int e = tid; e < n * (P / 4); e += 256) {
-      const int row = e / (P / 4), p = 4 * (e % (P / 4));
-      float4 y = *reinterpret_cast<const float4*>(ys + row * YS + p);
-      if (D) {
-        const float4 xv = ld4(x + toff(d.sx, b, t0 + row) + (int64_t)(h / d.xrep) * P + p);
-        y.x = fmaf(Dh, xv.x, y.x);
-        y.y = fmaf(Dh, xv.y, y.y);
-        y.z = fmaf(Dh, xv.z, y.z);
-        y.w = fmaf(Dh, xv.w, y.w);
+#pragma unroll
+    for (int bt = 0; bt < kEl / kBatch; ++bt) {
+      if (bt > 0) load_batch(bt);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = tid + 256 * (bt * kBatch + u);
+        const int row = e / (P / 4), p = 4 * (e % (P / 4));
+        if (row >= n) continue;
+        float4 y = *reinterpret_cast<const float4*>(ys + row * YS + p);
+        if (kXZ && D) {
+          y.x = fmaf(Dh, xv[u].x, y.x);
+          y.y = fmaf(Dh, xv[u].y, y.y);
+          y.z = fmaf(Dh, xv[u].z, y.z);
+          y.w = fmaf(Dh, xv[u].w, y.w);
+        }
+        if (kXZ && z) {
+          y.x *= zv[u].x / (1.f + __expf(-zv[u].x));
+          y.y *= zv[u].y / (1.f + __expf(-zv[u].y));
+          y.z *= zv[u].z / (1.f + __expf(-zv[u].z));
+          y.w *= zv[u].w / (1.f + __expf(-zv[u].w));
+        }
+        *reinterpret_cast<float4*>(out + (((int64_t)b * d.seqlen + t0 + row) * d.nheads + h) * P +
+                                   p) = y;
       }
-      if (z) {
-        const float4 zv = ld4(z + toff(d.sz, b, t0 + row) + (int64_t)h * P + p);
-        y.x *= zv.x / (1.f + __expf(-zv.x));
-        y.y *= zv.y / (1.f + __expf(-zv.y));
-        y.z *= zv.z / (1.f + __expf(-zv.z));
-        y.w *= zv.w / (1.f + __expf(-zv.w));
-      }
-      *reinterpret_cast<float4*>(out + (((int64_t)b * d.seqlen + t0 + row) * d.nheads + h) * P +
-                                 p) = y;
     }
   }
   tc::fence_before_sync();
@@ -496,7 +562,7 @@ __global__ void __launch_bounds__(256) chunk_scan_tc32_kernel(
   if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
-constexpr size_t kSmem = 1024 + 2 * kQ * 256;   // two split tiles of up to 128 rows
+constexpr size_t kSmem = 1024 + 2 * kBuf;   // two buffers of split tiles
 // chunk_scan holds 256 TMEM columns: its shared-memory request keeps it at
 // two CTAs per SM, so that no third CTA waits inside tcgen05.alloc
 constexpr size_t kSmemScan = 80 * 1024;
@@ -563,16 +629,18 @@ cudaError_t launch_chunk_scan_tc32(const float* x, const float* B, const float* 
                                    const Dims& d, float* out, cudaStream_t st, int strict) {
   using namespace tc32;
   dim3 grid((unsigned)(d.batch * d.nchunks), (unsigned)d.nheads);
-#define SSD_TC32_SCAN(P)                                                                        \
-  if (d.headdim == P) {                                                                         \
-    static cudaError_t prep = prepare(chunk_scan_tc32_kernel<P>, kSmemScan);                         \
+#define SSD_TC32_SCAN(P, XZ)                                                                    \
+  if (d.headdim == P && (D != nullptr || z != nullptr) == XZ) {                                 \
+    static cudaError_t prep = prepare(chunk_scan_tc32_kernel<P, XZ>, kSmemScan);                \
     if (prep != cudaSuccess) return prep;                                                       \
-    chunk_scan_tc32_kernel<P><<<grid, 256, kSmemScan, st>>>(x, B, C, dtp, cs, seg, prev, D, z, d,    \
-                                                        out, strict);                           \
+    chunk_scan_tc32_kernel<P, XZ><<<grid, 256, kSmemScan, st>>>(x, B, C, dtp, cs, seg, prev, D, \
+                                                                z, d, out, strict);             \
     return cudaGetLastError();                                                                  \
   }
-  SSD_TC32_SCAN(64)
-  SSD_TC32_SCAN(128)
+  SSD_TC32_SCAN(64, true)
+  SSD_TC32_SCAN(64, false)
+  SSD_TC32_SCAN(128, true)
+  SSD_TC32_SCAN(128, false)
 #undef SSD_TC32_SCAN
   return cudaErrorInvalidValue;
 }
