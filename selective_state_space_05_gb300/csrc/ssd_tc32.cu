@@ -30,7 +30,7 @@ namespace tc32 {
 __device__ int g_status32;
 
 constexpr int kQ = 128;                       // tokens per chunk = MMA rows
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s (the default wait limit)
 constexpr int kErrWait = 8;                   // status bit of a timed-out wait
 
 __device__ __forceinline__ uint64_t gtimer() {
@@ -39,11 +39,11 @@ __device__ __forceinline__ uint64_t gtimer() {
   return t;
 }
 
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint64_t wait_ns) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = gtimer();
   while (!tc::mbar_try_wait(bar, parity)) {
-    if (gtimer() - t0 > kWaitNs) {
+    if (gtimer() - t0 > wait_ns) {
       atomicOr(&g_status32, kErrWait);
       return false;
     }
@@ -152,12 +152,19 @@ constexpr int kBuf = 2 * kQ * 64 * 2;   // bytes per buffer
 // slice s + 2, then, once every thread has stored, one thread issues the
 // slice's MMAs and commits them to the buffer's mbarrier.  Returns false if a
 // bounded wait gave up (uniform over the CTA).
+// (`Limits`: the wait limit, and the test-only option under which the first
+// CTA leaves its first slice uncommitted, so that a wait runs out.)
+struct Limits {
+  uint64_t wait_ns;
+  int stall;
+};
+
 template <typename Store, typename Load, typename Issue>
 __device__ __forceinline__ bool pipeline_step(int s, int nS, uint64_t* bars, int tid,
-                                             int& ok_all, Store&& store, Load&& load,
-                                             Issue&& issue) {
+                                             int& ok_all, const Limits& lim, Store&& store,
+                                             Load&& load, Issue&& issue) {
   bool ok = true;
-  if (s >= 2) ok = wait_phase(&bars[s & 1], ((s - 2) >> 1) & 1);
+  if (s >= 2) ok = wait_phase(&bars[s & 1], ((s - 2) >> 1) & 1, lim.wait_ns);
   tc::fence_after_sync();
   if (ok) store(s);
   if (s + 2 < nS) load(s + 2);
@@ -168,16 +175,17 @@ __device__ __forceinline__ bool pipeline_step(int s, int nS, uint64_t* bars, int
   tc::fence_after_sync();
   if (tid == 0) {
     issue(s);
-    tc::mma_commit(&bars[s & 1]);
+    if (!(lim.stall && s == 0 && blockIdx.x == 0 && blockIdx.y == 0)) tc::mma_commit(&bars[s & 1]);
   }
   return true;
 }
 
 // Waits for the last slice's MMAs (so every earlier one) before the
 // accumulators are read or the TMEM is freed.
-__device__ __forceinline__ bool pipeline_drain(int nS, uint64_t* bars, int& ok_all) {
+__device__ __forceinline__ bool pipeline_drain(int nS, uint64_t* bars, int& ok_all,
+                                               const Limits& lim) {
   bool ok = true;
-  if (nS > 0) ok = wait_phase(&bars[(nS - 1) & 1], ((nS - 1) >> 1) & 1);
+  if (nS > 0) ok = wait_phase(&bars[(nS - 1) & 1], ((nS - 1) >> 1) & 1, lim.wait_ns);
   tc::fence_after_sync();
   if (!ok) ok_all = 0;
   return __syncthreads_and(ok) != 0;
@@ -194,7 +202,7 @@ template <int P, int N>
 __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
     const float* __restrict__ x, const float* __restrict__ Bm, const float* __restrict__ dtp,
     const float* __restrict__ cs, const int32_t* __restrict__ seg, Dims d,
-    float* __restrict__ states) {
+    float* __restrict__ states, Limits lim) {
   constexpr bool kT = (N == 128);
   constexpr int NR = kT ? P : N;   // MMA N: the other dimension
   constexpr int XQ = P / 64, BQ = N / 64;   // row quads per thread and slice (16 per warp)
@@ -281,13 +289,13 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
   if (nS > 1) load_into(1, rx1, rb1);
   bool run = true;
   for (int s = 0; run && s < nS; s += 2) {
-    run = pipeline_step(s, nS, bars, tid, ok_all, [&](int t) { store_from(t, rx0, rb0); },
+    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, rx0, rb0); },
                         [&](int t) { load_into(t, rx0, rb0); }, issue);
     if (run && s + 1 < nS)
-      run = pipeline_step(s + 1, nS, bars, tid, ok_all, [&](int t) { store_from(t, rx1, rb1); },
+      run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, rx1, rb1); },
                           [&](int t) { load_into(t, rx1, rb1); }, issue);
   }
-  if (run) run = pipeline_drain(nS, bars, ok_all);
+  if (run) run = pipeline_drain(nS, bars, ok_all, lim);
   if (run) {
     // each warp: TMEM lane quarter warp % 4, half of the NR columns
     const int q = warp & 3, half = warp >> 2;
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     const float* __restrict__ dtp, const float* __restrict__ cs,
     const int32_t* __restrict__ seg, const float* __restrict__ prev,
     const float* __restrict__ D, const float* __restrict__ z, Dims d, float* __restrict__ out,
-    int strict) {
+    int strict, Limits lim) {
   constexpr int PQ = P / 64;   // H row pairs / x quads per thread and slice
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = aligned_smem(smem_raw);
@@ -485,10 +493,10 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   if (nS > 1) load_into(1, ra1, rb1);
   bool run = true;
   for (int s = 0; run && s < nS; s += 2) {
-    run = pipeline_step(s, nS, bars, tid, ok_all, [&](int t) { store_from(t, ra0, rb0); },
+    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra0, rb0); },
                         [&](int t) { load_into(t, ra0, rb0); }, issue);
     if (run && s + 1 < nS)
-      run = pipeline_step(s + 1, nS, bars, tid, ok_all, [&](int t) { store_from(t, ra1, rb1); },
+      run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra1, rb1); },
                           [&](int t) { load_into(t, ra1, rb1); }, issue);
   }
   // epilogue: the output tile goes from TMEM through shared memory (rows of
@@ -513,7 +521,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     }
   };
   if (run) load_batch(0);
-  if (run) run = pipeline_drain(nS, bars, ok_all);
+  if (run) run = pipeline_drain(nS, bars, ok_all, lim);
   if (run) {
     constexpr int YS = P + 4;
     float* ys = reinterpret_cast<float*>(base);   // 128 x YS floats
@@ -576,6 +584,18 @@ bool disabled() {
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Wait limit (SSD_TC32_WAIT_NS) and the test-only stall (SSD_TC32_TEST_STALL=1),
+// read at every launch as the fused kernel's options are.
+Limits limits() {
+  Limits l{kWaitNs, 0};
+  if (const char* e = getenv("SSD_TC32_WAIT_NS")) {
+    const long long v = atoll(e);
+    if (v > 0) l.wait_ns = (uint64_t)v;
+  }
+  if (const char* e = getenv("SSD_TC32_TEST_STALL")) l.stall = atoi(e) == 1;
+  return l;
+}
 bool stride_ok(const TokStride& s) { return s.b % 4 == 0 && s.t % 4 == 0; }
 
 template <typename K>
@@ -612,7 +632,8 @@ cudaError_t launch_chunk_state_tc32(const float* x, const float* B, const float*
   if (d.headdim == P && d.dstate == N) {                                                        \
     static cudaError_t prep = prepare(chunk_state_tc32_kernel<P, N>, kSmem);                          \
     if (prep != cudaSuccess) return prep;                                                       \
-    chunk_state_tc32_kernel<P, N><<<grid, 256, kSmem, st>>>(x, B, dtp, cs, seg, d, states);     \
+    chunk_state_tc32_kernel<P, N><<<grid, 256, kSmem, st>>>(x, B, dtp, cs, seg, d, states,      \
+                                                           limits());                           \
     return cudaGetLastError();                                                                  \
   }
   SSD_TC32_STATE(64, 128)
@@ -634,7 +655,7 @@ cudaError_t launch_chunk_scan_tc32(const float* x, const float* B, const float* 
     static cudaError_t prep = prepare(chunk_scan_tc32_kernel<P, XZ>, kSmemScan);                \
     if (prep != cudaSuccess) return prep;                                                       \
     chunk_scan_tc32_kernel<P, XZ><<<grid, 256, kSmemScan, st>>>(x, B, C, dtp, cs, seg, prev, D, \
-                                                                z, d, out, strict);             \
+                                                                z, d, out, strict, limits());   \
     return cudaGetLastError();                                                                  \
   }
   SSD_TC32_SCAN(64, true)

@@ -113,3 +113,33 @@ def test_forward_fp32_tc_status_clean():
     ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=128,
                      dt_bias=g["dt_bias"], D=g["D"], z=g["z"], check=True)
     ssd.scan_status()
+
+
+def test_tc32_timeout_is_reported(monkeypatch):
+    """A test-only launch option leaves the first slice of the first CTA
+    uncommitted, so that its buffer's mbarrier never completes: the bounded
+    wait (shortened to 0.2 s) gives up, the CTA ends without touching the
+    accumulators, and ssd_scan_status reports SSD_ERR_TIMEOUT.  The next
+    normal launch is correct again."""
+    import selective_state_space_05_gb300 as ssd
+    from selective_state_space_05_gb300._lib import SSD_ERR_TIMEOUT, SSDError
+    d = si.random_small(3400, batch=1, seqlen=256, nheads=2, headdim=64, dstate=128, ngroups=1,
+                        chunk_size=128, dtype="f32")
+    g = to_dev(d)
+    ssd.scan_status(reset=True)
+    monkeypatch.setenv("SSD_TC32_WAIT_NS", "200000000")
+    monkeypatch.setenv("SSD_TC32_TEST_STALL", "1")
+    ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=128,
+                     dt_bias=g["dt_bias"], D=g["D"], z=g["z"])
+    with pytest.raises(SSDError) as ei:
+        ssd.scan_status(reset=True)
+    assert ei.value.code == SSD_ERR_TIMEOUT
+    assert "8 fp32 tensor-core stage" in str(ei.value)
+    ssd.scan_status(reset=True)                      # cleared
+    monkeypatch.delenv("SSD_TC32_TEST_STALL")
+    monkeypatch.delenv("SSD_TC32_WAIT_NS")
+    y, f = run_gpu(d)
+    ssd.scan_status(reset=True)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["f32"], "out after the time-out")
+    assert_close(f, rf, TOL["f32"], "final after the time-out")
