@@ -83,10 +83,18 @@ struct Workspace {
   float* cs;
   int32_t* seg;
   float* states;
+  float* cb;   // C B^T per (batch, chunk, group) for the fp32 tensor-core stages, or nullptr
   size_t bytes;
 };
 
-Workspace carve(const ssd::Dims& d, void* base) {
+// Whether fp32 at these sizes takes the fp32 tensor-core chunk_scan, which
+// reads C B^T computed once per group (the workspace then holds it).
+bool fp32_shared_cb(const ssd::Dims& d) {
+  return d.chunk == 128 && (d.headdim == 64 || d.headdim == 128) && d.dstate % 32 == 0 &&
+         d.dstate <= 256;
+}
+
+Workspace carve(const ssd::Dims& d, void* base, bool with_cb = false) {
   const size_t nq = (size_t)d.batch * d.nheads * d.nchunks * d.chunk;
   const size_t sq = (size_t)d.batch * d.nchunks * d.chunk;
   const size_t st = (size_t)d.batch * d.nchunks * d.nheads * d.headdim * d.dstate;
@@ -103,6 +111,12 @@ Workspace carve(const ssd::Dims& d, void* base) {
   off = round_up(off + sq * sizeof(int32_t), 256);
   w.states = reinterpret_cast<float*>(p + off);
   off = round_up(off + st * sizeof(float), 256);
+  w.cb = nullptr;
+  if (with_cb) {
+    w.cb = reinterpret_cast<float*>(p + off);
+    off = round_up(off + (size_t)d.batch * d.nchunks * d.ngroups * d.chunk * d.chunk *
+                             sizeof(float), 256);
+  }
   w.bytes = off;
   return w;
 }
@@ -160,7 +174,8 @@ size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int h
   if (check_dtype(dtype) != SSD_OK) return 0;
   if (check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d) != SSD_OK)
     return 0;
-  return carve(fwd_dims(d, dtype), nullptr).bytes;
+  const ssd::Dims e = fwd_dims(d, dtype);
+  return carve(e, nullptr, dtype == SSD_DTYPE_F32 && fp32_shared_cb(e)).bytes;
 }
 
 int ssd_dt_cumsum(const void* dt, const float* dt_bias, int dt_softplus, float lo, float hi,
@@ -326,7 +341,8 @@ int scan_fwd_run(const ssd::Dims& d_in, const void* x, const void* dt, const flo
                  void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const ssd::Dims d = fwd_dims(d_in, dtype);
-  const size_t need = carve(d, nullptr).bytes;
+  const bool with_cb = dtype == SSD_DTYPE_F32 && fp32_shared_cb(d);
+  const size_t need = carve(d, nullptr, with_cb).bytes;
   void* base = workspace;
   bool owned = false;
   if (base == nullptr) {
@@ -336,7 +352,7 @@ int scan_fwd_run(const ssd::Dims& d_in, const void* x, const void* dt, const flo
   } else if (workspace_bytes < need) {
     return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   }
-  Workspace w = carve(d, base);
+  Workspace w = carve(d, base, with_cb);
   int32_t* seg = seq_idx ? w.seg : nullptr;
   const int clamp = do_clamp_of(dt_limit_lo, dt_limit_hi);
   cudaError_t e;
@@ -350,11 +366,18 @@ int scan_fwd_run(const ssd::Dims& d_in, const void* x, const void* dt, const flo
                                          w.states, st);
     if (e == cudaSuccess)
       e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, d, st);
+    const float* Bf = static_cast<const float*>(B);
+    const float* Cf = static_cast<const float*>(C);
+    const float* zf = static_cast<const float*>(z);
+    // C B^T once per (batch, chunk, group) where chunk_scan runs on tensor cores
+    const bool cb = w.cb != nullptr && ssd::cb_tc32_fits(Bf, Cf, d) &&
+                    ssd::chunk_scan_tc32_fits(xf, Bf, Cf, zf, d);
+    if (e == cudaSuccess && cb) e = ssd::launch_cb_tc32(Bf, Cf, d, w.cb, nullptr, st);
     if (e == cudaSuccess)
-      e = ssd::launch_chunk_scan<float>(xf, static_cast<const float*>(B),
-                                        static_cast<const float*>(C), w.dt, w.cs, seg, w.states,
-                                        D, static_cast<const float*>(z), d,
-                                        static_cast<float*>(out), st);
+      e = cb ? ssd::launch_chunk_scan_tc32(xf, Bf, Cf, w.dt, w.cs, seg, w.states, D, zf, d,
+                                           static_cast<float*>(out), st, 0, w.cb, 0)
+             : ssd::launch_chunk_scan<float>(xf, Bf, Cf, w.dt, w.cs, seg, w.states, D, zf, d,
+                                             static_cast<float*>(out), st);
   } else {
     using bf = __nv_bfloat16;
     const bf* xb = static_cast<const bf*>(x);

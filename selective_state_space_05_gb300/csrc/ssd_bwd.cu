@@ -332,7 +332,7 @@ int bwd_chunk(int chunk_size, int P, int N) {
 // Workspace pieces, 256-byte aligned.  Reversed arrays span Lp = nc Qb tokens.
 struct BwdLayout {
   size_t dtF, csF, segF, statesF, yo, dy, dyR, xR, CR, BR, aR, seqR, csR, dtRo, segR, ones,
-      states1, finR, goR, states2, oB, h0T, oC, q, xg, dyx, bnd, total;
+      states1, finR, goR, states2, oB, h0T, oC, q, xg, dyx, bnd, cb, cbT, total;
 };
 
 BwdLayout bwd_layout(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
@@ -376,6 +376,11 @@ BwdLayout bwd_layout(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
   l.xg = take(tok);
   l.dyx = take(tok);
   l.bnd = take((size_t)Bz * H * nc);
+  // C B^T per (batch, chunk, group) and its transpose, shared by the heads
+  // (used where the scans take the fp32 tensor-core stages, 128-token chunks)
+  const size_t cbn = Q == 128 ? (size_t)Bz * nc * G * Q * Q : 0;
+  l.cb = take(cbn);
+  l.cbT = take(cbn);
   l.total = o;
   return l;
 }
@@ -494,9 +499,19 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   if (e == cudaSuccess)
     e = ssd::launch_state_passing(F(lay.statesF), F(lay.csF), segF, initial_states, nullptr, d,
                                   st);
+  // C B^T once per (batch, chunk, group) for the two scans in the forward
+  // orientation (the g scan reads its transpose, reversed)
+  const bool shared_cb = Q == 128 && ssd::cb_tc32_fits(B, C, d) &&
+                         ssd::chunk_scan_tc32_fits(x, B, C, nullptr, d);
+  if (e == cudaSuccess && shared_cb)
+    e = ssd::launch_cb_tc32(B, C, d, F(lay.cb), F(lay.cbT), st);
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_scan<float>(x, B, C, F(lay.dtF), F(lay.csF), segF, F(lay.statesF),
-                                      nullptr, nullptr, d, F(lay.yo), st, 1);
+    e = shared_cb ? ssd::launch_chunk_scan_tc32(x, B, C, F(lay.dtF), F(lay.csF), segF,
+                                                F(lay.statesF), nullptr, nullptr, d, F(lay.yo),
+                                                st, 1, F(lay.cb), 0)
+                  : ssd::launch_chunk_scan<float>(x, B, C, F(lay.dtF), F(lay.csF), segF,
+                                                  F(lay.statesF), nullptr, nullptr, d, F(lay.yo),
+                                                  st, 1);
   // gate, reversed copies, the reversed decays
   if (e == cudaSuccess) {
     reversed_prep_kernel<<<blocks_for(Bz * Lp * H * P / 4, 256), 256, 0, st>>>(
@@ -526,9 +541,13 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
     e = ssd::launch_state_passing(F(lay.states1), F(lay.csR), segR, nullptr, F(lay.finR), dR,
                                   st);
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_scan<float>(F(lay.dyR), F(lay.CR), F(lay.BR), F(lay.ones), F(lay.csR),
-                                      segR, F(lay.states1), nullptr, nullptr, dR, F(lay.goR), st,
-                                      1);
+    e = shared_cb && ssd::chunk_scan_tc32_fits(F(lay.dyR), F(lay.CR), F(lay.BR), nullptr, dR)
+            ? ssd::launch_chunk_scan_tc32(F(lay.dyR), F(lay.CR), F(lay.BR), F(lay.ones),
+                                          F(lay.csR), segR, F(lay.states1), nullptr, nullptr, dR,
+                                          F(lay.goR), st, 1, F(lay.cbT), 1)
+            : ssd::launch_chunk_scan<float>(F(lay.dyR), F(lay.CR), F(lay.BR), F(lay.ones),
+                                            F(lay.csR), segR, F(lay.states1), nullptr, nullptr,
+                                            dR, F(lay.goR), st, 1);
   if (e == cudaSuccess) {
     boundary_kernel<<<dim3((unsigned)nc, (unsigned)H, (unsigned)Bz), 256, 0, st>>>(
         F(lay.statesF), F(lay.states1), segF, F(lay.dtF), A, H, P * N, nc, Q, F(lay.bnd));

@@ -123,10 +123,21 @@ bool chunk_scan_tc32_fits(const float* x, const float* B, const float* C, const 
 cudaError_t launch_chunk_state_tc32(const float* x, const float* B, const float* dtp,
                                     const float* cs, const int32_t* seg, const Dims& d,
                                     float* states, cudaStream_t st);
+// Sg: C B^T of every (batch x chunk, group) computed beforehand by
+// launch_cb_tc32 (nullptr: the kernel computes it itself); srev: read it for
+// a time-reversed scan (chunk nc - 1 - c, indices 127 - i, 127 - j; pass the
+// transposed copy there).
 cudaError_t launch_chunk_scan_tc32(const float* x, const float* B, const float* C,
                                    const float* dtp, const float* cs, const int32_t* seg,
                                    const float* prev, const float* D, const float* z,
-                                   const Dims& d, float* out, cudaStream_t st, int strict);
+                                   const Dims& d, float* out, cudaStream_t st, int strict,
+                                   const float* Sg = nullptr, int srev = 0);
+// C B^T per (batch x chunk, group) into S [B][nc][G][128][128] fp32 (and its
+// transpose into ST unless nullptr), for 128-token chunks, dstate a multiple
+// of 16 up to 256.
+bool cb_tc32_fits(const float* B, const float* C, const Dims& d);
+cudaError_t launch_cb_tc32(const float* B, const float* C, const Dims& d, float* S, float* ST,
+                           cudaStream_t st);
 // Status bits of their bounded waits (8: a wait gave up), as fused_status.
 int tc32_status(int reset, cudaStream_t st, int* bits);
 

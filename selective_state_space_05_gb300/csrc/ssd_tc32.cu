@@ -10,14 +10,16 @@
 //   chunk_state  S_c[p,n] = sum_j w_j x_j[p] B_j[n],  w_j = exp(cs_last - cs_j) dt_j
 //   chunk_scan   y_i = sum_{j<=i} exp(cs_i - cs_j) (C_i . B_j) dt_j x_j
 //                      + keep_i exp(cs_i) C_i . H_{c-1} + D x_i,  then * silu(z_i)
-// Operands are split and written K-major into 128-byte-swizzled shared
+// Operands are split and written K-major into 64-byte-swizzled shared
 // tiles by the CUDA cores (transposed where the token index is the K
-// dimension), one 32-element K slice at a time; one thread issues the MMAs.
-// The chunk_scan CTA runs three K loops: C B^T into TMEM (K = dstate), the
+// dimension), one 16-element K slice at a time into two alternating
+// buffers, so that a slice is staged while the previous one's MMAs run; one
+// thread issues the MMAs.  chunk_scan runs C B^T into TMEM (K = dstate)
+// unless it is given C B^T computed once per group (cb_tc32_kernel), the
 // inter-chunk term (e^cs C) H^T into the output accumulator (K = dstate),
-// then the decay-masked matrix M = (C B^T) o L o dt, built from TMEM by the
-// CUDA cores, times x (K = tokens).  Every mbarrier wait is bounded by the
-// global timer and records a status bit instead of hanging.
+// then the decay-masked matrix M = (C B^T) o L o dt, built by the CUDA cores,
+// times x (K = tokens).  Every mbarrier wait is bounded by the global timer
+// and records a status bit instead of hanging.
 #include <stdio.h>
 #include <stdlib.h>
 
@@ -338,16 +340,22 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
 // [0, 128) hold C B^T (rows i, columns j), [128, 128 + P) the output.
 // Slices: N/16 of C B^T (K = dstate), N/16 of the inter-chunk term, then one
 // per 16 tokens of M x (K = tokens).  kXZ: D or z given (the epilogue reads
-// x and z); without them the epilogue only copies the tile out.
+// x and z); without them the epilogue only copies the tile out.  kS: C B^T
+// is given (Sg, computed once per group by cb_tc32_kernel): no C B^T slices,
+// the decay-matrix build reads it from memory, TMEM holds the output only.
+// Element (i, j) of the chunk's C B^T is Sg[cf][ri][rj], (cf, ri, rj) =
+// (c, i, j), or with srev (nc - 1 - c, 127 - i, 127 - j): the time-reversed
+// scans of the backward, whose chunks are the forward chunks reversed.
 // ---------------------------------------------------------------------------
-template <int P, bool kXZ>
+template <int P, bool kXZ, bool kS>
 __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     const float* __restrict__ x, const float* __restrict__ Bm, const float* __restrict__ Cm,
     const float* __restrict__ dtp, const float* __restrict__ cs,
     const int32_t* __restrict__ seg, const float* __restrict__ prev,
     const float* __restrict__ D, const float* __restrict__ z, Dims d, float* __restrict__ out,
-    int strict, Limits lim) {
+    int strict, Limits lim, const float* __restrict__ Sg, int srev) {
   constexpr int PQ = P / 64;   // H row pairs / x quads per thread and slice
+  constexpr int kBufK = kS ? kQ * 128 + P * 128 : kBuf;   // bytes per buffer
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = aligned_smem(smem_raw);
   __shared__ float cs_s[kQ], dt_s[kQ], sc_s[kQ];
@@ -378,14 +386,15 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     tc::mbar_fence_init();
     ok_all = 1;
   }
+  constexpr uint32_t kCols = kS ? 128 : 256;
   if (warp == 0) {
-    tc::tmem_alloc(&tmem_base, 256);
+    tc::tmem_alloc(&tmem_base, kCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = tmem_base, tS = tmem, tY = tmem + 128;
+  const uint32_t tmem = tmem_base, tS = tmem, tY = kS ? tmem : tmem + 128;
   const float* Hp = prev + (((int64_t)b * d.nchunks + c) * d.nheads + h) * (int64_t)P * N;
   const float* xh = x + (int64_t)(h / d.xrep) * P;
   const float* cg = Cm + (int64_t)g * N;
@@ -393,24 +402,32 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   // token-major operands: 4 threads per row, rows sr + 64 u, columns sk .. sk + 3
   const int sr = tid >> 2, sk = (tid & 3) * 4;
-  const int n1 = N / kK, n3 = (n + kK - 1) / kK, nS = 2 * n1 + n3;
+  // slices: [0, s1) C B^T, [s1, s2) inter-chunk term, [s2, nS) M x
+  const int n1 = N / kK, n3 = (n + kK - 1) / kK;
+  const int s1 = kS ? 0 : n1, s2 = s1 + n1, nS = s2 + n3;
   const int q = warp & 3, half = warp >> 2;
   const int i = 32 * q + lane;   // the row this thread builds M for and writes out
   const int jl = lane & 15, qh = lane >> 4;   // x^T: token in the slice, row-quad half
-  auto tA = [&](int u) { return base + u * kBuf; };
-  auto tB = [&](int u) { return base + u * kBuf + kQ * 128; };
+  auto tA = [&](int u) { return base + u * kBufK; };
+  auto tB = [&](int u) { return base + u * kBufK + kQ * 128; };
+  // the row of the given C B^T this thread reads (kS)
+  const float* srow = nullptr;
+  if (kS) {
+    const int cf = srev ? d.nchunks - 1 - c : c, ri = srev ? kQ - 1 - i : i;
+    srow = Sg + ((((int64_t)b * d.nchunks + cf) * d.ngroups + g) * kQ + ri) * kQ;
+  }
 
   // two register sets: slice s + 2 loads while slice s is stored / multiplied
   float4 ra0[2], rb0[2], ra1[2], rb1[2];
   auto load_into = [&](int s, float4(&ra)[2], float4(&rb)[2]) {
-    if (s < 2 * n1) {   // C (both), B (C B^T) or H (inter-chunk)
-      const int k0 = kK * (s < n1 ? s : s - n1);
+    if (s < s2) {   // C (both), B (C B^T) or H (inter-chunk)
+      const int k0 = kK * (s < s1 ? s : s - s1);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int r = sr + 64 * u;
         ra[u] = r < n ? ld4(cg + toff(d.sC, b, t0 + r) + k0 + sk) : zero4;
       }
-      if (s < n1) {
+      if (s < s1) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int r = sr + 64 * u;
@@ -421,23 +438,37 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
         for (int u = 0; u < PQ; ++u) rb[u] = ld4(Hp + (int64_t)(sr + 64 * u) * N + k0 + sk);
       }
     } else {            // x of tokens j0 .. j0 + 15 (16 lanes on the tokens)
-      const int j = kK * (s - 2 * n1) + jl;
+      const int j0 = kK * (s - s2);
+      const int j = j0 + jl;
       const bool tv = j < n;
       const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0));
 #pragma unroll
       for (int u = 0; u < PQ; ++u) rb[u] = tv ? ld4(xh + tx + 4 * (2 * warp + qh + 16 * u)) : zero4;
+      if (kS) {         // and this row's 8 values of C B^T for the slice
+        const int jb = j0 + 8 * half;
+        if (32 * q + 31 < j0) {
+          ra[0] = ra[1] = zero4;
+        } else if (!srev) {
+          ra[0] = ld4(srow + jb);
+          ra[1] = ld4(srow + jb + 4);
+        } else {        // columns 127 - jb - 7 .. 127 - jb, in reverse order
+          const float4 lo = ld4(srow + (kQ - 8 - jb)), hi = ld4(srow + (kQ - 4 - jb));
+          ra[0] = make_float4(hi.w, hi.z, hi.y, hi.x);
+          ra[1] = make_float4(lo.w, lo.z, lo.y, lo.x);
+        }
+      }
     }
   };
   auto store_from = [&](int s, const float4(&ra)[2], const float4(&rb)[2]) {
     unsigned char* a = tA(s & 1);
     unsigned char* bt = tB(s & 1);
-    if (s < n1) {
+    if (s < s1) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         put4(a, kQ, sr + 64 * u, sk, ra[u]);
         put4(bt, kQ, sr + 64 * u, sk, rb[u]);
       }
-    } else if (s < 2 * n1) {
+    } else if (s < s2) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) put4(a, kQ, sr + 64 * u, sk, scale4(ra[u], sc_s[sr + 64 * u]));
 #pragma unroll
@@ -445,22 +476,29 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     } else {
       // M_ij = (C_i . B_j) e^(cs_i - cs_j) dt_j over j <= i (j < i if strict)
       // of one document: row i, columns j0 + 8 half .. + 7
-      const int j0 = kK * (s - 2 * n1), jb = j0 + 8 * half;
+      const int j0 = kK * (s - s2), jb = j0 + 8 * half;
       float m[8];
       if (32 * q + 31 < j0) {   // every row of this block precedes the slice
 #pragma unroll
         for (int u = 0; u < 8; ++u) m[u] = 0.f;
       } else {
         uint32_t r[8];
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                       "=r"(r[6]), "=r"(r[7])
-                     : "r"(tS + (static_cast<uint32_t>(32 * q) << 16) + jb));
-        asm volatile("tcgen05.wait::ld.sync.aligned;"
-                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                       "+r"(r[6]), "+r"(r[7])
-                     :
-                     : "memory");
+        if (kS) {
+          r[0] = __float_as_uint(ra[0].x), r[1] = __float_as_uint(ra[0].y);
+          r[2] = __float_as_uint(ra[0].z), r[3] = __float_as_uint(ra[0].w);
+          r[4] = __float_as_uint(ra[1].x), r[5] = __float_as_uint(ra[1].y);
+          r[6] = __float_as_uint(ra[1].z), r[7] = __float_as_uint(ra[1].w);
+        } else {
+          asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                         "=r"(r[6]), "=r"(r[7])
+                       : "r"(tS + (static_cast<uint32_t>(32 * q) << 16) + jb));
+          asm volatile("tcgen05.wait::ld.sync.aligned;"
+                       : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                         "+r"(r[6]), "+r"(r[7])
+                       :
+                       : "memory");
+        }
         const float csi = cs_s[i];
         const int sgi = sg_s[i];
 #pragma unroll
@@ -483,10 +521,10 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     }
   };
   auto issue = [&](int s) {
-    if (s < n1)
+    if (s < s1)
       mma_slice(tS, tA(s & 1), tB(s & 1), kQ, idesc_tf32(kQ, kQ), s > 0);
     else
-      mma_slice(tY, tA(s & 1), tB(s & 1), P, idesc_tf32(kQ, P), s > n1);
+      mma_slice(tY, tA(s & 1), tB(s & 1), P, idesc_tf32(kQ, P), s > s1);
   };
 
   load_into(0, ra0, rb0);
@@ -567,10 +605,117 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, kCols);
+}
+
+
+// ---------------------------------------------------------------------------
+// C B^T of every (batch x chunk, group), once for all the heads of the
+// group: S[b][c][g][i][j] = C_i . B_j over dstate (rows and columns past the
+// sequence's end zero), and with ST its transpose.  One CTA per (batch x
+// chunk, group), 256 threads, the slice pipeline above (K = dstate).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) cb_tc32_kernel(const float* __restrict__ Bm,
+                                                      const float* __restrict__ Cm, Dims d,
+                                                      float* __restrict__ S,
+                                                      float* __restrict__ ST, Limits lim) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = aligned_smem(smem_raw);
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int ok_all;
+  const int N = d.dstate;
+  const int bc = blockIdx.x, g = blockIdx.y;
+  const int b = bc / d.nchunks, c = bc % d.nchunks;
+  const int64_t t0 = (int64_t)c * kQ;
+  const int n = (int)min((int64_t)kQ, d.seqlen - t0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::mbar_fence_init();
+    ok_all = 1;
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 128);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const float* cg = Cm + (int64_t)g * N;
+  const float* bg = Bm + (int64_t)g * N;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int sr = tid >> 2, sk = (tid & 3) * 4;
+  auto tA = [&](int u) { return base + u * kBuf; };
+  auto tB = [&](int u) { return base + u * kBuf + kQ * 128; };
+  const int nS = N / kK;
+  float4 ra0[2], rb0[2], ra1[2], rb1[2];
+  auto load_into = [&](int s, float4(&ra)[2], float4(&rb)[2]) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int r = sr + 64 * u;
+      ra[u] = r < n ? ld4(cg + toff(d.sC, b, t0 + r) + kK * s + sk) : zero4;
+      rb[u] = r < n ? ld4(bg + toff(d.sB, b, t0 + r) + kK * s + sk) : zero4;
+    }
+  };
+  auto store_from = [&](int s, const float4(&ra)[2], const float4(&rb)[2]) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      put4(tA(s & 1), kQ, sr + 64 * u, sk, ra[u]);
+      put4(tB(s & 1), kQ, sr + 64 * u, sk, rb[u]);
+    }
+  };
+  auto issue = [&](int s) {
+    mma_slice(tmem, tA(s & 1), tB(s & 1), kQ, idesc_tf32(kQ, kQ), s > 0);
+  };
+  load_into(0, ra0, rb0);
+  if (nS > 1) load_into(1, ra1, rb1);
+  bool run = true;
+  for (int s = 0; run && s < nS; s += 2) {
+    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra0, rb0); },
+                        [&](int t) { load_into(t, ra0, rb0); }, issue);
+    if (run && s + 1 < nS)
+      run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
+                          [&](int t) { store_from(t, ra1, rb1); },
+                          [&](int t) { load_into(t, ra1, rb1); }, issue);
+  }
+  if (run) run = pipeline_drain(nS, bars, ok_all, lim);
+  if (run) {
+    const int q = warp & 3, half = warp >> 2;
+    const int i = 32 * q + lane;
+    const int64_t off = (((int64_t)b * d.nchunks + c) * d.ngroups + g) * kQ * kQ;
+    float* srow = S + off + (int64_t)i * kQ;
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      const int col0 = 64 * half + c0;
+      uint32_t r[32];
+      tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col0, r);
+      tc::tmem_ld_wait_regs(r);
+#pragma unroll
+      for (int u = 0; u < 32; u += 4)
+        *reinterpret_cast<float4*>(srow + col0 + u) =
+            make_float4(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
+                        __uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]));
+      if (ST) {   // lanes on consecutive i: each store one 128-byte piece of a row of ST
+#pragma unroll
+        for (int u = 0; u < 32; ++u) ST[off + (int64_t)(col0 + u) * kQ + i] = __uint_as_float(r[u]);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
 constexpr size_t kSmem = 1024 + 2 * kBuf;   // two buffers of split tiles
+// chunk_scan with C B^T given: two buffers of (128 + P) rows, or the
+// epilogue's 128 x (P + 4) floats if that is more
+constexpr size_t smem_scan_given(int P) {
+  return 1024 + ((2 * (kQ + P) * 128 > kQ * (P + 4) * 4) ? 2 * (kQ + P) * 128
+                                                           : kQ * (P + 4) * 4);
+}
 // chunk_scan holds 256 TMEM columns: its shared-memory request keeps it at
 // two CTAs per SM, so that no third CTA waits inside tcgen05.alloc
 constexpr size_t kSmemScan = 80 * 1024;
@@ -644,24 +789,47 @@ cudaError_t launch_chunk_state_tc32(const float* x, const float* B, const float*
   return e;
 }
 
+bool cb_tc32_fits(const float* B, const float* C, const Dims& d) {
+  using namespace tc32;
+  const int N = d.dstate;
+  return !disabled() && d.chunk == kQ && N % 16 == 0 && N >= 16 && N <= 256 && aligned16(B) &&
+         aligned16(C) && stride_ok(d.sB) && stride_ok(d.sC);
+}
+
+cudaError_t launch_cb_tc32(const float* B, const float* C, const Dims& d, float* S, float* ST,
+                           cudaStream_t st) {
+  using namespace tc32;
+  static cudaError_t prep = prepare(cb_tc32_kernel, kSmem);
+  if (prep != cudaSuccess) return prep;
+  dim3 grid((unsigned)(d.batch * d.nchunks), (unsigned)d.ngroups);
+  cb_tc32_kernel<<<grid, 256, kSmem, st>>>(B, C, d, S, ST, limits());
+  return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_scan_tc32(const float* x, const float* B, const float* C,
                                    const float* dtp, const float* cs, const int32_t* seg,
                                    const float* prev, const float* D, const float* z,
-                                   const Dims& d, float* out, cudaStream_t st, int strict) {
+                                   const Dims& d, float* out, cudaStream_t st, int strict,
+                                   const float* Sg, int srev) {
   using namespace tc32;
   dim3 grid((unsigned)(d.batch * d.nchunks), (unsigned)d.nheads);
-#define SSD_TC32_SCAN(P, XZ)                                                                    \
-  if (d.headdim == P && (D != nullptr || z != nullptr) == XZ) {                                 \
-    static cudaError_t prep = prepare(chunk_scan_tc32_kernel<P, XZ>, kSmemScan);                \
+#define SSD_TC32_SCAN(P, XZ, S_)                                                                \
+  if (d.headdim == P && (D != nullptr || z != nullptr) == XZ && (Sg != nullptr) == S_) {        \
+    constexpr size_t smem = S_ ? smem_scan_given(P) : kSmemScan;                                \
+    static cudaError_t prep = prepare(chunk_scan_tc32_kernel<P, XZ, S_>, smem);                 \
     if (prep != cudaSuccess) return prep;                                                       \
-    chunk_scan_tc32_kernel<P, XZ><<<grid, 256, kSmemScan, st>>>(x, B, C, dtp, cs, seg, prev, D, \
-                                                                z, d, out, strict, limits());   \
+    chunk_scan_tc32_kernel<P, XZ, S_><<<grid, 256, smem, st>>>(                                 \
+        x, B, C, dtp, cs, seg, prev, D, z, d, out, strict, limits(), Sg, srev);                 \
     return cudaGetLastError();                                                                  \
   }
-  SSD_TC32_SCAN(64, true)
-  SSD_TC32_SCAN(64, false)
-  SSD_TC32_SCAN(128, true)
-  SSD_TC32_SCAN(128, false)
+  SSD_TC32_SCAN(64, true, false)
+  SSD_TC32_SCAN(64, false, false)
+  SSD_TC32_SCAN(128, true, false)
+  SSD_TC32_SCAN(128, false, false)
+  SSD_TC32_SCAN(64, true, true)
+  SSD_TC32_SCAN(64, false, true)
+  SSD_TC32_SCAN(128, true, true)
+  SSD_TC32_SCAN(128, false, true)
 #undef SSD_TC32_SCAN
   return cudaErrorInvalidValue;
 }
