@@ -500,14 +500,18 @@ def backward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None):
     alg = f4 * (5 * Bz * L * H * P + 2 * Bz * L * H + 4 * Bz * L * G * N + 2 * Bz * H * P * N
                 + 6 * H)
     # MMA work per (batch row, 128-token chunk, head): two scans in each
-    # orientation (headdim x dstate and dstate x headdim), each C B^T, the
-    # inter-chunk term, M x and the chunk state, 3 tf32 products per fp32 one
+    # orientation (headdim x dstate and dstate x headdim), each the
+    # inter-chunk term, M x and the chunk state, and C B^T -- once per group
+    # for the headdim x dstate scans (one product serves both), per head for
+    # the swapped ones; 3 tf32 products per fp32 one
     Q = 128
-    tiles = Bz * ((L + Q - 1) // Q) * H
+    nc = (L + Q - 1) // Q
+    tiles = Bz * nc * H
 
     def scan_macs(p, n_):
-        return Q * Q * n_ + Q * p * n_ + Q * p * Q + p * n_ * Q
-    macs = 2 * (scan_macs(P, N) + scan_macs(N, P)) * tiles
+        return Q * p * n_ + Q * p * Q + p * n_ * Q
+    macs = (2 * scan_macs(P, N) + 2 * scan_macs(N, P) + 2 * Q * Q * P) * tiles \
+        + Bz * nc * G * Q * Q * N
     fl_alg = 2 * macs
     fl_exec = 3 * fl_alg
     peak_tf32 = peaks["bf16_tflops"] / 2
