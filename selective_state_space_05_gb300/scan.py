@@ -493,3 +493,47 @@ def ssd_scan_bwd(dout: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch
         _ptr(g["dz"]), _ptr(g["d_initial_states"]), _ptr(workspace), ws_bytes,
         _stream(stream)))
     return g
+
+
+# --- autograd ----------------------------------------------------------------
+
+class _SSDScan(torch.autograd.Function):
+    """ssd_scan_fwd forward, ssd_scan_bwd backward (fp32)."""
+
+    @staticmethod
+    def forward(ctx, x, dt, A, B, C, dt_bias, D, z, initial_states, seq_idx, chunk_size,
+                dt_softplus, dt_limit):
+        out = ssd_scan_fwd(x, dt, A, B, C, chunk_size=chunk_size, dt_bias=dt_bias,
+                           dt_softplus=dt_softplus, dt_limit=dt_limit, D=D, z=z,
+                           initial_states=initial_states, seq_idx=seq_idx)
+        ctx.save_for_backward(x, dt, A, B, C, dt_bias, D, z, initial_states, seq_idx)
+        ctx.opts = (chunk_size, dt_softplus, dt_limit)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        x, dt, A, B, C, dt_bias, D, z, initial_states, seq_idx = ctx.saved_tensors
+        chunk_size, dt_softplus, dt_limit = ctx.opts
+        # the backward takes dense tensors (views of a projection are copied)
+        x, dt, B, C = x.contiguous(), dt.contiguous(), B.contiguous(), C.contiguous()
+        z = None if z is None else z.contiguous()
+        g = ssd_scan_bwd(dout.contiguous(), x, dt, A, B, C, chunk_size=chunk_size,
+                         dt_bias=dt_bias, dt_softplus=dt_softplus, dt_limit=dt_limit, D=D, z=z,
+                         initial_states=initial_states, seq_idx=seq_idx)
+        return (g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"],
+                g["d_dt_bias"] if dt_bias is not None else None,
+                g["dD"] if D is not None else None, g["dz"], g["d_initial_states"],
+                None, None, None, None)
+
+
+def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+             C: torch.Tensor, *, chunk_size: int = 256, dt_bias: Optional[torch.Tensor] = None,
+             dt_softplus: bool = True, dt_limit: Tuple[float, float] = (0.0, math.inf),
+             D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+             initial_states: Optional[torch.Tensor] = None,
+             seq_idx: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The scan as a differentiable torch function (fp32, dense tensors):
+    the forward is ssd_scan_fwd, the backward ssd_scan_bwd, giving gradients
+    for x, dt (raw), A, B, C, dt_bias, D, z and initial_states.  Returns out."""
+    return _SSDScan.apply(x, dt, A, B, C, dt_bias, D, z, initial_states, seq_idx, chunk_size,
+                          dt_softplus, tuple(dt_limit))
