@@ -65,8 +65,8 @@ enum {
  *   1  the calls below up to ssd_scan_fwd_host
  *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status, ssd_scan_fwd_strided, the
  *      block calls ssd_causal_conv1d and ssd_group_rmsnorm,
- *      ssd_decode_step and the backward ssd_scan_bwd (with
- *      ssd_scan_bwd_workspace_bytes); every version-1 symbol is unchanged */
+ *      ssd_decode_step and the backward ssd_scan_bwd and ssd_scan_bwd_ex
+ *      (with their workspace queries); every version-1 symbol is unchanged */
 int ssd_abi_version(void);
 
 /* Message for the last error returned on the calling host thread ("" if
@@ -456,6 +456,30 @@ int ssd_scan_bwd(const float *x, const float *dt, const float *dt_bias,
                  float *d_dt_bias, float *dA, float *dB, float *dC, float *dD,
                  float *dz, float *d_initial_states, void *workspace,
                  size_t workspace_bytes, void *stream);
+
+/* The backward with its element-wise tensors in a given dtype.  dtype
+ * SSD_DTYPE_F32 is ssd_scan_bwd.  SSD_DTYPE_BF16: x, dt, B, C, z and dout are
+ * bf16 (the inputs and upstream gradient of a bf16 forward, e.g. a bf16
+ * training step), and so are the gradients dx, ddt, dB, dC and dz written;
+ * A, dt_bias, D, initial_states and their gradients stay float.  The bf16
+ * values are converted to fp32 in the workspace, the fp32 backward runs on
+ * them, and the fp32 gradients are rounded to bf16 at the end.  Workspace:
+ * ssd_scan_bwd_ex_workspace_bytes (0 for unsupported sizes or dtypes).
+ * Sizes, layouts, alignment and errors otherwise as for ssd_scan_bwd. */
+size_t ssd_scan_bwd_ex_workspace_bytes(int64_t batch, int64_t seqlen,
+                                       int nheads, int headdim, int dstate,
+                                       int ngroups, int chunk_size,
+                                       ssd_dtype_t dtype);
+int ssd_scan_bwd_ex(const void *x, const void *dt, const float *dt_bias,
+                    int dt_softplus, float dt_limit_lo, float dt_limit_hi,
+                    const float *A, const void *B, const void *C,
+                    const float *D, const void *z, const float *initial_states,
+                    const int32_t *seq_idx, const void *dout, int64_t batch,
+                    int64_t seqlen, int nheads, int headdim, int dstate,
+                    int ngroups, int chunk_size, ssd_dtype_t dtype, void *dx,
+                    void *ddt, float *d_dt_bias, float *dA, void *dB, void *dC,
+                    float *dD, void *dz, float *d_initial_states,
+                    void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

@@ -320,6 +320,34 @@ __global__ void dh0_kernel(const float* __restrict__ F, const float* __restrict_
   dh0[i] = __expf(dtF[chunk_index(bh / H, h, 0, H, nc, Q)] * A[h]) * F[i];
 }
 
+// bf16 <-> fp32 copies for the bf16 entry point: four elements per thread,
+// the last partial group one by one.
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, int64_t n,
+                                   float* __restrict__ out) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  if (i + 4 <= n) {
+    const __nv_bfloat162 a = reinterpret_cast<const __nv_bfloat162*>(in + i)[0];
+    const __nv_bfloat162 b = reinterpret_cast<const __nv_bfloat162*>(in + i)[1];
+    const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    *reinterpret_cast<float4*>(out + i) = make_float4(fa.x, fa.y, fb.x, fb.y);
+  } else {
+    for (int64_t k = i; k < n; ++k) out[k] = __bfloat162float(in[k]);
+  }
+}
+__global__ void f32_to_bf16_kernel(const float* __restrict__ in, int64_t n,
+                                   __nv_bfloat16* __restrict__ out) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  if (i + 4 <= n) {
+    const float4 v = *reinterpret_cast<const float4*>(in + i);
+    reinterpret_cast<__nv_bfloat162*>(out + i)[0] = __floats2bfloat162_rn(v.x, v.y);
+    reinterpret_cast<__nv_bfloat162*>(out + i)[1] = __floats2bfloat162_rn(v.z, v.w);
+  } else {
+    for (int64_t k = i; k < n; ++k) out[k] = __float2bfloat16_rn(in[k]);
+  }
+}
+
 // The backward's own chunk length: 128 where its scans (headdim x dstate
 // and the swapped dstate x headdim) take the fp32 tensor-core stages,
 // otherwise at most kBwdChunk (shorter in-chunk sums, see above).
@@ -602,6 +630,134 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   if (e != cudaSuccess) {
     char m[200];
     snprintf(m, sizeof(m), "ssd_scan_bwd launch: %s", cudaGetErrorString(e));
+    return bfail(SSD_ERR_CUDA, m);
+  }
+  return SSD_OK;
+}
+
+
+// The bf16 entry point's extra workspace (after the fp32 backward's): fp32
+// copies of x, dt, B, C, z, dout and the fp32 gradients before their bf16
+// copies.
+namespace {
+struct ExLayout {
+  size_t x, dt, B, C, z, dout, dx, ddt, dB, dC, dz, total;
+};
+ExLayout ex_layout(size_t base, int64_t Bz, int64_t L, int H, int P, int N, int G) {
+  const size_t xs = (size_t)Bz * L * H * P, ts = (size_t)Bz * L * H, bs = (size_t)Bz * L * G * N;
+  ExLayout e;
+  size_t o = (base + 255) / 256 * 256;
+  auto take = [&](size_t elems) {
+    const size_t at = o;
+    o = (o + elems * 4 + 255) / 256 * 256;
+    return at;
+  };
+  e.x = take(xs);
+  e.dt = take(ts);
+  e.B = take(bs);
+  e.C = take(bs);
+  e.z = take(xs);
+  e.dout = take(xs);
+  e.dx = take(xs);
+  e.ddt = take(ts);
+  e.dB = take(bs);
+  e.dC = take(bs);
+  e.dz = take(xs);
+  e.total = o;
+  return e;
+}
+}  // namespace
+
+size_t ssd_scan_bwd_ex_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int headdim,
+                                       int dstate, int ngroups, int chunk_size,
+                                       ssd_dtype_t dtype) {
+  const size_t base = ssd_scan_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                                   ngroups, chunk_size);
+  if (base == 0) return 0;
+  if (dtype == SSD_DTYPE_F32) return base;
+  if (dtype != SSD_DTYPE_BF16) return 0;
+  return ex_layout(base, batch, seqlen, nheads, headdim, dstate, ngroups).total;
+}
+
+int ssd_scan_bwd_ex(const void* x, const void* dt, const float* dt_bias, int dt_softplus,
+                    float dt_limit_lo, float dt_limit_hi, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const float* initial_states,
+                    const int32_t* seq_idx, const void* dout, int64_t batch, int64_t seqlen,
+                    int nheads, int headdim, int dstate, int ngroups, int chunk_size,
+                    ssd_dtype_t dtype, void* dx, void* ddt, float* d_dt_bias, float* dA,
+                    void* dB, void* dC, float* dD, void* dz, float* d_initial_states,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace ssd::bwd;
+  using bf = __nv_bfloat16;
+  if (dtype == SSD_DTYPE_F32)
+    return ssd_scan_bwd(static_cast<const float*>(x), static_cast<const float*>(dt), dt_bias,
+                        dt_softplus, dt_limit_lo, dt_limit_hi, A, static_cast<const float*>(B),
+                        static_cast<const float*>(C), D, static_cast<const float*>(z),
+                        initial_states, seq_idx, static_cast<const float*>(dout), batch, seqlen,
+                        nheads, headdim, dstate, ngroups, chunk_size, static_cast<float*>(dx),
+                        static_cast<float*>(ddt), d_dt_bias, dA, static_cast<float*>(dB),
+                        static_cast<float*>(dC), dD, static_cast<float*>(dz), d_initial_states,
+                        workspace, workspace_bytes, stream);
+  if (dtype != SSD_DTYPE_BF16) return bfail(SSD_ERR_ARG, "unknown dtype");
+  const size_t base = ssd_scan_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
+                                                   ngroups, chunk_size);
+  if (base == 0)
+    return bfail(SSD_ERR_UNSUPPORTED,
+                 "ssd_scan_bwd_ex: headdim and dstate in {16, 32, 64, 128}, chunk_size a power "
+                 "of two in [16, 256], ngroups dividing nheads and at most 8192");
+  if (!x || !dt || !A || !B || !C || !dout || !dx || !ddt || !dA || !dB || !dC || !workspace)
+    return bfail(SSD_ERR_NULL, "x, dt, A, B, C, dout, dx, ddt, dA, dB, dC, workspace required");
+  if (z && !dz) return bfail(SSD_ERR_NULL, "dz is required with z");
+  const void* ptrs[] = {x, dt, B, C, z, dout, dx, ddt, dB, dC, dz, workspace};
+  for (const void* p : ptrs)
+    if (((uintptr_t)p & 15u) != 0) return bfail(SSD_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const ExLayout ex = ex_layout(base, batch, seqlen, nheads, headdim, dstate, ngroups);
+  if (workspace_bytes < ex.total) {
+    char m[160];
+    snprintf(m, sizeof(m), "workspace of %zu bytes < %zu needed", workspace_bytes, ex.total);
+    return bfail(SSD_ERR_WORKSPACE, m);
+  }
+  char* ws = static_cast<char*>(workspace);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t xs = batch * seqlen * nheads * headdim, ts = batch * seqlen * nheads;
+  const int64_t bs = batch * seqlen * ngroups * dstate;
+  auto up = [&](const void* in, int64_t n, size_t off) {
+    bf16_to_f32_kernel<<<blocks_for((n + 3) / 4, 256), 256, 0, st>>>(static_cast<const bf*>(in),
+                                                                    n, F(off));
+  };
+  auto down = [&](size_t off, int64_t n, void* out) {
+    f32_to_bf16_kernel<<<blocks_for((n + 3) / 4, 256), 256, 0, st>>>(F(off), n,
+                                                                    static_cast<bf*>(out));
+  };
+  up(x, xs, ex.x);
+  up(dt, ts, ex.dt);
+  up(B, bs, ex.B);
+  up(C, bs, ex.C);
+  if (z) up(z, xs, ex.z);
+  up(dout, xs, ex.dout);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    char m[200];
+    snprintf(m, sizeof(m), "ssd_scan_bwd_ex launch: %s", cudaGetErrorString(e));
+    return bfail(SSD_ERR_CUDA, m);
+  }
+  const int rc = ssd_scan_bwd(F(ex.x), F(ex.dt), dt_bias, dt_softplus, dt_limit_lo, dt_limit_hi,
+                              A, F(ex.B), F(ex.C), D, z ? F(ex.z) : nullptr, initial_states,
+                              seq_idx, F(ex.dout), batch, seqlen, nheads, headdim, dstate,
+                              ngroups, chunk_size, F(ex.dx), F(ex.ddt), d_dt_bias, dA, F(ex.dB),
+                              F(ex.dC), dD, z ? F(ex.dz) : nullptr, d_initial_states, workspace,
+                              base, stream);
+  if (rc != SSD_OK) return rc;
+  down(ex.dx, xs, dx);
+  down(ex.ddt, ts, ddt);
+  down(ex.dB, bs, dB);
+  down(ex.dC, bs, dC);
+  if (z) down(ex.dz, xs, dz);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    char m[200];
+    snprintf(m, sizeof(m), "ssd_scan_bwd_ex launch: %s", cudaGetErrorString(e));
     return bfail(SSD_ERR_CUDA, m);
   }
   return SSD_OK;

@@ -440,9 +440,11 @@ def ssd_decode_step(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch
 
 # --- backward -----------------------------------------------------------------
 
-def bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size) -> int:
-    return int(_lib.load().ssd_scan_bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
-                                                        ngroups, chunk_size))
+def bwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
+                        dtype=torch.float32) -> int:
+    return int(_lib.load().ssd_scan_bwd_ex_workspace_bytes(batch, seqlen, nheads, headdim,
+                                                           dstate, ngroups, chunk_size,
+                                                           _DT[dtype]))
 
 
 def ssd_scan_bwd(dout: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor,
@@ -454,26 +456,32 @@ def ssd_scan_bwd(dout: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch
                  seq_idx: Optional[torch.Tensor] = None,
                  workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
     """Gradients of sum(out * dout) for the forward ssd_scan_fwd with the same
-    arguments (ssd_scan_bwd; fp32, dense tensors).  Returns a dict with
-    dx, ddt (w.r.t. the raw dt), dA, dB, dC, d_dt_bias, dD, and dz /
-    d_initial_states when z / initial_states are given."""
+    arguments (dense tensors).  x, dt, B, C, z and dout are fp32
+    (ssd_scan_bwd) or all bf16 (ssd_scan_bwd_ex: computed in fp32, the
+    element-wise gradients returned in bf16); A, dt_bias, D, initial_states
+    fp32.  Returns a dict with dx, ddt (w.r.t. the raw dt), dA, dB, dC,
+    d_dt_bias, dD, and dz / d_initial_states when z / initial_states are
+    given."""
     f32 = torch.float32
+    xd = x.dtype
+    if xd not in _DT:
+        raise ValueError(f"x must be float32 or bfloat16, got {xd}")
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     dev = x.device
-    _need(dout, "dout", f32, (Bsz, L, H, P), dev)
-    _need(x, "x", f32, device=dev)
-    _need(dt, "dt", f32, (Bsz, L, H), dev)
+    _need(dout, "dout", xd, (Bsz, L, H, P), dev)
+    _need(x, "x", xd, device=dev)
+    _need(dt, "dt", xd, (Bsz, L, H), dev)
     _need(A, "A", f32, (H,), dev)
-    _need(B, "B", f32, (Bsz, L, G, N), dev)
-    _need(C, "C", f32, (Bsz, L, G, N), dev)
+    _need(B, "B", xd, (Bsz, L, G, N), dev)
+    _need(C, "C", xd, (Bsz, L, G, N), dev)
     _need(dt_bias, "dt_bias", f32, (H,), dev, optional=True)
     _need(D, "D", f32, (H,), dev, optional=True)
-    _need(z, "z", f32, (Bsz, L, H, P), dev, optional=True)
+    _need(z, "z", xd, (Bsz, L, H, P), dev, optional=True)
     _need(initial_states, "initial_states", f32, (Bsz, H, P, N), dev, optional=True)
     _need(seq_idx, "seq_idx", torch.int32, (Bsz, L), dev, optional=True)
     lib = _lib.load()
-    ws_need = int(lib.ssd_scan_bwd_workspace_bytes(Bsz, L, H, P, N, G, chunk_size))
+    ws_need = int(lib.ssd_scan_bwd_ex_workspace_bytes(Bsz, L, H, P, N, G, chunk_size, _DT[xd]))
     if workspace is None and ws_need > 0:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -485,12 +493,12 @@ def ssd_scan_bwd(dout: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch
          "d_initial_states": (None if initial_states is None
                               else torch.empty_like(initial_states))}
     lo, hi = dt_limit
-    _lib.check(lib.ssd_scan_bwd(
+    _lib.check(lib.ssd_scan_bwd_ex(
         _ptr(x), _ptr(dt), _ptr(dt_bias), int(bool(dt_softplus)), float(lo), float(hi),
         _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(initial_states), _ptr(seq_idx),
-        _ptr(dout), Bsz, L, H, P, N, G, int(chunk_size), _ptr(g["dx"]), _ptr(g["ddt"]),
-        _ptr(g["d_dt_bias"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
-        _ptr(g["dz"]), _ptr(g["d_initial_states"]), _ptr(workspace), ws_bytes,
+        _ptr(dout), Bsz, L, H, P, N, G, int(chunk_size), _DT[xd], _ptr(g["dx"]),
+        _ptr(g["ddt"]), _ptr(g["d_dt_bias"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+        _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["d_initial_states"]), _ptr(workspace), ws_bytes,
         _stream(stream)))
     return g
 
@@ -498,7 +506,7 @@ def ssd_scan_bwd(dout: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch
 # --- autograd ----------------------------------------------------------------
 
 class _SSDScan(torch.autograd.Function):
-    """ssd_scan_fwd forward, ssd_scan_bwd backward (fp32)."""
+    """ssd_scan_fwd forward, ssd_scan_bwd backward."""
 
     @staticmethod
     def forward(ctx, x, dt, A, B, C, dt_bias, D, z, initial_states, seq_idx, chunk_size,
@@ -532,8 +540,9 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
              D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
              initial_states: Optional[torch.Tensor] = None,
              seq_idx: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """The scan as a differentiable torch function (fp32, dense tensors):
-    the forward is ssd_scan_fwd, the backward ssd_scan_bwd, giving gradients
-    for x, dt (raw), A, B, C, dt_bias, D, z and initial_states.  Returns out."""
+    """The scan as a differentiable torch function (x, dt, B, C, z fp32 or
+    bf16): the forward is ssd_scan_fwd, the backward ssd_scan_bwd (computed
+    in fp32), giving gradients for x, dt (raw), A, B, C, dt_bias, D, z and
+    initial_states.  Returns out."""
     return _SSDScan.apply(x, dt, A, B, C, dt_bias, D, z, initial_states, seq_idx, chunk_size,
                           dt_softplus, tuple(dt_limit))

@@ -196,3 +196,27 @@ def test_backward_validation_before_any_launch(lib):
     assert call(z=16) == -2                # dz is required with z
     assert call(dB=24) == -3
     assert call(wsb=need - 1) == -5
+
+
+def test_backward_ex_workspace_and_validation(lib):
+    B, L, H, P, N, G, Q = 2, 100, 4, 32, 64, 2, 64
+    f32 = lib.ssd_scan_bwd_ex_workspace_bytes(B, L, H, P, N, G, Q, _lib.SSD_DTYPE_F32)
+    assert f32 == lib.ssd_scan_bwd_workspace_bytes(B, L, H, P, N, G, Q)
+    bf = lib.ssd_scan_bwd_ex_workspace_bytes(B, L, H, P, N, G, Q, _lib.SSD_DTYPE_BF16)
+    assert bf > f32
+    assert lib.ssd_scan_bwd_ex_workspace_bytes(B, L, H, P, N, G, Q, 7) == 0
+    assert lib.ssd_scan_bwd_ex_workspace_bytes(B, L, H, P, 48, G, Q, _lib.SSD_DTYPE_BF16) == 0
+
+    def call(**kw):
+        a = dict(x=16, dt=16, B=16, C=16, z=None, dout=16, dtype=_lib.SSD_DTYPE_BF16, dx=16,
+                 ddt=16, dB=16, dC=16, dz=None, wsb=bf)
+        a.update(kw)
+        return lib.ssd_scan_bwd_ex(a["x"], a["dt"], None, 1, 0.0, math.inf, 16, a["B"], a["C"],
+                                   None, a["z"], None, None, a["dout"], B, L, H, P, N, G, Q,
+                                   a["dtype"], a["dx"], a["ddt"], None, 16, a["dB"], a["dC"],
+                                   None, a["dz"], None, 16, a["wsb"], None)
+    assert call(dtype=7) == -1
+    assert call(dout=None) == -2
+    assert call(z=16) == -2
+    assert call(dC=24) == -3
+    assert call(wsb=bf - 1) == -5

@@ -65,3 +65,28 @@ def test_gradients_flow_through_surrounding_ops():
     gx = proj.grad[:, :, :H * P].reshape(d["x"].shape).double().cpu().numpy()
     assert_close(gx, ref["x"], TOL["f32"], "d proj (x part)")
     assert float(proj.grad[:, :, H * P:].abs().max()) == 0.0
+
+
+def test_bf16_training_step():
+    """bf16 leaves: the forward is the bf16 path, loss.backward() gives bf16
+    gradients for x, dt, B, C, z and fp32 ones for A, dt_bias, D, within the
+    bf16 bound of the oracle's."""
+    import selective_state_space_05_gb300 as ssd
+    d = si.random_small(620, batch=1, seqlen=300, nheads=4, headdim=64, dstate=128, ngroups=2,
+                        chunk_size=256, dtype="bf16")
+    w = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(11))
+    t = _leaves(d)
+    out = ssd.ssd_scan(t["x"], t["dt"], t["A"], t["B"], t["C"], chunk_size=256,
+                       dt_bias=t["dt_bias"], D=t["D"], z=t["z"])
+    assert out.dtype == torch.bfloat16
+    (out.float() * w.cuda()).sum().backward()
+    d32 = {k: (v.float() if torch.is_tensor(v) and v.dtype == torch.bfloat16 else v)
+           for k, v in d.items()}
+    # the upstream gradient reaching the scan is w rounded to bf16
+    ref = so.scan_backward(d32, w.bfloat16().float())
+    for k in ("x", "dt", "B", "C", "z"):
+        assert t[k].grad.dtype == torch.bfloat16
+        assert_close(t[k].grad.double().cpu().numpy(), ref[k], TOL["bf16"], k)
+    for k in ("A", "dt_bias", "D"):
+        assert t[k].grad.dtype == torch.float32
+        assert_close(t[k].grad.double().cpu().numpy(), ref[k], TOL["bf16"], k)

@@ -193,3 +193,36 @@ def test_backward_full_size_sampled_pairs():
         g = got["d_initial_states"][b:b + 1, h:h + 1].double().cpu().numpy()
         rep["dinitial_states"] = assert_close(g, ref["initial_states"], TOL["f32"],
                                               f"({b},{h}) dh0")
+
+
+def test_bf16_backward_is_the_fp32_backward_rounded():
+    """bf16 inputs (ssd_scan_bwd_ex): the gradients are the fp32 backward's on
+    the same values, rounded to bf16 (bit for bit) for the element-wise ones,
+    the same for the fp32 ones (up to the order of the per-head atomic sums);
+    and against the oracle within the bf16
+    bound (element-wise) and the fp32 bound (per-head sums, initial states)."""
+    d = si.random_small(520, batch=2, seqlen=300, nheads=4, headdim=64, dstate=128, ngroups=2,
+                        chunk_size=256, dtype="bf16", init_std=0.3, seq_idx_lengths=[150, 150])
+    dout = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(21)).bfloat16()
+    gb = _run(d, dout)
+    d32 = {k: (v.float() if torch.is_tensor(v) and v.dtype == torch.bfloat16 else v)
+           for k, v in d.items()}
+    g32 = _run(d32, dout.float())
+    for k in ("dx", "ddt", "dB", "dC", "dz"):
+        assert gb[k].dtype == torch.bfloat16
+        assert torch.equal(gb[k], g32[k].bfloat16()), k
+    for k in ("dA", "d_dt_bias", "dD", "d_initial_states"):
+        assert gb[k].dtype == torch.float32
+    assert torch.equal(gb["d_initial_states"], g32["d_initial_states"])
+    # the per-head sums add warps' partial sums with atomics, in no fixed order
+    for k in ("dA", "d_dt_bias", "dD"):
+        assert torch.allclose(gb[k], g32[k], rtol=1e-5, atol=0.0), k
+    ref = so.scan_backward(d32, dout.float())
+    scale = _head_terms(d32, dout.float(), ref)
+    for name, k in (("x", "dx"), ("dt", "ddt"), ("B", "dB"), ("C", "dC"), ("z", "dz")):
+        assert_close(gb[k].double().cpu().numpy(), ref[name], TOL["bf16"], k)
+    assert_close(gb["d_initial_states"].double().cpu().numpy(), ref["initial_states"],
+                 TOL["f32"], "dh0")
+    for name, k in (("A", "dA"), ("dt_bias", "d_dt_bias"), ("D", "dD")):
+        err = np.abs(gb[k].double().cpu().numpy() - ref[name])
+        assert (err <= TOL["f32"] * scale[name] + 1e-30).all(), k
