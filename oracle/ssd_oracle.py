@@ -505,3 +505,79 @@ def decay_gradient(inp: dict, dout):
                         dt_limit=(lo, hi), a=a)
     (out * torch.as_tensor(dout).to(f)).sum().backward()
     return a.grad.numpy(), d.numpy()
+
+
+def decay_gradient_pairs(inp: dict, dout):
+    """dA written as its sum over token pairs, in fp64 (quadratic, small
+    cases): every pair j < i of one document contributes
+    P_ij = exp(a_{j+1} + ... + a_i) (C_i . B_j) dt_j (dy_i . x_j), and every
+    token i of the first document the initial-state term
+    exp(a_0 + ... + a_i) dy_i . (h0 C_i); the decay exponents a_k = dt_k A
+    that a pair spans get its term, so dA = sum P_ij (dt_{j+1} + ... + dt_i)
+    (+ the initial-state terms times dt_0 + ... + dt_i), with dy = dout
+    silu(z).  Returns (dA from the pairs, scale), both [nheads], the scale
+    being the sum over the elementary products the pair terms are made of,
+    exp(..) dt_j |C_in B_jn| |dy_ip x_jp| (and exp(..) |dy_ip h0_pn C_in|),
+    each times its span: the standard bound for a sum computed from products
+    each known to a relative precision (the dot products over dstate and
+    headdim inside a pair term cancel, as do the pairs)."""
+    x = np.asarray(torch_to_np(inp["x"]), dtype=np.float64)
+    Bsz, L, H, P = x.shape
+    Bm = np.asarray(torch_to_np(inp["B"]), dtype=np.float64)
+    Cm = np.asarray(torch_to_np(inp["C"]), dtype=np.float64)
+    G = Bm.shape[2]
+    rep = H // G
+    A = np.asarray(torch_to_np(inp["A"]), dtype=np.float64)
+    raw = np.asarray(torch_to_np(inp["dt"]), dtype=np.float64)
+    if inp.get("dt_bias") is not None:
+        raw = raw + np.asarray(torch_to_np(inp["dt_bias"]), dtype=np.float64)
+    d = np.logaddexp(0.0, raw) if inp.get("dt_softplus", True) else raw
+    lo, hi = inp.get("dt_limit", (0.0, float("inf")))
+    if not (lo == 0.0 and hi == float("inf")):
+        d = np.clip(d, lo, hi)
+    dy = np.asarray(torch_to_np(dout), dtype=np.float64)
+    if inp.get("z") is not None:
+        zz = np.asarray(torch_to_np(inp["z"]), dtype=np.float64)
+        dy = dy * zz / (1.0 + np.exp(-zz))
+    h0 = inp.get("initial_states")
+    h0 = None if h0 is None else np.asarray(torch_to_np(h0), dtype=np.float64)
+    seq = inp.get("seq_idx")
+    seq = None if seq is None else np.asarray(torch_to_np(seq))
+    dA = np.zeros(H)
+    scale = np.zeros(H)
+    for b in range(Bsz):
+        doc = np.zeros(L, dtype=np.int64) if seq is None else seq[b].astype(np.int64)
+        same = (doc[:, None] == doc[None, :]) & np.tril(np.ones((L, L), dtype=bool), -1)
+        # a document starts where the id changes; the first document is the one
+        # containing token 0 until its first change
+        first = np.ones(L, dtype=bool)
+        if seq is not None:
+            change = np.nonzero(doc[1:] != doc[:-1])[0]
+            if change.size:
+                first[change[0] + 1:] = False
+        for h in range(H):
+            g = h // rep
+            a = d[b, :, h] * A[h]
+            S = np.cumsum(a)                  # S_i = a_0 + ... + a_i
+            Dt = np.cumsum(d[b, :, h])        # dt_0 + ... + dt_i
+            decay = np.exp(np.where(same, S[:, None] - S[None, :], -np.inf))
+            Pm = decay * (Cm[b, :, g] @ Bm[b, :, g].T) * d[b, :, h][None, :] * \
+                (dy[b, :, h] @ x[b, :, h].T)
+            span = np.abs(Dt[:, None] - Dt[None, :])
+            dA[h] += (Pm * (Dt[:, None] - Dt[None, :])).sum()
+            Pabs = decay * (np.abs(Cm[b, :, g]) @ np.abs(Bm[b, :, g]).T) * \
+                np.abs(d[b, :, h])[None, :] * (np.abs(dy[b, :, h]) @ np.abs(x[b, :, h]).T)
+            scale[h] += (Pabs * span).sum()
+            if h0 is not None:
+                pin = np.where(first, np.exp(S) * np.einsum("ip,pn,in->i", dy[b, :, h],
+                                                            h0[b, h], Cm[b, :, g]), 0.0)
+                pabs = np.where(first, np.exp(S) * np.einsum(
+                    "ip,pn,in->i", np.abs(dy[b, :, h]), np.abs(h0[b, h]), np.abs(Cm[b, :, g])), 0.0)
+                dA[h] += (pin * Dt).sum()
+                scale[h] += (pabs * np.abs(Dt)).sum()
+    return dA, scale
+
+
+def torch_to_np(v):
+    """numpy view of a torch tensor or array (test-side convenience)."""
+    return v.detach().cpu().double().numpy() if hasattr(v, "detach") else v

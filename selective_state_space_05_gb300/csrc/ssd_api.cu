@@ -84,6 +84,7 @@ struct Workspace {
   int32_t* seg;
   float* states;
   float* cb;   // C B^T per (batch, chunk, group) for the fp32 tensor-core stages, or nullptr
+  float* tg;   // B as chunk_state's pre-split tiles (fp32, dstate 128), or nullptr
   size_t bytes;
 };
 
@@ -112,10 +113,16 @@ Workspace carve(const ssd::Dims& d, void* base, bool with_cb = false) {
   w.states = reinterpret_cast<float*>(p + off);
   off = round_up(off + st * sizeof(float), 256);
   w.cb = nullptr;
+  w.tg = nullptr;
   if (with_cb) {
     w.cb = reinterpret_cast<float*>(p + off);
     off = round_up(off + (size_t)d.batch * d.nchunks * d.ngroups * d.chunk * d.chunk *
                              sizeof(float), 256);
+    if (d.dstate == 128) {
+      w.tg = reinterpret_cast<float*>(p + off);
+      off = round_up(off + (size_t)d.batch * d.nchunks * d.ngroups * (d.chunk / 16) *
+                               ssd::group_tile_floats() * sizeof(float), 256);
+    }
   }
   w.bytes = off;
   return w;
@@ -361,9 +368,16 @@ int scan_fwd_run(const ssd::Dims& d_in, const void* x, const void* dt, const flo
     e = ssd::launch_dt_cumsum<float>(static_cast<const float*>(dt), dt_bias, dt_softplus,
                                      dt_limit_lo, dt_limit_hi, clamp, A, seq_idx, d, w.dt, w.cs,
                                      seg, st);
+    // chunk_state with B pre-split once per group where it runs on tensor cores
+    const bool tg = w.tg != nullptr && ssd::chunk_state_tc32_fits(xf, static_cast<const float*>(B), d);
+    if (e == cudaSuccess && tg)
+      e = ssd::launch_group_tiles_tc32(static_cast<const float*>(B), d.sB, d.ngroups, d.batch,
+                                       d.seqlen, d.nchunks, w.tg, st);
     if (e == cudaSuccess)
-      e = ssd::launch_chunk_state<float>(xf, static_cast<const float*>(B), w.dt, w.cs, seg, d,
-                                         w.states, st);
+      e = tg ? ssd::launch_chunk_state_tc32(xf, static_cast<const float*>(B), w.dt, w.cs, seg, d,
+                                            w.states, st, w.tg)
+             : ssd::launch_chunk_state<float>(xf, static_cast<const float*>(B), w.dt, w.cs, seg,
+                                              d, w.states, st);
     if (e == cudaSuccess)
       e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, d, st);
     const float* Bf = static_cast<const float*>(B);

@@ -360,7 +360,7 @@ int bwd_chunk(int chunk_size, int P, int N) {
 // Workspace pieces, 256-byte aligned.  Reversed arrays span Lp = nc Qb tokens.
 struct BwdLayout {
   size_t dtF, csF, segF, statesF, yo, dy, dyR, xR, CR, BR, aR, seqR, csR, dtRo, segR, ones,
-      states1, finR, goR, states2, oB, h0T, oC, q, xg, dyx, bnd, cb, cbT, total;
+      states1, finR, goR, states2, oB, h0T, oC, q, xg, dyx, bnd, cb, cbT, tgB, tgCR, total;
 };
 
 BwdLayout bwd_layout(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
@@ -409,6 +409,10 @@ BwdLayout bwd_layout(int64_t Bz, int64_t L, int H, int P, int N, int G, int Q) {
   const size_t cbn = Q == 128 ? (size_t)Bz * nc * G * Q * Q : 0;
   l.cb = take(cbn);
   l.cbT = take(cbn);
+  // B and the reversed C as chunk_state's pre-split A tiles (dstate 128)
+  const size_t tgn = (Q == 128 && N == 128) ? (size_t)Bz * nc * G * 8 * 4096 : 0;
+  l.tgB = take(tgn);
+  l.tgCR = take(tgn);
   l.total = o;
   return l;
 }
@@ -522,8 +526,21 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   // without D x and without the diagonal (strict)
   e = ssd::launch_dt_cumsum<float>(dt, dt_bias, dt_softplus, dt_limit_lo, dt_limit_hi, clamp, A,
                                    seq_idx, d, F(lay.dtF), F(lay.csF), segF, st);
+  // chunk_state on tensor cores with the per-group operand pre-split once:
+  // B for the forward-orientation scans and (headdim 64) the dC scan, the
+  // reversed C for the g scan and (headdim 64) the dB scan
+  const bool tiles = Q == 128 && N == 128 && ssd::chunk_state_tc32_fits(x, B, d);
+  const bool tiles_swapped = tiles && P == 64;
+  if (e == cudaSuccess && tiles)
+    e = ssd::launch_group_tiles_tc32(B, d.sB, G, Bz, L, nc, F(lay.tgB), st);
+  auto state = [&](const float* xo, const float* Bo, const float* dto, const float* cso,
+                   const int32_t* sgo, const ssd::Dims& dd, float* out, const float* tg) {
+    return tg ? ssd::launch_chunk_state_tc32(xo, Bo, dto, cso, sgo, dd, out, st, tg)
+              : ssd::launch_chunk_state<float>(xo, Bo, dto, cso, sgo, dd, out, st);
+  };
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_state<float>(x, B, F(lay.dtF), F(lay.csF), segF, d, F(lay.statesF), st);
+    e = state(x, B, F(lay.dtF), F(lay.csF), segF, d, F(lay.statesF),
+              tiles ? F(lay.tgB) : nullptr);
   if (e == cudaSuccess)
     e = ssd::launch_state_passing(F(lay.statesF), F(lay.csF), segF, initial_states, nullptr, d,
                                   st);
@@ -555,6 +572,8 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
         F(lay.ones), Bz * H * (int64_t)nc * Q, 1.f);
     ok();
   }
+  if (e == cudaSuccess && tiles)
+    e = ssd::launch_group_tiles_tc32(F(lay.CR), dR.sC, G, Bz, Lp, nc, F(lay.tgCR), st);
   // stage 1 of the reversed scans: cumsum of the shifted decays (A' = 1, no softplus)
   if (e == cudaSuccess)
     e = ssd::launch_dt_cumsum<float>(F(lay.aR), nullptr, 0, 0.f, INFINITY, 0, F(lay.q),
@@ -563,8 +582,8 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   // g without the diagonal: reversed strict scan of dy with B' = C, C' = B,
   // value coefficient 1; its chunk states are the dH of the boundaries
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_state<float>(F(lay.dyR), F(lay.CR), F(lay.ones), F(lay.csR), segR, dR,
-                                       F(lay.states1), st);
+    e = state(F(lay.dyR), F(lay.CR), F(lay.ones), F(lay.csR), segR, dR, F(lay.states1),
+              tiles ? F(lay.tgCR) : nullptr);
   if (e == cudaSuccess)
     e = ssd::launch_state_passing(F(lay.states1), F(lay.csR), segR, nullptr, F(lay.finR), dR,
                                   st);
@@ -584,8 +603,8 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
   // dB before the dt factor: reversed scan with x' = C (per group), B' = dy,
   // C' = x
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_state<float>(F(lay.CR), F(lay.dyR), F(lay.ones), F(lay.csR), segR,
-                                       dsR, F(lay.states2), st);
+    e = state(F(lay.CR), F(lay.dyR), F(lay.ones), F(lay.csR), segR, dsR, F(lay.states2),
+              tiles_swapped ? F(lay.tgCR) : nullptr);
   if (e == cudaSuccess)
     e = ssd::launch_state_passing(F(lay.states2), F(lay.csR), segR, nullptr, nullptr, dsR, st);
   if (e == cudaSuccess)
@@ -599,8 +618,8 @@ int ssd_scan_bwd(const float* x, const float* dt, const float* dt_bias, int dt_s
     ok();
   }
   if (e == cudaSuccess)
-    e = ssd::launch_chunk_state<float>(B, x, F(lay.dtF), F(lay.csF), segF, ds, F(lay.states2),
-                                       st);
+    e = state(B, x, F(lay.dtF), F(lay.csF), segF, ds, F(lay.states2),
+              tiles_swapped ? F(lay.tgB) : nullptr);
   if (e == cudaSuccess)
     e = ssd::launch_state_passing(F(lay.states2), F(lay.csF), segF,
                                   initial_states ? F(lay.h0T) : nullptr, nullptr, ds, st);

@@ -120,9 +120,17 @@ cudaError_t launch_chunk_scan_tc(const __nv_bfloat16* x, const __nv_bfloat16* B,
 bool chunk_state_tc32_fits(const float* x, const float* B, const Dims& d);
 bool chunk_scan_tc32_fits(const float* x, const float* B, const float* C, const float* z,
                           const Dims& d);
+// Tg: the 128-row per-group operand's split tiles from launch_group_tiles_tc32
+// (B when dstate is 128; x, read through xrep, otherwise), or nullptr.
 cudaError_t launch_chunk_state_tc32(const float* x, const float* B, const float* dtp,
                                     const float* cs, const int32_t* seg, const Dims& d,
-                                    float* states, cudaStream_t st);
+                                    float* states, cudaStream_t st, const float* Tg = nullptr);
+// A per-group operand Y [batch, seqlen, groups, 128] (token strides sY) as
+// chunk_state's split A tiles: T holds batch x nchunks x groups x 8 slices of
+// group_tile_floats() floats (128-token chunks).
+constexpr int64_t group_tile_floats() { return 128 * 16 * 2; }
+cudaError_t launch_group_tiles_tc32(const float* Y, TokStride sY, int groups, int64_t batch,
+                                    int64_t seqlen, int nchunks, float* T, cudaStream_t st);
 // Sg: C B^T of every (batch x chunk, group) computed beforehand by
 // launch_cb_tc32 (nullptr: the kernel computes it itself); srev: read it for
 // a time-reversed scan (chunk nc - 1 - c, indices 127 - i, 127 - j; pass the

@@ -194,17 +194,53 @@ __device__ __forceinline__ bool pipeline_drain(int nS, uint64_t* bars, int& ok_a
 }
 
 // ---------------------------------------------------------------------------
+// A per-group operand Y [batch, seqlen, groups, 128] (B, or the reversed C)
+// written once as chunk_state's A tiles: for every (batch x chunk, group)
+// and 16-token slice, the 128 x 16 transpose (row = Y's feature, K = token)
+// split into hi and lo and laid out as the shared tile (64-byte swizzle),
+// 16 KB per slice, so that chunk_state copies it instead of staging it for
+// every head.  One CTA per (batch x chunk, group, slice), 256 threads:
+// thread (row = tid % 128, tokens 8 (tid / 128) .. + 7).
+// ---------------------------------------------------------------------------
+constexpr int kTileFloats = kQ * kK * 2;   // floats per split slice (hi + lo)
+
+__global__ void __launch_bounds__(256) group_tiles_kernel(const float* __restrict__ Y,
+                                                          TokStride sY, int groups,
+                                                          int64_t seqlen, int nchunks,
+                                                          float* __restrict__ T) {
+  const int bc = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int64_t b = bc / nchunks;
+  const int c = bc % nchunks;
+  const int row = threadIdx.x % kQ, k0 = 8 * (threadIdx.x / kQ);
+  const int64_t t0 = (int64_t)c * kQ + kK * s;
+  unsigned char* tile = reinterpret_cast<unsigned char*>(
+      T + (((int64_t)bc * groups + g) * (kQ / kK) + s) * kTileFloats);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int k = k0 + u;
+    const int64_t t = t0 + k;
+    const float v = t < seqlen ? Y[toff(sY, b, t) + (int64_t)g * kQ + row] : 0.f;
+    put1(tile, kQ, row, k, v);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // chunk_state: one CTA per (batch x chunk, head), 256 threads.  The MMA rows
 // are the 128-wide one of headdim / dstate: with dstate 128 the transposed
 // state S^T = B^T (w o x) (rows n), else S = (w o x)^T B (rows p).  K = the
 // chunk's tokens, 16-token slices; both operands are staged transposed
 // (16 lanes on the tokens, the other half-warp on the next row quad).
 // ---------------------------------------------------------------------------
-template <int P, int N>
+// kG: the 128-row operand is per group (B when dstate is 128; x, read
+// through xrep, when headdim is 128) and comes pre-split from Tg
+// (group_tiles_kernel); the weights w_j then go on the other, per-head
+// operand (the sum over j of w_j x_j B_j^T does not care which factor
+// carries them), the only one staged here.
+template <int P, int N, bool kG>
 __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
     const float* __restrict__ x, const float* __restrict__ Bm, const float* __restrict__ dtp,
     const float* __restrict__ cs, const int32_t* __restrict__ seg, Dims d,
-    float* __restrict__ states, Limits lim) {
+    float* __restrict__ states, Limits lim, const float* __restrict__ Tg) {
   constexpr bool kT = (N == 128);
   constexpr int NR = kT ? P : N;   // MMA N: the other dimension
   constexpr int XQ = P / 64, BQ = N / 64;   // row quads per thread and slice (16 per warp)
@@ -287,15 +323,67 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
   };
   auto issue = [&](int s) { mma_slice(tmem, tA(s & 1), tB(s & 1), NR, idesc, s > 0); };
 
-  load_into(0, rx0, rb0);
-  if (nS > 1) load_into(1, rx1, rb1);
+  // kG: the tile copy (four float4 per thread and slice) and the per-head
+  // operand, weighted
+  constexpr int VQ = kT ? XQ : BQ, VR = kT ? P : N;
+  const float* tg = nullptr;
+  if (kG) {
+    const int tgroups = kT ? d.ngroups : d.nheads / d.xrep;
+    const int gi = kT ? g : h / d.xrep;
+    tg = Tg + ((int64_t)bc * tgroups + gi) * (kQ / kK) * kTileFloats;
+  }
+  float4 rt0[4], rv0[VQ], rt1[4], rv1[VQ];
+  auto gload_into = [&](int s, float4(&rt)[4], float4(&rv)[VQ]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      rt[u] = ld4(tg + (int64_t)s * kTileFloats + 4 * (tid + 256 * u));
+    const int j = kK * s + jl;
+    const bool tv = j < n;
+    const float* src = kT ? xh + toff(d.sx, b, t0 + (tv ? j : 0))
+                          : Bm + toff(d.sB, b, t0 + (tv ? j : 0)) + (int64_t)g * N;
+#pragma unroll
+    for (int u = 0; u < VQ; ++u) rv[u] = tv ? ld4(src + 4 * (2 * warp + qh + 16 * u)) : zero4;
+  };
+  auto gstore_from = [&](int s, const float4(&rt)[4], const float4(&rv)[VQ]) {
+    float4* a = reinterpret_cast<float4*>(tA(s & 1));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a[tid + 256 * u] = rt[u];
+    unsigned char* bt = tB(s & 1);
+    const float wj = (kK * s + jl < n) ? wsh[kK * s + jl] : 0.f;
+#pragma unroll
+    for (int u = 0; u < VQ; ++u) {
+      const int r = 4 * (2 * warp + qh + 16 * u);
+      put1(bt, VR, r, jl, rv[u].x * wj);
+      put1(bt, VR, r + 1, jl, rv[u].y * wj);
+      put1(bt, VR, r + 2, jl, rv[u].z * wj);
+      put1(bt, VR, r + 3, jl, rv[u].w * wj);
+    }
+  };
+
   bool run = true;
-  for (int s = 0; run && s < nS; s += 2) {
-    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, rx0, rb0); },
-                        [&](int t) { load_into(t, rx0, rb0); }, issue);
-    if (run && s + 1 < nS)
-      run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, rx1, rb1); },
-                          [&](int t) { load_into(t, rx1, rb1); }, issue);
+  if constexpr (kG) {
+    gload_into(0, rt0, rv0);
+    if (nS > 1) gload_into(1, rt1, rv1);
+    for (int s = 0; run && s < nS; s += 2) {
+      run = pipeline_step(s, nS, bars, tid, ok_all, lim,
+                          [&](int t) { gstore_from(t, rt0, rv0); },
+                          [&](int t) { gload_into(t, rt0, rv0); }, issue);
+      if (run && s + 1 < nS)
+        run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
+                            [&](int t) { gstore_from(t, rt1, rv1); },
+                            [&](int t) { gload_into(t, rt1, rv1); }, issue);
+    }
+  } else {
+    load_into(0, rx0, rb0);
+    if (nS > 1) load_into(1, rx1, rb1);
+    for (int s = 0; run && s < nS; s += 2) {
+      run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, rx0, rb0); },
+                          [&](int t) { load_into(t, rx0, rb0); }, issue);
+      if (run && s + 1 < nS)
+        run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
+                            [&](int t) { store_from(t, rx1, rb1); },
+                            [&](int t) { load_into(t, rx1, rb1); }, issue);
+    }
   }
   if (run) run = pipeline_drain(nS, bars, ok_all, lim);
   if (run) {
@@ -769,24 +857,33 @@ bool chunk_scan_tc32_fits(const float* x, const float* B, const float* C, const 
 
 cudaError_t launch_chunk_state_tc32(const float* x, const float* B, const float* dtp,
                                     const float* cs, const int32_t* seg, const Dims& d,
-                                    float* states, cudaStream_t st) {
+                                    float* states, cudaStream_t st, const float* Tg) {
   using namespace tc32;
   dim3 grid((unsigned)(d.batch * d.nchunks), (unsigned)d.nheads);
-  cudaError_t e = cudaSuccess;
-#define SSD_TC32_STATE(P, N)                                                                    \
-  if (d.headdim == P && d.dstate == N) {                                                        \
-    static cudaError_t prep = prepare(chunk_state_tc32_kernel<P, N>, kSmem);                          \
+#define SSD_TC32_STATE(P, N, G_)                                                                \
+  if (d.headdim == P && d.dstate == N && (Tg != nullptr) == G_) {                               \
+    static cudaError_t prep = prepare(chunk_state_tc32_kernel<P, N, G_>, kSmem);                \
     if (prep != cudaSuccess) return prep;                                                       \
-    chunk_state_tc32_kernel<P, N><<<grid, 256, kSmem, st>>>(x, B, dtp, cs, seg, d, states,      \
-                                                           limits());                           \
+    chunk_state_tc32_kernel<P, N, G_><<<grid, 256, kSmem, st>>>(x, B, dtp, cs, seg, d, states,  \
+                                                               limits(), Tg);                   \
     return cudaGetLastError();                                                                  \
   }
-  SSD_TC32_STATE(64, 128)
-  SSD_TC32_STATE(128, 128)
-  SSD_TC32_STATE(128, 64)
+  SSD_TC32_STATE(64, 128, false)
+  SSD_TC32_STATE(128, 128, false)
+  SSD_TC32_STATE(128, 64, false)
+  SSD_TC32_STATE(64, 128, true)
+  SSD_TC32_STATE(128, 128, true)
+  SSD_TC32_STATE(128, 64, true)
 #undef SSD_TC32_STATE
-  e = cudaErrorInvalidValue;
-  return e;
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_group_tiles_tc32(const float* Y, TokStride sY, int groups, int64_t batch,
+                                    int64_t seqlen, int nchunks, float* T, cudaStream_t st) {
+  using namespace tc32;
+  dim3 grid((unsigned)(batch * nchunks), (unsigned)groups, kQ / kK);
+  group_tiles_kernel<<<grid, 256, 0, st>>>(Y, sY, groups, seqlen, nchunks, T);
+  return cudaGetLastError();
 }
 
 bool cb_tc32_fits(const float* B, const float* C, const Dims& d) {

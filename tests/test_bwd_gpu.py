@@ -9,10 +9,14 @@ Each is a sum of fp32 products over at most one chunk's tokens times dstate
 (or headdim) terms per scan, plus a sum over the chunks through the state
 chain; with fp32's 6e-8 unit roundoff and sums of random sign that stays
 near 1e-6 relative, and 1e-4 leaves the margin the forward's tests leave.
-The per-head gradients (dt_bias, A, D) are sums over every token of a head
-of per-token terms t (ddt; da dt with da the gradient of the decay exponent
-a = dt A; dy x), so the bound that the elementwise one implies is
-|err_h| <= 1e-4 sum |t_h|: a sum of terms each within a relative 1e-4.
+The per-head gradients (dt_bias, A, D) are sums of terms t (ddt per token;
+dy x per element; for dA the elementary products of its pair form, each
+pair of tokens j < i of a document contributing L_ij dt_j C_in B_jn
+dy_ip x_jp over n and p, times the dt it spans), so the bound that the
+elementwise one implies is |err_h| <= 1e-4 sum |t_h|: a sum of terms each
+within a relative 1e-4.  (The per-token decay gradient is not such a term:
+it is itself a sum over the pairs around a token, and those cancel, as do
+the dot products inside a pair.)
 
 Cases span several chunks with a ragged tail, grouped B/C, documents
 (seq_idx, a one-token document among them), clamps that bite, dt without
@@ -53,6 +57,10 @@ CASES = [
     ("mamba2_2p7b_heads", dict(batch=1, seqlen=700, nheads=2, headdim=64, dstate=128,
                                ngroups=1, chunk_size=256, init_std=0.1,
                                seq_idx_lengths=[300, 400])),
+    ("hd128_ds128", dict(batch=1, seqlen=300, nheads=4, headdim=128, dstate=128, ngroups=2,
+                         chunk_size=128, init_std=0.2, seq_idx_lengths=[129, 171])),
+    ("hd128_ds64", dict(batch=2, seqlen=200, nheads=2, headdim=128, dstate=64, ngroups=1,
+                        chunk_size=128, init_std=0.2)),
 ]
 
 
@@ -68,16 +76,17 @@ def _run(d, dout):
 
 
 def _head_terms(d, dout, ref):
-    """Per-token terms of the per-head gradients, as [.., H] arrays summed
-    over everything but the head: d_dt_bias <- ddt, dA <- da dt, dD <- dy x."""
-    da, dtp = so.decay_gradient(d, dout)
+    """The scale of each per-head gradient, [H]: the sum of the absolute
+    values of the terms it adds up -- d_dt_bias: ddt per token; dD: dy x per
+    element; dA: the elementary products of its pair form (oracle
+    decay_gradient_pairs), each times the dt it spans."""
     x = d["x"].double().numpy()
     dy = dout.double().numpy()
     if d["z"] is not None:
         z = d["z"].double().numpy()
         dy = dy * z / (1.0 + np.exp(-z))
     return {"dt_bias": np.abs(ref["dt"]).sum(axis=(0, 1)),
-            "A": np.abs(da * dtp).sum(axis=(0, 1)),
+            "A": so.decay_gradient_pairs(d, dout)[1],
             "D": np.abs(dy * x).sum(axis=(0, 1, 3))}
 
 

@@ -512,3 +512,23 @@ def test_decay_gradient_by_finite_differences_and_chain_rule():
         assert abs(fd - da[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, da[idx])
     g = so.scan_backward(d, dout)
     assert rel((da * dtp).sum(axis=(0, 1)), g["A"]) < TIGHT
+
+
+@pytest.mark.parametrize("kw", [
+    dict(batch=2, seqlen=40, nheads=4, ngroups=2, headdim=3, dstate=5, init_std=0.5,
+         seq_idx_lengths=[10, 1, 29]),
+    dict(batch=1, seqlen=30, nheads=2, ngroups=1, headdim=4, dstate=3, dt_limit=(0.0, 0.5),
+         init_std=0.3),
+    dict(batch=1, seqlen=25, nheads=2, ngroups=2, headdim=4, dstate=3, has_z=False,
+         dt_bias=False),
+])
+def test_decay_gradient_pairs_sum_to_autograd_dA(kw):
+    """dA written as its sum over token pairs (and initial-state terms), each
+    term times the dt it spans, equals the autograd oracle's dA; the scale
+    (absolute terms) bounds it."""
+    d = si.random_small(73, **kw)
+    dout = torch.randn(d["x"].shape, generator=torch.Generator().manual_seed(5))
+    dA, scale = so.decay_gradient_pairs(d, dout)
+    ref = so.scan_backward(d, dout)["A"]
+    assert rel(dA, ref) < TIGHT
+    assert (scale >= np.abs(ref) * (1 - 1e-12)).all()
