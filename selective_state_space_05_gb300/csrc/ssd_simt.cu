@@ -60,19 +60,39 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(
   }
 
   const int E = Q >= 32 ? Q / 32 : 1;  // consecutive positions per lane
+  const int lq = __ffs(Q) - 1;          // Q is a power of two
   for (int hg = hb * 32; hg < min(H, hb * 32 + 32); hg += 32) {
     const int hw = min(32, H - hg);
-    for (int idx = tid; idx < Q * 32; idx += 256) {
-      const int t = idx >> 5, j = idx & 31;
-      float v = 0.f;
-      if (t < n && j < hw) {
-        v = to_f(dt[toff(d.sdt, b, t0 + t) + hg + j]);
-        if (dt_bias) v += dt_bias[hg + j];
-        if (softplus) v = v <= 20.f ? log1pf(__expf(v)) : v;
-        if (do_clamp) v = fminf(fmaxf(v, lo), hi);
+    // four positions per thread at a time: their loads first, then the arithmetic
+    for (int i0 = tid; i0 < Q * 32; i0 += 4 * 256) {
+      float raw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = i0 + 256 * u, t = idx >> 5, j = idx & 31;
+        raw[u] = (idx < Q * 32 && t < n && j < hw) ? to_f(dt[toff(d.sdt, b, t0 + t) + hg + j])
+                                                    : 0.f;
       }
-      tile[t][j] = v;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = i0 + 256 * u, t = idx >> 5, j = idx & 31;
+        if (idx >= Q * 32) break;
+        float v = raw[u];
+        if (t < n && j < hw) {
+          if (dt_bias) v += dt_bias[hg + j];
+          if (softplus) v = v <= 20.f ? log1pf(__expf(v)) : v;
+          if (do_clamp) v = fminf(fmaxf(v, lo), hi);
+        }
+        tile[t][j] = v;
+      }
     }
+    __syncthreads();
+    // the outputs leave with consecutive threads on consecutive positions of
+    // one head's row ([B, H, nc, Q]): dt first, then the cumsum, which the
+    // scans below write over the tile
+    auto row_of = [&](int j) { return (((int64_t)b * H + hg + j) * d.nchunks + c) << lq; };
+#pragma unroll 4
+    for (int idx = tid; idx < hw << lq; idx += 256)
+      dt_out[row_of(idx >> lq) + (idx & (Q - 1))] = tile[idx & (Q - 1)][idx >> lq];
     __syncthreads();
     for (int j = warp; j < hw; j += 8) {
       const float a = A[hg + j];
@@ -94,18 +114,18 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(
         if (lane >= off) incl += o;
       }
       const float excl = incl - run;
-      const int64_t base = (((int64_t)b * H + hg + j) * d.nchunks + c) * Q;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         if (e < E) {
           const int t = lane * E + e;
-          if (t < Q) {
-            cs_out[base + t] = excl + loc[e];
-            dt_out[base + t] = tile[t][j];
-          }
+          if (t < Q) tile[t][j] = excl + loc[e];
         }
       }
     }
+    __syncthreads();
+#pragma unroll 4
+    for (int idx = tid; idx < hw << lq; idx += 256)
+      cs_out[row_of(idx >> lq) + (idx & (Q - 1))] = tile[idx & (Q - 1)][idx >> lq];
     __syncthreads();
   }
 }
