@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   constexpr int kBufK = kS ? kQ * 128 + P * 128 : kBuf;   // bytes per buffer
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = aligned_smem(smem_raw);
-  __shared__ float cs_s[kQ], dt_s[kQ], sc_s[kQ];
+  __shared__ float cs_s[kQ], dt_s[kQ], sc_s[kQ], cf_s[kQ];
   __shared__ int sg_s[kQ];
   __shared__ uint64_t bars[2];
   __shared__ uint32_t tmem_base;
@@ -460,6 +460,9 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   const int n = (int)min((int64_t)kQ, d.seqlen - t0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t hc = (((int64_t)b * d.nheads + h) * d.nchunks + c) * kQ;
+  // the decay factors below (the decay-matrix build) need a cumsum that
+  // never rises and whose 16-token slices decay by at most e^60 each
+  bool mono_t = true;
   if (tid < kQ) {
     const int32_t* sp = seg ? seg + ((int64_t)b * d.nchunks + c) * kQ : nullptr;
     const float v = cs[hc + tid];
@@ -467,6 +470,8 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     dt_s[tid] = dtp[hc + tid];
     sg_s[tid] = sp ? sp[tid] : 0;
     sc_s[tid] = (sp == nullptr || sp[tid] == 0) ? ex2(v * kLog2e) : 0.f;   // keep_i e^cs_i
+    if (tid + 1 < kQ) mono_t = cs[hc + tid + 1] <= v;
+    mono_t = mono_t && v - cs[hc + (tid | (kK - 1))] <= 60.f;
   }
   if (tid == 0) {
     tc::mbar_init(&bars[0], 1);
@@ -480,8 +485,14 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  const bool mono = __syncthreads_and(mono_t) != 0;
   tc::fence_after_sync();
+  // and a chunk of one document
+  const bool factored = mono && sg_s[0] == sg_s[kQ - 1];
+  // column factor of position j against the last position e of its 16-token
+  // slice, e^(cs_e - cs_j) dt_j (at most dt_j; read only after the slice
+  // pipeline's first barrier)
+  if (tid < kQ) cf_s[tid] = ex2((cs_s[tid | (kK - 1)] - cs_s[tid]) * kLog2e) * dt_s[tid];
   const uint32_t tmem = tmem_base, tS = tmem, tY = kS ? tmem : tmem + 128;
   const float* Hp = prev + (((int64_t)b * d.nchunks + c) * d.nheads + h) * (int64_t)P * N;
   const float* xh = x + (int64_t)(h / d.xrep) * P;
@@ -506,8 +517,10 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   }
 
   // two register sets: slice s + 2 loads while slice s is stored / multiplied
+  // (with, for a token slice of a factored chunk, this row's factor rf)
   float4 ra0[2], rb0[2], ra1[2], rb1[2];
-  auto load_into = [&](int s, float4(&ra)[2], float4(&rb)[2]) {
+  float rf0 = 0.f, rf1 = 0.f;
+  auto load_into = [&](int s, float4(&ra)[2], float4(&rb)[2], float& rf) {
     if (s < s2) {   // C (both), B (C B^T) or H (inter-chunk)
       const int k0 = kK * (s < s1 ? s : s - s1);
 #pragma unroll
@@ -527,6 +540,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       }
     } else {            // x of tokens j0 .. j0 + 15 (16 lanes on the tokens)
       const int j0 = kK * (s - s2);
+      if (factored) rf = ex2((cs_s[i] - cs_s[j0 + kK - 1]) * kLog2e);
       const int j = j0 + jl;
       const bool tv = j < n;
       const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0));
@@ -547,7 +561,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       }
     }
   };
-  auto store_from = [&](int s, const float4(&ra)[2], const float4(&rb)[2]) {
+  auto store_from = [&](int s, const float4(&ra)[2], const float4(&rb)[2], float rf) {
     unsigned char* a = tA(s & 1);
     unsigned char* bt = tB(s & 1);
     if (s < s1) {
@@ -587,24 +601,39 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
                        :
                        : "memory");
         }
-        const float csi = cs_s[i];
-        const int sgi = sg_s[i];
+        if (factored) {
+          // e^(cs_i - cs_j) dt_j = e^(cs_i - cs_e) * e^(cs_e - cs_j) dt_j with e
+          // the slice's last position: the row factor rf here, the column
+          // factor on x (below); both within e^60 of 1 (rows past the
+          // chunk's end are not written out)
+          if (i >= j0 + kK - 1 + strict) {   // every column of the slice precedes row i
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = jb + u;
-          const bool valid = j + strict <= i && j < n && sg_s[j] == sgi;
-          m[u] = valid ? __uint_as_float(r[u]) * ex2((csi - cs_s[j]) * kLog2e) * dt_s[j] : 0.f;
+            for (int u = 0; u < 8; ++u) m[u] = __uint_as_float(r[u]) * rf;
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) m[u] = jb + u + strict <= i ? __uint_as_float(r[u]) * rf : 0.f;
+          }
+        } else {
+          const float csi = cs_s[i];
+          const int sgi = sg_s[i];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = jb + u;
+            const bool valid = j + strict <= i && j < n && sg_s[j] == sgi;
+            m[u] = valid ? __uint_as_float(r[u]) * ex2((csi - cs_s[j]) * kLog2e) * dt_s[j] : 0.f;
+          }
         }
       }
       put4(a, kQ, i, 8 * half, make_float4(m[0], m[1], m[2], m[3]));
       put4(a, kQ, i, 8 * half + 4, make_float4(m[4], m[5], m[6], m[7]));
+      const float xs = factored ? cf_s[j0 + jl] : 1.f;   // token j0 + jl's column factor
 #pragma unroll
       for (int u = 0; u < PQ; ++u) {
         const int r = 4 * (2 * warp + qh + 16 * u);
-        put1(bt, P, r, jl, rb[u].x);
-        put1(bt, P, r + 1, jl, rb[u].y);
-        put1(bt, P, r + 2, jl, rb[u].z);
-        put1(bt, P, r + 3, jl, rb[u].w);
+        put1(bt, P, r, jl, rb[u].x * xs);
+        put1(bt, P, r + 1, jl, rb[u].y * xs);
+        put1(bt, P, r + 2, jl, rb[u].z * xs);
+        put1(bt, P, r + 3, jl, rb[u].w * xs);
       }
     }
   };
@@ -615,15 +644,16 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       mma_slice(tY, tA(s & 1), tB(s & 1), P, idesc_tf32(kQ, P), s > s1);
   };
 
-  load_into(0, ra0, rb0);
-  if (nS > 1) load_into(1, ra1, rb1);
+  load_into(0, ra0, rb0, rf0);
+  if (nS > 1) load_into(1, ra1, rb1, rf1);
   bool run = true;
   for (int s = 0; run && s < nS; s += 2) {
-    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra0, rb0); },
-                        [&](int t) { load_into(t, ra0, rb0); }, issue);
+    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra0, rb0, rf0); },
+                        [&](int t) { load_into(t, ra0, rb0, rf0); }, issue);
     if (run && s + 1 < nS)
-      run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra1, rb1); },
-                          [&](int t) { load_into(t, ra1, rb1); }, issue);
+      run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
+                          [&](int t) { store_from(t, ra1, rb1, rf1); },
+                          [&](int t) { load_into(t, ra1, rb1, rf1); }, issue);
   }
   // epilogue: the output tile goes from TMEM through shared memory (rows of
   // P + 4 floats, over the tiles, which the completed MMAs no longer read),
