@@ -490,9 +490,9 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   // and a chunk of one document
   const bool factored = mono && sg_s[0] == sg_s[kQ - 1];
   // column factor of position j against the last position e of its 16-token
-  // slice, e^(cs_e - cs_j) dt_j (at most dt_j; read only after the slice
-  // pipeline's first barrier)
+  // slice, e^(cs_e - cs_j) dt_j (at most dt_j); the slices' loads read it
   if (tid < kQ) cf_s[tid] = ex2((cs_s[tid | (kK - 1)] - cs_s[tid]) * kLog2e) * dt_s[tid];
+  __syncthreads();
   const uint32_t tmem = tmem_base, tS = tmem, tY = kS ? tmem : tmem + 128;
   const float* Hp = prev + (((int64_t)b * d.nchunks + c) * d.nheads + h) * (int64_t)P * N;
   const float* xh = x + (int64_t)(h / d.xrep) * P;
@@ -507,6 +507,8 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   const int q = warp & 3, half = warp >> 2;
   const int i = 32 * q + lane;   // the row this thread builds M for and writes out
   const int jl = lane & 15, qh = lane >> 4;   // x^T: token in the slice, row-quad half
+  // per-row values the slices reuse, read once (not on a slice's chain)
+  const float cs_i = cs_s[i], sc_r0 = sc_s[sr], sc_r1 = sc_s[sr + 64];
   auto tA = [&](int u) { return base + u * kBufK; };
   auto tB = [&](int u) { return base + u * kBufK + kQ * 128; };
   // the row of the given C B^T this thread reads (kS)
@@ -517,10 +519,11 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   }
 
   // two register sets: slice s + 2 loads while slice s is stored / multiplied
-  // (with, for a token slice of a factored chunk, this row's factor rf)
+  // (with, for a token slice, f.x = this row's factor and f.y = the column
+  // factor of this lane's token, both 1 outside factored chunks)
   float4 ra0[2], rb0[2], ra1[2], rb1[2];
-  float rf0 = 0.f, rf1 = 0.f;
-  auto load_into = [&](int s, float4(&ra)[2], float4(&rb)[2], float& rf) {
+  float2 f0 = make_float2(1.f, 1.f), f1 = make_float2(1.f, 1.f);
+  auto load_into = [&](int s, float4(&ra)[2], float4(&rb)[2], float2& f) {
     if (s < s2) {   // C (both), B (C B^T) or H (inter-chunk)
       const int k0 = kK * (s < s1 ? s : s - s1);
 #pragma unroll
@@ -540,7 +543,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       }
     } else {            // x of tokens j0 .. j0 + 15 (16 lanes on the tokens)
       const int j0 = kK * (s - s2);
-      if (factored) rf = ex2((cs_s[i] - cs_s[j0 + kK - 1]) * kLog2e);
+      if (factored) f = make_float2(ex2((cs_i - cs_s[j0 + kK - 1]) * kLog2e), cf_s[j0 + jl]);
       const int j = j0 + jl;
       const bool tv = j < n;
       const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0));
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       }
     }
   };
-  auto store_from = [&](int s, const float4(&ra)[2], const float4(&rb)[2], float rf) {
+  auto store_from = [&](int s, const float4(&ra)[2], const float4(&rb)[2], float2 f) {
     unsigned char* a = tA(s & 1);
     unsigned char* bt = tB(s & 1);
     if (s < s1) {
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       }
     } else if (s < s2) {
 #pragma unroll
-      for (int u = 0; u < 2; ++u) put4(a, kQ, sr + 64 * u, sk, scale4(ra[u], sc_s[sr + 64 * u]));
+      for (int u = 0; u < 2; ++u) put4(a, kQ, sr + 64 * u, sk, scale4(ra[u], u ? sc_r1 : sc_r0));
 #pragma unroll
       for (int u = 0; u < PQ; ++u) put4(bt, P, sr + 64 * u, sk, rb[u]);
     } else {
@@ -603,15 +606,15 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
         }
         if (factored) {
           // e^(cs_i - cs_j) dt_j = e^(cs_i - cs_e) * e^(cs_e - cs_j) dt_j with e
-          // the slice's last position: the row factor rf here, the column
-          // factor on x (below); both within e^60 of 1 (rows past the
+          // the slice's last position: the row factor f.x here, the column
+          // factor f.y on x (below); both within e^60 of 1 (rows past the
           // chunk's end are not written out)
           if (i >= j0 + kK - 1 + strict) {   // every column of the slice precedes row i
 #pragma unroll
-            for (int u = 0; u < 8; ++u) m[u] = __uint_as_float(r[u]) * rf;
+            for (int u = 0; u < 8; ++u) m[u] = __uint_as_float(r[u]) * f.x;
           } else {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) m[u] = jb + u + strict <= i ? __uint_as_float(r[u]) * rf : 0.f;
+            for (int u = 0; u < 8; ++u) m[u] = jb + u + strict <= i ? __uint_as_float(r[u]) * f.x : 0.f;
           }
         } else {
           const float csi = cs_s[i];
@@ -626,7 +629,7 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       }
       put4(a, kQ, i, 8 * half, make_float4(m[0], m[1], m[2], m[3]));
       put4(a, kQ, i, 8 * half + 4, make_float4(m[4], m[5], m[6], m[7]));
-      const float xs = factored ? cf_s[j0 + jl] : 1.f;   // token j0 + jl's column factor
+      const float xs = f.y;   // token j0 + jl's column factor (1 outside factored chunks)
 #pragma unroll
       for (int u = 0; u < PQ; ++u) {
         const int r = 4 * (2 * warp + qh + 16 * u);
@@ -644,16 +647,16 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
       mma_slice(tY, tA(s & 1), tB(s & 1), P, idesc_tf32(kQ, P), s > s1);
   };
 
-  load_into(0, ra0, rb0, rf0);
-  if (nS > 1) load_into(1, ra1, rb1, rf1);
+  load_into(0, ra0, rb0, f0);
+  if (nS > 1) load_into(1, ra1, rb1, f1);
   bool run = true;
   for (int s = 0; run && s < nS; s += 2) {
-    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra0, rb0, rf0); },
-                        [&](int t) { load_into(t, ra0, rb0, rf0); }, issue);
+    run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, ra0, rb0, f0); },
+                        [&](int t) { load_into(t, ra0, rb0, f0); }, issue);
     if (run && s + 1 < nS)
       run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
-                          [&](int t) { store_from(t, ra1, rb1, rf1); },
-                          [&](int t) { load_into(t, ra1, rb1, rf1); }, issue);
+                          [&](int t) { store_from(t, ra1, rb1, f1); },
+                          [&](int t) { load_into(t, ra1, rb1, f1); }, issue);
   }
   // epilogue: the output tile goes from TMEM through shared memory (rows of
   // P + 4 floats, over the tiles, which the completed MMAs no longer read),

@@ -24,6 +24,8 @@ SHAPES = [
     ("p128_n128", 128, 128),
     ("p64_n64", 64, 64),
     ("p64_n96", 64, 96),
+    # two dstate slices: the first token slice loads in the pipeline's first step
+    ("p64_n32", 64, 32),
 ]
 
 CASES = [
