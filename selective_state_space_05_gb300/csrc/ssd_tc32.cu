@@ -236,8 +236,9 @@ __global__ void __launch_bounds__(256) group_tiles_kernel(const float* __restric
 // (group_tiles_kernel); the weights w_j then go on the other, per-head
 // operand (the sum over j of w_j x_j B_j^T does not care which factor
 // carries them), the only one staged here.
+// (three CTAs per SM, as its shared memory allows: up to 85 registers)
 template <int P, int N, bool kG>
-__global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
+__global__ void __launch_bounds__(256, 3) chunk_state_tc32_kernel(
     const float* __restrict__ x, const float* __restrict__ Bm, const float* __restrict__ dtp,
     const float* __restrict__ cs, const int32_t* __restrict__ seg, Dims d,
     float* __restrict__ states, Limits lim, const float* __restrict__ Tg) {
@@ -290,20 +291,22 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
 
   const int nS = (n + kK - 1) / kK;
   // two register sets: slice s + 2 loads while slice s is stored / multiplied
+  // (with the weight w of this lane's token, read from shared memory then)
   float4 rx0[XQ], rb0[BQ], rx1[XQ], rb1[BQ];
-  auto load_into = [&](int s, float4(&rx)[XQ], float4(&rb)[BQ]) {
+  float w0 = 0.f, w1 = 0.f;
+  auto load_into = [&](int s, float4(&rx)[XQ], float4(&rb)[BQ], float& w) {
     const int j = kK * s + jl;
     const bool tv = j < n;
+    w = tv ? wsh[j] : 0.f;
     const int64_t tx = toff(d.sx, b, t0 + (tv ? j : 0)), tb = toff(d.sB, b, t0 + (tv ? j : 0));
 #pragma unroll
     for (int u = 0; u < XQ; ++u) rx[u] = tv ? ld4(xh + tx + 4 * (2 * warp + qh + 16 * u)) : zero4;
 #pragma unroll
     for (int u = 0; u < BQ; ++u) rb[u] = tv ? ld4(bg + tb + 4 * (2 * warp + qh + 16 * u)) : zero4;
   };
-  auto store_from = [&](int s, const float4(&rx)[XQ], const float4(&rb)[BQ]) {
+  auto store_from = [&](int s, const float4(&rx)[XQ], const float4(&rb)[BQ], float wj) {
     unsigned char* tX = kT ? tB(s & 1) : tA(s & 1);    // (w o x)^T: P rows
     unsigned char* tBt = kT ? tA(s & 1) : tB(s & 1);   // B^T: N rows
-    const float wj = (kK * s + jl < n) ? wsh[kK * s + jl] : 0.f;
 #pragma unroll
     for (int u = 0; u < XQ; ++u) {
       const int r = 4 * (2 * warp + qh + 16 * u);
@@ -333,23 +336,23 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
     tg = Tg + ((int64_t)bc * tgroups + gi) * (kQ / kK) * kTileFloats;
   }
   float4 rt0[4], rv0[VQ], rt1[4], rv1[VQ];
-  auto gload_into = [&](int s, float4(&rt)[4], float4(&rv)[VQ]) {
+  auto gload_into = [&](int s, float4(&rt)[4], float4(&rv)[VQ], float& w) {
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       rt[u] = ld4(tg + (int64_t)s * kTileFloats + 4 * (tid + 256 * u));
     const int j = kK * s + jl;
     const bool tv = j < n;
+    w = tv ? wsh[j] : 0.f;
     const float* src = kT ? xh + toff(d.sx, b, t0 + (tv ? j : 0))
                           : Bm + toff(d.sB, b, t0 + (tv ? j : 0)) + (int64_t)g * N;
 #pragma unroll
     for (int u = 0; u < VQ; ++u) rv[u] = tv ? ld4(src + 4 * (2 * warp + qh + 16 * u)) : zero4;
   };
-  auto gstore_from = [&](int s, const float4(&rt)[4], const float4(&rv)[VQ]) {
+  auto gstore_from = [&](int s, const float4(&rt)[4], const float4(&rv)[VQ], float wj) {
     float4* a = reinterpret_cast<float4*>(tA(s & 1));
 #pragma unroll
     for (int u = 0; u < 4; ++u) a[tid + 256 * u] = rt[u];
     unsigned char* bt = tB(s & 1);
-    const float wj = (kK * s + jl < n) ? wsh[kK * s + jl] : 0.f;
 #pragma unroll
     for (int u = 0; u < VQ; ++u) {
       const int r = 4 * (2 * warp + qh + 16 * u);
@@ -362,27 +365,28 @@ __global__ void __launch_bounds__(256) chunk_state_tc32_kernel(
 
   bool run = true;
   if constexpr (kG) {
-    gload_into(0, rt0, rv0);
-    if (nS > 1) gload_into(1, rt1, rv1);
+    gload_into(0, rt0, rv0, w0);
+    if (nS > 1) gload_into(1, rt1, rv1, w1);
     for (int s = 0; run && s < nS; s += 2) {
       run = pipeline_step(s, nS, bars, tid, ok_all, lim,
-                          [&](int t) { gstore_from(t, rt0, rv0); },
-                          [&](int t) { gload_into(t, rt0, rv0); }, issue);
+                          [&](int t) { gstore_from(t, rt0, rv0, w0); },
+                          [&](int t) { gload_into(t, rt0, rv0, w0); }, issue);
       if (run && s + 1 < nS)
         run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
-                            [&](int t) { gstore_from(t, rt1, rv1); },
-                            [&](int t) { gload_into(t, rt1, rv1); }, issue);
+                            [&](int t) { gstore_from(t, rt1, rv1, w1); },
+                            [&](int t) { gload_into(t, rt1, rv1, w1); }, issue);
     }
   } else {
-    load_into(0, rx0, rb0);
-    if (nS > 1) load_into(1, rx1, rb1);
+    load_into(0, rx0, rb0, w0);
+    if (nS > 1) load_into(1, rx1, rb1, w1);
     for (int s = 0; run && s < nS; s += 2) {
-      run = pipeline_step(s, nS, bars, tid, ok_all, lim, [&](int t) { store_from(t, rx0, rb0); },
-                          [&](int t) { load_into(t, rx0, rb0); }, issue);
+      run = pipeline_step(s, nS, bars, tid, ok_all, lim,
+                          [&](int t) { store_from(t, rx0, rb0, w0); },
+                          [&](int t) { load_into(t, rx0, rb0, w0); }, issue);
       if (run && s + 1 < nS)
         run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
-                            [&](int t) { store_from(t, rx1, rb1); },
-                            [&](int t) { load_into(t, rx1, rb1); }, issue);
+                            [&](int t) { store_from(t, rx1, rb1, w1); },
+                            [&](int t) { load_into(t, rx1, rb1, w1); }, issue);
     }
   }
   if (run) run = pipeline_drain(nS, bars, ok_all, lim);
