@@ -438,6 +438,11 @@ __global__ void __launch_bounds__(256, 3) chunk_state_tc32_kernel(
 // Element (i, j) of the chunk's C B^T is Sg[cf][ri][rj], (cf, ri, rj) =
 // (c, i, j), or with srev (nc - 1 - c, 127 - i, 127 - j): the time-reversed
 // scans of the backward, whose chunks are the forward chunks reversed.
+// In a chunk of one document whose cumsum never rises (and whose 16-token
+// slices decay by at most e^60 each), M's decay is split at each slice's
+// last position into a row factor and a column factor carried by x, so that
+// building M takes no per-element exp2 and nothing it needs is read after
+// the slice's wait.
 // ---------------------------------------------------------------------------
 template <int P, bool kXZ, bool kS>
 __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
