@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [
     # (id, headdim, dstate): the first three take both stages on tensor
-    # cores, the last two chunk_scan only
+    # cores, the others chunk_scan only
     ("p64_n128", 64, 128),
     ("p128_n64", 128, 64),
     ("p128_n128", 128, 128),
@@ -26,6 +26,10 @@ SHAPES = [
     ("p64_n96", 64, 96),
     # two dstate slices: the first token slice loads in the pipeline's first step
     ("p64_n32", 64, 32),
+    # the largest dstate chunk_scan takes: 16 slices of C B^T and of the
+    # inter-chunk term
+    ("p64_n256", 64, 256),
+    ("p128_n256", 128, 256),
 ]
 
 CASES = [
@@ -80,10 +84,15 @@ def test_forward_fp32_chunk128_strided_views():
     assert_close(f.double().cpu().numpy(), rf, TOL["f32"], "final")
 
 
-@pytest.mark.parametrize("shape", SHAPES[:3], ids=[s[0] for s in SHAPES[:3]])
+# the stage exports compute C B^T inside chunk_scan (dstate 256: 40 slices)
+STAGE_SHAPES = SHAPES[:3] + [("p64_n256", 64, 256)]
+
+
+@pytest.mark.parametrize("shape", STAGE_SHAPES, ids=[s[0] for s in STAGE_SHAPES])
 def test_stage_exports_fp32_chunk128_match_chunked_oracle(shape):
     """ssd_chunk_state and ssd_chunk_scan at chunk 128 in fp32 (the
-    tensor-core kernels) against the chunked oracle's intermediates."""
+    tensor-core kernels; chunk_state on the SIMT kernel for dstate 256)
+    against the chunked oracle's intermediates."""
     import selective_state_space_05_gb300 as ssd
     _, P, N = shape
     Q = 128
