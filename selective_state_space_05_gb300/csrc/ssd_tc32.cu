@@ -428,6 +428,157 @@ __global__ void __launch_bounds__(256, 3) chunk_state_tc32_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// chunk_state for two heads at once where the per-group operand is the
+// 128-row one and comes pre-split (kG above) and the per-head operand has 64
+// rows (headdim 64 with dstate 128, or dstate 64 with headdim 128): the two
+// heads' weighted operands stack into one 128-row B tile, so that every MMA
+// has N = 128 (about the time of an N = 64 one, for twice the work) and the
+// group tile is copied once for both.  One CTA per (batch x chunk, head
+// pair), 256 threads; the pair's heads share the per-group operand.
+// Accumulator columns 64 e .. 64 e + 63 belong to head h0 + e.
+// ---------------------------------------------------------------------------
+template <int P, int N>
+__global__ void __launch_bounds__(256, 3) chunk_state_pair_tc32_kernel(
+    const float* __restrict__ x, const float* __restrict__ Bm, const float* __restrict__ dtp,
+    const float* __restrict__ cs, const int32_t* __restrict__ seg, Dims d,
+    float* __restrict__ states, Limits lim, const float* __restrict__ Tg) {
+  constexpr bool kT = (N == 128);
+  static_assert((kT ? P : N) == 64, "two 64-row per-head operands fill the 128-row B tile");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = aligned_smem(smem_raw);
+  __shared__ float wsh[2][kQ];
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int ok_all;
+
+  const int bc = blockIdx.x, h0 = 2 * blockIdx.y;
+  const int b = bc / d.nchunks, c = bc % d.nchunks;
+  const int64_t t0 = (int64_t)c * kQ;
+  const int n = (int)min((int64_t)kQ, d.seqlen - t0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {   // thread (head e, position t): the weight w_t of head h0 + e
+    const int e = tid / kQ, t = tid % kQ;
+    const int64_t hc = (((int64_t)b * d.nheads + h0 + e) * d.nchunks + c) * kQ;
+    const int32_t* sp = seg ? seg + ((int64_t)b * d.nchunks + c) * kQ : nullptr;
+    float w = 0.f;
+    if (t < n && (sp == nullptr || sp[t] == sp[kQ - 1]))
+      w = ex2((cs[hc + kQ - 1] - cs[hc + t]) * kLog2e) * dtp[hc + t];
+    wsh[e][t] = w;
+  }
+  if (tid == 0) {
+    tc::mbar_init(&bars[0], 1);
+    tc::mbar_init(&bars[1], 1);
+    tc::mbar_fence_init();
+    ok_all = 1;
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 128);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  constexpr uint32_t idesc = idesc_tf32(kQ, kQ);
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int hpg = d.nheads / d.ngroups;
+  // the per-head operand of head h0 + e at token t: x (kT), else B (whose
+  // groups are the heads there)
+  auto head_row = [&](int e, int64_t t) -> const float* {
+    return kT ? x + toff(d.sx, b, t) + (int64_t)((h0 + e) / d.xrep) * P
+              : Bm + toff(d.sB, b, t) + (int64_t)((h0 + e) / hpg) * N;
+  };
+  const int tgroups = kT ? d.ngroups : d.nheads / d.xrep;
+  const int gi = kT ? h0 / hpg : h0 / d.xrep;
+  const float* tg = Tg + ((int64_t)bc * tgroups + gi) * (kQ / kK) * kTileFloats;
+  const int jl = lane & 15, qh = lane >> 4;   // token in the slice, row-quad half
+  const int r0 = 4 * (2 * warp + qh);         // this thread's row quad of a head's 64 rows
+  auto tA = [&](int u) { return base + u * kBuf; };
+  auto tB = [&](int u) { return base + u * kBuf + kQ * 128; };
+  const int nS = (n + kK - 1) / kK;
+  // two register sets: slice s + 2 loads while slice s is stored / multiplied
+  float4 rt0[4], rv0[2], rt1[4], rv1[2];
+  float2 w0 = make_float2(0.f, 0.f), w1 = make_float2(0.f, 0.f);
+  auto load_into = [&](int s, float4(&rt)[4], float4(&rv)[2], float2& w) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      rt[u] = ld4(tg + (int64_t)s * kTileFloats + 4 * (tid + 256 * u));
+    const int j = kK * s + jl;
+    const bool tv = j < n;
+    const int64_t t = t0 + (tv ? j : 0);
+    w = tv ? make_float2(wsh[0][j], wsh[1][j]) : make_float2(0.f, 0.f);
+    rv[0] = tv ? ld4(head_row(0, t) + r0) : zero4;
+    rv[1] = tv ? ld4(head_row(1, t) + r0) : zero4;
+  };
+  auto store_from = [&](int s, const float4(&rt)[4], const float4(&rv)[2], float2 w) {
+    float4* a = reinterpret_cast<float4*>(tA(s & 1));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a[tid + 256 * u] = rt[u];
+    unsigned char* bt = tB(s & 1);   // head e's rows at 64 e
+    put1(bt, kQ, r0, jl, rv[0].x * w.x);
+    put1(bt, kQ, r0 + 1, jl, rv[0].y * w.x);
+    put1(bt, kQ, r0 + 2, jl, rv[0].z * w.x);
+    put1(bt, kQ, r0 + 3, jl, rv[0].w * w.x);
+    put1(bt, kQ, 64 + r0, jl, rv[1].x * w.y);
+    put1(bt, kQ, 64 + r0 + 1, jl, rv[1].y * w.y);
+    put1(bt, kQ, 64 + r0 + 2, jl, rv[1].z * w.y);
+    put1(bt, kQ, 64 + r0 + 3, jl, rv[1].w * w.y);
+  };
+  auto issue = [&](int s) { mma_slice(tmem, tA(s & 1), tB(s & 1), kQ, idesc, s > 0); };
+
+  bool run = true;
+  load_into(0, rt0, rv0, w0);
+  if (nS > 1) load_into(1, rt1, rv1, w1);
+  for (int s = 0; run && s < nS; s += 2) {
+    run = pipeline_step(s, nS, bars, tid, ok_all, lim,
+                        [&](int t) { store_from(t, rt0, rv0, w0); },
+                        [&](int t) { load_into(t, rt0, rv0, w0); }, issue);
+    if (run && s + 1 < nS)
+      run = pipeline_step(s + 1, nS, bars, tid, ok_all, lim,
+                          [&](int t) { store_from(t, rt1, rv1, w1); },
+                          [&](int t) { load_into(t, rt1, rv1, w1); }, issue);
+  }
+  if (run) run = pipeline_drain(nS, bars, ok_all, lim);
+  if (run) {
+    // each warp: TMEM lane quarter warp % 4, the 64 columns of head h0 + half
+    const int q = warp & 3, half = warp >> 2;
+    const int row = 32 * q + lane;   // n (kT) or p
+    float* sp = states + (((int64_t)b * d.nchunks + c) * d.nheads + h0 + half) * (int64_t)P * N;
+    float* ys = reinterpret_cast<float*>(base);
+    constexpr int YS = kQ + 4;   // !kT: rows p of both heads' n, 132 floats
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t r[32];
+      tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 64 * half + c0, r);
+      tc::tmem_ld_wait_regs(r);
+      if (kT) {   // S^T of head h0 + half: lanes on consecutive n
+#pragma unroll
+        for (int u = 0; u < 32; ++u) sp[(int64_t)(c0 + u) * N + row] = __uint_as_float(r[u]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; u += 4)
+          *reinterpret_cast<float4*>(ys + row * YS + 64 * half + c0 + u) =
+              make_float4(__uint_as_float(r[u]), __uint_as_float(r[u + 1]),
+                          __uint_as_float(r[u + 2]), __uint_as_float(r[u + 3]));
+      }
+    }
+    if (!kT) {   // then out with consecutive threads on consecutive n, head by head
+      __syncthreads();
+      for (int e = tid; e < 2 * P * (N / 4); e += 256) {
+        const int hh = e / (P * (N / 4)), rem = e % (P * (N / 4));
+        const int pr = rem / (N / 4), c4 = 4 * (rem % (N / 4));
+        float* so = states + (((int64_t)b * d.nchunks + c) * d.nheads + h0 + hh) * (int64_t)P * N;
+        *reinterpret_cast<float4*>(so + (int64_t)pr * N + c4) =
+            *reinterpret_cast<const float4*>(ys + pr * YS + hh * N + c4);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+// ---------------------------------------------------------------------------
 // chunk_scan: one CTA per (batch x chunk, head), 256 threads; TMEM columns
 // [0, 128) hold C B^T (rows i, columns j), [128, 128 + P) the output.
 // Slices: N/16 of C B^T (K = dstate), N/16 of the inter-chunk term, then one
@@ -677,15 +828,16 @@ __global__ void __launch_bounds__(256, 2) chunk_scan_tc32_kernel(
   constexpr int kBatch = kXZ ? 8 : 1;
   float4 xv[kBatch], zv[kBatch];
   auto load_batch = [&](int bt) {
-    if (!kXZ) return;
+    if constexpr (kXZ) {
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int e = tid + 256 * (bt * kBatch + u);
-      const int row = e / (P / 4), p = 4 * (e % (P / 4));
-      const bool ok_row = row < n;
-      xv[u] = (D && ok_row) ? ld4(x + toff(d.sx, b, t0 + row) + (int64_t)(h / d.xrep) * P + p)
-                            : zero4;
-      zv[u] = (z && ok_row) ? ld4(z + toff(d.sz, b, t0 + row) + (int64_t)h * P + p) : zero4;
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = tid + 256 * (bt * kBatch + u);
+        const int row = e / (P / 4), p = 4 * (e % (P / 4));
+        const bool ok_row = row < n;
+        xv[u] = (D && ok_row) ? ld4(x + toff(d.sx, b, t0 + row) + (int64_t)(h / d.xrep) * P + p)
+                              : zero4;
+        zv[u] = (z && ok_row) ? ld4(z + toff(d.sz, b, t0 + row) + (int64_t)h * P + p) : zero4;
+      }
     }
   };
   if (run) load_batch(0);
@@ -901,6 +1053,28 @@ cudaError_t launch_chunk_state_tc32(const float* x, const float* B, const float*
                                     const float* cs, const int32_t* seg, const Dims& d,
                                     float* states, cudaStream_t st, const float* Tg) {
   using namespace tc32;
+  // two heads per CTA where the per-group operand comes pre-split, the
+  // per-head one has 64 rows and the two heads of a pair share the former
+  const bool kT = d.dstate == 128;
+  const bool pair = Tg != nullptr && d.nheads % 2 == 0 &&
+                    ((kT && d.headdim == 64 && (d.nheads / d.ngroups) % 2 == 0) ||
+                     (!kT && d.headdim == 128 && d.dstate == 64 && d.xrep % 2 == 0));
+  if (pair) {
+    dim3 g2((unsigned)(d.batch * d.nchunks), (unsigned)(d.nheads / 2));
+    if (kT) {
+      static cudaError_t prep = prepare(chunk_state_pair_tc32_kernel<64, 128>, kSmem);
+      if (prep != cudaSuccess) return prep;
+      chunk_state_pair_tc32_kernel<64, 128><<<g2, 256, kSmem, st>>>(x, B, dtp, cs, seg, d, states,
+                                                                   limits(), Tg);
+    } else {   // the epilogue's rows of both heads' columns need more than the two buffers
+      constexpr size_t smem = 1024 + kQ * (kQ + 4) * 4;
+      static cudaError_t prep = prepare(chunk_state_pair_tc32_kernel<128, 64>, smem);
+      if (prep != cudaSuccess) return prep;
+      chunk_state_pair_tc32_kernel<128, 64><<<g2, 256, smem, st>>>(x, B, dtp, cs, seg, d, states,
+                                                                  limits(), Tg);
+    }
+    return cudaGetLastError();
+  }
   dim3 grid((unsigned)(d.batch * d.nchunks), (unsigned)d.nheads);
 #define SSD_TC32_STATE(P, N, G_)                                                                \
   if (d.headdim == P && d.dstate == N && (Tg != nullptr) == G_) {                               \
