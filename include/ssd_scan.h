@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 2
+#define SSD_ABI_VERSION 3
 
 typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype_t;
 
@@ -66,7 +66,12 @@ enum {
  *   2  adds SSD_ERR_TIMEOUT, ssd_scan_status, ssd_scan_fwd_strided, the
  *      block calls ssd_causal_conv1d and ssd_group_rmsnorm,
  *      ssd_decode_step and the backward ssd_scan_bwd and ssd_scan_bwd_ex
- *      (with their workspace queries); every version-1 symbol is unchanged */
+ *      (with their workspace queries); every version-1 symbol is unchanged
+ *   3  adds ssd_scan_workspace_bytes_min: bf16 shapes outside the fused
+ *      kernel run the fp32 tensor-core stages on fp32 copies when the
+ *      workspace holds them (ssd_scan_workspace_bytes counts the copies; a
+ *      workspace of the version-2 size still works, on the stage kernels);
+ *      every version-2 symbol is unchanged */
 int ssd_abi_version(void);
 
 /* Message for the last error returned on the calling host thread ("" if
@@ -106,10 +111,28 @@ int ssd_scan_status(int reset, void *stream);
  * chunks and hands it on between segments; the segment length is chosen from
  * the shape (the longest that leaves every SM about twelve work items) unless
  * the environment variable SSD_FUSED_SEGMENT_CHUNKS gives one (a tuning /
- * test override; results agree to rounding for every length). */
+ * test override; results agree to rounding for every length).
+ *
+ * fp32 inputs with headdim 64 or 128, dstate a multiple of 32 up to 256 and
+ * chunk_size 128 or 256 run chunk_state / chunk_scan on the tensor cores
+ * (3xTF32, 128-token stages; the workspace then also holds C B^T per
+ * (batch, chunk, group) and B pre-split for the tensor cores).  bf16 inputs
+ * of those shapes that the fused kernel does not take run the same way on
+ * fp32 copies of x, B, C, z and out in the workspace (the values exactly,
+ * out rounded to bf16 once); the size returned here includes the copies. */
 size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads,
                                 int headdim, int dstate, int ngroups,
                                 int chunk_size, ssd_dtype_t dtype);
+
+/* The least workspace ssd_scan_fwd (and ssd_scan_fwd_strided) accepts for
+ * these sizes: ssd_scan_workspace_bytes without the fp32 copies above.  With
+ * a workspace too small for the copies, those bf16 shapes run the bf16 stage
+ * kernels instead (slower; the result agrees to rounding).  0 on bad sizes.
+ * ssd_scan_fwd_noalloc's static scratch is checked against this size.
+ * (ABI version 3.) */
+size_t ssd_scan_workspace_bytes_min(int64_t batch, int64_t seqlen, int nheads,
+                                    int headdim, int dstate, int ngroups,
+                                    int chunk_size, ssd_dtype_t dtype);
 
 /*
  * Full SSD chunked-scan forward.

@@ -44,6 +44,7 @@ SIGNATURES = {
                                   _vp, _vp, _st, _vp, _vp, _i64, _i64, _i, _i, _i, _i, _i, _i,
                                   _vp, _vp, _vp, _sz, _vp]),
     "ssd_scan_workspace_bytes": (_sz, [_i64, _i64, _i, _i, _i, _i, _i, _i]),
+    "ssd_scan_workspace_bytes_min": (_sz, [_i64, _i64, _i, _i, _i, _i, _i, _i]),
     "ssd_scan_bwd_workspace_bytes": (_sz, [_i64, _i64, _i, _i, _i, _i, _i]),
     "ssd_scan_bwd_ex_workspace_bytes": (_sz, [_i64, _i64, _i, _i, _i, _i, _i, _i]),
     "ssd_scan_bwd_ex": (_i, [_vp, _vp, _vp, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,

@@ -2,6 +2,8 @@
 // workspace carving and the launch sequence.  Declared in include/ssd_scan.h.
 #include <math.h>
 #include <stdarg.h>
+
+#include <algorithm>
 #include <stdio.h>
 #include <string.h>
 
@@ -130,6 +132,104 @@ Workspace carve(const ssd::Dims& d, void* base, bool with_cb = false) {
 
 int do_clamp_of(float lo, float hi) { return !(lo == 0.f && isinf(hi) && hi > 0.f); }
 
+// bf16 shapes outside the fused kernel that the fp32 tensor-core stages take
+// run there, on fp32 copies of x, B, C and z (exact) made in the workspace,
+// with out computed in fp32 and rounded to bf16 once (d: the caller's sizes).
+bool bf16_via_fp32(const ssd::Dims& d) {
+  return !ssd::fused_eligible(d, true) && (d.headdim == 64 || d.headdim == 128) &&
+         d.dstate % 32 == 0 && d.dstate <= 256 && (d.chunk == 128 || d.chunk == 256);
+}
+
+// The fp32 copies, after the workspace regions that end at `end`: x, z and
+// out [B, L, H, P], B and C [B, L, G, N], dense.
+struct Copies {
+  float *x, *z, *B, *C, *out;
+  size_t bytes;
+};
+Copies copies_carve(const ssd::Dims& d, size_t end, void* base) {
+  const size_t xs = (size_t)d.batch * d.seqlen * d.nheads * d.headdim;
+  const size_t bs = (size_t)d.batch * d.seqlen * d.ngroups * d.dstate;
+  char* p = static_cast<char*>(base);
+  size_t off = round_up(end, 256);
+  Copies c;
+  auto take = [&](size_t elems) {
+    float* at = reinterpret_cast<float*>(p + off);
+    off = round_up(off + elems * sizeof(float), 256);
+    return at;
+  };
+  c.x = take(xs);
+  c.z = take(xs);
+  c.out = take(xs);
+  c.B = take(bs);
+  c.C = take(bs);
+  c.bytes = off;
+  return c;
+}
+
+// bf16 rows of `row` elements, one per (batch, token) with token strides s
+// (elements), into dense fp32; kVec: 8 elements per step (16-byte loads,
+// strides and row multiples of 8).
+template <bool kVec>
+__global__ void __launch_bounds__(256) bf16_rows_to_f32_kernel(const __nv_bfloat16* __restrict__ src,
+                                                               ssd::TokStride s, int64_t L, int row,
+                                                               int64_t rows, float* __restrict__ dst) {
+  constexpr int V = kVec ? 8 : 1;
+  const int per = row / V;
+  const int64_t total = rows * per;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per, b = r / L, t = r % L;
+    const int k = (int)(i % per) * V;
+    const __nv_bfloat16* sp = src + ssd::toff(s, b, t) + k;
+    float* dp = dst + r * row + k;
+    if constexpr (kVec) {
+      const uint4 v = *reinterpret_cast<const uint4*>(sp);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float f[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        f[2 * u] = __uint_as_float(w[u] << 16);
+        f[2 * u + 1] = __uint_as_float(w[u] & 0xFFFF0000u);
+      }
+      *reinterpret_cast<float4*>(dp) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(dp + 4) = make_float4(f[4], f[5], f[6], f[7]);
+    } else {
+      *dp = __bfloat162float(*sp);
+    }
+  }
+}
+
+// dense fp32 -> dense bf16 (round to nearest even), 8 elements per step
+__global__ void __launch_bounds__(256) f32_to_bf16_rows_kernel(const float* __restrict__ src,
+                                                               int64_t n8, __nv_bfloat16* __restrict__ dst) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = *reinterpret_cast<const float4*>(src + 8 * i);
+    const float4 c = *reinterpret_cast<const float4*>(src + 8 * i + 4);
+    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                           __floats2bfloat162_rn(c.x, c.y), __floats2bfloat162_rn(c.z, c.w)};
+    *reinterpret_cast<uint4*>(dst + 8 * i) = *reinterpret_cast<const uint4*>(o);
+  }
+}
+
+unsigned grid_for(int64_t n) {
+  return (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)152 * 64);
+}
+
+// One bf16 tensor of rows (batch, token) into its dense fp32 copy.
+cudaError_t rows_to_f32(const void* src, ssd::TokStride s, const ssd::Dims& d, int row, float* dst,
+                        cudaStream_t st) {
+  const int64_t rows = d.batch * d.seqlen;
+  const bool vec = row % 8 == 0 && s.b % 8 == 0 && s.t % 8 == 0;
+  if (vec)
+    bf16_rows_to_f32_kernel<true><<<grid_for(rows * (row / 8)), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(src), s, d.seqlen, row, rows, dst);
+  else
+    bf16_rows_to_f32_kernel<false><<<grid_for(rows * row), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(src), s, d.seqlen, row, rows, dst);
+  return cudaGetLastError();
+}
+
 // The chunk length the forward's stages run at.  fp32 at chunk 256 runs them
 // at 128 tokens when the headdim / dstate are ones the fp32 tensor-core
 // stages take: the scan does not depend on the chunk length (only its
@@ -137,7 +237,8 @@ int do_clamp_of(float lo, float hi) { return !(lo == 0.f && isinf(hi) && hi > 0.
 ssd::Dims fwd_dims(const ssd::Dims& d, ssd_dtype_t dtype) {
   ssd::Dims e = d;
   const bool tc = (d.headdim == 64 || d.headdim == 128) && d.dstate % 32 == 0 && d.dstate <= 256;
-  if (dtype == SSD_DTYPE_F32 && d.chunk == 256 && tc) {
+  const bool f32 = dtype == SSD_DTYPE_F32 || (dtype == SSD_DTYPE_BF16 && bf16_via_fp32(d));
+  if (f32 && d.chunk == 256 && tc) {
     e.chunk = 128;
     e.nchunks = (int)((d.seqlen + 127) / 128);
   }
@@ -149,6 +250,21 @@ ssd::Dims fwd_dims(const ssd::Dims& d, ssd_dtype_t dtype) {
 namespace ssd {
 // Records an error message for ssd_last_error() from another translation unit.
 int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+// The forward's workspace without the fp32 copies of bf16 inputs (the least
+// a call takes: with less room for the copies it runs the bf16 stage
+// kernels); 0 for invalid sizes.
+size_t fwd_workspace_bytes_least(int64_t batch, int64_t seqlen, int nheads, int headdim,
+                                 int dstate, int ngroups, int chunk_size, int dtype_in) {
+  const ssd_dtype_t dtype = static_cast<ssd_dtype_t>(dtype_in);
+  ssd::Dims d;
+  if (check_dtype(dtype) != SSD_OK) return 0;
+  if (check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d) != SSD_OK)
+    return 0;
+  if (dtype == SSD_DTYPE_BF16) return carve(d, nullptr, false).bytes;
+  const ssd::Dims e = fwd_dims(d, dtype);
+  return carve(e, nullptr, fp32_shared_cb(e)).bytes;
+}
 }  // namespace ssd
 
 extern "C" {
@@ -182,7 +298,9 @@ size_t ssd_scan_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int h
   if (check_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, true, &d) != SSD_OK)
     return 0;
   const ssd::Dims e = fwd_dims(d, dtype);
-  return carve(e, nullptr, dtype == SSD_DTYPE_F32 && fp32_shared_cb(e)).bytes;
+  const bool copies = dtype == SSD_DTYPE_BF16 && bf16_via_fp32(d);
+  const size_t base = carve(e, nullptr, (dtype == SSD_DTYPE_F32 || copies) && fp32_shared_cb(e)).bytes;
+  return copies ? copies_carve(e, base, nullptr).bytes : base;
 }
 
 int ssd_dt_cumsum(const void* dt, const float* dt_bias, int dt_softplus, float lo, float hi,
@@ -297,6 +415,12 @@ int ssd_chunk_scan(const void* x, const void* B, const void* C, const float* dt_
   return e == cudaSuccess ? SSD_OK : cuda_fail(e, "chunk_scan launch");
 }
 
+size_t ssd_scan_workspace_bytes_min(int64_t batch, int64_t seqlen, int nheads, int headdim,
+                                    int dstate, int ngroups, int chunk_size, ssd_dtype_t dtype) {
+  return ssd::fwd_workspace_bytes_least(batch, seqlen, nheads, headdim, dstate, ngroups,
+                                        chunk_size, dtype);
+}
+
 int ssd_chunk_fused(const void* x, const void* B, const void* C, const float* dt_out,
                     const float* dA_cumsum, const int32_t* chunk_seg, const float* D,
                     const void* z, const float* initial_states, int64_t batch, int64_t seqlen,
@@ -347,9 +471,23 @@ int scan_fwd_run(const ssd::Dims& d_in, const void* x, const void* dt, const flo
                  void* out, float* final_states, void* workspace, size_t workspace_bytes,
                  void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const ssd::Dims d = fwd_dims(d_in, dtype);
-  const bool with_cb = dtype == SSD_DTYPE_F32 && fp32_shared_cb(d);
-  const size_t need = carve(d, nullptr, with_cb).bytes;
+  // bf16 through the fp32 stages on fp32 copies, unless a caller's workspace
+  // has no room for the copies (the bf16 stage kernels then run)
+  bool copies = dtype == SSD_DTYPE_BF16 && bf16_via_fp32(d_in);
+  ssd::Dims d = fwd_dims(d_in, dtype);
+  bool with_cb = (dtype == SSD_DTYPE_F32 || copies) && fp32_shared_cb(d);
+  size_t need = carve(d, nullptr, with_cb).bytes;
+  if (copies) {
+    const size_t with_copies = copies_carve(d, need, nullptr).bytes;
+    if (workspace != nullptr && workspace_bytes < with_copies) {
+      copies = false;
+      d = d_in;
+      with_cb = false;
+      need = carve(d, nullptr, false).bytes;
+    } else {
+      need = with_copies;
+    }
+  }
   void* base = workspace;
   bool owned = false;
   if (base == nullptr) {
@@ -362,36 +500,62 @@ int scan_fwd_run(const ssd::Dims& d_in, const void* x, const void* dt, const flo
   Workspace w = carve(d, base, with_cb);
   int32_t* seg = seq_idx ? w.seg : nullptr;
   const int clamp = do_clamp_of(dt_limit_lo, dt_limit_hi);
-  cudaError_t e;
-  if (dtype == SSD_DTYPE_F32) {
+  cudaError_t e = cudaSuccess;
+  if (dtype == SSD_DTYPE_F32 || copies) {
     const float* xf = static_cast<const float*>(x);
-    e = ssd::launch_dt_cumsum<float>(static_cast<const float*>(dt), dt_bias, dt_softplus,
-                                     dt_limit_lo, dt_limit_hi, clamp, A, seq_idx, d, w.dt, w.cs,
-                                     seg, st);
-    // chunk_state with B pre-split once per group where it runs on tensor cores
-    const bool tg = w.tg != nullptr && ssd::chunk_state_tc32_fits(xf, static_cast<const float*>(B), d);
-    if (e == cudaSuccess && tg)
-      e = ssd::launch_group_tiles_tc32(static_cast<const float*>(B), d.sB, d.ngroups, d.batch,
-                                       d.seqlen, d.nchunks, w.tg, st);
-    if (e == cudaSuccess)
-      e = tg ? ssd::launch_chunk_state_tc32(xf, static_cast<const float*>(B), w.dt, w.cs, seg, d,
-                                            w.states, st, w.tg)
-             : ssd::launch_chunk_state<float>(xf, static_cast<const float*>(B), w.dt, w.cs, seg,
-                                              d, w.states, st);
-    if (e == cudaSuccess)
-      e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, d, st);
     const float* Bf = static_cast<const float*>(B);
     const float* Cf = static_cast<const float*>(C);
     const float* zf = static_cast<const float*>(z);
-    // C B^T once per (batch, chunk, group) where chunk_scan runs on tensor cores
-    const bool cb = w.cb != nullptr && ssd::cb_tc32_fits(Bf, Cf, d) &&
-                    ssd::chunk_scan_tc32_fits(xf, Bf, Cf, zf, d);
-    if (e == cudaSuccess && cb) e = ssd::launch_cb_tc32(Bf, Cf, d, w.cb, nullptr, st);
+    float* of = static_cast<float*>(out);
+    ssd::Dims df = d;   // the fp32 operands' layout
+    if (copies) {       // dense fp32 copies of the bf16 x, B, C, z
+      const Copies cp = copies_carve(d, w.bytes, base);
+      const int hp = d.nheads * d.headdim, gn = d.ngroups * d.dstate;
+      e = rows_to_f32(x, d.sx, d, hp, cp.x, st);
+      if (e == cudaSuccess) e = rows_to_f32(B, d.sB, d, gn, cp.B, st);
+      if (e == cudaSuccess) e = rows_to_f32(C, d.sC, d, gn, cp.C, st);
+      if (e == cudaSuccess && z) e = rows_to_f32(z, d.sz, d, hp, cp.z, st);
+      xf = cp.x;
+      Bf = cp.B;
+      Cf = cp.C;
+      zf = z ? cp.z : nullptr;
+      of = cp.out;
+      df.sx = df.sz = {d.seqlen * hp, (int64_t)hp};
+      df.sB = df.sC = {d.seqlen * gn, (int64_t)gn};
+    }
     if (e == cudaSuccess)
-      e = cb ? ssd::launch_chunk_scan_tc32(xf, Bf, Cf, w.dt, w.cs, seg, w.states, D, zf, d,
-                                           static_cast<float*>(out), st, 0, w.cb, 0)
-             : ssd::launch_chunk_scan<float>(xf, Bf, Cf, w.dt, w.cs, seg, w.states, D, zf, d,
-                                             static_cast<float*>(out), st);
+      e = copies ? ssd::launch_dt_cumsum<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(dt),
+                                                        dt_bias, dt_softplus, dt_limit_lo,
+                                                        dt_limit_hi, clamp, A, seq_idx, d, w.dt,
+                                                        w.cs, seg, st)
+                 : ssd::launch_dt_cumsum<float>(static_cast<const float*>(dt), dt_bias,
+                                                dt_softplus, dt_limit_lo, dt_limit_hi, clamp, A,
+                                                seq_idx, d, w.dt, w.cs, seg, st);
+    // chunk_state with B pre-split once per group where it runs on tensor cores
+    const bool tg = w.tg != nullptr && ssd::chunk_state_tc32_fits(xf, Bf, df);
+    if (e == cudaSuccess && tg)
+      e = ssd::launch_group_tiles_tc32(Bf, df.sB, df.ngroups, df.batch, df.seqlen, df.nchunks,
+                                       w.tg, st);
+    if (e == cudaSuccess)
+      e = tg ? ssd::launch_chunk_state_tc32(xf, Bf, w.dt, w.cs, seg, df, w.states, st, w.tg)
+             : ssd::launch_chunk_state<float>(xf, Bf, w.dt, w.cs, seg, df, w.states, st);
+    if (e == cudaSuccess)
+      e = ssd::launch_state_passing(w.states, w.cs, seg, initial_states, final_states, df, st);
+    // C B^T once per (batch, chunk, group) where chunk_scan runs on tensor cores
+    const bool cb = w.cb != nullptr && ssd::cb_tc32_fits(Bf, Cf, df) &&
+                    ssd::chunk_scan_tc32_fits(xf, Bf, Cf, zf, df);
+    if (e == cudaSuccess && cb) e = ssd::launch_cb_tc32(Bf, Cf, df, w.cb, nullptr, st);
+    if (e == cudaSuccess)
+      e = cb ? ssd::launch_chunk_scan_tc32(xf, Bf, Cf, w.dt, w.cs, seg, w.states, D, zf, df, of,
+                                           st, 0, w.cb, 0)
+             : ssd::launch_chunk_scan<float>(xf, Bf, Cf, w.dt, w.cs, seg, w.states, D, zf, df,
+                                             of, st);
+    if (e == cudaSuccess && copies) {   // out rounded to bf16 once
+      const int64_t n8 = d.batch * d.seqlen * d.nheads * d.headdim / 8;
+      f32_to_bf16_rows_kernel<<<grid_for(n8), 256, 0, st>>>(of, n8,
+                                                            static_cast<__nv_bfloat16*>(out));
+      e = cudaGetLastError();
+    }
   } else {
     using bf = __nv_bfloat16;
     const bf* xb = static_cast<const bf*>(x);

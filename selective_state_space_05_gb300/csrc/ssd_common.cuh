@@ -162,4 +162,10 @@ cudaError_t launch_fused(const __nv_bfloat16* x, const __nv_bfloat16* B, const _
 // Sets the per-thread message returned by ssd_last_error(); returns code.
 int set_error(int code, const char* msg);
 
+// The forward's workspace without the fp32 copies that bf16 shapes outside
+// the fused kernel take when there is room (then the bf16 stage kernels run).
+// (dtype: an ssd_dtype_t value)
+size_t fwd_workspace_bytes_least(int64_t batch, int64_t seqlen, int nheads, int headdim,
+                                 int dstate, int ngroups, int chunk_size, int dtype);
+
 }  // namespace ssd

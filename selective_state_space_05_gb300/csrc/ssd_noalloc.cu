@@ -42,8 +42,10 @@ int ssd_scan_fwd_noalloc(const void* x, const void* dt, const float* dt_bias, in
                          int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
                          int chunk_size, ssd_dtype_t dtype, void* out, float* final_states,
                          void* stream) {
-  const size_t need = ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups,
-                                               chunk_size, dtype);
+  // (bf16 shapes outside the fused kernel run on the bf16 stage kernels when
+  // the scratch has no room for fp32 copies of their inputs)
+  const size_t need = ssd::fwd_workspace_bytes_least(batch, seqlen, nheads, headdim, dstate,
+                                                     ngroups, chunk_size, dtype);
   if (need > kScratchBytes) {
     char m[256];
     snprintf(m, sizeof(m),

@@ -74,9 +74,12 @@ def scan_status(reset: bool = True, stream=None) -> None:
 
 
 def workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size,
-                    dtype=torch.bfloat16) -> int:
-    return int(_lib.load().ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, dstate,
-                                                    ngroups, chunk_size, _DT[dtype]))
+                    dtype=torch.bfloat16, least: bool = False) -> int:
+    """ssd_scan_workspace_bytes, or with least=True ssd_scan_workspace_bytes_min
+    (the smallest workspace ssd_scan_fwd accepts)."""
+    f = (_lib.load().ssd_scan_workspace_bytes_min if least
+         else _lib.load().ssd_scan_workspace_bytes)
+    return int(f(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, _DT[dtype]))
 
 
 def ssd_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,

@@ -31,7 +31,8 @@ def test_header_declares_the_expected_calls():
     names = declared_functions()
     for n in ("ssd_scan_fwd", "ssd_last_error", "ssd_abi_version", "ssd_scan_workspace_bytes",
               "ssd_dt_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
-              "ssd_chunk_fused", "ssd_scan_bwd", "ssd_scan_bwd_workspace_bytes"):
+              "ssd_chunk_fused", "ssd_scan_bwd", "ssd_scan_bwd_workspace_bytes",
+              "ssd_scan_workspace_bytes_min"):
         assert n in names
 
 
@@ -42,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert lib.ssd_abi_version() == 2
+    assert lib.ssd_abi_version() == 3
 
 
 def test_workspace_bytes(lib):

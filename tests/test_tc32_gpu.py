@@ -2,9 +2,11 @@
 chunk_state and chunk_scan through the forward call and through the stage
 exports, against the oracle, for every headdim / dstate combination they
 take (and the ones where only chunk_scan does), with documents, initial
-states, ragged tails, strided views and the optional inputs missing.
-Tolerance: the forward's fp32 bound, max|err| / max|ref| <= 1e-4; the
-3xTF32 products are within about 2^-22 of fp32 ones."""
+states, ragged tails, strided views and the optional inputs missing; and
+bf16 inputs of the shapes the fused kernel does not take, which run the same
+stages on fp32 copies.  Tolerance: the forward's fp32 bound, max|err| /
+max|ref| <= 1e-4 (the 3xTF32 products are within about 2^-22 of fp32 ones),
+and the bf16 bound for bf16 inputs."""
 import numpy as np
 import pytest
 import torch
@@ -154,3 +156,82 @@ def test_tc32_timeout_is_reported(monkeypatch):
     ry, rf = oracle.scan_sequential(d)
     assert_close(y, ry, TOL["f32"], "out after the time-out")
     assert_close(f, rf, TOL["f32"], "final after the time-out")
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
+def test_forward_bf16_through_fp32_stages(shape, case):
+    """bf16 shapes the fused kernel does not take (headdim 128, dstate other
+    than 128, an odd number of heads per group) run the fp32 tensor-core
+    stages on exact fp32 copies of their inputs, out rounded to bf16 once
+    (chunk 256, run at 128); the others run the fused kernel.  bf16 bound."""
+    _, P, N = shape
+    name, kw = case
+    d = si.random_small(3500 + P + N + len(name), headdim=P, dstate=N, chunk_size=256,
+                        dtype="bf16", **kw)
+    y, f = run_gpu(d)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y, ry, TOL["bf16"], "out")
+    assert_close(f, rf, TOL["bf16"], "final")
+
+
+def _proj_views(d, H, P, N, extra):
+    """x, z, B, C of d as slices of one projection row per token, the row
+    `extra` elements longer than the four (a token stride of any length)."""
+    B_, L = d["x"].shape[:2]
+    W = 2 * H * P + 2 * N + extra
+    proj = torch.zeros(B_, L, W, dtype=d["x"].dtype)
+    proj[:, :, :H * P] = d["z"].reshape(B_, L, -1)
+    proj[:, :, H * P:2 * H * P] = d["x"].reshape(B_, L, -1)
+    proj[:, :, 2 * H * P:2 * H * P + N] = d["B"].reshape(B_, L, -1)
+    proj[:, :, 2 * H * P + N:2 * H * P + 2 * N] = d["C"].reshape(B_, L, -1)
+    pg = proj.cuda()
+    return (pg[:, :, H * P:2 * H * P].unflatten(2, (H, P)), pg[:, :, :H * P].unflatten(2, (H, P)),
+            pg[:, :, 2 * H * P:2 * H * P + N].unflatten(2, (1, N)),
+            pg[:, :, 2 * H * P + N:2 * H * P + 2 * N].unflatten(2, (1, N)))
+
+
+@pytest.mark.parametrize("extra", [8, 3], ids=["stride_x8", "stride_odd"])
+def test_forward_bf16_through_fp32_stages_strided(extra):
+    """Strided bf16 views (slices of a projection row) into the fp32 copies:
+    16-byte loads when the token stride is a multiple of 8 elements, one
+    element at a time otherwise."""
+    import selective_state_space_05_gb300 as ssd
+    H, P, N = 2, 128, 64
+    d = si.random_small(3600 + extra, batch=2, seqlen=200, nheads=H, headdim=P, dstate=N,
+                        ngroups=1, chunk_size=256, dtype="bf16", init_std=0.2)
+    x, z, Bm, Cm = _proj_views(d, H, P, N, extra)
+    g = to_dev(d)
+    y, f = ssd.ssd_scan_fwd(x, g["dt"], g["A"], Bm, Cm, chunk_size=256, dt_bias=g["dt_bias"],
+                            D=g["D"], z=z, initial_states=g["initial_states"],
+                            return_final_states=True, check=True)
+    ry, rf = oracle.scan_sequential(d)
+    assert_close(y.double().cpu().numpy(), ry, TOL["bf16"], "out")
+    assert_close(f.double().cpu().numpy(), rf, TOL["bf16"], "final")
+
+
+def test_forward_bf16_least_workspace_runs_stage_kernels():
+    """A workspace of ssd_scan_workspace_bytes_min has no room for the fp32
+    copies: the same bf16 call then runs the bf16 stage kernels, and agrees
+    with the oracle (and, to bf16 rounding, with the call on the full
+    workspace)."""
+    import selective_state_space_05_gb300 as ssd
+    H, P, N, Q = 4, 128, 64, 256
+    d = si.random_small(3700, batch=2, seqlen=300, nheads=H, headdim=P, dstate=N, ngroups=2,
+                        chunk_size=Q, dtype="bf16", init_std=0.3, seq_idx_lengths=[120, 180])
+    g = to_dev(d)
+    full = ssd.workspace_bytes(2, 300, H, P, N, 2, Q, torch.bfloat16)
+    least = ssd.workspace_bytes(2, 300, H, P, N, 2, Q, torch.bfloat16, least=True)
+    assert 0 < least < full
+    outs = []
+    for nbytes in (least, full):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        y, f = ssd.ssd_scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], chunk_size=Q,
+                                dt_bias=g["dt_bias"], D=g["D"], z=g["z"],
+                                initial_states=g["initial_states"], seq_idx=g["seq_idx"],
+                                return_final_states=True, workspace=ws, check=True)
+        outs.append((y.double().cpu().numpy(), f.double().cpu().numpy()))
+    ry, rf = oracle.scan_sequential(d)
+    for y, f in outs:
+        assert_close(y, ry, TOL["bf16"], "out")
+        assert_close(f, rf, TOL["bf16"], "final")
