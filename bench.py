@@ -38,6 +38,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SSD chunked-scan fwd tokens/s at 2.7B shape, bf16; % of roofline"
+# the 2.7B shape's inner width (5120) with headdim 128: a bf16 shape the fused
+# kernel does not take
+HD128 = (40, 128)
 UNIT = "tokens/s"
 WORKLOAD = "mamba2_2p7b"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
@@ -53,7 +56,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
                     help="mamba2_2p7b (default), or one other workload alone: chained, packed, "
-                         "backward, forward_fp32")
+                         "backward, forward_fp32, forward_bf16_hd128")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -532,18 +535,23 @@ def backward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None):
             "data": "synthetic, drawn on the device"}
 
 
-def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None):
+def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None, dtype="f32",
+                          heads_dim=None):
     """The forward in fp32 at the 2.7B shape: the four stage kernels, with
     chunk_state and chunk_scan on the tensor cores (3xTF32, run at 128-token
-    chunks); HBM roofline on the call's algorithmic bytes."""
-    cfg = si.CONFIGS["mamba2_2p7b"].with_(dtype="f32")
+    chunks); HBM roofline on the call's algorithmic bytes.  With dtype
+    "bf16" and heads_dim (nheads, headdim) a bf16 shape the fused kernel does
+    not take, which runs the same stages on fp32 copies of its inputs."""
+    cfg = si.CONFIGS["mamba2_2p7b"].with_(dtype=dtype)
+    if heads_dim:
+        cfg = cfg.with_(nheads=heads_dim[0], headdim=heads_dim[1])
     if batch:
         cfg = cfg.with_(batch=batch)
     d = si.make_inputs(cfg, 93, device=dev)
     Bz, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
     out = torch.empty_like(d["x"])
     fin = torch.empty(Bz, H, P, N, device=dev)
-    ws = torch.empty(ssd.workspace_bytes(Bz, L, H, P, N, G, cfg.chunk_size, torch.float32),
+    ws = torch.empty(ssd.workspace_bytes(Bz, L, H, P, N, G, cfg.chunk_size, d["x"].dtype),
                      dtype=torch.uint8, device=dev)
 
     def step():
@@ -556,10 +564,13 @@ def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None)
     torch.cuda.synchronize()
     n = max(5, min(steps, 20))
     ms, per = time_calls(torch, step, n, stream)
-    alg = 4 * (3 * Bz * L * H * P + Bz * L * H + 2 * Bz * L * G * N + Bz * H * P * N + 3 * H)
+    e = 2 if dtype == "bf16" else 4
+    alg = (e * (3 * Bz * L * H * P + Bz * L * H + 2 * Bz * L * G * N)
+           + 4 * (Bz * H * P * N + 3 * H))
     ach = alg / (ms / 1e3) / 1e9
-    return {"workload": f"forward fp32: batch {Bz}, seqlen {L}, nheads {H}, headdim {P}, dstate "
-                        f"{N}, ngroups {G}, chunk {cfg.chunk_size} (stages at 128), z gate, D, "
+    route = "(stages at 128)" if dtype == "f32" else "(fp32 stages at 128 on fp32 copies)"
+    return {"workload": f"forward {dtype}: batch {Bz}, seqlen {L}, nheads {H}, headdim {P}, dstate "
+                        f"{N}, ngroups {G}, chunk {cfg.chunk_size} {route}, z gate, D, "
                         "final states",
             "ms_per_call": ms, "per_call_ms": spread(per), "calls": n,
             "value": Bz * L / (ms / 1e3), "unit": "tokens/s",
@@ -571,20 +582,26 @@ def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None)
 def main():
     args = parse_args()
     import ssd_inputs as si
-    if args.workload in ("backward", "forward_fp32"):
-        # the backward or the fp32 forward alone (for profiling it): its own line
+    if args.workload in ("backward", "forward_fp32", "forward_bf16_hd128"):
+        # the backward or a stage-kernel forward alone (for profiling it): its own line
         import torch
         import selective_state_space_05_gb300 as ssd
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        fn = backward_workload if args.workload == "backward" else fp32_forward_workload
-        res = fn(torch, ssd, si, dev, torch.cuda.current_stream(), load_peaks(), args.steps,
-                 batch=args.batch)
-        metric = ("SSD scan backward (all gradients) tokens/s at 2.7B shape, fp32"
-                  if args.workload == "backward" else
-                  "SSD chunked-scan fwd tokens/s at 2.7B shape, fp32")
+        st0, pk = torch.cuda.current_stream(), load_peaks()
+        if args.workload == "backward":
+            res = backward_workload(torch, ssd, si, dev, st0, pk, args.steps, batch=args.batch)
+            metric, dtype = "SSD scan backward (all gradients) tokens/s at 2.7B shape, fp32", "f32"
+        elif args.workload == "forward_fp32":
+            res = fp32_forward_workload(torch, ssd, si, dev, st0, pk, args.steps, batch=args.batch)
+            metric, dtype = "SSD chunked-scan fwd tokens/s at 2.7B shape, fp32", "f32"
+        else:
+            res = fp32_forward_workload(torch, ssd, si, dev, st0, pk, args.steps, batch=args.batch,
+                                        dtype="bf16", heads_dim=HD128)
+            metric = "SSD chunked-scan fwd tokens/s at 2.7B width, headdim 128, bf16"
+            dtype = "bf16"
         print(json.dumps({"metric": metric, **res, "n_gpus": 1, "higher_is_better": True,
-                          "dtype": "f32"}), flush=True)
+                          "dtype": dtype}), flush=True)
         return
     cfg = si.CONFIGS[args.workload]
     if args.impl == "reference":
@@ -783,6 +800,8 @@ def main():
         others["decode"] = decode_workload(torch, ssd, si, dev, stream, peaks, args.steps)
         others["forward_fp32"] = fp32_forward_workload(torch, ssd, si, dev, stream, peaks,
                                                        args.steps)
+        others["forward_bf16_hd128"] = fp32_forward_workload(
+            torch, ssd, si, dev, stream, peaks, args.steps, dtype="bf16", heads_dim=HD128)
         others["backward"] = backward_workload(torch, ssd, si, dev, stream, peaks, args.steps)
 
     cpu = parity = None
