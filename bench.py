@@ -16,8 +16,10 @@ MEASURED_PEAKS.json.  `cpu_baseline` times the fp64 CPU oracle on a bounded
 sample of the same workload, and `parity` compares that sample with the GPU
 output (max and mean relative error, mean signed error, 99.9th percentile).
 `other_configs` times the chained-prefill and packed-documents workloads the
-same way (inputs drawn on the device), the decode step, the forward in fp32
-and the backward (ssd_scan_bwd, fp32) at the same shape.
+same way (inputs drawn on the device), the decode step, the forward in fp32,
+a bf16 shape outside the fused kernel (headdim 128 at the same width), the
+backward (ssd_scan_bwd, fp32) and the block's conv1d and grouped RMSNorm
+passes at the same shape.
 
 `--impl reference` times the oracle alone (the only reference this workload
 has) and prints its own line.
@@ -579,6 +581,45 @@ def fp32_forward_workload(torch, ssd, si, dev, stream, peaks, steps, batch=None,
             "data": "synthetic, drawn on the device"}
 
 
+def block_workload(torch, ssd, dev, stream, peaks, steps):
+    """The block around the scan on the 2.7B shape (d_inner 5120, 1 group,
+    dstate 128): the causal depthwise conv1d (width 4, bias, SiLU) over the
+    xBC slice of the input projection zxbcdt (a strided view), and the grouped
+    RMSNorm of the gated out (in place); HBM roofline on each pass's bytes."""
+    Bz, L, H, P, G, N, W = 8, 4096, 80, 64, 1, 128, 4
+    di, cbc = H * P, H * P + 2 * G * N
+    g = torch.Generator(device=dev).manual_seed(95)
+    zxbcdt = torch.randn(Bz, L, 2 * di + 2 * G * N + H, generator=g, device=dev).bfloat16()
+    xbc = zxbcdt[:, :, di:di + cbc]
+    wconv = torch.randn(cbc, W, generator=g, device=dev) * 0.5
+    bconv = torch.randn(cbc, generator=g, device=dev) * 0.1
+    conv_out = torch.empty(Bz, L, cbc, dtype=torch.bfloat16, device=dev)
+    y = torch.randn(Bz, L, di, generator=g, device=dev).bfloat16()
+    wnorm = torch.rand(di, generator=g, device=dev) + 0.5
+    n = max(5, min(steps, 20))
+    res = {}
+    for name, step, nbytes in (
+            ("conv1d", lambda: ssd.causal_conv1d(xbc, wconv, bconv, out=conv_out, stream=stream),
+             2 * Bz * L * cbc * 2 + cbc * (W + 1) * 4),
+            ("group_rmsnorm", lambda: ssd.group_rmsnorm_(y, wnorm, group_size=di // G,
+                                                         stream=stream),
+             2 * Bz * L * di * 2 + di * 4)):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        ms, per = time_calls(torch, step, n, stream)
+        ach = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"ms_per_call": ms, "per_call_ms": spread(per), "calls": n,
+                     "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                                  "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                                  "alg_bytes_per_call": nbytes}}
+    res["workload"] = (f"block around the scan: batch {Bz}, seqlen {L}, d_inner {di}, ngroups {G}, "
+                       f"dstate {N}; conv1d width {W} + SiLU over the xBC slice of zxbcdt, "
+                       "grouped RMSNorm of out in place")
+    res["data"] = "synthetic, drawn on the device"
+    return res
+
+
 def main():
     args = parse_args()
     import ssd_inputs as si
@@ -803,6 +844,7 @@ def main():
         others["forward_bf16_hd128"] = fp32_forward_workload(
             torch, ssd, si, dev, stream, peaks, args.steps, dtype="bf16", heads_dim=HD128)
         others["backward"] = backward_workload(torch, ssd, si, dev, stream, peaks, args.steps)
+        others["block"] = block_workload(torch, ssd, dev, stream, peaks, args.steps)
 
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
