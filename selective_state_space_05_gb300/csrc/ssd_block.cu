@@ -65,10 +65,38 @@ __device__ __forceinline__ void store8<float>(float* p, const float (&v)[kVec]) 
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// The raw bits of one token's kVec channels (16 bytes of bf16 or 32 of
+// fp32), held in registers ahead of their use, and their values.
+struct Raw8 {
+  uint4 a, b;
+};
+template <typename T>
+__device__ __forceinline__ void raw_load(const T* p, Raw8& r) {
+  r.a = *reinterpret_cast<const uint4*>(p);
+  if constexpr (sizeof(T) == 4) r.b = *reinterpret_cast<const uint4*>(p + 4);
+}
+template <typename T>
+__device__ __forceinline__ void raw_values(const Raw8& r, float (&v)[kVec]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t u[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(u[i] << 16);
+      v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+  } else {
+    const uint32_t u[8] = {r.a.x, r.a.y, r.a.z, r.a.w, r.b.x, r.b.y, r.b.z, r.b.w};
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) v[i] = __uint_as_float(u[i]);
+  }
+}
+
 // grid (ceil(C/8 / 128), ceil(L / kConvRun), B), 128 threads: thread ->
 // 8 consecutive channels, a run of kConvRun tokens, with the filter and the
 // last W inputs in registers.  A warp's loads of one token are 32 x 16
-// contiguous bytes.
+// contiguous bytes; each thread keeps the next two tokens' loads in flight
+// (as raw bits, converted when used), since with the filter in registers
+// few warps fit on an SM and one load each would leave HBM latency exposed.
 template <typename T, int W>
 __global__ void __launch_bounds__(128)
     causal_conv1d_kernel(const T* __restrict__ x, TokStride sx, const float* __restrict__ w,
@@ -103,8 +131,12 @@ __global__ void __launch_bounds__(128)
       sq_win[k] = sq ? sq[t] : 0;
     }
   }
-  for (int64_t t = t0; t < t1; ++t) {
-    load8(x + toff(sx, b, t) + c0, win[W - 1]);
+  Raw8 ra, rb;   // tokens t and t + 1, loaded ahead
+  if (t0 < t1) raw_load(x + toff(sx, b, t0) + c0, ra);
+  if (t0 + 1 < t1) raw_load(x + toff(sx, b, t0 + 1) + c0, rb);
+  auto step = [&](int64_t t, Raw8& r) {
+    raw_values<T>(r, win[W - 1]);
+    if (t + 2 < t1) raw_load(x + toff(sx, b, t + 2) + c0, r);   // this slot's next token
     const int sq_t = sq ? sq[t] : 0;
     sq_win[W - 1] = sq_t;
     float acc[kVec];
@@ -128,6 +160,10 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
       for (int i = 0; i < kVec; ++i) win[k][i] = win[k + 1][i];
     }
+  };
+  for (int64_t t = t0; t < t1; t += 2) {   // two tokens a turn: the slots alternate
+    step(t, ra);
+    if (t + 1 < t1) step(t + 1, rb);
   }
 }
 
