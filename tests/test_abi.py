@@ -68,6 +68,36 @@ def test_workspace_bytes(lib):
     assert lib.ssd_scan_workspace_bytes(B, L, 80, P, N, 3, Q, 1) == 0       # H % G != 0
 
 
+def test_least_workspace(lib):
+    """ssd_scan_workspace_bytes_min: below the full size only for bf16 shapes
+    outside the fused kernel, by the fp32 copies of x, z, out (B*L*H*P each)
+    and B, C (B*L*G*N each), each piece on a 256-byte boundary; the least
+    size is then the bf16 stage kernels' workspace at the caller's chunk."""
+    BF, F32 = _lib.SSD_DTYPE_BF16, _lib.SSD_DTYPE_F32
+
+    def sizes(*a):
+        return lib.ssd_scan_workspace_bytes(*a), lib.ssd_scan_workspace_bytes_min(*a)
+
+    def up(v):
+        return (v + 255) // 256 * 256
+
+    # fused shape (bf16) and fp32: nothing to leave out
+    for dt in (BF, F32):
+        full, least = sizes(8, 4096, 80, 64, 128, 1, 256, dt)
+        assert 0 < least == full
+    # bf16, headdim 128: the fp32 stages on copies
+    B, L, H, P, N, G, Q = 2, 1000, 4, 128, 64, 2, 256
+    full, least = sizes(B, L, H, P, N, G, Q, BF)
+    xs, bs = B * L * H * P * 4, B * L * G * N * 4
+    copies = 3 * up(xs) + 2 * up(bs)
+    nc = -(-L // Q)   # the stage kernels' chunk: the caller's 256
+    stage = ((64 + B * H) * 4 + 2 * B * H * nc * Q * 4 + B * nc * Q * 4
+             + B * nc * H * P * N * 4)
+    assert stage <= least <= stage + 5 * 256
+    assert least < full and full >= copies
+    assert lib.ssd_scan_workspace_bytes_min(B, L, H, 48, N, G, Q, BF) == 0   # bad headdim
+
+
 def _fwd(lib, **kw):
     a = dict(x=16, dt=16, dt_bias=None, sp=1, lo=0.0, hi=math.inf, A=16, B=16, C=16, D=None,
              z=None, init=None, seq=None, batch=1, L=64, H=2, P=16, N=16, G=1, Q=64, dtype=0,
